@@ -1,0 +1,31 @@
+/* Selective-scan oracle (fp64, sequential). TEST INFRASTRUCTURE ONLY: see mamba_oracle.c. */
+#ifndef MAMBA_ORACLE_H
+#define MAMBA_ORACLE_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Forward over rows [row_begin, row_end), row = b * d_inner + d. Writes out (and y if non-null)
+   at those rows only. Returns 0, 1 on bad arguments, 2 on allocation failure. */
+int mamba_oracle_fwd_rows(const double* delta, const double* u, const double* B,
+                          const double* C, const double* gate, const double* A_log,
+                          const double* D, int64_t batch, int64_t T, int64_t d_inner,
+                          int64_t d_state, int64_t row_begin, int64_t row_end, double* out,
+                          double* y);
+
+/* Forward + backward over rows [row_begin, row_end). Writes d_delta, d_u, d_gate at those
+   rows; ADDS the rows' contributions into d_B_acc, d_C_acc [batch, T, d_state],
+   d_A_log_acc [d_inner, d_state] and d_D_acc [d_inner]. */
+int mamba_oracle_bwd_rows(const double* delta, const double* u, const double* B,
+                          const double* C, const double* gate, const double* A_log,
+                          const double* D, const double* dy, int64_t batch, int64_t T,
+                          int64_t d_inner, int64_t d_state, int64_t row_begin, int64_t row_end,
+                          double* d_delta, double* d_u, double* d_gate, double* d_B_acc,
+                          double* d_C_acc, double* d_A_log_acc, double* d_D_acc);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

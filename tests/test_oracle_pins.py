@@ -1,0 +1,304 @@
+"""Pins of the fp64 oracle against facts that the pages and the mathematics fix (CPU only).
+
+None of these re-types the oracle's formulas. The checks are:
+  * finite differences of the scalar loss sum(dy * out), over every input element (tiny shapes);
+  * symbolic differentiation of the forward definition (sympy; an independent derivation of BPTT);
+  * the closed-form geometric series for constant delta, u, B, C (forward);
+  * the delta == 0 special case. It reduces to the inclusive reverse running sum of
+    cumsum_backward_row (rlx-cpu src/training_bwd.rs). A hand-worked integer fixture covers it.
+  * T == 1, where every gradient is a hand-computable product;
+  * the Euler identities: out is homogeneous of degree 1 in u, in B, in C and in D;
+  * the SiLU-gradient identity sigma*(1 + x*(1 - sigma)) == sigma*(1 - silu) + silu.
+    The first form is from mamba-rs src/mamba_ssm/cpu/backward.rs, Phase B2; the second from
+    luma-tensor src/grad/backprop.rs, UnaryOp::Silu.
+Planted mistakes also go in: edited copies of the oracle source, each of which must fail at
+least one pin.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+GRAD_KEYS = ("d_delta", "d_u", "d_B", "d_C", "d_gate", "d_A_log", "d_D")
+INPUT_OF = {"d_delta": "delta", "d_u": "u", "d_B": "B", "d_C": "C", "d_gate": "gate",
+            "d_A_log": "A_log", "d_D": "D"}
+
+
+def _tiny_random(seed=3, batch=2, T=5, Di=3, N=4):
+    x = oracle.as64(synth.random_inputs(batch, T, Di, N, seed=seed, a_log_random=True))
+    return x
+
+
+def fd_max_rel_err(x, lib=None, per_tensor=None, seed=0):
+    """max over tensors of max|fd - analytic| / max(1, max|analytic|)."""
+    g = oracle.bwd(x, lib=lib)
+    rng = np.random.default_rng(seed)
+    worst = 0.0
+    for gk in GRAD_KEYS:
+        xk = INPUT_OF[gk]
+        flat = x[xk].reshape(-1)
+        idx = np.arange(flat.size)
+        if per_tensor is not None and flat.size > per_tensor:
+            idx = rng.choice(flat.size, per_tensor, replace=False)
+        an = g[gk].reshape(-1)
+        scale = max(1.0, float(np.abs(an).max()))
+        for i in idx:
+            orig = flat[i]
+            h = 1e-6 * max(1.0, abs(orig))
+            flat[i] = orig + h
+            lp = oracle.loss(x, lib=lib)
+            flat[i] = orig - h
+            lm = oracle.loss(x, lib=lib)
+            flat[i] = orig
+            fd = (lp - lm) / (2 * h)
+            worst = max(worst, abs(fd - an[i]) / scale)
+    return worst
+
+
+def geo_max_rel_err(lib=None):
+    """Constant delta, u, B, C over t: h_t[n] = delta*u*B[n] * (1 - a^(t+1)) / (1 - a)."""
+    batch, T, Di, N = 2, 40, 3, 5
+    rng = np.random.default_rng(11)
+    dl = rng.uniform(0.05, 0.6, size=(batch, Di))
+    uu = rng.normal(size=(batch, Di))
+    Bn = rng.normal(size=(batch, N))
+    Cn = rng.normal(size=(batch, N))
+    A_log = rng.uniform(-1, 1, size=(Di, N))
+    D = rng.uniform(0.5, 1.5, size=Di)
+    gate = rng.normal(size=(batch, T, Di))
+    x = {"delta": np.repeat(dl[:, None, :], T, 1), "u": np.repeat(uu[:, None, :], T, 1),
+         "B": np.repeat(Bn[:, None, :], T, 1), "C": np.repeat(Cn[:, None, :], T, 1),
+         "gate": gate, "A_log": A_log, "D": D, "dy": np.zeros((batch, T, Di))}
+    x = oracle.as64(x)
+    out, y = oracle.fwd(x, lib=lib)
+    A = -np.exp(A_log)                                   # [Di, N]
+    a = np.exp(dl[:, :, None] * A[None])                 # [batch, Di, N]
+    t = np.arange(T)[None, :, None, None]
+    h = (dl * uu)[:, None, :, None] * Bn[:, None, None, :] * (1 - a[:, None] ** (t + 1)) / (1 - a[:, None])
+    y_ref = np.einsum("btdn,bn->btd", h, Cn) + D[None, None, :] * uu[:, None, :]
+    sig = 1 / (1 + np.exp(-gate))
+    out_ref = y_ref * gate * sig
+    return max(float(np.abs(y - y_ref).max() / np.abs(y_ref).max()),
+               float(np.abs(out - out_ref).max() / np.abs(out_ref).max()))
+
+
+def delta_zero_max_err(lib=None):
+    """delta == 0: h == 0, y = D*u, d_B = d_C = d_A_log = 0, d_u = d_y*D and
+    d_delta_t = u_t * sum_n B_t[n] * S_t[n] with S the inclusive reverse running sum of d_y*C."""
+    batch, T, Di, N = 2, 30, 4, 3
+    x = oracle.as64(synth.random_inputs(batch, T, Di, N, seed=5, a_log_random=True))
+    x["delta"][:] = 0.0
+    g = oracle.bwd(x, lib=lib)
+    out, y = oracle.fwd(x, lib=lib)
+    sig = 1 / (1 + np.exp(-x["gate"]))
+    d_y = x["dy"] * x["gate"] * sig                                  # [b,T,Di]
+    contrib = d_y[..., None] * x["C"][:, :, None, :]                 # [b,T,Di,N]
+    S = np.empty_like(contrib)
+    run = np.zeros_like(contrib[:, 0])
+    for t in range(T - 1, -1, -1):                                   # inclusive suffix sum
+        run = run + contrib[:, t]
+        S[:, t] = run
+    dd_ref = x["u"] * np.einsum("btdn,btn->btd", S, x["B"])
+    errs = [np.abs(y - x["D"] * x["u"]).max(),
+            np.abs(g["d_B"]).max(), np.abs(g["d_C"]).max(), np.abs(g["d_A_log"]).max(),
+            np.abs(g["d_u"] - d_y * x["D"]).max() / max(1.0, np.abs(d_y * x["D"]).max()),
+            np.abs(g["d_delta"] - dd_ref).max() / np.abs(dd_ref).max()]
+    return float(max(errs))
+
+
+def t1_max_err(lib=None):
+    """T == 1: h = delta*u*B; every gradient is a closed-form product."""
+    batch, T, Di, N = 3, 1, 4, 5
+    x = oracle.as64(synth.random_inputs(batch, T, Di, N, seed=7, a_log_random=True))
+    g = oracle.bwd(x, lib=lib)
+    out, y = oracle.fwd(x, lib=lib)
+    dl, uu, gt, dy = (x[k][:, 0] for k in ("delta", "u", "gate", "dy"))   # [b, Di]
+    Bn, Cn = x["B"][:, 0], x["C"][:, 0]                                   # [b, N]
+    CB = np.sum(Cn * Bn, axis=1)[:, None]                                 # [b, 1]
+    s = 1 / (1 + np.exp(-gt))
+    y_ref = dl * uu * CB + x["D"] * uu
+    d_y = dy * gt * s
+    ref = {
+        "out": y_ref * gt * s,
+        "d_delta": d_y * uu * CB,
+        "d_u": d_y * (dl * CB + x["D"]),
+        "d_gate": dy * y_ref * s * (1 + gt * (1 - s)),
+        "d_B": np.einsum("bd,bn->bn", d_y * dl * uu, Cn),
+        "d_C": np.einsum("bd,bn->bn", d_y * dl * uu, Bn),
+        "d_D": np.sum(d_y * uu, axis=0),
+        "d_A_log": np.zeros_like(x["A_log"]),
+    }
+    got = {"out": out[:, 0], "d_delta": g["d_delta"][:, 0], "d_u": g["d_u"][:, 0],
+           "d_gate": g["d_gate"][:, 0], "d_B": g["d_B"][:, 0], "d_C": g["d_C"][:, 0],
+           "d_D": g["d_D"], "d_A_log": g["d_A_log"]}
+    return max(float(np.abs(got[k] - ref[k]).max() / max(1.0, np.abs(ref[k]).max())) for k in ref)
+
+
+def euler_max_err(lib=None):
+    x = oracle.as64(synth.random_inputs(2, 50, 8, 6, seed=9, a_log_random=True))
+    g = oracle.bwd(x, lib=lib)
+    out, y = oracle.fwd(x, lib=lib)
+    s = 1 / (1 + np.exp(-x["gate"]))
+    w = x["dy"] * x["gate"] * s                         # dL/dy
+    lhs_rhs = [
+        (np.sum(g["d_u"] * x["u"]), np.sum(x["dy"] * out)),
+        (np.sum(g["d_B"] * x["B"]), np.sum(w * (y - x["D"] * x["u"]))),
+        (np.sum(g["d_C"] * x["C"]), np.sum(w * (y - x["D"] * x["u"]))),
+        (np.sum(g["d_D"] * x["D"]), np.sum(w * x["D"] * x["u"])),
+    ]
+    return max(abs(a - b) / max(1.0, abs(b)) for a, b in lhs_rhs)
+
+
+PINS = {
+    "fd": lambda lib: fd_max_rel_err(_tiny_random(), lib=lib) < 1e-6,
+    "geo": lambda lib: geo_max_rel_err(lib) < 1e-12,
+    "delta0": lambda lib: delta_zero_max_err(lib) < 1e-12,
+    "t1": lambda lib: t1_max_err(lib) < 1e-12,
+    "euler": lambda lib: euler_max_err(lib) < 1e-10,
+}
+
+
+# ----------------------------------------------------------------------------------------------
+def test_fd_all_elements_tiny():
+    assert fd_max_rel_err(_tiny_random()) < 1e-6
+
+
+def test_fd_all_elements_odd_shape():
+    assert fd_max_rel_err(_tiny_random(seed=4, batch=1, T=9, Di=2, N=3)) < 1e-6
+
+
+def test_fd_sampled_tiny_workload():
+    x = oracle.as64(synth.make_inputs(synth.BY_NAME["tiny"]))
+    assert fd_max_rel_err(x, per_tensor=12, seed=1) < 1e-6
+
+
+def test_geometric_closed_form():
+    assert geo_max_rel_err() < 1e-12
+
+
+def test_delta_zero_reduces_to_suffix_sum():
+    assert delta_zero_max_err() < 1e-12
+
+
+def test_t1_closed_form():
+    assert t1_max_err() < 1e-12
+
+
+def test_euler_identities():
+    assert euler_max_err() < 1e-10
+
+
+def _read_golden(name):
+    vals = {}
+    with open(os.path.join(os.path.dirname(__file__), "golden", name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            k, *v = line.split()
+            vals[k] = np.array([float(t) for t in v])
+    return vals
+
+
+def test_golden_delta_zero_integer_example():
+    g = _read_golden("delta_zero_suffix_sum.txt")
+    b, T, Di, N = (int(g[k][0]) for k in ("batch", "T", "d_inner", "d_state"))
+    x = {"delta": g["delta"].reshape(b, T, Di), "u": g["u"].reshape(b, T, Di),
+         "B": g["B"].reshape(b, T, N), "C": g["C"].reshape(b, T, N),
+         "gate": g["gate"].reshape(b, T, Di), "dy": g["dy"].reshape(b, T, Di),
+         "A_log": g["A_log"].reshape(Di, N), "D": g["D"].reshape(Di)}
+    x = oracle.as64(x)
+    out, y = oracle.fwd(x)
+    gr = oracle.bwd(x)
+    np.testing.assert_array_equal(out.reshape(-1), g["expect_out"])
+    np.testing.assert_array_equal(y.reshape(-1), g["expect_y"])
+    for k in GRAD_KEYS:
+        np.testing.assert_array_equal(gr[k].reshape(-1), g["expect_" + k], err_msg=k)
+
+
+def test_silu_gradient_two_forms():
+    """Phase B2's sigma*(1 + x*(1 - sigma)) equals luma-tensor's sigma*(1 - silu) + silu, and
+    the oracle's d_gate equals dy * y * (either form)."""
+    xs = np.linspace(-30, 30, 2001)
+    s = 1 / (1 + np.exp(-xs))
+    silu = xs * s
+    np.testing.assert_allclose(s * (1 + xs * (1 - s)), s * (1 - silu) + silu, rtol=1e-12, atol=1e-15)
+    x = _tiny_random(seed=8)
+    g = oracle.bwd(x)
+    out, y = oracle.fwd(x)
+    sg = 1 / (1 + np.exp(-x["gate"]))
+    sl = x["gate"] * sg
+    np.testing.assert_allclose(g["d_gate"], x["dy"] * y * (sg * (1 - sl) + sl), rtol=1e-12, atol=1e-14)
+
+
+def test_sympy_autodiff_tiny():
+    """Differentiate the forward definition symbolically; compare every gradient."""
+    sp = pytest.importorskip("sympy")
+    batch, T, Di, N = 1, 3, 2, 2
+    x = _tiny_random(seed=12, batch=batch, T=T, Di=Di, N=N)
+    sym = {k: np.empty(v.shape, dtype=object) for k, v in x.items() if k != "dy"}
+    subs = {}
+    for k, arr in sym.items():
+        for idx in np.ndindex(arr.shape):
+            s = sp.Symbol(f"{k}_{'_'.join(map(str, idx))}")
+            arr[idx] = s
+            subs[s] = sp.Float(float(x[k][idx]), 30)
+    L = 0
+    for b in range(batch):
+        for d in range(Di):
+            h = [0] * N
+            for t in range(T):
+                for n in range(N):
+                    a = sp.exp(sym["delta"][b, t, d] * (-sp.exp(sym["A_log"][d, n])))
+                    h[n] = a * h[n] + sym["delta"][b, t, d] * sym["u"][b, t, d] * sym["B"][b, t, n]
+                yv = sum(sym["C"][b, t, n] * h[n] for n in range(N)) + sym["D"][d] * sym["u"][b, t, d]
+                g = sym["gate"][b, t, d]
+                L += float(x["dy"][b, t, d]) * yv * g / (1 + sp.exp(-g))
+    gr = oracle.bwd(x)
+    for gk in GRAD_KEYS:
+        arr = sym[INPUT_OF[gk]]
+        for idx in np.ndindex(arr.shape):
+            ref = float(sp.diff(L, arr[idx]).evalf(25, subs=subs))
+            assert abs(gr[gk][idx] - ref) <= 1e-12 * max(1.0, abs(ref)), (gk, idx, gr[gk][idx], ref)
+
+
+def test_row_split_threads_consistent():
+    x = synth.random_inputs(3, 20, 7, 5, seed=2)
+    g1 = oracle.bwd(x, threads=1)
+    g4 = oracle.bwd(x, threads=4)
+    for k in GRAD_KEYS:
+        np.testing.assert_allclose(g4[k], g1[k], rtol=1e-13, atol=1e-13)
+
+
+MUTANTS = {
+    "carry_without_decay": ("dh[n] = da * g_h;", "dh[n] = g_h;"),
+    "dropped_A_term_in_d_delta": ("ddl += g_h * (A[n] * da * hp + uu * bn);", "ddl += g_h * (uu * bn);"),
+    "d_C_uses_h_prev": ("d_C_acc[bt * N + n] += dyv * hc;", "d_C_acc[bt * N + n] += dyv * hp;"),
+    "wrong_sign_of_A": ("-exp(A_log[d * N + n])", "exp(A_log[d * N + n])"),
+    "fwd_input_term_without_delta": ("h[n] = da * h[n] + delta[i] * u[i] * Bm[bt * N + n];",
+                                     "h[n] = da * h[n] + u[i] * Bm[bt * N + n];"),
+    "silu_grad_sign": ("(s * (1.0 + g * (1.0 - s)))", "(s * (1.0 - g * (1.0 - s)))"),
+    "d_A_log_without_A": ("+= g_h * da * dl * A[n] * hp;", "+= g_h * da * dl * hp;"),
+    "B_C_transposed_in_bwd": ("const double bn = Bm[bt * N + n];", "const double bn = Cm[bt * N + n];"),
+    "d_u_skip_term_missing": ("double du = dyv * Dp[d];", "double du = 0.0;"),
+    "time_index_off_by_one": ("const double hp = (t > 0) ? H[(t - 1) * N + n] : 0.0;\n        const double hc",
+                              "const double hp = (t > 1) ? H[(t - 2) * N + n] : 0.0;\n        const double hc"),
+}
+
+
+def test_real_oracle_passes_every_pin():
+    failing = [name for name, pin in PINS.items() if not pin(None)]
+    assert failing == []
+
+
+@pytest.mark.parametrize("mutant", sorted(MUTANTS))
+def test_planted_mistake_fails_a_pin(mutant, tmp_path):
+    find, repl = MUTANTS[mutant]
+    src = oracle.source()
+    assert find in src, mutant
+    lib = oracle.compile_variant(src.replace(find, repl), str(tmp_path))
+    failing = [name for name, pin in PINS.items() if not pin(lib)]
+    assert failing, f"planted mistake {mutant} passed every pin"
