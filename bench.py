@@ -1,0 +1,353 @@
+#!/usr/bin/env python3
+"""Selective-scan forward + backward throughput on GB300 (one JSON line on stdout).
+
+A step is one mamba_scan_fwd plus one mamba_scan_bwd over one batch of synthetic inputs that
+already sit in HBM. That is every step of the hot path: the A = -exp(A_log) prologue, the
+chunked forward scan with its checkpoints, the gating backward, the recompute, the reverse
+recurrence and the fixed-order reductions.
+  metric = (batch * T * d_inner) / (t_fwd + t_bwd), in elements/s.
+  e2e    = the same metric through mamba_scan_fwd_bwd_host with pinned HOST buffers: the
+           host->device copies of the inputs and the device->host copies of out and all seven
+           gradients fall inside the timed region.
+The default workload is the Mamba-130M-width layer (batch 8, T 1024, d_inner 1536, d_state 16).
+--workload picks another. --impl reference times the fp64 CPU oracle on a bounded sample of the
+same workload instead.
+
+Multi-GPU runs (torchrun) are independent replicas, one per GPU. The scan has no cross-device
+exchange, so there is no collective on the data path. value = all ranks' elements / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "selective-scan fwd+bwd (batch*T*d_inner)/sec"
+UNIT = "elements/s"
+DEFAULT_WORKLOAD = "mamba130m"
+
+
+def minimal_bytes(w) -> dict:
+    """Algorithmic (minimal) HBM bytes: each input read once, each output written once; fp32."""
+    btd, btn, dn, d = w.btd, w.btn, w.d_inner * w.d_state, w.d_inner
+    return {
+        "fwd": 4 * (4 * btd + 2 * btn + dn + d),
+        "bwd": 4 * (7 * btd + 4 * btn + 2 * dn + 2 * d),
+        "total": 4 * (11 * btd + 6 * btn + 3 * dn + 3 * d),
+    }
+
+
+def read_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons; keeps only samples taken inside
+    [start, stop] of the timed region."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.t0 = self.t1 = None
+        self._stop = threading.Event()
+        self._thr = None
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                r = subprocess.run(
+                    ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                     "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=5)
+                now = time.time()
+                if r.returncode == 0 and r.stdout.strip():
+                    self.samples.append((now, [c.strip() for c in r.stdout.strip().split(",")]))
+            except Exception:
+                return
+            self._stop.wait(0.05)
+
+    def start(self):
+        self._thr = threading.Thread(target=self._run, daemon=True)
+        self._thr.start()
+
+    def mark(self, t0, t1):
+        self.t0, self.t1 = t0, t1
+
+    def stop(self) -> dict:
+        self._stop.set()
+        if self._thr:
+            self._thr.join(timeout=10)
+        inside = [s for t, s in self.samples if self.t0 is not None and self.t0 <= t <= self.t1]
+        if not inside and self.samples and self.t0 is not None:   # nearest sample to the region
+            mid = 0.5 * (self.t0 + self.t1)
+            inside = [min(self.samples, key=lambda ts: abs(ts[0] - mid))[1]]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(s[1]) for s in inside if num(s[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in inside for i in range(4) if s[5 + i].strip() == "Active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": num(inside[0][2]), "reasons": reasons, "samples": len(inside)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_gpu(args):
+    import torch
+    import selective_state_space_06_gb300 as ms
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    w = synth.BY_NAME[args.workload]
+    x_np = synth.make_inputs(w, seed=0)
+    x = {k: torch.from_numpy(v).to(dev) for k, v in x_np.items()}
+    bufs = ms.alloc_like_outputs(x["delta"], x["B"], x["A_log"], x["D"])
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ms.mamba_scan_fwd(x["delta"], x["u"], x["B"], x["C"], x["gate"], x["A_log"], x["D"],
+                          bufs["out"], None, bufs["ckpt"], stream=stream)
+        nf = ms.mamba_scan_last_launch_count()
+        ev_mid.record(stream)
+        ms.mamba_scan_bwd(x["delta"], x["u"], x["B"], x["C"], x["gate"], x["A_log"], x["D"],
+                          x["dy"], bufs["ckpt"], bufs["scratch"], bufs["d_delta"], bufs["d_u"],
+                          bufs["d_B"], bufs["d_C"], bufs["d_A_log"], bufs["d_D"], bufs["d_gate"],
+                          stream=stream)
+        return nf + ms.mamba_scan_last_launch_count()
+
+    ev_mid = torch.cuda.Event(enable_timing=True)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # timed region: K steps; per-step events on the launching stream split fwd from bwd
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    t_host0 = time.time()
+    outer0 = torch.cuda.Event(enable_timing=True)
+    outer1 = torch.cuda.Event(enable_timing=True)
+    outer0.record(stream)
+    launches = 0
+    for i in range(args.steps):
+        starts[i].record(stream)
+        ev_mid = mids[i]
+        launches += step()
+        ends[i].record(stream)
+    outer1.record(stream)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    t_host1 = time.time()
+    sampler.mark(t_host0, t_host1)
+    clocks = sampler.stop()
+    total_ms = outer0.elapsed_time(outer1)
+    fwd_ms = [starts[i].elapsed_time(mids[i]) for i in range(args.steps)]
+    bwd_ms = [mids[i].elapsed_time(ends[i]) for i in range(args.steps)]
+    if pg:
+        t = torch.tensor([total_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # end-to-end through the host-buffer entry point (pinned host memory)
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda a: torch.from_numpy(a).pin_memory()  # noqa: E731
+        hin = {k: pin(v) for k, v in x_np.items()}
+        b, T, Di, N = w.shape()
+        hout = {k: torch.empty(s, dtype=torch.float32).pin_memory() for k, s in {
+            "out": (b, T, Di), "d_delta": (b, T, Di), "d_u": (b, T, Di), "d_gate": (b, T, Di),
+            "d_B": (b, T, N), "d_C": (b, T, N), "d_A_log": (Di, N), "d_D": (Di,)}.items()}
+        wsb = ms.mamba_scan_host_workspace_bytes(b, T, Di, N)
+        wsbuf = torch.empty(wsb, dtype=torch.uint8, device=dev)
+
+        def e2e_step():
+            ms.mamba_scan_fwd_bwd_host(hin["delta"], hin["u"], hin["B"], hin["C"], hin["gate"],
+                                       hin["A_log"], hin["D"], hin["dy"], hout["out"],
+                                       hout["d_delta"], hout["d_u"], hout["d_B"], hout["d_C"],
+                                       hout["d_A_log"], hout["d_D"], hout["d_gate"], wsbuf,
+                                       stream=stream)
+        for _ in range(2):
+            e2e_step()
+        ke = max(3, min(args.steps, 30))
+        if pg:
+            pg.barrier()
+        t0 = time.perf_counter()
+        for _ in range(ke):
+            e2e_step()
+        el = time.perf_counter() - t0
+        if pg:
+            t = torch.tensor([el], device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            el = float(t.item())
+        h2d = sum(v.numel() * 4 for k, v in hin.items())
+        d2h = sum(v.numel() * 4 for v in hout.values())
+        e2e = {"value": ws * w.btd * ke / el, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": ke, "ms_per_step": 1e3 * el / ke}
+        del wsbuf
+
+    mb = minimal_bytes(w)
+    peaks = read_peaks()
+    bwd_mean_s = float(np.mean(bwd_ms)) * 1e-3
+    fwd_mean_s = float(np.mean(fwd_ms)) * 1e-3
+    achieved = mb["bwd"] / bwd_mean_s / 1e9
+    value = ws * w.btd * args.steps / (total_ms * 1e-3)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "T": w.T, "d_inner": w.d_inner,
+                   "d_state": w.d_state, "seed": 0,
+                   "l2": "no flush: per-step working set > 126 MB L2 "
+                         f"(inputs {4 * (4 * w.btd + 2 * w.btn) / 1e6:.0f} MB)",
+                   "parallelism": f"replicas x{ws}"},
+        "fwd_ms": 1e3 * fwd_mean_s, "bwd_ms": 1e3 * bwd_mean_s,
+        "hbm_frac_step": (mb["total"] / (total_ms * 1e-3 / args.steps) / 1e9) / peaks["hbm_gbs"],
+        "roofline": {"kernel": "mamba_scan_bwd (scan_bwd_kernel + scan_reduce_kernel)",
+                     "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "peak_source": peaks["source"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "algorithmic_bytes_per_launch": mb["bwd"]},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+def cpu_baseline(w, budget_s: float = 12.0) -> dict:
+    """The oracle as it stands (single-threaded fp64 C, forward + backward per row) on a bounded
+    sample of rows of the workload; scaled to elements/s."""
+    import oracle
+    x = oracle.as64(synth.make_inputs(w, seed=0))
+    b, T, Di, N = w.shape()
+    rows_total = b * Di
+    # calibrate on a few rows, then take as many rows as fit the budget
+    r = max(1, min(rows_total, 4))
+    t0 = time.perf_counter()
+    oracle.fwd(x, rows=(0, r))
+    oracle.bwd(x, rows=(0, r))
+    per_row = (time.perf_counter() - t0) / r
+    rows = int(max(1, min(rows_total, budget_s / max(per_row, 1e-9))))
+    out = np.full((b, T, Di), np.nan)
+    y = np.full((b, T, Di), np.nan)
+    t0 = time.perf_counter()
+    oracle.fwd(x, rows=(0, rows), out=out, y=y)
+    oracle.bwd(x, rows=(0, rows))
+    el = time.perf_counter() - t0
+    return {"value": rows * T / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{rows} of {rows_total} rows (b,d) x T={T}, fwd+bwd, fp64, 1 thread; "
+                      f"{el:.1f} s"}
+
+
+def run_reference(args):
+    """Reference arm: the fp64 CPU oracle timed on the host cores, on a bounded sample of the
+    same workload per step; rank 0 only."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    w = synth.BY_NAME[args.workload]
+    x = oracle.as64(synth.make_inputs(w, seed=0))
+    b, T, Di, N = w.shape()
+    rows_total = b * Di
+    t0 = time.perf_counter()
+    oracle.bwd(x, rows=(0, 2))
+    oracle.fwd(x, rows=(0, 2))
+    per_row = (time.perf_counter() - t0) / 2
+    total_budget = 120.0
+    rows = int(max(1, min(rows_total, total_budget / max(1, args.steps + args.warmup) / per_row)))
+    out = np.full((b, T, Di), np.nan)
+    y = np.full((b, T, Di), np.nan)
+    for _ in range(args.warmup):
+        oracle.fwd(x, rows=(0, rows), out=out, y=y)
+        oracle.bwd(x, rows=(0, rows))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.fwd(x, rows=(0, rows), out=out, y=y)
+        oracle.bwd(x, rows=(0, rows))
+    el = time.perf_counter() - t0
+    value = rows * T * args.steps / el
+    sample = f"{rows} of {rows_total} rows (b,d) x T={T} per step, fwd+bwd, fp64, 1 thread"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "T": w.T, "d_inner": w.d_inner,
+                   "d_state": w.d_state, "seed": 0},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.BY_NAME))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,124 @@
+/*
+ * mamba_scan.h: C ABI of the GB300 (sm_103a) selective-scan library, libmambascan.so.
+ *
+ * The operation is the selective state-space scan of a Mamba layer and its reverse-time
+ * backward (BPTT). With A = -exp(A_log), it runs independently for every row (b, d) and every
+ * state n:
+ *
+ *   h_t[d,n] = exp(delta_t[d] * A[d,n]) * h_{t-1}[d,n] + delta_t[d] * u_t[d] * B_t[n],  h_{-1} = 0
+ *   y_t[d]   = sum_n C_t[n] * h_t[d,n] + D[d] * u_t[d]
+ *   out_t[d] = y_t[d] * SiLU(gate_t[d])
+ *
+ * The backward follows mamba-rs src/mamba_ssm/cpu/backward.rs. Phase B2 is the gating
+ * backward: d_y = dy * SiLU(gate), d_gate = dy * y * sigmoid(g) * (1 + g * (1 - sigmoid(g))).
+ * Phase B3 is the sequential SSM BPTT. Running t from T-1 down to 0 with d_h = 0 at t = T, it
+ * does d_h += d_y*C, then accumulates d_delta, d_u, d_B, d_C, d_A_log and d_D, and finally
+ * sets d_h = exp(delta*A) * d_h. The pre-computation a_neg = -exp(A_log), which saves
+ * d_inner*d_state transcendentals per step, is that file's "O3" optimisation. Here it runs
+ * once per call, inside the kernels.
+ *
+ * Conventions for every entry point below.
+ *  - Tensors are float32, row-major, dense, in DEVICE memory owned by the caller:
+ *      delta, u, gate, dy, out, y, d_delta, d_u, d_gate : [batch, T, d_inner]  (d fastest)
+ *      B, C, d_B, d_C                                   : [batch, T, d_state]  (n fastest)
+ *      A_log, d_A_log                                   : [d_inner, d_state]
+ *      D, d_D                                           : [d_inner]
+ *    Every pointer must be 16-byte aligned. Inputs are read-only. Outputs must not alias any
+ *    input or one another.
+ *  - The library never allocates or frees memory. The checkpoint buffer and the scratch
+ *    buffer are sized by the *_bytes functions and owned by the caller.
+ *  - Calls are asynchronous on `stream`. `stream` is a cudaStream_t passed as void*; NULL
+ *    means the legacy default stream. The call returns after enqueueing the work, and errors
+ *    that surface only on the device appear at the next synchronisation
+ *    (see mamba_scan_status).
+ *  - Gradients are OVERWRITTEN, not accumulated. This deviates from the page's `+=` into
+ *    weight gradients. d_A_log and d_D are summed over batch and time, d_B and d_C over
+ *    d_inner.
+ *  - dy is the gradient of the loss with respect to `out`. d_delta is taken with respect to
+ *    the post-softplus delta that is passed in, and d_gate with respect to the pre-SiLU gate.
+ *  - Sizes: batch >= 1, T >= 1, d_inner >= 1, 1 <= d_state <= 64, batch <= 65535,
+ *    batch*T*d_inner < 2^31 and batch*T*d_state < 2^31.
+ *  - Results are deterministic: the same inputs give bitwise-identical outputs on every call.
+ *
+ * Return codes (int): MAMBA_OK or one of the errors below. On any error nothing is launched,
+ * except for MAMBA_ERR_CUDA, which reports a launch failure.
+ */
+#ifndef MAMBA_SCAN_H
+#define MAMBA_SCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MAMBA_OK 0
+#define MAMBA_ERR_INVALID_ARG 1 /* null pointer, size out of range, or aliasing outputs      */
+#define MAMBA_ERR_MISALIGNED 2  /* a pointer is not 16-byte aligned                          */
+#define MAMBA_ERR_WORKSPACE 3   /* checkpoint or scratch buffer smaller than required        */
+#define MAMBA_ERR_CUDA 4        /* a CUDA runtime call or kernel launch failed               */
+#define MAMBA_ERR_UNSUPPORTED 5 /* d_state outside 1..64                                     */
+
+/* Bytes of the checkpoint buffer that mamba_scan_fwd writes and mamba_scan_bwd reads. The
+ * forward stores the state h at every chunk boundary of the time axis, so that the backward
+ * recomputes h inside one chunk at a time instead of storing it for every t. May be 0 (then
+ * the ckpt pointer may be NULL). Returns 0 for invalid sizes as well; mamba_scan_fwd then
+ * reports the error. */
+size_t mamba_scan_ckpt_bytes(int64_t batch, int64_t T, int64_t d_inner, int64_t d_state);
+
+/* Bytes of the scratch buffer mamba_scan_bwd needs for its deterministic two-level reductions
+ * (per-CTA partial sums of d_B, d_C, d_A_log, d_D, summed in a fixed order by a second kernel).
+ * The contents need no initialisation and are meaningless after the call. */
+size_t mamba_scan_scratch_bytes(int64_t batch, int64_t T, int64_t d_inner, int64_t d_state);
+
+/* Forward scan. Writes out and, when y is non-NULL, y = sum_n C*h + D*u (the pre-gate
+ * output). Writes the checkpoint buffer (ckpt_bytes >= mamba_scan_ckpt_bytes(...)).
+ * Mamba-rs keeps h_prev, h_curr and exp(delta*A) for every t (the "MambaLayerFlat"
+ * activations); this library keeps only the chunk-boundary states. */
+int mamba_scan_fwd(const float* delta, const float* u, const float* B, const float* C,
+                   const float* gate, const float* A_log, const float* D, float* out, float* y,
+                   void* ckpt, size_t ckpt_bytes, int64_t batch, int64_t T, int64_t d_inner,
+                   int64_t d_state, void* stream);
+
+/* Backward scan (Phases B2 and B3 of the page). Needs the inputs of the matching forward call
+ * and the checkpoint buffer it wrote. Writes all seven gradients. The scratch buffer must hold
+ * mamba_scan_scratch_bytes(...) bytes. Scratch and ckpt must not overlap each other or any
+ * other argument. */
+int mamba_scan_bwd(const float* delta, const float* u, const float* B, const float* C,
+                   const float* gate, const float* A_log, const float* D, const float* dy,
+                   const void* ckpt, size_t ckpt_bytes, void* scratch, size_t scratch_bytes,
+                   float* d_delta, float* d_u, float* d_B, float* d_C, float* d_A_log,
+                   float* d_D, float* d_gate, int64_t batch, int64_t T, int64_t d_inner,
+                   int64_t d_state, void* stream);
+
+/* End-to-end call for callers that hold their data in HOST memory (pinned memory lets the
+ * copies overlap; pageable memory works too, but more slowly). The call copies the eight
+ * inputs host->device into `workspace`, runs the forward and the backward there, copies out
+ * and the seven gradients device->host, and synchronises `stream` before it returns. All
+ * tensor pointers here are HOST pointers, with the same layouts as above. `workspace` is DEVICE
+ * memory of at least mamba_scan_host_workspace_bytes(...) bytes, owned by the caller. */
+size_t mamba_scan_host_workspace_bytes(int64_t batch, int64_t T, int64_t d_inner, int64_t d_state);
+int mamba_scan_fwd_bwd_host(const float* delta, const float* u, const float* B, const float* C,
+                            const float* gate, const float* A_log, const float* D,
+                            const float* dy, float* out, float* d_delta, float* d_u, float* d_B,
+                            float* d_C, float* d_A_log, float* d_D, float* d_gate,
+                            void* workspace, size_t workspace_bytes, int64_t batch, int64_t T,
+                            int64_t d_inner, int64_t d_state, void* stream);
+
+/* Synchronises `stream` and reports any asynchronous CUDA error (MAMBA_OK or
+ * MAMBA_ERR_CUDA). */
+int mamba_scan_status(void* stream);
+
+/* Static, human-readable text of a return code. When the code is MAMBA_ERR_CUDA it names the
+ * last CUDA error this library saw. Never NULL. */
+const char* mamba_scan_strerror(int code);
+
+/* Number of kernel launches the last successful mamba_scan_fwd / mamba_scan_bwd call on this
+ * host thread enqueued. The bench's launch count relies on it. */
+int mamba_scan_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MAMBA_SCAN_H */

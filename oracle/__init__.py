@@ -94,14 +94,17 @@ def _dims(x):
 _FWD_KEYS = ("delta", "u", "B", "C", "gate", "A_log", "D")
 
 
-def fwd(x: dict, rows=None, lib=None):
+def fwd(x: dict, rows=None, lib=None, out=None, y=None):
     """Forward. Returns (out, y) as float64 [batch, T, d_inner]. ``rows``: optional (begin, end)
-    row range (row = b*d_inner + d); other rows are left as NaN."""
+    row range (row = b*d_inner + d); other rows are left as NaN, or untouched when the caller
+    passes its own float64 ``out`` and ``y`` arrays (threads may fill disjoint rows of them)."""
     x = as64(x)
     b, T, Di, N = _dims(x)
     r0, r1 = rows if rows is not None else (0, b * Di)
-    out = np.full((b, T, Di), np.nan)
-    y = np.full((b, T, Di), np.nan)
+    if out is None:
+        out = np.full((b, T, Di), np.nan)
+    if y is None:
+        y = np.full((b, T, Di), np.nan)
     rc = (lib or _load()).mamba_oracle_fwd_rows(*[_p(x[k]) for k in _FWD_KEYS], b, T, Di, N, r0, r1,
                                         _p(out), _p(y))
     if rc != 0:

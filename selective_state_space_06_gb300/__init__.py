@@ -1,0 +1,226 @@
+"""Python binding of libmambascan.so, the GB300 selective-scan library.
+
+The binding only marshals arguments. Every step of the scan runs in the library's CUDA kernels.
+There is no fallback of any kind: if the library has not been built, importing this package
+raises ImportError. To build it, run ``python -m selective_state_space_06_gb300.build`` or
+``__graft_entry__.build()``.
+
+The functions mirror the C ABI in include/mamba_scan.h and keep its names:
+  mamba_scan_ckpt_bytes, mamba_scan_scratch_bytes, mamba_scan_fwd, mamba_scan_bwd,
+  mamba_scan_host_workspace_bytes, mamba_scan_fwd_bwd_host, mamba_scan_status,
+  mamba_scan_strerror, mamba_scan_last_launch_count.
+Tensor arguments are torch tensors: float32, contiguous, on a CUDA device. The host entry point
+takes CPU tensors instead. ``stream`` defaults to torch's current stream on the tensors' device.
+Nonzero return codes raise MambaScanError.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmambascan.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python -m selective_state_space_06_gb300.build` "
+        "(nvcc, sm_103a). This package has no CPU or Python fallback.")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+MAMBA_OK = 0
+MAMBA_ERR_INVALID_ARG = 1
+MAMBA_ERR_MISALIGNED = 2
+MAMBA_ERR_WORKSPACE = 3
+MAMBA_ERR_CUDA = 4
+MAMBA_ERR_UNSUPPORTED = 5
+
+EXPORTED = (
+    "mamba_scan_ckpt_bytes", "mamba_scan_scratch_bytes", "mamba_scan_fwd", "mamba_scan_bwd",
+    "mamba_scan_host_workspace_bytes", "mamba_scan_fwd_bwd_host", "mamba_scan_status",
+    "mamba_scan_strerror", "mamba_scan_last_launch_count",
+)
+
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_sz = ctypes.c_size_t
+
+_lib.mamba_scan_ckpt_bytes.argtypes = [_i64] * 4
+_lib.mamba_scan_ckpt_bytes.restype = _sz
+_lib.mamba_scan_scratch_bytes.argtypes = [_i64] * 4
+_lib.mamba_scan_scratch_bytes.restype = _sz
+_lib.mamba_scan_host_workspace_bytes.argtypes = [_i64] * 4
+_lib.mamba_scan_host_workspace_bytes.restype = _sz
+_lib.mamba_scan_fwd.argtypes = [_vp] * 10 + [_sz] + [_i64] * 4 + [_vp]
+_lib.mamba_scan_fwd.restype = ctypes.c_int
+_lib.mamba_scan_bwd.argtypes = [_vp] * 9 + [_sz, _vp, _sz] + [_vp] * 7 + [_i64] * 4 + [_vp]
+_lib.mamba_scan_bwd.restype = ctypes.c_int
+_lib.mamba_scan_fwd_bwd_host.argtypes = [_vp] * 17 + [_sz] + [_i64] * 4 + [_vp]
+_lib.mamba_scan_fwd_bwd_host.restype = ctypes.c_int
+_lib.mamba_scan_status.argtypes = [_vp]
+_lib.mamba_scan_status.restype = ctypes.c_int
+_lib.mamba_scan_strerror.argtypes = [ctypes.c_int]
+_lib.mamba_scan_strerror.restype = ctypes.c_char_p
+_lib.mamba_scan_last_launch_count.argtypes = []
+_lib.mamba_scan_last_launch_count.restype = ctypes.c_int
+
+
+class MambaScanError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: error {code}: {mamba_scan_strerror(code)}")
+
+
+def raw_library() -> ctypes.CDLL:
+    """The ctypes handle of libmambascan.so (for callers that pass raw pointers)."""
+    return _lib
+
+
+def mamba_scan_strerror(code: int) -> str:
+    return _lib.mamba_scan_strerror(int(code)).decode()
+
+
+def mamba_scan_ckpt_bytes(batch: int, T: int, d_inner: int, d_state: int) -> int:
+    return int(_lib.mamba_scan_ckpt_bytes(batch, T, d_inner, d_state))
+
+
+def mamba_scan_scratch_bytes(batch: int, T: int, d_inner: int, d_state: int) -> int:
+    return int(_lib.mamba_scan_scratch_bytes(batch, T, d_inner, d_state))
+
+
+def mamba_scan_host_workspace_bytes(batch: int, T: int, d_inner: int, d_state: int) -> int:
+    return int(_lib.mamba_scan_host_workspace_bytes(batch, T, d_inner, d_state))
+
+
+def mamba_scan_last_launch_count() -> int:
+    return int(_lib.mamba_scan_last_launch_count())
+
+
+def _ptr(t, name, device=None, allow_none=False, host=False):
+    if t is None:
+        if allow_none:
+            return None
+        raise ValueError(f"{name} is required")
+    import torch
+    if t.dtype != torch.float32 and name not in ("ckpt", "scratch", "workspace"):
+        raise TypeError(f"{name} must be float32, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if host:
+        if t.is_cuda:
+            raise ValueError(f"{name} must be a host (CPU) tensor")
+    else:
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if device is not None and t.device != device:
+            raise ValueError(f"{name} is on {t.device}, expected {device}")
+    return t.data_ptr()
+
+
+def _stream_ptr(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dims(delta, B):
+    if delta.dim() != 3 or B.dim() != 3:
+        raise ValueError("delta must be [batch, T, d_inner] and B must be [batch, T, d_state]")
+    b, T, Di = delta.shape
+    return int(b), int(T), int(Di), int(B.shape[2])
+
+
+def mamba_scan_fwd(delta, u, B, C, gate, A_log, D, out, y=None, ckpt=None, stream=None):
+    """Forward scan on device tensors. ``ckpt`` is a device buffer (any dtype) of at least
+    mamba_scan_ckpt_bytes bytes, or None when that size is 0."""
+    b, T, Di, N = _dims(delta, B)
+    dev = delta.device
+    ck_bytes = 0 if ckpt is None else ckpt.numel() * ckpt.element_size()
+    rc = _lib.mamba_scan_fwd(
+        _ptr(delta, "delta", dev), _ptr(u, "u", dev), _ptr(B, "B", dev), _ptr(C, "C", dev),
+        _ptr(gate, "gate", dev), _ptr(A_log, "A_log", dev), _ptr(D, "D", dev),
+        _ptr(out, "out", dev), _ptr(y, "y", dev, allow_none=True),
+        _ptr(ckpt, "ckpt", dev, allow_none=True), ck_bytes, b, T, Di, N, _stream_ptr(stream, dev))
+    if rc != MAMBA_OK:
+        raise MambaScanError(rc, "mamba_scan_fwd")
+
+
+def mamba_scan_bwd(delta, u, B, C, gate, A_log, D, dy, ckpt, scratch, d_delta, d_u, d_B, d_C,
+                   d_A_log, d_D, d_gate, stream=None):
+    """Backward scan on device tensors (all seven gradients are overwritten)."""
+    b, T, Di, N = _dims(delta, B)
+    dev = delta.device
+    ck_bytes = 0 if ckpt is None else ckpt.numel() * ckpt.element_size()
+    rc = _lib.mamba_scan_bwd(
+        _ptr(delta, "delta", dev), _ptr(u, "u", dev), _ptr(B, "B", dev), _ptr(C, "C", dev),
+        _ptr(gate, "gate", dev), _ptr(A_log, "A_log", dev), _ptr(D, "D", dev),
+        _ptr(dy, "dy", dev), _ptr(ckpt, "ckpt", dev, allow_none=True), ck_bytes,
+        _ptr(scratch, "scratch", dev), scratch.numel() * scratch.element_size(),
+        _ptr(d_delta, "d_delta", dev), _ptr(d_u, "d_u", dev), _ptr(d_B, "d_B", dev),
+        _ptr(d_C, "d_C", dev), _ptr(d_A_log, "d_A_log", dev), _ptr(d_D, "d_D", dev),
+        _ptr(d_gate, "d_gate", dev), b, T, Di, N, _stream_ptr(stream, dev))
+    if rc != MAMBA_OK:
+        raise MambaScanError(rc, "mamba_scan_bwd")
+
+
+def mamba_scan_fwd_bwd_host(delta, u, B, C, gate, A_log, D, dy, out, d_delta, d_u, d_B, d_C,
+                            d_A_log, d_D, d_gate, workspace, stream=None):
+    """End-to-end forward + backward from HOST tensors (ideally pinned) through a device
+    workspace of mamba_scan_host_workspace_bytes bytes; returns after the results are on the
+    host."""
+    b, T, Di, N = _dims(delta, B)
+    dev = workspace.device
+    h = dict(host=True)
+    rc = _lib.mamba_scan_fwd_bwd_host(
+        _ptr(delta, "delta", **h), _ptr(u, "u", **h), _ptr(B, "B", **h), _ptr(C, "C", **h),
+        _ptr(gate, "gate", **h), _ptr(A_log, "A_log", **h), _ptr(D, "D", **h), _ptr(dy, "dy", **h),
+        _ptr(out, "out", **h), _ptr(d_delta, "d_delta", **h), _ptr(d_u, "d_u", **h),
+        _ptr(d_B, "d_B", **h), _ptr(d_C, "d_C", **h), _ptr(d_A_log, "d_A_log", **h),
+        _ptr(d_D, "d_D", **h), _ptr(d_gate, "d_gate", **h),
+        _ptr(workspace, "workspace", dev), workspace.numel() * workspace.element_size(),
+        b, T, Di, N, _stream_ptr(stream, dev))
+    if rc != MAMBA_OK:
+        raise MambaScanError(rc, "mamba_scan_fwd_bwd_host")
+
+
+def mamba_scan_status(stream=None, device=None) -> None:
+    import torch
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    rc = _lib.mamba_scan_status(_stream_ptr(stream, dev))
+    if rc != MAMBA_OK:
+        raise MambaScanError(rc, "mamba_scan_status")
+
+
+# ----------------------------------------------------------------------------------------------
+# Convenience layer: allocate outputs and buffers with torch, then call the entry points above.
+def alloc_like_outputs(delta, B, A_log, D):
+    import torch
+    b, T, Di, N = _dims(delta, B)
+    dev = delta.device
+    ck = mamba_scan_ckpt_bytes(b, T, Di, N)
+    sc = mamba_scan_scratch_bytes(b, T, Di, N)
+    e = lambda *s: torch.empty(*s, dtype=torch.float32, device=dev)  # noqa: E731
+    return {
+        "out": e(b, T, Di), "y": e(b, T, Di),
+        "ckpt": torch.empty(max(ck, 16), dtype=torch.uint8, device=dev) if ck else None,
+        "scratch": torch.empty(max(sc, 16), dtype=torch.uint8, device=dev),
+        "d_delta": e(b, T, Di), "d_u": e(b, T, Di), "d_gate": e(b, T, Di),
+        "d_B": e(b, T, N), "d_C": e(b, T, N), "d_A_log": e(Di, N), "d_D": e(Di),
+    }
+
+
+def forward_backward(x: dict, bufs: dict | None = None, with_y: bool = True, stream=None) -> dict:
+    """Runs mamba_scan_fwd then mamba_scan_bwd on a dict of device tensors (keys delta, u, B, C,
+    gate, A_log, D, dy); returns the dict of outputs (out, y, d_delta, d_u, d_B, d_C, d_A_log,
+    d_D, d_gate plus the ckpt/scratch buffers)."""
+    if bufs is None:
+        bufs = alloc_like_outputs(x["delta"], x["B"], x["A_log"], x["D"])
+    mamba_scan_fwd(x["delta"], x["u"], x["B"], x["C"], x["gate"], x["A_log"], x["D"], bufs["out"],
+                   bufs["y"] if with_y else None, bufs["ckpt"], stream=stream)
+    mamba_scan_bwd(x["delta"], x["u"], x["B"], x["C"], x["gate"], x["A_log"], x["D"], x["dy"],
+                   bufs["ckpt"], bufs["scratch"], bufs["d_delta"], bufs["d_u"], bufs["d_B"],
+                   bufs["d_C"], bufs["d_A_log"], bufs["d_D"], bufs["d_gate"], stream=stream)
+    return bufs

@@ -1,0 +1,112 @@
+"""Parity of the CUDA path with the fp64 oracle, through the C ABI on cuda:0.
+
+The bar is max|got - ref| <= 1e-4 * max|ref| per output tensor, where ref is the fp64 oracle
+on the same float32 inputs. It is checked element by element on every output, for the five
+benchmark workloads at their full sizes (the launch configuration the bench times) and for edge
+cases: ragged T, d_inner and d_state, T = 1, delta = 0, saturated gates. Outputs are
+NaN-poisoned before every call, so an element the kernels do not write fails too.
+"""
+import numpy as np
+import pytest
+
+import synth
+from gpu_helpers import OUT_KEYS, assert_parity, oracle_all, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import selective_state_space_06_gb300  # noqa: F401  (fails loudly if the library is missing)
+
+
+@pytest.mark.parametrize("name", ["tiny", "mamba130m", "mamba370m", "mamba1p4b"])
+def test_workload_full_parity(name):
+    x = synth.make_inputs(synth.BY_NAME[name])
+    got = run_gpu(x)
+    ref = oracle_all(x)
+    assert_parity(got, ref, label=name)
+
+
+def test_longseq_full_parity():
+    """batch=1, T=65536, d_inner=2560, d_state=64: every output element against the oracle."""
+    x = synth.make_inputs(synth.BY_NAME["longseq"])
+    got = run_gpu(x)
+    ref = oracle_all(x)
+    assert_parity(got, ref, label="longseq")
+
+
+EDGE_SHAPES = [
+    # (batch, T, d_inner, d_state)
+    (1, 1, 1, 1),
+    (1, 1, 7, 16),
+    (2, 15, 3, 4),
+    (2, 16, 64, 16),
+    (2, 17, 65, 16),
+    (3, 37, 50, 5),
+    (1, 100, 130, 8),
+    (2, 33, 33, 13),
+    (1, 48, 40, 17),
+    (2, 31, 20, 32),
+    (1, 40, 18, 33),
+    (1, 64, 33, 63),
+    (2, 50, 17, 64),
+    (4, 129, 257, 16),
+]
+
+
+@pytest.mark.parametrize("shape", EDGE_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_edge_shapes(shape):
+    x = synth.random_inputs(*shape, seed=sum(shape), a_log_random=True)
+    assert_parity(run_gpu(x), oracle_all(x), label=str(shape))
+
+
+def test_delta_zero():
+    x = synth.random_inputs(2, 40, 70, 16, seed=1)
+    x["delta"][:] = 0.0
+    got = run_gpu(x)
+    ref = oracle_all(x)
+    for k in ("d_B", "d_C", "d_A_log"):
+        assert np.all(got[k] == 0.0), k
+    assert_parity(got, ref, keys=("out", "y", "d_delta", "d_u", "d_D", "d_gate"), label="delta0")
+
+
+def test_saturated_gates_and_large_delta():
+    x = synth.random_inputs(2, 40, 70, 16, seed=2)
+    x["gate"] = (x["gate"] * 60).astype(np.float32)          # sigmoid saturates both ways
+    x["delta"][:, ::5] = 40.0                                 # exp(delta*A) underflows to 0
+    got = run_gpu(x)
+    ref = oracle_all(x)
+    assert_parity(got, ref, label="saturated")
+
+
+def test_bitwise_deterministic():
+    x = synth.make_inputs(synth.BY_NAME["mamba130m"].resized(batch=2, T=300, name="det"))
+    a = run_gpu(x)
+    b = run_gpu(x)
+    for k in OUT_KEYS:
+        assert np.array_equal(a[k], b[k], equal_nan=False), k
+
+
+def test_euler_identities_full_size_longseq():
+    """Exact identities of the method at full size (out is homogeneous of degree 1 in u, B, C
+    and D). Checked on the GPU results alone, in float64 sums, at the longseq workload."""
+    x = synth.make_inputs(synth.BY_NAME["longseq"])
+    g = run_gpu(x)
+    f64 = lambda a: np.asarray(a, dtype=np.float64)  # noqa: E731
+    s = 1 / (1 + np.exp(-f64(x["gate"])))
+    w = f64(x["dy"]) * f64(x["gate"]) * s
+    y_minus_du = f64(g["y"]) - f64(x["D"]) * f64(x["u"])
+    pairs = {
+        "u": (np.sum(f64(g["d_u"]) * f64(x["u"])), np.sum(f64(x["dy"]) * f64(g["out"]))),
+        "B": (np.sum(f64(g["d_B"]) * f64(x["B"])), np.sum(w * y_minus_du)),
+        "C": (np.sum(f64(g["d_C"]) * f64(x["C"])), np.sum(w * y_minus_du)),
+        "D": (np.sum(f64(g["d_D"]) * f64(x["D"])), np.sum(w * f64(x["D"]) * f64(x["u"]))),
+    }
+    for k, (lhs, rhs) in pairs.items():
+        # relative to the sum of magnitudes: fp32 rounding of 1e8 terms
+        mag = np.sum(np.abs(w * y_minus_du)) + np.sum(np.abs(f64(x["dy"]) * f64(g["out"])))
+        assert abs(lhs - rhs) <= 1e-5 * mag, (k, lhs, rhs, mag)
