@@ -2,7 +2,7 @@
 
 The binding only marshals arguments. Every step of the scan runs in the library's CUDA kernels.
 There is no fallback of any kind: if the library has not been built, importing this package
-raises ImportError. To build it, run ``python -m selective_state_space_06_gb300.build`` or
+raises ImportError. To build it, run ``python selective_state_space_06_gb300/build.py`` or
 ``__graft_entry__.build()``.
 
 The functions mirror the C ABI in include/mamba_scan.h and keep its names:
@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(_HERE, "libmambascan.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
-        f"{LIB_PATH} is missing: build it with `python -m selective_state_space_06_gb300.build` "
+        f"{LIB_PATH} is missing: build it with `python selective_state_space_06_gb300/build.py` "
         "(nvcc, sm_103a). This package has no CPU or Python fallback.")
 
 _lib = ctypes.CDLL(LIB_PATH)

@@ -1,7 +1,8 @@
 """Builds libmambascan.so in-tree with nvcc for sm_103a (no torch extension machinery).
 
 Each .cu file compiles to an object in parallel; the objects then link into one shared
-library next to this file. ``python -m selective_state_space_06_gb300.build`` runs it.
+library next to this file. ``python selective_state_space_06_gb300/build.py`` runs it (the
+package itself cannot be imported before the library exists).
 """
 from __future__ import annotations
 
