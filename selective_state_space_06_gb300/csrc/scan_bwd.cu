@@ -1,220 +1,374 @@
-// Backward selective scan (sm_103a): the gating backward and the reverse-time SSM BPTT of
-// mamba-rs src/mamba_ssm/cpu/backward.rs (Phases B2 and B3), with h recomputed per chunk from
-// the forward's checkpoints instead of being stored for every t.
+// Backward selective scan (sm_103a). This is the gating backward and the reverse-time SSM
+// BPTT of mamba-rs src/mamba_ssm/cpu/backward.rs (Phases B2 and B3). h is recomputed per chunk
+// from the forward's checkpoints instead of being stored for every t.
 //
-// Per row (b, d), walking the chunks from last to first:
+// Per row (b, d), the chunks are walked from last to first (thread mapping as in the forward:
+// 2 channels x 4 states per thread, G lanes per channel group):
+//   0. gating (Phase B2), once per (t, d) of the chunk and cooperatively:
+//        d_y = dy * g * s  and  gfac = dy * s * (1 + g*(1 - s)),  s = sigmoid(g).
+//      Both overwrite the staged gate/dy tiles, so d_gate = y * gfac later.
 //   1. recompute: restart from the chunk's checkpoint (zero for chunk 0) and run the forward
-//      recurrence over the chunk, keeping h_t for the chunk's kChunk steps in registers;
-//   2. reverse: for t = last .. first of the chunk
-//        y = sum_n C*h_t + D*u                              (recomputed, for d_gate)
-//        d_y = dy*SiLU(g),  d_gate = dy*y*s*(1 + g*(1-s))  (Phase B2)
-//        d_h = d_h + d_y*C                                  (Phase B3, in the page's order)
+//      recurrence over the chunk, kSub steps at a time, keeping those h_t in registers;
+//   2. reverse (Phase B3, in the page's order), for t = last .. first of the chunk:
+//        d_h += d_y*C;  y = sum_n C*h_t + D*u
 //        d_delta = sum_n d_h*(A*da*h_{t-1} + u*B),  d_u = d_y*D + sum_n d_h*delta*B
-//        d_B[t,n] += d_h*delta*u,  d_C[t,n] += d_y*h_t    (summed over d)
-//        d_A_log += d_h*da*delta*A*h_{t-1},  d_D += d_y*u (summed over b, t)
+//        d_B[t,n] += d_h*delta*u,  d_C[t,n] += d_y*h_t           (over d)
+//        d_A_log += d_h*da*delta*A*h_{t-1},  d_D += d_y*u         (over b, t)
 //        d_h = da*d_h
-//   The code uses r = (da*d_h)*h_{t-1}, so the A-term of d_delta is ln2 * sum_n a2*r and
-//   d_A_log = ln2 * a2 * sum_t delta*r, where a2 = A*log2(e) is the register constant of ex2.
+//      The code forms r = (da*d_h)*h_{t-1}. With a2 = A*log2(e), the register constant of ex2,
+//      the A-term of d_delta is ln2 * sum_n a2*r and d_A_log = ln2 * a2 * sum_t delta*r.
 // Reductions, all in a fixed order (deterministic):
-//   d_B, d_C over d: in-thread over the thread's 2 channels, then an xor butterfly over the
-//   warp's channel lanes, then the CTA's warps summed through shared memory. That gives one
-//   partial per CTA, written to scratch [blk][b][t][n]. scan_reduce_kernel then sums the
-//   partials over blk in index order.
-//   d_A_log, d_D over (b, t): register accumulators over t, then one partial per b in
-//   scratch, summed over b in index order by scan_reduce_kernel.
+//   * sum over n (y, the A-term, the B-term): in-thread, then a butterfly reduce-scatter over
+//     the G state lanes, batched over P = G/2 steps. Each lane ends with one (step, channel),
+//     and stores d_delta, d_u and d_gate for it.
+//   * d_B, d_C over d: in-thread over the thread's 2 channels, then a reduce-scatter over the
+//     warp's channel lanes, then the warps summed through shared memory. That gives one partial
+//     per CTA, written to scratch [blk][b][t][n]; scan_reduce_kernel sums the partials over blk
+//     in index order.
+//   * d_A_log, d_D over (b, t): register accumulators over t, then one partial per batch row in
+//     scratch, summed over b in index order by scan_reduce_kernel.
 #include "scan_common.cuh"
 
 namespace mscan {
 
+constexpr int kBwdStages = 3;
+constexpr int kSub = 8;                  // steps kept in registers at a time
+constexpr int kNSub = kChunk / kSub;
+
 template <int NP>
+struct BwdShape {
+  static constexpr int G = NP / kNPT;
+  static constexpr int DW = (32 / G) * kDPT;
+  static constexpr int DC = kWarps * DW;
+  static constexpr int P = G >= 2 ? G / 2 : 1;
+  static constexpr int kStageFloats = kChunk * (4 * DC + 2 * NP);
+  static constexpr int kRedFloats = kWarps * kChunk * 2 * NP;
+  static constexpr size_t kSmemBytes =
+      ((size_t)kBwdStages * kStageFloats + kRedFloats) * sizeof(float);
+};
+
+template <int NP, bool VEC>
+__device__ __forceinline__ void bwd_load_chunk(const BwdParams& p, float* st, int c, int b,
+                                               int dblk0) {
+  using S = BwdShape<NP>;
+  constexpr int DC = S::DC, NTH = kWarps * 32;
+  float* s_dl = st;
+  float* s_u = st + kChunk * DC;
+  float* s_g = st + 2 * kChunk * DC;
+  float* s_dy = st + 3 * kChunk * DC;
+  float* s_B = st + 4 * kChunk * DC;
+  float* s_C = s_B + kChunk * NP;
+  const int t0 = c * kChunk;
+  const size_t rowb = (size_t)b * p.T;
+  if constexpr (VEC) {
+    for (int q = threadIdx.x; q < kChunk * DC / 4; q += NTH) {
+      const int i = q / (DC / 4), col = (q % (DC / 4)) * 4;
+      const int t = t0 + i, d = dblk0 + col;
+      const bool v = t < p.T && d < p.Di;
+      const size_t go = v ? (rowb + t) * p.Di + d : 0;
+      cp_async16(s_dl + i * DC + col, p.delta + go, v);
+      cp_async16(s_u + i * DC + col, p.u + go, v);
+      cp_async16(s_g + i * DC + col, p.gate + go, v);
+      cp_async16(s_dy + i * DC + col, p.dy + go, v);
+    }
+    for (int q = threadIdx.x; q < kChunk * NP / 4; q += NTH) {
+      const int i = q / (NP / 4), n = (q % (NP / 4)) * 4;
+      const int t = t0 + i;
+      const bool v = t < p.T && n < p.N;
+      const size_t go = v ? (rowb + t) * p.N + n : 0;
+      cp_async16(s_B + i * NP + n, p.B + go, v);
+      cp_async16(s_C + i * NP + n, p.C + go, v);
+    }
+  } else {
+    for (int q = threadIdx.x; q < kChunk * DC; q += NTH) {
+      const int i = q / DC, col = q % DC;
+      const int t = t0 + i, d = dblk0 + col;
+      const bool v = t < p.T && d < p.Di;
+      const size_t go = v ? (rowb + t) * p.Di + d : 0;
+      cp_async4(s_dl + i * DC + col, p.delta + go, v);
+      cp_async4(s_u + i * DC + col, p.u + go, v);
+      cp_async4(s_g + i * DC + col, p.gate + go, v);
+      cp_async4(s_dy + i * DC + col, p.dy + go, v);
+    }
+    for (int q = threadIdx.x; q < kChunk * NP; q += NTH) {
+      const int i = q / NP, n = q % NP;
+      const int t = t0 + i;
+      const bool v = t < p.T && n < p.N;
+      const size_t go = v ? (rowb + t) * p.N + n : 0;
+      cp_async4(s_B + i * NP + n, p.B + go, v);
+      cp_async4(s_C + i * NP + n, p.C + go, v);
+    }
+  }
+  cp_async_commit();
+}
+
+// Forward recurrence of step i of the staged chunk on the thread's 2 x 4 states hc.
+template <int NP, int DC>
+__device__ __forceinline__ void bwd_step_fwd(int i, const float* s_dl, const float* s_u,
+                                             const float* s_B, int cl, int n0,
+                                             const float2 (&a2)[kDPT][2], float2 (&hc)[kDPT][2]) {
+  const float2 dlv = *reinterpret_cast<const float2*>(s_dl + i * DC + cl);
+  const float2 uv = *reinterpret_cast<const float2*>(s_u + i * DC + cl);
+  const float4 Bv = *reinterpret_cast<const float4*>(s_B + i * NP + n0);
+  const float2 Bp[2] = {make_float2(Bv.x, Bv.y), make_float2(Bv.z, Bv.w)};
+#pragma unroll
+  for (int j = 0; j < kDPT; ++j) {
+    const float dl = j ? dlv.y : dlv.x;
+    const float uu = j ? uv.y : uv.x;
+    const float2 dl2 = splat2(dl), du2 = splat2(dl * uu);
+#pragma unroll
+    for (int pp = 0; pp < 2; ++pp) {
+      const float2 da = ex2_2(mul2(dl2, a2[j][pp]));
+      hc[j][pp] = fma2(da, hc[j][pp], mul2(du2, Bp[pp]));
+    }
+  }
+}
+
+template <int NP, bool VEC>
 __global__ void __launch_bounds__(kWarps * 32)
 scan_bwd_kernel(const BwdParams p) {
-  constexpr int G = NP / kNPT;
-  constexpr int DW = (32 / G) * kDPT;
-  constexpr int DC = kWarps * DW;
-  __shared__ float redB[kWarps][kChunk][NP];
-  __shared__ float redC[kWarps][kChunk][NP];
+  using S = BwdShape<NP>;
+  constexpr int G = S::G, DW = S::DW, DC = S::DC, P = S::P, NTH = kWarps * 32;
+  extern __shared__ __align__(16) float smem[];
+  float* red = smem + kBwdStages * S::kStageFloats;   // [kWarps][kChunk][2*NP]
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ng = lane % G, dg = lane / G;
   const int b = blockIdx.y;
-  const int d0 = blockIdx.x * DC + warp * DW + dg * kDPT;
+  const int dblk0 = blockIdx.x * DC;
+  const int cl = warp * DW + dg * kDPT;
+  const int d0 = dblk0 + cl;
   const int n0 = ng * kNPT;
   const int Di = p.Di, N = p.N, T = p.T;
 
-  bool dv[kDPT];
-  float a2[kDPT][kNPT], dh[kDPT][kNPT], accA[kDPT][kNPT], Dd[kDPT], dD[kDPT];
+  float2 a2[kDPT][2], dh[kDPT][2], accA[kDPT][2];
+  float Dd[kDPT], dD[kDPT];
 #pragma unroll
   for (int j = 0; j < kDPT; ++j) {
     const int d = d0 + j;
-    dv[j] = d < Di;
-    Dd[j] = dv[j] ? p.D[d] : 0.f;
+    const bool dv = d < Di;
+    Dd[j] = dv ? p.D[d] : 0.f;
     dD[j] = 0.f;
+    float t4[kNPT];
 #pragma unroll
     for (int k = 0; k < kNPT; ++k) {
       const int n = n0 + k;
-      a2[j][k] = (dv[j] && n < N) ? -expf(p.A_log[(size_t)d * N + n]) * kLog2e : 0.f;
-      dh[j][k] = 0.f;
-      accA[j][k] = 0.f;
+      t4[k] = (dv && n < N) ? -expf(p.A_log[(size_t)d * N + n]) * kLog2e : 0.f;
     }
+    a2[j][0] = make_float2(t4[0], t4[1]);
+    a2[j][1] = make_float2(t4[2], t4[3]);
+    dh[j][0] = dh[j][1] = accA[j][0] = accA[j][1] = make_float2(0.f, 0.f);
   }
-  const bool owner[kDPT] = {ng == 0, ng == (G > 1 ? 1 : 0)};
-  const size_t row0 = (size_t)b * T;
 
-  for (int c = p.nchunks - 1; c >= 0; --c) {
-    const int t0 = c * kChunk;
-    const int len = min(kChunk, T - t0);
-    const float* ck = (c > 0) ? p.ckpt + ((size_t)b * (p.nchunks - 1) + (c - 1)) * (size_t)Di * N
-                              : nullptr;
+  using RSn = ReduceScatter<6 * P, G / 2, 1>;    // (y, A-term, B-term) x 2 channels x P steps
+  using RSd = ReduceScatter<8, 16, G>;            // (d_B x 4, d_C x 4) over the channel lanes
+  const int nbase = RSn::base(lane);
+  constexpr int kN = RSn::kept();
+  const int dbase = RSd::base(lane);
+  const bool dwriter = RSd::writer(lane);
+  constexpr int kD = RSd::kept();
+  const size_t rowb = (size_t)b * T;
+  const int last = p.nchunks - 1;
 
-    // ---- 1. recompute h over the chunk --------------------------------------------------
-    float hs[kChunk][kDPT][kNPT];
+#pragma unroll
+  for (int s = 0; s < kBwdStages - 1; ++s) {
+    if (last - s >= 0) bwd_load_chunk<NP, VEC>(p, smem + s * S::kStageFloats, last - s, b, dblk0);
+    else cp_async_commit();
+  }
+
+  for (int it = 0; it <= last; ++it) {
+    const int c = last - it;
+    cp_async_wait<kBwdStages - 2>();
+    __syncthreads();
     {
-      float hc[kDPT][kNPT];
+      const int itn = it + kBwdStages - 1;
+      if (last - itn >= 0)
+        bwd_load_chunk<NP, VEC>(p, smem + (itn % kBwdStages) * S::kStageFloats, last - itn, b,
+                                dblk0);
+      else
+        cp_async_commit();
+    }
+    float* st = smem + (it % kBwdStages) * S::kStageFloats;
+    const float* s_dl = st;
+    const float* s_u = st + kChunk * DC;
+    float* s_g = st + 2 * kChunk * DC;    // becomes d_y
+    float* s_dy = st + 3 * kChunk * DC;   // becomes gfac
+    const float* s_B = st + 4 * kChunk * DC;
+    const float* s_C = s_B + kChunk * NP;
+    const int t0 = c * kChunk;
+
+    // ---- 0. gating backward for the whole chunk tile -------------------------------------
+    for (int e = threadIdx.x; e < kChunk * DC; e += NTH) {
+      const float g = s_g[e], go = s_dy[e];
+      const float s = sigmoid_fast(g);
+      s_g[e] = go * (g * s);
+      s_dy[e] = go * (s * fmaf(g, 1.f - s, 1.f));
+    }
+    __syncthreads();
+
+    // ---- 1./2. recompute + reverse, one sub-block of kSub steps at a time ----------------
+    // The sub-block start states come from one recompute pass without stash. Then, for each
+    // sub-block from last to first, the states are recomputed into registers and walked in
+    // reverse. That is 1.5x the recompute work of a full-chunk stash, but half the registers.
+    const float* ck = (c > 0) ? p.ckpt + ((size_t)b * last + (c - 1)) * (size_t)Di * N : nullptr;
+    float2 hsub[kNSub][kDPT][2];
 #pragma unroll
-      for (int j = 0; j < kDPT; ++j)
+    for (int j = 0; j < kDPT; ++j) {
+      const int d = d0 + j;
+      float hv[kNPT] = {0.f, 0.f, 0.f, 0.f};
+      if (ck && d < Di) {
+        if constexpr (VEC) {
+          const float4 q = *reinterpret_cast<const float4*>(ck + (size_t)d * N + n0);
+          hv[0] = q.x; hv[1] = q.y; hv[2] = q.z; hv[3] = q.w;
+        } else {
 #pragma unroll
-        for (int k = 0; k < kNPT; ++k)
-          hc[j][k] = (ck && dv[j] && n0 + k < N) ? ck[(size_t)(d0 + j) * N + n0 + k] : 0.f;
+          for (int k = 0; k < kNPT; ++k)
+            if (n0 + k < N) hv[k] = ck[(size_t)d * N + n0 + k];
+        }
+      }
+      hsub[0][j][0] = make_float2(hv[0], hv[1]);
+      hsub[0][j][1] = make_float2(hv[2], hv[3]);
+    }
+    {
+      float2 hc[kDPT][2] = {{hsub[0][0][0], hsub[0][0][1]}, {hsub[0][1][0], hsub[0][1][1]}};
 #pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
-        if (i < len) {
-          const size_t xo = (row0 + t0 + i) * Di;
-          const size_t bo = (row0 + t0 + i) * N;
-          float dl[kDPT], uu[kDPT], Bn[kNPT];
+      for (int sb = 1; sb < kNSub; ++sb) {
+#pragma unroll
+        for (int q = 0; q < kSub; ++q)
+          bwd_step_fwd<NP, DC>((sb - 1) * kSub + q, s_dl, s_u, s_B, cl, n0, a2, hc);
+#pragma unroll
+        for (int j = 0; j < kDPT; ++j) {
+          hsub[sb][j][0] = hc[j][0];
+          hsub[sb][j][1] = hc[j][1];
+        }
+      }
+    }
+
+#pragma unroll
+    for (int sq = 0; sq < kNSub; ++sq) {
+      const int sb = kNSub - 1 - sq;
+      float2 hs[kSub][kDPT][2];
+      {
+        float2 hc[kDPT][2] = {{hsub[sb][0][0], hsub[sb][0][1]}, {hsub[sb][1][0], hsub[sb][1][1]}};
+#pragma unroll
+        for (int q = 0; q < kSub; ++q) {
+          step_fence();
+          bwd_step_fwd<NP, DC>(sb * kSub + q, s_dl, s_u, s_B, cl, n0, a2, hc);
 #pragma unroll
           for (int j = 0; j < kDPT; ++j) {
-            dl[j] = dv[j] ? ld_stream(p.delta + xo + d0 + j) : 0.f;
-            uu[j] = dv[j] ? ld_stream(p.u + xo + d0 + j) : 0.f;
+            hs[q][j][0] = hc[j][0];
+            hs[q][j][1] = hc[j][1];
           }
+        }
+      }
 #pragma unroll
-          for (int k = 0; k < kNPT; ++k) Bn[k] = (n0 + k < N) ? ld_stream(p.B + bo + n0 + k) : 0.f;
+      for (int gq = 0; gq < kSub / P; ++gq) {
+        const int gl = kSub / P - 1 - gq;          // group inside the sub-block
+        float vn[6 * P];
+#pragma unroll
+        for (int tq = 0; tq < P; ++tq) {
+          const int tt = P - 1 - tq;
+          const int q = gl * P + tt;               // step inside the sub-block
+          const int i = sb * kSub + q;             // step inside the chunk
+          step_fence();
+          const float2 dlv = *reinterpret_cast<const float2*>(s_dl + i * DC + cl);
+          const float2 uv = *reinterpret_cast<const float2*>(s_u + i * DC + cl);
+          const float2 dyv = *reinterpret_cast<const float2*>(s_g + i * DC + cl);
+          const float4 Bv = *reinterpret_cast<const float4*>(s_B + i * NP + n0);
+          const float4 Cv = *reinterpret_cast<const float4*>(s_C + i * NP + n0);
+          const float2 Bp[2] = {make_float2(Bv.x, Bv.y), make_float2(Bv.z, Bv.w)};
+          const float2 Cp[2] = {make_float2(Cv.x, Cv.y), make_float2(Cv.z, Cv.w)};
+          float2 xb[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+          float2 xc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
           for (int j = 0; j < kDPT; ++j) {
-            const float du = dl[j] * uu[j];
+            const float dl = j ? dlv.y : dlv.x;
+            const float uu = j ? uv.y : uv.x;
+            const float dyj = j ? dyv.y : dyv.x;
+            const float2 dl2 = splat2(dl), du2 = splat2(dl * uu), dy2 = splat2(dyj);
+            float2 ya = make_float2(0.f, 0.f), sa = ya, sb2 = ya;
 #pragma unroll
-            for (int k = 0; k < kNPT; ++k) {
-              const float da = ex2_sfu(dl[j] * a2[j][k]);
-              hc[j][k] = fmaf(da, hc[j][k], du * Bn[k]);
-              hs[i][j][k] = hc[j][k];
+            for (int pp = 0; pp < 2; ++pp) {
+              const float2 hcur = hs[q][j][pp];
+              const float2 hprev = (q > 0) ? hs[q > 0 ? q - 1 : 0][j][pp] : hsub[sb][j][pp];
+              ya = fma2(Cp[pp], hcur, ya);
+              const float2 da = ex2_2(mul2(dl2, a2[j][pp]));
+              const float2 gh = fma2(dy2, Cp[pp], dh[j][pp]);   // d_h += d_y*C
+              const float2 cr = mul2(da, gh);                    // carried to t-1
+              const float2 r = mul2(cr, hprev);                  // d_h*da*h_{t-1}
+              accA[j][pp] = fma2(r, dl2, accA[j][pp]);
+              sa = fma2(a2[j][pp], r, sa);
+              sb2 = fma2(gh, Bp[pp], sb2);
+              xb[pp] = fma2(gh, du2, xb[pp]);
+              xc[pp] = fma2(dy2, hcur, xc[pp]);
+              dh[j][pp] = cr;
+            }
+            vn[(tt * 2 + j) * 3 + 0] = ya.x + ya.y;
+            vn[(tt * 2 + j) * 3 + 1] = sa.x + sa.y;
+            vn[(tt * 2 + j) * 3 + 2] = sb2.x + sb2.y;
+            dD[j] = fmaf(dyj, uu, dD[j]);
+          }
+          // d_B / d_C of this step: sum over the warp's channels
+          float vd[8] = {xb[0].x, xb[0].y, xb[1].x, xb[1].y, xc[0].x, xc[0].y, xc[1].x, xc[1].y};
+          RSd::run(vd, lane);
+          if (dwriter) {
+#pragma unroll
+            for (int r = 0; r < kD; ++r) {
+              const int idx = dbase + r;        // 0..3: d_B of state n0+idx, 4..7: d_C
+              red[(warp * kChunk + i) * 2 * NP + (idx >> 2) * NP + n0 + (idx & 3)] = vd[r];
             }
           }
         }
-      }
-    }
-
-    // ---- 2. reverse recurrence over the chunk -------------------------------------------
+        // sums over n, scattered so that each lane finishes one (step, channel)
+        RSn::run(vn, lane);
 #pragma unroll
-    for (int ii = 0; ii < kChunk; ++ii) {
-      const int i = kChunk - 1 - ii;
-      if (i < len) {
-        const size_t xo = (row0 + t0 + i) * Di;
-        const size_t bo = (row0 + t0 + i) * N;
-        float dl[kDPT], uu[kDPT], gt[kDPT], go[kDPT], Bn[kNPT], Cn[kNPT];
-#pragma unroll
-        for (int j = 0; j < kDPT; ++j) {
-          dl[j] = dv[j] ? ld_stream(p.delta + xo + d0 + j) : 0.f;
-          uu[j] = dv[j] ? ld_stream(p.u + xo + d0 + j) : 0.f;
-          gt[j] = dv[j] ? ld_stream(p.gate + xo + d0 + j) : 0.f;
-          go[j] = dv[j] ? ld_stream(p.dy + xo + d0 + j) : 0.f;
-        }
-#pragma unroll
-        for (int k = 0; k < kNPT; ++k) {
-          Bn[k] = (n0 + k < N) ? ld_stream(p.B + bo + n0 + k) : 0.f;
-          Cn[k] = (n0 + k < N) ? ld_stream(p.C + bo + n0 + k) : 0.f;
-        }
-        // state before step i: the previous stash entry, or the chunk's checkpoint
-        float hp[kDPT][kNPT];
-#pragma unroll
-        for (int j = 0; j < kDPT; ++j)
-#pragma unroll
-          for (int k = 0; k < kNPT; ++k) {
-            if (i > 0) hp[j][k] = hs[i > 0 ? i - 1 : 0][j][k];
-            else hp[j][k] = (ck && dv[j] && n0 + k < N) ? ck[(size_t)(d0 + j) * N + n0 + k] : 0.f;
-          }
-
-        float y[kDPT], s[kDPT], d_y[kDPT];
-#pragma unroll
-        for (int j = 0; j < kDPT; ++j) {
-          float yp = 0.f;
-#pragma unroll
-          for (int k = 0; k < kNPT; ++k) yp = fmaf(Cn[k], hs[i][j][k], yp);
-          y[j] = fmaf(Dd[j], uu[j], sum_over_state_lanes<G>(yp));
-          s[j] = sigmoid_fast(gt[j]);
-          d_y[j] = go[j] * (gt[j] * s[j]);
-        }
-
-        float sA[kDPT], sB[kDPT], xb[kNPT], xc[kNPT];
-#pragma unroll
-        for (int k = 0; k < kNPT; ++k) { xb[k] = 0.f; xc[k] = 0.f; }
-#pragma unroll
-        for (int j = 0; j < kDPT; ++j) {
-          const float du = dl[j] * uu[j];
-          sA[j] = 0.f;
-          sB[j] = 0.f;
-#pragma unroll
-          for (int k = 0; k < kNPT; ++k) {
-            const float da = ex2_sfu(dl[j] * a2[j][k]);
-            const float gh = fmaf(d_y[j], Cn[k], dh[j][k]);   // d_h += d_y*C
-            const float cr = da * gh;                          // carry to t-1
-            const float r = cr * hp[j][k];                     // d_h*da*h_{t-1}
-            accA[j][k] = fmaf(r, dl[j], accA[j][k]);
-            sA[j] = fmaf(a2[j][k], r, sA[j]);
-            sB[j] = fmaf(gh, Bn[k], sB[j]);
-            xb[k] = fmaf(gh, du, xb[k]);
-            xc[k] = fmaf(d_y[j], hs[i][j][k], xc[k]);
-            dh[j][k] = cr;
-          }
-          sA[j] = sum_over_state_lanes<G>(sA[j]);
-          sB[j] = sum_over_state_lanes<G>(sB[j]);
-          dD[j] = fmaf(d_y[j], uu[j], dD[j]);
-        }
-#pragma unroll
-        for (int j = 0; j < kDPT; ++j) {
-          if (dv[j] && owner[j]) {
-            p.d_delta[xo + d0 + j] = fmaf(sA[j], kLn2, uu[j] * sB[j]);
-            p.d_u[xo + d0 + j] = fmaf(d_y[j], Dd[j], dl[j] * sB[j]);
-            p.d_gate[xo + d0 + j] = go[j] * y[j] * (s[j] * fmaf(gt[j], 1.f - s[j], 1.f));
-          }
-        }
-#pragma unroll
-        for (int k = 0; k < kNPT; ++k) {
-          xb[k] = sum_over_channel_lanes<G>(xb[k]);
-          xc[k] = sum_over_channel_lanes<G>(xc[k]);
-          if (dg == 0) {
-            redB[warp][i][n0 + k] = xb[k];
-            redC[warp][i][n0 + k] = xc[k];
+        for (int r = 0; r < kN / 3; ++r) {
+          const int qq = nbase / 3 + r;
+          const int tt = qq >> 1, j = qq & 1;
+          const int i = sb * kSub + gl * P + tt;
+          const int t = t0 + i, d = d0 + j;
+          const int e = i * DC + cl + j;
+          const float uu = s_u[e], dl = s_dl[e], dyj = s_g[e], gf = s_dy[e];
+          const float Dj = j ? Dd[1] : Dd[0];
+          const float y = fmaf(Dj, uu, vn[3 * r]);
+          const float sA = vn[3 * r + 1], sB = vn[3 * r + 2];
+          if (t < T && d < Di) {
+            const size_t o = (rowb + t) * Di + d;
+            p.d_delta[o] = fmaf(sA, kLn2, uu * sB);
+            p.d_u[o] = fmaf(dyj, Dj, dl * sB);
+            p.d_gate[o] = y * gf;
           }
         }
       }
     }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < kChunk * NP; idx += kWarps * 32) {
-      const int i = idx / NP, n = idx % NP;
-      if (i < len && n < N) {
-        float sb = 0.f, sc = 0.f;
+    // CTA partial of d_B / d_C for this chunk: fixed-order sum over the warps
+    for (int e = threadIdx.x; e < kChunk * 2 * NP; e += NTH) {
+      const int i = e / (2 * NP), kn = e % (2 * NP);
+      const int kind = kn / NP, n = kn % NP;
+      const int t = t0 + i;
+      if (t < T && n < N) {
+        float sum = 0.f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-          sb += redB[w][i][n];
-          sc += redC[w][i][n];
-        }
-        const size_t o = (((size_t)blockIdx.x * p.batch + b) * T + t0 + i) * N + n;
-        p.partB[o] = sb;
-        p.partC[o] = sc;
+        for (int w = 0; w < kWarps; ++w) sum += red[(w * kChunk + i) * 2 * NP + kn];
+        const size_t o = (((size_t)blockIdx.x * p.batch + b) * T + t) * N + n;
+        (kind ? p.partC : p.partB)[o] = sum;
       }
     }
-    __syncthreads();
   }
+  cp_async_wait<0>();
 
   // per-batch partials of d_A_log (= A * sum_t delta*r = ln2*a2*accA) and d_D
 #pragma unroll
   for (int j = 0; j < kDPT; ++j) {
-    if (!dv[j]) continue;
+    const int d = d0 + j;
+    if (d >= Di) continue;
+    const float av[4] = {kLn2 * a2[j][0].x * accA[j][0].x, kLn2 * a2[j][0].y * accA[j][0].y,
+                         kLn2 * a2[j][1].x * accA[j][1].x, kLn2 * a2[j][1].y * accA[j][1].y};
 #pragma unroll
     for (int k = 0; k < kNPT; ++k)
-      if (n0 + k < N)
-        p.partA[((size_t)b * Di + d0 + j) * N + n0 + k] = kLn2 * a2[j][k] * accA[j][k];
-    if (ng == 0) p.partD[(size_t)b * Di + d0 + j] = dD[j];
+      if (n0 + k < N) p.partA[((size_t)b * Di + d) * N + n0 + k] = av[k];
+    if (ng == 0) p.partD[(size_t)b * Di + d] = dD[j];
   }
 }
 
@@ -247,28 +401,39 @@ __global__ void scan_reduce_kernel(const BwdParams p) {
   }
 }
 
+template <int NP, bool VEC>
+static int launch_np(const Plan& plan, const BwdParams& p, cudaStream_t s) {
+  using S = BwdShape<NP>;
+  if (cudaFuncSetAttribute(scan_bwd_kernel<NP, VEC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)S::kSmemBytes) != cudaSuccess)
+    return -1;
+  dim3 grid((unsigned)((plan.Di + S::DC - 1) / S::DC), (unsigned)plan.batch);
+  scan_bwd_kernel<NP, VEC><<<grid, kWarps * 32, S::kSmemBytes, s>>>(p);
+  return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
+}
+
 template <int NP>
-static void launch_np(const Plan& plan, const BwdParams& p, cudaStream_t s) {
-  dim3 grid(plan.nblk, (unsigned)plan.batch);
-  scan_bwd_kernel<NP><<<grid, kWarps * 32, 0, s>>>(p);
+static int launch_vec(const Plan& plan, const BwdParams& p, cudaStream_t s) {
+  const bool vec = (plan.Di % 4 == 0) && (plan.N % 4 == 0);
+  return vec ? launch_np<NP, true>(plan, p, s) : launch_np<NP, false>(plan, p, s);
 }
 
 int launch_bwd(const Plan& plan, const BwdParams& p, cudaStream_t s) {
+  int n;
   switch (plan.NP) {
-    case 4: launch_np<4>(plan, p, s); break;
-    case 8: launch_np<8>(plan, p, s); break;
-    case 16: launch_np<16>(plan, p, s); break;
-    case 32: launch_np<32>(plan, p, s); break;
-    case 64: launch_np<64>(plan, p, s); break;
+    case 4: n = launch_vec<4>(plan, p, s); break;
+    case 8: n = launch_vec<8>(plan, p, s); break;
+    case 16: n = launch_vec<16>(plan, p, s); break;
+    case 32: n = launch_vec<32>(plan, p, s); break;
+    case 64: n = launch_vec<64>(plan, p, s); break;
     default: return -1;
   }
-  if (cudaPeekAtLastError() != cudaSuccess) return -1;
-  int sms = 152;
-  int dev = 0;
+  if (n < 0) return -1;
+  int sms = 152, dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   scan_reduce_kernel<<<sms * 4, 256, 0, s>>>(p);
-  return cudaPeekAtLastError() == cudaSuccess ? 2 : -1;
+  return cudaPeekAtLastError() == cudaSuccess ? n + 1 : -1;
 }
 
 }  // namespace mscan

@@ -9,9 +9,10 @@ namespace mscan {
 
 constexpr float kLog2e = 1.4426950408889634f;  // log2(e)
 constexpr float kLn2 = 0.6931471805599453f;    // ln(2)
+constexpr unsigned kFull = 0xffffffffu;
 
-// 2^x on the special-function unit (PTX ex2.approx.ftz.f32). Here x <= 0 always, so the
-// result lies in [0, 1]; very negative x flushes to 0.
+// 2^x on the special-function unit (PTX ex2.approx.ftz.f32). In the scan x <= 0, so the result
+// lies in [0, 1]; very negative x flushes to 0.
 __device__ __forceinline__ float ex2_sfu(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -24,23 +25,92 @@ __device__ __forceinline__ float sigmoid_fast(float g) {
   return __fdividef(1.0f, 1.0f + ex2_sfu(-g * kLog2e));
 }
 
-// Read-only, streamed-once global load.
-__device__ __forceinline__ float ld_stream(const float* p) { return __ldg(p); }
+// Packed fp32x2 arithmetic (one issue slot for two lanes of work on sm_100+).
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 splat2(float v) { return make_float2(v, v); }
+__device__ __forceinline__ float2 ex2_2(float2 x) { return make_float2(ex2_sfu(x.x), ex2_sfu(x.y)); }
 
-// Sum over the G lanes that share a channel group (they differ in the low log2(G) lane bits).
-template <int G>
-__device__ __forceinline__ float sum_over_state_lanes(float v) {
-#pragma unroll
-  for (int off = 1; off < G; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  return v;
+// Compiler-only barrier (no instruction is emitted). The step loops are fully unrolled so that
+// the register stash is statically indexed. Without a barrier per step, the compiler hoists the
+// shared-memory loads of many future steps and runs out of registers.
+__device__ __forceinline__ void step_fence() { asm volatile("" ::: "memory"); }
+
+// ---- asynchronous global->shared copies (cp.async, completion tracked by commit groups) ----
+// A source size of 0 writes zeros: that is how rows past T and channels past d_inner stay 0.
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_addr(dst)),
+               "l"(src), "r"(valid ? 16 : 0));
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(smem_addr(dst)), "l"(src),
+               "r"(valid ? 4 : 0));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
 }
 
-// Sum over the channel groups of a warp (lanes that differ in the bits above log2(G)).
-template <int G>
-__device__ __forceinline__ float sum_over_channel_lanes(float v) {
+// ---- butterfly reduce-scatter across lanes -------------------------------------------------
+// Sums v[] over the lanes that differ in the lane bits MASK, MASK/2, ..., MLO (powers of two).
+// While more than one value is left, each level keeps half of them: the upper half on lanes
+// whose bit is set, the lower half otherwise. Once a single value is left, the remaining
+// levels are plain all-reduce steps. Afterwards v[0 .. kept) holds sums of the original
+// indices rs_base(lane) + r.
+template <int S, int MASK, int MLO>
+struct ReduceScatter {
+  static __device__ __forceinline__ void run(float* v, int lane) {
+    if constexpr (MASK >= MLO && MASK >= 1) {
+      if constexpr (S >= 2) {
+        constexpr int H = S / 2;
+        const bool up = (lane & MASK) != 0;
 #pragma unroll
-  for (int off = G; off < 32; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  return v;
-}
+        for (int i = 0; i < H; ++i) {
+          const float send = up ? v[i] : v[i + H];
+          const float keep = up ? v[i + H] : v[i];
+          v[i] = keep + __shfl_xor_sync(kFull, send, MASK);
+        }
+        ReduceScatter<H, MASK / 2, MLO>::run(v, lane);
+      } else {
+        v[0] += __shfl_xor_sync(kFull, v[0], MASK);
+        ReduceScatter<1, MASK / 2, MLO>::run(v, lane);
+      }
+    }
+  }
+  // number of values left per lane
+  static __host__ __device__ constexpr int kept() {
+    int s = S;
+    for (int m = MASK; m >= MLO && m >= 1; m /= 2)
+      if (s >= 2) s /= 2;
+    return s;
+  }
+  // original index of v[0] on this lane
+  static __device__ __forceinline__ int base(int lane) {
+    int b = 0, s = S;
+#pragma unroll
+    for (int m = MASK; m >= MLO && m >= 1; m /= 2) {
+      if (s >= 2) {
+        s /= 2;
+        if (lane & m) b += s;
+      }
+    }
+    return b;
+  }
+  // true on one lane of each group that the all-reduce levels left with equal values
+  static __device__ __forceinline__ bool writer(int lane) {
+    int s = S;
+    bool w = true;
+#pragma unroll
+    for (int m = MASK; m >= MLO && m >= 1; m /= 2) {
+      if (s >= 2) s /= 2;
+      else if (lane & m) w = false;
+    }
+    return w;
+  }
+};
 
 }  // namespace mscan

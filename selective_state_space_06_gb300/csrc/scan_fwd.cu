@@ -3,126 +3,252 @@
 // What it computes, for every row (b, d) and state n (h_{-1} = 0, A = -exp(A_log)):
 //   h_t = exp(delta_t * A) * h_{t-1} + delta_t * u_t * B_t[n]
 //   y_t = sum_n C_t[n] * h_t + D * u_t,     out_t = y_t * SiLU(gate_t)
-// This is the recurrence whose derivatives are the SSM BPTT of mamba-rs
-// src/mamba_ssm/cpu/backward.rs (Phase B3). That page precomputes a_neg = -exp(A_log) (its
-// "O3") to avoid a transcendental per step. Here the same happens in registers, with the
-// log2(e) factor folded in, so each step costs one ex2.
+// The Phase B3 SSM BPTT of mamba-rs src/mamba_ssm/cpu/backward.rs is the derivative of this
+// recurrence. That page precomputes a_neg = -exp(A_log) (its "O3"). Here the same constant
+// lives in registers with log2(e) folded in (a2), so a step costs one ex2 per state.
 //
 // Mapping. grid = (ceil(d_inner / DC), batch). A CTA owns one batch row b and DC consecutive
-// channels, and runs the whole time axis for them.
-//   lane = dg * G + ng :  ng picks the state group [ng*4, ng*4+4), and dg picks the pair of
-//                         channels [2*dg, 2*dg+2) inside the warp's 2*(32/G) channels.
-// So each thread carries 2 x 4 states in registers. The reduction of C*h over n is 4 in-thread
-// FMAs followed by a log2(G)-step xor butterfly. Loads of delta/u/gate are coalesced along d,
-// and all lanes of a state group load the same B/C words (broadcast).
+// channels, and walks the whole time axis for them in chunks of kChunk steps.
+//   lane = dg * G + ng :  ng picks the states [4*ng, 4*ng+4), and dg picks the channel pair
+//                         [2*dg, 2*dg+2) of the warp's 2*(32/G) channels.
+// A thread keeps 2 channels x 4 states in registers as float2 pairs and updates them with
+// packed fp32x2 FMAs.
 //
-// Every kChunk steps the state is written to the checkpoint buffer [batch][chunk][d][n]
-// (chunk = 0 .. nchunks-2, the state after that chunk). The backward restarts each chunk from
-// these states.
+// Staging. Each chunk's tiles (delta, u and gate [kChunk][DC]; B and C [kChunk][NP]) go
+// global -> shared with cp.async, STAGES chunks ahead of the compute. Rows past T and channels
+// past d_inner arrive as zeros. For those the recurrence is an exact no-op (decay 1, input 0),
+// so the control flow needs no tail special cases.
+//
+// y = sum_n C*h. In-thread FMAs first, then a butterfly reduce-scatter over the G state
+// lanes, batched over P = G/2 steps. It leaves each lane the complete y of exactly one
+// (step, channel). That lane then applies D*u and the SiLU gate and stores out. So no
+// sigmoid is computed twice.
+//
+// Every kChunk steps the state goes to the checkpoint buffer [batch][chunk][d][n] (the state
+// after chunk 0 .. nchunks-2). The backward restarts each chunk from these states.
 #include "scan_common.cuh"
 
 namespace mscan {
 
+constexpr int kFwdStages = 4;
+
 template <int NP>
+struct FwdShape {
+  static constexpr int G = NP / kNPT;                  // lanes per channel group
+  static constexpr int DW = (32 / G) * kDPT;           // channels per warp
+  static constexpr int DC = kWarps * DW;               // channels per CTA
+  static constexpr int P = G >= 2 ? G / 2 : 1;         // steps per output group
+  static constexpr int kStageFloats = kChunk * (3 * DC + 2 * NP);
+  static constexpr size_t kSmemBytes = (size_t)kFwdStages * kStageFloats * sizeof(float);
+};
+
+template <int NP, bool VEC>
+__device__ __forceinline__ void fwd_load_chunk(const FwdParams& p, float* st, int c, int b,
+                                               int dblk0) {
+  using S = FwdShape<NP>;
+  constexpr int DC = S::DC, NTH = kWarps * 32;
+  float* s_dl = st;
+  float* s_u = st + kChunk * DC;
+  float* s_g = st + 2 * kChunk * DC;
+  float* s_B = st + 3 * kChunk * DC;
+  float* s_C = s_B + kChunk * NP;
+  const int t0 = c * kChunk;
+  const size_t rowb = (size_t)b * p.T;
+  if constexpr (VEC) {
+    for (int q = threadIdx.x; q < kChunk * DC / 4; q += NTH) {
+      const int i = q / (DC / 4), col = (q % (DC / 4)) * 4;
+      const int t = t0 + i, d = dblk0 + col;
+      const bool v = t < p.T && d < p.Di;
+      const size_t go = v ? (rowb + t) * p.Di + d : 0;
+      cp_async16(s_dl + i * DC + col, p.delta + go, v);
+      cp_async16(s_u + i * DC + col, p.u + go, v);
+      cp_async16(s_g + i * DC + col, p.gate + go, v);
+    }
+    for (int q = threadIdx.x; q < kChunk * NP / 4; q += NTH) {
+      const int i = q / (NP / 4), n = (q % (NP / 4)) * 4;
+      const int t = t0 + i;
+      const bool v = t < p.T && n < p.N;
+      const size_t go = v ? (rowb + t) * p.N + n : 0;
+      cp_async16(s_B + i * NP + n, p.B + go, v);
+      cp_async16(s_C + i * NP + n, p.C + go, v);
+    }
+  } else {
+    for (int q = threadIdx.x; q < kChunk * DC; q += NTH) {
+      const int i = q / DC, col = q % DC;
+      const int t = t0 + i, d = dblk0 + col;
+      const bool v = t < p.T && d < p.Di;
+      const size_t go = v ? (rowb + t) * p.Di + d : 0;
+      cp_async4(s_dl + i * DC + col, p.delta + go, v);
+      cp_async4(s_u + i * DC + col, p.u + go, v);
+      cp_async4(s_g + i * DC + col, p.gate + go, v);
+    }
+    for (int q = threadIdx.x; q < kChunk * NP; q += NTH) {
+      const int i = q / NP, n = q % NP;
+      const int t = t0 + i;
+      const bool v = t < p.T && n < p.N;
+      const size_t go = v ? (rowb + t) * p.N + n : 0;
+      cp_async4(s_B + i * NP + n, p.B + go, v);
+      cp_async4(s_C + i * NP + n, p.C + go, v);
+    }
+  }
+  cp_async_commit();
+}
+
+template <int NP, bool VEC>
 __global__ void __launch_bounds__(kWarps * 32)
 scan_fwd_kernel(const FwdParams p) {
-  constexpr int G = NP / kNPT;
-  constexpr int DW = (32 / G) * kDPT;
-  constexpr int DC = kWarps * DW;
+  using S = FwdShape<NP>;
+  constexpr int G = S::G, DW = S::DW, DC = S::DC, P = S::P;
+  extern __shared__ __align__(16) float smem[];
+
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ng = lane % G, dg = lane / G;
   const int b = blockIdx.y;
-  const int d0 = blockIdx.x * DC + warp * DW + dg * kDPT;
+  const int dblk0 = blockIdx.x * DC;
+  const int cl = warp * DW + dg * kDPT;   // first channel of this thread inside the CTA tile
+  const int d0 = dblk0 + cl;
   const int n0 = ng * kNPT;
   const int Di = p.Di, N = p.N, T = p.T;
 
-  bool dv[kDPT];
-  float a2[kDPT][kNPT], h[kDPT][kNPT], Dd[kDPT];
+  float2 a2[kDPT][2], h[kDPT][2];
+  float Dd[kDPT];
 #pragma unroll
   for (int j = 0; j < kDPT; ++j) {
     const int d = d0 + j;
-    dv[j] = d < Di;
-    Dd[j] = dv[j] ? p.D[d] : 0.f;
+    const bool dv = d < Di;
+    Dd[j] = dv ? p.D[d] : 0.f;
+    float t4[kNPT];
 #pragma unroll
     for (int k = 0; k < kNPT; ++k) {
       const int n = n0 + k;
-      a2[j][k] = (dv[j] && n < N) ? -expf(p.A_log[(size_t)d * N + n]) * kLog2e : 0.f;
-      h[j][k] = 0.f;
+      t4[k] = (dv && n < N) ? -expf(p.A_log[(size_t)d * N + n]) * kLog2e : 0.f;
     }
+    a2[j][0] = make_float2(t4[0], t4[1]);
+    a2[j][1] = make_float2(t4[2], t4[3]);
+    h[j][0] = h[j][1] = make_float2(0.f, 0.f);
   }
-  // lane that finishes channel j (after the butterfly every lane of the group holds y)
-  const bool owner[kDPT] = {ng == 0, ng == (G > 1 ? 1 : 0)};
 
-  const size_t row0 = (size_t)b * T;
+  using RSy = ReduceScatter<2 * P, G / 2, 1>;
+  const int ybase = RSy::base(lane);
+  constexpr int kY = RSy::kept();
+  const size_t rowb = (size_t)b * T;
+
+#pragma unroll
+  for (int s = 0; s < kFwdStages - 1; ++s) {
+    if (s < p.nchunks) fwd_load_chunk<NP, VEC>(p, smem + s * S::kStageFloats, s, b, dblk0);
+    else cp_async_commit();
+  }
+
   for (int c = 0; c < p.nchunks; ++c) {
+    cp_async_wait<kFwdStages - 2>();
+    __syncthreads();
+    {
+      const int cn = c + kFwdStages - 1;
+      if (cn < p.nchunks)
+        fwd_load_chunk<NP, VEC>(p, smem + (cn % kFwdStages) * S::kStageFloats, cn, b, dblk0);
+      else
+        cp_async_commit();
+    }
+    const float* st = smem + (c % kFwdStages) * S::kStageFloats;
+    const float* s_dl = st;
+    const float* s_u = st + kChunk * DC;
+    const float* s_g = st + 2 * kChunk * DC;
+    const float* s_B = st + 3 * kChunk * DC;
+    const float* s_C = s_B + kChunk * NP;
     const int t0 = c * kChunk;
-    const int len = min(kChunk, T - t0);
+
 #pragma unroll
-    for (int i = 0; i < kChunk; ++i) {
-      if (i < len) {
-        const size_t xo = (row0 + t0 + i) * Di;
-        const size_t bo = (row0 + t0 + i) * N;
-        float dl[kDPT], uu[kDPT], Bn[kNPT], Cn[kNPT], yp[kDPT];
+    for (int gi = 0; gi < kChunk / P; ++gi) {
+      float yv[2 * P];
 #pragma unroll
-        for (int j = 0; j < kDPT; ++j) {
-          dl[j] = dv[j] ? ld_stream(p.delta + xo + d0 + j) : 0.f;
-          uu[j] = dv[j] ? ld_stream(p.u + xo + d0 + j) : 0.f;
-        }
-#pragma unroll
-        for (int k = 0; k < kNPT; ++k) {
-          Bn[k] = (n0 + k < N) ? ld_stream(p.B + bo + n0 + k) : 0.f;
-          Cn[k] = (n0 + k < N) ? ld_stream(p.C + bo + n0 + k) : 0.f;
-        }
+      for (int tt = 0; tt < P; ++tt) {
+        const int i = gi * P + tt;
+        const float2 dlv = *reinterpret_cast<const float2*>(s_dl + i * DC + cl);
+        const float2 uv = *reinterpret_cast<const float2*>(s_u + i * DC + cl);
+        const float4 Bv = *reinterpret_cast<const float4*>(s_B + i * NP + n0);
+        const float4 Cv = *reinterpret_cast<const float4*>(s_C + i * NP + n0);
+        const float2 Bp[2] = {make_float2(Bv.x, Bv.y), make_float2(Bv.z, Bv.w)};
+        const float2 Cp[2] = {make_float2(Cv.x, Cv.y), make_float2(Cv.z, Cv.w)};
 #pragma unroll
         for (int j = 0; j < kDPT; ++j) {
-          const float du = dl[j] * uu[j];
-          yp[j] = 0.f;
+          const float dl = j ? dlv.y : dlv.x;
+          const float uu = j ? uv.y : uv.x;
+          const float2 dl2 = splat2(dl), du2 = splat2(dl * uu);
+          float2 ya = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int k = 0; k < kNPT; ++k) {
-            const float da = ex2_sfu(dl[j] * a2[j][k]);
-            h[j][k] = fmaf(da, h[j][k], du * Bn[k]);
-            yp[j] = fmaf(Cn[k], h[j][k], yp[j]);
+          for (int pp = 0; pp < 2; ++pp) {
+            const float2 da = ex2_2(mul2(dl2, a2[j][pp]));
+            h[j][pp] = fma2(da, h[j][pp], mul2(du2, Bp[pp]));
+            ya = fma2(Cp[pp], h[j][pp], ya);
           }
-          yp[j] = sum_over_state_lanes<G>(yp[j]);
+          yv[tt * 2 + j] = ya.x + ya.y;
         }
+      }
+      RSy::run(yv, lane);
 #pragma unroll
-        for (int j = 0; j < kDPT; ++j) {
-          if (dv[j] && owner[j]) {
-            const float g = ld_stream(p.gate + xo + d0 + j);
-            const float y = fmaf(Dd[j], uu[j], yp[j]);
-            p.out[xo + d0 + j] = y * (g * sigmoid_fast(g));
-            if (p.y) p.y[xo + d0 + j] = y;
-          }
+      for (int r = 0; r < kY; ++r) {
+        const int idx = ybase + r;
+        const int tt = idx >> 1, j = idx & 1;
+        const int i = gi * P + tt;
+        const int t = t0 + i, d = d0 + j;
+        const float uu = s_u[i * DC + cl + j];
+        const float g = s_g[i * DC + cl + j];
+        const float y = fmaf(j ? Dd[1] : Dd[0], uu, yv[r]);
+        if (t < T && d < Di) {
+          const size_t o = (rowb + t) * Di + d;
+          p.out[o] = y * (g * sigmoid_fast(g));
+          if (p.y) p.y[o] = y;
         }
       }
     }
+
     if (c + 1 < p.nchunks) {
       float* ck = p.ckpt + ((size_t)b * (p.nchunks - 1) + c) * (size_t)Di * N;
 #pragma unroll
-      for (int j = 0; j < kDPT; ++j)
+      for (int j = 0; j < kDPT; ++j) {
+        const int d = d0 + j;
+        if (d >= Di) continue;
+        if constexpr (VEC) {
+          *reinterpret_cast<float4*>(ck + (size_t)d * N + n0) =
+              make_float4(h[j][0].x, h[j][0].y, h[j][1].x, h[j][1].y);
+        } else {
+          const float hv[4] = {h[j][0].x, h[j][0].y, h[j][1].x, h[j][1].y};
 #pragma unroll
-        for (int k = 0; k < kNPT; ++k)
-          if (dv[j] && n0 + k < N) ck[(size_t)(d0 + j) * N + n0 + k] = h[j][k];
+          for (int k = 0; k < kNPT; ++k)
+            if (n0 + k < N) ck[(size_t)d * N + n0 + k] = hv[k];
+        }
+      }
     }
   }
+  cp_async_wait<0>();
+}
+
+template <int NP, bool VEC>
+static int launch_np(const Plan& plan, const FwdParams& p, cudaStream_t s) {
+  using S = FwdShape<NP>;
+  if (cudaFuncSetAttribute(scan_fwd_kernel<NP, VEC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)S::kSmemBytes) != cudaSuccess)
+    return -1;
+  dim3 grid((unsigned)((plan.Di + S::DC - 1) / S::DC), (unsigned)plan.batch);
+  scan_fwd_kernel<NP, VEC><<<grid, kWarps * 32, S::kSmemBytes, s>>>(p);
+  return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
 }
 
 template <int NP>
-static void launch_np(const Plan& plan, const FwdParams& p, cudaStream_t s) {
-  dim3 grid(plan.nblk, (unsigned)plan.batch);
-  scan_fwd_kernel<NP><<<grid, kWarps * 32, 0, s>>>(p);
+static int launch_vec(const Plan& plan, const FwdParams& p, cudaStream_t s) {
+  const bool vec = (plan.Di % 4 == 0) && (plan.N % 4 == 0);
+  return vec ? launch_np<NP, true>(plan, p, s) : launch_np<NP, false>(plan, p, s);
 }
 
 int launch_fwd(const Plan& plan, const FwdParams& p, cudaStream_t s) {
   switch (plan.NP) {
-    case 4: launch_np<4>(plan, p, s); break;
-    case 8: launch_np<8>(plan, p, s); break;
-    case 16: launch_np<16>(plan, p, s); break;
-    case 32: launch_np<32>(plan, p, s); break;
-    case 64: launch_np<64>(plan, p, s); break;
+    case 4: return launch_vec<4>(plan, p, s);
+    case 8: return launch_vec<8>(plan, p, s);
+    case 16: return launch_vec<16>(plan, p, s);
+    case 32: return launch_vec<32>(plan, p, s);
+    case 64: return launch_vec<64>(plan, p, s);
     default: return -1;
   }
-  return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
 }
 
 }  // namespace mscan
