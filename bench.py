@@ -262,29 +262,44 @@ def run_gpu(args):
         pg.destroy_process_group()
 
 
-def cpu_baseline(w, budget_s: float = 12.0) -> dict:
-    """The oracle as it stands (single-threaded fp64 C, forward + backward per row) on a bounded
-    sample of rows of the workload; scaled to elements/s."""
+def _oracle_rows_runner(w):
+    """(run(rows) -> seconds) for the oracle over the first `rows` rows of the workload, with
+    the output arrays allocated once outside the timed calls."""
     import oracle
     x = oracle.as64(synth.make_inputs(w, seed=0))
     b, T, Di, N = w.shape()
-    rows_total = b * Di
-    # calibrate on a few rows, then take as many rows as fit the budget
-    r = max(1, min(rows_total, 4))
-    t0 = time.perf_counter()
-    oracle.fwd(x, rows=(0, r))
-    oracle.bwd(x, rows=(0, r))
-    per_row = (time.perf_counter() - t0) / r
-    rows = int(max(1, min(rows_total, budget_s / max(per_row, 1e-9))))
     out = np.full((b, T, Di), np.nan)
     y = np.full((b, T, Di), np.nan)
-    t0 = time.perf_counter()
-    oracle.fwd(x, rows=(0, rows), out=out, y=y)
-    oracle.bwd(x, rows=(0, rows))
-    el = time.perf_counter() - t0
-    return {"value": rows * T / el, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{rows} of {rows_total} rows (b,d) x T={T}, fwd+bwd, fp64, 1 thread; "
-                      f"{el:.1f} s"}
+
+    def run(rows):
+        t0 = time.perf_counter()
+        oracle.fwd(x, rows=(0, rows), out=out, y=y)
+        oracle.bwd(x, rows=(0, rows))
+        return time.perf_counter() - t0
+    return run
+
+
+def _calibrated_rows(w, run, budget_s):
+    rows_total = w.batch * w.d_inner
+    r = 1
+    while True:                        # grow the probe until it takes a measurable time
+        el = run(r)
+        if el > 0.5 or r >= rows_total:
+            break
+        r = min(rows_total, r * 4)
+    per_row = el / r
+    return int(max(1, min(rows_total, budget_s / max(per_row, 1e-12))))
+
+
+def cpu_baseline(w, budget_s: float = 12.0) -> dict:
+    """The oracle as it stands (single-threaded fp64 C, forward + backward per row) on a bounded
+    sample of rows of the workload; scaled to elements/s."""
+    run = _oracle_rows_runner(w)
+    rows = _calibrated_rows(w, run, budget_s)
+    el = run(rows)
+    return {"value": rows * w.T / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{rows} of {w.batch * w.d_inner} rows (b,d) x T={w.T}, fwd+bwd, fp64, "
+                      f"1 thread; {el:.1f} s"}
 
 
 def run_reference(args):
@@ -293,29 +308,16 @@ def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return
-    import oracle
     w = synth.BY_NAME[args.workload]
-    x = oracle.as64(synth.make_inputs(w, seed=0))
-    b, T, Di, N = w.shape()
-    rows_total = b * Di
-    t0 = time.perf_counter()
-    oracle.bwd(x, rows=(0, 2))
-    oracle.fwd(x, rows=(0, 2))
-    per_row = (time.perf_counter() - t0) / 2
+    run = _oracle_rows_runner(w)
     total_budget = 120.0
-    rows = int(max(1, min(rows_total, total_budget / max(1, args.steps + args.warmup) / per_row)))
-    out = np.full((b, T, Di), np.nan)
-    y = np.full((b, T, Di), np.nan)
+    rows = _calibrated_rows(w, run, total_budget / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
-        oracle.fwd(x, rows=(0, rows), out=out, y=y)
-        oracle.bwd(x, rows=(0, rows))
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle.fwd(x, rows=(0, rows), out=out, y=y)
-        oracle.bwd(x, rows=(0, rows))
-    el = time.perf_counter() - t0
-    value = rows * T * args.steps / el
-    sample = f"{rows} of {rows_total} rows (b,d) x T={T} per step, fwd+bwd, fp64, 1 thread"
+        run(rows)
+    el = sum(run(rows) for _ in range(args.steps))
+    value = rows * w.T * args.steps / el
+    sample = (f"{rows} of {w.batch * w.d_inner} rows (b,d) x T={w.T} per step, fwd+bwd, fp64, "
+              "1 thread")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,

@@ -25,7 +25,7 @@ bool make_plan(int64_t batch, int64_t T, int64_t Di, int64_t N, Plan* pl) {
   Plan p;
   p.batch = batch; p.T = T; p.Di = Di; p.N = N;
   p.NP = N <= 4 ? 4 : N <= 8 ? 8 : N <= 16 ? 16 : N <= 32 ? 32 : 64;
-  p.G = p.NP / kNPT;
+  p.G = p.NP / states_per_thread(p.NP);
   p.DC = kWarps * (32 / p.G) * kDPT;
   p.nblk = (int)((Di + p.DC - 1) / p.DC);
   p.nchunks = (int)((T + kChunk - 1) / kChunk);

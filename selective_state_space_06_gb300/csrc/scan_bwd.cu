@@ -3,7 +3,7 @@
 // from the forward's checkpoints instead of being stored for every t.
 //
 // Per row (b, d), the chunks are walked from last to first (thread mapping as in the forward:
-// 2 channels x 4 states per thread, G lanes per channel group):
+// 2 channels x NPT states per thread, G lanes per channel group):
 //   0. gating (Phase B2), once per (t, d) of the chunk and cooperatively:
 //        d_y = dy * g * s  and  gfac = dy * s * (1 + g*(1 - s)),  s = sigmoid(g).
 //      Both overwrite the staged gate/dy tiles, so d_gate = y * gfac later.
@@ -32,12 +32,14 @@
 namespace mscan {
 
 constexpr int kBwdStages = 3;
-constexpr int kSub = 8;                  // steps kept in registers at a time
-constexpr int kNSub = kChunk / kSub;
 
 template <int NP>
 struct BwdShape {
-  static constexpr int G = NP / kNPT;
+  static constexpr int NPT = states_per_thread(NP);
+  static constexpr int NPR = NPT / 2;
+  static constexpr int kSub = 32 / NPT;         // steps kept in registers at a time (64 floats)
+  static constexpr int kNSub = kChunk / kSub;
+  static constexpr int G = NP / NPT;
   static constexpr int DW = (32 / G) * kDPT;
   static constexpr int DC = kWarps * DW;
   static constexpr int P = G >= 2 ? G / 2 : 1;
@@ -103,21 +105,22 @@ __device__ __forceinline__ void bwd_load_chunk(const BwdParams& p, float* st, in
 }
 
 // Forward recurrence of step i of the staged chunk on the thread's 2 x 4 states hc.
-template <int NP, int DC>
+template <int NP, int DC, int NPR>
 __device__ __forceinline__ void bwd_step_fwd(int i, const float* s_dl, const float* s_u,
                                              const float* s_B, int cl, int n0,
-                                             const float2 (&a2)[kDPT][2], float2 (&hc)[kDPT][2]) {
-  const float2 dlv = *reinterpret_cast<const float2*>(s_dl + i * DC + cl);
-  const float2 uv = *reinterpret_cast<const float2*>(s_u + i * DC + cl);
-  const float4 Bv = *reinterpret_cast<const float4*>(s_B + i * NP + n0);
-  const float2 Bp[2] = {make_float2(Bv.x, Bv.y), make_float2(Bv.z, Bv.w)};
+                                             const float2 (&a2)[kDPT][NPR],
+                                             float2 (&hc)[kDPT][NPR]) {
+  const float2 dlv = lds2(s_dl + i * DC + cl);
+  const float2 uv = lds2(s_u + i * DC + cl);
+  float2 Bp[NPR];
+  lds_pairs<NPR>(s_B + i * NP + n0, Bp);
 #pragma unroll
   for (int j = 0; j < kDPT; ++j) {
     const float dl = j ? dlv.y : dlv.x;
     const float uu = j ? uv.y : uv.x;
     const float2 dl2 = splat2(dl), du2 = splat2(dl * uu);
 #pragma unroll
-    for (int pp = 0; pp < 2; ++pp) {
+    for (int pp = 0; pp < NPR; ++pp) {
       const float2 da = ex2_2(mul2(dl2, a2[j][pp]));
       hc[j][pp] = fma2(da, hc[j][pp], mul2(du2, Bp[pp]));
     }
@@ -129,6 +132,7 @@ __global__ void __launch_bounds__(kWarps * 32)
 scan_bwd_kernel(const BwdParams p) {
   using S = BwdShape<NP>;
   constexpr int G = S::G, DW = S::DW, DC = S::DC, P = S::P, NTH = kWarps * 32;
+  constexpr int NPT = S::NPT, NPR = S::NPR, kSub = S::kSub, kNSub = S::kNSub;
   extern __shared__ __align__(16) float smem[];
   float* red = smem + kBwdStages * S::kStageFloats;   // [kWarps][kChunk][2*NP]
 
@@ -138,10 +142,10 @@ scan_bwd_kernel(const BwdParams p) {
   const int dblk0 = blockIdx.x * DC;
   const int cl = warp * DW + dg * kDPT;
   const int d0 = dblk0 + cl;
-  const int n0 = ng * kNPT;
+  const int n0 = ng * NPT;
   const int Di = p.Di, N = p.N, T = p.T;
 
-  float2 a2[kDPT][2], dh[kDPT][2], accA[kDPT][2];
+  float2 a2[kDPT][NPR], dh[kDPT][NPR], accA[kDPT][NPR];
   float Dd[kDPT], dD[kDPT];
 #pragma unroll
   for (int j = 0; j < kDPT; ++j) {
@@ -149,19 +153,21 @@ scan_bwd_kernel(const BwdParams p) {
     const bool dv = d < Di;
     Dd[j] = dv ? p.D[d] : 0.f;
     dD[j] = 0.f;
-    float t4[kNPT];
+    float t4[NPT];
 #pragma unroll
-    for (int k = 0; k < kNPT; ++k) {
+    for (int k = 0; k < NPT; ++k) {
       const int n = n0 + k;
       t4[k] = (dv && n < N) ? -expf(p.A_log[(size_t)d * N + n]) * kLog2e : 0.f;
     }
-    a2[j][0] = make_float2(t4[0], t4[1]);
-    a2[j][1] = make_float2(t4[2], t4[3]);
-    dh[j][0] = dh[j][1] = accA[j][0] = accA[j][1] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < NPR; ++q) {
+      a2[j][q] = make_float2(t4[2 * q], t4[2 * q + 1]);
+      dh[j][q] = accA[j][q] = make_float2(0.f, 0.f);
+    }
   }
 
   using RSn = ReduceScatter<6 * P, G / 2, 1>;    // (y, A-term, B-term) x 2 channels x P steps
-  using RSd = ReduceScatter<8, 16, G>;            // (d_B x 4, d_C x 4) over the channel lanes
+  using RSd = ReduceScatter<2 * NPT, 16, G>;      // (d_B x NPT, d_C x NPT) over channel lanes
   const int nbase = RSn::base(lane);
   constexpr int kN = RSn::kept();
   const int dbase = RSd::base(lane);
@@ -211,54 +217,59 @@ scan_bwd_kernel(const BwdParams p) {
     // sub-block from last to first, the states are recomputed into registers and walked in
     // reverse. That is 1.5x the recompute work of a full-chunk stash, but half the registers.
     const float* ck = (c > 0) ? p.ckpt + ((size_t)b * last + (c - 1)) * (size_t)Di * N : nullptr;
-    float2 hsub[kNSub][kDPT][2];
+    float2 hsub[kNSub][kDPT][NPR];
 #pragma unroll
     for (int j = 0; j < kDPT; ++j) {
       const int d = d0 + j;
-      float hv[kNPT] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int q = 0; q < NPR; ++q) hsub[0][j][q] = make_float2(0.f, 0.f);
       if (ck && d < Di) {
         if constexpr (VEC) {
-          const float4 q = *reinterpret_cast<const float4*>(ck + (size_t)d * N + n0);
-          hv[0] = q.x; hv[1] = q.y; hv[2] = q.z; hv[3] = q.w;
+          ld_pairs<NPR>(ck + (size_t)d * N + n0, hsub[0][j]);
         } else {
+          float hv[NPT];
 #pragma unroll
-          for (int k = 0; k < kNPT; ++k)
-            if (n0 + k < N) hv[k] = ck[(size_t)d * N + n0 + k];
+          for (int k = 0; k < NPT; ++k) hv[k] = (n0 + k < N) ? ck[(size_t)d * N + n0 + k] : 0.f;
+#pragma unroll
+          for (int q = 0; q < NPR; ++q) hsub[0][j][q] = make_float2(hv[2 * q], hv[2 * q + 1]);
         }
       }
-      hsub[0][j][0] = make_float2(hv[0], hv[1]);
-      hsub[0][j][1] = make_float2(hv[2], hv[3]);
     }
     {
-      float2 hc[kDPT][2] = {{hsub[0][0][0], hsub[0][0][1]}, {hsub[0][1][0], hsub[0][1][1]}};
+      float2 hc[kDPT][NPR];
+#pragma unroll
+      for (int j = 0; j < kDPT; ++j)
+#pragma unroll
+        for (int q = 0; q < NPR; ++q) hc[j][q] = hsub[0][j][q];
 #pragma unroll
       for (int sb = 1; sb < kNSub; ++sb) {
 #pragma unroll
         for (int q = 0; q < kSub; ++q)
-          bwd_step_fwd<NP, DC>((sb - 1) * kSub + q, s_dl, s_u, s_B, cl, n0, a2, hc);
+          bwd_step_fwd<NP, DC, NPR>((sb - 1) * kSub + q, s_dl, s_u, s_B, cl, n0, a2, hc);
 #pragma unroll
-        for (int j = 0; j < kDPT; ++j) {
-          hsub[sb][j][0] = hc[j][0];
-          hsub[sb][j][1] = hc[j][1];
-        }
+        for (int j = 0; j < kDPT; ++j)
+#pragma unroll
+          for (int q = 0; q < NPR; ++q) hsub[sb][j][q] = hc[j][q];
       }
     }
 
 #pragma unroll
     for (int sq = 0; sq < kNSub; ++sq) {
       const int sb = kNSub - 1 - sq;
-      float2 hs[kSub][kDPT][2];
+      float2 hs[kSub][kDPT][NPR];
       {
-        float2 hc[kDPT][2] = {{hsub[sb][0][0], hsub[sb][0][1]}, {hsub[sb][1][0], hsub[sb][1][1]}};
+        float2 hc[kDPT][NPR];
+#pragma unroll
+        for (int j = 0; j < kDPT; ++j)
+#pragma unroll
+          for (int q = 0; q < NPR; ++q) hc[j][q] = hsub[sb][j][q];
 #pragma unroll
         for (int q = 0; q < kSub; ++q) {
-          step_fence();
-          bwd_step_fwd<NP, DC>(sb * kSub + q, s_dl, s_u, s_B, cl, n0, a2, hc);
+          bwd_step_fwd<NP, DC, NPR>(sb * kSub + q, s_dl, s_u, s_B, cl, n0, a2, hc);
 #pragma unroll
-          for (int j = 0; j < kDPT; ++j) {
-            hs[q][j][0] = hc[j][0];
-            hs[q][j][1] = hc[j][1];
-          }
+          for (int j = 0; j < kDPT; ++j)
+#pragma unroll
+            for (int qq = 0; qq < NPR; ++qq) hs[q][j][qq] = hc[j][qq];
         }
       }
 #pragma unroll
@@ -270,16 +281,14 @@ scan_bwd_kernel(const BwdParams p) {
           const int tt = P - 1 - tq;
           const int q = gl * P + tt;               // step inside the sub-block
           const int i = sb * kSub + q;             // step inside the chunk
-          step_fence();
-          const float2 dlv = *reinterpret_cast<const float2*>(s_dl + i * DC + cl);
-          const float2 uv = *reinterpret_cast<const float2*>(s_u + i * DC + cl);
-          const float2 dyv = *reinterpret_cast<const float2*>(s_g + i * DC + cl);
-          const float4 Bv = *reinterpret_cast<const float4*>(s_B + i * NP + n0);
-          const float4 Cv = *reinterpret_cast<const float4*>(s_C + i * NP + n0);
-          const float2 Bp[2] = {make_float2(Bv.x, Bv.y), make_float2(Bv.z, Bv.w)};
-          const float2 Cp[2] = {make_float2(Cv.x, Cv.y), make_float2(Cv.z, Cv.w)};
-          float2 xb[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-          float2 xc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+          const float2 dlv = lds2(s_dl + i * DC + cl);
+          const float2 uv = lds2(s_u + i * DC + cl);
+          const float2 dyv = lds2(s_g + i * DC + cl);
+          float2 Bp[NPR], Cp[NPR], xb[NPR], xc[NPR];
+          lds_pairs<NPR>(s_B + i * NP + n0, Bp);
+          lds_pairs<NPR>(s_C + i * NP + n0, Cp);
+#pragma unroll
+          for (int pp = 0; pp < NPR; ++pp) xb[pp] = xc[pp] = make_float2(0.f, 0.f);
 #pragma unroll
           for (int j = 0; j < kDPT; ++j) {
             const float dl = j ? dlv.y : dlv.x;
@@ -288,7 +297,7 @@ scan_bwd_kernel(const BwdParams p) {
             const float2 dl2 = splat2(dl), du2 = splat2(dl * uu), dy2 = splat2(dyj);
             float2 ya = make_float2(0.f, 0.f), sa = ya, sb2 = ya;
 #pragma unroll
-            for (int pp = 0; pp < 2; ++pp) {
+            for (int pp = 0; pp < NPR; ++pp) {
               const float2 hcur = hs[q][j][pp];
               const float2 hprev = (q > 0) ? hs[q > 0 ? q - 1 : 0][j][pp] : hsub[sb][j][pp];
               ya = fma2(Cp[pp], hcur, ya);
@@ -309,13 +318,20 @@ scan_bwd_kernel(const BwdParams p) {
             dD[j] = fmaf(dyj, uu, dD[j]);
           }
           // d_B / d_C of this step: sum over the warp's channels
-          float vd[8] = {xb[0].x, xb[0].y, xb[1].x, xb[1].y, xc[0].x, xc[0].y, xc[1].x, xc[1].y};
+          float vd[2 * NPT];
+#pragma unroll
+          for (int pp = 0; pp < NPR; ++pp) {
+            vd[2 * pp] = xb[pp].x;
+            vd[2 * pp + 1] = xb[pp].y;
+            vd[NPT + 2 * pp] = xc[pp].x;
+            vd[NPT + 2 * pp + 1] = xc[pp].y;
+          }
           RSd::run(vd, lane);
           if (dwriter) {
 #pragma unroll
             for (int r = 0; r < kD; ++r) {
-              const int idx = dbase + r;        // 0..3: d_B of state n0+idx, 4..7: d_C
-              red[(warp * kChunk + i) * 2 * NP + (idx >> 2) * NP + n0 + (idx & 3)] = vd[r];
+              const int idx = dbase + r;   // < NPT: d_B of state n0+idx, else d_C of n0+idx-NPT
+              red[(warp * kChunk + i) * 2 * NP + (idx / NPT) * NP + n0 + (idx % NPT)] = vd[r];
             }
           }
         }
@@ -363,11 +379,12 @@ scan_bwd_kernel(const BwdParams p) {
   for (int j = 0; j < kDPT; ++j) {
     const int d = d0 + j;
     if (d >= Di) continue;
-    const float av[4] = {kLn2 * a2[j][0].x * accA[j][0].x, kLn2 * a2[j][0].y * accA[j][0].y,
-                         kLn2 * a2[j][1].x * accA[j][1].x, kLn2 * a2[j][1].y * accA[j][1].y};
 #pragma unroll
-    for (int k = 0; k < kNPT; ++k)
-      if (n0 + k < N) p.partA[((size_t)b * Di + d) * N + n0 + k] = av[k];
+    for (int k = 0; k < NPT; ++k) {
+      const float2 aa = a2[j][k >> 1], ac = accA[j][k >> 1];
+      if (n0 + k < N)
+        p.partA[((size_t)b * Di + d) * N + n0 + k] = kLn2 * ((k & 1) ? aa.y * ac.y : aa.x * ac.x);
+    }
     if (ng == 0) p.partD[(size_t)b * Di + d] = dD[j];
   }
 }

@@ -25,22 +25,71 @@ __device__ __forceinline__ float sigmoid_fast(float g) {
   return __fdividef(1.0f, 1.0f + ex2_sfu(-g * kLog2e));
 }
 
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
 // Packed fp32x2 arithmetic (one issue slot for two lanes of work on sm_100+).
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 __device__ __forceinline__ float2 splat2(float v) { return make_float2(v, v); }
 __device__ __forceinline__ float2 ex2_2(float2 x) { return make_float2(ex2_sfu(x.x), ex2_sfu(x.y)); }
 
-// Compiler-only barrier (no instruction is emitted). The step loops are fully unrolled so that
-// the register stash is statically indexed. Without a barrier per step, the compiler hoists the
-// shared-memory loads of many future steps and runs out of registers.
-__device__ __forceinline__ void step_fence() { asm volatile("" ::: "memory"); }
+// Shared-memory loads of the staged tiles, as volatile asm. The step loops are fully unrolled
+// so that the register stash is statically indexed. With plain loads the compiler hoists the
+// loads of many future steps and runs out of registers. Volatile loads stay in program order
+// among themselves, while the arithmetic, shuffles and stores around them may still overlap
+// neighbouring steps. The tiles are written by cp.async and published by __syncthreads, so no
+// ordering inside a thread is lost.
+__device__ __forceinline__ float lds1(const float* p) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(smem_addr(p)));
+  return v;
+}
+__device__ __forceinline__ float2 lds2(const float* p) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(smem_addr(p)));
+  return v;
+}
+__device__ __forceinline__ float4 lds4(const float* p) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(smem_addr(p)));
+  return v;
+}
+
+// NPR float2 pairs of consecutive states from shared memory (8- or 16-byte aligned).
+template <int NPR>
+__device__ __forceinline__ void lds_pairs(const float* p, float2 (&out)[NPR]) {
+  static_assert(NPR == 1 || NPR == 2, "2 or 4 states per thread");
+  if constexpr (NPR == 2) {
+    const float4 v = lds4(p);
+    out[0] = make_float2(v.x, v.y);
+    out[1] = make_float2(v.z, v.w);
+  } else {
+    out[0] = lds2(p);
+  }
+}
+// NPR float2 pairs to global memory with one vector store.
+template <int NPR>
+__device__ __forceinline__ void st_pairs(float* p, const float2 (&v)[NPR]) {
+  if constexpr (NPR == 2) *reinterpret_cast<float4*>(p) = make_float4(v[0].x, v[0].y, v[1].x, v[1].y);
+  else *reinterpret_cast<float2*>(p) = v[0];
+}
+template <int NPR>
+__device__ __forceinline__ void ld_pairs(const float* p, float2 (&out)[NPR]) {
+  if constexpr (NPR == 2) {
+    const float4 v = *reinterpret_cast<const float4*>(p);
+    out[0] = make_float2(v.x, v.y);
+    out[1] = make_float2(v.z, v.w);
+  } else {
+    out[0] = *reinterpret_cast<const float2*>(p);
+  }
+}
 
 // ---- asynchronous global->shared copies (cp.async, completion tracked by commit groups) ----
 // A source size of 0 writes zeros: that is how rows past T and channels past d_inner stay 0.
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_addr(dst)),
                "l"(src), "r"(valid ? 16 : 0));

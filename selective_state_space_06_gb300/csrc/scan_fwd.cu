@@ -9,9 +9,9 @@
 //
 // Mapping. grid = (ceil(d_inner / DC), batch). A CTA owns one batch row b and DC consecutive
 // channels, and walks the whole time axis for them in chunks of kChunk steps.
-//   lane = dg * G + ng :  ng picks the states [4*ng, 4*ng+4), and dg picks the channel pair
-//                         [2*dg, 2*dg+2) of the warp's 2*(32/G) channels.
-// A thread keeps 2 channels x 4 states in registers as float2 pairs and updates them with
+//   lane = dg * G + ng :  ng picks the states [NPT*ng, NPT*ng+NPT), and dg picks the channel
+//                         pair [2*dg, 2*dg+2) of the warp's 2*(32/G) channels.
+// A thread keeps 2 channels x NPT states in registers as float2 pairs and updates them with
 // packed fp32x2 FMAs.
 //
 // Staging. Each chunk's tiles (delta, u and gate [kChunk][DC]; B and C [kChunk][NP]) go
@@ -34,7 +34,9 @@ constexpr int kFwdStages = 4;
 
 template <int NP>
 struct FwdShape {
-  static constexpr int G = NP / kNPT;                  // lanes per channel group
+  static constexpr int NPT = states_per_thread(NP);    // states per thread
+  static constexpr int NPR = NPT / 2;                  // float2 pairs of states per thread
+  static constexpr int G = NP / NPT;                   // lanes per channel group
   static constexpr int DW = (32 / G) * kDPT;           // channels per warp
   static constexpr int DC = kWarps * DW;               // channels per CTA
   static constexpr int P = G >= 2 ? G / 2 : 1;         // steps per output group
@@ -98,7 +100,7 @@ template <int NP, bool VEC>
 __global__ void __launch_bounds__(kWarps * 32)
 scan_fwd_kernel(const FwdParams p) {
   using S = FwdShape<NP>;
-  constexpr int G = S::G, DW = S::DW, DC = S::DC, P = S::P;
+  constexpr int G = S::G, DW = S::DW, DC = S::DC, P = S::P, NPT = S::NPT, NPR = S::NPR;
   extern __shared__ __align__(16) float smem[];
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -107,25 +109,27 @@ scan_fwd_kernel(const FwdParams p) {
   const int dblk0 = blockIdx.x * DC;
   const int cl = warp * DW + dg * kDPT;   // first channel of this thread inside the CTA tile
   const int d0 = dblk0 + cl;
-  const int n0 = ng * kNPT;
+  const int n0 = ng * NPT;
   const int Di = p.Di, N = p.N, T = p.T;
 
-  float2 a2[kDPT][2], h[kDPT][2];
+  float2 a2[kDPT][NPR], h[kDPT][NPR];
   float Dd[kDPT];
 #pragma unroll
   for (int j = 0; j < kDPT; ++j) {
     const int d = d0 + j;
     const bool dv = d < Di;
     Dd[j] = dv ? p.D[d] : 0.f;
-    float t4[kNPT];
+    float t4[NPT];
 #pragma unroll
-    for (int k = 0; k < kNPT; ++k) {
+    for (int k = 0; k < NPT; ++k) {
       const int n = n0 + k;
       t4[k] = (dv && n < N) ? -expf(p.A_log[(size_t)d * N + n]) * kLog2e : 0.f;
     }
-    a2[j][0] = make_float2(t4[0], t4[1]);
-    a2[j][1] = make_float2(t4[2], t4[3]);
-    h[j][0] = h[j][1] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < NPR; ++q) {
+      a2[j][q] = make_float2(t4[2 * q], t4[2 * q + 1]);
+      h[j][q] = make_float2(0.f, 0.f);
+    }
   }
 
   using RSy = ReduceScatter<2 * P, G / 2, 1>;
@@ -163,12 +167,11 @@ scan_fwd_kernel(const FwdParams p) {
 #pragma unroll
       for (int tt = 0; tt < P; ++tt) {
         const int i = gi * P + tt;
-        const float2 dlv = *reinterpret_cast<const float2*>(s_dl + i * DC + cl);
-        const float2 uv = *reinterpret_cast<const float2*>(s_u + i * DC + cl);
-        const float4 Bv = *reinterpret_cast<const float4*>(s_B + i * NP + n0);
-        const float4 Cv = *reinterpret_cast<const float4*>(s_C + i * NP + n0);
-        const float2 Bp[2] = {make_float2(Bv.x, Bv.y), make_float2(Bv.z, Bv.w)};
-        const float2 Cp[2] = {make_float2(Cv.x, Cv.y), make_float2(Cv.z, Cv.w)};
+        const float2 dlv = lds2(s_dl + i * DC + cl);
+        const float2 uv = lds2(s_u + i * DC + cl);
+        float2 Bp[NPR], Cp[NPR];
+        lds_pairs<NPR>(s_B + i * NP + n0, Bp);
+        lds_pairs<NPR>(s_C + i * NP + n0, Cp);
 #pragma unroll
         for (int j = 0; j < kDPT; ++j) {
           const float dl = j ? dlv.y : dlv.x;
@@ -176,7 +179,7 @@ scan_fwd_kernel(const FwdParams p) {
           const float2 dl2 = splat2(dl), du2 = splat2(dl * uu);
           float2 ya = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int pp = 0; pp < 2; ++pp) {
+          for (int pp = 0; pp < NPR; ++pp) {
             const float2 da = ex2_2(mul2(dl2, a2[j][pp]));
             h[j][pp] = fma2(da, h[j][pp], mul2(du2, Bp[pp]));
             ya = fma2(Cp[pp], h[j][pp], ya);
@@ -209,13 +212,11 @@ scan_fwd_kernel(const FwdParams p) {
         const int d = d0 + j;
         if (d >= Di) continue;
         if constexpr (VEC) {
-          *reinterpret_cast<float4*>(ck + (size_t)d * N + n0) =
-              make_float4(h[j][0].x, h[j][0].y, h[j][1].x, h[j][1].y);
+          st_pairs<NPR>(ck + (size_t)d * N + n0, h[j]);
         } else {
-          const float hv[4] = {h[j][0].x, h[j][0].y, h[j][1].x, h[j][1].y};
 #pragma unroll
-          for (int k = 0; k < kNPT; ++k)
-            if (n0 + k < N) ck[(size_t)d * N + n0 + k] = hv[k];
+          for (int k = 0; k < NPT; ++k)
+            if (n0 + k < N) ck[(size_t)d * N + n0 + k] = (k & 1) ? h[j][k >> 1].y : h[j][k >> 1].x;
         }
       }
     }

@@ -8,11 +8,17 @@
 namespace mscan {
 
 // Thread mapping of both scan kernels (see scan_fwd.cu for the picture):
-//   a thread owns kDPT consecutive channels d and kNPT consecutive states n;
-//   G = NP / kNPT lanes of a warp share the same channels and split the states between them;
-//   a warp therefore covers (32 / G) * kDPT channels; a CTA has kWarps warps.
-constexpr int kNPT = 4;     // states per thread
+//   a thread owns kDPT consecutive channels d and NPT = states_per_thread(NP) consecutive
+//   states n; G = NP / NPT lanes of a warp share the same channels and split the states
+//   between them; a warp therefore covers (32 / G) * kDPT channels; a CTA has kWarps warps.
 constexpr int kDPT = 2;     // channels per thread
+#ifndef MSCAN_NPT
+#define MSCAN_NPT 4
+#endif
+// states per thread (2 or 4) for d_state padded to NP
+__host__ __device__ constexpr int states_per_thread(int NP) {
+  return NP < MSCAN_NPT ? NP : MSCAN_NPT;
+}
 constexpr int kWarps = 4;   // warps per CTA
 constexpr int kChunk = 16;  // time steps per chunk (= checkpoint interval)
 constexpr int kMaxState = 64;
