@@ -59,6 +59,8 @@ extern "C" {
 #define MAMBA_ERR_WORKSPACE 3   /* checkpoint or scratch buffer smaller than required        */
 #define MAMBA_ERR_CUDA 4        /* a CUDA runtime call or kernel launch failed               */
 #define MAMBA_ERR_UNSUPPORTED 5 /* d_state outside 1..64                                     */
+#define MAMBA_ERR_NOALLOC_LIMIT 6 /* mamba_scan_bwd_noalloc: the sizes need more scratch than
+                                     MAMBA_SCAN_NOALLOC_SCRATCH_BYTES                        */
 
 /* Bytes of the checkpoint buffer that mamba_scan_fwd writes and mamba_scan_bwd reads. The
  * forward stores the state h at every chunk boundary of the time axis, so that the backward
@@ -105,6 +107,29 @@ int mamba_scan_fwd_bwd_host(const float* delta, const float* u, const float* B, 
                             float* d_C, float* d_A_log, float* d_D, float* d_gate,
                             void* workspace, size_t workspace_bytes, int64_t batch, int64_t T,
                             int64_t d_inner, int64_t d_state, void* stream);
+
+/* Backward scan that allocates nothing: the same computation and arguments as mamba_scan_bwd
+ * minus the scratch buffer. The paper has no counterpart to this entry point.
+ *
+ * It is for callers that are handed only their input and output buffers and may not allocate
+ * device memory: a plugin inside a host framework that owns all device memory, or a
+ * latency-critical loop that forbids cudaMalloc (which can synchronise the device). The scratch
+ * comes from a static device array of MAMBA_SCAN_NOALLOC_SCRATCH_BYTES that the library holds
+ * on every GPU that loads it, until the process exits. Sizes whose
+ * mamba_scan_scratch_bytes(...) exceeds that limit are rejected with MAMBA_ERR_NOALLOC_LIMIT
+ * before anything is launched. The first call on each device looks up the array's device
+ * address (with that device current) and caches it, so that first call should come before any
+ * stream capture. All calls on a device share the array, and it keeps the last call's contents.
+ * Nothing needs clearing, because the backward rewrites all the scratch it reads. Calls that
+ * overlap on the GPU race on the array: order them (one stream, or explicit events). No
+ * cudaMalloc, cudaFree or allocating library routine is called. */
+#define MAMBA_SCAN_NOALLOC_SCRATCH_BYTES (32u << 20) /* 32 MiB */
+int mamba_scan_bwd_noalloc(const float* delta, const float* u, const float* B, const float* C,
+                           const float* gate, const float* A_log, const float* D,
+                           const float* dy, const void* ckpt, size_t ckpt_bytes, float* d_delta,
+                           float* d_u, float* d_B, float* d_C, float* d_A_log, float* d_D,
+                           float* d_gate, int64_t batch, int64_t T, int64_t d_inner,
+                           int64_t d_state, void* stream);
 
 /* Synchronises `stream` and reports any asynchronous CUDA error (MAMBA_OK or
  * MAMBA_ERR_CUDA). */

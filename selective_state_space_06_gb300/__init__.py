@@ -34,11 +34,13 @@ MAMBA_ERR_MISALIGNED = 2
 MAMBA_ERR_WORKSPACE = 3
 MAMBA_ERR_CUDA = 4
 MAMBA_ERR_UNSUPPORTED = 5
+MAMBA_ERR_NOALLOC_LIMIT = 6
+MAMBA_SCAN_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 EXPORTED = (
     "mamba_scan_ckpt_bytes", "mamba_scan_scratch_bytes", "mamba_scan_fwd", "mamba_scan_bwd",
     "mamba_scan_host_workspace_bytes", "mamba_scan_fwd_bwd_host", "mamba_scan_status",
-    "mamba_scan_strerror", "mamba_scan_last_launch_count",
+    "mamba_scan_strerror", "mamba_scan_last_launch_count", "mamba_scan_bwd_noalloc",
 )
 
 _vp = ctypes.c_void_p
@@ -55,6 +57,8 @@ _lib.mamba_scan_fwd.argtypes = [_vp] * 10 + [_sz] + [_i64] * 4 + [_vp]
 _lib.mamba_scan_fwd.restype = ctypes.c_int
 _lib.mamba_scan_bwd.argtypes = [_vp] * 9 + [_sz, _vp, _sz] + [_vp] * 7 + [_i64] * 4 + [_vp]
 _lib.mamba_scan_bwd.restype = ctypes.c_int
+_lib.mamba_scan_bwd_noalloc.argtypes = [_vp] * 9 + [_sz] + [_vp] * 7 + [_i64] * 4 + [_vp]
+_lib.mamba_scan_bwd_noalloc.restype = ctypes.c_int
 _lib.mamba_scan_fwd_bwd_host.argtypes = [_vp] * 17 + [_sz] + [_i64] * 4 + [_vp]
 _lib.mamba_scan_fwd_bwd_host.restype = ctypes.c_int
 _lib.mamba_scan_status.argtypes = [_vp]
@@ -164,6 +168,25 @@ def mamba_scan_bwd(delta, u, B, C, gate, A_log, D, dy, ckpt, scratch, d_delta, d
         _ptr(d_gate, "d_gate", dev), b, T, Di, N, _stream_ptr(stream, dev))
     if rc != MAMBA_OK:
         raise MambaScanError(rc, "mamba_scan_bwd")
+
+
+def mamba_scan_bwd_noalloc(delta, u, B, C, gate, A_log, D, dy, ckpt, d_delta, d_u, d_B, d_C,
+                           d_A_log, d_D, d_gate, stream=None):
+    """Backward scan without a scratch argument, for callers that may not allocate device
+    memory. Scratch comes from the library's static 32 MiB device array, shared by every call
+    on the device; calls that overlap on the GPU race on it."""
+    b, T, Di, N = _dims(delta, B)
+    dev = delta.device
+    ck_bytes = 0 if ckpt is None else ckpt.numel() * ckpt.element_size()
+    rc = _lib.mamba_scan_bwd_noalloc(
+        _ptr(delta, "delta", dev), _ptr(u, "u", dev), _ptr(B, "B", dev), _ptr(C, "C", dev),
+        _ptr(gate, "gate", dev), _ptr(A_log, "A_log", dev), _ptr(D, "D", dev),
+        _ptr(dy, "dy", dev), _ptr(ckpt, "ckpt", dev, allow_none=True), ck_bytes,
+        _ptr(d_delta, "d_delta", dev), _ptr(d_u, "d_u", dev), _ptr(d_B, "d_B", dev),
+        _ptr(d_C, "d_C", dev), _ptr(d_A_log, "d_A_log", dev), _ptr(d_D, "d_D", dev),
+        _ptr(d_gate, "d_gate", dev), b, T, Di, N, _stream_ptr(stream, dev))
+    if rc != MAMBA_OK:
+        raise MambaScanError(rc, "mamba_scan_bwd_noalloc")
 
 
 def mamba_scan_fwd_bwd_host(delta, u, B, C, gate, A_log, D, dy, out, d_delta, d_u, d_B, d_C,

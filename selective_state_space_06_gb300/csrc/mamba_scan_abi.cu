@@ -269,6 +269,8 @@ const char* mamba_scan_strerror(int code) {
     case MAMBA_ERR_WORKSPACE: return "checkpoint, scratch or workspace buffer too small";
     case MAMBA_ERR_CUDA: return cudaGetErrorString(g_last_cuda);
     case MAMBA_ERR_UNSUPPORTED: return "d_state outside 1..64 is not supported";
+    case MAMBA_ERR_NOALLOC_LIMIT:
+      return "mamba_scan_bwd_noalloc: these sizes need more scratch than the static 32 MiB array";
     default: return "unknown error code";
   }
 }
