@@ -327,12 +327,11 @@ scan_bwd_kernel(const BwdParams p) {
             vd[NPT + 2 * pp + 1] = xc[pp].y;
           }
           RSd::run(vd, lane);
-          if (dwriter) {
 #pragma unroll
-            for (int r = 0; r < kD; ++r) {
-              const int idx = dbase + r;   // < NPT: d_B of state n0+idx, else d_C of n0+idx-NPT
-              red[(warp * kChunk + i) * 2 * NP + (idx / NPT) * NP + n0 + (idx % NPT)] = vd[r];
-            }
+          for (int r = 0; r < kD; ++r) {
+            const int idx = dbase + r;   // < NPT: d_B of state n0+idx, else d_C of n0+idx-NPT
+            st_shared_if(red + (warp * kChunk + i) * 2 * NP + (idx / NPT) * NP + n0 + (idx % NPT),
+                         vd[r], dwriter);
           }
         }
         // sums over n, scattered so that each lane finishes one (step, channel)
@@ -348,12 +347,11 @@ scan_bwd_kernel(const BwdParams p) {
           const float Dj = j ? Dd[1] : Dd[0];
           const float y = fmaf(Dj, uu, vn[3 * r]);
           const float sA = vn[3 * r + 1], sB = vn[3 * r + 2];
-          if (t < T && d < Di) {
-            const size_t o = (rowb + t) * Di + d;
-            p.d_delta[o] = fmaf(sA, kLn2, uu * sB);
-            p.d_u[o] = fmaf(dyj, Dj, dl * sB);
-            p.d_gate[o] = y * gf;
-          }
+          const bool ok = (t < T) && (d < Di);
+          const size_t o = (rowb + t) * Di + d;
+          st_global_if(p.d_delta + o, fmaf(sA, kLn2, uu * sB), ok);
+          st_global_if(p.d_u + o, fmaf(dyj, Dj, dl * sB), ok);
+          st_global_if(p.d_gate + o, y * gf, ok);
         }
       }
     }

@@ -59,6 +59,20 @@ __device__ __forceinline__ float4 lds4(const float* p) {
   return v;
 }
 
+// Predicated stores without a branch. A conditional store inside the unrolled step loops would
+// split them into basic blocks and stop the scheduler from overlapping neighbouring steps. When
+// the predicate is false the address is never accessed, so it may point past the buffer.
+__device__ __forceinline__ void st_global_if(float* p, float v, bool pred) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q st.global.f32 [%0], %1;\n\t}"
+      ::"l"(p), "f"(v), "r"((unsigned)pred) : "memory");
+}
+__device__ __forceinline__ void st_shared_if(float* p, float v, bool pred) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q st.shared.f32 [%0], %1;\n\t}"
+      ::"r"(smem_addr(p)), "f"(v), "r"((unsigned)pred) : "memory");
+}
+
 // NPR float2 pairs of consecutive states from shared memory (8- or 16-byte aligned).
 template <int NPR>
 __device__ __forceinline__ void lds_pairs(const float* p, float2 (&out)[NPR]) {

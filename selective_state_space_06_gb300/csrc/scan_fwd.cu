@@ -96,7 +96,7 @@ __device__ __forceinline__ void fwd_load_chunk(const FwdParams& p, float* st, in
   cp_async_commit();
 }
 
-template <int NP, bool VEC>
+template <int NP, bool VEC, bool WITH_Y>
 __global__ void __launch_bounds__(kWarps * 32)
 scan_fwd_kernel(const FwdParams p) {
   using S = FwdShape<NP>;
@@ -197,11 +197,10 @@ scan_fwd_kernel(const FwdParams p) {
         const float uu = s_u[i * DC + cl + j];
         const float g = s_g[i * DC + cl + j];
         const float y = fmaf(j ? Dd[1] : Dd[0], uu, yv[r]);
-        if (t < T && d < Di) {
-          const size_t o = (rowb + t) * Di + d;
-          p.out[o] = y * (g * sigmoid_fast(g));
-          if (p.y) p.y[o] = y;
-        }
+        const bool ok = (t < T) && (d < Di);
+        const size_t o = (rowb + t) * Di + d;
+        st_global_if(p.out + o, y * (g * sigmoid_fast(g)), ok);
+        if constexpr (WITH_Y) st_global_if(p.y + o, y, ok);
       }
     }
 
@@ -224,21 +223,23 @@ scan_fwd_kernel(const FwdParams p) {
   cp_async_wait<0>();
 }
 
-template <int NP, bool VEC>
+template <int NP, bool VEC, bool WITH_Y>
 static int launch_np(const Plan& plan, const FwdParams& p, cudaStream_t s) {
   using S = FwdShape<NP>;
-  if (cudaFuncSetAttribute(scan_fwd_kernel<NP, VEC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto kern = scan_fwd_kernel<NP, VEC, WITH_Y>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)S::kSmemBytes) != cudaSuccess)
     return -1;
   dim3 grid((unsigned)((plan.Di + S::DC - 1) / S::DC), (unsigned)plan.batch);
-  scan_fwd_kernel<NP, VEC><<<grid, kWarps * 32, S::kSmemBytes, s>>>(p);
+  kern<<<grid, kWarps * 32, S::kSmemBytes, s>>>(p);
   return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
 }
 
 template <int NP>
 static int launch_vec(const Plan& plan, const FwdParams& p, cudaStream_t s) {
   const bool vec = (plan.Di % 4 == 0) && (plan.N % 4 == 0);
-  return vec ? launch_np<NP, true>(plan, p, s) : launch_np<NP, false>(plan, p, s);
+  if (p.y) return vec ? launch_np<NP, true, true>(plan, p, s) : launch_np<NP, false, true>(plan, p, s);
+  return vec ? launch_np<NP, true, false>(plan, p, s) : launch_np<NP, false, false>(plan, p, s);
 }
 
 int launch_fwd(const Plan& plan, const FwdParams& p, cudaStream_t s) {
