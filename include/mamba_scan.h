@@ -123,7 +123,7 @@ int mamba_scan_fwd_bwd_host(const float* delta, const float* u, const float* B, 
  * Nothing needs clearing, because the backward rewrites all the scratch it reads. Calls that
  * overlap on the GPU race on the array: order them (one stream, or explicit events). No
  * cudaMalloc, cudaFree or allocating library routine is called. */
-#define MAMBA_SCAN_NOALLOC_SCRATCH_BYTES (32u << 20) /* 32 MiB */
+#define MAMBA_SCAN_NOALLOC_SCRATCH_BYTES (64u << 20) /* 64 MiB */
 int mamba_scan_bwd_noalloc(const float* delta, const float* u, const float* B, const float* C,
                            const float* gate, const float* A_log, const float* D,
                            const float* dy, const void* ckpt, size_t ckpt_bytes, float* d_delta,

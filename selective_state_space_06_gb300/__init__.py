@@ -35,7 +35,7 @@ MAMBA_ERR_WORKSPACE = 3
 MAMBA_ERR_CUDA = 4
 MAMBA_ERR_UNSUPPORTED = 5
 MAMBA_ERR_NOALLOC_LIMIT = 6
-MAMBA_SCAN_NOALLOC_SCRATCH_BYTES = 32 << 20
+MAMBA_SCAN_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 EXPORTED = (
     "mamba_scan_ckpt_bytes", "mamba_scan_scratch_bytes", "mamba_scan_fwd", "mamba_scan_bwd",
@@ -173,7 +173,7 @@ def mamba_scan_bwd(delta, u, B, C, gate, A_log, D, dy, ckpt, scratch, d_delta, d
 def mamba_scan_bwd_noalloc(delta, u, B, C, gate, A_log, D, dy, ckpt, d_delta, d_u, d_B, d_C,
                            d_A_log, d_D, d_gate, stream=None):
     """Backward scan without a scratch argument, for callers that may not allocate device
-    memory. Scratch comes from the library's static 32 MiB device array, shared by every call
+    memory. Scratch comes from the library's static 64 MiB device array, shared by every call
     on the device; calls that overlap on the GPU race on it."""
     b, T, Di, N = _dims(delta, B)
     dev = delta.device

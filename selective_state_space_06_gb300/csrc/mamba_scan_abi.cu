@@ -25,17 +25,39 @@ bool make_plan(int64_t batch, int64_t T, int64_t Di, int64_t N, Plan* pl) {
   Plan p;
   p.batch = batch; p.T = T; p.Di = Di; p.N = N;
   p.NP = N <= 4 ? 4 : N <= 8 ? 8 : N <= 16 ? 16 : N <= 32 ? 32 : 64;
-  p.G = p.NP / states_per_thread(p.NP);
-  p.DC = kWarps * (32 / p.G) * kDPT;
-  p.nblk = (int)((Di + p.DC - 1) / p.DC);
   p.nchunks = (int)((T + kChunk - 1) / kChunk);
-  p.ckpt_elems = (size_t)batch * (size_t)(p.nchunks - 1) * (size_t)Di * (size_t)N;
-  const size_t part_bc = (size_t)p.nblk * (size_t)batch * (size_t)T * (size_t)N;
+  auto pass = [&](int npt, int target) {
+    PassPlan q;
+    q.NPT = npt;
+    q.G = p.NP / npt;
+    q.DC = kWarps * (32 / q.G) * kDPT;
+    q.nblk = (int)((Di + q.DC - 1) / q.DC);
+    const int64_t rows = (int64_t)batch * q.nblk;
+    int64_t want = (target + rows - 1) / rows;
+    if (want < 1) want = 1;
+    if (want > p.nchunks) want = p.nchunks;
+    q.seg_chunks = (int)((p.nchunks + want - 1) / want);
+    q.nseg = (p.nchunks + q.seg_chunks - 1) / q.seg_chunks;
+    return q;
+  };
+  p.fwd = pass(states_per_thread_fwd(p.NP), kTargetUnitsFwd);
+  p.bwd = pass(states_per_thread_bwd(p.NP), kTargetUnitsBwd);
+  const size_t bdn = (size_t)batch * (size_t)Di * (size_t)N;
+  const size_t bd = (size_t)batch * (size_t)Di;
+  size_t ck = round_up((size_t)(p.nchunks - 1) * bdn, kAlignFloats);
+  if (p.fwd.nseg > 1) {
+    p.off_fagg_h = ck; ck = round_up(ck + (size_t)p.fwd.nseg * bdn, kAlignFloats);
+    p.off_fagg_sd = ck; ck = round_up(ck + (size_t)p.fwd.nseg * bd, kAlignFloats);
+  }
+  p.ckpt_elems = (p.nchunks > 1 || p.fwd.nseg > 1) ? ck : 0;
+  const size_t part_bc = (size_t)p.bwd.nblk * (size_t)batch * (size_t)T * (size_t)N;
   size_t off = 0;
   p.off_partB = off; off = round_up(off + part_bc, kAlignFloats);
   p.off_partC = off; off = round_up(off + part_bc, kAlignFloats);
-  p.off_partA = off; off = round_up(off + (size_t)batch * Di * N, kAlignFloats);
-  p.off_partD = off; off = round_up(off + (size_t)batch * Di, kAlignFloats);
+  p.off_partA = off; off = round_up(off + (size_t)p.bwd.nseg * bdn, kAlignFloats);
+  p.off_partD = off; off = round_up(off + (size_t)p.bwd.nseg * bd, kAlignFloats);
+  p.off_bagg_L = off; off = round_up(off + (size_t)p.bwd.nseg * bdn, kAlignFloats);
+  p.off_bagg_sd = off; off = round_up(off + (size_t)p.bwd.nseg * bd, kAlignFloats);
   p.scratch_elems = off;
   *pl = p;
   return true;
@@ -111,8 +133,11 @@ int mamba_scan_fwd(const float* delta, const float* u, const float* B, const flo
   mscan::FwdParams p;
   p.delta = delta; p.u = u; p.B = B; p.C = C; p.gate = gate; p.A_log = A_log; p.D = D;
   p.out = out; p.y = y; p.ckpt = (float*)ckpt;
+  p.agg_h = plan.fwd.nseg > 1 ? (float*)ckpt + plan.off_fagg_h : nullptr;
+  p.agg_sd = plan.fwd.nseg > 1 ? (float*)ckpt + plan.off_fagg_sd : nullptr;
   p.batch = (int)batch; p.T = (int)T; p.Di = (int)d_inner; p.N = (int)d_state;
-  p.nchunks = plan.nchunks;
+  p.nchunks = plan.nchunks; p.nblk = plan.fwd.nblk;
+  p.seg_chunks = plan.fwd.seg_chunks; p.nseg = plan.fwd.nseg;
   const int n = mscan::launch_fwd(plan, p, (cudaStream_t)stream);
   if (n < 0) return set_cuda_error(cudaGetLastError());
   g_last_launches = n;
@@ -165,9 +190,11 @@ int mamba_scan_bwd(const float* delta, const float* u, const float* B, const flo
   p.d_delta = d_delta; p.d_u = d_u; p.d_gate = d_gate;
   p.partB = sc + plan.off_partB; p.partC = sc + plan.off_partC;
   p.partA = sc + plan.off_partA; p.partD = sc + plan.off_partD;
+  p.agg_L = sc + plan.off_bagg_L; p.agg_sd = sc + plan.off_bagg_sd;
   p.d_B = d_B; p.d_C = d_C; p.d_A_log = d_A_log; p.d_D = d_D;
   p.batch = (int)batch; p.T = (int)T; p.Di = (int)d_inner; p.N = (int)d_state;
-  p.nchunks = plan.nchunks; p.nblk = plan.nblk;
+  p.nchunks = plan.nchunks; p.nblk = plan.bwd.nblk;
+  p.seg_chunks = plan.bwd.seg_chunks; p.nseg = plan.bwd.nseg;
   const int n = mscan::launch_bwd(plan, p, (cudaStream_t)stream);
   if (n < 0) return set_cuda_error(cudaGetLastError());
   g_last_launches = n;
@@ -270,7 +297,7 @@ const char* mamba_scan_strerror(int code) {
     case MAMBA_ERR_CUDA: return cudaGetErrorString(g_last_cuda);
     case MAMBA_ERR_UNSUPPORTED: return "d_state outside 1..64 is not supported";
     case MAMBA_ERR_NOALLOC_LIMIT:
-      return "mamba_scan_bwd_noalloc: these sizes need more scratch than the static 32 MiB array";
+      return "mamba_scan_bwd_noalloc: these sizes need more scratch than the static 64 MiB array";
     default: return "unknown error code";
   }
 }

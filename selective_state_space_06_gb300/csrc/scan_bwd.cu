@@ -35,7 +35,7 @@ constexpr int kBwdStages = 3;
 
 template <int NP>
 struct BwdShape {
-  static constexpr int NPT = states_per_thread(NP);
+  static constexpr int NPT = states_per_thread_bwd(NP);
   static constexpr int NPR = NPT / 2;
   static constexpr int kSub = 32 / NPT;         // steps kept in registers at a time (64 floats)
   static constexpr int kNSub = kChunk / kSub;
@@ -43,13 +43,16 @@ struct BwdShape {
   static constexpr int DW = (32 / G) * kDPT;
   static constexpr int DC = kWarps * DW;
   static constexpr int P = G >= 2 ? G / 2 : 1;
-  static constexpr int kStageFloats = kChunk * (4 * DC + 2 * NP);
+  // per stage: delta, u, gate, dy [kChunk][DC]; B, C [kChunk][NP]; the chunk's starting
+  // checkpoint [DC][N] (N <= NP)
+  static constexpr int kStageFloats = kChunk * (4 * DC + 2 * NP) + DC * NP;
   static constexpr int kRedFloats = kWarps * kChunk * 2 * NP;
   static constexpr size_t kSmemBytes =
       ((size_t)kBwdStages * kStageFloats + kRedFloats) * sizeof(float);
 };
 
-template <int NP, bool VEC>
+// AGG: the segment pre-pass needs only delta, gate, dy and C.
+template <int NP, bool VEC, bool AGG = false>
 __device__ __forceinline__ void bwd_load_chunk(const BwdParams& p, float* st, int c, int b,
                                                int dblk0) {
   using S = BwdShape<NP>;
@@ -69,7 +72,7 @@ __device__ __forceinline__ void bwd_load_chunk(const BwdParams& p, float* st, in
       const bool v = t < p.T && d < p.Di;
       const size_t go = v ? (rowb + t) * p.Di + d : 0;
       cp_async16(s_dl + i * DC + col, p.delta + go, v);
-      cp_async16(s_u + i * DC + col, p.u + go, v);
+      if (!AGG) cp_async16(s_u + i * DC + col, p.u + go, v);
       cp_async16(s_g + i * DC + col, p.gate + go, v);
       cp_async16(s_dy + i * DC + col, p.dy + go, v);
     }
@@ -78,7 +81,7 @@ __device__ __forceinline__ void bwd_load_chunk(const BwdParams& p, float* st, in
       const int t = t0 + i;
       const bool v = t < p.T && n < p.N;
       const size_t go = v ? (rowb + t) * p.N + n : 0;
-      cp_async16(s_B + i * NP + n, p.B + go, v);
+      if (!AGG) cp_async16(s_B + i * NP + n, p.B + go, v);
       cp_async16(s_C + i * NP + n, p.C + go, v);
     }
   } else {
@@ -88,7 +91,7 @@ __device__ __forceinline__ void bwd_load_chunk(const BwdParams& p, float* st, in
       const bool v = t < p.T && d < p.Di;
       const size_t go = v ? (rowb + t) * p.Di + d : 0;
       cp_async4(s_dl + i * DC + col, p.delta + go, v);
-      cp_async4(s_u + i * DC + col, p.u + go, v);
+      if (!AGG) cp_async4(s_u + i * DC + col, p.u + go, v);
       cp_async4(s_g + i * DC + col, p.gate + go, v);
       cp_async4(s_dy + i * DC + col, p.dy + go, v);
     }
@@ -97,11 +100,141 @@ __device__ __forceinline__ void bwd_load_chunk(const BwdParams& p, float* st, in
       const int t = t0 + i;
       const bool v = t < p.T && n < p.N;
       const size_t go = v ? (rowb + t) * p.N + n : 0;
-      cp_async4(s_B + i * NP + n, p.B + go, v);
+      if (!AGG) cp_async4(s_B + i * NP + n, p.B + go, v);
       cp_async4(s_C + i * NP + n, p.C + go, v);
     }
   }
+  if constexpr (!AGG) {
+    // state entering chunk c (checkpoint slot c-1); zeros for the first chunk
+    float* s_h0 = s_C + kChunk * NP;
+    const bool have = c > 0;
+    const float* src = have ? p.ckpt + (((size_t)b * (p.nchunks - 1) + (c - 1)) * p.Di + dblk0) * p.N
+                            : p.ckpt;
+    const int rowlen = DC * p.N;
+    if constexpr (VEC) {
+      for (int q = threadIdx.x * 4; q < rowlen; q += NTH * 4) {
+        const bool v = have && (dblk0 + q / p.N < p.Di);
+        cp_async16(s_h0 + q, v ? src + q : p.delta, v);
+      }
+    } else {
+      for (int q = threadIdx.x; q < rowlen; q += NTH) {
+        const bool v = have && (dblk0 + q / p.N < p.Di);
+        cp_async4(s_h0 + q, v ? src + q : p.delta, v);
+      }
+    }
+  }
   cp_async_commit();
+}
+
+// Segment pre-pass of the backward: for every segment but the first, run the d_h recurrence of
+// Phase B3 from a zero carry at the segment's end back to its start. That gives the local
+// prefix L = sum_t (prod_{s<=t} exp(delta_s*A)) * d_y_t * C_t[n] (products from the segment's
+// first step to t), plus the segment's sum of delta. The carry leaving a segment towards
+// earlier time is L + exp(A * sum(delta)) * (carry entering it from later time), so the main
+// kernel composes these exactly. The sum is accumulated in forward order, with the staging of
+// the main kernel.
+template <int NP, bool VEC>
+__global__ void __launch_bounds__(kWarps * 32)
+scan_bwd_agg_kernel(const BwdParams p) {
+  using S = BwdShape<NP>;
+  constexpr int G = S::G, DW = S::DW, DC = S::DC, NPT = S::NPT, NPR = S::NPR;
+  constexpr int NTH = kWarps * 32;
+  extern __shared__ __align__(16) float smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ng = lane % G, dg = lane / G;
+  const int b = blockIdx.y;
+  const int blk = blockIdx.x % p.nblk, seg = 1 + blockIdx.x / p.nblk;
+  const int dblk0 = blk * DC;
+  const int cl = warp * DW + dg * kDPT;
+  const int d0 = dblk0 + cl;
+  const int n0 = ng * NPT;
+  const int Di = p.Di, N = p.N;
+  const int c_begin = seg * p.seg_chunks;
+  const int c_end = min(p.nchunks, c_begin + p.seg_chunks);
+
+  float2 a2[kDPT][NPR], cum[kDPT][NPR], L[kDPT][NPR];
+  float sd[kDPT] = {0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < kDPT; ++j) {
+    const int d = d0 + j;
+    const bool dv = d < Di;
+    float t4[NPT];
+#pragma unroll
+    for (int k = 0; k < NPT; ++k) {
+      const int n = n0 + k;
+      t4[k] = (dv && n < N) ? -expf(p.A_log[(size_t)d * N + n]) * kLog2e : 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < NPR; ++q) {
+      a2[j][q] = make_float2(t4[2 * q], t4[2 * q + 1]);
+      cum[j][q] = make_float2(1.f, 1.f);
+      L[j][q] = make_float2(0.f, 0.f);
+    }
+  }
+
+#pragma unroll
+  for (int s = 0; s < kBwdStages - 1; ++s) {
+    if (c_begin + s < c_end)
+      bwd_load_chunk<NP, VEC, true>(p, smem + s * S::kStageFloats, c_begin + s, b, dblk0);
+    else
+      cp_async_commit();
+  }
+  for (int c = c_begin; c < c_end; ++c) {
+    const int it = c - c_begin;
+    cp_async_wait<kBwdStages - 2>();
+    __syncthreads();
+    {
+      const int cn = c + kBwdStages - 1;
+      if (cn < c_end)
+        bwd_load_chunk<NP, VEC, true>(
+            p, smem + ((it + kBwdStages - 1) % kBwdStages) * S::kStageFloats, cn, b, dblk0);
+      else
+        cp_async_commit();
+    }
+    float* st = smem + (it % kBwdStages) * S::kStageFloats;
+    const float* s_dl = st;
+    float* s_g = st + 2 * kChunk * DC;    // becomes d_y
+    const float* s_dy = st + 3 * kChunk * DC;
+    const float* s_C = st + 4 * kChunk * DC + kChunk * NP;
+    for (int e = threadIdx.x; e < kChunk * DC; e += NTH) {
+      const float g = s_g[e];
+      s_g[e] = s_dy[e] * (g * sigmoid_fast(g));
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i) {
+      const float2 dlv = lds2(s_dl + i * DC + cl);
+      const float2 dyv = lds2(s_g + i * DC + cl);
+      float2 Cp[NPR];
+      lds_pairs<NPR>(s_C + i * NP + n0, Cp);
+#pragma unroll
+      for (int j = 0; j < kDPT; ++j) {
+        const float dl = j ? dlv.y : dlv.x;
+        sd[j] += dl;
+        const float2 dl2 = splat2(dl), dy2 = splat2(j ? dyv.y : dyv.x);
+#pragma unroll
+        for (int q = 0; q < NPR; ++q) {
+          cum[j][q] = mul2(cum[j][q], ex2_2(mul2(dl2, a2[j][q])));
+          L[j][q] = fma2(cum[j][q], mul2(dy2, Cp[q]), L[j][q]);
+        }
+      }
+    }
+  }
+  cp_async_wait<0>();
+#pragma unroll
+  for (int j = 0; j < kDPT; ++j) {
+    const int d = d0 + j;
+    if (d >= Di) continue;
+    const size_t row = ((size_t)b * p.nseg + seg) * Di + d;
+    if (ng == 0) p.agg_sd[row] = sd[j];
+    if constexpr (VEC) {
+      if (n0 < N) st_pairs<NPR>(p.agg_L + row * N + n0, L[j]);   // N % 4 == 0 here
+    } else {
+#pragma unroll
+      for (int k = 0; k < NPT; ++k)
+        if (n0 + k < N) p.agg_L[row * N + n0 + k] = (k & 1) ? L[j][k >> 1].y : L[j][k >> 1].x;
+    }
+  }
 }
 
 // Forward recurrence of step i of the staged chunk on the thread's 2 x 4 states hc.
@@ -139,11 +272,14 @@ scan_bwd_kernel(const BwdParams p) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ng = lane % G, dg = lane / G;
   const int b = blockIdx.y;
-  const int dblk0 = blockIdx.x * DC;
+  const int blk = blockIdx.x % p.nblk, seg = blockIdx.x / p.nblk;
+  const int dblk0 = blk * DC;
   const int cl = warp * DW + dg * kDPT;
   const int d0 = dblk0 + cl;
   const int n0 = ng * NPT;
   const int Di = p.Di, N = p.N, T = p.T;
+  const int c_begin = seg * p.seg_chunks;
+  const int c_end = min(p.nchunks, c_begin + p.seg_chunks);
 
   float2 a2[kDPT][NPR], dh[kDPT][NPR], accA[kDPT][NPR];
   float Dd[kDPT], dD[kDPT];
@@ -174,21 +310,53 @@ scan_bwd_kernel(const BwdParams p) {
   const bool dwriter = RSd::writer(lane);
   constexpr int kD = RSd::kept();
   const size_t rowb = (size_t)b * T;
-  const int last = p.nchunks - 1;
+  const int last = c_end - 1;           // chunks of this segment, walked last to first
+  const int nck = c_end - c_begin;
 
 #pragma unroll
   for (int s = 0; s < kBwdStages - 1; ++s) {
-    if (last - s >= 0) bwd_load_chunk<NP, VEC>(p, smem + s * S::kStageFloats, last - s, b, dblk0);
+    if (s < nck) bwd_load_chunk<NP, VEC>(p, smem + s * S::kStageFloats, last - s, b, dblk0);
     else cp_async_commit();
   }
 
-  for (int it = 0; it <= last; ++it) {
+  // d_h entering the segment from the future: compose the later segments' aggregates,
+  // d_h <- L + exp(A * sum(delta)) * d_h, from the last segment down to seg + 1
+  for (int sp = p.nseg - 1; sp > seg; --sp) {
+#pragma unroll
+    for (int j = 0; j < kDPT; ++j) {
+      const int d = d0 + j;
+      if (d >= Di) continue;
+      const size_t row = ((size_t)b * p.nseg + sp) * Di + d;
+      const float sd = p.agg_sd[row];
+      float2 Lv[NPR];
+      if constexpr (VEC) {
+        if (n0 < N) {
+          ld_pairs<NPR>(p.agg_L + row * N + n0, Lv);
+        } else {
+#pragma unroll
+          for (int q = 0; q < NPR; ++q) Lv[q] = make_float2(0.f, 0.f);
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < NPR; ++q) {
+          const int n = n0 + 2 * q;
+          Lv[q] = make_float2(n < N ? p.agg_L[row * N + n] : 0.f,
+                              n + 1 < N ? p.agg_L[row * N + n + 1] : 0.f);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < NPR; ++q)
+        dh[j][q] = fma2(ex2_2(mul2(splat2(sd), a2[j][q])), dh[j][q], Lv[q]);
+    }
+  }
+
+  for (int it = 0; it < nck; ++it) {
     const int c = last - it;
     cp_async_wait<kBwdStages - 2>();
     __syncthreads();
     {
       const int itn = it + kBwdStages - 1;
-      if (last - itn >= 0)
+      if (itn < nck)
         bwd_load_chunk<NP, VEC>(p, smem + (itn % kBwdStages) * S::kStageFloats, last - itn, b,
                                 dblk0);
       else
@@ -216,23 +384,25 @@ scan_bwd_kernel(const BwdParams p) {
     // The sub-block start states come from one recompute pass without stash. Then, for each
     // sub-block from last to first, the states are recomputed into registers and walked in
     // reverse. That is 1.5x the recompute work of a full-chunk stash, but half the registers.
-    const float* ck = (c > 0) ? p.ckpt + ((size_t)b * last + (c - 1)) * (size_t)Di * N : nullptr;
+    // the chunk's starting state, staged with the chunk (zeros for chunk 0)
+    const float* s_h0 = s_C + kChunk * NP;
     float2 hsub[kNSub][kDPT][NPR];
 #pragma unroll
     for (int j = 0; j < kDPT; ++j) {
-      const int d = d0 + j;
-#pragma unroll
-      for (int q = 0; q < NPR; ++q) hsub[0][j][q] = make_float2(0.f, 0.f);
-      if (ck && d < Di) {
-        if constexpr (VEC) {
-          ld_pairs<NPR>(ck + (size_t)d * N + n0, hsub[0][j]);
+      const int e = (cl + j) * N + n0;
+      if constexpr (VEC) {
+        if (n0 < N) {
+          lds_pairs<NPR>(s_h0 + e, hsub[0][j]);
         } else {
-          float hv[NPT];
 #pragma unroll
-          for (int k = 0; k < NPT; ++k) hv[k] = (n0 + k < N) ? ck[(size_t)d * N + n0 + k] : 0.f;
-#pragma unroll
-          for (int q = 0; q < NPR; ++q) hsub[0][j][q] = make_float2(hv[2 * q], hv[2 * q + 1]);
+          for (int q = 0; q < NPR; ++q) hsub[0][j][q] = make_float2(0.f, 0.f);
         }
+      } else {
+        float hv[NPT];
+#pragma unroll
+        for (int k = 0; k < NPT; ++k) hv[k] = (n0 + k < N && d0 + j < Di) ? s_h0[e + k] : 0.f;
+#pragma unroll
+        for (int q = 0; q < NPR; ++q) hsub[0][j][q] = make_float2(hv[2 * q], hv[2 * q + 1]);
       }
     }
     {
@@ -243,8 +413,8 @@ scan_bwd_kernel(const BwdParams p) {
         for (int q = 0; q < NPR; ++q) hc[j][q] = hsub[0][j][q];
 #pragma unroll
       for (int sb = 1; sb < kNSub; ++sb) {
-#pragma unroll
-        for (int q = 0; q < kSub; ++q)
+#pragma unroll 1
+        for (int q = 0; q < kSub; ++q)   // no stash here: a rolled loop keeps the code small
           bwd_step_fwd<NP, DC, NPR>((sb - 1) * kSub + q, s_dl, s_u, s_B, cl, n0, a2, hc);
 #pragma unroll
         for (int j = 0; j < kDPT; ++j)
@@ -365,29 +535,30 @@ scan_bwd_kernel(const BwdParams p) {
         float sum = 0.f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) sum += red[(w * kChunk + i) * 2 * NP + kn];
-        const size_t o = (((size_t)blockIdx.x * p.batch + b) * T + t) * N + n;
+        const size_t o = (((size_t)blk * p.batch + b) * T + t) * N + n;
         (kind ? p.partC : p.partB)[o] = sum;
       }
     }
   }
   cp_async_wait<0>();
 
-  // per-batch partials of d_A_log (= A * sum_t delta*r = ln2*a2*accA) and d_D
+  // per-(batch, segment) partials of d_A_log (= A * sum_t delta*r = ln2*a2*accA) and d_D
 #pragma unroll
   for (int j = 0; j < kDPT; ++j) {
     const int d = d0 + j;
     if (d >= Di) continue;
+    const size_t row = ((size_t)b * p.nseg + seg) * Di + d;
 #pragma unroll
     for (int k = 0; k < NPT; ++k) {
       const float2 aa = a2[j][k >> 1], ac = accA[j][k >> 1];
-      if (n0 + k < N)
-        p.partA[((size_t)b * Di + d) * N + n0 + k] = kLn2 * ((k & 1) ? aa.y * ac.y : aa.x * ac.x);
+      if (n0 + k < N) p.partA[row * N + n0 + k] = kLn2 * ((k & 1) ? aa.y * ac.y : aa.x * ac.x);
     }
-    if (ng == 0) p.partD[(size_t)b * Di + d] = dD[j];
+    if (ng == 0) p.partD[row] = dD[j];
   }
 }
 
-// Fixed-order sums of the partials: d_B/d_C over CTAs along d, d_A_log/d_D over batch.
+// Fixed-order sums of the partials: d_B/d_C over CTAs along d, d_A_log/d_D over
+// (batch, segment).
 __global__ void scan_reduce_kernel(const BwdParams p) {
   const size_t btn = (size_t)p.batch * p.T * p.N;
   const size_t dn = (size_t)p.Di * p.N;
@@ -405,12 +576,12 @@ __global__ void scan_reduce_kernel(const BwdParams p) {
     } else if (e < btn + dn) {
       const size_t q = e - btn;
       float sa = 0.f;
-      for (int bb = 0; bb < p.batch; ++bb) sa += p.partA[(size_t)bb * dn + q];
+      for (int k = 0; k < p.batch * p.nseg; ++k) sa += p.partA[(size_t)k * dn + q];
       p.d_A_log[q] = sa;
     } else {
       const size_t q = e - btn - dn;
       float sd = 0.f;
-      for (int bb = 0; bb < p.batch; ++bb) sd += p.partD[(size_t)bb * p.Di + q];
+      for (int k = 0; k < p.batch * p.nseg; ++k) sd += p.partD[(size_t)k * p.Di + q];
       p.d_D[q] = sd;
     }
   }
@@ -422,9 +593,20 @@ static int launch_np(const Plan& plan, const BwdParams& p, cudaStream_t s) {
   if (cudaFuncSetAttribute(scan_bwd_kernel<NP, VEC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)S::kSmemBytes) != cudaSuccess)
     return -1;
-  dim3 grid((unsigned)((plan.Di + S::DC - 1) / S::DC), (unsigned)plan.batch);
+  int n = 0;
+  if (plan.bwd.nseg > 1) {
+    if (cudaFuncSetAttribute(scan_bwd_agg_kernel<NP, VEC>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)S::kSmemBytes) != cudaSuccess)
+      return -1;
+    dim3 ga((unsigned)(plan.bwd.nblk * (plan.bwd.nseg - 1)), (unsigned)plan.batch);
+    scan_bwd_agg_kernel<NP, VEC><<<ga, kWarps * 32, S::kSmemBytes, s>>>(p);
+    if (cudaPeekAtLastError() != cudaSuccess) return -1;
+    ++n;
+  }
+  dim3 grid((unsigned)(plan.bwd.nblk * plan.bwd.nseg), (unsigned)plan.batch);
   scan_bwd_kernel<NP, VEC><<<grid, kWarps * 32, S::kSmemBytes, s>>>(p);
-  return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
+  return cudaPeekAtLastError() == cudaSuccess ? n + 1 : -1;
 }
 
 template <int NP>

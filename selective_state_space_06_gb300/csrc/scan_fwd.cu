@@ -34,7 +34,7 @@ constexpr int kFwdStages = 4;
 
 template <int NP>
 struct FwdShape {
-  static constexpr int NPT = states_per_thread(NP);    // states per thread
+  static constexpr int NPT = states_per_thread_fwd(NP);    // states per thread
   static constexpr int NPR = NPT / 2;                  // float2 pairs of states per thread
   static constexpr int G = NP / NPT;                   // lanes per channel group
   static constexpr int DW = (32 / G) * kDPT;           // channels per warp
@@ -44,7 +44,8 @@ struct FwdShape {
   static constexpr size_t kSmemBytes = (size_t)kFwdStages * kStageFloats * sizeof(float);
 };
 
-template <int NP, bool VEC>
+// AGG: the segment pre-pass needs only delta, u and B.
+template <int NP, bool VEC, bool AGG = false>
 __device__ __forceinline__ void fwd_load_chunk(const FwdParams& p, float* st, int c, int b,
                                                int dblk0) {
   using S = FwdShape<NP>;
@@ -64,7 +65,7 @@ __device__ __forceinline__ void fwd_load_chunk(const FwdParams& p, float* st, in
       const size_t go = v ? (rowb + t) * p.Di + d : 0;
       cp_async16(s_dl + i * DC + col, p.delta + go, v);
       cp_async16(s_u + i * DC + col, p.u + go, v);
-      cp_async16(s_g + i * DC + col, p.gate + go, v);
+      if (!AGG) cp_async16(s_g + i * DC + col, p.gate + go, v);
     }
     for (int q = threadIdx.x; q < kChunk * NP / 4; q += NTH) {
       const int i = q / (NP / 4), n = (q % (NP / 4)) * 4;
@@ -72,7 +73,7 @@ __device__ __forceinline__ void fwd_load_chunk(const FwdParams& p, float* st, in
       const bool v = t < p.T && n < p.N;
       const size_t go = v ? (rowb + t) * p.N + n : 0;
       cp_async16(s_B + i * NP + n, p.B + go, v);
-      cp_async16(s_C + i * NP + n, p.C + go, v);
+      if (!AGG) cp_async16(s_C + i * NP + n, p.C + go, v);
     }
   } else {
     for (int q = threadIdx.x; q < kChunk * DC; q += NTH) {
@@ -82,7 +83,7 @@ __device__ __forceinline__ void fwd_load_chunk(const FwdParams& p, float* st, in
       const size_t go = v ? (rowb + t) * p.Di + d : 0;
       cp_async4(s_dl + i * DC + col, p.delta + go, v);
       cp_async4(s_u + i * DC + col, p.u + go, v);
-      cp_async4(s_g + i * DC + col, p.gate + go, v);
+      if (!AGG) cp_async4(s_g + i * DC + col, p.gate + go, v);
     }
     for (int q = threadIdx.x; q < kChunk * NP; q += NTH) {
       const int i = q / NP, n = q % NP;
@@ -90,10 +91,111 @@ __device__ __forceinline__ void fwd_load_chunk(const FwdParams& p, float* st, in
       const bool v = t < p.T && n < p.N;
       const size_t go = v ? (rowb + t) * p.N + n : 0;
       cp_async4(s_B + i * NP + n, p.B + go, v);
-      cp_async4(s_C + i * NP + n, p.C + go, v);
+      if (!AGG) cp_async4(s_C + i * NP + n, p.C + go, v);
     }
   }
   cp_async_commit();
+}
+
+// Segment pre-pass of the forward: for every segment but the last, run the recurrence from a
+// zero state and keep the end state and the sum of delta over the segment, per (b, d, n).
+// Since h_end = exp(A * sum(delta)) * h_start + h_end(from zero), the main kernel composes these
+// to obtain the exact state entering each segment. Staging is the same as the main kernel's.
+template <int NP, bool VEC>
+__global__ void __launch_bounds__(kWarps * 32)
+scan_fwd_agg_kernel(const FwdParams p) {
+  using S = FwdShape<NP>;
+  constexpr int G = S::G, DW = S::DW, DC = S::DC, NPT = S::NPT, NPR = S::NPR;
+  extern __shared__ __align__(16) float smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ng = lane % G, dg = lane / G;
+  const int b = blockIdx.y;
+  const int blk = blockIdx.x % p.nblk, seg = blockIdx.x / p.nblk;
+  const int dblk0 = blk * DC;
+  const int cl = warp * DW + dg * kDPT;
+  const int d0 = dblk0 + cl;
+  const int n0 = ng * NPT;
+  const int Di = p.Di, N = p.N;
+  const int c_begin = seg * p.seg_chunks;
+  const int c_end = min(p.nchunks, c_begin + p.seg_chunks);
+
+  float2 a2[kDPT][NPR], h[kDPT][NPR];
+  float sd[kDPT] = {0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < kDPT; ++j) {
+    const int d = d0 + j;
+    const bool dv = d < Di;
+    float t4[NPT];
+#pragma unroll
+    for (int k = 0; k < NPT; ++k) {
+      const int n = n0 + k;
+      t4[k] = (dv && n < N) ? -expf(p.A_log[(size_t)d * N + n]) * kLog2e : 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < NPR; ++q) {
+      a2[j][q] = make_float2(t4[2 * q], t4[2 * q + 1]);
+      h[j][q] = make_float2(0.f, 0.f);
+    }
+  }
+
+#pragma unroll
+  for (int s = 0; s < kFwdStages - 1; ++s) {
+    if (c_begin + s < c_end)
+      fwd_load_chunk<NP, VEC, true>(p, smem + s * S::kStageFloats, c_begin + s, b, dblk0);
+    else
+      cp_async_commit();
+  }
+  for (int c = c_begin; c < c_end; ++c) {
+    const int it = c - c_begin;
+    cp_async_wait<kFwdStages - 2>();
+    __syncthreads();
+    {
+      const int cn = c + kFwdStages - 1;
+      if (cn < c_end)
+        fwd_load_chunk<NP, VEC, true>(
+            p, smem + ((it + kFwdStages - 1) % kFwdStages) * S::kStageFloats, cn, b, dblk0);
+      else
+        cp_async_commit();
+    }
+    const float* st = smem + (it % kFwdStages) * S::kStageFloats;
+    const float* s_dl = st;
+    const float* s_u = st + kChunk * DC;
+    const float* s_B = st + 3 * kChunk * DC;
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i) {
+      const float2 dlv = lds2(s_dl + i * DC + cl);
+      const float2 uv = lds2(s_u + i * DC + cl);
+      float2 Bp[NPR];
+      lds_pairs<NPR>(s_B + i * NP + n0, Bp);
+#pragma unroll
+      for (int j = 0; j < kDPT; ++j) {
+        const float dl = j ? dlv.y : dlv.x;
+        const float uu = j ? uv.y : uv.x;
+        sd[j] += dl;
+        const float2 dl2 = splat2(dl), du2 = splat2(dl * uu);
+#pragma unroll
+        for (int q = 0; q < NPR; ++q) {
+          const float2 da = ex2_2(mul2(dl2, a2[j][q]));
+          h[j][q] = fma2(da, h[j][q], mul2(du2, Bp[q]));
+        }
+      }
+    }
+  }
+  cp_async_wait<0>();
+#pragma unroll
+  for (int j = 0; j < kDPT; ++j) {
+    const int d = d0 + j;
+    if (d >= Di) continue;
+    const size_t row = ((size_t)b * p.nseg + seg) * Di + d;
+    if (ng == 0) p.agg_sd[row] = sd[j];
+    if constexpr (VEC) {
+      if (n0 < N) st_pairs<NPR>(p.agg_h + row * N + n0, h[j]);   // N % 4 == 0 here
+    } else {
+#pragma unroll
+      for (int k = 0; k < NPT; ++k)
+        if (n0 + k < N) p.agg_h[row * N + n0 + k] = (k & 1) ? h[j][k >> 1].y : h[j][k >> 1].x;
+    }
+  }
 }
 
 template <int NP, bool VEC, bool WITH_Y>
@@ -106,11 +208,14 @@ scan_fwd_kernel(const FwdParams p) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ng = lane % G, dg = lane / G;
   const int b = blockIdx.y;
-  const int dblk0 = blockIdx.x * DC;
+  const int blk = blockIdx.x % p.nblk, seg = blockIdx.x / p.nblk;
+  const int dblk0 = blk * DC;
   const int cl = warp * DW + dg * kDPT;   // first channel of this thread inside the CTA tile
   const int d0 = dblk0 + cl;
   const int n0 = ng * NPT;
   const int Di = p.Di, N = p.N, T = p.T;
+  const int c_begin = seg * p.seg_chunks;
+  const int c_end = min(p.nchunks, c_begin + p.seg_chunks);
 
   float2 a2[kDPT][NPR], h[kDPT][NPR];
   float Dd[kDPT];
@@ -139,21 +244,56 @@ scan_fwd_kernel(const FwdParams p) {
 
 #pragma unroll
   for (int s = 0; s < kFwdStages - 1; ++s) {
-    if (s < p.nchunks) fwd_load_chunk<NP, VEC>(p, smem + s * S::kStageFloats, s, b, dblk0);
-    else cp_async_commit();
+    if (c_begin + s < c_end)
+      fwd_load_chunk<NP, VEC>(p, smem + s * S::kStageFloats, c_begin + s, b, dblk0);
+    else
+      cp_async_commit();
   }
 
-  for (int c = 0; c < p.nchunks; ++c) {
+  // state entering the segment: compose the earlier segments' aggregates,
+  // h <- exp(A * sum(delta)) * h + (segment end state from zero)
+  for (int sp = 0; sp < seg; ++sp) {
+#pragma unroll
+    for (int j = 0; j < kDPT; ++j) {
+      const int d = d0 + j;
+      if (d >= Di) continue;
+      const size_t row = ((size_t)b * p.nseg + sp) * Di + d;
+      const float sd = p.agg_sd[row];
+      float2 hl[NPR];
+      if constexpr (VEC) {
+        if (n0 < N) {
+          ld_pairs<NPR>(p.agg_h + row * N + n0, hl);
+        } else {
+#pragma unroll
+          for (int q = 0; q < NPR; ++q) hl[q] = make_float2(0.f, 0.f);
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < NPR; ++q) {
+          const int n = n0 + 2 * q;
+          hl[q] = make_float2(n < N ? p.agg_h[row * N + n] : 0.f,
+                              n + 1 < N ? p.agg_h[row * N + n + 1] : 0.f);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < NPR; ++q)
+        h[j][q] = fma2(ex2_2(mul2(splat2(sd), a2[j][q])), h[j][q], hl[q]);
+    }
+  }
+
+  for (int c = c_begin; c < c_end; ++c) {
+    const int it = c - c_begin;
     cp_async_wait<kFwdStages - 2>();
     __syncthreads();
     {
       const int cn = c + kFwdStages - 1;
-      if (cn < p.nchunks)
-        fwd_load_chunk<NP, VEC>(p, smem + (cn % kFwdStages) * S::kStageFloats, cn, b, dblk0);
+      if (cn < c_end)
+        fwd_load_chunk<NP, VEC>(p, smem + ((it + kFwdStages - 1) % kFwdStages) * S::kStageFloats,
+                                cn, b, dblk0);
       else
         cp_async_commit();
     }
-    const float* st = smem + (c % kFwdStages) * S::kStageFloats;
+    const float* st = smem + (it % kFwdStages) * S::kStageFloats;
     const float* s_dl = st;
     const float* s_u = st + kChunk * DC;
     const float* s_g = st + 2 * kChunk * DC;
@@ -211,7 +351,7 @@ scan_fwd_kernel(const FwdParams p) {
         const int d = d0 + j;
         if (d >= Di) continue;
         if constexpr (VEC) {
-          st_pairs<NPR>(ck + (size_t)d * N + n0, h[j]);
+          if (n0 < N) st_pairs<NPR>(ck + (size_t)d * N + n0, h[j]);
         } else {
 #pragma unroll
           for (int k = 0; k < NPT; ++k)
@@ -230,9 +370,20 @@ static int launch_np(const Plan& plan, const FwdParams& p, cudaStream_t s) {
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)S::kSmemBytes) != cudaSuccess)
     return -1;
-  dim3 grid((unsigned)((plan.Di + S::DC - 1) / S::DC), (unsigned)plan.batch);
+  int n = 0;
+  if (plan.fwd.nseg > 1) {
+    if (cudaFuncSetAttribute(scan_fwd_agg_kernel<NP, VEC>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)S::kSmemBytes) != cudaSuccess)
+      return -1;
+    dim3 ga((unsigned)(plan.fwd.nblk * (plan.fwd.nseg - 1)), (unsigned)plan.batch);
+    scan_fwd_agg_kernel<NP, VEC><<<ga, kWarps * 32, S::kSmemBytes, s>>>(p);
+    if (cudaPeekAtLastError() != cudaSuccess) return -1;
+    ++n;
+  }
+  dim3 grid((unsigned)(plan.fwd.nblk * plan.fwd.nseg), (unsigned)plan.batch);
   kern<<<grid, kWarps * 32, S::kSmemBytes, s>>>(p);
-  return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
+  return cudaPeekAtLastError() == cudaSuccess ? n + 1 : -1;
 }
 
 template <int NP>

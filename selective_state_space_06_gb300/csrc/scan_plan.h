@@ -12,27 +12,61 @@ namespace mscan {
 //   states n; G = NP / NPT lanes of a warp share the same channels and split the states
 //   between them; a warp therefore covers (32 / G) * kDPT channels; a CTA has kWarps warps.
 constexpr int kDPT = 2;     // channels per thread
-#ifndef MSCAN_NPT
-#define MSCAN_NPT 4
+#ifndef MSCAN_NPT_FWD
+#define MSCAN_NPT_FWD 4
 #endif
-// states per thread (2 or 4) for d_state padded to NP
-__host__ __device__ constexpr int states_per_thread(int NP) {
-  return NP < MSCAN_NPT ? NP : MSCAN_NPT;
+#ifndef MSCAN_NPT_BWD
+#define MSCAN_NPT_BWD 4
+#endif
+// states per thread (2 or 4) for d_state padded to NP, in the forward and the backward passes
+__host__ __device__ constexpr int states_per_thread_fwd(int NP) {
+  return NP < MSCAN_NPT_FWD ? NP : MSCAN_NPT_FWD;
+}
+__host__ __device__ constexpr int states_per_thread_bwd(int NP) {
+  return NP < MSCAN_NPT_BWD ? NP : MSCAN_NPT_BWD;
 }
 constexpr int kWarps = 4;   // warps per CTA
 constexpr int kChunk = 16;  // time steps per chunk (= checkpoint interval)
 constexpr int kMaxState = 64;
 
+// The time axis is cut into nseg segments of seg_chunks chunks. One CTA handles one unit
+// (batch row, block of DC channels, segment). The state entering a segment comes from a small
+// pre-pass kernel that scans every segment independently from zero (the forward's aggregates:
+// the local end state and the sum of delta). For the backward, the pre-pass gives the local
+// d_h prefix and the sum of delta. The linear recurrence composes these aggregates exactly, so
+// the segments run in parallel.
+#ifndef MSCAN_UNITS_FWD
+#define MSCAN_UNITS_FWD 2048
+#endif
+#ifndef MSCAN_UNITS_BWD
+#define MSCAN_UNITS_BWD 2048
+#endif
+constexpr int kTargetUnitsFwd = MSCAN_UNITS_FWD;   // aim for this many units per pass
+constexpr int kTargetUnitsBwd = MSCAN_UNITS_BWD;
+
+// Work decomposition of one pass (forward or backward); the two may differ.
+struct PassPlan {
+  int NPT = 0;         // states per thread
+  int G = 0;           // lanes per channel group
+  int DC = 0;          // channels per CTA
+  int nblk = 0;        // CTAs along d_inner
+  int seg_chunks = 0;  // chunks per segment
+  int nseg = 0;        // segments along T
+};
+
 struct Plan {
   int64_t batch = 0, T = 0, Di = 0, N = 0;
-  int NP = 0;        // d_state padded to 4, 8, 16, 32 or 64
-  int G = 0;         // lanes per channel group
-  int DC = 0;        // channels per CTA
-  int nblk = 0;      // CTAs along d_inner
-  int nchunks = 0;   // chunks along T
-  size_t ckpt_elems = 0;
+  int NP = 0;          // d_state padded to 4, 8, 16, 32 or 64
+  int nchunks = 0;     // chunks along T
+  PassPlan fwd, bwd;
+  // checkpoint buffer layout (float offsets, 256-byte aligned regions):
+  //   [batch][nchunks-1][Di][N] chunk-boundary states, then the forward aggregates
+  //   [batch][fwd.nseg][Di][N] segment end states (from zero) and [batch][fwd.nseg][Di] sums
+  //   of delta
+  size_t off_fagg_h = 0, off_fagg_sd = 0, ckpt_elems = 0;
   // scratch layout (float offsets, each region 256-byte aligned)
-  size_t off_partB = 0, off_partC = 0, off_partA = 0, off_partD = 0, scratch_elems = 0;
+  size_t off_partB = 0, off_partC = 0, off_partA = 0, off_partD = 0;
+  size_t off_bagg_L = 0, off_bagg_sd = 0, scratch_elems = 0;
 };
 
 // Returns false when the sizes are outside what the kernels support.
@@ -42,7 +76,8 @@ struct FwdParams {
   const float* delta; const float* u; const float* B; const float* C; const float* gate;
   const float* A_log; const float* D;
   float* out; float* y; float* ckpt;
-  int batch, T, Di, N, nchunks;
+  float* agg_h; float* agg_sd;   // forward segment aggregates (inside the ckpt buffer)
+  int batch, T, Di, N, nchunks, nblk, seg_chunks, nseg;
 };
 
 struct BwdParams {
@@ -50,11 +85,15 @@ struct BwdParams {
   const float* A_log; const float* D; const float* dy; const float* ckpt;
   float* d_delta; float* d_u; float* d_gate;
   float* partB; float* partC; float* partA; float* partD;   // scratch
+  float* agg_L; float* agg_sd;                               // scratch: backward aggregates
   float* d_B; float* d_C; float* d_A_log; float* d_D;
-  int batch, T, Di, N, nchunks, nblk;
+  int batch, T, Di, N, nchunks, nblk, seg_chunks, nseg;
 };
 
 // Each returns the number of kernels enqueued (>= 1) or -1 on a launch error.
+// launch_fwd enqueues the segment pre-pass (when nseg > 1) and the forward scan; launch_bwd
+// enqueues the backward pre-pass (when nseg > 1), the backward scan and the fixed-order
+// reduction.
 int launch_fwd(const Plan& plan, const FwdParams& p, cudaStream_t stream);
 int launch_bwd(const Plan& plan, const BwdParams& p, cudaStream_t stream);
 

@@ -55,6 +55,13 @@ EDGE_SHAPES = [
     (1, 64, 33, 63),
     (2, 50, 17, 64),
     (4, 129, 257, 16),
+    # vectorised path (d_inner % 4 == 0, d_state % 4 == 0) with d_state below its padding
+    (2, 40, 64, 12),
+    (1, 50, 32, 20),
+    (2, 33, 16, 60),
+    (1, 70, 128, 4),
+    (2, 45, 96, 8),
+    (1, 300, 64, 28),
 ]
 
 

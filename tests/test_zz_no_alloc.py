@@ -2,7 +2,7 @@
 
 Some callers get only their input and output buffers. A plugin inside a framework that owns
 all device memory is one; a latency-critical loop that forbids cudaMalloc is another. For them
-the library takes the backward's scratch from a static 32 MiB device array instead of from the
+the library takes the backward's scratch from a static 64 MiB device array instead of from the
 caller.
 
 The GPU test calls the entry point through the C ABI, twice in a row on the same inputs. Each
@@ -85,4 +85,4 @@ def test_noalloc_rejects_sizes_beyond_the_static_scratch():
     rc = lib.mamba_scan_bwd_noalloc(*ptrs[:9], 1 << 40, *[big * (20 + i) for i in range(7)],
                                     b, T, Di, N, None)
     assert rc == ms.MAMBA_ERR_NOALLOC_LIMIT
-    assert "32 MiB" in ms.mamba_scan_strerror(rc)
+    assert "64 MiB" in ms.mamba_scan_strerror(rc)
