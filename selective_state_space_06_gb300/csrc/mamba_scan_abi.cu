@@ -40,8 +40,8 @@ bool make_plan(int64_t batch, int64_t T, int64_t Di, int64_t N, Plan* pl) {
     q.nseg = (p.nchunks + q.seg_chunks - 1) / q.seg_chunks;
     return q;
   };
-  p.fwd = pass(states_per_thread_fwd(p.NP), kTargetUnitsFwd);
-  p.bwd = pass(states_per_thread_bwd(p.NP), kTargetUnitsBwd);
+  p.fwd = pass(states_per_thread_fwd(p.NP), target_units_fwd(p.NP));
+  p.bwd = pass(states_per_thread_bwd(p.NP), target_units_bwd(p.NP));
   const size_t bdn = (size_t)batch * (size_t)Di * (size_t)N;
   const size_t bd = (size_t)batch * (size_t)Di;
   size_t ck = round_up((size_t)(p.nchunks - 1) * bdn, kAlignFloats);

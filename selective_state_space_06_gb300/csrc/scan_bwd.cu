@@ -49,6 +49,10 @@ struct BwdShape {
   static constexpr int kRedFloats = kWarps * kChunk * 2 * NP;
   static constexpr size_t kSmemBytes =
       ((size_t)kBwdStages * kStageFloats + kRedFloats) * sizeof(float);
+  // segment pre-pass: compact stages (delta, gate, dy [kChunk][DC]; C [kChunk][NP])
+  static constexpr int kAggStages = 4;
+  static constexpr int kAggStageFloats = kChunk * (3 * DC + NP);
+  static constexpr size_t kAggSmemBytes = (size_t)kAggStages * kAggStageFloats * sizeof(float);
 };
 
 // AGG: the segment pre-pass needs only delta, gate, dy and C.
@@ -57,12 +61,14 @@ __device__ __forceinline__ void bwd_load_chunk(const BwdParams& p, float* st, in
                                                int dblk0) {
   using S = BwdShape<NP>;
   constexpr int DC = S::DC, NTH = kWarps * 32;
+  // main layout: delta, u, gate, dy, B, C, checkpoint row; compact pre-pass layout: delta,
+  // gate, dy, C
   float* s_dl = st;
   float* s_u = st + kChunk * DC;
-  float* s_g = st + 2 * kChunk * DC;
-  float* s_dy = st + 3 * kChunk * DC;
+  float* s_g = st + (AGG ? 1 : 2) * kChunk * DC;
+  float* s_dy = st + (AGG ? 2 : 3) * kChunk * DC;
   float* s_B = st + 4 * kChunk * DC;
-  float* s_C = s_B + kChunk * NP;
+  float* s_C = AGG ? st + 3 * kChunk * DC : s_B + kChunk * NP;
   const int t0 = c * kChunk;
   const size_t rowb = (size_t)b * p.T;
   if constexpr (VEC) {
@@ -173,29 +179,29 @@ scan_bwd_agg_kernel(const BwdParams p) {
   }
 
 #pragma unroll
-  for (int s = 0; s < kBwdStages - 1; ++s) {
+  for (int s = 0; s < S::kAggStages - 1; ++s) {
     if (c_begin + s < c_end)
-      bwd_load_chunk<NP, VEC, true>(p, smem + s * S::kStageFloats, c_begin + s, b, dblk0);
+      bwd_load_chunk<NP, VEC, true>(p, smem + s * S::kAggStageFloats, c_begin + s, b, dblk0);
     else
       cp_async_commit();
   }
   for (int c = c_begin; c < c_end; ++c) {
     const int it = c - c_begin;
-    cp_async_wait<kBwdStages - 2>();
+    cp_async_wait<S::kAggStages - 2>();
     __syncthreads();
     {
-      const int cn = c + kBwdStages - 1;
+      const int cn = c + S::kAggStages - 1;
       if (cn < c_end)
         bwd_load_chunk<NP, VEC, true>(
-            p, smem + ((it + kBwdStages - 1) % kBwdStages) * S::kStageFloats, cn, b, dblk0);
+            p, smem + ((it + S::kAggStages - 1) % S::kAggStages) * S::kAggStageFloats, cn, b, dblk0);
       else
         cp_async_commit();
     }
-    float* st = smem + (it % kBwdStages) * S::kStageFloats;
+    float* st = smem + (it % S::kAggStages) * S::kAggStageFloats;
     const float* s_dl = st;
-    float* s_g = st + 2 * kChunk * DC;    // becomes d_y
-    const float* s_dy = st + 3 * kChunk * DC;
-    const float* s_C = st + 4 * kChunk * DC + kChunk * NP;
+    float* s_g = st + kChunk * DC;         // becomes d_y
+    const float* s_dy = st + 2 * kChunk * DC;
+    const float* s_C = st + 3 * kChunk * DC;
     for (int e = threadIdx.x; e < kChunk * DC; e += NTH) {
       const float g = s_g[e];
       s_g[e] = s_dy[e] * (g * sigmoid_fast(g));
@@ -597,10 +603,10 @@ static int launch_np(const Plan& plan, const BwdParams& p, cudaStream_t s) {
   if (plan.bwd.nseg > 1) {
     if (cudaFuncSetAttribute(scan_bwd_agg_kernel<NP, VEC>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)S::kSmemBytes) != cudaSuccess)
+                             (int)S::kAggSmemBytes) != cudaSuccess)
       return -1;
     dim3 ga((unsigned)(plan.bwd.nblk * (plan.bwd.nseg - 1)), (unsigned)plan.batch);
-    scan_bwd_agg_kernel<NP, VEC><<<ga, kWarps * 32, S::kSmemBytes, s>>>(p);
+    scan_bwd_agg_kernel<NP, VEC><<<ga, kWarps * 32, S::kAggSmemBytes, s>>>(p);
     if (cudaPeekAtLastError() != cudaSuccess) return -1;
     ++n;
   }

@@ -42,6 +42,9 @@ struct FwdShape {
   static constexpr int P = G >= 2 ? G / 2 : 1;         // steps per output group
   static constexpr int kStageFloats = kChunk * (3 * DC + 2 * NP);
   static constexpr size_t kSmemBytes = (size_t)kFwdStages * kStageFloats * sizeof(float);
+  // segment pre-pass: compact stages (delta, u [kChunk][DC]; B [kChunk][NP])
+  static constexpr int kAggStageFloats = kChunk * (2 * DC + NP);
+  static constexpr size_t kAggSmemBytes = (size_t)kFwdStages * kAggStageFloats * sizeof(float);
 };
 
 // AGG: the segment pre-pass needs only delta, u and B.
@@ -53,7 +56,8 @@ __device__ __forceinline__ void fwd_load_chunk(const FwdParams& p, float* st, in
   float* s_dl = st;
   float* s_u = st + kChunk * DC;
   float* s_g = st + 2 * kChunk * DC;
-  float* s_B = st + 3 * kChunk * DC;
+  // main layout: delta, u, gate, B, C; compact pre-pass layout: delta, u, B
+  float* s_B = st + (AGG ? 2 : 3) * kChunk * DC;
   float* s_C = s_B + kChunk * NP;
   const int t0 = c * kChunk;
   const size_t rowb = (size_t)b * p.T;
@@ -141,7 +145,7 @@ scan_fwd_agg_kernel(const FwdParams p) {
 #pragma unroll
   for (int s = 0; s < kFwdStages - 1; ++s) {
     if (c_begin + s < c_end)
-      fwd_load_chunk<NP, VEC, true>(p, smem + s * S::kStageFloats, c_begin + s, b, dblk0);
+      fwd_load_chunk<NP, VEC, true>(p, smem + s * S::kAggStageFloats, c_begin + s, b, dblk0);
     else
       cp_async_commit();
   }
@@ -153,14 +157,14 @@ scan_fwd_agg_kernel(const FwdParams p) {
       const int cn = c + kFwdStages - 1;
       if (cn < c_end)
         fwd_load_chunk<NP, VEC, true>(
-            p, smem + ((it + kFwdStages - 1) % kFwdStages) * S::kStageFloats, cn, b, dblk0);
+            p, smem + ((it + kFwdStages - 1) % kFwdStages) * S::kAggStageFloats, cn, b, dblk0);
       else
         cp_async_commit();
     }
-    const float* st = smem + (it % kFwdStages) * S::kStageFloats;
+    const float* st = smem + (it % kFwdStages) * S::kAggStageFloats;
     const float* s_dl = st;
     const float* s_u = st + kChunk * DC;
-    const float* s_B = st + 3 * kChunk * DC;
+    const float* s_B = st + 2 * kChunk * DC;
 #pragma unroll
     for (int i = 0; i < kChunk; ++i) {
       const float2 dlv = lds2(s_dl + i * DC + cl);
@@ -374,10 +378,10 @@ static int launch_np(const Plan& plan, const FwdParams& p, cudaStream_t s) {
   if (plan.fwd.nseg > 1) {
     if (cudaFuncSetAttribute(scan_fwd_agg_kernel<NP, VEC>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)S::kSmemBytes) != cudaSuccess)
+                             (int)S::kAggSmemBytes) != cudaSuccess)
       return -1;
     dim3 ga((unsigned)(plan.fwd.nblk * (plan.fwd.nseg - 1)), (unsigned)plan.batch);
-    scan_fwd_agg_kernel<NP, VEC><<<ga, kWarps * 32, S::kSmemBytes, s>>>(p);
+    scan_fwd_agg_kernel<NP, VEC><<<ga, kWarps * 32, S::kAggSmemBytes, s>>>(p);
     if (cudaPeekAtLastError() != cudaSuccess) return -1;
     ++n;
   }

@@ -12,19 +12,11 @@ namespace mscan {
 //   states n; G = NP / NPT lanes of a warp share the same channels and split the states
 //   between them; a warp therefore covers (32 / G) * kDPT channels; a CTA has kWarps warps.
 constexpr int kDPT = 2;     // channels per thread
-#ifndef MSCAN_NPT_FWD
-#define MSCAN_NPT_FWD 4
-#endif
-#ifndef MSCAN_NPT_BWD
-#define MSCAN_NPT_BWD 4
-#endif
-// states per thread (2 or 4) for d_state padded to NP, in the forward and the backward passes
-__host__ __device__ constexpr int states_per_thread_fwd(int NP) {
-  return NP < MSCAN_NPT_FWD ? NP : MSCAN_NPT_FWD;
-}
-__host__ __device__ constexpr int states_per_thread_bwd(int NP) {
-  return NP < MSCAN_NPT_BWD ? NP : MSCAN_NPT_BWD;
-}
+// States per thread (2 or 4) for d_state padded to NP. Measured on GB300: the forward is
+// fastest with 2 states per thread up to d_state 16 (twice the threads, so more latency hiding)
+// and with 4 beyond; the backward is fastest with 4 (fewer cross-lane reductions per element).
+__host__ __device__ constexpr int states_per_thread_fwd(int NP) { return NP <= 16 ? 2 : 4; }
+__host__ __device__ constexpr int states_per_thread_bwd(int NP) { return NP < 4 ? NP : 4; }
 constexpr int kWarps = 4;   // warps per CTA
 constexpr int kChunk = 16;  // time steps per chunk (= checkpoint interval)
 constexpr int kMaxState = 64;
@@ -35,14 +27,10 @@ constexpr int kMaxState = 64;
 // the local end state and the sum of delta). For the backward, the pre-pass gives the local
 // d_h prefix and the sum of delta. The linear recurrence composes these aggregates exactly, so
 // the segments run in parallel.
-#ifndef MSCAN_UNITS_FWD
-#define MSCAN_UNITS_FWD 2048
-#endif
-#ifndef MSCAN_UNITS_BWD
-#define MSCAN_UNITS_BWD 2048
-#endif
-constexpr int kTargetUnitsFwd = MSCAN_UNITS_FWD;   // aim for this many units per pass
-constexpr int kTargetUnitsBwd = MSCAN_UNITS_BWD;
+// Units (CTAs) to aim for per pass. The forward segments the time axis only at d_state > 16:
+// below that its pre-pass costs more than the extra parallelism gains (measured on GB300).
+__host__ __device__ constexpr int target_units_fwd(int NP) { return NP <= 16 ? 1 : 2048; }
+__host__ __device__ constexpr int target_units_bwd(int NP) { return 2048; }
 
 // Work decomposition of one pass (forward or backward); the two may differ.
 struct PassPlan {
