@@ -63,10 +63,11 @@ extern "C" {
                                      MAMBA_SCAN_NOALLOC_SCRATCH_BYTES                        */
 
 /* Bytes of the checkpoint buffer that mamba_scan_fwd writes and mamba_scan_bwd reads. The
- * forward stores the state h at every chunk boundary of the time axis, so that the backward
- * recomputes h inside one chunk at a time instead of storing it for every t. May be 0 (then
- * the ckpt pointer may be NULL). Returns 0 for invalid sizes as well; mamba_scan_fwd then
- * reports the error. */
+ * forward stores the state h at every 16-step chunk boundary of the time axis, so that the
+ * backward recomputes h inside one chunk at a time instead of storing it for every t. It also
+ * stores the per-segment aggregates of its time-parallel scan, and y = sum_n C*h + D*u, which
+ * the gating backward needs. The layout is internal to the library. Returns 0 for invalid
+ * sizes; mamba_scan_fwd then reports the error. */
 size_t mamba_scan_ckpt_bytes(int64_t batch, int64_t T, int64_t d_inner, int64_t d_state);
 
 /* Bytes of the scratch buffer mamba_scan_bwd needs for its deterministic two-level reductions

@@ -49,7 +49,8 @@ bool make_plan(int64_t batch, int64_t T, int64_t Di, int64_t N, Plan* pl) {
     p.off_fagg_h = ck; ck = round_up(ck + (size_t)p.fwd.nseg * bdn, kAlignFloats);
     p.off_fagg_sd = ck; ck = round_up(ck + (size_t)p.fwd.nseg * bd, kAlignFloats);
   }
-  p.ckpt_elems = (p.nchunks > 1 || p.fwd.nseg > 1) ? ck : 0;
+  p.off_y = ck; ck = round_up(ck + (size_t)batch * (size_t)T * (size_t)Di, kAlignFloats);
+  p.ckpt_elems = ck;
   const size_t part_bc = (size_t)p.bwd.nblk * (size_t)batch * (size_t)T * (size_t)N;
   size_t off = 0;
   p.off_partB = off; off = round_up(off + part_bc, kAlignFloats);
@@ -135,6 +136,7 @@ int mamba_scan_fwd(const float* delta, const float* u, const float* B, const flo
   p.out = out; p.y = y; p.ckpt = (float*)ckpt;
   p.agg_h = plan.fwd.nseg > 1 ? (float*)ckpt + plan.off_fagg_h : nullptr;
   p.agg_sd = plan.fwd.nseg > 1 ? (float*)ckpt + plan.off_fagg_sd : nullptr;
+  p.y_ck = (float*)ckpt + plan.off_y;
   p.batch = (int)batch; p.T = (int)T; p.Di = (int)d_inner; p.N = (int)d_state;
   p.nchunks = plan.nchunks; p.nblk = plan.fwd.nblk;
   p.seg_chunks = plan.fwd.seg_chunks; p.nseg = plan.fwd.nseg;
@@ -186,7 +188,7 @@ int mamba_scan_bwd(const float* delta, const float* u, const float* B, const flo
   float* sc = (float*)scratch;
   mscan::BwdParams p;
   p.delta = delta; p.u = u; p.B = B; p.C = C; p.gate = gate; p.A_log = A_log; p.D = D;
-  p.dy = dy; p.ckpt = (const float*)ckpt;
+  p.dy = dy; p.ckpt = (const float*)ckpt; p.y_ck = (const float*)ckpt + plan.off_y;
   p.d_delta = d_delta; p.d_u = d_u; p.d_gate = d_gate;
   p.partB = sc + plan.off_partB; p.partC = sc + plan.off_partC;
   p.partA = sc + plan.off_partA; p.partD = sc + plan.off_partD;

@@ -5,12 +5,12 @@
 // Per row (b, d), the chunks are walked from last to first (thread mapping as in the forward:
 // 2 channels x NPT states per thread, G lanes per channel group):
 //   0. gating (Phase B2), once per (t, d) of the chunk and cooperatively:
-//        d_y = dy * g * s  and  gfac = dy * s * (1 + g*(1 - s)),  s = sigmoid(g).
-//      Both overwrite the staged gate/dy tiles, so d_gate = y * gfac later.
+//        d_y = dy * g * s  (into the staged gate tile) and d_gate = dy * y * s * (1 + g*(1 - s))
+//      (stored at once), s = sigmoid(g), with the y the forward kept.
 //   1. recompute: restart from the chunk's checkpoint (zero for chunk 0) and run the forward
 //      recurrence over the chunk, kSub steps at a time, keeping those h_t in registers;
 //   2. reverse (Phase B3, in the page's order), for t = last .. first of the chunk:
-//        d_h += d_y*C;  y = sum_n C*h_t + D*u
+//        d_h += d_y*C
 //        d_delta = sum_n d_h*(A*da*h_{t-1} + u*B),  d_u = d_y*D + sum_n d_h*delta*B
 //        d_B[t,n] += d_h*delta*u,  d_C[t,n] += d_y*h_t           (over d)
 //        d_A_log += d_h*da*delta*A*h_{t-1},  d_D += d_y*u         (over b, t)
@@ -18,9 +18,9 @@
 //      The code forms r = (da*d_h)*h_{t-1}. With a2 = A*log2(e), the register constant of ex2,
 //      the A-term of d_delta is ln2 * sum_n a2*r and d_A_log = ln2 * a2 * sum_t delta*r.
 // Reductions, all in a fixed order (deterministic):
-//   * sum over n (y, the A-term, the B-term): in-thread, then a butterfly reduce-scatter over
+//   * sum over n (the A-term, the B-term): in-thread, then a butterfly reduce-scatter over
 //     the G state lanes, batched over P = G/2 steps. Each lane ends with one (step, channel),
-//     and stores d_delta, d_u and d_gate for it.
+//     and stores d_delta and d_u for it.
 //   * d_B, d_C over d: in-thread over the thread's 2 channels, then a reduce-scatter over the
 //     warp's channel lanes, then the warps summed through shared memory. That gives one partial
 //     per CTA, written to scratch [blk][b][t][n]; scan_reduce_kernel sums the partials over blk
@@ -46,29 +46,23 @@ struct BwdShape {
   // per stage: delta, u, gate, dy [kChunk][DC]; B, C [kChunk][NP]; the chunk's starting
   // checkpoint [DC][N] (N <= NP)
   static constexpr int kStageFloats = kChunk * (4 * DC + 2 * NP) + DC * NP;
-  static constexpr int kRedFloats = kWarps * kChunk * 2 * NP;
+  static constexpr int kRedFloats = kWarps * kChunk * 2 * NP;   // per-warp d_B/d_C sums
   static constexpr size_t kSmemBytes =
       ((size_t)kBwdStages * kStageFloats + kRedFloats) * sizeof(float);
-  // segment pre-pass: compact stages (delta, gate, dy [kChunk][DC]; C [kChunk][NP])
-  static constexpr int kAggStages = 4;
-  static constexpr int kAggStageFloats = kChunk * (3 * DC + NP);
-  static constexpr size_t kAggSmemBytes = (size_t)kAggStages * kAggStageFloats * sizeof(float);
 };
 
-// AGG: the segment pre-pass needs only delta, gate, dy and C.
-template <int NP, bool VEC, bool AGG = false>
+template <int NP, bool VEC>
 __device__ __forceinline__ void bwd_load_chunk(const BwdParams& p, float* st, int c, int b,
                                                int dblk0) {
   using S = BwdShape<NP>;
   constexpr int DC = S::DC, NTH = kWarps * 32;
-  // main layout: delta, u, gate, dy, B, C, checkpoint row; compact pre-pass layout: delta,
-  // gate, dy, C
+  // layout: delta, u, gate, dy [kChunk][DC]; B, C [kChunk][NP]; checkpoint row [DC][N]
   float* s_dl = st;
   float* s_u = st + kChunk * DC;
-  float* s_g = st + (AGG ? 1 : 2) * kChunk * DC;
-  float* s_dy = st + (AGG ? 2 : 3) * kChunk * DC;
+  float* s_g = st + 2 * kChunk * DC;
+  float* s_dy = st + 3 * kChunk * DC;
   float* s_B = st + 4 * kChunk * DC;
-  float* s_C = AGG ? st + 3 * kChunk * DC : s_B + kChunk * NP;
+  float* s_C = s_B + kChunk * NP;
   const int t0 = c * kChunk;
   const size_t rowb = (size_t)b * p.T;
   if constexpr (VEC) {
@@ -78,7 +72,7 @@ __device__ __forceinline__ void bwd_load_chunk(const BwdParams& p, float* st, in
       const bool v = t < p.T && d < p.Di;
       const size_t go = v ? (rowb + t) * p.Di + d : 0;
       cp_async16(s_dl + i * DC + col, p.delta + go, v);
-      if (!AGG) cp_async16(s_u + i * DC + col, p.u + go, v);
+      cp_async16(s_u + i * DC + col, p.u + go, v);
       cp_async16(s_g + i * DC + col, p.gate + go, v);
       cp_async16(s_dy + i * DC + col, p.dy + go, v);
     }
@@ -87,7 +81,7 @@ __device__ __forceinline__ void bwd_load_chunk(const BwdParams& p, float* st, in
       const int t = t0 + i;
       const bool v = t < p.T && n < p.N;
       const size_t go = v ? (rowb + t) * p.N + n : 0;
-      if (!AGG) cp_async16(s_B + i * NP + n, p.B + go, v);
+      cp_async16(s_B + i * NP + n, p.B + go, v);
       cp_async16(s_C + i * NP + n, p.C + go, v);
     }
   } else {
@@ -97,7 +91,7 @@ __device__ __forceinline__ void bwd_load_chunk(const BwdParams& p, float* st, in
       const bool v = t < p.T && d < p.Di;
       const size_t go = v ? (rowb + t) * p.Di + d : 0;
       cp_async4(s_dl + i * DC + col, p.delta + go, v);
-      if (!AGG) cp_async4(s_u + i * DC + col, p.u + go, v);
+      cp_async4(s_u + i * DC + col, p.u + go, v);
       cp_async4(s_g + i * DC + col, p.gate + go, v);
       cp_async4(s_dy + i * DC + col, p.dy + go, v);
     }
@@ -106,11 +100,11 @@ __device__ __forceinline__ void bwd_load_chunk(const BwdParams& p, float* st, in
       const int t = t0 + i;
       const bool v = t < p.T && n < p.N;
       const size_t go = v ? (rowb + t) * p.N + n : 0;
-      if (!AGG) cp_async4(s_B + i * NP + n, p.B + go, v);
+      cp_async4(s_B + i * NP + n, p.B + go, v);
       cp_async4(s_C + i * NP + n, p.C + go, v);
     }
   }
-  if constexpr (!AGG) {
+  {
     // state entering chunk c (checkpoint slot c-1); zeros for the first chunk
     float* s_h0 = s_C + kChunk * NP;
     const bool have = c > 0;
@@ -137,26 +131,42 @@ __device__ __forceinline__ void bwd_load_chunk(const BwdParams& p, float* st, in
 // prefix L = sum_t (prod_{s<=t} exp(delta_s*A)) * d_y_t * C_t[n] (products from the segment's
 // first step to t), plus the segment's sum of delta. The carry leaving a segment towards
 // earlier time is L + exp(A * sum(delta)) * (carry entering it from later time), so the main
-// kernel composes these exactly. The sum is accumulated in forward order, with the staging of
-// the main kernel.
+// kernel composes these exactly. The sum is accumulated in forward order. A CTA covers
+// kAggWarps warps of channels and agg_k consecutive segments, with the chunk pipeline
+// running straight through the segment boundaries.
+template <int NP>
+struct BwdAggShape {
+  using S = BwdShape<NP>;
+  static constexpr int AW = kAggWarps;
+  static constexpr int DC = AW * S::DW;
+  static constexpr int NTH = AW * 32;
+  static constexpr int kStages = 4;
+  static constexpr int kStageFloats = kChunk * (3 * DC + NP);   // delta, gate, dy, C
+  static constexpr size_t kSmemBytes = (size_t)kStages * kStageFloats * sizeof(float);
+};
+
 template <int NP, bool VEC>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kAggWarps * 32)
 scan_bwd_agg_kernel(const BwdParams p) {
   using S = BwdShape<NP>;
-  constexpr int G = S::G, DW = S::DW, DC = S::DC, NPT = S::NPT, NPR = S::NPR;
-  constexpr int NTH = kWarps * 32;
+  using A = BwdAggShape<NP>;
+  constexpr int G = S::G, DW = S::DW, NPT = S::NPT, NPR = S::NPR, DC = A::DC, NTH = A::NTH;
   extern __shared__ __align__(16) float smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ng = lane % G, dg = lane / G;
   const int b = blockIdx.y;
-  const int blk = blockIdx.x % p.nblk, seg = 1 + blockIdx.x / p.nblk;
+  const int nblk_a = (p.Di + DC - 1) / DC;
+  const int blk = blockIdx.x % nblk_a, grp = blockIdx.x / nblk_a;
   const int dblk0 = blk * DC;
   const int cl = warp * DW + dg * kDPT;
   const int d0 = dblk0 + cl;
   const int n0 = ng * NPT;
-  const int Di = p.Di, N = p.N;
-  const int c_begin = seg * p.seg_chunks;
-  const int c_end = min(p.nchunks, c_begin + p.seg_chunks);
+  const int Di = p.Di, N = p.N, T = p.T;
+  const int seg_lo = 1 + grp * p.agg_k;                   // segments 1 .. nseg-1 need aggregates
+  const int seg_hi = min(p.nseg, seg_lo + p.agg_k);
+  const int c_begin = seg_lo * p.seg_chunks;
+  const int c_end = min(p.nchunks, seg_hi * p.seg_chunks);
+  const size_t row0 = (size_t)b * T;
 
   float2 a2[kDPT][NPR], cum[kDPT][NPR], L[kDPT][NPR];
   float sd[kDPT] = {0.f, 0.f};
@@ -178,28 +188,28 @@ scan_bwd_agg_kernel(const BwdParams p) {
     }
   }
 
+  auto load = [&](int stage, int c) {
+    float* st = smem + stage * A::kStageFloats;
+    stage_tile<DC, NTH, VEC>(st, p.delta, row0, c * kChunk, T, Di, dblk0);
+    stage_tile<DC, NTH, VEC>(st + kChunk * DC, p.gate, row0, c * kChunk, T, Di, dblk0);
+    stage_tile<DC, NTH, VEC>(st + 2 * kChunk * DC, p.dy, row0, c * kChunk, T, Di, dblk0);
+    stage_tile<NP, NTH, VEC>(st + 3 * kChunk * DC, p.C, row0, c * kChunk, T, N, 0);
+    cp_async_commit();
+  };
 #pragma unroll
-  for (int s = 0; s < S::kAggStages - 1; ++s) {
-    if (c_begin + s < c_end)
-      bwd_load_chunk<NP, VEC, true>(p, smem + s * S::kAggStageFloats, c_begin + s, b, dblk0);
-    else
-      cp_async_commit();
+  for (int s = 0; s < A::kStages - 1; ++s) {
+    if (c_begin + s < c_end) load(s, c_begin + s);
+    else cp_async_commit();
   }
   for (int c = c_begin; c < c_end; ++c) {
     const int it = c - c_begin;
-    cp_async_wait<S::kAggStages - 2>();
+    cp_async_wait<A::kStages - 2>();
     __syncthreads();
-    {
-      const int cn = c + S::kAggStages - 1;
-      if (cn < c_end)
-        bwd_load_chunk<NP, VEC, true>(
-            p, smem + ((it + S::kAggStages - 1) % S::kAggStages) * S::kAggStageFloats, cn, b, dblk0);
-      else
-        cp_async_commit();
-    }
-    float* st = smem + (it % S::kAggStages) * S::kAggStageFloats;
+    if (c + A::kStages - 1 < c_end) load((it + A::kStages - 1) % A::kStages, c + A::kStages - 1);
+    else cp_async_commit();
+    float* st = smem + (it % A::kStages) * A::kStageFloats;
     const float* s_dl = st;
-    float* s_g = st + kChunk * DC;         // becomes d_y
+    float* s_g = st + kChunk * DC;          // becomes d_y
     const float* s_dy = st + 2 * kChunk * DC;
     const float* s_C = st + 3 * kChunk * DC;
     for (int e = threadIdx.x; e < kChunk * DC; e += NTH) {
@@ -225,22 +235,33 @@ scan_bwd_agg_kernel(const BwdParams p) {
         }
       }
     }
-  }
-  cp_async_wait<0>();
+    if ((c + 1) % p.seg_chunks == 0 || c + 1 == p.nchunks) {   // a segment ends: emit, restart
+      const int seg = c / p.seg_chunks;
 #pragma unroll
-  for (int j = 0; j < kDPT; ++j) {
-    const int d = d0 + j;
-    if (d >= Di) continue;
-    const size_t row = ((size_t)b * p.nseg + seg) * Di + d;
-    if (ng == 0) p.agg_sd[row] = sd[j];
-    if constexpr (VEC) {
-      if (n0 < N) st_pairs<NPR>(p.agg_L + row * N + n0, L[j]);   // N % 4 == 0 here
-    } else {
+      for (int j = 0; j < kDPT; ++j) {
+        const int d = d0 + j;
+        if (d < Di) {
+          const size_t row = ((size_t)b * p.nseg + seg) * Di + d;
+          if (ng == 0) p.agg_sd[row] = sd[j];
+          if constexpr (VEC) {
+            if (n0 < N) st_pairs<NPR>(p.agg_L + row * N + n0, L[j]);   // N % 4 == 0 here
+          } else {
 #pragma unroll
-      for (int k = 0; k < NPT; ++k)
-        if (n0 + k < N) p.agg_L[row * N + n0 + k] = (k & 1) ? L[j][k >> 1].y : L[j][k >> 1].x;
+            for (int k = 0; k < NPT; ++k)
+              if (n0 + k < N)
+                p.agg_L[row * N + n0 + k] = (k & 1) ? L[j][k >> 1].y : L[j][k >> 1].x;
+          }
+        }
+        sd[j] = 0.f;
+#pragma unroll
+        for (int q = 0; q < NPR; ++q) {
+          cum[j][q] = make_float2(1.f, 1.f);
+          L[j][q] = make_float2(0.f, 0.f);
+        }
+      }
     }
   }
+  cp_async_wait<0>();
 }
 
 // Forward recurrence of step i of the staged chunk on the thread's 2 x 4 states hc.
@@ -308,7 +329,7 @@ scan_bwd_kernel(const BwdParams p) {
     }
   }
 
-  using RSn = ReduceScatter<6 * P, G / 2, 1>;    // (y, A-term, B-term) x 2 channels x P steps
+  using RSn = ReduceScatter<4 * P, G / 2, 1>;    // (A-term, B-term) x 2 channels x P steps
   using RSd = ReduceScatter<2 * NPT, 16, G>;      // (d_B x NPT, d_C x NPT) over channel lanes
   const int nbase = RSn::base(lane);
   constexpr int kN = RSn::kept();
@@ -377,12 +398,21 @@ scan_bwd_kernel(const BwdParams p) {
     const float* s_C = s_B + kChunk * NP;
     const int t0 = c * kChunk;
 
-    // ---- 0. gating backward for the whole chunk tile -------------------------------------
-    for (int e = threadIdx.x; e < kChunk * DC; e += NTH) {
+    // ---- 0. gating backward (Phase B2) for the whole chunk tile: d_y into the gate tile, and
+    // d_gate = dy * y * s * (1 + g*(1 - s)) straight to global memory, with the y the forward
+    // kept (coalesced along d)
+    static_assert((kChunk * DC) % NTH == 0, "tile must split evenly over the CTA");
+#pragma unroll
+    for (int k = 0; k < kChunk * DC / NTH; ++k) {
+      const int e = k * NTH + threadIdx.x;
+      const int i = e / DC, col = e % DC;
+      const bool ok = (t0 + i < T) && (dblk0 + col < Di);
+      const size_t o = (rowb + t0 + i) * Di + dblk0 + col;
+      const float yv = ok ? __ldg(p.y_ck + o) : 0.f;
       const float g = s_g[e], go = s_dy[e];
       const float s = sigmoid_fast(g);
       s_g[e] = go * (g * s);
-      s_dy[e] = go * (s * fmaf(g, 1.f - s, 1.f));
+      st_global_if(p.d_gate + o, go * yv * (s * fmaf(g, 1.f - s, 1.f)), ok);
     }
     __syncthreads();
 
@@ -451,7 +481,7 @@ scan_bwd_kernel(const BwdParams p) {
 #pragma unroll
       for (int gq = 0; gq < kSub / P; ++gq) {
         const int gl = kSub / P - 1 - gq;          // group inside the sub-block
-        float vn[6 * P];
+        float vn[4 * P];
 #pragma unroll
         for (int tq = 0; tq < P; ++tq) {
           const int tt = P - 1 - tq;
@@ -471,12 +501,11 @@ scan_bwd_kernel(const BwdParams p) {
             const float uu = j ? uv.y : uv.x;
             const float dyj = j ? dyv.y : dyv.x;
             const float2 dl2 = splat2(dl), du2 = splat2(dl * uu), dy2 = splat2(dyj);
-            float2 ya = make_float2(0.f, 0.f), sa = ya, sb2 = ya;
+            float2 sa = make_float2(0.f, 0.f), sb2 = sa;
 #pragma unroll
             for (int pp = 0; pp < NPR; ++pp) {
               const float2 hcur = hs[q][j][pp];
               const float2 hprev = (q > 0) ? hs[q > 0 ? q - 1 : 0][j][pp] : hsub[sb][j][pp];
-              ya = fma2(Cp[pp], hcur, ya);
               const float2 da = ex2_2(mul2(dl2, a2[j][pp]));
               const float2 gh = fma2(dy2, Cp[pp], dh[j][pp]);   // d_h += d_y*C
               const float2 cr = mul2(da, gh);                    // carried to t-1
@@ -488,9 +517,8 @@ scan_bwd_kernel(const BwdParams p) {
               xc[pp] = fma2(dy2, hcur, xc[pp]);
               dh[j][pp] = cr;
             }
-            vn[(tt * 2 + j) * 3 + 0] = ya.x + ya.y;
-            vn[(tt * 2 + j) * 3 + 1] = sa.x + sa.y;
-            vn[(tt * 2 + j) * 3 + 2] = sb2.x + sb2.y;
+            vn[(tt * 2 + j) * 2 + 0] = sa.x + sa.y;
+            vn[(tt * 2 + j) * 2 + 1] = sb2.x + sb2.y;
             dD[j] = fmaf(dyj, uu, dD[j]);
           }
           // d_B / d_C of this step: sum over the warp's channels
@@ -513,21 +541,19 @@ scan_bwd_kernel(const BwdParams p) {
         // sums over n, scattered so that each lane finishes one (step, channel)
         RSn::run(vn, lane);
 #pragma unroll
-        for (int r = 0; r < kN / 3; ++r) {
-          const int qq = nbase / 3 + r;
+        for (int r = 0; r < kN / 2; ++r) {
+          const int qq = nbase / 2 + r;
           const int tt = qq >> 1, j = qq & 1;
           const int i = sb * kSub + gl * P + tt;
           const int t = t0 + i, d = d0 + j;
           const int e = i * DC + cl + j;
-          const float uu = s_u[e], dl = s_dl[e], dyj = s_g[e], gf = s_dy[e];
+          const float uu = s_u[e], dl = s_dl[e], dyj = s_g[e];
           const float Dj = j ? Dd[1] : Dd[0];
-          const float y = fmaf(Dj, uu, vn[3 * r]);
-          const float sA = vn[3 * r + 1], sB = vn[3 * r + 2];
+          const float sA = vn[2 * r], sB = vn[2 * r + 1];
           const bool ok = (t < T) && (d < Di);
           const size_t o = (rowb + t) * Di + d;
           st_global_if(p.d_delta + o, fmaf(sA, kLn2, uu * sB), ok);
           st_global_if(p.d_u + o, fmaf(dyj, Dj, dl * sB), ok);
-          st_global_if(p.d_gate + o, y * gf, ok);
         }
       }
     }
@@ -594,19 +620,24 @@ __global__ void scan_reduce_kernel(const BwdParams p) {
 }
 
 template <int NP, bool VEC>
-static int launch_np(const Plan& plan, const BwdParams& p, cudaStream_t s) {
+static int launch_np(const Plan& plan, const BwdParams& p0, cudaStream_t s) {
+  BwdParams p = p0;
   using S = BwdShape<NP>;
   if (cudaFuncSetAttribute(scan_bwd_kernel<NP, VEC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)S::kSmemBytes) != cudaSuccess)
     return -1;
   int n = 0;
   if (plan.bwd.nseg > 1) {
+    using A = BwdAggShape<NP>;
     if (cudaFuncSetAttribute(scan_bwd_agg_kernel<NP, VEC>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)S::kAggSmemBytes) != cudaSuccess)
+                             (int)A::kSmemBytes) != cudaSuccess)
       return -1;
-    dim3 ga((unsigned)(plan.bwd.nblk * (plan.bwd.nseg - 1)), (unsigned)plan.batch);
-    scan_bwd_agg_kernel<NP, VEC><<<ga, kWarps * 32, S::kAggSmemBytes, s>>>(p);
+    const int nblk_a = (int)((plan.Di + A::DC - 1) / A::DC);
+    p.agg_k = 1;   // one segment per CTA measured fastest (the kernel accepts more)
+    const int ngrp = (plan.bwd.nseg - 1 + p.agg_k - 1) / p.agg_k;
+    dim3 ga((unsigned)(nblk_a * ngrp), (unsigned)plan.batch);
+    scan_bwd_agg_kernel<NP, VEC><<<ga, A::NTH, A::kSmemBytes, s>>>(p);
     if (cudaPeekAtLastError() != cudaSuccess) return -1;
     ++n;
   }

@@ -11,6 +11,10 @@ constexpr float kLog2e = 1.4426950408889634f;  // log2(e)
 constexpr float kLn2 = 0.6931471805599453f;    // ln(2)
 constexpr unsigned kFull = 0xffffffffu;
 
+// Warps per CTA of the segment pre-pass kernels (the main kernels' CTA shape measured best;
+// wider CTAs with several segments each were slower on GB300).
+constexpr int kAggWarps = kWarps;
+
 // 2^x on the special-function unit (PTX ex2.approx.ftz.f32). In the scan x <= 0, so the result
 // lies in [0, 1]; very negative x flushes to 0.
 __device__ __forceinline__ float ex2_sfu(float x) {
@@ -116,6 +120,27 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+// Stages rows t0 .. t0+kChunk-1 of a row-major [.., T, W] tensor, columns col0 .. col0+TW-1,
+// into a [kChunk][TW] shared tile with cp.async; rows past T and columns past W become zeros.
+// VEC needs W % 4 == 0 and col0 % 4 == 0 (then every 16-byte piece is inside or outside W).
+template <int TW, int NTH, bool VEC>
+__device__ __forceinline__ void stage_tile(float* dst, const float* src, size_t row0, int t0,
+                                           int T, int W, int col0) {
+  if constexpr (VEC) {
+    for (int q = threadIdx.x; q < kChunk * TW / 4; q += NTH) {
+      const int i = q / (TW / 4), col = (q % (TW / 4)) * 4;
+      const bool v = (t0 + i < T) && (col0 + col < W);
+      cp_async16(dst + i * TW + col, v ? src + (row0 + t0 + i) * W + col0 + col : src, v);
+    }
+  } else {
+    for (int q = threadIdx.x; q < kChunk * TW; q += NTH) {
+      const int i = q / TW, col = q % TW;
+      const bool v = (t0 + i < T) && (col0 + col < W);
+      cp_async4(dst + i * TW + col, v ? src + (row0 + t0 + i) * W + col0 + col : src, v);
+    }
+  }
 }
 
 // ---- butterfly reduce-scatter across lanes -------------------------------------------------

@@ -42,13 +42,9 @@ struct FwdShape {
   static constexpr int P = G >= 2 ? G / 2 : 1;         // steps per output group
   static constexpr int kStageFloats = kChunk * (3 * DC + 2 * NP);
   static constexpr size_t kSmemBytes = (size_t)kFwdStages * kStageFloats * sizeof(float);
-  // segment pre-pass: compact stages (delta, u [kChunk][DC]; B [kChunk][NP])
-  static constexpr int kAggStageFloats = kChunk * (2 * DC + NP);
-  static constexpr size_t kAggSmemBytes = (size_t)kFwdStages * kAggStageFloats * sizeof(float);
 };
 
-// AGG: the segment pre-pass needs only delta, u and B.
-template <int NP, bool VEC, bool AGG = false>
+template <int NP, bool VEC>
 __device__ __forceinline__ void fwd_load_chunk(const FwdParams& p, float* st, int c, int b,
                                                int dblk0) {
   using S = FwdShape<NP>;
@@ -56,8 +52,7 @@ __device__ __forceinline__ void fwd_load_chunk(const FwdParams& p, float* st, in
   float* s_dl = st;
   float* s_u = st + kChunk * DC;
   float* s_g = st + 2 * kChunk * DC;
-  // main layout: delta, u, gate, B, C; compact pre-pass layout: delta, u, B
-  float* s_B = st + (AGG ? 2 : 3) * kChunk * DC;
+  float* s_B = st + 3 * kChunk * DC;
   float* s_C = s_B + kChunk * NP;
   const int t0 = c * kChunk;
   const size_t rowb = (size_t)b * p.T;
@@ -69,7 +64,7 @@ __device__ __forceinline__ void fwd_load_chunk(const FwdParams& p, float* st, in
       const size_t go = v ? (rowb + t) * p.Di + d : 0;
       cp_async16(s_dl + i * DC + col, p.delta + go, v);
       cp_async16(s_u + i * DC + col, p.u + go, v);
-      if (!AGG) cp_async16(s_g + i * DC + col, p.gate + go, v);
+      cp_async16(s_g + i * DC + col, p.gate + go, v);
     }
     for (int q = threadIdx.x; q < kChunk * NP / 4; q += NTH) {
       const int i = q / (NP / 4), n = (q % (NP / 4)) * 4;
@@ -77,7 +72,7 @@ __device__ __forceinline__ void fwd_load_chunk(const FwdParams& p, float* st, in
       const bool v = t < p.T && n < p.N;
       const size_t go = v ? (rowb + t) * p.N + n : 0;
       cp_async16(s_B + i * NP + n, p.B + go, v);
-      if (!AGG) cp_async16(s_C + i * NP + n, p.C + go, v);
+      cp_async16(s_C + i * NP + n, p.C + go, v);
     }
   } else {
     for (int q = threadIdx.x; q < kChunk * DC; q += NTH) {
@@ -87,7 +82,7 @@ __device__ __forceinline__ void fwd_load_chunk(const FwdParams& p, float* st, in
       const size_t go = v ? (rowb + t) * p.Di + d : 0;
       cp_async4(s_dl + i * DC + col, p.delta + go, v);
       cp_async4(s_u + i * DC + col, p.u + go, v);
-      if (!AGG) cp_async4(s_g + i * DC + col, p.gate + go, v);
+      cp_async4(s_g + i * DC + col, p.gate + go, v);
     }
     for (int q = threadIdx.x; q < kChunk * NP; q += NTH) {
       const int i = q / NP, n = q % NP;
@@ -95,7 +90,7 @@ __device__ __forceinline__ void fwd_load_chunk(const FwdParams& p, float* st, in
       const bool v = t < p.T && n < p.N;
       const size_t go = v ? (rowb + t) * p.N + n : 0;
       cp_async4(s_B + i * NP + n, p.B + go, v);
-      if (!AGG) cp_async4(s_C + i * NP + n, p.C + go, v);
+      cp_async4(s_C + i * NP + n, p.C + go, v);
     }
   }
   cp_async_commit();
@@ -104,24 +99,42 @@ __device__ __forceinline__ void fwd_load_chunk(const FwdParams& p, float* st, in
 // Segment pre-pass of the forward: for every segment but the last, run the recurrence from a
 // zero state and keep the end state and the sum of delta over the segment, per (b, d, n).
 // Since h_end = exp(A * sum(delta)) * h_start + h_end(from zero), the main kernel composes these
-// to obtain the exact state entering each segment. Staging is the same as the main kernel's.
+// to obtain the exact state entering each segment. A CTA covers kAggWarps warps of
+// channels and agg_k consecutive segments, with the chunk pipeline running straight through the
+// segment boundaries.
+template <int NP>
+struct FwdAggShape {
+  using S = FwdShape<NP>;
+  static constexpr int AW = kAggWarps;
+  static constexpr int DC = AW * S::DW;
+  static constexpr int NTH = AW * 32;
+  static constexpr int kStages = 4;
+  static constexpr int kStageFloats = kChunk * (2 * DC + NP);   // delta, u, B
+  static constexpr size_t kSmemBytes = (size_t)kStages * kStageFloats * sizeof(float);
+};
+
 template <int NP, bool VEC>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kAggWarps * 32)
 scan_fwd_agg_kernel(const FwdParams p) {
   using S = FwdShape<NP>;
-  constexpr int G = S::G, DW = S::DW, DC = S::DC, NPT = S::NPT, NPR = S::NPR;
+  using A = FwdAggShape<NP>;
+  constexpr int G = S::G, DW = S::DW, NPT = S::NPT, NPR = S::NPR, DC = A::DC, NTH = A::NTH;
   extern __shared__ __align__(16) float smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ng = lane % G, dg = lane / G;
   const int b = blockIdx.y;
-  const int blk = blockIdx.x % p.nblk, seg = blockIdx.x / p.nblk;
+  const int nblk_a = (p.Di + DC - 1) / DC;
+  const int blk = blockIdx.x % nblk_a, grp = blockIdx.x / nblk_a;
   const int dblk0 = blk * DC;
   const int cl = warp * DW + dg * kDPT;
   const int d0 = dblk0 + cl;
   const int n0 = ng * NPT;
-  const int Di = p.Di, N = p.N;
-  const int c_begin = seg * p.seg_chunks;
-  const int c_end = min(p.nchunks, c_begin + p.seg_chunks);
+  const int Di = p.Di, N = p.N, T = p.T;
+  const int seg_lo = grp * p.agg_k;                       // segments 0 .. nseg-2 need aggregates
+  const int seg_hi = min(p.nseg - 1, seg_lo + p.agg_k);
+  const int c_begin = seg_lo * p.seg_chunks;
+  const int c_end = min(p.nchunks, seg_hi * p.seg_chunks);
+  const size_t row0 = (size_t)b * T;
 
   float2 a2[kDPT][NPR], h[kDPT][NPR];
   float sd[kDPT] = {0.f, 0.f};
@@ -142,26 +155,25 @@ scan_fwd_agg_kernel(const FwdParams p) {
     }
   }
 
+  auto load = [&](int stage, int c) {
+    float* st = smem + stage * A::kStageFloats;
+    stage_tile<DC, NTH, VEC>(st, p.delta, row0, c * kChunk, T, Di, dblk0);
+    stage_tile<DC, NTH, VEC>(st + kChunk * DC, p.u, row0, c * kChunk, T, Di, dblk0);
+    stage_tile<NP, NTH, VEC>(st + 2 * kChunk * DC, p.B, row0, c * kChunk, T, N, 0);
+    cp_async_commit();
+  };
 #pragma unroll
-  for (int s = 0; s < kFwdStages - 1; ++s) {
-    if (c_begin + s < c_end)
-      fwd_load_chunk<NP, VEC, true>(p, smem + s * S::kAggStageFloats, c_begin + s, b, dblk0);
-    else
-      cp_async_commit();
+  for (int s = 0; s < A::kStages - 1; ++s) {
+    if (c_begin + s < c_end) load(s, c_begin + s);
+    else cp_async_commit();
   }
   for (int c = c_begin; c < c_end; ++c) {
     const int it = c - c_begin;
-    cp_async_wait<kFwdStages - 2>();
+    cp_async_wait<A::kStages - 2>();
     __syncthreads();
-    {
-      const int cn = c + kFwdStages - 1;
-      if (cn < c_end)
-        fwd_load_chunk<NP, VEC, true>(
-            p, smem + ((it + kFwdStages - 1) % kFwdStages) * S::kAggStageFloats, cn, b, dblk0);
-      else
-        cp_async_commit();
-    }
-    const float* st = smem + (it % kFwdStages) * S::kAggStageFloats;
+    if (c + A::kStages - 1 < c_end) load((it + A::kStages - 1) % A::kStages, c + A::kStages - 1);
+    else cp_async_commit();
+    const float* st = smem + (it % A::kStages) * A::kStageFloats;
     const float* s_dl = st;
     const float* s_u = st + kChunk * DC;
     const float* s_B = st + 2 * kChunk * DC;
@@ -184,22 +196,30 @@ scan_fwd_agg_kernel(const FwdParams p) {
         }
       }
     }
-  }
-  cp_async_wait<0>();
+    if ((c + 1) % p.seg_chunks == 0) {   // the last chunk of a segment: emit, then restart
+      const int seg = c / p.seg_chunks;
 #pragma unroll
-  for (int j = 0; j < kDPT; ++j) {
-    const int d = d0 + j;
-    if (d >= Di) continue;
-    const size_t row = ((size_t)b * p.nseg + seg) * Di + d;
-    if (ng == 0) p.agg_sd[row] = sd[j];
-    if constexpr (VEC) {
-      if (n0 < N) st_pairs<NPR>(p.agg_h + row * N + n0, h[j]);   // N % 4 == 0 here
-    } else {
+      for (int j = 0; j < kDPT; ++j) {
+        const int d = d0 + j;
+        if (d < Di) {
+          const size_t row = ((size_t)b * p.nseg + seg) * Di + d;
+          if (ng == 0) p.agg_sd[row] = sd[j];
+          if constexpr (VEC) {
+            if (n0 < N) st_pairs<NPR>(p.agg_h + row * N + n0, h[j]);   // N % 4 == 0 here
+          } else {
 #pragma unroll
-      for (int k = 0; k < NPT; ++k)
-        if (n0 + k < N) p.agg_h[row * N + n0 + k] = (k & 1) ? h[j][k >> 1].y : h[j][k >> 1].x;
+            for (int k = 0; k < NPT; ++k)
+              if (n0 + k < N)
+                p.agg_h[row * N + n0 + k] = (k & 1) ? h[j][k >> 1].y : h[j][k >> 1].x;
+          }
+        }
+        sd[j] = 0.f;
+#pragma unroll
+        for (int q = 0; q < NPR; ++q) h[j][q] = make_float2(0.f, 0.f);
+      }
     }
   }
+  cp_async_wait<0>();
 }
 
 template <int NP, bool VEC, bool WITH_Y>
@@ -344,6 +364,7 @@ scan_fwd_kernel(const FwdParams p) {
         const bool ok = (t < T) && (d < Di);
         const size_t o = (rowb + t) * Di + d;
         st_global_if(p.out + o, y * (g * sigmoid_fast(g)), ok);
+        st_global_if(p.y_ck + o, y, ok);            // kept for the backward's d_gate
         if constexpr (WITH_Y) st_global_if(p.y + o, y, ok);
       }
     }
@@ -368,7 +389,8 @@ scan_fwd_kernel(const FwdParams p) {
 }
 
 template <int NP, bool VEC, bool WITH_Y>
-static int launch_np(const Plan& plan, const FwdParams& p, cudaStream_t s) {
+static int launch_np(const Plan& plan, const FwdParams& p0, cudaStream_t s) {
+  FwdParams p = p0;
   using S = FwdShape<NP>;
   auto kern = scan_fwd_kernel<NP, VEC, WITH_Y>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -376,12 +398,16 @@ static int launch_np(const Plan& plan, const FwdParams& p, cudaStream_t s) {
     return -1;
   int n = 0;
   if (plan.fwd.nseg > 1) {
+    using A = FwdAggShape<NP>;
     if (cudaFuncSetAttribute(scan_fwd_agg_kernel<NP, VEC>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)S::kAggSmemBytes) != cudaSuccess)
+                             (int)A::kSmemBytes) != cudaSuccess)
       return -1;
-    dim3 ga((unsigned)(plan.fwd.nblk * (plan.fwd.nseg - 1)), (unsigned)plan.batch);
-    scan_fwd_agg_kernel<NP, VEC><<<ga, kWarps * 32, S::kAggSmemBytes, s>>>(p);
+    const int nblk_a = (int)((plan.Di + A::DC - 1) / A::DC);
+    p.agg_k = 1;   // one segment per CTA measured fastest (the kernel accepts more)
+    const int ngrp = (plan.fwd.nseg - 1 + p.agg_k - 1) / p.agg_k;
+    dim3 ga((unsigned)(nblk_a * ngrp), (unsigned)plan.batch);
+    scan_fwd_agg_kernel<NP, VEC><<<ga, A::NTH, A::kSmemBytes, s>>>(p);
     if (cudaPeekAtLastError() != cudaSuccess) return -1;
     ++n;
   }

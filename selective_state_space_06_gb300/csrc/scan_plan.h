@@ -51,7 +51,8 @@ struct Plan {
   //   [batch][nchunks-1][Di][N] chunk-boundary states, then the forward aggregates
   //   [batch][fwd.nseg][Di][N] segment end states (from zero) and [batch][fwd.nseg][Di] sums
   //   of delta
-  size_t off_fagg_h = 0, off_fagg_sd = 0, ckpt_elems = 0;
+  //   and y [batch][T][Di], which the backward needs for d_gate
+  size_t off_fagg_h = 0, off_fagg_sd = 0, off_y = 0, ckpt_elems = 0;
   // scratch layout (float offsets, each region 256-byte aligned)
   size_t off_partB = 0, off_partC = 0, off_partA = 0, off_partD = 0;
   size_t off_bagg_L = 0, off_bagg_sd = 0, scratch_elems = 0;
@@ -65,17 +66,21 @@ struct FwdParams {
   const float* A_log; const float* D;
   float* out; float* y; float* ckpt;
   float* agg_h; float* agg_sd;   // forward segment aggregates (inside the ckpt buffer)
+  float* y_ck;                   // y = sum_n C*h + D*u for the backward (inside the ckpt buffer)
   int batch, T, Di, N, nchunks, nblk, seg_chunks, nseg;
+  int agg_k;                     // pre-pass: consecutive segments per CTA
 };
 
 struct BwdParams {
   const float* delta; const float* u; const float* B; const float* C; const float* gate;
   const float* A_log; const float* D; const float* dy; const float* ckpt;
+  const float* y_ck;   // y saved by the forward (inside the ckpt buffer)
   float* d_delta; float* d_u; float* d_gate;
   float* partB; float* partC; float* partA; float* partD;   // scratch
   float* agg_L; float* agg_sd;                               // scratch: backward aggregates
   float* d_B; float* d_C; float* d_A_log; float* d_D;
   int batch, T, Di, N, nchunks, nblk, seg_chunks, nseg;
+  int agg_k;  // pre-pass: consecutive segments per CTA
 };
 
 // Each returns the number of kernels enqueued (>= 1) or -1 on a launch error.

@@ -45,13 +45,14 @@ def test_library_exports_every_declared_symbol(ms):
 
 
 def test_buffer_sizes(ms):
-    # checkpoints: the state after every 16-step chunk except the last ([b][chunk][d][n] fp32),
-    # plus the forward's per-segment aggregates (end state and sum of delta)
+    # checkpoint buffer: the state after every 16-step chunk except the last ([b][chunk][d][n]
+    # fp32), the forward's per-segment aggregates, and y [b][T][d] for the backward's d_gate
     states = 8 * (1024 // 16 - 1) * 1536 * 16 * 4
+    y = 8 * 1024 * 1536 * 4
     ck = ms.mamba_scan_ckpt_bytes(8, 1024, 1536, 16)
-    assert states <= ck <= 2 * states and ck % 256 == 0
-    assert ms.mamba_scan_ckpt_bytes(1, 16, 32, 16) == 0        # one chunk, one segment
-    assert ms.mamba_scan_ckpt_bytes(1, 17, 32, 16) >= 1 * 1 * 32 * 16 * 4
+    assert states + y <= ck <= 2 * (states + y) and ck % 256 == 0
+    assert ms.mamba_scan_ckpt_bytes(1, 16, 32, 16) == 16 * 32 * 4     # one chunk: y only
+    assert ms.mamba_scan_ckpt_bytes(1, 17, 32, 16) >= 1 * 1 * 32 * 16 * 4 + 17 * 32 * 4
     assert ms.mamba_scan_ckpt_bytes(0, 16, 32, 16) == 0
     sc = ms.mamba_scan_scratch_bytes(2, 100, 130, 16)
     nblk = -(-130 // 64)

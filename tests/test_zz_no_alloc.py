@@ -77,7 +77,7 @@ def test_noalloc_rejects_sizes_beyond_the_static_scratch():
     import __graft_entry__
     __graft_entry__.build()
     import selective_state_space_06_gb300 as ms
-    b, T, Di, N = 8, 2048, 2048, 16
+    b, T, Di, N = 1, 65536, 2560, 64          # the long-sequence workload
     assert ms.mamba_scan_scratch_bytes(b, T, Di, N) > ms.MAMBA_SCAN_NOALLOC_SCRATCH_BYTES
     lib = ms.raw_library()
     big = 1 << 32
