@@ -31,7 +31,7 @@
 
 namespace mscan {
 
-constexpr int kBwdStages = 3;
+constexpr int kBwdStages = 2;
 
 template <int NP>
 struct BwdShape {
@@ -44,8 +44,8 @@ struct BwdShape {
   static constexpr int DC = kWarps * DW;
   static constexpr int P = G >= 2 ? G / 2 : 1;
   // per stage: delta, u, gate, dy [kChunk][DC]; B, C [kChunk][NP]; the chunk's starting
-  // checkpoint [DC][N] (N <= NP)
-  static constexpr int kStageFloats = kChunk * (4 * DC + 2 * NP) + DC * NP;
+  // checkpoint [DC][N] (N <= NP); the forward's y [kChunk][DC]
+  static constexpr int kStageFloats = kChunk * (5 * DC + 2 * NP) + DC * NP;
   static constexpr int kRedFloats = kWarps * kChunk * 2 * NP;   // per-warp d_B/d_C sums
   static constexpr size_t kSmemBytes =
       ((size_t)kBwdStages * kStageFloats + kRedFloats) * sizeof(float);
@@ -104,6 +104,8 @@ __device__ __forceinline__ void bwd_load_chunk(const BwdParams& p, float* st, in
       cp_async4(s_C + i * NP + n, p.C + go, v);
     }
   }
+  stage_tile<DC, NTH, VEC>(s_C + kChunk * NP + DC * NP, p.y_ck, (size_t)b * p.T, t0, p.T, p.Di,
+                           dblk0);
   {
     // state entering chunk c (checkpoint slot c-1); zeros for the first chunk
     float* s_h0 = s_C + kChunk * NP;
@@ -396,6 +398,7 @@ scan_bwd_kernel(const BwdParams p) {
     float* s_dy = st + 3 * kChunk * DC;   // becomes gfac
     const float* s_B = st + 4 * kChunk * DC;
     const float* s_C = s_B + kChunk * NP;
+    const float* s_y = s_C + kChunk * NP + DC * NP;
     const int t0 = c * kChunk;
 
     // ---- 0. gating backward (Phase B2) for the whole chunk tile: d_y into the gate tile, and
@@ -408,7 +411,7 @@ scan_bwd_kernel(const BwdParams p) {
       const int i = e / DC, col = e % DC;
       const bool ok = (t0 + i < T) && (dblk0 + col < Di);
       const size_t o = (rowb + t0 + i) * Di + dblk0 + col;
-      const float yv = ok ? __ldg(p.y_ck + o) : 0.f;
+      const float yv = s_y[e];
       const float g = s_g[e], go = s_dy[e];
       const float s = sigmoid_fast(g);
       s_g[e] = go * (g * s);
