@@ -132,10 +132,11 @@ __device__ __forceinline__ void bwd_load_chunk(const BwdParams& p, float* st, in
 // Phase B3 from a zero carry at the segment's end back to its start. That gives the local
 // prefix L = sum_t (prod_{s<=t} exp(delta_s*A)) * d_y_t * C_t[n] (products from the segment's
 // first step to t), plus the segment's sum of delta. The carry leaving a segment towards
-// earlier time is L + exp(A * sum(delta)) * (carry entering it from later time), so the main
-// kernel composes these exactly. The sum is accumulated in forward order. A CTA covers
-// kAggWarps warps of channels and agg_k consecutive segments, with the chunk pipeline
-// running straight through the segment boundaries.
+// earlier time is L + exp(A * sum(delta)) * (carry entering it from later time), so the
+// segments compose exactly (scan_bwd_compose_kernel). The sum is accumulated in forward order,
+// and the product is taken as exp(A * running sum of delta), which leaves no serial multiply
+// chain. A CTA covers kAggWarps warps of channels and one sub-segment (a segment may be split
+// into nsub sub-segments, which compose the same way, to give the pre-pass more CTAs).
 template <int NP>
 struct BwdAggShape {
   using S = BwdShape<NP>;
@@ -164,13 +165,14 @@ scan_bwd_agg_kernel(const BwdParams p) {
   const int d0 = dblk0 + cl;
   const int n0 = ng * NPT;
   const int Di = p.Di, N = p.N, T = p.T;
-  const int seg_lo = 1 + grp * p.agg_k;                   // segments 1 .. nseg-1 need aggregates
-  const int seg_hi = min(p.nseg, seg_lo + p.agg_k);
-  const int c_begin = seg_lo * p.seg_chunks;
-  const int c_end = min(p.nchunks, seg_hi * p.seg_chunks);
+  // segments 1 .. nseg-1 need aggregates; sub-segment j of segment sg (may be empty)
+  const int sg = 1 + grp / p.nsub, j_sub = grp % p.nsub;
+  const int slot = sg * p.nsub + j_sub;
+  const int c_begin = sg * p.seg_chunks + j_sub * p.sub_chunks;
+  const int c_end = min(min(p.nchunks, (sg + 1) * p.seg_chunks), c_begin + p.sub_chunks);
   const size_t row0 = (size_t)b * T;
 
-  float2 a2[kDPT][NPR], cum[kDPT][NPR], L[kDPT][NPR];
+  float2 a2[kDPT][NPR], L[kDPT][NPR];
   float sd[kDPT] = {0.f, 0.f};
 #pragma unroll
   for (int j = 0; j < kDPT; ++j) {
@@ -185,7 +187,6 @@ scan_bwd_agg_kernel(const BwdParams p) {
 #pragma unroll
     for (int q = 0; q < NPR; ++q) {
       a2[j][q] = make_float2(t4[2 * q], t4[2 * q + 1]);
-      cum[j][q] = make_float2(1.f, 1.f);
       L[j][q] = make_float2(0.f, 0.f);
     }
   }
@@ -227,43 +228,70 @@ scan_bwd_agg_kernel(const BwdParams p) {
       lds_pairs<NPR>(s_C + i * NP + n0, Cp);
 #pragma unroll
       for (int j = 0; j < kDPT; ++j) {
-        const float dl = j ? dlv.y : dlv.x;
-        sd[j] += dl;
-        const float2 dl2 = splat2(dl), dy2 = splat2(j ? dyv.y : dyv.x);
+        sd[j] += j ? dlv.y : dlv.x;
+        const float2 sd2 = splat2(sd[j]), dy2 = splat2(j ? dyv.y : dyv.x);
 #pragma unroll
         for (int q = 0; q < NPR; ++q) {
-          cum[j][q] = mul2(cum[j][q], ex2_2(mul2(dl2, a2[j][q])));
-          L[j][q] = fma2(cum[j][q], mul2(dy2, Cp[q]), L[j][q]);
-        }
-      }
-    }
-    if ((c + 1) % p.seg_chunks == 0 || c + 1 == p.nchunks) {   // a segment ends: emit, restart
-      const int seg = c / p.seg_chunks;
-#pragma unroll
-      for (int j = 0; j < kDPT; ++j) {
-        const int d = d0 + j;
-        if (d < Di) {
-          const size_t row = ((size_t)b * p.nseg + seg) * Di + d;
-          if (ng == 0) p.agg_sd[row] = sd[j];
-          if constexpr (VEC) {
-            if (n0 < N) st_pairs<NPR>(p.agg_L + row * N + n0, L[j]);   // N % 4 == 0 here
-          } else {
-#pragma unroll
-            for (int k = 0; k < NPT; ++k)
-              if (n0 + k < N)
-                p.agg_L[row * N + n0 + k] = (k & 1) ? L[j][k >> 1].y : L[j][k >> 1].x;
-          }
-        }
-        sd[j] = 0.f;
-#pragma unroll
-        for (int q = 0; q < NPR; ++q) {
-          cum[j][q] = make_float2(1.f, 1.f);
-          L[j][q] = make_float2(0.f, 0.f);
+          // prod_{s<=t} exp(delta_s*A) = exp(A * sum_{s<=t} delta_s): no serial product chain
+          const float2 cum = ex2_2(mul2(sd2, a2[j][q]));
+          L[j][q] = fma2(cum, mul2(dy2, Cp[q]), L[j][q]);
         }
       }
     }
   }
   cp_async_wait<0>();
+  // emit the sub-segment's aggregate (zeros for an empty one)
+#pragma unroll
+  for (int j = 0; j < kDPT; ++j) {
+    const int d = d0 + j;
+    if (d < Di) {
+      const size_t row = ((size_t)b * p.nseg * p.nsub + slot) * Di + d;
+      if (ng == 0) p.agg_sd[row] = sd[j];
+      if constexpr (VEC) {
+        if (n0 < N) st_pairs<NPR>(p.agg_L + row * N + n0, L[j]);   // N % 4 == 0 here
+      } else {
+#pragma unroll
+        for (int k = 0; k < NPT; ++k)
+          if (n0 + k < N) p.agg_L[row * N + n0 + k] = (k & 1) ? L[j][k >> 1].y : L[j][k >> 1].x;
+      }
+    }
+  }
+}
+
+// Composition of the backward segment aggregates, in place: for every (b, d, n), walking the
+// sub-segments from last to first, carry <- L + exp(A * sum_delta) * carry. The carry entering
+// segment s from later time (zero for the last) replaces the aggregate in the first sub-slot
+// of s; slot 0 receives the carry entering segment 0.
+__global__ void scan_bwd_compose_kernel(const BwdParams p) {
+  const size_t dn = (size_t)p.Di * p.N;
+  const size_t total = (size_t)p.batch * dn;
+  const int nslot = p.nseg * p.nsub;
+  for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < total;
+       e += (size_t)gridDim.x * blockDim.x) {
+    const size_t b = e / dn, q = e % dn;
+    const size_t d = q / p.N;
+    const float a2 = -expf(p.A_log[q]) * kLog2e;
+    float carry = 0.f;
+    for (int sg = p.nseg - 1; sg >= 1; --sg) {
+      const float carry_in = carry;
+      // four sub-slots at a time: their loads do not depend on the carry, so they are all in
+      // flight together (a missing slot reads as L = 0, sum 0: the identity)
+      for (int j0 = p.nsub - 1; j0 >= 0; j0 -= 4) {
+        float Lv[4], sv[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int j = j0 - k;
+          const size_t row = b * nslot + (size_t)sg * p.nsub + (j >= 0 ? j : 0);
+          Lv[k] = j >= 0 ? p.agg_L[row * dn + q] : 0.f;
+          sv[k] = j >= 0 ? p.agg_sd[row * p.Di + d] : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) carry = fmaf(ex2_sfu(sv[k] * a2), carry, Lv[k]);
+      }
+      p.agg_L[(b * nslot + (size_t)sg * p.nsub) * dn + q] = carry_in;
+    }
+    p.agg_L[(b * nslot) * dn + q] = carry;
+  }
 }
 
 // Forward recurrence of step i of the staged chunk on the thread's 2 x 4 states hc.
@@ -637,8 +665,7 @@ static int launch_np(const Plan& plan, const BwdParams& p0, cudaStream_t s) {
                              (int)A::kSmemBytes) != cudaSuccess)
       return -1;
     const int nblk_a = (int)((plan.Di + A::DC - 1) / A::DC);
-    p.agg_k = 1;   // one segment per CTA measured fastest (the kernel accepts more)
-    const int ngrp = (plan.bwd.nseg - 1 + p.agg_k - 1) / p.agg_k;
+    const int ngrp = (plan.bwd.nseg - 1) * plan.bwd.nsub;
     dim3 ga((unsigned)(nblk_a * ngrp), (unsigned)plan.batch);
     scan_bwd_agg_kernel<NP, VEC><<<ga, A::NTH, A::kSmemBytes, s>>>(p);
     if (cudaPeekAtLastError() != cudaSuccess) return -1;
@@ -647,6 +674,24 @@ static int launch_np(const Plan& plan, const BwdParams& p0, cudaStream_t s) {
   dim3 grid((unsigned)(plan.bwd.nblk * plan.bwd.nseg), (unsigned)plan.batch);
   scan_bwd_kernel<NP, VEC><<<grid, kWarps * 32, S::kSmemBytes, s>>>(p);
   return cudaPeekAtLastError() == cudaSuccess ? n + 1 : -1;
+}
+
+// d_state > 8: the pre-pass of scan_bwd_tmem.cu, the composition of its aggregates, then the
+// tensor-memory main kernel.
+template <int NP>
+static int launch_agg_tmem(const Plan& plan, const BwdParams& p, cudaStream_t s) {
+  int na = launch_bwd_agg_tmem(plan, p, s);
+  if (na < 0) return -1;
+  if (plan.bwd.nseg > 1) {
+    int sms = 152, dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    scan_bwd_compose_kernel<<<sms * 4, 256, 0, s>>>(p);
+    if (cudaPeekAtLastError() != cudaSuccess) return -1;
+    ++na;
+  }
+  const int nm = launch_bwd_main_tmem(plan, p, s);
+  return nm < 0 ? -1 : na + nm;
 }
 
 template <int NP>
@@ -660,9 +705,9 @@ int launch_bwd(const Plan& plan, const BwdParams& p, cudaStream_t s) {
   switch (plan.NP) {
     case 4: n = launch_vec<4>(plan, p, s); break;
     case 8: n = launch_vec<8>(plan, p, s); break;
-    case 16: n = launch_vec<16>(plan, p, s); break;
-    case 32: n = launch_vec<32>(plan, p, s); break;
-    case 64: n = launch_vec<64>(plan, p, s); break;
+    case 16: n = launch_agg_tmem<16>(plan, p, s); break;
+    case 32: n = launch_agg_tmem<32>(plan, p, s); break;
+    case 64: n = launch_agg_tmem<64>(plan, p, s); break;
     default: return -1;
   }
   if (n < 0) return -1;

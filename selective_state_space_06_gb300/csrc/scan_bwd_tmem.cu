@@ -1,0 +1,642 @@
+// Backward selective scan for d_state 16, 32 and 64 (sm_103a), with the per-chunk states kept
+// in tensor memory. It computes the same Phases B2 (gating) and B3 (reverse-time BPTT) of
+// mamba-rs src/mamba_ssm/cpu/backward.rs as scan_bwd_kernel, with the same outputs and
+// partials; only the work layout differs.
+//
+// Mapping. A thread owns 4 channels x 4 states. The channels are packed as two float2 pairs
+// (so the per-channel scalars delta, u, d_y come straight from shared memory as pairs) and the
+// per-state scalars B, C are staged duplicated ({B, B}) for the packed multiplies.
+//   lane = dg * G + ng, G = d_state_padded / 4 state lanes, LD = 32 / G channel lanes
+//   ng picks the states 4*ng .. 4*ng+3, dg picks the channels 4*dg .. 4*dg+3 of the warp.
+//
+// Chunk walk (chunks of 16 steps, last to first):
+//   0. gating: d_y into the gate tile, d_gate to global memory (as in scan_bwd_kernel), and
+//      the duplicated B / C tiles for the packed multiplies;
+//   1. forward recompute of the chunk from its checkpoint. The state before every step goes
+//      to tensor memory: 16 steps x 16 floats = 256 columns per thread lane;
+//   2. reverse walk: the state before the step comes back from tensor memory; the state after
+//      it is the one read for the later step. No step is recomputed twice.
+//
+// Reductions without select instructions where possible. A butterfly level that halves the
+// values a lane keeps normally needs two selects per exchanged value (which half to keep,
+// which to send). Here each lane stores its channels and states in a lane-dependent order,
+// chosen so that at those levels every lane keeps its first half and sends its second:
+//   * over states (d_delta, d_u): the lane with bit G/2 set holds its two channel pairs
+//     swapped, so the first level keeps the first pair; the second level (inside a pair) uses
+//     selects; further levels are plain all-reduce steps;
+//   * over channels (d_B, d_C): the lane with bit 16 set holds its two state pairs swapped, and
+//     the lane with bit 8 set (when it takes part) holds the states of each pair swapped (it
+//     reads B, C from a pair-swapped copy); the last level (B or C) uses selects.
+#include "scan_common.cuh"
+
+namespace mscan {
+
+constexpr int kTmemStages = 2;   // cp.async pipeline depth
+
+template <int NP>
+struct BwdTmemShape {
+  static constexpr int DPT = 4, NPT = 4;
+  static constexpr int G = NP / NPT;                     // state lanes: 4, 8, 16
+  static constexpr int LG = G == 4 ? 2 : G == 8 ? 3 : 4;
+  static constexpr int LD = 32 / G;                      // channel lanes: 8, 4, 2
+  static constexpr int DW = LD * DPT;                    // channels per warp
+  static constexpr int DC = kWarps * DW;                 // channels per CTA: 128, 64, 32
+  static constexpr bool SWAP = LD >= 4;                  // channel reduction splits inside pairs
+  static constexpr bool KIND = LD >= 8;                  // ... and on B / C
+  static constexpr int TILE = kChunk * DC;
+  // per stage: delta, u, gate (-> d_y), dy, y [kChunk][DC]; B, C [kChunk][NP]; the chunk's
+  // starting checkpoint [DC][N]
+  static constexpr int kStageFloats = 5 * TILE + 2 * kChunk * NP + DC * NP;
+  // duplicated B, C [kChunk][NP][2] (and their pair-swapped copies)
+  static constexpr int kDupFloats = kChunk * NP * 2 * (SWAP ? 4 : 2);
+  // per-warp d_B / d_C sums of the chunk [kWarps][kChunk][2][NP]; they fit in the dy and y
+  // tiles of the current stage (dead after the gating step) when d_state is 16
+  static constexpr int kRedFloats = kWarps * kChunk * 2 * NP;
+  static constexpr bool RED_ALIAS = kRedFloats <= 2 * TILE;
+  static constexpr size_t kSmemBytes =
+      ((size_t)kTmemStages * kStageFloats + kDupFloats + (RED_ALIAS ? 0 : kRedFloats)) *
+      sizeof(float);
+  static constexpr uint32_t kTmemCols = kChunk * DPT * NPT;   // 256
+  // tensor memory holds 512 columns per SM: at most two CTAs may be resident
+  static_assert(3 * (kSmemBytes + 1024) > 228 * 1024, "shared memory must cap CTAs per SM at 2");
+};
+
+template <int NP, bool VEC>
+__device__ __forceinline__ void bwd_tmem_load_chunk(const BwdParams& p, float* st, int c, int b,
+                                                    int dblk0) {
+  using S = BwdTmemShape<NP>;
+  constexpr int DC = S::DC, NTH = kWarps * 32, TILE = S::TILE;
+  const size_t row0 = (size_t)b * p.T;
+  const int t0 = c * kChunk;
+  stage_tile<DC, NTH, VEC>(st, p.delta, row0, t0, p.T, p.Di, dblk0);
+  stage_tile<DC, NTH, VEC>(st + TILE, p.u, row0, t0, p.T, p.Di, dblk0);
+  stage_tile<DC, NTH, VEC>(st + 2 * TILE, p.gate, row0, t0, p.T, p.Di, dblk0);
+  stage_tile<DC, NTH, VEC>(st + 3 * TILE, p.dy, row0, t0, p.T, p.Di, dblk0);
+  stage_tile<DC, NTH, VEC>(st + 4 * TILE, p.y_ck, row0, t0, p.T, p.Di, dblk0);
+  stage_tile<NP, NTH, VEC>(st + 5 * TILE, p.B, row0, t0, p.T, p.N, 0);
+  stage_tile<NP, NTH, VEC>(st + 5 * TILE + kChunk * NP, p.C, row0, t0, p.T, p.N, 0);
+  {
+    // state entering chunk c (checkpoint slot c-1); zeros for the first chunk
+    float* s_h0 = st + 5 * TILE + 2 * kChunk * NP;
+    const bool have = c > 0;
+    const float* src =
+        have ? p.ckpt + (((size_t)b * (p.nchunks - 1) + (c - 1)) * p.Di + dblk0) * p.N : p.ckpt;
+    const int rowlen = DC * p.N;
+    if constexpr (VEC) {
+      for (int q = threadIdx.x * 4; q < rowlen; q += NTH * 4) {
+        const bool v = have && (dblk0 + q / p.N < p.Di);
+        cp_async16(s_h0 + q, v ? src + q : p.delta, v);
+      }
+    } else {
+      for (int q = threadIdx.x; q < rowlen; q += NTH) {
+        const bool v = have && (dblk0 + q / p.N < p.Di);
+        cp_async4(s_h0 + q, v ? src + q : p.delta, v);
+      }
+    }
+  }
+  cp_async_commit();
+}
+
+template <int NP, bool VEC>
+__global__ void __launch_bounds__(kWarps * 32, 2)
+scan_bwd_tmem_kernel(const BwdParams p) {
+  using S = BwdTmemShape<NP>;
+  constexpr int G = S::G, LG = S::LG, DW = S::DW, DC = S::DC, TILE = S::TILE;
+  constexpr int NTH = kWarps * 32;
+  extern __shared__ __align__(16) float smem[];
+  __shared__ uint32_t s_tmem;
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ng = lane & (G - 1), dg = lane >> LG;
+  const int b = blockIdx.y;
+  const int blk = blockIdx.x % p.nblk, seg = blockIdx.x / p.nblk;
+  const int dblk0 = blk * DC;
+  const int cl = warp * DW + dg * 4;     // first channel of the thread inside the CTA block
+  const int d0 = dblk0 + cl;
+  const int n0 = ng * 4;
+  const int Di = p.Di, N = p.N, T = p.T;
+  const int c_begin = seg * p.seg_chunks;
+  const int c_end = min(p.nchunks, c_begin + p.seg_chunks);
+
+  // lane-dependent storage order (see the file comment)
+  const int mc = (lane >> (LG - 1)) & 1;               // channel pairs swapped
+  const int mx = (lane >> (LG - 2)) & 1;               // channel inside the pair after the reduction
+  const int m1 = (lane >> 4) & 1;                      // state pairs swapped
+  const int m0 = S::SWAP ? (lane >> 3) & 1 : 0;        // states inside each pair swapped
+  const int mk = S::KIND ? (lane >> 2) & 1 : 0;        // keeps C (1) or B (0) after the reduction
+  // channel of physical pair q, element k: d0 + 2*(q ^ mc) + k
+  // state of physical slot s = 2*pp + e:   n0 + 2*(pp ^ m1) + (e ^ m0)
+  auto chan = [&](int q, int k) { return 2 * (q ^ mc) + k; };
+  auto state = [&](int s) { return n0 + 2 * ((s >> 1) ^ m1) + ((s & 1) ^ m0); };
+
+  // the channel whose d_delta / d_u this lane stores after the reduction over states
+  const int j_out = 2 * mc + mx;
+  const int d_out = d0 + j_out;
+  const int wsel = lane & (G / 4 - 1);
+  const bool w_delta = wsel == 0;
+  const bool w_u = (G == 4) ? true : wsel == 1;
+  const float D_out = d_out < Di ? p.D[d_out] : 0.f;
+  float dD_out = 0.f;
+
+  float2 a2[2][4], dh[2][4], accA[2][4];
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const int n = state(s);
+      float v[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int d = d0 + chan(q, k);
+        v[k] = (d < Di && n < N) ? -expf(p.A_log[(size_t)d * N + n]) * kLog2e : 0.f;
+      }
+      a2[q][s] = make_float2(v[0], v[1]);
+      dh[q][s] = accA[q][s] = make_float2(0.f, 0.f);
+    }
+
+  if (warp == 0) tmem_alloc(&s_tmem, S::kTmemCols);
+  tmem_fence_before_sync();
+  __syncthreads();
+  tmem_fence_after_sync();
+  const uint32_t taddr = s_tmem + ((uint32_t)(32 * warp) << 16);
+
+  float* dup = smem + kTmemStages * S::kStageFloats;
+  float* const s_Bw = dup;                         // {B, B} per (step, state)
+  float* const s_Cw = dup + kChunk * NP * 2;
+  float* const s_Bsw = dup + 2 * kChunk * NP * 2;  // pair-swapped copies (SWAP only)
+  float* const s_Csw = dup + 3 * kChunk * NP * 2;
+  const float* Bsrc = (S::SWAP && m0) ? s_Bsw : s_Bw;
+  const float* Csrc = (S::SWAP && m0) ? s_Csw : s_Cw;
+  float* const red_fixed = dup + S::kDupFloats;
+
+  const int last = c_end - 1;
+  const int nck = c_end - c_begin;
+#pragma unroll
+  for (int s = 0; s < kTmemStages - 1; ++s) {
+    if (s < nck) bwd_tmem_load_chunk<NP, VEC>(p, smem + s * S::kStageFloats, last - s, b, dblk0);
+    else cp_async_commit();
+  }
+
+  // d_h entering the segment from the future: the composed carry of the later segments
+  // (scan_bwd_compose_kernel), zero for the last segment
+  if (seg + 1 < p.nseg) {
+    const size_t rowbase = ((size_t)b * p.nseg * p.nsub + (size_t)seg * p.nsub) * Di;
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        const int n = state(s);
+        float L[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int d = d0 + chan(q, k);
+          L[k] = (d < Di && n < N) ? p.agg_L[(rowbase + d) * N + n] : 0.f;
+        }
+        dh[q][s] = make_float2(L[0], L[1]);
+      }
+  }
+
+  const size_t rowb = (size_t)b * T;
+  int offc[2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) offc[q] = cl + chan(q, 0);
+  int offn[2];
+#pragma unroll
+  for (int pp = 0; pp < 2; ++pp) offn[pp] = (n0 + 2 * (pp ^ m1)) * 2;
+  // where this lane's reduced d_B / d_C values go inside a [2][NP] row of the warp's sums
+  const int n_res = n0 + 2 * m1 + m0;
+  const float4* pB[2] = {reinterpret_cast<const float4*>(Bsrc + offn[0]),
+                         reinterpret_cast<const float4*>(Bsrc + offn[1])};
+  const float4* pC[2] = {reinterpret_cast<const float4*>(Csrc + offn[0]),
+                         reinterpret_cast<const float4*>(Csrc + offn[1])};
+
+  for (int it = 0; it < nck; ++it) {
+    const int c = last - it;
+    cp_async_wait<kTmemStages - 2>();
+    __syncthreads();
+    {
+      const int itn = it + kTmemStages - 1;
+      if (itn < nck)
+        bwd_tmem_load_chunk<NP, VEC>(p, smem + (itn % kTmemStages) * S::kStageFloats, last - itn,
+                                     b, dblk0);
+      else
+        cp_async_commit();
+    }
+    float* st = smem + (it % kTmemStages) * S::kStageFloats;
+    const float* s_dl = st;
+    const float* s_u = st + TILE;
+    float* s_g = st + 2 * TILE;          // becomes d_y
+    const float* s_dy = st + 3 * TILE;
+    const float* s_y = st + 4 * TILE;
+    const float* s_B = st + 5 * TILE;
+    const float* s_C = s_B + kChunk * NP;
+    const float* s_h0 = s_C + kChunk * NP;
+    float* red = S::RED_ALIAS ? st + 3 * TILE : red_fixed;
+    float* const red_lane = red + warp * kChunk * 2 * NP + (S::KIND ? mk * NP : 0) + n_res;
+    const int t0 = c * kChunk;
+
+    // ---- 0. gating backward (Phase B2) and the duplicated B / C tiles --------------------
+    static_assert(TILE % NTH == 0, "tile must split evenly over the CTA");
+#pragma unroll 4
+    for (int k = 0; k < TILE / NTH; ++k) {
+      const int e = k * NTH + threadIdx.x;
+      const int i = e / DC, col = e % DC;
+      const bool ok = (t0 + i < T) && (dblk0 + col < Di);
+      const size_t o = (rowb + t0 + i) * Di + dblk0 + col;
+      const float yv = s_y[e];
+      const float g = s_g[e], go = s_dy[e];
+      const float sg = sigmoid_fast(g);
+      s_g[e] = go * (g * sg);
+      st_global_if(p.d_gate + o, go * yv * (sg * fmaf(g, 1.f - sg, 1.f)), ok);
+    }
+    for (int e = threadIdx.x; e < kChunk * NP; e += NTH) {
+      const float bv = s_B[e], cv = s_C[e];
+      *reinterpret_cast<float2*>(s_Bw + 2 * e) = make_float2(bv, bv);
+      *reinterpret_cast<float2*>(s_Cw + 2 * e) = make_float2(cv, cv);
+      if constexpr (S::SWAP) {
+        const int es = e ^ 1;   // (step, state ^ 1)
+        *reinterpret_cast<float2*>(s_Bsw + 2 * es) = make_float2(bv, bv);
+        *reinterpret_cast<float2*>(s_Csw + 2 * es) = make_float2(cv, cv);
+      }
+    }
+    __syncthreads();
+
+    // ---- 1. forward recompute; the state before each step goes to tensor memory ---------
+    float2 h[2][4];
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        const int n = state(s);
+        float v[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+          v[k] = n < N ? lds1(s_h0 + (cl + chan(q, k)) * N + n) : 0.f;
+        h[q][s] = make_float2(v[0], v[1]);
+      }
+    // per-thread views of the staged tiles (the step loops are unrolled by two: measured
+    // faster than full unrolling, which runs out of registers)
+    const float2* pdl[2] = {reinterpret_cast<const float2*>(s_dl + offc[0]),
+                            reinterpret_cast<const float2*>(s_dl + offc[1])};
+    const float2* pu[2] = {reinterpret_cast<const float2*>(s_u + offc[0]),
+                           reinterpret_cast<const float2*>(s_u + offc[1])};
+    const float2* pdy[2] = {reinterpret_cast<const float2*>(s_g + offc[0]),
+                            reinterpret_cast<const float2*>(s_g + offc[1])};
+#pragma unroll 2
+    for (int i = 0; i < kChunk; ++i) {
+      step_fence();
+      tmem_st16(taddr + 16 * i, reinterpret_cast<const float2(&)[8]>(h));
+      float2 dl2[2], du2[2], B2[4];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        dl2[q] = pdl[q][i * DC / 2];
+        du2[q] = mul2(dl2[q], pu[q][i * DC / 2]);
+      }
+#pragma unroll
+      for (int pp = 0; pp < 2; ++pp) {
+        const float4 v = pB[pp][i * NP / 2];
+        B2[2 * pp] = make_float2(v.x, v.y);
+        B2[2 * pp + 1] = make_float2(v.z, v.w);
+      }
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          const float2 da = ex2_2(mul2(dl2[q], a2[q][s]));
+          h[q][s] = fma2(da, h[q][s], mul2(du2[q], B2[s]));
+        }
+    }
+    tmem_wait_st();
+
+    // ---- 2. reverse walk (Phase B3) ------------------------------------------------------
+    // output rows of this chunk for the lane's channel; rows at or past T are not stored
+    float* const out_dd = p.d_delta + (rowb + t0) * Di + d_out;
+    float* const out_du = p.d_u + (rowb + t0) * Di + d_out;
+    const int lim_dd = (w_delta && d_out < Di) ? T - t0 : 0;
+    const int lim_du = (w_u && d_out < Di) ? T - t0 : 0;
+#pragma unroll 2
+    for (int ii = 0; ii < kChunk; ++ii) {
+      const int i = kChunk - 1 - ii;
+      step_fence();
+      float2 hp[2][4];   // state before step i
+      tmem_ld16(taddr + 16 * i, reinterpret_cast<float2(&)[8]>(hp));
+      float2 dl2[2], u2[2], dy2[2], du2[2], B2[4], C2[4];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        dl2[q] = pdl[q][i * DC / 2];
+        u2[q] = pu[q][i * DC / 2];
+        dy2[q] = pdy[q][i * DC / 2];
+        du2[q] = mul2(dl2[q], u2[q]);
+      }
+#pragma unroll
+      for (int pp = 0; pp < 2; ++pp) {
+        const float4 vb = pB[pp][i * NP / 2];
+        const float4 vc = pC[pp][i * NP / 2];
+        B2[2 * pp] = make_float2(vb.x, vb.y);
+        B2[2 * pp + 1] = make_float2(vb.z, vb.w);
+        C2[2 * pp] = make_float2(vc.x, vc.y);
+        C2[2 * pp + 1] = make_float2(vc.z, vc.w);
+      }
+      tmem_wait_ld(reinterpret_cast<float2(&)[8]>(hp));
+      float2 sa2[2], sb2[2], xb2[4], xc2[4];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) sa2[q] = sb2[q] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int s = 0; s < 4; ++s) xb2[s] = xc2[s] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          const float2 da = ex2_2(mul2(dl2[q], a2[q][s]));
+          const float2 gh = fma2(dy2[q], C2[s], dh[q][s]);   // d_h += d_y*C
+          const float2 cr = mul2(da, gh);                      // carried to t-1
+          const float2 r = mul2(cr, hp[q][s]);                 // d_h*da*h_{t-1}
+          accA[q][s] = fma2(r, dl2[q], accA[q][s]);
+          sa2[q] = fma2(a2[q][s], r, sa2[q]);
+          sb2[q] = fma2(gh, B2[s], sb2[q]);
+          xb2[s] = fma2(gh, du2[q], xb2[s]);
+          xc2[s] = fma2(dy2[q], h[q][s], xc2[s]);
+          dh[q][s] = cr;
+        }
+      // d_B / d_C of this step: sum over the warp's channels
+      float v[8];
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        v[s] = xb2[s].x + xb2[s].y;
+        v[4 + s] = xc2[s].x + xc2[s].y;
+      }
+      // level 16: the state pairs (lanes with bit 16 hold them swapped)
+      v[0] += __shfl_xor_sync(kFull, v[2], 16);
+      v[1] += __shfl_xor_sync(kFull, v[3], 16);
+      v[4] += __shfl_xor_sync(kFull, v[6], 16);
+      v[5] += __shfl_xor_sync(kFull, v[7], 16);
+      if constexpr (S::SWAP) {   // level 8: inside the pair (lanes with bit 8 hold it swapped)
+        v[0] += __shfl_xor_sync(kFull, v[1], 8);
+        v[4] += __shfl_xor_sync(kFull, v[5], 8);
+      }
+      float* rrow = red_lane + i * 2 * NP;
+      if constexpr (S::KIND) {   // level 4: B or C
+        const float send = mk ? v[0] : v[4];
+        const float keep = mk ? v[4] : v[0];
+        rrow[0] = keep + __shfl_xor_sync(kFull, send, 4);
+      } else if constexpr (S::SWAP) {
+        rrow[0] = v[0];
+        rrow[NP] = v[4];
+      } else {
+        *reinterpret_cast<float2*>(rrow) = make_float2(v[0], v[1]);
+        *reinterpret_cast<float2*>(rrow + NP) = make_float2(v[4], v[5]);
+      }
+      // sums over n: level G/2 over the channel pairs (lanes with that bit hold them swapped)
+      sa2[0] = make_float2(sa2[0].x + __shfl_xor_sync(kFull, sa2[1].x, G / 2),
+                           sa2[0].y + __shfl_xor_sync(kFull, sa2[1].y, G / 2));
+      sb2[0] = make_float2(sb2[0].x + __shfl_xor_sync(kFull, sb2[1].x, G / 2),
+                           sb2[0].y + __shfl_xor_sync(kFull, sb2[1].y, G / 2));
+      // level G/4: inside the pair, with selects
+      float sA = (mx ? sa2[0].y : sa2[0].x) +
+                 __shfl_xor_sync(kFull, mx ? sa2[0].x : sa2[0].y, G / 4);
+      float sB = (mx ? sb2[0].y : sb2[0].x) +
+                 __shfl_xor_sync(kFull, mx ? sb2[0].x : sb2[0].y, G / 4);
+#pragma unroll
+      for (int m = G / 8; m >= 1; m /= 2) {
+        sA += __shfl_xor_sync(kFull, sA, m);
+        sB += __shfl_xor_sync(kFull, sB, m);
+      }
+      {
+        const float uo = mx ? u2[0].y : u2[0].x;
+        const float dlo = mx ? dl2[0].y : dl2[0].x;
+        const float dyo = mx ? dy2[0].y : dy2[0].x;
+        dD_out = fmaf(dyo, uo, dD_out);
+        const size_t o = (size_t)i * Di;
+        st_global_lt(out_dd + o, fmaf(sA, kLn2, uo * sB), i, lim_dd);
+        st_global_lt(out_du + o, fmaf(dyo, D_out, dlo * sB), i, lim_du);
+      }
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int s = 0; s < 4; ++s) h[q][s] = hp[q][s];
+    }
+    __syncthreads();
+    // CTA partial of d_B / d_C for this chunk: fixed-order sum over the warps
+    for (int e = threadIdx.x; e < kChunk * 2 * NP; e += NTH) {
+      const int i = e / (2 * NP), kn = e % (2 * NP);
+      const int kind = kn / NP, n = kn % NP;
+      const int t = t0 + i;
+      if (t < T && n < N) {
+        float sum = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) sum += red[(w * kChunk + i) * 2 * NP + kn];
+        const size_t o = (((size_t)blk * p.batch + b) * T + t) * N + n;
+        (kind ? p.partC : p.partB)[o] = sum;
+      }
+    }
+  }
+  cp_async_wait<0>();
+
+  // per-(batch, segment) partials of d_A_log (= A * sum_t delta*r = ln2*a2*accA) and d_D
+  {
+    const size_t rowbase = ((size_t)b * p.nseg + seg) * Di;
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        const int n = state(s);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int d = d0 + chan(q, k);
+          const float aa = k ? a2[q][s].y : a2[q][s].x;
+          const float ac = k ? accA[q][s].y : accA[q][s].x;
+          if (d < Di && n < N) p.partA[(rowbase + d) * N + n] = kLn2 * aa * ac;
+        }
+      }
+    if (w_delta && d_out < Di) p.partD[rowbase + d_out] = dD_out;
+  }
+
+  tmem_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(s_tmem, S::kTmemCols);
+}
+
+// Segment pre-pass with the main kernel's channel blocks (the same aggregates as
+// scan_bwd_agg_kernel: L = sum_t exp(A * sum_{s<=t} delta_s) * d_y_t * C_t[n] and the sum of
+// delta over one sub-segment). A thread owns 4 channels x 4 states, channel-packed, so no
+// value needs a splat and nothing crosses lanes.
+template <int NP>
+struct BwdAgg4Shape {
+  using S = BwdTmemShape<NP>;
+  static constexpr int kStages = 2;
+  // per stage: delta, gate (-> d_y), dy [kChunk][DC]; C [kChunk][NP]
+  static constexpr int kStageFloats = 3 * S::TILE + kChunk * NP;
+  static constexpr int kDupFloats = kChunk * NP * 2;   // {C, C} of the current chunk
+  static constexpr size_t kSmemBytes = ((size_t)kStages * kStageFloats + kDupFloats) * sizeof(float);
+};
+
+template <int NP, bool VEC>
+__global__ void __launch_bounds__(kWarps * 32)
+scan_bwd_agg4_kernel(const BwdParams p) {
+  using S = BwdTmemShape<NP>;
+  using A = BwdAgg4Shape<NP>;
+  constexpr int G = S::G, LG = S::LG, DW = S::DW, DC = S::DC, TILE = S::TILE;
+  constexpr int NTH = kWarps * 32;
+  extern __shared__ __align__(16) float smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ng = lane & (G - 1), dg = lane >> LG;
+  const int b = blockIdx.y;
+  const int blk = blockIdx.x % p.nblk, grp = blockIdx.x / p.nblk;
+  const int dblk0 = blk * DC;
+  const int cl = warp * DW + dg * 4;
+  const int d0 = dblk0 + cl;
+  const int n0 = ng * 4;
+  const int Di = p.Di, N = p.N, T = p.T;
+  // segments 1 .. nseg-1 need aggregates; sub-segment j of segment sg (may be empty)
+  const int sg = 1 + grp / p.nsub, j_sub = grp % p.nsub;
+  const int slot = sg * p.nsub + j_sub;
+  const int c_begin = sg * p.seg_chunks + j_sub * p.sub_chunks;
+  const int c_end = min(min(p.nchunks, (sg + 1) * p.seg_chunks), c_begin + p.sub_chunks);
+  const size_t row0 = (size_t)b * T;
+
+  float2 a2[2][4], L[2][4];
+  float2 P2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};   // running sums of delta
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const int n = n0 + s;
+      float v[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int d = d0 + 2 * q + k;
+        v[k] = (d < Di && n < N) ? -expf(p.A_log[(size_t)d * N + n]) * kLog2e : 0.f;
+      }
+      a2[q][s] = make_float2(v[0], v[1]);
+      L[q][s] = make_float2(0.f, 0.f);
+    }
+
+  float* dupC = smem + A::kStages * A::kStageFloats;
+  auto load = [&](int stage, int c) {
+    float* st = smem + stage * A::kStageFloats;
+    stage_tile<DC, NTH, VEC>(st, p.delta, row0, c * kChunk, T, Di, dblk0);
+    stage_tile<DC, NTH, VEC>(st + TILE, p.gate, row0, c * kChunk, T, Di, dblk0);
+    stage_tile<DC, NTH, VEC>(st + 2 * TILE, p.dy, row0, c * kChunk, T, Di, dblk0);
+    stage_tile<NP, NTH, VEC>(st + 3 * TILE, p.C, row0, c * kChunk, T, N, 0);
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int s = 0; s < A::kStages - 1; ++s) {
+    if (c_begin + s < c_end) load(s, c_begin + s);
+    else cp_async_commit();
+  }
+  const float4* pC[2] = {reinterpret_cast<const float4*>(dupC + 2 * n0),
+                         reinterpret_cast<const float4*>(dupC + 2 * n0 + 4)};
+  for (int c = c_begin; c < c_end; ++c) {
+    const int it = c - c_begin;
+    cp_async_wait<A::kStages - 2>();
+    __syncthreads();
+    if (c + A::kStages - 1 < c_end) load((it + A::kStages - 1) % A::kStages, c + A::kStages - 1);
+    else cp_async_commit();
+    float* st = smem + (it % A::kStages) * A::kStageFloats;
+    const float* s_dl = st;
+    float* s_g = st + TILE;             // becomes d_y
+    const float* s_dy = st + 2 * TILE;
+    const float* s_C = st + 3 * TILE;
+#pragma unroll 4
+    for (int e = threadIdx.x; e < TILE; e += NTH) {
+      const float g = s_g[e];
+      s_g[e] = s_dy[e] * (g * sigmoid_fast(g));
+    }
+    for (int e = threadIdx.x; e < kChunk * NP; e += NTH) {
+      const float cv = s_C[e];
+      *reinterpret_cast<float2*>(dupC + 2 * e) = make_float2(cv, cv);
+    }
+    __syncthreads();
+    const float4* pdl = reinterpret_cast<const float4*>(s_dl + cl);
+    const float4* pdy = reinterpret_cast<const float4*>(s_g + cl);
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i) {
+      const float4 dl = pdl[i * DC / 4];
+      const float4 dy = pdy[i * DC / 4];
+      P2[0] = __fadd2_rn(P2[0], make_float2(dl.x, dl.y));
+      P2[1] = __fadd2_rn(P2[1], make_float2(dl.z, dl.w));
+      const float2 dy2[2] = {make_float2(dy.x, dy.y), make_float2(dy.z, dy.w)};
+      const float4 c01 = pC[0][i * NP / 2], c23 = pC[1][i * NP / 2];
+      const float2 C2[4] = {make_float2(c01.x, c01.y), make_float2(c01.z, c01.w),
+                            make_float2(c23.x, c23.y), make_float2(c23.z, c23.w)};
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          const float2 cum = ex2_2(mul2(P2[q], a2[q][s]));
+          L[q][s] = fma2(cum, mul2(dy2[q], C2[s]), L[q][s]);
+        }
+    }
+  }
+  cp_async_wait<0>();
+  // emit the sub-segment's aggregate (zeros for an empty one)
+  const size_t rowbase = ((size_t)b * p.nseg * p.nsub + slot) * Di;
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int d = d0 + 2 * q + k;
+      if (d >= Di) continue;
+      if (ng == 0) p.agg_sd[rowbase + d] = k ? P2[q].y : P2[q].x;
+      float v[4];
+#pragma unroll
+      for (int s = 0; s < 4; ++s) v[s] = k ? L[q][s].y : L[q][s].x;
+      float* dst = p.agg_L + (rowbase + d) * N + n0;
+      if constexpr (VEC) {
+        if (n0 < N) *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+      } else {
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          if (n0 + s < N) dst[s] = v[s];
+      }
+    }
+}
+
+template <int NP, bool VEC>
+static int launch_agg4(const Plan& plan, const BwdParams& p, cudaStream_t s) {
+  using A = BwdAgg4Shape<NP>;
+  if (cudaFuncSetAttribute(scan_bwd_agg4_kernel<NP, VEC>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)A::kSmemBytes) != cudaSuccess)
+    return -1;
+  dim3 grid((unsigned)(plan.bwd.nblk * (plan.bwd.nseg - 1) * plan.bwd.nsub),
+            (unsigned)plan.batch);
+  scan_bwd_agg4_kernel<NP, VEC><<<grid, kWarps * 32, A::kSmemBytes, s>>>(p);
+  return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
+}
+
+int launch_bwd_agg_tmem(const Plan& plan, const BwdParams& p, cudaStream_t s) {
+  if (plan.bwd.nseg <= 1) return 0;
+  const bool vec = (plan.Di % 4 == 0) && (plan.N % 4 == 0);
+  switch (plan.NP) {
+    case 16: return vec ? launch_agg4<16, true>(plan, p, s) : launch_agg4<16, false>(plan, p, s);
+    case 32: return vec ? launch_agg4<32, true>(plan, p, s) : launch_agg4<32, false>(plan, p, s);
+    case 64: return vec ? launch_agg4<64, true>(plan, p, s) : launch_agg4<64, false>(plan, p, s);
+    default: return -1;
+  }
+}
+
+template <int NP, bool VEC>
+static int launch_np(const Plan& plan, const BwdParams& p, cudaStream_t s) {
+  using S = BwdTmemShape<NP>;
+  if (cudaFuncSetAttribute(scan_bwd_tmem_kernel<NP, VEC>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)S::kSmemBytes) != cudaSuccess)
+    return -1;
+  dim3 grid((unsigned)(plan.bwd.nblk * plan.bwd.nseg), (unsigned)plan.batch);
+  scan_bwd_tmem_kernel<NP, VEC><<<grid, kWarps * 32, S::kSmemBytes, s>>>(p);
+  return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
+}
+
+int launch_bwd_main_tmem(const Plan& plan, const BwdParams& p, cudaStream_t s) {
+  const bool vec = (plan.Di % 4 == 0) && (plan.N % 4 == 0);
+  switch (plan.NP) {
+    case 16: return vec ? launch_np<16, true>(plan, p, s) : launch_np<16, false>(plan, p, s);
+    case 32: return vec ? launch_np<32, true>(plan, p, s) : launch_np<32, false>(plan, p, s);
+    case 64: return vec ? launch_np<64, true>(plan, p, s) : launch_np<64, false>(plan, p, s);
+    default: return -1;
+  }
+}
+
+}  // namespace mscan

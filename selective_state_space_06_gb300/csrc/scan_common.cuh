@@ -11,9 +11,6 @@ constexpr float kLog2e = 1.4426950408889634f;  // log2(e)
 constexpr float kLn2 = 0.6931471805599453f;    // ln(2)
 constexpr unsigned kFull = 0xffffffffu;
 
-// Warps per CTA of the segment pre-pass kernels (the main kernels' CTA shape measured best;
-// wider CTAs with several segments each were slower on GB300).
-constexpr int kAggWarps = kWarps;
 
 // 2^x on the special-function unit (PTX ex2.approx.ftz.f32). In the scan x <= 0, so the result
 // lies in [0, 1]; very negative x flushes to 0.
@@ -76,6 +73,17 @@ __device__ __forceinline__ void st_shared_if(float* p, float v, bool pred) {
       "{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q st.shared.f32 [%0], %1;\n\t}"
       ::"r"(smem_addr(p)), "f"(v), "r"((unsigned)pred) : "memory");
 }
+
+// Predicated store "if (a < b) *p = v" without a branch.
+__device__ __forceinline__ void st_global_lt(float* p, float v, int a, int b) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.lt.s32 q, %2, %3;\n\t@q st.global.f32 [%0], %1;\n\t}"
+      ::"l"(p), "f"(v), "r"(a), "r"(b) : "memory");
+}
+
+// Compiler-level fence between the steps of a fully unrolled loop: no memory access moves
+// across it, so the loads of later steps are not hoisted (and kept live in registers) early.
+__device__ __forceinline__ void step_fence() { asm volatile("" ::: "memory"); }
 
 // NPR float2 pairs of consecutive states from shared memory (8- or 16-byte aligned).
 template <int NPR>
@@ -200,5 +208,61 @@ struct ReduceScatter {
     return w;
   }
 };
+
+}  // namespace mscan
+
+namespace mscan {
+
+// ---- tensor memory (tcgen05, sm_100 family) -------------------------------------------------
+// A CTA allocates columns of the SM's 128-lane x 512-column tensor memory; warp w of the CTA
+// reaches lanes 32*(w%4) .. 32*(w%4)+31, and with the 32x32b shape each thread reads and writes
+// its own lane. Allocation blocks while the SM has too few free columns, so a kernel must cap
+// its resident CTAs per SM (through its shared memory) at 512 / columns.
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {   // one warp
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+               ::"r"(smem_addr(slot)), "r"(ncols) : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {  // one warp
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// 16 consecutive 32-bit columns of the thread's lane, from / to 8 float2 registers.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float2 (&v)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "f"(v[0].x), "f"(v[0].y), "f"(v[1].x), "f"(v[1].y), "f"(v[2].x), "f"(v[2].y), "f"(v[3].x),
+      "f"(v[3].y), "f"(v[4].x), "f"(v[4].y), "f"(v[5].x), "f"(v[5].y), "f"(v[6].x), "f"(v[6].y),
+      "f"(v[7].x), "f"(v[7].y));
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float2 (&v)[8]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=f"(v[0].x), "=f"(v[0].y), "=f"(v[1].x), "=f"(v[1].y), "=f"(v[2].x), "=f"(v[2].y),
+        "=f"(v[3].x), "=f"(v[3].y), "=f"(v[4].x), "=f"(v[4].y), "=f"(v[5].x), "=f"(v[5].y),
+        "=f"(v[6].x), "=f"(v[6].y), "=f"(v[7].x), "=f"(v[7].y)
+      : "r"(taddr));
+}
+// Completion of the thread's earlier tcgen05.st (before reading the columns back).
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+// Completion of tcgen05.ld into v. The registers are in-out operands so that no use of them
+// is scheduled before the wait.
+__device__ __forceinline__ void tmem_wait_ld(float2 (&v)[8]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+f"(v[0].x), "+f"(v[0].y), "+f"(v[1].x), "+f"(v[1].y), "+f"(v[2].x),
+                 "+f"(v[2].y), "+f"(v[3].x), "+f"(v[3].y), "+f"(v[4].x), "+f"(v[4].y),
+                 "+f"(v[5].x), "+f"(v[5].y), "+f"(v[6].x), "+f"(v[6].y), "+f"(v[7].x),
+                 "+f"(v[7].y));
+}
 
 }  // namespace mscan

@@ -18,6 +18,11 @@ constexpr int kDPT = 2;     // channels per thread
 __host__ __device__ constexpr int states_per_thread_fwd(int NP) { return NP <= 16 ? 2 : 4; }
 __host__ __device__ constexpr int states_per_thread_bwd(int NP) { return NP < 4 ? NP : 4; }
 constexpr int kWarps = 4;   // warps per CTA
+// Warps per CTA of the segment pre-pass kernels (the main kernels' CTA shape measured best;
+// wider CTAs with several segments each were slower on GB300).
+constexpr int kAggWarps = kWarps;
+// CTAs to aim for in the backward pre-pass of the tensor-memory path (two waves of four)
+constexpr int kBwdAggTarget = 2 * 4 * 152;
 constexpr int kChunk = 16;  // time steps per chunk (= checkpoint interval)
 constexpr int kMaxState = 64;
 
@@ -31,6 +36,12 @@ constexpr int kMaxState = 64;
 // below that its pre-pass costs more than the extra parallelism gains (measured on GB300).
 __host__ __device__ constexpr int target_units_fwd(int NP) { return NP <= 16 ? 1 : 2048; }
 __host__ __device__ constexpr int target_units_bwd(int NP) { return 2048; }
+// The backward for d_state > 8 runs scan_bwd_tmem_kernel: 4 channels x 4 states per thread,
+// at most 2 CTAs per SM (its tensor-memory columns), so its segments are chosen to fill whole
+// waves of 2 x 152 CTAs.
+constexpr int kTmemMinNP = 16;
+constexpr int kTmemDPT = 4;
+constexpr int kTmemSlots = 2 * 152;
 
 // Work decomposition of one pass (forward or backward); the two may differ.
 struct PassPlan {
@@ -40,6 +51,11 @@ struct PassPlan {
   int nblk = 0;        // CTAs along d_inner
   int seg_chunks = 0;  // chunks per segment
   int nseg = 0;        // segments along T
+  // backward only: the segment pre-pass works on sub-segments of sub_chunks chunks (nsub per
+  // segment, the last ones possibly shorter or empty), so that it has enough CTAs even when
+  // the main kernel wants few, long segments
+  int sub_chunks = 0;
+  int nsub = 1;
 };
 
 struct Plan {
@@ -77,10 +93,10 @@ struct BwdParams {
   const float* y_ck;   // y saved by the forward (inside the ckpt buffer)
   float* d_delta; float* d_u; float* d_gate;
   float* partB; float* partC; float* partA; float* partD;   // scratch
-  float* agg_L; float* agg_sd;                               // scratch: backward aggregates
+  float* agg_L; float* agg_sd;     // scratch: backward aggregates [batch][nseg*nsub][Di](N)
   float* d_B; float* d_C; float* d_A_log; float* d_D;
   int batch, T, Di, N, nchunks, nblk, seg_chunks, nseg;
-  int agg_k;  // pre-pass: consecutive segments per CTA
+  int sub_chunks, nsub;            // pre-pass sub-segments (see PassPlan)
 };
 
 // Each returns the number of kernels enqueued (>= 1) or -1 on a launch error.
@@ -89,5 +105,9 @@ struct BwdParams {
 // reduction.
 int launch_fwd(const Plan& plan, const FwdParams& p, cudaStream_t stream);
 int launch_bwd(const Plan& plan, const BwdParams& p, cudaStream_t stream);
+// the main backward kernel alone for d_state padded to 16, 32 or 64 (scan_bwd_tmem.cu)
+int launch_bwd_main_tmem(const Plan& plan, const BwdParams& p, cudaStream_t stream);
+// its segment pre-pass (0 kernels when there is one segment)
+int launch_bwd_agg_tmem(const Plan& plan, const BwdParams& p, cudaStream_t stream);
 
 }  // namespace mscan
