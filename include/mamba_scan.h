@@ -61,6 +61,9 @@ extern "C" {
 #define MAMBA_ERR_UNSUPPORTED 5 /* d_state outside 1..64                                     */
 #define MAMBA_ERR_NOALLOC_LIMIT 6 /* mamba_scan_bwd_noalloc: the sizes need more scratch than
                                      MAMBA_SCAN_NOALLOC_SCRATCH_BYTES                        */
+#define MAMBA_ERR_TIMEOUT 7     /* reported by mamba_scan_status: a kernel gave up waiting
+                                   (1 s) for one of its own asynchronous copies; the outputs
+                                   of the calls since the last status check are invalid     */
 
 /* Bytes of the checkpoint buffer that mamba_scan_fwd writes and mamba_scan_bwd reads. The
  * forward stores the state h at every 16-step chunk boundary of the time axis, so that the
@@ -132,8 +135,9 @@ int mamba_scan_bwd_noalloc(const float* delta, const float* u, const float* B, c
                            float* d_gate, int64_t batch, int64_t T, int64_t d_inner,
                            int64_t d_state, void* stream);
 
-/* Synchronises `stream` and reports any asynchronous CUDA error (MAMBA_OK or
- * MAMBA_ERR_CUDA). */
+/* Synchronises `stream` and reports any asynchronous CUDA error (MAMBA_ERR_CUDA) or a
+ * kernel that gave up waiting for its own copies (MAMBA_ERR_TIMEOUT; the flag is then
+ * cleared). MAMBA_OK otherwise. */
 int mamba_scan_status(void* stream);
 
 /* Static, human-readable text of a return code. When the code is MAMBA_ERR_CUDA it names the

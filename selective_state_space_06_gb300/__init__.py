@@ -35,6 +35,7 @@ MAMBA_ERR_WORKSPACE = 3
 MAMBA_ERR_CUDA = 4
 MAMBA_ERR_UNSUPPORTED = 5
 MAMBA_ERR_NOALLOC_LIMIT = 6
+MAMBA_ERR_TIMEOUT = 7
 MAMBA_SCAN_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 EXPORTED = (

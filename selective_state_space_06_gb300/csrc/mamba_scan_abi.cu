@@ -320,6 +320,7 @@ int mamba_scan_fwd_bwd_host(const float* delta, const float* u, const float* B, 
   }
   cudaError_t e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return set_cuda_error(e);
+  if (mscan::bwd_take_fault()) return MAMBA_ERR_TIMEOUT;
   return MAMBA_OK;
 }
 
@@ -327,6 +328,7 @@ int mamba_scan_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return set_cuda_error(e);
+  if (mscan::bwd_take_fault()) return MAMBA_ERR_TIMEOUT;
   return MAMBA_OK;
 }
 
@@ -341,6 +343,8 @@ const char* mamba_scan_strerror(int code) {
     case MAMBA_ERR_UNSUPPORTED: return "d_state outside 1..64 is not supported";
     case MAMBA_ERR_NOALLOC_LIMIT:
       return "mamba_scan_bwd_noalloc: these sizes need more scratch than the static 64 MiB array";
+    case MAMBA_ERR_TIMEOUT:
+      return "a kernel gave up waiting for its asynchronous copies; recent outputs are invalid";
     default: return "unknown error code";
   }
 }

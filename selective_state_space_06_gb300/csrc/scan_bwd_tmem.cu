@@ -27,6 +27,11 @@
 //   * over channels (d_B, d_C): the lane with bit 16 set holds its two state pairs swapped, and
 //     the lane with bit 8 set (when it takes part) holds the states of each pair swapped (it
 //     reads B, C from a pair-swapped copy); the last level (B or C) uses selects.
+#include <cudaTypedefs.h>   // PFN_cuTensorMapEncodeTiled
+#include <string.h>
+
+#include <mutex>
+
 #include "scan_common.cuh"
 
 namespace mscan {
@@ -45,66 +50,104 @@ struct BwdTmemShape {
   static constexpr bool KIND = LD >= 8;                  // ... and on B / C
   static constexpr int TILE = kChunk * DC;
   // per stage: delta, u, gate (-> d_y), dy, y [kChunk][DC]; B, C [kChunk][NP]; the chunk's
-  // starting checkpoint [DC][N]
+  // starting checkpoint [DC][NP] (states past d_state are zeros or unused)
   static constexpr int kStageFloats = 5 * TILE + 2 * kChunk * NP + DC * NP;
+  static constexpr uint32_t kStageBytes = kStageFloats * sizeof(float);
   // duplicated B, C [kChunk][NP][2] (and their pair-swapped copies)
   static constexpr int kDupFloats = kChunk * NP * 2 * (SWAP ? 4 : 2);
   // per-warp d_B / d_C sums of the chunk [kWarps][kChunk][2][NP]; they fit in the dy and y
   // tiles of the current stage (dead after the gating step) when d_state is 16
   static constexpr int kRedFloats = kWarps * kChunk * 2 * NP;
   static constexpr bool RED_ALIAS = kRedFloats <= 2 * TILE;
-  static constexpr size_t kSmemBytes =
-      ((size_t)kTmemStages * kStageFloats + kDupFloats + (RED_ALIAS ? 0 : kRedFloats)) *
-      sizeof(float);
+  static constexpr size_t kDataFloats =
+      (size_t)kTmemStages * kStageFloats + kDupFloats + (RED_ALIAS ? 0 : kRedFloats);
+  // + the stage barriers, + slack to align the base to 128 bytes (TMA destinations)
+  static constexpr size_t kSmemBytes = kDataFloats * sizeof(float) + 8 * kTmemStages + 128;
   static constexpr uint32_t kTmemCols = kChunk * DPT * NPT;   // 256
   // tensor memory holds 512 columns per SM: at most two CTAs may be resident
   static_assert(3 * (kSmemBytes + 1024) > 228 * 1024, "shared memory must cap CTAs per SM at 2");
+  static_assert(kStageBytes % 128 == 0 && (TILE * 4) % 128 == 0 && (kChunk * NP * 4) % 128 == 0,
+                "TMA destinations must stay 128-byte aligned");
 };
 
-template <int NP, bool VEC>
-__device__ __forceinline__ void bwd_tmem_load_chunk(const BwdParams& p, float* st, int c, int b,
+static __device__ unsigned int g_bwd_fault;   // set when a bounded wait gave up
+
+// Stage layout: delta, u, gate, dy, y tiles, then B, C, then the checkpoint row.
+template <int NP, bool VEC, bool TMA>
+__device__ __forceinline__ void bwd_tmem_load_chunk(const BwdMaps& maps, const BwdParams& p,
+                                                    float* st, uint64_t* bar, int c, int b,
                                                     int dblk0) {
   using S = BwdTmemShape<NP>;
   constexpr int DC = S::DC, NTH = kWarps * 32, TILE = S::TILE;
-  const size_t row0 = (size_t)b * p.T;
   const int t0 = c * kChunk;
-  stage_tile<DC, NTH, VEC>(st, p.delta, row0, t0, p.T, p.Di, dblk0);
-  stage_tile<DC, NTH, VEC>(st + TILE, p.u, row0, t0, p.T, p.Di, dblk0);
-  stage_tile<DC, NTH, VEC>(st + 2 * TILE, p.gate, row0, t0, p.T, p.Di, dblk0);
-  stage_tile<DC, NTH, VEC>(st + 3 * TILE, p.dy, row0, t0, p.T, p.Di, dblk0);
-  stage_tile<DC, NTH, VEC>(st + 4 * TILE, p.y_ck, row0, t0, p.T, p.Di, dblk0);
-  stage_tile<NP, NTH, VEC>(st + 5 * TILE, p.B, row0, t0, p.T, p.N, 0);
-  stage_tile<NP, NTH, VEC>(st + 5 * TILE + kChunk * NP, p.C, row0, t0, p.T, p.N, 0);
-  {
-    // state entering chunk c (checkpoint slot c-1); zeros for the first chunk
-    float* s_h0 = st + 5 * TILE + 2 * kChunk * NP;
+  float* s_h0 = st + 5 * TILE + 2 * kChunk * NP;
+  if constexpr (TMA) {
+    // one thread issues the whole stage; rows past T, channels past d_inner, states past
+    // d_state and the (absent) checkpoint before chunk 0 arrive as zeros
+    if (threadIdx.x == 0) {
+      mbar_expect_tx(bar, S::kStageBytes);
+      tma_load_3d(st, &maps.delta, bar, dblk0, t0, b);
+      tma_load_3d(st + TILE, &maps.u, bar, dblk0, t0, b);
+      tma_load_3d(st + 2 * TILE, &maps.gate, bar, dblk0, t0, b);
+      tma_load_3d(st + 3 * TILE, &maps.dy, bar, dblk0, t0, b);
+      tma_load_3d(st + 4 * TILE, &maps.y, bar, dblk0, t0, b);
+      tma_load_3d(st + 5 * TILE, &maps.B, bar, 0, t0, b);
+      tma_load_3d(st + 5 * TILE + kChunk * NP, &maps.C, bar, 0, t0, b);
+      tma_load_4d(s_h0, &maps.ckpt, bar, 0, dblk0, c - 1, b);
+    }
+  } else {
+    const size_t row0 = (size_t)b * p.T;
+    stage_tile<DC, NTH, VEC>(st, p.delta, row0, t0, p.T, p.Di, dblk0);
+    stage_tile<DC, NTH, VEC>(st + TILE, p.u, row0, t0, p.T, p.Di, dblk0);
+    stage_tile<DC, NTH, VEC>(st + 2 * TILE, p.gate, row0, t0, p.T, p.Di, dblk0);
+    stage_tile<DC, NTH, VEC>(st + 3 * TILE, p.dy, row0, t0, p.T, p.Di, dblk0);
+    stage_tile<DC, NTH, VEC>(st + 4 * TILE, p.y_ck, row0, t0, p.T, p.Di, dblk0);
+    stage_tile<NP, NTH, VEC>(st + 5 * TILE, p.B, row0, t0, p.T, p.N, 0);
+    stage_tile<NP, NTH, VEC>(st + 5 * TILE + kChunk * NP, p.C, row0, t0, p.T, p.N, 0);
+    // state entering chunk c (checkpoint slot c-1), rows of N states at a stride of NP;
+    // zeros for the first chunk and for channels past d_inner
     const bool have = c > 0;
     const float* src =
         have ? p.ckpt + (((size_t)b * (p.nchunks - 1) + (c - 1)) * p.Di + dblk0) * p.N : p.ckpt;
     const int rowlen = DC * p.N;
     if constexpr (VEC) {
       for (int q = threadIdx.x * 4; q < rowlen; q += NTH * 4) {
-        const bool v = have && (dblk0 + q / p.N < p.Di);
-        cp_async16(s_h0 + q, v ? src + q : p.delta, v);
+        const int row = q / p.N, col = q % p.N;
+        const bool v = have && (dblk0 + row < p.Di);
+        cp_async16(s_h0 + row * NP + col, v ? src + q : p.delta, v);
       }
     } else {
       for (int q = threadIdx.x; q < rowlen; q += NTH) {
-        const bool v = have && (dblk0 + q / p.N < p.Di);
-        cp_async4(s_h0 + q, v ? src + q : p.delta, v);
+        const int row = q / p.N, col = q % p.N;
+        const bool v = have && (dblk0 + row < p.Di);
+        cp_async4(s_h0 + row * NP + col, v ? src + q : p.delta, v);
       }
     }
+    cp_async_commit();
   }
-  cp_async_commit();
 }
 
-template <int NP, bool VEC>
+// Waits until stage `stage` (its use number `use`) has landed in shared memory.
+template <bool TMA>
+__device__ __forceinline__ void bwd_tmem_wait_stage(uint64_t* bars, int stage, int use) {
+  if constexpr (TMA) {
+    if (!mbar_wait(bars + stage, (uint32_t)(use & 1))) atomicOr(&g_bwd_fault, 1u);
+  } else {
+    cp_async_wait<kTmemStages - 2>();
+  }
+}
+
+template <int NP, bool VEC, bool TMA>
 __global__ void __launch_bounds__(kWarps * 32, 2)
-scan_bwd_tmem_kernel(const BwdParams p) {
+scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
   using S = BwdTmemShape<NP>;
   constexpr int G = S::G, LG = S::LG, DW = S::DW, DC = S::DC, TILE = S::TILE;
   constexpr int NTH = kWarps * 32;
-  extern __shared__ __align__(16) float smem[];
+  extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ uint32_t s_tmem;
+  float* smem = reinterpret_cast<float*>(
+      smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u));   // 128-byte aligned
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kDataFloats);
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ng = lane & (G - 1), dg = lane >> LG;
@@ -117,6 +160,25 @@ scan_bwd_tmem_kernel(const BwdParams p) {
   const int Di = p.Di, N = p.N, T = p.T;
   const int c_begin = seg * p.seg_chunks;
   const int c_end = min(p.nchunks, c_begin + p.seg_chunks);
+  const int last = c_end - 1;
+  const int nck = c_end - c_begin;
+
+  // the first stage's copies go out before anything else, to overlap the set-up below
+  if constexpr (TMA) {
+    if (threadIdx.x == 0) {
+#pragma unroll
+      for (int s = 0; s < kTmemStages; ++s) mbar_init(bars + s, 1);
+      fence_mbar_init();
+    }
+  }
+#pragma unroll
+  for (int s = 0; s < kTmemStages - 1; ++s) {
+    if (s < nck)
+      bwd_tmem_load_chunk<NP, VEC, TMA>(maps, p, smem + s * S::kStageFloats, bars + s, last - s,
+                                        b, dblk0);
+    else if constexpr (!TMA)
+      cp_async_commit();
+  }
 
   // lane-dependent storage order (see the file comment)
   const int mc = (lane >> (LG - 1)) & 1;               // channel pairs swapped
@@ -153,30 +215,6 @@ scan_bwd_tmem_kernel(const BwdParams p) {
       a2[q][s] = make_float2(v[0], v[1]);
       dh[q][s] = accA[q][s] = make_float2(0.f, 0.f);
     }
-
-  if (warp == 0) tmem_alloc(&s_tmem, S::kTmemCols);
-  tmem_fence_before_sync();
-  __syncthreads();
-  tmem_fence_after_sync();
-  const uint32_t taddr = s_tmem + ((uint32_t)(32 * warp) << 16);
-
-  float* dup = smem + kTmemStages * S::kStageFloats;
-  float* const s_Bw = dup;                         // {B, B} per (step, state)
-  float* const s_Cw = dup + kChunk * NP * 2;
-  float* const s_Bsw = dup + 2 * kChunk * NP * 2;  // pair-swapped copies (SWAP only)
-  float* const s_Csw = dup + 3 * kChunk * NP * 2;
-  const float* Bsrc = (S::SWAP && m0) ? s_Bsw : s_Bw;
-  const float* Csrc = (S::SWAP && m0) ? s_Csw : s_Cw;
-  float* const red_fixed = dup + S::kDupFloats;
-
-  const int last = c_end - 1;
-  const int nck = c_end - c_begin;
-#pragma unroll
-  for (int s = 0; s < kTmemStages - 1; ++s) {
-    if (s < nck) bwd_tmem_load_chunk<NP, VEC>(p, smem + s * S::kStageFloats, last - s, b, dblk0);
-    else cp_async_commit();
-  }
-
   // d_h entering the segment from the future: the composed carry of the later segments
   // (scan_bwd_compose_kernel), zero for the last segment
   if (seg + 1 < p.nseg) {
@@ -196,6 +234,21 @@ scan_bwd_tmem_kernel(const BwdParams p) {
       }
   }
 
+  if (warp == 0) tmem_alloc(&s_tmem, S::kTmemCols);
+  tmem_fence_before_sync();
+  __syncthreads();
+  tmem_fence_after_sync();
+  const uint32_t taddr = s_tmem + ((uint32_t)(32 * warp) << 16);
+
+  float* dup = smem + kTmemStages * S::kStageFloats;
+  float* const s_Bw = dup;                         // {B, B} per (step, state)
+  float* const s_Cw = dup + kChunk * NP * 2;
+  float* const s_Bsw = dup + 2 * kChunk * NP * 2;  // pair-swapped copies (SWAP only)
+  float* const s_Csw = dup + 3 * kChunk * NP * 2;
+  const float* Bsrc = (S::SWAP && m0) ? s_Bsw : s_Bw;
+  const float* Csrc = (S::SWAP && m0) ? s_Csw : s_Cw;
+  float* const red_fixed = dup + S::kDupFloats;
+
   const size_t rowb = (size_t)b * T;
   int offc[2];
 #pragma unroll
@@ -212,14 +265,14 @@ scan_bwd_tmem_kernel(const BwdParams p) {
 
   for (int it = 0; it < nck; ++it) {
     const int c = last - it;
-    cp_async_wait<kTmemStages - 2>();
+    bwd_tmem_wait_stage<TMA>(bars, it % kTmemStages, it / kTmemStages);
     __syncthreads();
     {
       const int itn = it + kTmemStages - 1;
       if (itn < nck)
-        bwd_tmem_load_chunk<NP, VEC>(p, smem + (itn % kTmemStages) * S::kStageFloats, last - itn,
-                                     b, dblk0);
-      else
+        bwd_tmem_load_chunk<NP, VEC, TMA>(maps, p, smem + (itn % kTmemStages) * S::kStageFloats,
+                                          bars + itn % kTmemStages, last - itn, b, dblk0);
+      else if constexpr (!TMA)
         cp_async_commit();
     }
     float* st = smem + (it % kTmemStages) * S::kStageFloats;
@@ -236,18 +289,45 @@ scan_bwd_tmem_kernel(const BwdParams p) {
     const int t0 = c * kChunk;
 
     // ---- 0. gating backward (Phase B2) and the duplicated B / C tiles --------------------
-    static_assert(TILE % NTH == 0, "tile must split evenly over the CTA");
+    // d_y = dy*g*s into the gate tile, d_gate = dy*y*s*(1 + g*(1-s)) straight to global memory
+    if constexpr (VEC) {   // four consecutive channels at a time (all inside d_inner or none)
+      static_assert(TILE % (4 * NTH) == 0, "tile must split evenly over the CTA");
+#pragma unroll 2
+      for (int k = 0; k < TILE / (4 * NTH); ++k) {
+        const int e = 4 * (k * NTH + threadIdx.x);
+        const int i = e / DC, col = e % DC;
+        const bool ok = (t0 + i < T) && (dblk0 + col < Di);
+        const float4 yv = *reinterpret_cast<const float4*>(s_y + e);
+        const float4 g = *reinterpret_cast<const float4*>(s_g + e);
+        const float4 go = *reinterpret_cast<const float4*>(s_dy + e);
+        float4 dyo, dgo;
+        {
+          const float s0 = sigmoid_fast(g.x), s1 = sigmoid_fast(g.y);
+          const float s2 = sigmoid_fast(g.z), s3 = sigmoid_fast(g.w);
+          dyo = make_float4(go.x * (g.x * s0), go.y * (g.y * s1), go.z * (g.z * s2),
+                            go.w * (g.w * s3));
+          dgo = make_float4(go.x * yv.x * (s0 * fmaf(g.x, 1.f - s0, 1.f)),
+                            go.y * yv.y * (s1 * fmaf(g.y, 1.f - s1, 1.f)),
+                            go.z * yv.z * (s2 * fmaf(g.z, 1.f - s2, 1.f)),
+                            go.w * yv.w * (s3 * fmaf(g.w, 1.f - s3, 1.f)));
+        }
+        *reinterpret_cast<float4*>(s_g + e) = dyo;
+        st_global4_if(p.d_gate + (rowb + t0 + i) * Di + dblk0 + col, dgo, ok);
+      }
+    } else {
+      static_assert(TILE % NTH == 0, "tile must split evenly over the CTA");
 #pragma unroll 4
-    for (int k = 0; k < TILE / NTH; ++k) {
-      const int e = k * NTH + threadIdx.x;
-      const int i = e / DC, col = e % DC;
-      const bool ok = (t0 + i < T) && (dblk0 + col < Di);
-      const size_t o = (rowb + t0 + i) * Di + dblk0 + col;
-      const float yv = s_y[e];
-      const float g = s_g[e], go = s_dy[e];
-      const float sg = sigmoid_fast(g);
-      s_g[e] = go * (g * sg);
-      st_global_if(p.d_gate + o, go * yv * (sg * fmaf(g, 1.f - sg, 1.f)), ok);
+      for (int k = 0; k < TILE / NTH; ++k) {
+        const int e = k * NTH + threadIdx.x;
+        const int i = e / DC, col = e % DC;
+        const bool ok = (t0 + i < T) && (dblk0 + col < Di);
+        const size_t o = (rowb + t0 + i) * Di + dblk0 + col;
+        const float yv = s_y[e];
+        const float g = s_g[e], go = s_dy[e];
+        const float sg = sigmoid_fast(g);
+        s_g[e] = go * (g * sg);
+        st_global_if(p.d_gate + o, go * yv * (sg * fmaf(g, 1.f - sg, 1.f)), ok);
+      }
     }
     for (int e = threadIdx.x; e < kChunk * NP; e += NTH) {
       const float bv = s_B[e], cv = s_C[e];
@@ -271,7 +351,7 @@ scan_bwd_tmem_kernel(const BwdParams p) {
         float v[2];
 #pragma unroll
         for (int k = 0; k < 2; ++k)
-          v[k] = n < N ? lds1(s_h0 + (cl + chan(q, k)) * N + n) : 0.f;
+          v[k] = (TMA || n < N) ? s_h0[(cl + chan(q, k)) * NP + n] : 0.f;
         h[q][s] = make_float2(v[0], v[1]);
       }
     // per-thread views of the staged tiles (the step loops are unrolled by two: measured
@@ -417,20 +497,39 @@ scan_bwd_tmem_kernel(const BwdParams p) {
     }
     __syncthreads();
     // CTA partial of d_B / d_C for this chunk: fixed-order sum over the warps
-    for (int e = threadIdx.x; e < kChunk * 2 * NP; e += NTH) {
-      const int i = e / (2 * NP), kn = e % (2 * NP);
-      const int kind = kn / NP, n = kn % NP;
-      const int t = t0 + i;
-      if (t < T && n < N) {
-        float sum = 0.f;
+    if constexpr (VEC) {   // four consecutive states at a time (d_state % 4 == 0)
+      for (int e = 4 * threadIdx.x; e < kChunk * 2 * NP; e += 4 * NTH) {
+        const int i = e / (2 * NP), kn = e % (2 * NP);
+        const int kind = kn / NP, n = kn % NP;
+        const int t = t0 + i;
+        float4 sum = *reinterpret_cast<const float4*>(red + i * 2 * NP + kn);
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) sum += red[(w * kChunk + i) * 2 * NP + kn];
+        for (int w = 1; w < kWarps; ++w) {
+          const float4 v = *reinterpret_cast<const float4*>(red + (w * kChunk + i) * 2 * NP + kn);
+          sum = make_float4(sum.x + v.x, sum.y + v.y, sum.z + v.z, sum.w + v.w);
+        }
         const size_t o = (((size_t)blk * p.batch + b) * T + t) * N + n;
-        (kind ? p.partC : p.partB)[o] = sum;
+        st_global4_if((kind ? p.partC : p.partB) + o, sum, t < T && n < N);
+      }
+    } else {
+      for (int e = threadIdx.x; e < kChunk * 2 * NP; e += NTH) {
+        const int i = e / (2 * NP), kn = e % (2 * NP);
+        const int kind = kn / NP, n = kn % NP;
+        const int t = t0 + i;
+        if (t < T && n < N) {
+          float sum = 0.f;
+#pragma unroll
+          for (int w = 0; w < kWarps; ++w) sum += red[(w * kChunk + i) * 2 * NP + kn];
+          const size_t o = (((size_t)blk * p.batch + b) * T + t) * N + n;
+          (kind ? p.partC : p.partB)[o] = sum;
+        }
       }
     }
+    // this thread's shared-memory writes (d_y, the warp sums) come before the copies that
+    // refill the stage
+    if constexpr (TMA) fence_proxy_async_smem();
   }
-  cp_async_wait<0>();
+  if constexpr (!TMA) cp_async_wait<0>();
 
   // per-(batch, segment) partials of d_A_log (= A * sum_t delta*r = ln2*a2*accA) and d_D
   {
@@ -617,24 +716,119 @@ int launch_bwd_agg_tmem(const Plan& plan, const BwdParams& p, cudaStream_t s) {
   }
 }
 
-template <int NP, bool VEC>
-static int launch_np(const Plan& plan, const BwdParams& p, cudaStream_t s) {
+// ---- host side: tensor maps ------------------------------------------------------------------
+using EncodeTiledFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+static bool encode_f32(CUtensorMap* m, const void* base, cuuint32_t rank, const cuuint64_t* dims,
+                       const cuuint64_t* strides, const cuuint32_t* box) {
+  const EncodeTiledFn f = encode_fn();
+  if (!f) return false;
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return f(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rank, const_cast<void*>(base), dims, strides, box,
+           es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The maps of one call; the last call's maps are kept and reused when nothing changed.
+template <int NP>
+static bool make_maps(const Plan& plan, const BwdParams& p, BwdMaps* m) {
   using S = BwdTmemShape<NP>;
-  if (cudaFuncSetAttribute(scan_bwd_tmem_kernel<NP, VEC>,
+  struct Key {
+    const void* ptr[8];
+    int64_t dims[4];
+  };
+  static std::mutex mu;
+  static Key last_key;
+  static BwdMaps last_maps;
+  static bool have_last = false;
+  const Key key = {{p.delta, p.u, p.gate, p.dy, p.y_ck, p.B, p.C, p.ckpt},
+                   {plan.batch, plan.T, plan.Di, plan.N}};
+  std::lock_guard<std::mutex> lock(mu);
+  if (have_last && memcmp(&key, &last_key, sizeof(Key)) == 0) {
+    *m = last_maps;
+    return true;
+  }
+  const cuuint64_t Di = plan.Di, T = plan.T, Bt = plan.batch, N = plan.N;
+  const cuuint64_t nck = plan.nchunks - 1;
+  const cuuint64_t dTD[3] = {Di, T, Bt}, sTD[2] = {Di * 4, T * Di * 4};
+  const cuuint32_t bTD[3] = {(cuuint32_t)S::DC, (cuuint32_t)kChunk, 1};
+  const cuuint64_t dTN[3] = {N, T, Bt}, sTN[2] = {N * 4, T * N * 4};
+  const cuuint32_t bTN[3] = {(cuuint32_t)NP, (cuuint32_t)kChunk, 1};
+  const cuuint64_t dCK[4] = {N, Di, nck, Bt}, sCK[3] = {N * 4, Di * N * 4, nck * Di * N * 4};
+  const cuuint32_t bCK[4] = {(cuuint32_t)NP, (cuuint32_t)S::DC, 1, 1};
+  BwdMaps mm;
+  memset(&mm, 0, sizeof(mm));
+  const bool ok = encode_f32(&mm.delta, p.delta, 3, dTD, sTD, bTD) &&
+                  encode_f32(&mm.u, p.u, 3, dTD, sTD, bTD) &&
+                  encode_f32(&mm.gate, p.gate, 3, dTD, sTD, bTD) &&
+                  encode_f32(&mm.dy, p.dy, 3, dTD, sTD, bTD) &&
+                  encode_f32(&mm.y, p.y_ck, 3, dTD, sTD, bTD) &&
+                  encode_f32(&mm.B, p.B, 3, dTN, sTN, bTN) &&
+                  encode_f32(&mm.C, p.C, 3, dTN, sTN, bTN) &&
+                  encode_f32(&mm.ckpt, p.ckpt, 4, dCK, sCK, bCK);
+  if (!ok) return false;
+  *m = mm;
+  last_key = key;
+  last_maps = mm;
+  have_last = true;
+  return true;
+}
+
+unsigned bwd_take_fault() {
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_bwd_fault, sizeof(v)) != cudaSuccess) return 0;
+  if (v) {
+    const unsigned zero = 0;
+    cudaMemcpyToSymbol(g_bwd_fault, &zero, sizeof(zero));
+  }
+  return v;
+}
+
+template <int NP, bool VEC, bool TMA>
+static int launch_main(const Plan& plan, const BwdMaps& maps, const BwdParams& p,
+                       cudaStream_t s) {
+  using S = BwdTmemShape<NP>;
+  if (cudaFuncSetAttribute(scan_bwd_tmem_kernel<NP, VEC, TMA>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)S::kSmemBytes) != cudaSuccess)
     return -1;
   dim3 grid((unsigned)(plan.bwd.nblk * plan.bwd.nseg), (unsigned)plan.batch);
-  scan_bwd_tmem_kernel<NP, VEC><<<grid, kWarps * 32, S::kSmemBytes, s>>>(p);
+  scan_bwd_tmem_kernel<NP, VEC, TMA><<<grid, kWarps * 32, S::kSmemBytes, s>>>(maps, p);
   return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
 }
 
-int launch_bwd_main_tmem(const Plan& plan, const BwdParams& p, cudaStream_t s) {
+// TMA needs 16-byte strides (d_inner and d_state multiples of 4) and a checkpoint tensor
+// (T > 16); otherwise the stages are filled with cp.async.
+template <int NP>
+static int launch_np(const Plan& plan, const BwdParams& p, cudaStream_t s) {
   const bool vec = (plan.Di % 4 == 0) && (plan.N % 4 == 0);
+  BwdMaps maps;
+  if (vec && plan.nchunks >= 2 && make_maps<NP>(plan, p, &maps))
+    return launch_main<NP, true, true>(plan, maps, p, s);
+  memset(&maps, 0, sizeof(maps));
+  return vec ? launch_main<NP, true, false>(plan, maps, p, s)
+             : launch_main<NP, false, false>(plan, maps, p, s);
+}
+
+int launch_bwd_main_tmem(const Plan& plan, const BwdParams& p, cudaStream_t s) {
   switch (plan.NP) {
-    case 16: return vec ? launch_np<16, true>(plan, p, s) : launch_np<16, false>(plan, p, s);
-    case 32: return vec ? launch_np<32, true>(plan, p, s) : launch_np<32, false>(plan, p, s);
-    case 64: return vec ? launch_np<64, true>(plan, p, s) : launch_np<64, false>(plan, p, s);
+    case 16: return launch_np<16>(plan, p, s);
+    case 32: return launch_np<32>(plan, p, s);
+    case 64: return launch_np<64>(plan, p, s);
     default: return -1;
   }
 }

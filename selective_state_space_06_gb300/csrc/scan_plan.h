@@ -1,6 +1,7 @@
 // Internal (not part of the C ABI): launch plan and kernel parameter blocks shared by the
 // host entry points (mamba_scan_abi.cu) and the kernel launchers (scan_fwd.cu, scan_bwd.cu).
 #pragma once
+#include <cuda.h>   // CUtensorMap (the type only)
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -98,6 +99,18 @@ struct BwdParams {
   int batch, T, Di, N, nchunks, nblk, seg_chunks, nseg;
   int sub_chunks, nsub;            // pre-pass sub-segments (see PassPlan)
 };
+
+// TMA descriptors of the tensor-memory backward, encoded on the host for each call:
+// delta, u, gate, dy, y as [batch][T][d_inner] with boxes of 16 steps x DC channels; B, C as
+// [batch][T][d_state] with boxes of 16 steps x NP states; the checkpoints as
+// [batch][chunk][d_inner][d_state] with boxes of DC channels x NP states.
+struct alignas(64) BwdMaps {
+  CUtensorMap delta, u, gate, dy, y, B, C, ckpt;
+};
+
+// Reads and clears the fault word that the backward kernels set when a bounded wait on an
+// asynchronous copy gave up (0: none). Synchronises with the device.
+unsigned bwd_take_fault();
 
 // Each returns the number of kernels enqueued (>= 1) or -1 on a launch error.
 // launch_fwd enqueues the segment pre-pass (when nseg > 1) and the forward scan; launch_bwd

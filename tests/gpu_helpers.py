@@ -35,6 +35,7 @@ def run_gpu(x: dict, poison: bool = True, stream=None) -> dict:
             bufs["ckpt"].fill_(0xFF)
     ms.forward_backward(xd, bufs, stream=stream)
     torch.cuda.synchronize()
+    ms.mamba_scan_status(stream)     # raises on a CUDA error or an expired copy wait
     return {k: bufs[k].cpu().numpy() for k in OUT_KEYS}
 
 

@@ -63,7 +63,7 @@ def test_buffer_sizes(ms):
 
 
 def test_strerror(ms):
-    for code in range(0, 6):
+    for code in range(0, 8):
         assert isinstance(ms.mamba_scan_strerror(code), str) and ms.mamba_scan_strerror(code)
     assert "unknown" in ms.mamba_scan_strerror(99)
 
