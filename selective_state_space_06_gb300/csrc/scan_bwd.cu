@@ -274,19 +274,19 @@ __global__ void scan_bwd_compose_kernel(const BwdParams p) {
     float carry = 0.f;
     for (int sg = p.nseg - 1; sg >= 1; --sg) {
       const float carry_in = carry;
-      // four sub-slots at a time: their loads do not depend on the carry, so they are all in
+      // eight sub-slots at a time: their loads do not depend on the carry, so they are all in
       // flight together (a missing slot reads as L = 0, sum 0: the identity)
-      for (int j0 = p.nsub - 1; j0 >= 0; j0 -= 4) {
-        float Lv[4], sv[4];
+      for (int j0 = p.nsub - 1; j0 >= 0; j0 -= 8) {
+        float Lv[8], sv[8];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < 8; ++k) {
           const int j = j0 - k;
           const size_t row = b * nslot + (size_t)sg * p.nsub + (j >= 0 ? j : 0);
           Lv[k] = j >= 0 ? p.agg_L[row * dn + q] : 0.f;
           sv[k] = j >= 0 ? p.agg_sd[row * p.Di + d] : 0.f;
         }
 #pragma unroll
-        for (int k = 0; k < 4; ++k) carry = fmaf(ex2_sfu(sv[k] * a2), carry, Lv[k]);
+        for (int k = 0; k < 8; ++k) carry = fmaf(ex2_sfu(sv[k] * a2), carry, Lv[k]);
       }
       p.agg_L[(b * nslot + (size_t)sg * p.nsub) * dn + q] = carry_in;
     }

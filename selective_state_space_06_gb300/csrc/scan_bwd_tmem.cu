@@ -565,18 +565,24 @@ struct BwdAgg4Shape {
   static constexpr int kStages = 2;
   // per stage: delta, gate (-> d_y), dy [kChunk][DC]; C [kChunk][NP]
   static constexpr int kStageFloats = 3 * S::TILE + kChunk * NP;
+  static constexpr uint32_t kStageBytes = kStageFloats * sizeof(float);
   static constexpr int kDupFloats = kChunk * NP * 2;   // {C, C} of the current chunk
-  static constexpr size_t kSmemBytes = ((size_t)kStages * kStageFloats + kDupFloats) * sizeof(float);
+  static constexpr size_t kDataFloats = (size_t)kStages * kStageFloats + kDupFloats;
+  static constexpr size_t kSmemBytes = kDataFloats * sizeof(float) + 8 * kStages + 128;
+  static_assert(kStageBytes % 128 == 0, "TMA destinations must stay 128-byte aligned");
 };
 
-template <int NP, bool VEC>
+template <int NP, bool VEC, bool TMA>
 __global__ void __launch_bounds__(kWarps * 32)
-scan_bwd_agg4_kernel(const BwdParams p) {
+scan_bwd_agg4_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
   using S = BwdTmemShape<NP>;
   using A = BwdAgg4Shape<NP>;
   constexpr int G = S::G, LG = S::LG, DW = S::DW, DC = S::DC, TILE = S::TILE;
   constexpr int NTH = kWarps * 32;
-  extern __shared__ __align__(16) float smem[];
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  float* smem = reinterpret_cast<float*>(
+      smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u));   // 128-byte aligned
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + A::kDataFloats);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ng = lane & (G - 1), dg = lane >> LG;
   const int b = blockIdx.y;
@@ -592,6 +598,40 @@ scan_bwd_agg4_kernel(const BwdParams p) {
   const int c_begin = sg * p.seg_chunks + j_sub * p.sub_chunks;
   const int c_end = min(min(p.nchunks, (sg + 1) * p.seg_chunks), c_begin + p.sub_chunks);
   const size_t row0 = (size_t)b * T;
+
+  auto load = [&](int stage, int c) {
+    float* st = smem + stage * A::kStageFloats;
+    if constexpr (TMA) {
+      if (threadIdx.x == 0) {
+        uint64_t* bar = bars + stage;
+        mbar_expect_tx(bar, A::kStageBytes);
+        tma_load_3d(st, &maps.delta, bar, dblk0, c * kChunk, b);
+        tma_load_3d(st + TILE, &maps.gate, bar, dblk0, c * kChunk, b);
+        tma_load_3d(st + 2 * TILE, &maps.dy, bar, dblk0, c * kChunk, b);
+        tma_load_3d(st + 3 * TILE, &maps.C, bar, 0, c * kChunk, b);
+      }
+    } else {
+      stage_tile<DC, NTH, VEC>(st, p.delta, row0, c * kChunk, T, Di, dblk0);
+      stage_tile<DC, NTH, VEC>(st + TILE, p.gate, row0, c * kChunk, T, Di, dblk0);
+      stage_tile<DC, NTH, VEC>(st + 2 * TILE, p.dy, row0, c * kChunk, T, Di, dblk0);
+      stage_tile<NP, NTH, VEC>(st + 3 * TILE, p.C, row0, c * kChunk, T, N, 0);
+      cp_async_commit();
+    }
+  };
+  // the first stage's copies go out before the set-up below
+  if constexpr (TMA) {
+    if (threadIdx.x == 0) {
+#pragma unroll
+      for (int s = 0; s < A::kStages; ++s) mbar_init(bars + s, 1);
+      fence_mbar_init();
+    }
+  }
+#pragma unroll
+  for (int s = 0; s < A::kStages - 1; ++s) {
+    if (c_begin + s < c_end) load(s, c_begin + s);
+    else if constexpr (!TMA) cp_async_commit();
+  }
+  if constexpr (TMA) __syncthreads();   // the barriers are initialised before anyone waits
 
   float2 a2[2][4], L[2][4];
   float2 P2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};   // running sums of delta
@@ -611,36 +651,39 @@ scan_bwd_agg4_kernel(const BwdParams p) {
     }
 
   float* dupC = smem + A::kStages * A::kStageFloats;
-  auto load = [&](int stage, int c) {
-    float* st = smem + stage * A::kStageFloats;
-    stage_tile<DC, NTH, VEC>(st, p.delta, row0, c * kChunk, T, Di, dblk0);
-    stage_tile<DC, NTH, VEC>(st + TILE, p.gate, row0, c * kChunk, T, Di, dblk0);
-    stage_tile<DC, NTH, VEC>(st + 2 * TILE, p.dy, row0, c * kChunk, T, Di, dblk0);
-    stage_tile<NP, NTH, VEC>(st + 3 * TILE, p.C, row0, c * kChunk, T, N, 0);
-    cp_async_commit();
-  };
-#pragma unroll
-  for (int s = 0; s < A::kStages - 1; ++s) {
-    if (c_begin + s < c_end) load(s, c_begin + s);
-    else cp_async_commit();
-  }
   const float4* pC[2] = {reinterpret_cast<const float4*>(dupC + 2 * n0),
                          reinterpret_cast<const float4*>(dupC + 2 * n0 + 4)};
   for (int c = c_begin; c < c_end; ++c) {
     const int it = c - c_begin;
-    cp_async_wait<A::kStages - 2>();
+    if constexpr (TMA) {
+      if (!mbar_wait(bars + it % A::kStages, (uint32_t)((it / A::kStages) & 1)))
+        atomicOr(&g_bwd_fault, 2u);
+    } else {
+      cp_async_wait<A::kStages - 2>();
+    }
     __syncthreads();
     if (c + A::kStages - 1 < c_end) load((it + A::kStages - 1) % A::kStages, c + A::kStages - 1);
-    else cp_async_commit();
+    else if constexpr (!TMA) cp_async_commit();
     float* st = smem + (it % A::kStages) * A::kStageFloats;
     const float* s_dl = st;
     float* s_g = st + TILE;             // becomes d_y
     const float* s_dy = st + 2 * TILE;
     const float* s_C = st + 3 * TILE;
+    if constexpr (VEC) {
+#pragma unroll 2
+      for (int e = 4 * threadIdx.x; e < TILE; e += 4 * NTH) {
+        const float4 g = *reinterpret_cast<const float4*>(s_g + e);
+        const float4 go = *reinterpret_cast<const float4*>(s_dy + e);
+        *reinterpret_cast<float4*>(s_g + e) =
+            make_float4(go.x * (g.x * sigmoid_fast(g.x)), go.y * (g.y * sigmoid_fast(g.y)),
+                        go.z * (g.z * sigmoid_fast(g.z)), go.w * (g.w * sigmoid_fast(g.w)));
+      }
+    } else {
 #pragma unroll 4
-    for (int e = threadIdx.x; e < TILE; e += NTH) {
-      const float g = s_g[e];
-      s_g[e] = s_dy[e] * (g * sigmoid_fast(g));
+      for (int e = threadIdx.x; e < TILE; e += NTH) {
+        const float g = s_g[e];
+        s_g[e] = s_dy[e] * (g * sigmoid_fast(g));
+      }
     }
     for (int e = threadIdx.x; e < kChunk * NP; e += NTH) {
       const float cv = s_C[e];
@@ -667,8 +710,10 @@ scan_bwd_agg4_kernel(const BwdParams p) {
           L[q][s] = fma2(cum, mul2(dy2[q], C2[s]), L[q][s]);
         }
     }
+    // the d_y writes above come before the copies that refill this stage
+    if constexpr (TMA) fence_proxy_async_smem();
   }
-  cp_async_wait<0>();
+  if constexpr (!TMA) cp_async_wait<0>();
   // emit the sub-segment's aggregate (zeros for an empty one)
   const size_t rowbase = ((size_t)b * p.nseg * p.nsub + slot) * Di;
 #pragma unroll
@@ -690,30 +735,6 @@ scan_bwd_agg4_kernel(const BwdParams p) {
           if (n0 + s < N) dst[s] = v[s];
       }
     }
-}
-
-template <int NP, bool VEC>
-static int launch_agg4(const Plan& plan, const BwdParams& p, cudaStream_t s) {
-  using A = BwdAgg4Shape<NP>;
-  if (cudaFuncSetAttribute(scan_bwd_agg4_kernel<NP, VEC>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)A::kSmemBytes) != cudaSuccess)
-    return -1;
-  dim3 grid((unsigned)(plan.bwd.nblk * (plan.bwd.nseg - 1) * plan.bwd.nsub),
-            (unsigned)plan.batch);
-  scan_bwd_agg4_kernel<NP, VEC><<<grid, kWarps * 32, A::kSmemBytes, s>>>(p);
-  return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
-}
-
-int launch_bwd_agg_tmem(const Plan& plan, const BwdParams& p, cudaStream_t s) {
-  if (plan.bwd.nseg <= 1) return 0;
-  const bool vec = (plan.Di % 4 == 0) && (plan.N % 4 == 0);
-  switch (plan.NP) {
-    case 16: return vec ? launch_agg4<16, true>(plan, p, s) : launch_agg4<16, false>(plan, p, s);
-    case 32: return vec ? launch_agg4<32, true>(plan, p, s) : launch_agg4<32, false>(plan, p, s);
-    case 64: return vec ? launch_agg4<64, true>(plan, p, s) : launch_agg4<64, false>(plan, p, s);
-    default: return -1;
-  }
 }
 
 // ---- host side: tensor maps ------------------------------------------------------------------
@@ -822,6 +843,41 @@ static int launch_np(const Plan& plan, const BwdParams& p, cudaStream_t s) {
   memset(&maps, 0, sizeof(maps));
   return vec ? launch_main<NP, true, false>(plan, maps, p, s)
              : launch_main<NP, false, false>(plan, maps, p, s);
+}
+
+template <int NP, bool VEC, bool TMA>
+static int launch_agg4(const Plan& plan, const BwdMaps& maps, const BwdParams& p,
+                       cudaStream_t s) {
+  using A = BwdAgg4Shape<NP>;
+  if (cudaFuncSetAttribute(scan_bwd_agg4_kernel<NP, VEC, TMA>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)A::kSmemBytes) != cudaSuccess)
+    return -1;
+  dim3 grid((unsigned)(plan.bwd.nblk * (plan.bwd.nseg - 1) * plan.bwd.nsub),
+            (unsigned)plan.batch);
+  scan_bwd_agg4_kernel<NP, VEC, TMA><<<grid, kWarps * 32, A::kSmemBytes, s>>>(maps, p);
+  return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
+}
+
+template <int NP>
+static int launch_agg_np(const Plan& plan, const BwdParams& p, cudaStream_t s) {
+  const bool vec = (plan.Di % 4 == 0) && (plan.N % 4 == 0);
+  BwdMaps maps;
+  if (vec && plan.nchunks >= 2 && make_maps<NP>(plan, p, &maps))
+    return launch_agg4<NP, true, true>(plan, maps, p, s);
+  memset(&maps, 0, sizeof(maps));
+  return vec ? launch_agg4<NP, true, false>(plan, maps, p, s)
+             : launch_agg4<NP, false, false>(plan, maps, p, s);
+}
+
+int launch_bwd_agg_tmem(const Plan& plan, const BwdParams& p, cudaStream_t s) {
+  if (plan.bwd.nseg <= 1) return 0;
+  switch (plan.NP) {
+    case 16: return launch_agg_np<16>(plan, p, s);
+    case 32: return launch_agg_np<32>(plan, p, s);
+    case 64: return launch_agg_np<64>(plan, p, s);
+    default: return -1;
+  }
 }
 
 int launch_bwd_main_tmem(const Plan& plan, const BwdParams& p, cudaStream_t s) {
