@@ -121,6 +121,15 @@ def dist_env():
     return ws, rank, local
 
 
+# The roofline is that of one mamba_scan_bwd call, the dominant part of the step.
+BWD_CALL_KERNELS = ("mamba_scan_bwd call: scan_bwd_agg4_kernel + scan_bwd_compose_kernel + "
+                    "scan_bwd_tmem_kernel + scan_reduce_kernel (d_state 16-64)")
+# DRAM bytes read + written by one mamba_scan_bwd call, summed over its kernels, from the ncu
+# capture in profiles/scan_kernels_mamba130m.md (dram__bytes_read.sum + dram__bytes_write.sum;
+# 103.1 + 10.1 + 433.1 + 15.1 MB). Workloads without a capture report null.
+BWD_TRAFFIC_BYTES = {"mamba130m": 561.4e6}
+
+
 def run_gpu(args):
     import torch
     import selective_state_space_06_gb300 as ms
@@ -244,10 +253,10 @@ def run_gpu(args):
                    "parallelism": f"replicas x{ws}"},
         "fwd_ms": 1e3 * fwd_mean_s, "bwd_ms": 1e3 * bwd_mean_s,
         "hbm_frac_step": (mb["total"] / (total_ms * 1e-3 / args.steps) / 1e9) / peaks["hbm_gbs"],
-        "roofline": {"kernel": "mamba_scan_bwd (scan_bwd_kernel + scan_reduce_kernel)",
-                     "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                     "peak_source": peaks["source"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+        "roofline": {"kernel": BWD_CALL_KERNELS, "bound": "hbm", "achieved": achieved,
+                     "peak": peaks["hbm_gbs"], "peak_source": peaks["source"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": BWD_TRAFFIC_BYTES.get(w.name),
                      "algorithmic_bytes_per_launch": mb["bwd"]},
         "gpu_launches": launches,
         "clocks": clocks,

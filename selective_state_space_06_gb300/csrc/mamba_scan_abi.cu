@@ -7,6 +7,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "../../include/mamba_scan.h"
 #include "scan_plan.h"
@@ -134,7 +135,98 @@ int check_dims(int64_t batch, int64_t T, int64_t Di, int64_t N, Plan* plan) {
   return MAMBA_OK;
 }
 
+// Device workspace of mamba_scan_fwd_bwd_host: the whole batch's inputs and outputs, then one
+// set of checkpoint + scratch buffers per slice, then the slices' d_A_log / d_D sums.
+constexpr int kHostSlices = 4;
+
+struct HostLayout {
+  int64_t rows = 0;            // batch rows per slice
+  int nslices = 0;
+  size_t off_in[8], off_out[8], off_ck[kHostSlices], off_sc[kHostSlices], off_part = 0;
+  size_t ck_bytes = 0, sc_bytes = 0, total = 0;
+  size_t dn_pad = 0, dd_pad = 0;   // floats
+};
+
+bool host_layout(int64_t batch, int64_t T, int64_t Di, int64_t N, HostLayout* L) {
+  Plan whole;
+  if (!mscan::make_plan(batch, T, Di, N, &whole)) return false;
+  HostLayout h;
+  // slices start on 16-byte boundaries only when a batch row is a multiple of 4 floats
+  const bool sliceable = (T * Di) % 4 == 0 && (T * N) % 4 == 0;
+  h.nslices = sliceable ? (int)std::min<int64_t>(batch, kHostSlices) : 1;
+  h.rows = (batch + h.nslices - 1) / h.nslices;
+  h.nslices = (int)((batch + h.rows - 1) / h.rows);
+  Plan slice;
+  if (!mscan::make_plan(h.rows, T, Di, N, &slice)) return false;
+  // a shorter last slice needs no more checkpoint or scratch than a full one
+  h.ck_bytes = slice.ckpt_elems * sizeof(float);
+  h.sc_bytes = slice.scratch_elems * sizeof(float);
+  const size_t a = 256;
+  const size_t btd = (size_t)batch * T * Di * 4, btn = (size_t)batch * T * N * 4;
+  // d_A_log | d_D of one slice, each padded to 16 bytes
+  h.dn_pad = round_up((size_t)Di * N, 4);
+  h.dd_pad = round_up((size_t)Di, 4);
+  const size_t dn = (size_t)Di * N * 4, dd = (size_t)Di * 4;
+  const size_t part = (h.dn_pad + h.dd_pad) * 4;
+  const size_t in_sz[8] = {btd, btd, btd, btd, btn, btn, dn, dd};    // delta u gate dy B C A D
+  const size_t out_sz[8] = {btd, btd, btd, btd, btn, btn, part, 0};   // out dd du dg dB dC dA|dD
+  size_t off = 0;
+  for (int i = 0; i < 8; ++i) { h.off_in[i] = off; off = round_up(off + in_sz[i], a); }
+  for (int i = 0; i < 8; ++i) { h.off_out[i] = off; off = round_up(off + out_sz[i], a); }
+  for (int i = 0; i < h.nslices; ++i) {
+    h.off_ck[i] = off; off = round_up(off + h.ck_bytes, a);
+    h.off_sc[i] = off; off = round_up(off + h.sc_bytes, a);
+  }
+  h.off_part = off; off = round_up(off + (size_t)h.nslices * part, a);
+  h.total = off;
+  *L = h;
+  return true;
+}
+
+// The library's extra streams (one per slice after the first) and one event per slice on the
+// current device, created once per device.
+struct AuxStreams {
+  cudaStream_t s[kHostSlices] = {};
+  cudaEvent_t ev[kHostSlices + 1] = {};      // slice done; [kHostSlices]: A_log, D copied
+  cudaEvent_t ev_in[kHostSlices] = {};       // slice's host->device copies done
+  cudaEvent_t ev_out[kHostSlices] = {};      // slice's device->host copies done
+};
+bool aux_streams(AuxStreams* out) {
+  static std::mutex mu;
+  static AuxStreams aux[64];
+  static bool ready[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  AuxStreams& x = aux[dev];
+  if (!ready[dev]) {
+    for (int i = 1; i < kHostSlices; ++i)
+      if (cudaStreamCreateWithFlags(&x.s[i], cudaStreamNonBlocking) != cudaSuccess) return false;
+    for (int i = 0; i <= kHostSlices; ++i)
+      if (cudaEventCreateWithFlags(&x.ev[i], cudaEventDisableTiming) != cudaSuccess) return false;
+    for (int i = 0; i < kHostSlices; ++i)
+      if (cudaEventCreateWithFlags(&x.ev_in[i], cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&x.ev_out[i], cudaEventDisableTiming) != cudaSuccess)
+        return false;
+    ready[dev] = true;
+  }
+  *out = x;
+  return true;
+}
+
 }  // namespace
+
+namespace mscan {
+// out[i] = sum over slices k (in order) of part[k][i]
+__global__ void sum_slices(const float* part, int nslices, size_t n, float* out) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    float acc = 0.f;
+    for (int k = 0; k < nslices; ++k) acc += part[(size_t)k * n + i];
+    out[i] = acc;
+  }
+}
+}  // namespace mscan
 
 extern "C" {
 
@@ -246,17 +338,9 @@ int mamba_scan_bwd(const float* delta, const float* u, const float* B, const flo
 
 size_t mamba_scan_host_workspace_bytes(int64_t batch, int64_t T, int64_t d_inner,
                                        int64_t d_state) {
-  Plan p;
-  if (!mscan::make_plan(batch, T, d_inner, d_state, &p)) return 0;
-  const size_t a = 256;
-  const size_t btd = round_up((size_t)batch * T * d_inner * sizeof(float), a);
-  const size_t btn = round_up((size_t)batch * T * d_state * sizeof(float), a);
-  const size_t dn = round_up((size_t)d_inner * d_state * sizeof(float), a);
-  const size_t dd = round_up((size_t)d_inner * sizeof(float), a);
-  // inputs: delta u gate dy (4 btd), B C (2 btn), A_log, D
-  // outputs: out d_delta d_u d_gate (4 btd), d_B d_C (2 btn), d_A_log, d_D
-  return 8 * btd + 4 * btn + 2 * dn + 2 * dd + round_up(p.ckpt_elems * sizeof(float), a) +
-         round_up(p.scratch_elems * sizeof(float), a);
+  HostLayout L;
+  if (!host_layout(batch, T, d_inner, d_state, &L)) return 0;
+  return L.total;
 }
 
 int mamba_scan_fwd_bwd_host(const float* delta, const float* u, const float* B, const float* C,
@@ -272,54 +356,98 @@ int mamba_scan_fwd_bwd_host(const float* delta, const float* u, const float* B, 
       !d_B || !d_C || !d_A_log || !d_D || !d_gate || !workspace)
     return MAMBA_ERR_INVALID_ARG;
   if (!aligned16(workspace)) return MAMBA_ERR_MISALIGNED;
-  if (workspace_bytes < mamba_scan_host_workspace_bytes(batch, T, d_inner, d_state))
-    return MAMBA_ERR_WORKSPACE;
-  const size_t a = 256;
-  const size_t btd = (size_t)batch * T * d_inner * sizeof(float);
-  const size_t btn = (size_t)batch * T * d_state * sizeof(float);
-  const size_t dn = (size_t)d_inner * d_state * sizeof(float);
-  const size_t dd = (size_t)d_inner * sizeof(float);
+  HostLayout L;
+  if (!host_layout(batch, T, d_inner, d_state, &L)) return MAMBA_ERR_INVALID_ARG;
+  if (workspace_bytes < L.total) return MAMBA_ERR_WORKSPACE;
   char* w = (char*)workspace;
-  auto take = [&](size_t bytes) {
-    char* q = w;
-    w += round_up(bytes, a);
-    return (float*)q;
+  auto at = [&](size_t off) { return (float*)(w + off); };
+  float *w_delta = at(L.off_in[0]), *w_u = at(L.off_in[1]), *w_gate = at(L.off_in[2]),
+        *w_dy = at(L.off_in[3]), *w_B = at(L.off_in[4]), *w_C = at(L.off_in[5]),
+        *w_A = at(L.off_in[6]), *w_D = at(L.off_in[7]);
+  float *w_out = at(L.off_out[0]), *w_dd = at(L.off_out[1]), *w_du = at(L.off_out[2]),
+        *w_dg = at(L.off_out[3]), *w_dB = at(L.off_out[4]), *w_dC = at(L.off_out[5]),
+        *w_dA = at(L.off_out[6]), *w_dD = at(L.off_out[7]);
+  const size_t td = (size_t)T * d_inner, tn = (size_t)T * d_state;
+  const size_t dn = (size_t)d_inner * d_state, dd = (size_t)d_inner;
+
+  // Each slice of the batch runs on its own stream (the caller's for the first, the library's
+  // for the others): its copies in, forward, backward and copies out. So the copies in both
+  // directions overlap each other and the kernels of other slices.
+  cudaStream_t s0 = (cudaStream_t)stream;
+  AuxStreams ax;
+  if (!aux_streams(&ax)) return set_cuda_error(cudaGetLastError());
+  ax.s[0] = s0;
+  auto cp = [&](void* dst, const void* src, size_t n, cudaMemcpyKind k, cudaStream_t st) {
+    return cudaMemcpyAsync(dst, src, n, k, st);
   };
-  float *w_delta = take(btd), *w_u = take(btd), *w_gate = take(btd), *w_dy = take(btd);
-  float *w_B = take(btn), *w_C = take(btn), *w_A = take(dn), *w_D = take(dd);
-  float *w_out = take(btd), *w_dd = take(btd), *w_du = take(btd), *w_dg = take(btd);
-  float *w_dB = take(btn), *w_dC = take(btn), *w_dA = take(dn), *w_dD = take(dd);
-  const size_t ck_bytes = plan.ckpt_elems * sizeof(float);
-  const size_t sc_bytes = plan.scratch_elems * sizeof(float);
-  float* w_ck = take(ck_bytes);
-  float* w_sc = take(sc_bytes);
-  cudaStream_t s = (cudaStream_t)stream;
-  struct Cp { void* dst; const void* src; size_t n; };
-  const Cp h2d[] = {{w_delta, delta, btd}, {w_u, u, btd},   {w_gate, gate, btd},
-                    {w_dy, dy, btd},       {w_B, B, btn},   {w_C, C, btn},
-                    {w_A, A_log, dn},      {w_D, D, dd}};
-  for (const Cp& c : h2d) {
-    cudaError_t e = cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, s);
-    if (e != cudaSuccess) return set_cuda_error(e);
+  cudaError_t e;
+  if ((e = cp(w_A, A_log, dn * 4, cudaMemcpyHostToDevice, s0)) != cudaSuccess ||
+      (e = cp(w_D, D, dd * 4, cudaMemcpyHostToDevice, s0)) != cudaSuccess ||
+      (e = cudaEventRecord(ax.ev[kHostSlices], s0)) != cudaSuccess)
+    return set_cuda_error(e);
+  for (int k = 1; k < L.nslices; ++k)
+    if ((e = cudaStreamWaitEvent(ax.s[k], ax.ev[kHostSlices], 0)) != cudaSuccess)
+      return set_cuda_error(e);
+  int launches = 0;
+  for (int k = 0; k < L.nslices; ++k) {
+    cudaStream_t st = ax.s[k];
+    const int64_t b0 = (int64_t)k * L.rows, nb = std::min<int64_t>(L.rows, batch - b0);
+    const size_t o_td = (size_t)b0 * td, o_tn = (size_t)b0 * tn;
+    const size_t n_td = (size_t)nb * td * 4, n_tn = (size_t)nb * tn * 4;
+    float* ck = at(L.off_ck[k]);
+    float* sc = at(L.off_sc[k]);
+    float* pdA = at(L.off_part) + (size_t)k * (L.dn_pad + L.dd_pad);
+    const struct { float* dst; const float* src; size_t n; } in[] = {
+        {w_delta + o_td, delta + o_td, n_td}, {w_u + o_td, u + o_td, n_td},
+        {w_gate + o_td, gate + o_td, n_td},   {w_dy + o_td, dy + o_td, n_td},
+        {w_B + o_tn, B + o_tn, n_tn},         {w_C + o_tn, C + o_tn, n_tn}};
+    // one slice's copies at a time in each direction (slice order), each at the link's full
+    // rate; the slice's kernels start as soon as its own inputs are in
+    if (k > 0 && (e = cudaStreamWaitEvent(st, ax.ev_in[k - 1], 0)) != cudaSuccess)
+      return set_cuda_error(e);
+    for (const auto& c : in)
+      if ((e = cp(c.dst, c.src, c.n, cudaMemcpyHostToDevice, st)) != cudaSuccess)
+        return set_cuda_error(e);
+    if ((e = cudaEventRecord(ax.ev_in[k], st)) != cudaSuccess) return set_cuda_error(e);
+    rc = mamba_scan_fwd(w_delta + o_td, w_u + o_td, w_B + o_tn, w_C + o_tn, w_gate + o_td, w_A,
+                        w_D, w_out + o_td, nullptr, L.ck_bytes ? ck : nullptr, L.ck_bytes, nb, T,
+                        d_inner, d_state, st);
+    if (rc != MAMBA_OK) return rc;
+    launches += g_last_launches;
+    rc = mamba_scan_bwd(w_delta + o_td, w_u + o_td, w_B + o_tn, w_C + o_tn, w_gate + o_td, w_A,
+                        w_D, w_dy + o_td, L.ck_bytes ? ck : nullptr, L.ck_bytes, sc, L.sc_bytes,
+                        w_dd + o_td, w_du + o_td, w_dB + o_tn, w_dC + o_tn, pdA, pdA + L.dn_pad,
+                        w_dg + o_td, nb, T, d_inner, d_state, st);
+    if (rc != MAMBA_OK) return rc;
+    launches += g_last_launches;
+    const struct { float* dst; const float* src; size_t n; } outs[] = {
+        {out + o_td, w_out + o_td, n_td},     {d_delta + o_td, w_dd + o_td, n_td},
+        {d_u + o_td, w_du + o_td, n_td},      {d_gate + o_td, w_dg + o_td, n_td},
+        {d_B + o_tn, w_dB + o_tn, n_tn},      {d_C + o_tn, w_dC + o_tn, n_tn}};
+    if (k > 0 && (e = cudaStreamWaitEvent(st, ax.ev_out[k - 1], 0)) != cudaSuccess)
+      return set_cuda_error(e);
+    for (const auto& c : outs)
+      if ((e = cp(c.dst, c.src, c.n, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+        return set_cuda_error(e);
+    if ((e = cudaEventRecord(ax.ev_out[k], st)) != cudaSuccess) return set_cuda_error(e);
   }
-  rc = mamba_scan_fwd(w_delta, w_u, w_B, w_C, w_gate, w_A, w_D, w_out, nullptr,
-                      ck_bytes ? w_ck : nullptr, ck_bytes, batch, T, d_inner, d_state, stream);
-  if (rc != MAMBA_OK) return rc;
-  const int nf = g_last_launches;
-  rc = mamba_scan_bwd(w_delta, w_u, w_B, w_C, w_gate, w_A, w_D, w_dy, ck_bytes ? w_ck : nullptr,
-                      ck_bytes, w_sc, sc_bytes, w_dd, w_du, w_dB, w_dC, w_dA, w_dD, w_dg, batch,
-                      T, d_inner, d_state, stream);
-  if (rc != MAMBA_OK) return rc;
-  g_last_launches += nf;
-  const Cp d2h[] = {{out, w_out, btd},   {d_delta, w_dd, btd}, {d_u, w_du, btd},
-                    {d_gate, w_dg, btd}, {d_B, w_dB, btn},     {d_C, w_dC, btn},
-                    {d_A_log, w_dA, dn}, {d_D, w_dD, dd}};
-  for (const Cp& c : d2h) {
-    cudaError_t e = cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyDeviceToHost, s);
-    if (e != cudaSuccess) return set_cuda_error(e);
-  }
-  cudaError_t e = cudaStreamSynchronize(s);
+  // d_A_log and d_D: the slices' sums, added in slice order
+  for (int k = 1; k < L.nslices; ++k)
+    if ((e = cudaEventRecord(ax.ev[k], ax.s[k])) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(s0, ax.ev[k], 0)) != cudaSuccess)
+      return set_cuda_error(e);
+  const size_t npart = L.dn_pad + L.dd_pad;
+  mscan::sum_slices<<<(unsigned)((npart + 255) / 256), 256, 0, s0>>>(at(L.off_part), L.nslices,
+                                                                      npart, w_dA);
+  if ((e = cudaPeekAtLastError()) != cudaSuccess) return set_cuda_error(e);
+  ++launches;
+  if ((e = cp(d_A_log, w_dA, dn * 4, cudaMemcpyDeviceToHost, s0)) != cudaSuccess ||
+      (e = cp(d_D, w_dA + L.dn_pad, dd * 4, cudaMemcpyDeviceToHost, s0)) != cudaSuccess)
+    return set_cuda_error(e);
+  (void)w_dD;
+  e = cudaStreamSynchronize(s0);
   if (e != cudaSuccess) return set_cuda_error(e);
+  g_last_launches = launches;
   if (mscan::bwd_take_fault()) return MAMBA_ERR_TIMEOUT;
   return MAMBA_OK;
 }
