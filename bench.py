@@ -48,6 +48,31 @@ def minimal_bytes(w) -> dict:
     }
 
 
+# Algorithmic compute per (b, t, d, n) of one step (forward + backward): 2 ex2 (the forward's
+# decay and the backward's, recomputed or kept) and about 15 fp32 operations (forward 4,
+# recompute 3, reverse 8), an FMA counting as one operation.
+EX2_PER_ELEMENT_STATE = 2
+FP32_OPS_PER_ELEMENT_STATE = 15
+# Unit counts of the GB300: 152 SMs, 128 fp32 lanes per SM, and an ex2 rate of 32 per clock per
+# SM (measured by a microbenchmark on this GPU); the peaks scale with the sampled SM clock.
+SMS, FP32_LANES_PER_SM, EX2_PER_CLK_PER_SM = 152, 128, 32
+
+
+def alu_roofline(w, step_s: float, sm_mhz: float) -> dict:
+    """Achieved fp32 and ex2 rates of the whole step against the unit-count peaks."""
+    ns = w.btd * w.d_state
+    ghz = sm_mhz / 1e3
+    out = {}
+    for key, per, lanes in (("fp32", FP32_OPS_PER_ELEMENT_STATE, FP32_LANES_PER_SM),
+                            ("ex2", EX2_PER_ELEMENT_STATE, EX2_PER_CLK_PER_SM)):
+        achieved = per * ns / step_s / 1e9
+        peak = SMS * lanes * ghz
+        out[key] = {"achieved": achieved, "peak": peak, "unit": "Gop/s", "frac": achieved / peak,
+                    "ops_per_element_state": per}
+    out["peak_source"] = f"unit counts x sampled SM clock {sm_mhz:.0f} MHz"
+    return out
+
+
 def read_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -258,6 +283,8 @@ def run_gpu(args):
                      "frac": achieved / peaks["hbm_gbs"],
                      "traffic": BWD_TRAFFIC_BYTES.get(w.name),
                      "algorithmic_bytes_per_launch": mb["bwd"]},
+        "alu_roofline": alu_roofline(w, total_ms * 1e-3 / args.steps,
+                                     float(clocks.get("sm_mhz") or 2070.0)),
         "gpu_launches": launches,
         "clocks": clocks,
         "e2e": e2e,
