@@ -45,6 +45,10 @@ def _bind(path):
     lib.mamba_oracle_fwd_rows.restype = ctypes.c_int
     lib.mamba_oracle_bwd_rows.argtypes = [dp] * 8 + [i64] * 6 + [dp] * 7
     lib.mamba_oracle_bwd_rows.restype = ctypes.c_int
+    lib.mamba_oracle_softplus.argtypes = [dp, dp, i64]
+    lib.mamba_oracle_softplus.restype = None
+    lib.mamba_oracle_softplus_bwd.argtypes = [dp, dp, dp, i64]
+    lib.mamba_oracle_softplus_bwd.restype = None
     return lib
 
 
@@ -163,3 +167,30 @@ def loss(x: dict, lib=None) -> float:
     """Scalar loss sum(dy * out) whose gradients ``bwd`` returns."""
     out, _ = fwd(x, lib=lib)
     return float(np.sum(np.asarray(x["dy"], dtype=np.float64) * out))
+
+
+# ---- the softplus before the scan (fused into the CUDA kernels as a variant) ----------------
+def softplus(raw, lib=None) -> np.ndarray:
+    """delta = softplus(raw), threshold 20 (C: mamba_oracle_softplus)."""
+    lib = lib or _load()
+    r = np.ascontiguousarray(raw, dtype=np.float64)
+    out = np.empty_like(r)
+    lib.mamba_oracle_softplus(_p(r), _p(out), r.size)
+    return out
+
+
+def softplus_bwd(raw, d_delta, lib=None) -> np.ndarray:
+    """d_raw from d_delta (C: mamba_oracle_softplus_bwd)."""
+    lib = lib or _load()
+    r = np.ascontiguousarray(raw, dtype=np.float64)
+    g = np.ascontiguousarray(d_delta, dtype=np.float64)
+    out = np.empty_like(r)
+    lib.mamba_oracle_softplus_bwd(_p(r), _p(g), _p(out), r.size)
+    return out
+
+
+def with_softplus(x: dict, lib=None) -> dict:
+    """The inputs of the scan when x carries the raw delta under "delta_raw"."""
+    y = dict(x)
+    y["delta"] = softplus(x["delta_raw"], lib).reshape(np.shape(x["delta_raw"]))
+    return y

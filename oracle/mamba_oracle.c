@@ -156,3 +156,17 @@ int mamba_oracle_bwd_rows(const double* delta, const double* u, const double* Bm
   free(dh);
   return 0;
 }
+
+/* Softplus with the threshold 20 of mamba-rs src/mamba_ssm/cpu/backward.rs ("Softplus
+   backward"): the identity above it, log(1 + e^x) below. */
+void mamba_oracle_softplus(const double* raw, double* delta, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) delta[i] = raw[i] > 20.0 ? raw[i] : log1p(exp(raw[i]));
+}
+
+/* The derivative of softplus is the logistic sigmoid; above the threshold it is 1 (same
+   passage). */
+void mamba_oracle_softplus_bwd(const double* raw, const double* d_delta, double* d_raw,
+                               int64_t n) {
+  for (int64_t i = 0; i < n; ++i)
+    d_raw[i] = raw[i] > 20.0 ? d_delta[i] : d_delta[i] * (1.0 / (1.0 + exp(-raw[i])));
+}

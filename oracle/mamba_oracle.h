@@ -25,6 +25,15 @@ int mamba_oracle_bwd_rows(const double* delta, const double* u, const double* B,
                           double* d_delta, double* d_u, double* d_gate, double* d_B_acc,
                           double* d_C_acc, double* d_A_log_acc, double* d_D_acc);
 
+/* Softplus of the raw delta, element-wise over n values: delta = raw for raw > 20, else
+   log(1 + exp(raw)) (the threshold of mamba-rs src/mamba_ssm/cpu/backward.rs, "Softplus
+   backward"; the forward is the function whose derivative that step takes). */
+void mamba_oracle_softplus(const double* raw, double* delta, int64_t n);
+
+/* Its backward: d_raw = d_delta for raw > 20, else d_delta * sigmoid(raw). */
+void mamba_oracle_softplus_bwd(const double* raw, const double* d_delta, double* d_raw,
+                               int64_t n);
+
 #ifdef __cplusplus
 }
 #endif

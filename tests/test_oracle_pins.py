@@ -152,7 +152,47 @@ def euler_max_err(lib=None):
     return max(abs(a - b) / max(1.0, abs(b)) for a, b in lhs_rhs)
 
 
+def softplus_chain_fd_max_rel_err(lib=None):
+    """The softplus variant end to end: with delta = softplus(raw), finite differences of the
+    loss over every raw element against softplus_bwd(raw, d_delta). Raw values straddle the
+    threshold 20 (the identity branch) and large negative values."""
+    x = _tiny_random(seed=7)
+    rng = np.random.default_rng(7)
+    raw = rng.normal(-1.0, 2.0, size=x["delta"].shape)
+    raw.reshape(-1)[:3] = [24.0, 20.5, -25.0]
+    x["delta_raw"] = raw
+    d_delta = oracle.bwd(oracle.with_softplus(x, lib), lib=lib)["d_delta"]
+    an = oracle.softplus_bwd(raw, d_delta, lib).reshape(-1)
+    scale = max(1.0, float(np.abs(an).max()))
+    flat = raw.reshape(-1)
+    worst = 0.0
+    for i in range(flat.size):
+        orig = flat[i]
+        h = 1e-6 * max(1.0, abs(orig))
+        flat[i] = orig + h
+        lp = oracle.loss(oracle.with_softplus(x, lib), lib=lib)
+        flat[i] = orig - h
+        lm = oracle.loss(oracle.with_softplus(x, lib), lib=lib)
+        flat[i] = orig
+        worst = max(worst, abs((lp - lm) / (2 * h) - an[i]) / scale)
+    return worst
+
+
+def softplus_identity_max_err(lib=None):
+    """softplus(x) - softplus(-x) = x for |x| <= 20 (log(1 + e^x) - log(1 + e^-x) = x), and the
+    identity branch above 20: softplus(x) = x and d_raw = d_delta exactly."""
+    x = np.linspace(-20.0, 20.0, 401)
+    e1 = float(np.abs(oracle.softplus(x, lib) - oracle.softplus(-x, lib) - x).max())
+    hi = np.array([20.0 + 1e-9, 25.0, 80.0])
+    g = np.array([0.3, -1.5, 2.0])
+    e2 = float(np.abs(oracle.softplus(hi, lib) - hi).max())
+    e3 = float(np.abs(oracle.softplus_bwd(hi, g, lib) - g).max())
+    return max(e1, e2, e3)
+
+
 PINS = {
+    "softplus_fd": lambda lib: softplus_chain_fd_max_rel_err(lib) < 1e-6,
+    "softplus_identity": lambda lib: softplus_identity_max_err(lib) < 1e-12,
     "fd": lambda lib: fd_max_rel_err(_tiny_random(), lib=lib) < 1e-6,
     "geo": lambda lib: geo_max_rel_err(lib) < 1e-12,
     "delta0": lambda lib: delta_zero_max_err(lib) < 1e-12,
@@ -173,6 +213,17 @@ def test_fd_all_elements_odd_shape():
 def test_fd_sampled_tiny_workload():
     x = oracle.as64(synth.make_inputs(synth.BY_NAME["tiny"]))
     assert fd_max_rel_err(x, per_tensor=12, seed=1) < 1e-6
+
+
+def test_softplus_chain_finite_differences():
+    assert softplus_chain_fd_max_rel_err() < 1e-6
+
+
+def test_softplus_identity_and_threshold():
+    assert softplus_identity_max_err() < 1e-12
+    # softplus(0) = ln 2 and softplus'(0) = 1/2 (values of the definition at zero)
+    assert abs(oracle.softplus(np.array([0.0]))[0] - np.log(2.0)) < 1e-15
+    assert oracle.softplus_bwd(np.array([0.0]), np.array([1.0]))[0] == 0.5
 
 
 def test_geometric_closed_form():
@@ -284,6 +335,11 @@ MUTANTS = {
     "d_A_log_without_A": ("+= g_h * da * dl * A[n] * hp;", "+= g_h * da * dl * hp;"),
     "B_C_transposed_in_bwd": ("const double bn = Bm[bt * N + n];", "const double bn = Cm[bt * N + n];"),
     "d_u_skip_term_missing": ("double du = dyv * Dp[d];", "double du = 0.0;"),
+    "softplus_grad_sigmoid_of_minus_x": ("d_delta[i] * (1.0 / (1.0 + exp(-raw[i])))",
+                                         "d_delta[i] * (1.0 / (1.0 + exp(raw[i])))"),
+    "softplus_threshold_branch_swapped": ("delta[i] = raw[i] > 20.0 ? raw[i] : log1p(exp(raw[i]));",
+                                          "delta[i] = raw[i] < 20.0 ? raw[i] : log1p(exp(raw[i]));"),
+    "softplus_without_log1p": ("log1p(exp(raw[i]))", "exp(raw[i])"),
     "time_index_off_by_one": ("const double hp = (t > 0) ? H[(t - 1) * N + n] : 0.0;\n        const double hc",
                               "const double hp = (t > 1) ? H[(t - 2) * N + n] : 0.0;\n        const double hc"),
 }
