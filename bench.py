@@ -261,6 +261,38 @@ def run_gpu(args):
                "d2h_bytes_per_step": d2h, "steps": ke, "ms_per_step": 1e3 * el / ke}
         del wsbuf
 
+    # variant: the softplus in front of the scan fused into the kernels (raw delta in,
+    # d_delta_raw out), on the raw delta that gives this workload's delta
+    variants = {}
+    if not args.no_variants:
+        raw_np = np.log(np.expm1(x_np["delta"].astype(np.float64))).astype(np.float32)
+        raw = torch.from_numpy(raw_np).to(dev)
+        del raw_np
+
+        def step_sp():
+            ms.mamba_scan_fwd_softplus(raw, x["u"], x["B"], x["C"], x["gate"], x["A_log"],
+                                       x["D"], bufs["out"], None, bufs["ckpt"], stream=stream)
+            ms.mamba_scan_bwd_softplus(raw, x["u"], x["B"], x["C"], x["gate"], x["A_log"],
+                                       x["D"], x["dy"], bufs["ckpt"], bufs["scratch"],
+                                       bufs["d_delta"], bufs["d_u"], bufs["d_B"], bufs["d_C"],
+                                       bufs["d_A_log"], bufs["d_D"], bufs["d_gate"],
+                                       stream=stream)
+        for _ in range(3):
+            step_sp()
+        kv = max(3, min(args.steps, 50))
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(kv):
+            step_sp()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms_sp = e0.elapsed_time(e1) / kv
+        variants["softplus_fused"] = {"ms_per_step": ms_sp, "value": w.btd / (ms_sp * 1e-3),
+                                      "unit": UNIT, "steps": kv}
+        del raw
+
     mb = minimal_bytes(w)
     peaks = read_peaks()
     bwd_mean_s = float(np.mean(bwd_ms)) * 1e-3
@@ -285,6 +317,7 @@ def run_gpu(args):
                      "algorithmic_bytes_per_launch": mb["bwd"]},
         "alu_roofline": alu_roofline(w, total_ms * 1e-3 / args.steps,
                                      float(clocks.get("sm_mhz") or 2070.0)),
+        "variants": variants,
         "gpu_launches": launches,
         "clocks": clocks,
         "e2e": e2e,
@@ -377,6 +410,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.BY_NAME))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip timing the fused-softplus variant")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
     if args.warmup < 3:

@@ -98,6 +98,26 @@ int mamba_scan_bwd(const float* delta, const float* u, const float* B, const flo
                    float* d_D, float* d_gate, int64_t batch, int64_t T, int64_t d_inner,
                    int64_t d_state, void* stream);
 
+/* The same two passes with the softplus in front of the scan fused into the kernels (the
+ * Softplus backward step of the page, with its threshold 20; the forward applies
+ * delta = raw > 20 ? raw : log(1 + exp(raw)), the function whose derivative that step takes).
+ * `delta_raw` replaces `delta`, with the same layout, in both calls. The backward writes
+ * d_delta_raw = d_delta * (raw > 20 ? 1 : sigmoid(raw)) in place of d_delta. Everything else,
+ * including the checkpoint and scratch sizes and the error codes, is as for mamba_scan_fwd
+ * and mamba_scan_bwd. */
+int mamba_scan_fwd_softplus(const float* delta_raw, const float* u, const float* B,
+                            const float* C, const float* gate, const float* A_log,
+                            const float* D, float* out, float* y, void* ckpt,
+                            size_t ckpt_bytes, int64_t batch, int64_t T, int64_t d_inner,
+                            int64_t d_state, void* stream);
+int mamba_scan_bwd_softplus(const float* delta_raw, const float* u, const float* B,
+                            const float* C, const float* gate, const float* A_log,
+                            const float* D, const float* dy, const void* ckpt,
+                            size_t ckpt_bytes, void* scratch, size_t scratch_bytes,
+                            float* d_delta_raw, float* d_u, float* d_B, float* d_C,
+                            float* d_A_log, float* d_D, float* d_gate, int64_t batch, int64_t T,
+                            int64_t d_inner, int64_t d_state, void* stream);
+
 /* End-to-end call for callers that hold their data in HOST memory (pinned memory lets the
  * copies overlap; pageable memory works too, but more slowly). The call copies the eight
  * inputs host->device into `workspace`, runs the forward and the backward there, copies out

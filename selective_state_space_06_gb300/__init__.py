@@ -42,6 +42,7 @@ EXPORTED = (
     "mamba_scan_ckpt_bytes", "mamba_scan_scratch_bytes", "mamba_scan_fwd", "mamba_scan_bwd",
     "mamba_scan_host_workspace_bytes", "mamba_scan_fwd_bwd_host", "mamba_scan_status",
     "mamba_scan_strerror", "mamba_scan_last_launch_count", "mamba_scan_bwd_noalloc",
+    "mamba_scan_fwd_softplus", "mamba_scan_bwd_softplus",
 )
 
 _vp = ctypes.c_void_p
@@ -58,6 +59,10 @@ _lib.mamba_scan_fwd.argtypes = [_vp] * 10 + [_sz] + [_i64] * 4 + [_vp]
 _lib.mamba_scan_fwd.restype = ctypes.c_int
 _lib.mamba_scan_bwd.argtypes = [_vp] * 9 + [_sz, _vp, _sz] + [_vp] * 7 + [_i64] * 4 + [_vp]
 _lib.mamba_scan_bwd.restype = ctypes.c_int
+_lib.mamba_scan_fwd_softplus.argtypes = _lib.mamba_scan_fwd.argtypes
+_lib.mamba_scan_fwd_softplus.restype = ctypes.c_int
+_lib.mamba_scan_bwd_softplus.argtypes = _lib.mamba_scan_bwd.argtypes
+_lib.mamba_scan_bwd_softplus.restype = ctypes.c_int
 _lib.mamba_scan_bwd_noalloc.argtypes = [_vp] * 9 + [_sz] + [_vp] * 7 + [_i64] * 4 + [_vp]
 _lib.mamba_scan_bwd_noalloc.restype = ctypes.c_int
 _lib.mamba_scan_fwd_bwd_host.argtypes = [_vp] * 17 + [_sz] + [_i64] * 4 + [_vp]
@@ -138,28 +143,36 @@ def _dims(delta, B):
     return int(b), int(T), int(Di), int(B.shape[2])
 
 
-def mamba_scan_fwd(delta, u, B, C, gate, A_log, D, out, y=None, ckpt=None, stream=None):
+def mamba_scan_fwd(delta, u, B, C, gate, A_log, D, out, y=None, ckpt=None, stream=None,
+                   _fn="mamba_scan_fwd"):
     """Forward scan on device tensors. ``ckpt`` is a device buffer (any dtype) of at least
     mamba_scan_ckpt_bytes bytes, or None when that size is 0."""
     b, T, Di, N = _dims(delta, B)
     dev = delta.device
     ck_bytes = 0 if ckpt is None else ckpt.numel() * ckpt.element_size()
-    rc = _lib.mamba_scan_fwd(
+    rc = getattr(_lib, _fn)(
         _ptr(delta, "delta", dev), _ptr(u, "u", dev), _ptr(B, "B", dev), _ptr(C, "C", dev),
         _ptr(gate, "gate", dev), _ptr(A_log, "A_log", dev), _ptr(D, "D", dev),
         _ptr(out, "out", dev), _ptr(y, "y", dev, allow_none=True),
         _ptr(ckpt, "ckpt", dev, allow_none=True), ck_bytes, b, T, Di, N, _stream_ptr(stream, dev))
     if rc != MAMBA_OK:
-        raise MambaScanError(rc, "mamba_scan_fwd")
+        raise MambaScanError(rc, _fn)
+
+
+def mamba_scan_fwd_softplus(delta_raw, u, B, C, gate, A_log, D, out, y=None, ckpt=None,
+                            stream=None):
+    """mamba_scan_fwd with delta = softplus(delta_raw) applied inside the kernels."""
+    mamba_scan_fwd(delta_raw, u, B, C, gate, A_log, D, out, y, ckpt, stream,
+                   _fn="mamba_scan_fwd_softplus")
 
 
 def mamba_scan_bwd(delta, u, B, C, gate, A_log, D, dy, ckpt, scratch, d_delta, d_u, d_B, d_C,
-                   d_A_log, d_D, d_gate, stream=None):
+                   d_A_log, d_D, d_gate, stream=None, _fn="mamba_scan_bwd"):
     """Backward scan on device tensors (all seven gradients are overwritten)."""
     b, T, Di, N = _dims(delta, B)
     dev = delta.device
     ck_bytes = 0 if ckpt is None else ckpt.numel() * ckpt.element_size()
-    rc = _lib.mamba_scan_bwd(
+    rc = getattr(_lib, _fn)(
         _ptr(delta, "delta", dev), _ptr(u, "u", dev), _ptr(B, "B", dev), _ptr(C, "C", dev),
         _ptr(gate, "gate", dev), _ptr(A_log, "A_log", dev), _ptr(D, "D", dev),
         _ptr(dy, "dy", dev), _ptr(ckpt, "ckpt", dev, allow_none=True), ck_bytes,
@@ -168,7 +181,15 @@ def mamba_scan_bwd(delta, u, B, C, gate, A_log, D, dy, ckpt, scratch, d_delta, d
         _ptr(d_C, "d_C", dev), _ptr(d_A_log, "d_A_log", dev), _ptr(d_D, "d_D", dev),
         _ptr(d_gate, "d_gate", dev), b, T, Di, N, _stream_ptr(stream, dev))
     if rc != MAMBA_OK:
-        raise MambaScanError(rc, "mamba_scan_bwd")
+        raise MambaScanError(rc, _fn)
+
+
+def mamba_scan_bwd_softplus(delta_raw, u, B, C, gate, A_log, D, dy, ckpt, scratch, d_delta_raw,
+                            d_u, d_B, d_C, d_A_log, d_D, d_gate, stream=None):
+    """mamba_scan_bwd for the softplus variant: d_delta_raw receives the gradient with respect
+    to the raw delta."""
+    mamba_scan_bwd(delta_raw, u, B, C, gate, A_log, D, dy, ckpt, scratch, d_delta_raw, d_u, d_B,
+                   d_C, d_A_log, d_D, d_gate, stream, _fn="mamba_scan_bwd_softplus")
 
 
 def mamba_scan_bwd_noalloc(delta, u, B, C, gate, A_log, D, dy, ckpt, d_delta, d_u, d_B, d_C,
@@ -236,15 +257,19 @@ def alloc_like_outputs(delta, B, A_log, D):
     }
 
 
-def forward_backward(x: dict, bufs: dict | None = None, with_y: bool = True, stream=None) -> dict:
+def forward_backward(x: dict, bufs: dict | None = None, with_y: bool = True, stream=None,
+                     softplus: bool = False) -> dict:
     """Runs mamba_scan_fwd then mamba_scan_bwd on a dict of device tensors (keys delta, u, B, C,
     gate, A_log, D, dy); returns the dict of outputs (out, y, d_delta, d_u, d_B, d_C, d_A_log,
-    d_D, d_gate plus the ckpt/scratch buffers)."""
+    d_D, d_gate plus the ckpt/scratch buffers). With softplus=True, x["delta"] holds the raw
+    delta, the _softplus entry points run, and bufs["d_delta"] receives d_delta_raw."""
     if bufs is None:
         bufs = alloc_like_outputs(x["delta"], x["B"], x["A_log"], x["D"])
-    mamba_scan_fwd(x["delta"], x["u"], x["B"], x["C"], x["gate"], x["A_log"], x["D"], bufs["out"],
-                   bufs["y"] if with_y else None, bufs["ckpt"], stream=stream)
-    mamba_scan_bwd(x["delta"], x["u"], x["B"], x["C"], x["gate"], x["A_log"], x["D"], x["dy"],
-                   bufs["ckpt"], bufs["scratch"], bufs["d_delta"], bufs["d_u"], bufs["d_B"],
-                   bufs["d_C"], bufs["d_A_log"], bufs["d_D"], bufs["d_gate"], stream=stream)
+    fwd = mamba_scan_fwd_softplus if softplus else mamba_scan_fwd
+    bwd = mamba_scan_bwd_softplus if softplus else mamba_scan_bwd
+    fwd(x["delta"], x["u"], x["B"], x["C"], x["gate"], x["A_log"], x["D"], bufs["out"],
+        bufs["y"] if with_y else None, bufs["ckpt"], stream=stream)
+    bwd(x["delta"], x["u"], x["B"], x["C"], x["gate"], x["A_log"], x["D"], x["dy"],
+        bufs["ckpt"], bufs["scratch"], bufs["d_delta"], bufs["d_u"], bufs["d_B"],
+        bufs["d_C"], bufs["d_A_log"], bufs["d_D"], bufs["d_gate"], stream=stream)
     return bufs

@@ -242,10 +242,10 @@ size_t mamba_scan_scratch_bytes(int64_t batch, int64_t T, int64_t d_inner, int64
   return p.scratch_elems * sizeof(float);
 }
 
-int mamba_scan_fwd(const float* delta, const float* u, const float* B, const float* C,
-                   const float* gate, const float* A_log, const float* D, float* out, float* y,
-                   void* ckpt, size_t ckpt_bytes, int64_t batch, int64_t T, int64_t d_inner,
-                   int64_t d_state, void* stream) {
+static int scan_fwd_impl(const float* delta, const float* u, const float* B, const float* C,
+                         const float* gate, const float* A_log, const float* D, float* out,
+                         float* y, void* ckpt, size_t ckpt_bytes, int64_t batch, int64_t T,
+                         int64_t d_inner, int64_t d_state, void* stream, int softplus) {
   Plan plan;
   int rc = check_dims(batch, T, d_inner, d_state, &plan);
   if (rc != MAMBA_OK) return rc;
@@ -272,18 +272,38 @@ int mamba_scan_fwd(const float* delta, const float* u, const float* B, const flo
   p.batch = (int)batch; p.T = (int)T; p.Di = (int)d_inner; p.N = (int)d_state;
   p.nchunks = plan.nchunks; p.nblk = plan.fwd.nblk;
   p.seg_chunks = plan.fwd.seg_chunks; p.nseg = plan.fwd.nseg;
+  p.agg_k = 1;
+  p.softplus = softplus;
   const int n = mscan::launch_fwd(plan, p, (cudaStream_t)stream);
   if (n < 0) return set_cuda_error(cudaGetLastError());
   g_last_launches = n;
   return MAMBA_OK;
 }
 
-int mamba_scan_bwd(const float* delta, const float* u, const float* B, const float* C,
-                   const float* gate, const float* A_log, const float* D, const float* dy,
-                   const void* ckpt, size_t ckpt_bytes, void* scratch, size_t scratch_bytes,
-                   float* d_delta, float* d_u, float* d_B, float* d_C, float* d_A_log,
-                   float* d_D, float* d_gate, int64_t batch, int64_t T, int64_t d_inner,
+int mamba_scan_fwd(const float* delta, const float* u, const float* B, const float* C,
+                   const float* gate, const float* A_log, const float* D, float* out, float* y,
+                   void* ckpt, size_t ckpt_bytes, int64_t batch, int64_t T, int64_t d_inner,
                    int64_t d_state, void* stream) {
+  return scan_fwd_impl(delta, u, B, C, gate, A_log, D, out, y, ckpt, ckpt_bytes, batch, T,
+                       d_inner, d_state, stream, 0);
+}
+
+int mamba_scan_fwd_softplus(const float* delta_raw, const float* u, const float* B,
+                            const float* C, const float* gate, const float* A_log,
+                            const float* D, float* out, float* y, void* ckpt,
+                            size_t ckpt_bytes, int64_t batch, int64_t T, int64_t d_inner,
+                            int64_t d_state, void* stream) {
+  return scan_fwd_impl(delta_raw, u, B, C, gate, A_log, D, out, y, ckpt, ckpt_bytes, batch, T,
+                       d_inner, d_state, stream, 1);
+}
+
+static int scan_bwd_impl(const float* delta, const float* u, const float* B, const float* C,
+                         const float* gate, const float* A_log, const float* D, const float* dy,
+                         const void* ckpt, size_t ckpt_bytes, void* scratch,
+                         size_t scratch_bytes, float* d_delta, float* d_u, float* d_B,
+                         float* d_C, float* d_A_log, float* d_D, float* d_gate, int64_t batch,
+                         int64_t T, int64_t d_inner, int64_t d_state, void* stream,
+                         int softplus) {
   Plan plan;
   int rc = check_dims(batch, T, d_inner, d_state, &plan);
   if (rc != MAMBA_OK) return rc;
@@ -330,10 +350,34 @@ int mamba_scan_bwd(const float* delta, const float* u, const float* B, const flo
   p.nchunks = plan.nchunks; p.nblk = plan.bwd.nblk;
   p.seg_chunks = plan.bwd.seg_chunks; p.nseg = plan.bwd.nseg;
   p.sub_chunks = plan.bwd.sub_chunks; p.nsub = plan.bwd.nsub;
+  p.softplus = softplus;
   const int n = mscan::launch_bwd(plan, p, (cudaStream_t)stream);
   if (n < 0) return set_cuda_error(cudaGetLastError());
   g_last_launches = n;
   return MAMBA_OK;
+}
+
+int mamba_scan_bwd(const float* delta, const float* u, const float* B, const float* C,
+                   const float* gate, const float* A_log, const float* D, const float* dy,
+                   const void* ckpt, size_t ckpt_bytes, void* scratch, size_t scratch_bytes,
+                   float* d_delta, float* d_u, float* d_B, float* d_C, float* d_A_log,
+                   float* d_D, float* d_gate, int64_t batch, int64_t T, int64_t d_inner,
+                   int64_t d_state, void* stream) {
+  return scan_bwd_impl(delta, u, B, C, gate, A_log, D, dy, ckpt, ckpt_bytes, scratch,
+                       scratch_bytes, d_delta, d_u, d_B, d_C, d_A_log, d_D, d_gate, batch, T,
+                       d_inner, d_state, stream, 0);
+}
+
+int mamba_scan_bwd_softplus(const float* delta_raw, const float* u, const float* B,
+                            const float* C, const float* gate, const float* A_log,
+                            const float* D, const float* dy, const void* ckpt,
+                            size_t ckpt_bytes, void* scratch, size_t scratch_bytes,
+                            float* d_delta_raw, float* d_u, float* d_B, float* d_C,
+                            float* d_A_log, float* d_D, float* d_gate, int64_t batch, int64_t T,
+                            int64_t d_inner, int64_t d_state, void* stream) {
+  return scan_bwd_impl(delta_raw, u, B, C, gate, A_log, D, dy, ckpt, ckpt_bytes, scratch,
+                       scratch_bytes, d_delta_raw, d_u, d_B, d_C, d_A_log, d_D, d_gate, batch,
+                       T, d_inner, d_state, stream, 1);
 }
 
 size_t mamba_scan_host_workspace_bytes(int64_t batch, int64_t T, int64_t d_inner,

@@ -219,6 +219,7 @@ scan_bwd_agg_kernel(const BwdParams p) {
       const float g = s_g[e];
       s_g[e] = s_dy[e] * (g * sigmoid_fast(g));
     }
+    if (p.softplus) softplus_tile<DC, NTH>(st, T - c * kChunk, Di - dblk0);   // raw -> delta
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < kChunk; ++i) {
@@ -420,10 +421,11 @@ scan_bwd_kernel(const BwdParams p) {
         cp_async_commit();
     }
     float* st = smem + (it % kBwdStages) * S::kStageFloats;
+    float* const s_dlw = st;
     const float* s_dl = st;
     const float* s_u = st + kChunk * DC;
     float* s_g = st + 2 * kChunk * DC;    // becomes d_y
-    float* s_dy = st + 3 * kChunk * DC;   // becomes gfac
+    float* s_dy = st + 3 * kChunk * DC;   // becomes d_delta/d_raw (softplus variant)
     const float* s_B = st + 4 * kChunk * DC;
     const float* s_C = s_B + kChunk * NP;
     const float* s_y = s_C + kChunk * NP + DC * NP;
@@ -444,6 +446,9 @@ scan_bwd_kernel(const BwdParams p) {
       const float s = sigmoid_fast(g);
       s_g[e] = go * (g * s);
       st_global_if(p.d_gate + o, go * yv * (s * fmaf(g, 1.f - s, 1.f)), ok);
+      if (p.softplus && ok) {   // raw -> delta, and the factor d_raw / d_delta
+        softplus_both(s_dlw[e], s_dlw[e], s_dy[e]);
+      }
     }
     __syncthreads();
 
@@ -583,7 +588,8 @@ scan_bwd_kernel(const BwdParams p) {
           const float sA = vn[2 * r], sB = vn[2 * r + 1];
           const bool ok = (t < T) && (d < Di);
           const size_t o = (rowb + t) * Di + d;
-          st_global_if(p.d_delta + o, fmaf(sA, kLn2, uu * sB), ok);
+          const float fac = p.softplus ? s_dy[e] : 1.f;
+          st_global_if(p.d_delta + o, fmaf(sA, kLn2, uu * sB) * fac, ok);
           st_global_if(p.d_u + o, fmaf(dyj, Dj, dl * sB), ok);
         }
       }

@@ -55,10 +55,11 @@ struct BwdTmemShape {
   static constexpr uint32_t kStageBytes = kStageFloats * sizeof(float);
   // duplicated B, C [kChunk][NP][2] (and their pair-swapped copies)
   static constexpr int kDupFloats = kChunk * NP * 2 * (SWAP ? 4 : 2);
-  // per-warp d_B / d_C sums of the chunk [kWarps][kChunk][2][NP]; they fit in the dy and y
-  // tiles of the current stage (dead after the gating step) when d_state is 16
+  // per-warp d_B / d_C sums of the chunk [kWarps][kChunk][2][NP]; they fit in the y tile of
+  // the current stage (dead after the gating step) when d_state is 16. (The dy tile then holds
+  // the softplus variant's factor d_raw / d_delta.)
   static constexpr int kRedFloats = kWarps * kChunk * 2 * NP;
-  static constexpr bool RED_ALIAS = kRedFloats <= 2 * TILE;
+  static constexpr bool RED_ALIAS = kRedFloats <= TILE;
   static constexpr size_t kDataFloats =
       (size_t)kTmemStages * kStageFloats + kDupFloats + (RED_ALIAS ? 0 : kRedFloats);
   // + the stage barriers, + slack to align the base to 128 bytes (TMA destinations)
@@ -137,7 +138,7 @@ __device__ __forceinline__ void bwd_tmem_wait_stage(uint64_t* bars, int stage, i
   }
 }
 
-template <int NP, bool VEC, bool TMA>
+template <int NP, bool VEC, bool TMA, bool SP>
 __global__ void __launch_bounds__(kWarps * 32, 2)
 scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
   using S = BwdTmemShape<NP>;
@@ -284,7 +285,7 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
     const float* s_B = st + 5 * TILE;
     const float* s_C = s_B + kChunk * NP;
     const float* s_h0 = s_C + kChunk * NP;
-    float* red = S::RED_ALIAS ? st + 3 * TILE : red_fixed;
+    float* red = S::RED_ALIAS ? st + 4 * TILE : red_fixed;
     float* const red_lane = red + warp * kChunk * 2 * NP + (S::KIND ? mk * NP : 0) + n_res;
     const int t0 = c * kChunk;
 
@@ -313,6 +314,12 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
         }
         *reinterpret_cast<float4*>(s_g + e) = dyo;
         st_global4_if(p.d_gate + (rowb + t0 + i) * Di + dblk0 + col, dgo, ok);
+        if (SP && ok) {   // raw -> delta, and the factor d_raw / d_delta
+          float* dl = const_cast<float*>(s_dl) + e;
+          float* fac = const_cast<float*>(s_dy) + e;
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) softplus_both(dl[k4], dl[k4], fac[k4]);
+        }
       }
     } else {
       static_assert(TILE % NTH == 0, "tile must split evenly over the CTA");
@@ -327,6 +334,9 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
         const float sg = sigmoid_fast(g);
         s_g[e] = go * (g * sg);
         st_global_if(p.d_gate + o, go * yv * (sg * fmaf(g, 1.f - sg, 1.f)), ok);
+        if (SP && ok) {   // raw -> delta, and the factor d_raw / d_delta
+          softplus_both(s_dl[e], const_cast<float*>(s_dl)[e], const_cast<float*>(s_dy)[e]);
+        }
       }
     }
     for (int e = threadIdx.x; e < kChunk * NP; e += NTH) {
@@ -487,7 +497,9 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
         const float dyo = mx ? dy2[0].y : dy2[0].x;
         dD_out = fmaf(dyo, uo, dD_out);
         const size_t o = (size_t)i * Di;
-        st_global_lt(out_dd + o, fmaf(sA, kLn2, uo * sB), i, lim_dd);
+        float ddo = fmaf(sA, kLn2, uo * sB);
+        if constexpr (SP) ddo *= s_dy[i * DC + cl + j_out];   // d_raw = d_delta * softplus'
+        st_global_lt(out_dd + o, ddo, i, lim_dd);
         st_global_lt(out_du + o, fmaf(dyo, D_out, dlo * sB), i, lim_du);
       }
 #pragma unroll
@@ -685,6 +697,7 @@ scan_bwd_agg4_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
         s_g[e] = s_dy[e] * (g * sigmoid_fast(g));
       }
     }
+    if (p.softplus) softplus_tile<DC, NTH>(st, T - c * kChunk, Di - dblk0);   // raw -> delta
     for (int e = threadIdx.x; e < kChunk * NP; e += NTH) {
       const float cv = s_C[e];
       *reinterpret_cast<float2*>(dupC + 2 * e) = make_float2(cv, cv);
@@ -823,12 +836,13 @@ template <int NP, bool VEC, bool TMA>
 static int launch_main(const Plan& plan, const BwdMaps& maps, const BwdParams& p,
                        cudaStream_t s) {
   using S = BwdTmemShape<NP>;
-  if (cudaFuncSetAttribute(scan_bwd_tmem_kernel<NP, VEC, TMA>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto kern = p.softplus ? scan_bwd_tmem_kernel<NP, VEC, TMA, true>
+                         : scan_bwd_tmem_kernel<NP, VEC, TMA, false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)S::kSmemBytes) != cudaSuccess)
     return -1;
   dim3 grid((unsigned)(plan.bwd.nblk * plan.bwd.nseg), (unsigned)plan.batch);
-  scan_bwd_tmem_kernel<NP, VEC, TMA><<<grid, kWarps * 32, S::kSmemBytes, s>>>(maps, p);
+  kern<<<grid, kWarps * 32, S::kSmemBytes, s>>>(maps, p);
   return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
 }
 

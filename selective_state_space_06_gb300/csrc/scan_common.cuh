@@ -82,6 +82,35 @@ __device__ __forceinline__ void st_global_lt(float* p, float v, int a, int b) {
       ::"l"(p), "f"(v), "r"(a), "r"(b) : "memory");
 }
 
+// Softplus of the raw delta with the threshold 20 (the identity above it), and its derivative
+// (the logistic sigmoid; 1 above the threshold), as in the Softplus backward step of mamba-rs
+// src/mamba_ssm/cpu/backward.rs.
+// On the SFU: e = 2^(x log2 e), log(1 + e) = log2(1 + e) ln 2. Below e = 2^-10 the rounding of
+// 1 + e would cost relative accuracy, and the series e (1 - e/2) is used instead (relative
+// error below e^2/3 < 4e-7); above it log2 near 1 is accurate to about 2^-22 absolute, a
+// relative error below 4e-6 of log(1 + e) >= 9.7e-4.
+__device__ __forceinline__ float log1p_of_exp(float e) {
+  return e > 0x1p-10f ? __log2f(1.f + e) * kLn2 : e * fmaf(-0.5f, e, 1.f);
+}
+__device__ __forceinline__ float softplus_f(float x) {
+  return x > 20.f ? x : log1p_of_exp(ex2_sfu(x * kLog2e));
+}
+// Both at once from one e^x; the derivative is e / (1 + e).
+__device__ __forceinline__ void softplus_both(float x, float& sp, float& grad) {
+  const float e = ex2_sfu(x * kLog2e);
+  sp = x > 20.f ? x : log1p_of_exp(e);
+  grad = x > 20.f ? 1.f : __fdividef(e, 1.f + e);
+}
+// In place over a staged [kChunk][TW] tile of raw delta: rows at or past rows_valid and columns
+// at or past cols_valid stay zero (zero delta is an exact no-op of the recurrences).
+template <int TW, int NTH>
+__device__ __forceinline__ void softplus_tile(float* tile, int rows_valid, int cols_valid) {
+  for (int e = threadIdx.x; e < kChunk * TW; e += NTH) {
+    const int i = e / TW, col = e % TW;
+    if (i < rows_valid && col < cols_valid) tile[e] = softplus_f(tile[e]);
+  }
+}
+
 // Compiler-level fence between the steps of a fully unrolled loop: no memory access moves
 // across it, so the loads of later steps are not hoisted (and kept live in registers) early.
 __device__ __forceinline__ void step_fence() { asm volatile("" ::: "memory"); }

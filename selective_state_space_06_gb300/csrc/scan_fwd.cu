@@ -173,7 +173,11 @@ scan_fwd_agg_kernel(const FwdParams p) {
     __syncthreads();
     if (c + A::kStages - 1 < c_end) load((it + A::kStages - 1) % A::kStages, c + A::kStages - 1);
     else cp_async_commit();
-    const float* st = smem + (it % A::kStages) * A::kStageFloats;
+    float* st = smem + (it % A::kStages) * A::kStageFloats;
+    if (p.softplus) {   // raw delta -> delta in shared memory, once per element
+      softplus_tile<DC, NTH>(st, T - c * kChunk, Di - dblk0);
+      __syncthreads();
+    }
     const float* s_dl = st;
     const float* s_u = st + kChunk * DC;
     const float* s_B = st + 2 * kChunk * DC;
@@ -222,7 +226,7 @@ scan_fwd_agg_kernel(const FwdParams p) {
   cp_async_wait<0>();
 }
 
-template <int NP, bool VEC, bool WITH_Y>
+template <int NP, bool VEC, bool WITH_Y, bool SP>
 __global__ void __launch_bounds__(kWarps * 32)
 scan_fwd_kernel(const FwdParams p) {
   using S = FwdShape<NP>;
@@ -317,7 +321,11 @@ scan_fwd_kernel(const FwdParams p) {
       else
         cp_async_commit();
     }
-    const float* st = smem + (it % kFwdStages) * S::kStageFloats;
+    float* st = smem + (it % kFwdStages) * S::kStageFloats;
+    if constexpr (SP) {   // raw delta -> delta in shared memory, once per element
+      softplus_tile<DC, kWarps * 32>(st, p.T - c * kChunk, p.Di - dblk0);
+      __syncthreads();
+    }
     const float* s_dl = st;
     const float* s_u = st + kChunk * DC;
     const float* s_g = st + 2 * kChunk * DC;
@@ -392,7 +400,8 @@ template <int NP, bool VEC, bool WITH_Y>
 static int launch_np(const Plan& plan, const FwdParams& p0, cudaStream_t s) {
   FwdParams p = p0;
   using S = FwdShape<NP>;
-  auto kern = scan_fwd_kernel<NP, VEC, WITH_Y>;
+  auto kern = p0.softplus ? scan_fwd_kernel<NP, VEC, WITH_Y, true>
+                          : scan_fwd_kernel<NP, VEC, WITH_Y, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)S::kSmemBytes) != cudaSuccess)
     return -1;

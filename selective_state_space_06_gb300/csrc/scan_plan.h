@@ -86,6 +86,7 @@ struct FwdParams {
   float* y_ck;                   // y = sum_n C*h + D*u for the backward (inside the ckpt buffer)
   int batch, T, Di, N, nchunks, nblk, seg_chunks, nseg;
   int agg_k;                     // pre-pass: consecutive segments per CTA
+  int softplus;                  // delta holds the raw delta: the kernels apply softplus
 };
 
 struct BwdParams {
@@ -98,6 +99,7 @@ struct BwdParams {
   float* d_B; float* d_C; float* d_A_log; float* d_D;
   int batch, T, Di, N, nchunks, nblk, seg_chunks, nseg;
   int sub_chunks, nsub;            // pre-pass sub-segments (see PassPlan)
+  int softplus;                    // delta holds the raw delta; d_delta receives d_raw
 };
 
 // TMA descriptors of the tensor-memory backward, encoded on the host for each call:

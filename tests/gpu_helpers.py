@@ -20,9 +20,10 @@ def to_device(x: dict, device="cuda"):
     return {k: torch.from_numpy(np.ascontiguousarray(x[k])).to(device) for k in IN_KEYS}
 
 
-def run_gpu(x: dict, poison: bool = True, stream=None) -> dict:
+def run_gpu(x: dict, poison: bool = True, stream=None, softplus: bool = False) -> dict:
     """Forward + backward through the C ABI on cuda:0; outputs are NaN-poisoned first so that
-    an element the kernels never write shows up as a mismatch."""
+    an element the kernels never write shows up as a mismatch. With softplus=True, x["delta"]
+    is the raw delta and the _softplus entry points run (d_delta is then d_delta_raw)."""
     import torch
     import selective_state_space_06_gb300 as ms
     xd = to_device(x)
@@ -33,7 +34,7 @@ def run_gpu(x: dict, poison: bool = True, stream=None) -> dict:
         bufs["scratch"].fill_(0xFF)            # NaN bit patterns in the partial sums
         if bufs["ckpt"] is not None:
             bufs["ckpt"].fill_(0xFF)
-    ms.forward_backward(xd, bufs, stream=stream)
+    ms.forward_backward(xd, bufs, stream=stream, softplus=softplus)
     torch.cuda.synchronize()
     ms.mamba_scan_status(stream)     # raises on a CUDA error or an expired copy wait
     return {k: bufs[k].cpu().numpy() for k in OUT_KEYS}
