@@ -49,6 +49,10 @@ def _bind(path):
     lib.mamba_oracle_softplus.restype = None
     lib.mamba_oracle_softplus_bwd.argtypes = [dp, dp, dp, i64]
     lib.mamba_oracle_softplus_bwd.restype = None
+    lib.mamba_oracle_conv_fwd.argtypes = [dp] * 3 + [i64] * 4 + [dp, dp]
+    lib.mamba_oracle_conv_fwd.restype = ctypes.c_int
+    lib.mamba_oracle_conv_bwd.argtypes = [dp] * 4 + [i64] * 4 + [dp] * 3
+    lib.mamba_oracle_conv_bwd.restype = ctypes.c_int
     return lib
 
 
@@ -194,3 +198,37 @@ def with_softplus(x: dict, lib=None) -> dict:
     y = dict(x)
     y["delta"] = softplus(x["delta_raw"], lib).reshape(np.shape(x["delta_raw"]))
     return y
+
+
+# ---- causal depthwise conv1d + SiLU (the step before the scan) ------------------------------
+def conv_fwd(x, w, bias, lib=None):
+    """u = SiLU(causal depthwise conv1d(x) + bias) (C: mamba_oracle_conv_fwd); returns (u, pre)."""
+    lib = lib or _load()
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    bias = np.ascontiguousarray(bias, dtype=np.float64)
+    b, T, Di = x.shape
+    K = w.shape[1]
+    u = np.empty_like(x)
+    pre = np.empty_like(x)
+    rc = lib.mamba_oracle_conv_fwd(_p(x), _p(w), _p(bias), b, T, Di, K, _p(u), _p(pre))
+    assert rc == 0, rc
+    return u, pre
+
+
+def conv_bwd(x, w, bias, d_u, lib=None) -> dict:
+    """d_x, d_w, d_bias of the conv + SiLU (C: mamba_oracle_conv_bwd)."""
+    lib = lib or _load()
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    bias = np.ascontiguousarray(bias, dtype=np.float64)
+    d_u = np.ascontiguousarray(d_u, dtype=np.float64)
+    b, T, Di = x.shape
+    K = w.shape[1]
+    d_x = np.empty_like(x)
+    d_w = np.empty_like(w)
+    d_b = np.empty_like(bias)
+    rc = lib.mamba_oracle_conv_bwd(_p(x), _p(w), _p(bias), _p(d_u), b, T, Di, K, _p(d_x),
+                                   _p(d_w), _p(d_b))
+    assert rc == 0, rc
+    return {"d_x": d_x, "d_w": d_w, "d_bias": d_b}

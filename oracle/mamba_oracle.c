@@ -170,3 +170,73 @@ void mamba_oracle_softplus_bwd(const double* raw, const double* d_delta, double*
   for (int64_t i = 0; i < n; ++i)
     d_raw[i] = raw[i] > 20.0 ? d_delta[i] : d_delta[i] * (1.0 / (1.0 + exp(-raw[i])));
 }
+
+/* ---- causal depthwise conv1d + SiLU (the step before the scan) ---------------------------- */
+/* Forward: the shift register of the last K inputs of channel d, dotted with w[d, :]. */
+int mamba_oracle_conv_fwd(const double* x, const double* w, const double* bias, int64_t batch,
+                          int64_t T, int64_t d_inner, int64_t K, double* u, double* pre) {
+  if (batch < 1 || T < 1 || d_inner < 1 || K < 1 || !x || !w || !bias || !u) return 1;
+  for (int64_t b = 0; b < batch; ++b)
+    for (int64_t d = 0; d < d_inner; ++d)
+      for (int64_t t = 0; t < T; ++t) {
+        double acc = bias[d];
+        for (int64_t j = 0; j < K; ++j) {
+          const int64_t ts = t - (K - 1) + j;
+          if (ts >= 0) acc += w[d * K + j] * x[(b * T + ts) * d_inner + d];
+        }
+        const double s = 1.0 / (1.0 + exp(-acc));
+        const int64_t i = (b * T + t) * d_inner + d;
+        u[i] = acc * s;
+        if (pre) pre[i] = acc;
+      }
+  return 0;
+}
+
+/* Backward (Phase B6): SiLU backward for every t, then the reverse pass with the carry. The
+   carry of channel d holds, for the next (earlier) step, sum_{m>=1} d_pre[t+m] * w[d, K-1-m];
+   it shifts by one tap per step. */
+int mamba_oracle_conv_bwd(const double* x, const double* w, const double* bias,
+                          const double* d_u, int64_t batch, int64_t T, int64_t d_inner,
+                          int64_t K, double* d_x, double* d_w, double* d_bias) {
+  if (batch < 1 || T < 1 || d_inner < 1 || K < 1 || !x || !w || !bias || !d_u || !d_x || !d_w ||
+      !d_bias)
+    return 1;
+  double* pre = (double*)malloc(sizeof(double) * (size_t)(batch * T * d_inner));
+  double* u = (double*)malloc(sizeof(double) * (size_t)(batch * T * d_inner));
+  double* carry = (double*)calloc((size_t)(K > 1 ? K - 1 : 1), sizeof(double));
+  if (!pre || !u || !carry) {
+    free(pre); free(u); free(carry);
+    return 2;
+  }
+  mamba_oracle_conv_fwd(x, w, bias, batch, T, d_inner, K, u, pre);
+  for (int64_t i = 0; i < d_inner * K; ++i) d_w[i] = 0.0;
+  for (int64_t d = 0; d < d_inner; ++d) d_bias[d] = 0.0;
+  for (int64_t b = 0; b < batch; ++b)
+    for (int64_t d = 0; d < d_inner; ++d) {
+      for (int64_t k = 0; k + 1 < K; ++k) carry[k] = 0.0;
+      for (int64_t t = T - 1; t >= 0; --t) {
+        const int64_t i = (b * T + t) * d_inner + d;
+        const double p = pre[i];
+        const double s = 1.0 / (1.0 + exp(-p));
+        const double dp = d_u[i] * s * (1.0 + p * (1.0 - s));
+        /* this step's tap and the parameter gradients (the register holds x[t-K+1 .. t]) */
+        double dx = dp * w[d * K + (K - 1)];
+        for (int64_t j = 0; j < K; ++j) {
+          const int64_t ts = t - (K - 1) + j;
+          if (ts >= 0) d_w[d * K + j] += dp * x[(b * T + ts) * d_inner + d];
+        }
+        d_bias[d] += dp;
+        /* carry from later steps, then shift it and add this step's taps for earlier steps */
+        if (K > 1) {
+          dx += carry[0];
+          for (int64_t k = 0; k + 2 < K; ++k) carry[k] = carry[k + 1] + dp * w[d * K + (K - 2 - k)];
+          carry[K - 2] = dp * w[d * K + 0];
+        }
+        d_x[i] = dx;
+      }
+    }
+  free(pre);
+  free(u);
+  free(carry);
+  return 0;
+}

@@ -34,6 +34,22 @@ void mamba_oracle_softplus(const double* raw, double* delta, int64_t n);
 void mamba_oracle_softplus_bwd(const double* raw, const double* d_delta, double* d_raw,
                                int64_t n);
 
+/* Causal depthwise conv1d + SiLU, the step before the scan (mamba-rs
+   src/mamba_ssm/cpu/backward.rs, Phase B6 is its backward). Forward, per (b, d):
+     pre[t] = bias[d] + sum_{j<K} w[d, j] * x[t - (K-1) + j]     (x = 0 before t = 0)
+     u[t]   = pre[t] * sigmoid(pre[t])
+   x, u, pre: [batch, T, d_inner]; w: [d_inner, K]; bias: [d_inner]. pre may be NULL. */
+int mamba_oracle_conv_fwd(const double* x, const double* w, const double* bias, int64_t batch,
+                          int64_t T, int64_t d_inner, int64_t K, double* u, double* pre);
+
+/* Backward, following Phase B6: d_pre = d_u * s * (1 + pre * (1 - s)); then, in reverse time,
+   the current tap d_x[t] = d_pre[t] * w[d, K-1] plus the shift-register carry of later steps,
+   and d_w[d, j] += d_pre[t] * x[t - (K-1) + j], d_bias[d] += d_pre[t]. d_x is written; d_w and
+   d_bias are OVERWRITTEN with the sums over (b, t). */
+int mamba_oracle_conv_bwd(const double* x, const double* w, const double* bias,
+                          const double* d_u, int64_t batch, int64_t T, int64_t d_inner,
+                          int64_t K, double* d_x, double* d_w, double* d_bias);
+
 #ifdef __cplusplus
 }
 #endif

@@ -190,7 +190,55 @@ def softplus_identity_max_err(lib=None):
     return max(e1, e2, e3)
 
 
+def conv_fd_max_rel_err(lib=None, K=4, shape=(2, 9, 3), seed=11):
+    """Causal conv1d + SiLU: finite differences of sum(d_u * u) over every element of x, w and
+    bias against the oracle's backward (Phase B6 with its shift-register carry)."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal(shape)
+    w = rng.standard_normal((shape[2], K)) * 0.7
+    bias = rng.standard_normal(shape[2]) * 0.3
+    d_u = rng.standard_normal(shape)
+    g = oracle.conv_bwd(x, w, bias, d_u, lib)
+
+    def loss():
+        return float(np.sum(d_u * oracle.conv_fwd(x, w, bias, lib)[0]))
+    worst = 0.0
+    for arr, key in ((x, "d_x"), (w, "d_w"), (bias, "d_bias")):
+        an = g[key].reshape(-1)
+        scale = max(1.0, float(np.abs(an).max()))
+        flat = arr.reshape(-1)
+        for i in range(flat.size):
+            orig = flat[i]
+            h = 1e-6 * max(1.0, abs(orig))
+            flat[i] = orig + h
+            lp = loss()
+            flat[i] = orig - h
+            lm = loss()
+            flat[i] = orig
+            worst = max(worst, abs((lp - lm) / (2 * h) - an[i]) / scale)
+    return worst
+
+
+def conv_impulse_max_err(lib=None, K=4):
+    """A unit impulse at step t0 with zero bias: pre[t0 + m] = w[d, K-1-m] for m < K and 0
+    elsewhere (a causal filter's impulse response); u = pre * sigmoid(pre)."""
+    T, Di, t0 = 10, 2, 3
+    w = np.arange(1, Di * K + 1, dtype=np.float64).reshape(Di, K) / 7.0
+    x = np.zeros((1, T, Di))
+    x[0, t0, :] = 1.0
+    u, pre = oracle.conv_fwd(x, w, np.zeros(Di), lib)
+    want = np.zeros((T, Di))
+    for m in range(K):
+        want[t0 + m] = w[:, K - 1 - m]
+    e1 = float(np.abs(pre[0] - want).max())
+    e2 = float(np.abs(u[0] - want / (1.0 + np.exp(-want))).max())
+    return max(e1, e2)
+
+
 PINS = {
+    "conv_fd": lambda lib: conv_fd_max_rel_err(lib) < 1e-6,
+    "conv_fd_k2": lambda lib: conv_fd_max_rel_err(lib, K=2, shape=(1, 6, 2), seed=5) < 1e-6,
+    "conv_impulse": lambda lib: conv_impulse_max_err(lib) < 1e-14,
     "softplus_fd": lambda lib: softplus_chain_fd_max_rel_err(lib) < 1e-6,
     "softplus_identity": lambda lib: softplus_identity_max_err(lib) < 1e-12,
     "fd": lambda lib: fd_max_rel_err(_tiny_random(), lib=lib) < 1e-6,
@@ -224,6 +272,33 @@ def test_softplus_identity_and_threshold():
     # softplus(0) = ln 2 and softplus'(0) = 1/2 (values of the definition at zero)
     assert abs(oracle.softplus(np.array([0.0]))[0] - np.log(2.0)) < 1e-15
     assert oracle.softplus_bwd(np.array([0.0]), np.array([1.0]))[0] == 0.5
+
+
+def test_conv_finite_differences():
+    assert conv_fd_max_rel_err() < 1e-6
+    assert conv_fd_max_rel_err(K=2, shape=(1, 6, 2), seed=5) < 1e-6
+    assert conv_fd_max_rel_err(K=1, shape=(2, 5, 3), seed=6) < 1e-6
+
+
+def test_conv_impulse_response():
+    assert conv_impulse_max_err() < 1e-14
+    assert conv_impulse_max_err(K=3) < 1e-14
+
+
+def test_conv_kernel_size_one_is_pointwise():
+    """K = 1: pre = w*x + b per element, so d_x = d_pre * w exactly as a product."""
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal((2, 4, 3))
+    w = rng.standard_normal((3, 1))
+    b = rng.standard_normal(3)
+    du = rng.standard_normal((2, 4, 3))
+    u, pre = oracle.conv_fwd(x, w, b)
+    assert np.allclose(pre, x * w[:, 0] + b, rtol=0, atol=1e-14)
+    g = oracle.conv_bwd(x, w, b, du)
+    s = 1.0 / (1.0 + np.exp(-pre))
+    dp = du * (s * (1 - pre * s) + pre * s)    # d/dp [p * sigmoid(p)], expanded differently
+    assert np.allclose(g["d_x"], dp * w[:, 0], rtol=1e-12, atol=1e-14)
+    assert np.allclose(g["d_bias"], dp.sum(axis=(0, 1)), rtol=1e-12, atol=1e-14)
 
 
 def test_geometric_closed_form():
@@ -340,6 +415,11 @@ MUTANTS = {
     "softplus_threshold_branch_swapped": ("delta[i] = raw[i] > 20.0 ? raw[i] : log1p(exp(raw[i]));",
                                           "delta[i] = raw[i] < 20.0 ? raw[i] : log1p(exp(raw[i]));"),
     "softplus_without_log1p": ("log1p(exp(raw[i]))", "exp(raw[i])"),
+    "conv_carry_taps_reversed": ("carry[k + 1] + dp * w[d * K + (K - 2 - k)];",
+                                 "carry[k + 1] + dp * w[d * K + (k + 1)];"),
+    "conv_carry_not_added": ("dx += carry[0];", "dx += 0.0;"),
+    "conv_causal_window_shifted": ("const int64_t ts = t - (K - 1) + j;\n          if (ts >= 0) acc",
+                                   "const int64_t ts = t - K + j;\n          if (ts >= 0) acc"),
     "time_index_off_by_one": ("const double hp = (t > 0) ? H[(t - 1) * N + n] : 0.0;\n        const double hc",
                               "const double hp = (t > 1) ? H[(t - 2) * N + n] : 0.0;\n        const double hc"),
 }
