@@ -155,6 +155,44 @@ BWD_CALL_KERNELS = ("mamba_scan_bwd call: scan_bwd_agg4_kernel + scan_bwd_compos
 BWD_TRAFFIC_BYTES = {"mamba130m": 561.4e6}
 
 
+def time_conv(ms, w, dev, stream, steps, hbm_gbs, K=4) -> dict:
+    """The causal conv1d + SiLU step before the scan (d_conv 4) on this workload's
+    [batch, T, d_inner]: CUDA-event times of its forward and backward, and their fractions of
+    HBM against the minimal bytes (fwd reads x, writes u; bwd reads x and d_u, writes d_x)."""
+    import torch
+    b, T, Di = w.batch, w.T, w.d_inner
+    g = torch.Generator(device=dev).manual_seed(0)
+    x = torch.randn(b, T, Di, device=dev, generator=g)
+    d_u = torch.randn(b, T, Di, device=dev, generator=g)
+    wt = torch.randn(Di, K, device=dev, generator=g) * 0.5
+    bias = torch.randn(Di, device=dev, generator=g) * 0.3
+    u, d_x = torch.empty_like(x), torch.empty_like(x)
+    d_w, d_b = torch.empty_like(wt), torch.empty_like(bias)
+    sc = torch.empty(ms.mamba_conv_scratch_bytes(b, T, Di, K) // 4, device=dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    for _ in range(3):
+        ms.mamba_conv_fwd(x, wt, bias, u, stream=stream)
+        ms.mamba_conv_bwd(x, wt, bias, d_u, sc, d_x, d_w, d_b, stream=stream)
+    fwd_ms = bwd_ms = 0.0
+    for _ in range(steps):
+        ev[0].record(stream)
+        ms.mamba_conv_fwd(x, wt, bias, u, stream=stream)
+        ev[1].record(stream)
+        ms.mamba_conv_bwd(x, wt, bias, d_u, sc, d_x, d_w, d_b, stream=stream)
+        ev[2].record(stream)
+        torch.cuda.synchronize()
+        fwd_ms += ev[0].elapsed_time(ev[1])
+        bwd_ms += ev[1].elapsed_time(ev[2])
+    fwd_ms /= steps
+    bwd_ms /= steps
+    btd = b * T * Di
+    fwd_bytes = 4 * (2 * btd + Di * K + Di)
+    bwd_bytes = 4 * (3 * btd + 2 * Di * K + 2 * Di)
+    return {"d_conv": K, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "steps": steps,
+            "fwd_hbm_frac": fwd_bytes / (fwd_ms * 1e-3) / 1e9 / hbm_gbs,
+            "bwd_hbm_frac": bwd_bytes / (bwd_ms * 1e-3) / 1e9 / hbm_gbs}
+
+
 def run_gpu(args):
     import torch
     import selective_state_space_06_gb300 as ms
@@ -292,6 +330,7 @@ def run_gpu(args):
         variants["softplus_fused"] = {"ms_per_step": ms_sp, "value": w.btd / (ms_sp * 1e-3),
                                       "unit": UNIT, "steps": kv}
         del raw
+        variants["conv1d_silu"] = time_conv(ms, w, dev, stream, kv, read_peaks()["hbm_gbs"])
 
     mb = minimal_bytes(w)
     peaks = read_peaks()

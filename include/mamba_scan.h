@@ -118,6 +118,23 @@ int mamba_scan_bwd_softplus(const float* delta_raw, const float* u, const float*
                             float* d_A_log, float* d_D, float* d_gate, int64_t batch, int64_t T,
                             int64_t d_inner, int64_t d_state, void* stream);
 
+/* Causal depthwise conv1d + SiLU, the step that feeds u to the scan (the page's Phase B6 is
+ * its backward):
+ *   pre[b,t,d] = bias[d] + sum_{j<d_conv} w[d,j] * x[b, t-(d_conv-1)+j, d]  (x = 0 before t=0)
+ *   u[b,t,d]   = pre * sigmoid(pre)
+ * x, u, d_u, d_x: [batch, T, d_inner]; w, d_w: [d_inner, d_conv]; bias, d_bias: [d_inner];
+ * device pointers, 16-byte aligned; 1 <= d_conv <= 8 (else MAMBA_ERR_UNSUPPORTED). The
+ * backward recomputes pre from x and OVERWRITES d_x, d_w and d_bias (d_w and d_bias summed over
+ * batch and time in a fixed order: deterministic). Its scratch holds
+ * mamba_conv_scratch_bytes(...) bytes of per-run partials. Asynchronous on `stream`; the return
+ * codes are those above. */
+size_t mamba_conv_scratch_bytes(int64_t batch, int64_t T, int64_t d_inner, int64_t d_conv);
+int mamba_conv_fwd(const float* x, const float* w, const float* bias, float* u, int64_t batch,
+                   int64_t T, int64_t d_inner, int64_t d_conv, void* stream);
+int mamba_conv_bwd(const float* x, const float* w, const float* bias, const float* d_u,
+                   void* scratch, size_t scratch_bytes, float* d_x, float* d_w, float* d_bias,
+                   int64_t batch, int64_t T, int64_t d_inner, int64_t d_conv, void* stream);
+
 /* End-to-end call for callers that hold their data in HOST memory (pinned memory lets the
  * copies overlap; pageable memory works too, but more slowly). The call copies the eight
  * inputs host->device into `workspace`, runs the forward and the backward there, copies out

@@ -43,6 +43,7 @@ EXPORTED = (
     "mamba_scan_host_workspace_bytes", "mamba_scan_fwd_bwd_host", "mamba_scan_status",
     "mamba_scan_strerror", "mamba_scan_last_launch_count", "mamba_scan_bwd_noalloc",
     "mamba_scan_fwd_softplus", "mamba_scan_bwd_softplus",
+    "mamba_conv_scratch_bytes", "mamba_conv_fwd", "mamba_conv_bwd",
 )
 
 _vp = ctypes.c_void_p
@@ -59,6 +60,12 @@ _lib.mamba_scan_fwd.argtypes = [_vp] * 10 + [_sz] + [_i64] * 4 + [_vp]
 _lib.mamba_scan_fwd.restype = ctypes.c_int
 _lib.mamba_scan_bwd.argtypes = [_vp] * 9 + [_sz, _vp, _sz] + [_vp] * 7 + [_i64] * 4 + [_vp]
 _lib.mamba_scan_bwd.restype = ctypes.c_int
+_lib.mamba_conv_scratch_bytes.argtypes = [_i64] * 4
+_lib.mamba_conv_scratch_bytes.restype = _sz
+_lib.mamba_conv_fwd.argtypes = [_vp] * 4 + [_i64] * 4 + [_vp]
+_lib.mamba_conv_fwd.restype = ctypes.c_int
+_lib.mamba_conv_bwd.argtypes = [_vp] * 5 + [_sz] + [_vp] * 3 + [_i64] * 4 + [_vp]
+_lib.mamba_conv_bwd.restype = ctypes.c_int
 _lib.mamba_scan_fwd_softplus.argtypes = _lib.mamba_scan_fwd.argtypes
 _lib.mamba_scan_fwd_softplus.restype = ctypes.c_int
 _lib.mamba_scan_bwd_softplus.argtypes = _lib.mamba_scan_bwd.argtypes
@@ -255,6 +262,37 @@ def alloc_like_outputs(delta, B, A_log, D):
         "d_delta": e(b, T, Di), "d_u": e(b, T, Di), "d_gate": e(b, T, Di),
         "d_B": e(b, T, N), "d_C": e(b, T, N), "d_A_log": e(Di, N), "d_D": e(Di),
     }
+
+
+# ---- causal depthwise conv1d + SiLU (the step before the scan) -------------------------------
+def mamba_conv_scratch_bytes(batch: int, T: int, d_inner: int, d_conv: int) -> int:
+    return int(_lib.mamba_conv_scratch_bytes(batch, T, d_inner, d_conv))
+
+
+def mamba_conv_fwd(x, w, bias, u, stream=None):
+    """u = SiLU(causal depthwise conv1d(x, w) + bias); x, u [batch, T, d_inner], w
+    [d_inner, d_conv], bias [d_inner] (device tensors)."""
+    b, T, Di = x.shape
+    K = w.shape[1]
+    dev = x.device
+    rc = _lib.mamba_conv_fwd(_ptr(x, "x", dev), _ptr(w, "w", dev), _ptr(bias, "bias", dev),
+                             _ptr(u, "u", dev), b, T, Di, K, _stream_ptr(stream, dev))
+    if rc != MAMBA_OK:
+        raise MambaScanError(rc, "mamba_conv_fwd")
+
+
+def mamba_conv_bwd(x, w, bias, d_u, scratch, d_x, d_w, d_bias, stream=None):
+    """Backward of mamba_conv_fwd: d_x, d_w, d_bias (overwritten) from d_u."""
+    b, T, Di = x.shape
+    K = w.shape[1]
+    dev = x.device
+    rc = _lib.mamba_conv_bwd(_ptr(x, "x", dev), _ptr(w, "w", dev), _ptr(bias, "bias", dev),
+                             _ptr(d_u, "d_u", dev), _ptr(scratch, "scratch", dev),
+                             scratch.numel() * scratch.element_size(), _ptr(d_x, "d_x", dev),
+                             _ptr(d_w, "d_w", dev), _ptr(d_bias, "d_bias", dev), b, T, Di, K,
+                             _stream_ptr(stream, dev))
+    if rc != MAMBA_OK:
+        raise MambaScanError(rc, "mamba_conv_bwd")
 
 
 def forward_backward(x: dict, bufs: dict | None = None, with_y: bool = True, stream=None,

@@ -19,7 +19,7 @@ def _header_functions():
     with open(os.path.join(ROOT, "include", "mamba_scan.h")) as f:
         src = f.read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(mamba_scan_\w+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(mamba_(?:scan|conv)_\w+)\s*\(", src)))
 
 
 @pytest.fixture(scope="module")
