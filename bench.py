@@ -139,6 +139,22 @@ class ClockSampler:
                 "sm_max_mhz": num(inside[0][2]), "reasons": reasons, "samples": len(inside)}
 
 
+def max_over_ranks(pg, value: float, device) -> float:
+    """The largest of every rank's value: a replicated job takes as long as its slowest rank.
+    pg is torch.distributed (any backend) or None for one rank."""
+    if pg is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], device=device, dtype=torch.float64)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world_size: int, seconds: float) -> float:
+    """Whole-job throughput of world_size replicas that each process units_per_rank units."""
+    return world_size * units_per_rank / seconds
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -257,10 +273,7 @@ def run_gpu(args):
     total_ms = outer0.elapsed_time(outer1)
     fwd_ms = [starts[i].elapsed_time(mids[i]) for i in range(args.steps)]
     bwd_ms = [mids[i].elapsed_time(ends[i]) for i in range(args.steps)]
-    if pg:
-        t = torch.tensor([total_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(pg, total_ms, dev)
 
     # end-to-end through the host-buffer entry point (pinned host memory)
     e2e = None
@@ -289,13 +302,11 @@ def run_gpu(args):
         for _ in range(ke):
             e2e_step()
         el = time.perf_counter() - t0
-        if pg:
-            t = torch.tensor([el], device=dev)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            el = float(t.item())
+        el = max_over_ranks(pg, el, dev)
         h2d = sum(v.numel() * 4 for k, v in hin.items())
         d2h = sum(v.numel() * 4 for v in hout.values())
-        e2e = {"value": ws * w.btd * ke / el, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e2e = {"value": job_throughput(w.btd * ke, ws, el), "unit": UNIT,
+               "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": ke, "ms_per_step": 1e3 * el / ke}
         del wsbuf
 
@@ -337,7 +348,7 @@ def run_gpu(args):
     bwd_mean_s = float(np.mean(bwd_ms)) * 1e-3
     fwd_mean_s = float(np.mean(fwd_ms)) * 1e-3
     achieved = mb["bwd"] / bwd_mean_s / 1e9
-    value = ws * w.btd * args.steps / (total_ms * 1e-3)
+    value = job_throughput(w.btd * args.steps, ws, total_ms * 1e-3)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
