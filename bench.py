@@ -178,29 +178,44 @@ def time_conv(ms, w, dev, stream, steps, hbm_gbs, K=4) -> dict:
     import torch
     b, T, Di = w.batch, w.T, w.d_inner
     g = torch.Generator(device=dev).manual_seed(0)
-    x = torch.randn(b, T, Di, device=dev, generator=g)
-    d_u = torch.randn(b, T, Di, device=dev, generator=g)
+    # three buffer sets used in turn: one set (x, u, d_u, d_x: 200 MB at mamba130m) would let a
+    # launch find the previous one's data in the 126 MB L2; three sets keep each launch on HBM
+    nset = 3
+    sets = []
+    for _ in range(nset):
+        x = torch.randn(b, T, Di, device=dev, generator=g)
+        sets.append({"x": x, "d_u": torch.randn(b, T, Di, device=dev, generator=g),
+                     "u": torch.empty_like(x), "d_x": torch.empty_like(x)})
     wt = torch.randn(Di, K, device=dev, generator=g) * 0.5
     bias = torch.randn(Di, device=dev, generator=g) * 0.3
-    u, d_x = torch.empty_like(x), torch.empty_like(x)
     d_w, d_b = torch.empty_like(wt), torch.empty_like(bias)
     sc = torch.empty(ms.mamba_conv_scratch_bytes(b, T, Di, K) // 4, device=dev)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-    for _ in range(3):
-        ms.mamba_conv_fwd(x, wt, bias, u, stream=stream)
-        ms.mamba_conv_bwd(x, wt, bias, d_u, sc, d_x, d_w, d_b, stream=stream)
-    fwd_ms = bwd_ms = 0.0
-    for _ in range(steps):
-        ev[0].record(stream)
-        ms.mamba_conv_fwd(x, wt, bias, u, stream=stream)
-        ev[1].record(stream)
-        ms.mamba_conv_bwd(x, wt, bias, d_u, sc, d_x, d_w, d_b, stream=stream)
-        ev[2].record(stream)
-        torch.cuda.synchronize()
-        fwd_ms += ev[0].elapsed_time(ev[1])
-        bwd_ms += ev[1].elapsed_time(ev[2])
-    fwd_ms /= steps
-    bwd_ms /= steps
+
+    def fwd(i):
+        z = sets[i % nset]
+        ms.mamba_conv_fwd(z["x"], wt, bias, z["u"], stream=stream)
+
+    def bwd(i):
+        z = sets[i % nset]
+        ms.mamba_conv_bwd(z["x"], wt, bias, z["d_u"], sc, z["d_x"], d_w, d_b, stream=stream)
+
+    for i in range(3):
+        fwd(i)
+        bwd(i)
+    # back-to-back launches between two events, so that the short kernels are timed with a
+    # full queue rather than with the host's launch latency
+    torch.cuda.synchronize()
+    ev[0].record(stream)
+    for i in range(steps):
+        fwd(i)
+    ev[1].record(stream)
+    for i in range(steps):
+        bwd(i)
+    ev[2].record(stream)
+    torch.cuda.synchronize()
+    fwd_ms = ev[0].elapsed_time(ev[1]) / steps
+    bwd_ms = ev[1].elapsed_time(ev[2]) / steps
     btd = b * T * Di
     fwd_bytes = 4 * (2 * btd + Di * K + Di)
     bwd_bytes = 4 * (3 * btd + 2 * Di * K + 2 * Di)

@@ -4,10 +4,13 @@
 //   u = pre * sigmoid(pre)
 // The page walks the backward in reverse time with a shift-register carry of the later steps'
 // taps. On the GPU the same sums are a stencil: d_x[t] = sum_{m<K} d_pre[t+m] * w[d, K-1-m].
-// A thread owns VW consecutive channels (4 when d_inner is a multiple of 4, else 1) of one
+// A thread owns VW consecutive channels (2 when d_inner is even, else 1) of one
 // batch row and a run of kConvRun consecutive steps. It slides a register window along the run,
 // so that every element is loaded once plus a halo of K-1 steps per run. The weight gradients
-// are summed per thread over its run, and a fixed-order kernel adds the runs' partials.
+// are summed per thread over its run, then over the 8 runs of its CTA in shared memory, and a
+// fixed-order kernel adds the CTAs' partials.
+#include <algorithm>
+
 #include "scan_common.cuh"
 #include "conv_plan.h"
 
@@ -26,6 +29,19 @@ struct Vec<4> {
   }
   static __device__ __forceinline__ void unpack(const float4& a, float (&v)[4]) {
     v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  }
+};
+template <>
+struct Vec<2> {
+  using T = float2;
+  static __device__ __forceinline__ float2 load(const float* p) {
+    return *reinterpret_cast<const float2*>(p);
+  }
+  static __device__ __forceinline__ void store(float* p, const float (&v)[2]) {
+    *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
+  }
+  static __device__ __forceinline__ void unpack(const float2& a, float (&v)[2]) {
+    v[0] = a.x; v[1] = a.y;
   }
 };
 template <>
@@ -60,6 +76,9 @@ __device__ __forceinline__ ConvThread conv_thread(const ConvParams& p, int VW) {
 
 __device__ __forceinline__ float silu_f(float p) { return p * sigmoid_fast(p); }
 
+// The register windows are rings of K slots indexed by (t - t0) mod K. Steps go in batches of
+// K, so inside a batch every slot index is a compile-time constant and nothing is shifted; the
+// loads of a batch are issued together, ahead of its arithmetic.
 template <int K, int VW>
 __global__ void __launch_bounds__(256) conv_fwd_kernel(const ConvParams p) {
   using V = Vec<VW>;
@@ -73,37 +92,38 @@ __global__ void __launch_bounds__(256) conv_fwd_kernel(const ConvParams p) {
     for (int j = 0; j < K; ++j) w[j][v] = p.w[(size_t)(c.d0 + v) * K + j];
   }
   const size_t row = (size_t)c.b * p.T;
-  // window of the K-1 previous inputs (zeros before t = 0)
-  float win[K > 1 ? K - 1 : 1][VW];
+  const float* __restrict__ xg = p.x;
+  float* __restrict__ ug = p.u;
+  float ring[K][VW];   // x[t'] at slot (t' - t0) mod K; the K-1 steps before t0 first (0 before t = 0)
 #pragma unroll
-  for (int j = 0; j < K - 1; ++j) {
-    const int ts = c.t0 - (K - 1) + j;
+  for (int s = 1; s < K; ++s) {
+    const int ts = c.t0 - K + s;
     if (ts >= 0) {
-      V::unpack(V::load(p.x + (row + ts) * p.Di + c.d0), win[j]);
+      V::unpack(V::load(xg + (row + ts) * p.Di + c.d0), ring[s]);
     } else {
 #pragma unroll
-      for (int v = 0; v < VW; ++v) win[j][v] = 0.f;
+      for (int v = 0; v < VW; ++v) ring[s][v] = 0.f;
     }
   }
-#pragma unroll 4
-  for (int t = c.t0; t < c.t1; ++t) {
-    float xv[VW], out[VW];
-    V::unpack(V::load(p.x + (row + t) * p.Di + c.d0), xv);
+  for (int tb = c.t0; tb < c.t1; tb += K) {
+    float xb[K][VW];
 #pragma unroll
-    for (int v = 0; v < VW; ++v) {
-      float acc = fmaf(w[K - 1][v], xv[v], bias[v]);
+    for (int q = 0; q < K; ++q)   // past the run: a repeated in-range load, unused
+      V::unpack(V::load(xg + (row + min(tb + q, c.t1 - 1)) * p.Di + c.d0), xb[q]);
 #pragma unroll
-      for (int j = 0; j < K - 1; ++j) acc = fmaf(w[j][v], win[j][v], acc);
-      out[v] = silu_f(acc);
-    }
-    V::store(p.u + (row + t) * p.Di + c.d0, out);
+    for (int q = 0; q < K; ++q) {
+      const int t = tb + q;
 #pragma unroll
-    for (int j = 0; j + 1 < K - 1; ++j)
+      for (int v = 0; v < VW; ++v) ring[q][v] = xb[q][v];
+      float out[VW];
 #pragma unroll
-      for (int v = 0; v < VW; ++v) win[j][v] = win[j + 1][v];
-    if constexpr (K > 1) {
+      for (int v = 0; v < VW; ++v) {
+        float acc = bias[v];
 #pragma unroll
-      for (int v = 0; v < VW; ++v) win[K - 2][v] = xv[v];
+        for (int j = 0; j < K; ++j) acc = fmaf(w[j][v], ring[(q + 1 + j) % K][v], acc);
+        out[v] = silu_f(acc);
+      }
+      if (t < c.t1) V::store(ug + (row + t) * p.Di + c.d0, out);
     }
   }
 }
@@ -114,8 +134,21 @@ __global__ void __launch_bounds__(256) conv_fwd_kernel(const ConvParams p) {
 template <int K, int VW>
 __global__ void __launch_bounds__(256) conv_bwd_kernel(const ConvParams p) {
   using V = Vec<VW>;
-  const ConvThread c = conv_thread(p, VW);
-  if (!c.valid) return;
+  // CTA = (batch row, group of 8 runs, 32 channel groups); warp = run, lane = channel group
+  __shared__ float s_red[kConvRunsPerCta][32][(K + 1) * VW];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ncg = p.Di / VW;
+  const int ncgb = (ncg + 31) / 32;
+  const int cgb = blockIdx.x % ncgb;
+  const int rg = (blockIdx.x / ncgb) % p.ngroups;
+  ConvThread c;
+  c.b = blockIdx.x / (ncgb * p.ngroups);
+  const int cg = cgb * 32 + lane;
+  const int run = rg * kConvRunsPerCta + warp;
+  c.valid = cg < ncg && run < p.nruns;
+  c.d0 = (cg < ncg ? cg : 0) * VW;
+  c.t0 = run * kConvRun;
+  c.t1 = c.valid ? min(p.T, c.t0 + kConvRun) : c.t0;
   float w[K][VW], bias[VW];
 #pragma unroll
   for (int v = 0; v < VW; ++v) {
@@ -124,134 +157,156 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(const ConvParams p) {
     for (int j = 0; j < K; ++j) w[j][v] = p.w[(size_t)(c.d0 + v) * K + j];
   }
   const size_t row = (size_t)c.b * p.T;
-  float xwin[K][VW];    // x[t-(K-1) .. t] (slot K-1 filled at each step)
-  float dpw[K][VW];     // d_pre[t-(K-1) .. t]
+  const float* __restrict__ xg = p.x;
+  const float* __restrict__ dug = p.d_u;
+  float* __restrict__ dxg = p.d_x;
+  float xr[K][VW];    // x[t'] at slot (t' - t0) mod K
+  float dr[K][VW];    // d_pre[t'] at slot (t' - t0) mod K
   float gw[K][VW], gb[VW];
 #pragma unroll
   for (int j = 0; j < K; ++j)
 #pragma unroll
     for (int v = 0; v < VW; ++v) {
-      dpw[j][v] = 0.f;
+      dr[j][v] = 0.f;
       gw[j][v] = 0.f;
     }
 #pragma unroll
   for (int v = 0; v < VW; ++v) gb[v] = 0.f;
 #pragma unroll
-  for (int j = 0; j < K - 1; ++j) {
-    const int ts = c.t0 - (K - 1) + j;
-    if (ts >= 0) {
-      V::unpack(V::load(p.x + (row + ts) * p.Di + c.d0), xwin[j]);
+  for (int s = 1; s < K; ++s) {
+    const int ts = c.t0 - K + s;
+    if (c.valid && ts >= 0) {
+      V::unpack(V::load(xg + (row + ts) * p.Di + c.d0), xr[s]);
     } else {
 #pragma unroll
-      for (int v = 0; v < VW; ++v) xwin[j][v] = 0.f;
+      for (int v = 0; v < VW; ++v) xr[s][v] = 0.f;
     }
   }
-  const int t_end = c.t1 + (K - 1);
-#pragma unroll 2
-  for (int t = c.t0; t < t_end; ++t) {
-    const bool in = t < p.T;
-    float dp[VW];
-    if (in) {
-      float xv[VW], du[VW];
-      V::unpack(V::load(p.x + (row + t) * p.Di + c.d0), xv);
-      V::unpack(V::load(p.d_u + (row + t) * p.Di + c.d0), du);
+  const int t_end = c.valid ? c.t1 + (K - 1) : c.t0;   // an invalid thread loads nothing
+  const int t_last = min(t_end, p.T) - 1;   // the last step that exists
+  for (int tb = c.t0; tb < t_end; tb += K) {
+    float xb[K][VW], db[K][VW];
+#pragma unroll
+    for (int q = 0; q < K; ++q) {   // past the end: a repeated in-range load, unused
+      const int t = min(tb + q, t_last);
+      V::unpack(V::load(xg + (row + t) * p.Di + c.d0), xb[q]);
+      V::unpack(V::load(dug + (row + t) * p.Di + c.d0), db[q]);
+    }
+#pragma unroll
+    for (int q = 0; q < K; ++q) {
+      const int t = tb + q;
+      const bool in = t < p.T;
 #pragma unroll
       for (int v = 0; v < VW; ++v) {
-        xwin[K - 1][v] = xv[v];
+        xr[q][v] = xb[q][v];
         float pre = bias[v];
 #pragma unroll
-        for (int j = 0; j < K; ++j) pre = fmaf(w[j][v], xwin[j][v], pre);
-        const float s = sigmoid_fast(pre);
-        dp[v] = du[v] * (s * fmaf(pre, 1.f - s, 1.f));
+        for (int j = 0; j < K; ++j) pre = fmaf(w[j][v], xr[(q + 1 + j) % K][v], pre);
+        const float sg = sigmoid_fast(pre);
+        dr[q][v] = in ? db[q][v] * (sg * fmaf(pre, 1.f - sg, 1.f)) : 0.f;
       }
-    } else {
+      // this thread's weight gradients: steps of its own run only
+      if (t < c.t1) {
 #pragma unroll
-      for (int v = 0; v < VW; ++v) dp[v] = 0.f;
-    }
-    // this thread's weight gradients: steps of its own run only
-    if (t < c.t1) {
+        for (int v = 0; v < VW; ++v) {
+          gb[v] += dr[q][v];
 #pragma unroll
-      for (int v = 0; v < VW; ++v) {
-        gb[v] += dp[v];
+          for (int j = 0; j < K; ++j) gw[j][v] = fmaf(dr[q][v], xr[(q + 1 + j) % K][v], gw[j][v]);
+        }
+      }
+      // d_x[t-(K-1)] = sum_m d_pre[t-(K-1)+m] * w[K-1-m]
+      const int to = t - (K - 1);
+      if (to >= c.t0 && to < c.t1) {
+        float dx[VW];
 #pragma unroll
-        for (int j = 0; j < K; ++j) gw[j][v] = fmaf(dp[v], xwin[j][v], gw[j][v]);
+        for (int v = 0; v < VW; ++v) {
+          float acc = 0.f;
+#pragma unroll
+          for (int m = 0; m < K; ++m) acc = fmaf(dr[(q + 1 + m) % K][v], w[K - 1 - m][v], acc);
+          dx[v] = acc;
+        }
+        V::store(dxg + (row + to) * p.Di + c.d0, dx);
       }
     }
-    // shift the d_pre window and complete d_x[t - (K-1)]
-#pragma unroll
-    for (int j = 0; j + 1 < K; ++j)
-#pragma unroll
-      for (int v = 0; v < VW; ++v) dpw[j][v] = dpw[j + 1][v];
-#pragma unroll
-    for (int v = 0; v < VW; ++v) dpw[K - 1][v] = dp[v];
-    const int to = t - (K - 1);
-    if (to >= c.t0) {
-      float dx[VW];
-#pragma unroll
-      for (int v = 0; v < VW; ++v) {
-        float acc = 0.f;
-#pragma unroll
-        for (int m = 0; m < K; ++m) acc = fmaf(dpw[m][v], w[K - 1 - m][v], acc);
-        dx[v] = acc;
-      }
-      V::store(p.d_x + (row + to) * p.Di + c.d0, dx);
-    }
-#pragma unroll
-    for (int j = 0; j + 1 < K; ++j)
-#pragma unroll
-      for (int v = 0; v < VW; ++v) xwin[j][v] = xwin[j + 1][v];
   }
-  // partials of this (batch row, run): [b * nruns + run][d][K] and [b * nruns + run][d]
-  const size_t part = (size_t)c.b * p.nruns + c.t0 / kConvRun;
+  // the CTA's 8 runs summed in shared memory in run order (invalid threads hold zeros), then one
+  // partial per (batch row, run group): [b * ngroups + group][d][K] and [..][d]
 #pragma unroll
   for (int v = 0; v < VW; ++v) {
-    p.part_b[part * p.Di + c.d0 + v] = gb[v];
+    s_red[warp][lane][K * VW + v] = gb[v];
 #pragma unroll
-    for (int j = 0; j < K; ++j) p.part_w[(part * p.Di + c.d0 + v) * K + j] = gw[j][v];
+    for (int j = 0; j < K; ++j) s_red[warp][lane][j * VW + v] = gw[j][v];
+  }
+  __syncthreads();
+  if (warp == 0 && cg < ncg) {
+    const size_t part = (size_t)c.b * p.ngroups + rg;
+#pragma unroll
+    for (int i = 0; i < (K + 1) * VW; ++i) {
+      float acc = 0.f;
+#pragma unroll
+      for (int r = 0; r < kConvRunsPerCta; ++r) acc += s_red[r][lane][i];
+      const int v = i % VW, j = i / VW;
+      if (j < K) p.part_w[(part * p.Di + c.d0 + v) * K + j] = acc;
+      else p.part_b[part * p.Di + c.d0 + v] = acc;
+    }
   }
 }
 
-// d_w and d_bias: the runs' partials summed in index order (eight loads in flight at a time).
+// d_w and d_bias: one warp per output sums the run groups' partials in a fixed order: lane l takes
+// runs l, l+32, ... in turn, then the lanes are added by a fixed butterfly (deterministic).
 __global__ void conv_reduce_kernel(const ConvParams p) {
   const size_t nw = (size_t)p.Di * p.K;
   const size_t total = nw + (size_t)p.Di;
-  const int nk = p.batch * p.nruns;
-  for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < total;
-       e += (size_t)gridDim.x * blockDim.x) {
+  const int nk = p.batch * p.ngroups;
+  const int lane = threadIdx.x & 31;
+  const size_t warps = (size_t)gridDim.x * (blockDim.x / 32);
+  for (size_t e = blockIdx.x * (size_t)(blockDim.x / 32) + (threadIdx.x >> 5); e < total;
+       e += warps) {
     const bool is_w = e < nw;
     const size_t q = is_w ? e : e - nw;
     const size_t stride = is_w ? nw : (size_t)p.Di;
     const float* part = is_w ? p.part_w : p.part_b;
     float acc = 0.f;
-    for (int k0 = 0; k0 < nk; k0 += 8) {
+    for (int k0 = lane; k0 < nk; k0 += 32 * 8) {   // eight loads in flight per lane
       float v[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) v[k] = k0 + k < nk ? part[(size_t)(k0 + k) * stride + q] : 0.f;
+      for (int i = 0; i < 8; ++i) {
+        const int k = k0 + 32 * i;
+        v[i] = k < nk ? part[(size_t)k * stride + q] : 0.f;
+      }
 #pragma unroll
-      for (int k = 0; k < 8; ++k) acc += v[k];
+      for (int i = 0; i < 8; ++i) acc += v[i];
     }
-    (is_w ? p.d_w : p.d_bias)[q] = acc;
+#pragma unroll
+    for (int m = 16; m >= 1; m /= 2) acc += __shfl_xor_sync(kFull, acc, m);
+    if (lane == 0) (is_w ? p.d_w : p.d_bias)[q] = acc;
   }
 }
 
 template <int K>
 static int launch_k(const ConvParams& p, bool bwd, cudaStream_t s) {
-  const bool vec = p.Di % 4 == 0;
-  const int VW = vec ? 4 : 1;
+  // 2 channels per thread (8-byte loads: still one 256-byte segment per warp row) keep the
+  // register windows small enough for high occupancy
+  const bool vec = p.Di % 2 == 0;
+  const int VW = vec ? 2 : 1;
   const long long threads = (long long)p.batch * p.nruns * (p.Di / VW);
   const unsigned blocks = (unsigned)((threads + 255) / 256);
   if (!bwd) {
-    if (vec) conv_fwd_kernel<K, 4><<<blocks, 256, 0, s>>>(p);
+    if (vec) conv_fwd_kernel<K, 2><<<blocks, 256, 0, s>>>(p);
     else conv_fwd_kernel<K, 1><<<blocks, 256, 0, s>>>(p);
     return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
   }
-  if (vec) conv_bwd_kernel<K, 4><<<blocks, 256, 0, s>>>(p);
-  else conv_bwd_kernel<K, 1><<<blocks, 256, 0, s>>>(p);
+  const int ncgb = (p.Di / VW + 31) / 32;
+  const unsigned bblocks = (unsigned)((long long)p.batch * p.ngroups * ncgb);
+  if (vec) conv_bwd_kernel<K, 2><<<bblocks, 256, 0, s>>>(p);
+  else conv_bwd_kernel<K, 1><<<bblocks, 256, 0, s>>>(p);
   if (cudaPeekAtLastError() != cudaSuccess) return -1;
   int sms = 152, dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  conv_reduce_kernel<<<sms * 2, 256, 0, s>>>(p);
+  const size_t outs = (size_t)p.Di * (p.K + 1);
+  const unsigned rblocks = (unsigned)std::min<size_t>((outs + 7) / 8, (size_t)sms * 16);
+  conv_reduce_kernel<<<rblocks, 256, 0, s>>>(p);
   return cudaPeekAtLastError() == cudaSuccess ? 2 : -1;
 }
 

@@ -15,16 +15,24 @@ struct ConvParams {
   const float* d_u;                 // backward input
   float* d_x; float* d_w; float* d_bias;
   float* part_w; float* part_b;     // scratch: per (batch row, run) weight-gradient partials
-  int batch, T, Di, K, nruns;
+  int batch, T, Di, K, nruns, ngroups;
 };
 
-// runs along T, and the scratch floats the backward needs (per-run partials of d_w, d_bias)
+// The backward's CTA holds 8 warps: 8 consecutive runs of the same 32 channel groups. It sums
+// their weight gradients in shared memory, so there is one partial per (batch row, 8 runs).
+constexpr int kConvRunsPerCta = 8;
+
+// runs along T, groups of 8 runs, and the scratch floats the backward needs (per-group partials
+// of d_w, d_bias)
 inline int conv_nruns(int64_t T) { return (int)((T + kConvRun - 1) / kConvRun); }
+inline int conv_ngroups(int64_t T) {
+  return (conv_nruns(T) + kConvRunsPerCta - 1) / kConvRunsPerCta;
+}
 inline size_t conv_part_w_floats(int64_t batch, int64_t T, int64_t Di, int64_t K) {
-  return (size_t)batch * conv_nruns(T) * Di * K;
+  return (size_t)batch * conv_ngroups(T) * Di * K;
 }
 inline size_t conv_part_b_floats(int64_t batch, int64_t T, int64_t Di) {
-  return (size_t)batch * conv_nruns(T) * Di;
+  return (size_t)batch * conv_ngroups(T) * Di;
 }
 
 // Enqueues the forward (1 kernel) or the backward (2 kernels); returns that count or -1.
