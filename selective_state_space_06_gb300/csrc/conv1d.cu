@@ -5,7 +5,7 @@
 // The page walks the backward in reverse time with a shift-register carry of the later steps'
 // taps. On the GPU the same sums are a stencil: d_x[t] = sum_{m<K} d_pre[t+m] * w[d, K-1-m].
 // A thread owns VW consecutive channels (2 when d_inner is even, else 1) of one
-// batch row and a run of kConvRun consecutive steps. It slides a register window along the run,
+// batch row and a run of consecutive steps (32 or more, picked per launch). It slides a register window along the run,
 // so that every element is loaded once plus a halo of K-1 steps per run. The weight gradients
 // are summed per thread over its run, then over the 8 runs of its CTA in shared memory, and a
 // fixed-order kernel adds the CTAs' partials.
@@ -69,8 +69,8 @@ __device__ __forceinline__ ConvThread conv_thread(const ConvParams& p, int VW) {
   const int r = (int)(rest % p.nruns);
   c.b = (int)(rest / p.nruns);
   c.d0 = cg * VW;
-  c.t0 = r * kConvRun;
-  c.t1 = min(p.T, c.t0 + kConvRun);
+  c.t0 = r * p.run;
+  c.t1 = min(p.T, c.t0 + p.run);
   return c;
 }
 
@@ -147,8 +147,8 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(const ConvParams p) {
   const int run = rg * kConvRunsPerCta + warp;
   c.valid = cg < ncg && run < p.nruns;
   c.d0 = (cg < ncg ? cg : 0) * VW;
-  c.t0 = run * kConvRun;
-  c.t1 = c.valid ? min(p.T, c.t0 + kConvRun) : c.t0;
+  c.t0 = run * p.run;
+  c.t1 = c.valid ? min(p.T, c.t0 + p.run) : c.t0;
   float w[K][VW], bias[VW];
 #pragma unroll
   for (int v = 0; v < VW; ++v) {
@@ -283,20 +283,64 @@ __global__ void conv_reduce_kernel(const ConvParams p) {
   }
 }
 
+// Run length. A launch of c CTAs with `slots` resident CTAs per GPU takes ceil(c / slots) waves
+// of about (run + K - 1) steps each, so the run length minimises that product; a run of 32
+// steps at mamba130m's size, for instance, would leave a second wave of 8 CTAs. Shortest run
+// on ties (more CTAs in flight). Never shorter than kConvRun, which sizes the scratch.
+template <typename CtaCount>
+static int pick_run(const ConvParams& p, long long slots, CtaCount ctas) {
+  int best = kConvRun;
+  long long best_cost = -1;
+  const int hi = std::max(kConvRun, std::min(p.T, kConvRunMax));
+  for (int r = kConvRun; r <= hi; ++r) {
+    const int nruns = (p.T + r - 1) / r;
+    if (r > kConvRun && (p.T + r - 2) / (r - 1) == nruns) continue;   // same runs, longer
+    const long long waves = (ctas(nruns) + slots - 1) / slots;
+    const long long cost = waves * (r + p.K - 1);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = r;
+    }
+  }
+  return best;
+}
+
+static long long resident_slots(const void* kern, int threads) {
+  int sms = 152, dev = 0, per_sm = 1;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  return (long long)sms * per_sm;
+}
+
 template <int K>
-static int launch_k(const ConvParams& p, bool bwd, cudaStream_t s) {
+static int launch_k(const ConvParams& p0, bool bwd, cudaStream_t s) {
   // 2 channels per thread (8-byte loads: still one 256-byte segment per warp row) keep the
   // register windows small enough for high occupancy
-  const bool vec = p.Di % 2 == 0;
+  const bool vec = p0.Di % 2 == 0;
   const int VW = vec ? 2 : 1;
-  const long long threads = (long long)p.batch * p.nruns * (p.Di / VW);
-  const unsigned blocks = (unsigned)((threads + 255) / 256);
+  const long long ncg = p0.Di / VW;
+  ConvParams p = p0;
   if (!bwd) {
+    const void* kern = vec ? (const void*)conv_fwd_kernel<K, 2> : (const void*)conv_fwd_kernel<K, 1>;
+    const long long slots = resident_slots(kern, 256);
+    p.run = pick_run(p, slots, [&](int nruns) { return (p.batch * nruns * ncg + 255) / 256; });
+    p.nruns = (p.T + p.run - 1) / p.run;
+    const unsigned blocks = (unsigned)(((long long)p.batch * p.nruns * ncg + 255) / 256);
     if (vec) conv_fwd_kernel<K, 2><<<blocks, 256, 0, s>>>(p);
     else conv_fwd_kernel<K, 1><<<blocks, 256, 0, s>>>(p);
     return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
   }
-  const int ncgb = (p.Di / VW + 31) / 32;
+  const long long ncgb = (ncg + 31) / 32;
+  const void* kern = vec ? (const void*)conv_bwd_kernel<K, 2> : (const void*)conv_bwd_kernel<K, 1>;
+  const long long slots = resident_slots(kern, 256);
+  p.run = pick_run(p, slots, [&](int nruns) {
+    return (long long)p.batch * ((nruns + kConvRunsPerCta - 1) / kConvRunsPerCta) * ncgb;
+  });
+  p.nruns = (p.T + p.run - 1) / p.run;
+  p.ngroups = (p.nruns + kConvRunsPerCta - 1) / kConvRunsPerCta;   // <= the scratch's count
   const unsigned bblocks = (unsigned)((long long)p.batch * p.ngroups * ncgb);
   if (vec) conv_bwd_kernel<K, 2><<<bblocks, 256, 0, s>>>(p);
   else conv_bwd_kernel<K, 1><<<bblocks, 256, 0, s>>>(p);

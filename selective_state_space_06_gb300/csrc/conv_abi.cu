@@ -47,6 +47,7 @@ int mamba_conv_fwd(const float* x, const float* w, const float* bias, float* u, 
   mscan::ConvParams p = {};
   p.x = x; p.w = w; p.bias = bias; p.u = u;
   p.batch = (int)batch; p.T = (int)T; p.Di = (int)d_inner; p.K = (int)d_conv;
+  p.run = mscan::kConvRun;   // the launch picks the run length
   p.nruns = mscan::conv_nruns(T);
   p.ngroups = mscan::conv_ngroups(T);
   const int k = mscan::launch_conv(p, false, (cudaStream_t)stream);
@@ -83,6 +84,7 @@ int mamba_conv_bwd(const float* x, const float* w, const float* bias, const floa
   p.part_w = sc;
   p.part_b = sc + (mscan::conv_part_w_floats(batch, T, d_inner, d_conv) + a - 1) / a * a;
   p.batch = (int)batch; p.T = (int)T; p.Di = (int)d_inner; p.K = (int)d_conv;
+  p.run = mscan::kConvRun;   // the launch picks the run length
   p.nruns = mscan::conv_nruns(T);
   p.ngroups = mscan::conv_ngroups(T);
   const int k = mscan::launch_conv(p, true, (cudaStream_t)stream);

@@ -6,7 +6,8 @@
 
 namespace mscan {
 
-constexpr int kConvRun = 32;    // consecutive steps per thread
+constexpr int kConvRun = 32;    // fewest consecutive steps per thread (the scratch is sized for it)
+constexpr int kConvRunMax = 256;
 constexpr int kConvMaxK = 8;    // largest kernel size
 
 struct ConvParams {
@@ -15,7 +16,9 @@ struct ConvParams {
   const float* d_u;                 // backward input
   float* d_x; float* d_w; float* d_bias;
   float* part_w; float* part_b;     // scratch: per (batch row, run) weight-gradient partials
-  int batch, T, Di, K, nruns, ngroups;
+  int batch, T, Di, K;
+  int run;                          // steps per thread, chosen per launch (>= kConvRun)
+  int nruns, ngroups;               // ceil(T / run), ceil(nruns / kConvRunsPerCta)
 };
 
 // The backward's CTA holds 8 warps: 8 consecutive runs of the same 32 channel groups. It sums
@@ -23,7 +26,7 @@ struct ConvParams {
 constexpr int kConvRunsPerCta = 8;
 
 // runs along T, groups of 8 runs, and the scratch floats the backward needs (per-group partials
-// of d_w, d_bias)
+// of d_w, d_bias), all at the shortest run, which has the most partials
 inline int conv_nruns(int64_t T) { return (int)((T + kConvRun - 1) / kConvRun); }
 inline int conv_ngroups(int64_t T) {
   return (conv_nruns(T) + kConvRunsPerCta - 1) / kConvRunsPerCta;
