@@ -356,6 +356,26 @@ def run_gpu(args):
         variants["softplus_fused"] = {"ms_per_step": ms_sp, "value": w.btd / (ms_sp * 1e-3),
                                       "unit": UNIT, "steps": kv}
         del raw
+
+        # variant: forward and backward in one call when dy is known up front (the forward
+        # keeps only the checkpoints; the backward forms y and writes out)
+        def step_fused():
+            ms.mamba_scan_fwd_bwd(x["delta"], x["u"], x["B"], x["C"], x["gate"], x["A_log"],
+                                  x["D"], x["dy"], bufs["out"], bufs["ckpt"], bufs["scratch"],
+                                  bufs["d_delta"], bufs["d_u"], bufs["d_B"], bufs["d_C"],
+                                  bufs["d_A_log"], bufs["d_D"], bufs["d_gate"], stream=stream)
+        for _ in range(3):
+            step_fused()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(kv):
+            step_fused()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms_fu = e0.elapsed_time(e1) / kv
+        variants["fused_fwd_bwd"] = {"ms_per_step": ms_fu, "value": w.btd / (ms_fu * 1e-3),
+                                     "unit": UNIT, "steps": kv,
+                                     "launches": ms.mamba_scan_last_launch_count()}
         variants["conv1d_silu"] = time_conv(ms, w, dev, stream, kv, read_peaks()["hbm_gbs"])
 
     mb = minimal_bytes(w)

@@ -118,6 +118,24 @@ int mamba_scan_bwd_softplus(const float* delta_raw, const float* u, const float*
                             float* d_A_log, float* d_D, float* d_gate, int64_t batch, int64_t T,
                             int64_t d_inner, int64_t d_state, void* stream);
 
+/* Forward and backward in one call, for a training step in which dy is known before the
+ * forward runs (the page's layer forward followed by its Phases B2 and B3). Writes out and the
+ * seven gradients, exactly what mamba_scan_fwd followed by mamba_scan_bwd writes (y is not
+ * returned). Same inputs, layouts, checkpoint and scratch buffers (mamba_scan_ckpt_bytes,
+ * mamba_scan_scratch_bytes) and error codes; out must not overlap any other argument, and
+ * every check runs before the first launch. For d_state 9..64 the forward pass keeps only the
+ * chunk-boundary states (it reads neither C nor gate and writes neither out nor y) and the
+ * backward forms y = sum_n C*h + D*u from the states it recomputes anyway, so out, y and the
+ * gate are not carried through device memory between the passes. For d_state <= 8 the call
+ * runs the two passes as the separate entry points do. The checkpoint buffer's contents
+ * afterwards are unspecified. Asynchronous on `stream`; device pointers, owned by the caller. */
+int mamba_scan_fwd_bwd(const float* delta, const float* u, const float* B, const float* C,
+                       const float* gate, const float* A_log, const float* D, const float* dy,
+                       float* out, void* ckpt, size_t ckpt_bytes, void* scratch,
+                       size_t scratch_bytes, float* d_delta, float* d_u, float* d_B, float* d_C,
+                       float* d_A_log, float* d_D, float* d_gate, int64_t batch, int64_t T,
+                       int64_t d_inner, int64_t d_state, void* stream);
+
 /* Causal depthwise conv1d + SiLU, the step that feeds u to the scan (the page's Phase B6 is
  * its backward):
  *   pre[b,t,d] = bias[d] + sum_{j<d_conv} w[d,j] * x[b, t-(d_conv-1)+j, d]  (x = 0 before t=0)

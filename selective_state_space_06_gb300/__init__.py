@@ -42,7 +42,7 @@ EXPORTED = (
     "mamba_scan_ckpt_bytes", "mamba_scan_scratch_bytes", "mamba_scan_fwd", "mamba_scan_bwd",
     "mamba_scan_host_workspace_bytes", "mamba_scan_fwd_bwd_host", "mamba_scan_status",
     "mamba_scan_strerror", "mamba_scan_last_launch_count", "mamba_scan_bwd_noalloc",
-    "mamba_scan_fwd_softplus", "mamba_scan_bwd_softplus",
+    "mamba_scan_fwd_softplus", "mamba_scan_bwd_softplus", "mamba_scan_fwd_bwd",
     "mamba_conv_scratch_bytes", "mamba_conv_fwd", "mamba_conv_bwd",
 )
 
@@ -70,6 +70,8 @@ _lib.mamba_scan_fwd_softplus.argtypes = _lib.mamba_scan_fwd.argtypes
 _lib.mamba_scan_fwd_softplus.restype = ctypes.c_int
 _lib.mamba_scan_bwd_softplus.argtypes = _lib.mamba_scan_bwd.argtypes
 _lib.mamba_scan_bwd_softplus.restype = ctypes.c_int
+_lib.mamba_scan_fwd_bwd.argtypes = [_vp] * 10 + [_sz, _vp, _sz] + [_vp] * 7 + [_i64] * 4 + [_vp]
+_lib.mamba_scan_fwd_bwd.restype = ctypes.c_int
 _lib.mamba_scan_bwd_noalloc.argtypes = [_vp] * 9 + [_sz] + [_vp] * 7 + [_i64] * 4 + [_vp]
 _lib.mamba_scan_bwd_noalloc.restype = ctypes.c_int
 _lib.mamba_scan_fwd_bwd_host.argtypes = [_vp] * 17 + [_sz] + [_i64] * 4 + [_vp]
@@ -197,6 +199,26 @@ def mamba_scan_bwd_softplus(delta_raw, u, B, C, gate, A_log, D, dy, ckpt, scratc
     to the raw delta."""
     mamba_scan_bwd(delta_raw, u, B, C, gate, A_log, D, dy, ckpt, scratch, d_delta_raw, d_u, d_B,
                    d_C, d_A_log, d_D, d_gate, stream, _fn="mamba_scan_bwd_softplus")
+
+
+def mamba_scan_fwd_bwd(delta, u, B, C, gate, A_log, D, dy, out, ckpt, scratch, d_delta, d_u,
+                       d_B, d_C, d_A_log, d_D, d_gate, stream=None):
+    """Forward and backward in one call when dy is known up front: writes out and all seven
+    gradients (y is not returned). The same checkpoint and scratch buffers as the separate
+    calls."""
+    b, T, Di, N = _dims(delta, B)
+    dev = delta.device
+    ck_bytes = 0 if ckpt is None else ckpt.numel() * ckpt.element_size()
+    rc = _lib.mamba_scan_fwd_bwd(
+        _ptr(delta, "delta", dev), _ptr(u, "u", dev), _ptr(B, "B", dev), _ptr(C, "C", dev),
+        _ptr(gate, "gate", dev), _ptr(A_log, "A_log", dev), _ptr(D, "D", dev),
+        _ptr(dy, "dy", dev), _ptr(out, "out", dev), _ptr(ckpt, "ckpt", dev, allow_none=True),
+        ck_bytes, _ptr(scratch, "scratch", dev), scratch.numel() * scratch.element_size(),
+        _ptr(d_delta, "d_delta", dev), _ptr(d_u, "d_u", dev), _ptr(d_B, "d_B", dev),
+        _ptr(d_C, "d_C", dev), _ptr(d_A_log, "d_A_log", dev), _ptr(d_D, "d_D", dev),
+        _ptr(d_gate, "d_gate", dev), b, T, Di, N, _stream_ptr(stream, dev))
+    if rc != MAMBA_OK:
+        raise MambaScanError(rc, "mamba_scan_fwd_bwd")
 
 
 def mamba_scan_bwd_noalloc(delta, u, B, C, gate, A_log, D, dy, ckpt, d_delta, d_u, d_B, d_C,

@@ -245,25 +245,27 @@ size_t mamba_scan_scratch_bytes(int64_t batch, int64_t T, int64_t d_inner, int64
 static int scan_fwd_impl(const float* delta, const float* u, const float* B, const float* C,
                          const float* gate, const float* A_log, const float* D, float* out,
                          float* y, void* ckpt, size_t ckpt_bytes, int64_t batch, int64_t T,
-                         int64_t d_inner, int64_t d_state, void* stream, int softplus) {
+                         int64_t d_inner, int64_t d_state, void* stream, int softplus,
+                         int states_only = 0) {
   Plan plan;
   int rc = check_dims(batch, T, d_inner, d_state, &plan);
   if (rc != MAMBA_OK) return rc;
   const size_t need_ck = plan.ckpt_elems * sizeof(float);
-  if (!delta || !u || !B || !C || !gate || !A_log || !D || !out) return MAMBA_ERR_INVALID_ARG;
+  if (!delta || !u || !B || !C || !gate || !A_log || !D || (!out && !states_only))
+    return MAMBA_ERR_INVALID_ARG;
   if (need_ck > 0 && !ckpt) return MAMBA_ERR_INVALID_ARG;
   const void* ptrs[] = {delta, u, B, C, gate, A_log, D, out, y, ckpt};
   for (const void* q : ptrs)
     if (q && !aligned16(q)) return MAMBA_ERR_MISALIGNED;
   if (ckpt_bytes < need_ck) return MAMBA_ERR_WORKSPACE;
   const size_t btd = (size_t)batch * T * d_inner * sizeof(float);
-  {
+  if (out) {
     Range ro = {(uintptr_t)out, (uintptr_t)out + btd};
     if (y && overlaps(ro, Range{(uintptr_t)y, (uintptr_t)y + btd})) return MAMBA_ERR_INVALID_ARG;
     if (need_ck && overlaps(ro, Range{(uintptr_t)ckpt, (uintptr_t)ckpt + need_ck}))
       return MAMBA_ERR_INVALID_ARG;
   }
-  mscan::FwdParams p;
+  mscan::FwdParams p = {};
   p.delta = delta; p.u = u; p.B = B; p.C = C; p.gate = gate; p.A_log = A_log; p.D = D;
   p.out = out; p.y = y; p.ckpt = (float*)ckpt;
   p.agg_h = plan.fwd.nseg > 1 ? (float*)ckpt + plan.off_fagg_h : nullptr;
@@ -274,6 +276,7 @@ static int scan_fwd_impl(const float* delta, const float* u, const float* B, con
   p.seg_chunks = plan.fwd.seg_chunks; p.nseg = plan.fwd.nseg;
   p.agg_k = 1;
   p.softplus = softplus;
+  p.states_only = states_only;
   const int n = mscan::launch_fwd(plan, p, (cudaStream_t)stream);
   if (n < 0) return set_cuda_error(cudaGetLastError());
   g_last_launches = n;
@@ -303,7 +306,8 @@ static int scan_bwd_impl(const float* delta, const float* u, const float* B, con
                          size_t scratch_bytes, float* d_delta, float* d_u, float* d_B,
                          float* d_C, float* d_A_log, float* d_D, float* d_gate, int64_t batch,
                          int64_t T, int64_t d_inner, int64_t d_state, void* stream,
-                         int softplus) {
+                         int softplus, float* out = nullptr, bool fuse_out = false,
+                         bool check_only = false) {
   Plan plan;
   int rc = check_dims(batch, T, d_inner, d_state, &plan);
   if (rc != MAMBA_OK) return rc;
@@ -314,7 +318,7 @@ static int scan_bwd_impl(const float* delta, const float* u, const float* B, con
     return MAMBA_ERR_INVALID_ARG;
   if (need_ck > 0 && !ckpt) return MAMBA_ERR_INVALID_ARG;
   const void* ptrs[] = {delta, u, B, C, gate, A_log, D, dy, ckpt, scratch,
-                        d_delta, d_u, d_B, d_C, d_A_log, d_D, d_gate};
+                        d_delta, d_u, d_B, d_C, d_A_log, d_D, d_gate, out};
   for (const void* q : ptrs)
     if (q && !aligned16(q)) return MAMBA_ERR_MISALIGNED;
   if (ckpt_bytes < need_ck || scratch_bytes < need_sc) return MAMBA_ERR_WORKSPACE;
@@ -330,15 +334,17 @@ static int scan_bwd_impl(const float* delta, const float* u, const float* B, con
         {(uintptr_t)d_A_log, (uintptr_t)d_A_log + (size_t)d_inner * d_state * sizeof(float)},
         {(uintptr_t)d_D, (uintptr_t)d_D + (size_t)d_inner * sizeof(float)},
         {(uintptr_t)scratch, (uintptr_t)scratch + need_sc},
+        {(uintptr_t)out, (uintptr_t)out + (out ? btd : 0)},
         {(uintptr_t)ckpt, (uintptr_t)ckpt + need_ck},
     };
-    const int nout = need_ck ? 9 : 8;
+    const int nout = need_ck ? 10 : 9;
     for (int i = 0; i < nout; ++i)
       for (int j = i + 1; j < nout; ++j)
         if (overlaps(outs[i], outs[j])) return MAMBA_ERR_INVALID_ARG;
   }
+  if (check_only) return MAMBA_OK;
   float* sc = (float*)scratch;
-  mscan::BwdParams p;
+  mscan::BwdParams p = {};
   p.delta = delta; p.u = u; p.B = B; p.C = C; p.gate = gate; p.A_log = A_log; p.D = D;
   p.dy = dy; p.ckpt = (const float*)ckpt; p.y_ck = (const float*)ckpt + plan.off_y;
   p.d_delta = d_delta; p.d_u = d_u; p.d_gate = d_gate;
@@ -351,6 +357,8 @@ static int scan_bwd_impl(const float* delta, const float* u, const float* B, con
   p.seg_chunks = plan.bwd.seg_chunks; p.nseg = plan.bwd.nseg;
   p.sub_chunks = plan.bwd.sub_chunks; p.nsub = plan.bwd.nsub;
   p.softplus = softplus;
+  p.out = fuse_out ? out : nullptr;
+  if (fuse_out) p.y_ck = nullptr;   // y is recomputed from the states
   const int n = mscan::launch_bwd(plan, p, (cudaStream_t)stream);
   if (n < 0) return set_cuda_error(cudaGetLastError());
   g_last_launches = n;
@@ -378,6 +386,35 @@ int mamba_scan_bwd_softplus(const float* delta_raw, const float* u, const float*
   return scan_bwd_impl(delta_raw, u, B, C, gate, A_log, D, dy, ckpt, ckpt_bytes, scratch,
                        scratch_bytes, d_delta_raw, d_u, d_B, d_C, d_A_log, d_D, d_gate, batch,
                        T, d_inner, d_state, stream, 1);
+}
+
+int mamba_scan_fwd_bwd(const float* delta, const float* u, const float* B, const float* C,
+                       const float* gate, const float* A_log, const float* D, const float* dy,
+                       float* out, void* ckpt, size_t ckpt_bytes, void* scratch,
+                       size_t scratch_bytes, float* d_delta, float* d_u, float* d_B, float* d_C,
+                       float* d_A_log, float* d_D, float* d_gate, int64_t batch, int64_t T,
+                       int64_t d_inner, int64_t d_state, void* stream) {
+  if (!out) return MAMBA_ERR_INVALID_ARG;
+  // everything is checked before the first launch
+  int rc = scan_bwd_impl(delta, u, B, C, gate, A_log, D, dy, ckpt, ckpt_bytes, scratch,
+                         scratch_bytes, d_delta, d_u, d_B, d_C, d_A_log, d_D, d_gate, batch, T,
+                         d_inner, d_state, stream, 0, out, false, true);
+  if (rc != MAMBA_OK) return rc;
+  Plan plan;
+  if (!mscan::make_plan(batch, T, d_inner, d_state, &plan)) return MAMBA_ERR_INVALID_ARG;
+  // d_state 9..64 (the tensor-memory backward): the forward keeps only the checkpoints and the
+  // backward forms y and out; smaller d_state runs the two passes as separate calls do
+  const bool fused = plan.NP >= mscan::kTmemMinNP;
+  rc = scan_fwd_impl(delta, u, B, C, gate, A_log, D, out, nullptr, ckpt, ckpt_bytes, batch, T,
+                     d_inner, d_state, stream, 0, fused ? 1 : 0);
+  if (rc != MAMBA_OK) return rc;
+  const int nf = g_last_launches;
+  rc = scan_bwd_impl(delta, u, B, C, gate, A_log, D, dy, ckpt, ckpt_bytes, scratch,
+                     scratch_bytes, d_delta, d_u, d_B, d_C, d_A_log, d_D, d_gate, batch, T,
+                     d_inner, d_state, stream, 0, out, fused, false);
+  if (rc != MAMBA_OK) return rc;
+  g_last_launches += nf;
+  return MAMBA_OK;
 }
 
 size_t mamba_scan_host_workspace_bytes(int64_t batch, int64_t T, int64_t d_inner,

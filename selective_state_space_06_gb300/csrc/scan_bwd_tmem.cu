@@ -73,8 +73,9 @@ struct BwdTmemShape {
 
 static __device__ unsigned int g_bwd_fault;   // set when a bounded wait gave up
 
-// Stage layout: delta, u, gate, dy, y tiles, then B, C, then the checkpoint row.
-template <int NP, bool VEC, bool TMA>
+// Stage layout: delta, u, gate, dy, y tiles, then B, C, then the checkpoint row. FY (the fused
+// call) leaves the y tile to the kernel, which fills it from the recomputed states.
+template <int NP, bool VEC, bool TMA, bool FY = false>
 __device__ __forceinline__ void bwd_tmem_load_chunk(const BwdMaps& maps, const BwdParams& p,
                                                     float* st, uint64_t* bar, int c, int b,
                                                     int dblk0) {
@@ -86,12 +87,12 @@ __device__ __forceinline__ void bwd_tmem_load_chunk(const BwdMaps& maps, const B
     // one thread issues the whole stage; rows past T, channels past d_inner, states past
     // d_state and the (absent) checkpoint before chunk 0 arrive as zeros
     if (threadIdx.x == 0) {
-      mbar_expect_tx(bar, S::kStageBytes);
+      mbar_expect_tx(bar, S::kStageBytes - (FY ? TILE * (uint32_t)sizeof(float) : 0u));
       tma_load_3d(st, &maps.delta, bar, dblk0, t0, b);
       tma_load_3d(st + TILE, &maps.u, bar, dblk0, t0, b);
       tma_load_3d(st + 2 * TILE, &maps.gate, bar, dblk0, t0, b);
       tma_load_3d(st + 3 * TILE, &maps.dy, bar, dblk0, t0, b);
-      tma_load_3d(st + 4 * TILE, &maps.y, bar, dblk0, t0, b);
+      if constexpr (!FY) tma_load_3d(st + 4 * TILE, &maps.y, bar, dblk0, t0, b);
       tma_load_3d(st + 5 * TILE, &maps.B, bar, 0, t0, b);
       tma_load_3d(st + 5 * TILE + kChunk * NP, &maps.C, bar, 0, t0, b);
       tma_load_4d(s_h0, &maps.ckpt, bar, 0, dblk0, c - 1, b);
@@ -102,7 +103,7 @@ __device__ __forceinline__ void bwd_tmem_load_chunk(const BwdMaps& maps, const B
     stage_tile<DC, NTH, VEC>(st + TILE, p.u, row0, t0, p.T, p.Di, dblk0);
     stage_tile<DC, NTH, VEC>(st + 2 * TILE, p.gate, row0, t0, p.T, p.Di, dblk0);
     stage_tile<DC, NTH, VEC>(st + 3 * TILE, p.dy, row0, t0, p.T, p.Di, dblk0);
-    stage_tile<DC, NTH, VEC>(st + 4 * TILE, p.y_ck, row0, t0, p.T, p.Di, dblk0);
+    if constexpr (!FY) stage_tile<DC, NTH, VEC>(st + 4 * TILE, p.y_ck, row0, t0, p.T, p.Di, dblk0);
     stage_tile<NP, NTH, VEC>(st + 5 * TILE, p.B, row0, t0, p.T, p.N, 0);
     stage_tile<NP, NTH, VEC>(st + 5 * TILE + kChunk * NP, p.C, row0, t0, p.T, p.N, 0);
     // state entering chunk c (checkpoint slot c-1), rows of N states at a stride of NP;
@@ -138,9 +139,13 @@ __device__ __forceinline__ void bwd_tmem_wait_stage(uint64_t* bars, int stage, i
   }
 }
 
-template <int NP, bool VEC, bool TMA, bool SP>
+// FY: the fused forward + backward call. The forward wrote only the checkpoints, so the
+// recompute also forms y = sum_n C*h + D*u (a reduce-scatter over the state lanes, as for the
+// d_delta sums) into the y tile, and the gating step runs after it and writes out as well.
+template <int NP, bool VEC, bool TMA, bool SP, bool FY>
 __global__ void __launch_bounds__(kWarps * 32, 2)
 scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
+  static_assert(!(SP && FY), "the fused call takes the plain delta");
   using S = BwdTmemShape<NP>;
   constexpr int G = S::G, LG = S::LG, DW = S::DW, DC = S::DC, TILE = S::TILE;
   constexpr int NTH = kWarps * 32;
@@ -175,8 +180,8 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
 #pragma unroll
   for (int s = 0; s < kTmemStages - 1; ++s) {
     if (s < nck)
-      bwd_tmem_load_chunk<NP, VEC, TMA>(maps, p, smem + s * S::kStageFloats, bars + s, last - s,
-                                        b, dblk0);
+      bwd_tmem_load_chunk<NP, VEC, TMA, FY>(maps, p, smem + s * S::kStageFloats, bars + s,
+                                            last - s, b, dblk0);
     else if constexpr (!TMA)
       cp_async_commit();
   }
@@ -271,8 +276,9 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
     {
       const int itn = it + kTmemStages - 1;
       if (itn < nck)
-        bwd_tmem_load_chunk<NP, VEC, TMA>(maps, p, smem + (itn % kTmemStages) * S::kStageFloats,
-                                          bars + itn % kTmemStages, last - itn, b, dblk0);
+        bwd_tmem_load_chunk<NP, VEC, TMA, FY>(maps, p,
+                                              smem + (itn % kTmemStages) * S::kStageFloats,
+                                              bars + itn % kTmemStages, last - itn, b, dblk0);
       else if constexpr (!TMA)
         cp_async_commit();
     }
@@ -281,7 +287,7 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
     const float* s_u = st + TILE;
     float* s_g = st + 2 * TILE;          // becomes d_y
     const float* s_dy = st + 3 * TILE;
-    const float* s_y = st + 4 * TILE;
+    float* s_y = st + 4 * TILE;   // y: loaded, or formed by the recompute (FY)
     const float* s_B = st + 5 * TILE;
     const float* s_C = s_B + kChunk * NP;
     const float* s_h0 = s_C + kChunk * NP;
@@ -291,54 +297,65 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
 
     // ---- 0. gating backward (Phase B2) and the duplicated B / C tiles --------------------
     // d_y = dy*g*s into the gate tile, d_gate = dy*y*s*(1 + g*(1-s)) straight to global memory
-    if constexpr (VEC) {   // four consecutive channels at a time (all inside d_inner or none)
-      static_assert(TILE % (4 * NTH) == 0, "tile must split evenly over the CTA");
+    // (and, in the fused call, out = y*g*s). The fused call runs it after the recompute, which
+    // forms y.
+    auto gating = [&]() {
+      if constexpr (VEC) {   // four consecutive channels at a time (all inside d_inner or none)
+        static_assert(TILE % (4 * NTH) == 0, "tile must split evenly over the CTA");
 #pragma unroll 2
-      for (int k = 0; k < TILE / (4 * NTH); ++k) {
-        const int e = 4 * (k * NTH + threadIdx.x);
-        const int i = e / DC, col = e % DC;
-        const bool ok = (t0 + i < T) && (dblk0 + col < Di);
-        const float4 yv = *reinterpret_cast<const float4*>(s_y + e);
-        const float4 g = *reinterpret_cast<const float4*>(s_g + e);
-        const float4 go = *reinterpret_cast<const float4*>(s_dy + e);
-        float4 dyo, dgo;
-        {
-          const float s0 = sigmoid_fast(g.x), s1 = sigmoid_fast(g.y);
-          const float s2 = sigmoid_fast(g.z), s3 = sigmoid_fast(g.w);
-          dyo = make_float4(go.x * (g.x * s0), go.y * (g.y * s1), go.z * (g.z * s2),
-                            go.w * (g.w * s3));
-          dgo = make_float4(go.x * yv.x * (s0 * fmaf(g.x, 1.f - s0, 1.f)),
-                            go.y * yv.y * (s1 * fmaf(g.y, 1.f - s1, 1.f)),
-                            go.z * yv.z * (s2 * fmaf(g.z, 1.f - s2, 1.f)),
-                            go.w * yv.w * (s3 * fmaf(g.w, 1.f - s3, 1.f)));
-        }
-        *reinterpret_cast<float4*>(s_g + e) = dyo;
-        st_global4_if(p.d_gate + (rowb + t0 + i) * Di + dblk0 + col, dgo, ok);
-        if (SP && ok) {   // raw -> delta, and the factor d_raw / d_delta
-          float* dl = const_cast<float*>(s_dl) + e;
-          float* fac = const_cast<float*>(s_dy) + e;
+        for (int k = 0; k < TILE / (4 * NTH); ++k) {
+          const int e = 4 * (k * NTH + threadIdx.x);
+          const int i = e / DC, col = e % DC;
+          const bool ok = (t0 + i < T) && (dblk0 + col < Di);
+          const float4 yv = *reinterpret_cast<const float4*>(s_y + e);
+          const float4 g = *reinterpret_cast<const float4*>(s_g + e);
+          const float4 go = *reinterpret_cast<const float4*>(s_dy + e);
+          float4 dyo, dgo;
+          {
+            const float s0 = sigmoid_fast(g.x), s1 = sigmoid_fast(g.y);
+            const float s2 = sigmoid_fast(g.z), s3 = sigmoid_fast(g.w);
+            dyo = make_float4(go.x * (g.x * s0), go.y * (g.y * s1), go.z * (g.z * s2),
+                              go.w * (g.w * s3));
+            dgo = make_float4(go.x * yv.x * (s0 * fmaf(g.x, 1.f - s0, 1.f)),
+                              go.y * yv.y * (s1 * fmaf(g.y, 1.f - s1, 1.f)),
+                              go.z * yv.z * (s2 * fmaf(g.z, 1.f - s2, 1.f)),
+                              go.w * yv.w * (s3 * fmaf(g.w, 1.f - s3, 1.f)));
+            if constexpr (FY)
+              st_global4_if(p.out + (rowb + t0 + i) * Di + dblk0 + col,
+                            make_float4(yv.x * (g.x * s0), yv.y * (g.y * s1), yv.z * (g.z * s2),
+                                        yv.w * (g.w * s3)),
+                            ok);
+          }
+          *reinterpret_cast<float4*>(s_g + e) = dyo;
+          st_global4_if(p.d_gate + (rowb + t0 + i) * Di + dblk0 + col, dgo, ok);
+          if (SP && ok) {   // raw -> delta, and the factor d_raw / d_delta
+            float* dl = const_cast<float*>(s_dl) + e;
+            float* fac = const_cast<float*>(s_dy) + e;
 #pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) softplus_both(dl[k4], dl[k4], fac[k4]);
+            for (int k4 = 0; k4 < 4; ++k4) softplus_both(dl[k4], dl[k4], fac[k4]);
+          }
         }
-      }
-    } else {
-      static_assert(TILE % NTH == 0, "tile must split evenly over the CTA");
+      } else {
+        static_assert(TILE % NTH == 0, "tile must split evenly over the CTA");
 #pragma unroll 4
-      for (int k = 0; k < TILE / NTH; ++k) {
-        const int e = k * NTH + threadIdx.x;
-        const int i = e / DC, col = e % DC;
-        const bool ok = (t0 + i < T) && (dblk0 + col < Di);
-        const size_t o = (rowb + t0 + i) * Di + dblk0 + col;
-        const float yv = s_y[e];
-        const float g = s_g[e], go = s_dy[e];
-        const float sg = sigmoid_fast(g);
-        s_g[e] = go * (g * sg);
-        st_global_if(p.d_gate + o, go * yv * (sg * fmaf(g, 1.f - sg, 1.f)), ok);
-        if (SP && ok) {   // raw -> delta, and the factor d_raw / d_delta
-          softplus_both(s_dl[e], const_cast<float*>(s_dl)[e], const_cast<float*>(s_dy)[e]);
+        for (int k = 0; k < TILE / NTH; ++k) {
+          const int e = k * NTH + threadIdx.x;
+          const int i = e / DC, col = e % DC;
+          const bool ok = (t0 + i < T) && (dblk0 + col < Di);
+          const size_t o = (rowb + t0 + i) * Di + dblk0 + col;
+          const float yv = s_y[e];
+          const float g = s_g[e], go = s_dy[e];
+          const float sg = sigmoid_fast(g);
+          s_g[e] = go * (g * sg);
+          st_global_if(p.d_gate + o, go * yv * (sg * fmaf(g, 1.f - sg, 1.f)), ok);
+          if constexpr (FY) st_global_if(p.out + o, yv * (g * sg), ok);
+          if (SP && ok) {   // raw -> delta, and the factor d_raw / d_delta
+            softplus_both(s_dl[e], const_cast<float*>(s_dl)[e], const_cast<float*>(s_dy)[e]);
+          }
         }
       }
-    }
+    };
+    if constexpr (!FY) gating();
     for (int e = threadIdx.x; e < kChunk * NP; e += NTH) {
       const float bv = s_B[e], cv = s_C[e];
       *reinterpret_cast<float2*>(s_Bw + 2 * e) = make_float2(bv, bv);
@@ -376,11 +393,12 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
     for (int i = 0; i < kChunk; ++i) {
       step_fence();
       tmem_st16(taddr + 16 * i, reinterpret_cast<const float2(&)[8]>(h));
-      float2 dl2[2], du2[2], B2[4];
+      float2 dl2[2], u2[2], du2[2], B2[4];
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         dl2[q] = pdl[q][i * DC / 2];
-        du2[q] = mul2(dl2[q], pu[q][i * DC / 2]);
+        u2[q] = pu[q][i * DC / 2];
+        du2[q] = mul2(dl2[q], u2[q]);
       }
 #pragma unroll
       for (int pp = 0; pp < 2; ++pp) {
@@ -395,8 +413,38 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
           const float2 da = ex2_2(mul2(dl2[q], a2[q][s]));
           h[q][s] = fma2(da, h[q][s], mul2(du2[q], B2[s]));
         }
+      if constexpr (FY) {   // y of this step: sum over n of C*h, then + D*u
+        float2 C2[4];
+#pragma unroll
+        for (int pp = 0; pp < 2; ++pp) {
+          const float4 v = pC[pp][i * NP / 2];
+          C2[2 * pp] = make_float2(v.x, v.y);
+          C2[2 * pp + 1] = make_float2(v.z, v.w);
+        }
+        float2 ya[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          ya[q] = mul2(C2[0], h[q][0]);
+#pragma unroll
+          for (int s = 1; s < 4; ++s) ya[q] = fma2(C2[s], h[q][s], ya[q]);
+        }
+        // same reduce-scatter as the d_delta sums: level G/2 over the channel pairs, level G/4
+        // inside the pair, then the remaining state lanes
+        ya[0] = make_float2(ya[0].x + __shfl_xor_sync(kFull, ya[1].x, G / 2),
+                            ya[0].y + __shfl_xor_sync(kFull, ya[1].y, G / 2));
+        float yv = (mx ? ya[0].y : ya[0].x) +
+                   __shfl_xor_sync(kFull, mx ? ya[0].x : ya[0].y, G / 4);
+#pragma unroll
+        for (int m = G / 8; m >= 1; m /= 2) yv += __shfl_xor_sync(kFull, yv, m);
+        if (w_delta) s_y[i * DC + cl + j_out] = fmaf(D_out, mx ? u2[0].y : u2[0].x, yv);
+      }
     }
     tmem_wait_st();
+    if constexpr (FY) {
+      __syncthreads();   // the y tile is complete
+      gating();
+      __syncthreads();   // d_y is in the gate tile
+    }
 
     // ---- 2. reverse walk (Phase B3) ------------------------------------------------------
     // output rows of this chunk for the lane's channel; rows at or past T are not stored
@@ -810,7 +858,8 @@ static bool make_maps(const Plan& plan, const BwdParams& p, BwdMaps* m) {
                   encode_f32(&mm.u, p.u, 3, dTD, sTD, bTD) &&
                   encode_f32(&mm.gate, p.gate, 3, dTD, sTD, bTD) &&
                   encode_f32(&mm.dy, p.dy, 3, dTD, sTD, bTD) &&
-                  encode_f32(&mm.y, p.y_ck, 3, dTD, sTD, bTD) &&
+                  // the fused call has no stored y: its map is never used
+                  encode_f32(&mm.y, p.y_ck ? p.y_ck : p.delta, 3, dTD, sTD, bTD) &&
                   encode_f32(&mm.B, p.B, 3, dTN, sTN, bTN) &&
                   encode_f32(&mm.C, p.C, 3, dTN, sTN, bTN) &&
                   encode_f32(&mm.ckpt, p.ckpt, 4, dCK, sCK, bCK);
@@ -836,8 +885,9 @@ template <int NP, bool VEC, bool TMA>
 static int launch_main(const Plan& plan, const BwdMaps& maps, const BwdParams& p,
                        cudaStream_t s) {
   using S = BwdTmemShape<NP>;
-  auto kern = p.softplus ? scan_bwd_tmem_kernel<NP, VEC, TMA, true>
-                         : scan_bwd_tmem_kernel<NP, VEC, TMA, false>;
+  auto kern = p.out        ? scan_bwd_tmem_kernel<NP, VEC, TMA, false, true>
+              : p.softplus ? scan_bwd_tmem_kernel<NP, VEC, TMA, true, false>
+                           : scan_bwd_tmem_kernel<NP, VEC, TMA, false, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)S::kSmemBytes) != cudaSuccess)
     return -1;

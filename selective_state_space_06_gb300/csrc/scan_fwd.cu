@@ -44,7 +44,7 @@ struct FwdShape {
   static constexpr size_t kSmemBytes = (size_t)kFwdStages * kStageFloats * sizeof(float);
 };
 
-template <int NP, bool VEC>
+template <int NP, bool VEC, bool ST = false>
 __device__ __forceinline__ void fwd_load_chunk(const FwdParams& p, float* st, int c, int b,
                                                int dblk0) {
   using S = FwdShape<NP>;
@@ -64,7 +64,7 @@ __device__ __forceinline__ void fwd_load_chunk(const FwdParams& p, float* st, in
       const size_t go = v ? (rowb + t) * p.Di + d : 0;
       cp_async16(s_dl + i * DC + col, p.delta + go, v);
       cp_async16(s_u + i * DC + col, p.u + go, v);
-      cp_async16(s_g + i * DC + col, p.gate + go, v);
+      if constexpr (!ST) cp_async16(s_g + i * DC + col, p.gate + go, v);
     }
     for (int q = threadIdx.x; q < kChunk * NP / 4; q += NTH) {
       const int i = q / (NP / 4), n = (q % (NP / 4)) * 4;
@@ -72,7 +72,7 @@ __device__ __forceinline__ void fwd_load_chunk(const FwdParams& p, float* st, in
       const bool v = t < p.T && n < p.N;
       const size_t go = v ? (rowb + t) * p.N + n : 0;
       cp_async16(s_B + i * NP + n, p.B + go, v);
-      cp_async16(s_C + i * NP + n, p.C + go, v);
+      if constexpr (!ST) cp_async16(s_C + i * NP + n, p.C + go, v);
     }
   } else {
     for (int q = threadIdx.x; q < kChunk * DC; q += NTH) {
@@ -82,7 +82,7 @@ __device__ __forceinline__ void fwd_load_chunk(const FwdParams& p, float* st, in
       const size_t go = v ? (rowb + t) * p.Di + d : 0;
       cp_async4(s_dl + i * DC + col, p.delta + go, v);
       cp_async4(s_u + i * DC + col, p.u + go, v);
-      cp_async4(s_g + i * DC + col, p.gate + go, v);
+      if constexpr (!ST) cp_async4(s_g + i * DC + col, p.gate + go, v);
     }
     for (int q = threadIdx.x; q < kChunk * NP; q += NTH) {
       const int i = q / NP, n = q % NP;
@@ -90,7 +90,7 @@ __device__ __forceinline__ void fwd_load_chunk(const FwdParams& p, float* st, in
       const bool v = t < p.T && n < p.N;
       const size_t go = v ? (rowb + t) * p.N + n : 0;
       cp_async4(s_B + i * NP + n, p.B + go, v);
-      cp_async4(s_C + i * NP + n, p.C + go, v);
+      if constexpr (!ST) cp_async4(s_C + i * NP + n, p.C + go, v);
     }
   }
   cp_async_commit();
@@ -226,9 +226,12 @@ scan_fwd_agg_kernel(const FwdParams p) {
   cp_async_wait<0>();
 }
 
-template <int NP, bool VEC, bool WITH_Y, bool SP>
+// ST (states only, for the fused forward + backward call): the recurrence and the checkpoints
+// alone; the backward then recomputes y from the states and writes out.
+template <int NP, bool VEC, bool WITH_Y, bool SP, bool ST>
 __global__ void __launch_bounds__(kWarps * 32)
 scan_fwd_kernel(const FwdParams p) {
+  static_assert(!(ST && (SP || WITH_Y)), "the states-only forward takes the plain delta");
   using S = FwdShape<NP>;
   constexpr int G = S::G, DW = S::DW, DC = S::DC, P = S::P, NPT = S::NPT, NPR = S::NPR;
   extern __shared__ __align__(16) float smem[];
@@ -273,7 +276,7 @@ scan_fwd_kernel(const FwdParams p) {
 #pragma unroll
   for (int s = 0; s < kFwdStages - 1; ++s) {
     if (c_begin + s < c_end)
-      fwd_load_chunk<NP, VEC>(p, smem + s * S::kStageFloats, c_begin + s, b, dblk0);
+      fwd_load_chunk<NP, VEC, ST>(p, smem + s * S::kStageFloats, c_begin + s, b, dblk0);
     else
       cp_async_commit();
   }
@@ -316,8 +319,8 @@ scan_fwd_kernel(const FwdParams p) {
     {
       const int cn = c + kFwdStages - 1;
       if (cn < c_end)
-        fwd_load_chunk<NP, VEC>(p, smem + ((it + kFwdStages - 1) % kFwdStages) * S::kStageFloats,
-                                cn, b, dblk0);
+        fwd_load_chunk<NP, VEC, ST>(p, smem + ((it + kFwdStages - 1) % kFwdStages) * S::kStageFloats,
+                                    cn, b, dblk0);
       else
         cp_async_commit();
     }
@@ -333,47 +336,66 @@ scan_fwd_kernel(const FwdParams p) {
     const float* s_C = s_B + kChunk * NP;
     const int t0 = c * kChunk;
 
-#pragma unroll
-    for (int gi = 0; gi < kChunk / P; ++gi) {
-      float yv[2 * P];
-#pragma unroll
-      for (int tt = 0; tt < P; ++tt) {
-        const int i = gi * P + tt;
+    if constexpr (ST) {
+#pragma unroll 4
+      for (int i = 0; i < kChunk; ++i) {
         const float2 dlv = lds2(s_dl + i * DC + cl);
         const float2 uv = lds2(s_u + i * DC + cl);
-        float2 Bp[NPR], Cp[NPR];
+        float2 Bp[NPR];
         lds_pairs<NPR>(s_B + i * NP + n0, Bp);
-        lds_pairs<NPR>(s_C + i * NP + n0, Cp);
 #pragma unroll
         for (int j = 0; j < kDPT; ++j) {
           const float dl = j ? dlv.y : dlv.x;
           const float uu = j ? uv.y : uv.x;
           const float2 dl2 = splat2(dl), du2 = splat2(dl * uu);
-          float2 ya = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int pp = 0; pp < NPR; ++pp) {
-            const float2 da = ex2_2(mul2(dl2, a2[j][pp]));
-            h[j][pp] = fma2(da, h[j][pp], mul2(du2, Bp[pp]));
-            ya = fma2(Cp[pp], h[j][pp], ya);
-          }
-          yv[tt * 2 + j] = ya.x + ya.y;
+          for (int pp = 0; pp < NPR; ++pp)
+            h[j][pp] = fma2(ex2_2(mul2(dl2, a2[j][pp])), h[j][pp], mul2(du2, Bp[pp]));
         }
       }
-      RSy::run(yv, lane);
+    } else {
 #pragma unroll
-      for (int r = 0; r < kY; ++r) {
-        const int idx = ybase + r;
-        const int tt = idx >> 1, j = idx & 1;
-        const int i = gi * P + tt;
-        const int t = t0 + i, d = d0 + j;
-        const float uu = s_u[i * DC + cl + j];
-        const float g = s_g[i * DC + cl + j];
-        const float y = fmaf(j ? Dd[1] : Dd[0], uu, yv[r]);
-        const bool ok = (t < T) && (d < Di);
-        const size_t o = (rowb + t) * Di + d;
-        st_global_if(p.out + o, y * (g * sigmoid_fast(g)), ok);
-        st_global_if(p.y_ck + o, y, ok);            // kept for the backward's d_gate
-        if constexpr (WITH_Y) st_global_if(p.y + o, y, ok);
+      for (int gi = 0; gi < kChunk / P; ++gi) {
+        float yv[2 * P];
+#pragma unroll
+        for (int tt = 0; tt < P; ++tt) {
+          const int i = gi * P + tt;
+          const float2 dlv = lds2(s_dl + i * DC + cl);
+          const float2 uv = lds2(s_u + i * DC + cl);
+          float2 Bp[NPR], Cp[NPR];
+          lds_pairs<NPR>(s_B + i * NP + n0, Bp);
+          lds_pairs<NPR>(s_C + i * NP + n0, Cp);
+#pragma unroll
+          for (int j = 0; j < kDPT; ++j) {
+            const float dl = j ? dlv.y : dlv.x;
+            const float uu = j ? uv.y : uv.x;
+            const float2 dl2 = splat2(dl), du2 = splat2(dl * uu);
+            float2 ya = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int pp = 0; pp < NPR; ++pp) {
+              const float2 da = ex2_2(mul2(dl2, a2[j][pp]));
+              h[j][pp] = fma2(da, h[j][pp], mul2(du2, Bp[pp]));
+              ya = fma2(Cp[pp], h[j][pp], ya);
+            }
+            yv[tt * 2 + j] = ya.x + ya.y;
+          }
+        }
+        RSy::run(yv, lane);
+#pragma unroll
+        for (int r = 0; r < kY; ++r) {
+          const int idx = ybase + r;
+          const int tt = idx >> 1, j = idx & 1;
+          const int i = gi * P + tt;
+          const int t = t0 + i, d = d0 + j;
+          const float uu = s_u[i * DC + cl + j];
+          const float g = s_g[i * DC + cl + j];
+          const float y = fmaf(j ? Dd[1] : Dd[0], uu, yv[r]);
+          const bool ok = (t < T) && (d < Di);
+          const size_t o = (rowb + t) * Di + d;
+          st_global_if(p.out + o, y * (g * sigmoid_fast(g)), ok);
+          st_global_if(p.y_ck + o, y, ok);            // kept for the backward's d_gate
+          if constexpr (WITH_Y) st_global_if(p.y + o, y, ok);
+        }
       }
     }
 
@@ -400,8 +422,9 @@ template <int NP, bool VEC, bool WITH_Y>
 static int launch_np(const Plan& plan, const FwdParams& p0, cudaStream_t s) {
   FwdParams p = p0;
   using S = FwdShape<NP>;
-  auto kern = p0.softplus ? scan_fwd_kernel<NP, VEC, WITH_Y, true>
-                          : scan_fwd_kernel<NP, VEC, WITH_Y, false>;
+  auto kern = p0.states_only ? scan_fwd_kernel<NP, VEC, false, false, true>
+             : p0.softplus   ? scan_fwd_kernel<NP, VEC, WITH_Y, true, false>
+                             : scan_fwd_kernel<NP, VEC, WITH_Y, false, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)S::kSmemBytes) != cudaSuccess)
     return -1;

@@ -87,6 +87,7 @@ struct FwdParams {
   int batch, T, Di, N, nchunks, nblk, seg_chunks, nseg;
   int agg_k;                     // pre-pass: consecutive segments per CTA
   int softplus;                  // delta holds the raw delta: the kernels apply softplus
+  int states_only;               // checkpoints only: no C, gate reads, no out, y (fused call)
 };
 
 struct BwdParams {
@@ -100,6 +101,8 @@ struct BwdParams {
   int batch, T, Di, N, nchunks, nblk, seg_chunks, nseg;
   int sub_chunks, nsub;            // pre-pass sub-segments (see PassPlan)
   int softplus;                    // delta holds the raw delta; d_delta receives d_raw
+  float* out;   // fused call: the backward recomputes y from the states and writes out (y_ck
+                // unused); null otherwise
 };
 
 // TMA descriptors of the tensor-memory backward, encoded on the host for each call:
