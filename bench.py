@@ -376,6 +376,32 @@ def run_gpu(args):
         variants["fused_fwd_bwd"] = {"ms_per_step": ms_fu, "value": w.btd / (ms_fu * 1e-3),
                                      "unit": UNIT, "steps": kv,
                                      "launches": ms.mamba_scan_last_launch_count()}
+        # variant: the fused call with bf16 I/O (inputs rounded to bf16; fp32 arithmetic)
+        if w.d_state % 8 == 0 and w.d_inner % 8 == 0 and 9 <= w.d_state <= 64 and w.T > 16:
+            bf = {k: x[k].to(torch.bfloat16) for k in ("delta", "u", "B", "C", "gate", "dy")}
+            ob = {k: torch.empty_like(bf["delta"]) for k in ("out", "d_delta", "d_u", "d_gate")}
+            ob["d_B"] = torch.empty_like(bf["B"])
+            ob["d_C"] = torch.empty_like(bf["C"])
+
+            def step_bf16():
+                ms.mamba_scan_fwd_bwd_bf16(bf["delta"], bf["u"], bf["B"], bf["C"], bf["gate"],
+                                           x["A_log"], x["D"], bf["dy"], ob["out"], bufs["ckpt"],
+                                           bufs["scratch"], ob["d_delta"], ob["d_u"], ob["d_B"],
+                                           ob["d_C"], bufs["d_A_log"], bufs["d_D"],
+                                           ob["d_gate"], stream=stream)
+            for _ in range(3):
+                step_bf16()
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(kv):
+                step_bf16()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms_bf = e0.elapsed_time(e1) / kv
+            variants["fused_fwd_bwd_bf16"] = {"ms_per_step": ms_bf,
+                                              "value": w.btd / (ms_bf * 1e-3), "unit": UNIT,
+                                              "steps": kv, "io": "bf16", "arithmetic": "f32"}
+            del bf, ob
         variants["conv1d_silu"] = time_conv(ms, w, dev, stream, kv, read_peaks()["hbm_gbs"])
 
     mb = minimal_bytes(w)

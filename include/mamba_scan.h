@@ -58,7 +58,8 @@ extern "C" {
 #define MAMBA_ERR_MISALIGNED 2  /* a pointer is not 16-byte aligned                          */
 #define MAMBA_ERR_WORKSPACE 3   /* checkpoint or scratch buffer smaller than required        */
 #define MAMBA_ERR_CUDA 4        /* a CUDA runtime call or kernel launch failed               */
-#define MAMBA_ERR_UNSUPPORTED 5 /* d_state outside 1..64                                     */
+#define MAMBA_ERR_UNSUPPORTED 5 /* d_state outside 1..64, or sizes a variant does not take
+                                   (mamba_scan_fwd_bwd_bf16, mamba_conv_*)                   */
 #define MAMBA_ERR_NOALLOC_LIMIT 6 /* mamba_scan_bwd_noalloc: the sizes need more scratch than
                                      MAMBA_SCAN_NOALLOC_SCRATCH_BYTES                        */
 #define MAMBA_ERR_TIMEOUT 7     /* reported by mamba_scan_status: a kernel gave up waiting
@@ -135,6 +136,22 @@ int mamba_scan_fwd_bwd(const float* delta, const float* u, const float* B, const
                        size_t scratch_bytes, float* d_delta, float* d_u, float* d_B, float* d_C,
                        float* d_A_log, float* d_D, float* d_gate, int64_t batch, int64_t T,
                        int64_t d_inner, int64_t d_state, void* stream);
+
+/* mamba_scan_fwd_bwd with bf16 I/O: delta, u, B, C, gate, dy and the outputs out, d_delta, d_u,
+ * d_B, d_C, d_gate are bfloat16 (2 bytes per element, same layouts); A_log, D, d_A_log and d_D
+ * stay fp32, and so do the checkpoint and scratch buffers (same sizes as for fp32). The
+ * kernels widen the inputs to fp32 in shared memory, compute everything in fp32 exactly as the
+ * fp32 call does, and round each bf16 output once, to nearest even. Takes 9 <= d_state <= 64,
+ * d_inner and d_state multiples of 8 and T > 16 (bf16 rows then start on 16-byte boundaries,
+ * which the tensor-memory copies need); other sizes return MAMBA_ERR_UNSUPPORTED before
+ * anything is launched. Pointers must be 16-byte aligned. */
+int mamba_scan_fwd_bwd_bf16(const void* delta, const void* u, const void* B, const void* C,
+                            const void* gate, const float* A_log, const float* D,
+                            const void* dy, void* out, void* ckpt, size_t ckpt_bytes,
+                            void* scratch, size_t scratch_bytes, void* d_delta, void* d_u,
+                            void* d_B, void* d_C, float* d_A_log, float* d_D, void* d_gate,
+                            int64_t batch, int64_t T, int64_t d_inner, int64_t d_state,
+                            void* stream);
 
 /* Causal depthwise conv1d + SiLU, the step that feeds u to the scan (the page's Phase B6 is
  * its backward):

@@ -43,6 +43,7 @@ EXPORTED = (
     "mamba_scan_host_workspace_bytes", "mamba_scan_fwd_bwd_host", "mamba_scan_status",
     "mamba_scan_strerror", "mamba_scan_last_launch_count", "mamba_scan_bwd_noalloc",
     "mamba_scan_fwd_softplus", "mamba_scan_bwd_softplus", "mamba_scan_fwd_bwd",
+    "mamba_scan_fwd_bwd_bf16",
     "mamba_conv_scratch_bytes", "mamba_conv_fwd", "mamba_conv_bwd",
 )
 
@@ -72,6 +73,8 @@ _lib.mamba_scan_bwd_softplus.argtypes = _lib.mamba_scan_bwd.argtypes
 _lib.mamba_scan_bwd_softplus.restype = ctypes.c_int
 _lib.mamba_scan_fwd_bwd.argtypes = [_vp] * 10 + [_sz, _vp, _sz] + [_vp] * 7 + [_i64] * 4 + [_vp]
 _lib.mamba_scan_fwd_bwd.restype = ctypes.c_int
+_lib.mamba_scan_fwd_bwd_bf16.argtypes = _lib.mamba_scan_fwd_bwd.argtypes
+_lib.mamba_scan_fwd_bwd_bf16.restype = ctypes.c_int
 _lib.mamba_scan_bwd_noalloc.argtypes = [_vp] * 9 + [_sz] + [_vp] * 7 + [_i64] * 4 + [_vp]
 _lib.mamba_scan_bwd_noalloc.restype = ctypes.c_int
 _lib.mamba_scan_fwd_bwd_host.argtypes = [_vp] * 17 + [_sz] + [_i64] * 4 + [_vp]
@@ -115,14 +118,15 @@ def mamba_scan_last_launch_count() -> int:
     return int(_lib.mamba_scan_last_launch_count())
 
 
-def _ptr(t, name, device=None, allow_none=False, host=False):
+def _ptr(t, name, device=None, allow_none=False, host=False, dtype=None):
     if t is None:
         if allow_none:
             return None
         raise ValueError(f"{name} is required")
     import torch
-    if t.dtype != torch.float32 and name not in ("ckpt", "scratch", "workspace"):
-        raise TypeError(f"{name} must be float32, got {t.dtype}")
+    want = torch.float32 if dtype is None else dtype
+    if t.dtype != want and name not in ("ckpt", "scratch", "workspace"):
+        raise TypeError(f"{name} must be {want}, got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if host:
@@ -219,6 +223,29 @@ def mamba_scan_fwd_bwd(delta, u, B, C, gate, A_log, D, dy, out, ckpt, scratch, d
         _ptr(d_gate, "d_gate", dev), b, T, Di, N, _stream_ptr(stream, dev))
     if rc != MAMBA_OK:
         raise MambaScanError(rc, "mamba_scan_fwd_bwd")
+
+
+def mamba_scan_fwd_bwd_bf16(delta, u, B, C, gate, A_log, D, dy, out, ckpt, scratch, d_delta,
+                            d_u, d_B, d_C, d_A_log, d_D, d_gate, stream=None):
+    """mamba_scan_fwd_bwd with bf16 I/O: delta, u, B, C, gate, dy, out, d_delta, d_u, d_B, d_C
+    and d_gate are torch.bfloat16; A_log, D, d_A_log, d_D float32. Needs 9 <= d_state <= 64,
+    d_inner and d_state multiples of 8 and T > 16."""
+    import torch
+    b, T, Di, N = _dims(delta, B)
+    dev = delta.device
+    h = dict(dtype=torch.bfloat16)
+    ck_bytes = 0 if ckpt is None else ckpt.numel() * ckpt.element_size()
+    rc = _lib.mamba_scan_fwd_bwd_bf16(
+        _ptr(delta, "delta", dev, **h), _ptr(u, "u", dev, **h), _ptr(B, "B", dev, **h),
+        _ptr(C, "C", dev, **h), _ptr(gate, "gate", dev, **h), _ptr(A_log, "A_log", dev),
+        _ptr(D, "D", dev), _ptr(dy, "dy", dev, **h), _ptr(out, "out", dev, **h),
+        _ptr(ckpt, "ckpt", dev, allow_none=True), ck_bytes, _ptr(scratch, "scratch", dev),
+        scratch.numel() * scratch.element_size(), _ptr(d_delta, "d_delta", dev, **h),
+        _ptr(d_u, "d_u", dev, **h), _ptr(d_B, "d_B", dev, **h), _ptr(d_C, "d_C", dev, **h),
+        _ptr(d_A_log, "d_A_log", dev), _ptr(d_D, "d_D", dev), _ptr(d_gate, "d_gate", dev, **h),
+        b, T, Di, N, _stream_ptr(stream, dev))
+    if rc != MAMBA_OK:
+        raise MambaScanError(rc, "mamba_scan_fwd_bwd_bf16")
 
 
 def mamba_scan_bwd_noalloc(delta, u, B, C, gate, A_log, D, dy, ckpt, d_delta, d_u, d_B, d_C,

@@ -246,7 +246,7 @@ static int scan_fwd_impl(const float* delta, const float* u, const float* B, con
                          const float* gate, const float* A_log, const float* D, float* out,
                          float* y, void* ckpt, size_t ckpt_bytes, int64_t batch, int64_t T,
                          int64_t d_inner, int64_t d_state, void* stream, int softplus,
-                         int states_only = 0) {
+                         int states_only = 0, int io_bf16 = 0) {
   Plan plan;
   int rc = check_dims(batch, T, d_inner, d_state, &plan);
   if (rc != MAMBA_OK) return rc;
@@ -258,7 +258,7 @@ static int scan_fwd_impl(const float* delta, const float* u, const float* B, con
   for (const void* q : ptrs)
     if (q && !aligned16(q)) return MAMBA_ERR_MISALIGNED;
   if (ckpt_bytes < need_ck) return MAMBA_ERR_WORKSPACE;
-  const size_t btd = (size_t)batch * T * d_inner * sizeof(float);
+  const size_t btd = (size_t)batch * T * d_inner * (io_bf16 ? 2 : sizeof(float));
   if (out) {
     Range ro = {(uintptr_t)out, (uintptr_t)out + btd};
     if (y && overlaps(ro, Range{(uintptr_t)y, (uintptr_t)y + btd})) return MAMBA_ERR_INVALID_ARG;
@@ -277,6 +277,7 @@ static int scan_fwd_impl(const float* delta, const float* u, const float* B, con
   p.agg_k = 1;
   p.softplus = softplus;
   p.states_only = states_only;
+  p.io_bf16 = io_bf16;
   const int n = mscan::launch_fwd(plan, p, (cudaStream_t)stream);
   if (n < 0) return set_cuda_error(cudaGetLastError());
   g_last_launches = n;
@@ -307,7 +308,7 @@ static int scan_bwd_impl(const float* delta, const float* u, const float* B, con
                          float* d_C, float* d_A_log, float* d_D, float* d_gate, int64_t batch,
                          int64_t T, int64_t d_inner, int64_t d_state, void* stream,
                          int softplus, float* out = nullptr, bool fuse_out = false,
-                         bool check_only = false) {
+                         bool check_only = false, int io_bf16 = 0) {
   Plan plan;
   int rc = check_dims(batch, T, d_inner, d_state, &plan);
   if (rc != MAMBA_OK) return rc;
@@ -323,8 +324,9 @@ static int scan_bwd_impl(const float* delta, const float* u, const float* B, con
     if (q && !aligned16(q)) return MAMBA_ERR_MISALIGNED;
   if (ckpt_bytes < need_ck || scratch_bytes < need_sc) return MAMBA_ERR_WORKSPACE;
   {
-    const size_t btd = (size_t)batch * T * d_inner * sizeof(float);
-    const size_t btn = (size_t)batch * T * d_state * sizeof(float);
+    const size_t es = io_bf16 ? 2 : sizeof(float);   // element size of the I/O tensors
+    const size_t btd = (size_t)batch * T * d_inner * es;
+    const size_t btn = (size_t)batch * T * d_state * es;
     const Range outs[] = {
         {(uintptr_t)d_delta, (uintptr_t)d_delta + btd},
         {(uintptr_t)d_u, (uintptr_t)d_u + btd},
@@ -359,6 +361,7 @@ static int scan_bwd_impl(const float* delta, const float* u, const float* B, con
   p.softplus = softplus;
   p.out = fuse_out ? out : nullptr;
   if (fuse_out) p.y_ck = nullptr;   // y is recomputed from the states
+  p.io_bf16 = io_bf16;
   const int n = mscan::launch_bwd(plan, p, (cudaStream_t)stream);
   if (n < 0) return set_cuda_error(cudaGetLastError());
   g_last_launches = n;
@@ -388,33 +391,62 @@ int mamba_scan_bwd_softplus(const float* delta_raw, const float* u, const float*
                        T, d_inner, d_state, stream, 1);
 }
 
-int mamba_scan_fwd_bwd(const float* delta, const float* u, const float* B, const float* C,
-                       const float* gate, const float* A_log, const float* D, const float* dy,
-                       float* out, void* ckpt, size_t ckpt_bytes, void* scratch,
-                       size_t scratch_bytes, float* d_delta, float* d_u, float* d_B, float* d_C,
-                       float* d_A_log, float* d_D, float* d_gate, int64_t batch, int64_t T,
-                       int64_t d_inner, int64_t d_state, void* stream) {
+static int fwd_bwd_impl(const float* delta, const float* u, const float* B, const float* C,
+                        const float* gate, const float* A_log, const float* D, const float* dy,
+                        float* out, void* ckpt, size_t ckpt_bytes, void* scratch,
+                        size_t scratch_bytes, float* d_delta, float* d_u, float* d_B,
+                        float* d_C, float* d_A_log, float* d_D, float* d_gate, int64_t batch,
+                        int64_t T, int64_t d_inner, int64_t d_state, void* stream, int io_bf16) {
   if (!out) return MAMBA_ERR_INVALID_ARG;
   // everything is checked before the first launch
   int rc = scan_bwd_impl(delta, u, B, C, gate, A_log, D, dy, ckpt, ckpt_bytes, scratch,
                          scratch_bytes, d_delta, d_u, d_B, d_C, d_A_log, d_D, d_gate, batch, T,
-                         d_inner, d_state, stream, 0, out, false, true);
+                         d_inner, d_state, stream, 0, out, false, true, io_bf16);
   if (rc != MAMBA_OK) return rc;
   Plan plan;
   if (!mscan::make_plan(batch, T, d_inner, d_state, &plan)) return MAMBA_ERR_INVALID_ARG;
   // d_state 9..64 (the tensor-memory backward): the forward keeps only the checkpoints and the
   // backward forms y and out; smaller d_state runs the two passes as separate calls do
   const bool fused = plan.NP >= mscan::kTmemMinNP;
+  // bf16 I/O: the fused path with TMA staging only (16-byte rows of bf16, two chunks or more)
+  if (io_bf16 && (!fused || d_inner % 8 != 0 || d_state % 8 != 0 || plan.nchunks < 2))
+    return MAMBA_ERR_UNSUPPORTED;
   rc = scan_fwd_impl(delta, u, B, C, gate, A_log, D, out, nullptr, ckpt, ckpt_bytes, batch, T,
-                     d_inner, d_state, stream, 0, fused ? 1 : 0);
+                     d_inner, d_state, stream, 0, fused ? 1 : 0, io_bf16);
   if (rc != MAMBA_OK) return rc;
   const int nf = g_last_launches;
   rc = scan_bwd_impl(delta, u, B, C, gate, A_log, D, dy, ckpt, ckpt_bytes, scratch,
                      scratch_bytes, d_delta, d_u, d_B, d_C, d_A_log, d_D, d_gate, batch, T,
-                     d_inner, d_state, stream, 0, out, fused, false);
+                     d_inner, d_state, stream, 0, out, fused, false, io_bf16);
   if (rc != MAMBA_OK) return rc;
   g_last_launches += nf;
   return MAMBA_OK;
+}
+
+int mamba_scan_fwd_bwd(const float* delta, const float* u, const float* B, const float* C,
+                       const float* gate, const float* A_log, const float* D, const float* dy,
+                       float* out, void* ckpt, size_t ckpt_bytes, void* scratch,
+                       size_t scratch_bytes, float* d_delta, float* d_u, float* d_B, float* d_C,
+                       float* d_A_log, float* d_D, float* d_gate, int64_t batch, int64_t T,
+                       int64_t d_inner, int64_t d_state, void* stream) {
+  return fwd_bwd_impl(delta, u, B, C, gate, A_log, D, dy, out, ckpt, ckpt_bytes, scratch,
+                      scratch_bytes, d_delta, d_u, d_B, d_C, d_A_log, d_D, d_gate, batch, T,
+                      d_inner, d_state, stream, 0);
+}
+
+int mamba_scan_fwd_bwd_bf16(const void* delta, const void* u, const void* B, const void* C,
+                            const void* gate, const float* A_log, const float* D,
+                            const void* dy, void* out, void* ckpt, size_t ckpt_bytes,
+                            void* scratch, size_t scratch_bytes, void* d_delta, void* d_u,
+                            void* d_B, void* d_C, float* d_A_log, float* d_D, void* d_gate,
+                            int64_t batch, int64_t T, int64_t d_inner, int64_t d_state,
+                            void* stream) {
+  // the kernels take the bf16 tensors through the same parameter slots (io_bf16 set)
+  auto in = [](const void* q) { return static_cast<const float*>(q); };
+  auto io = [](void* q) { return static_cast<float*>(q); };
+  return fwd_bwd_impl(in(delta), in(u), in(B), in(C), in(gate), A_log, D, in(dy), io(out), ckpt,
+                      ckpt_bytes, scratch, scratch_bytes, io(d_delta), io(d_u), io(d_B), io(d_C),
+                      d_A_log, d_D, io(d_gate), batch, T, d_inner, d_state, stream, 1);
 }
 
 size_t mamba_scan_host_workspace_bytes(int64_t batch, int64_t T, int64_t d_inner,

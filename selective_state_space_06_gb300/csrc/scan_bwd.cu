@@ -640,8 +640,14 @@ __global__ void scan_reduce_kernel(const BwdParams p) {
         sb += p.partB[(size_t)k * btn + e];
         sc += p.partC[(size_t)k * btn + e];
       }
-      p.d_B[e] = sb;
-      p.d_C[e] = sc;
+      if (p.io_bf16) {   // the fused bf16 call: d_B, d_C in bf16 (rounded to nearest even)
+        const uint32_t w = pack_bf16x2(sb, sc);
+        reinterpret_cast<uint16_t*>(p.d_B)[e] = (uint16_t)(w & 0xffffu);
+        reinterpret_cast<uint16_t*>(p.d_C)[e] = (uint16_t)(w >> 16);
+      } else {
+        p.d_B[e] = sb;
+        p.d_C[e] = sc;
+      }
     } else if (e < btn + dn) {
       const size_t q = e - btn;
       float sa = 0.f;

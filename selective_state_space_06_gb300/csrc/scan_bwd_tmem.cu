@@ -75,7 +75,7 @@ static __device__ unsigned int g_bwd_fault;   // set when a bounded wait gave up
 
 // Stage layout: delta, u, gate, dy, y tiles, then B, C, then the checkpoint row. FY (the fused
 // call) leaves the y tile to the kernel, which fills it from the recomputed states.
-template <int NP, bool VEC, bool TMA, bool FY = false>
+template <int NP, bool VEC, bool TMA, bool FY = false, bool BF = false>
 __device__ __forceinline__ void bwd_tmem_load_chunk(const BwdMaps& maps, const BwdParams& p,
                                                     float* st, uint64_t* bar, int c, int b,
                                                     int dblk0) {
@@ -85,9 +85,14 @@ __device__ __forceinline__ void bwd_tmem_load_chunk(const BwdMaps& maps, const B
   float* s_h0 = st + 5 * TILE + 2 * kChunk * NP;
   if constexpr (TMA) {
     // one thread issues the whole stage; rows past T, channels past d_inner, states past
-    // d_state and the (absent) checkpoint before chunk 0 arrive as zeros
+    // d_state and the (absent) checkpoint before chunk 0 arrive as zeros. With BF the tiles
+    // are bf16 and land in the first half of their slots; the checkpoint row stays fp32.
+    constexpr uint32_t kEl = BF ? 2u : 4u;
+    constexpr uint32_t kBytes = (4u * TILE + (FY ? 0u : TILE) + 2u * kChunk * NP) * kEl +
+                                (uint32_t)(DC * NP) * 4u;
+    static_assert(BF || kBytes == S::kStageBytes - (FY ? TILE * 4u : 0u), "stage bytes");
     if (threadIdx.x == 0) {
-      mbar_expect_tx(bar, S::kStageBytes - (FY ? TILE * (uint32_t)sizeof(float) : 0u));
+      mbar_expect_tx(bar, kBytes);
       tma_load_3d(st, &maps.delta, bar, dblk0, t0, b);
       tma_load_3d(st + TILE, &maps.u, bar, dblk0, t0, b);
       tma_load_3d(st + 2 * TILE, &maps.gate, bar, dblk0, t0, b);
@@ -142,10 +147,13 @@ __device__ __forceinline__ void bwd_tmem_wait_stage(uint64_t* bars, int stage, i
 // FY: the fused forward + backward call. The forward wrote only the checkpoints, so the
 // recompute also forms y = sum_n C*h + D*u (a reduce-scatter over the state lanes, as for the
 // d_delta sums) into the y tile, and the gating step runs after it and writes out as well.
-template <int NP, bool VEC, bool TMA, bool SP, bool FY>
+// BF (fused bf16 call): delta, u, gate, dy, B, C arrive as bf16 and are widened in shared
+// memory; out, d_gate, d_delta and d_u are stored as bf16.
+template <int NP, bool VEC, bool TMA, bool SP, bool FY, bool BF = false>
 __global__ void __launch_bounds__(kWarps * 32, 2)
 scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
   static_assert(!(SP && FY), "the fused call takes the plain delta");
+  static_assert(!BF || (FY && TMA && VEC), "bf16 I/O is the fused call's, with TMA staging");
   using S = BwdTmemShape<NP>;
   constexpr int G = S::G, LG = S::LG, DW = S::DW, DC = S::DC, TILE = S::TILE;
   constexpr int NTH = kWarps * 32;
@@ -180,8 +188,8 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
 #pragma unroll
   for (int s = 0; s < kTmemStages - 1; ++s) {
     if (s < nck)
-      bwd_tmem_load_chunk<NP, VEC, TMA, FY>(maps, p, smem + s * S::kStageFloats, bars + s,
-                                            last - s, b, dblk0);
+      bwd_tmem_load_chunk<NP, VEC, TMA, FY, BF>(maps, p, smem + s * S::kStageFloats, bars + s,
+                                                last - s, b, dblk0);
     else if constexpr (!TMA)
       cp_async_commit();
   }
@@ -276,13 +284,31 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
     {
       const int itn = it + kTmemStages - 1;
       if (itn < nck)
-        bwd_tmem_load_chunk<NP, VEC, TMA, FY>(maps, p,
-                                              smem + (itn % kTmemStages) * S::kStageFloats,
-                                              bars + itn % kTmemStages, last - itn, b, dblk0);
+        bwd_tmem_load_chunk<NP, VEC, TMA, FY, BF>(maps, p,
+                                                  smem + (itn % kTmemStages) * S::kStageFloats,
+                                                  bars + itn % kTmemStages, last - itn, b, dblk0);
       else if constexpr (!TMA)
         cp_async_commit();
     }
     float* st = smem + (it % kTmemStages) * S::kStageFloats;
+    if constexpr (BF) {   // widen the bf16 tiles in place (the checkpoint row is fp32)
+      BfTile<TILE, NTH> w0, w1, w2, w3;
+      BfTile<kChunk * NP, NTH> wB, wC;
+      w0.read(st);
+      w1.read(st + TILE);
+      w2.read(st + 2 * TILE);
+      w3.read(st + 3 * TILE);
+      wB.read(st + 5 * TILE);
+      wC.read(st + 5 * TILE + kChunk * NP);
+      __syncthreads();
+      w0.write(st);
+      w1.write(st + TILE);
+      w2.write(st + 2 * TILE);
+      w3.write(st + 3 * TILE);
+      wB.write(st + 5 * TILE);
+      wC.write(st + 5 * TILE + kChunk * NP);
+      __syncthreads();
+    }
     const float* s_dl = st;
     const float* s_u = st + TILE;
     float* s_g = st + 2 * TILE;          // becomes d_y
@@ -320,14 +346,20 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
                               go.y * yv.y * (s1 * fmaf(g.y, 1.f - s1, 1.f)),
                               go.z * yv.z * (s2 * fmaf(g.z, 1.f - s2, 1.f)),
                               go.w * yv.w * (s3 * fmaf(g.w, 1.f - s3, 1.f)));
-            if constexpr (FY)
-              st_global4_if(p.out + (rowb + t0 + i) * Di + dblk0 + col,
-                            make_float4(yv.x * (g.x * s0), yv.y * (g.y * s1), yv.z * (g.z * s2),
-                                        yv.w * (g.w * s3)),
-                            ok);
+            if constexpr (FY) {
+              const float4 ov = make_float4(yv.x * (g.x * s0), yv.y * (g.y * s1),
+                                            yv.z * (g.z * s2), yv.w * (g.w * s3));
+              const size_t o = (rowb + t0 + i) * Di + dblk0 + col;
+              if constexpr (BF) st_global_bf16x4_if(reinterpret_cast<uint16_t*>(p.out) + o, ov, ok);
+              else st_global4_if(p.out + o, ov, ok);
+            }
           }
           *reinterpret_cast<float4*>(s_g + e) = dyo;
-          st_global4_if(p.d_gate + (rowb + t0 + i) * Di + dblk0 + col, dgo, ok);
+          if constexpr (BF)
+            st_global_bf16x4_if(reinterpret_cast<uint16_t*>(p.d_gate) + (rowb + t0 + i) * Di +
+                                    dblk0 + col, dgo, ok);
+          else
+            st_global4_if(p.d_gate + (rowb + t0 + i) * Di + dblk0 + col, dgo, ok);
           if (SP && ok) {   // raw -> delta, and the factor d_raw / d_delta
             float* dl = const_cast<float*>(s_dl) + e;
             float* fac = const_cast<float*>(s_dy) + e;
@@ -547,8 +579,15 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
         const size_t o = (size_t)i * Di;
         float ddo = fmaf(sA, kLn2, uo * sB);
         if constexpr (SP) ddo *= s_dy[i * DC + cl + j_out];   // d_raw = d_delta * softplus'
-        st_global_lt(out_dd + o, ddo, i, lim_dd);
-        st_global_lt(out_du + o, fmaf(dyo, D_out, dlo * sB), i, lim_du);
+        if constexpr (BF) {
+          st_global_bf16_lt(reinterpret_cast<uint16_t*>(p.d_delta) + (rowb + t0) * Di + d_out + o,
+                            ddo, i, lim_dd);
+          st_global_bf16_lt(reinterpret_cast<uint16_t*>(p.d_u) + (rowb + t0) * Di + d_out + o,
+                            fmaf(dyo, D_out, dlo * sB), i, lim_du);
+        } else {
+          st_global_lt(out_dd + o, ddo, i, lim_dd);
+          st_global_lt(out_du + o, fmaf(dyo, D_out, dlo * sB), i, lim_du);
+        }
       }
 #pragma unroll
       for (int q = 0; q < 2; ++q)
@@ -632,9 +671,10 @@ struct BwdAgg4Shape {
   static_assert(kStageBytes % 128 == 0, "TMA destinations must stay 128-byte aligned");
 };
 
-template <int NP, bool VEC, bool TMA>
+template <int NP, bool VEC, bool TMA, bool BF = false>
 __global__ void __launch_bounds__(kWarps * 32)
 scan_bwd_agg4_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
+  static_assert(!BF || TMA, "bf16 tiles come by TMA");
   using S = BwdTmemShape<NP>;
   using A = BwdAgg4Shape<NP>;
   constexpr int G = S::G, LG = S::LG, DW = S::DW, DC = S::DC, TILE = S::TILE;
@@ -664,7 +704,7 @@ scan_bwd_agg4_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
     if constexpr (TMA) {
       if (threadIdx.x == 0) {
         uint64_t* bar = bars + stage;
-        mbar_expect_tx(bar, A::kStageBytes);
+        mbar_expect_tx(bar, BF ? A::kStageBytes / 2 : A::kStageBytes);
         tma_load_3d(st, &maps.delta, bar, dblk0, c * kChunk, b);
         tma_load_3d(st + TILE, &maps.gate, bar, dblk0, c * kChunk, b);
         tma_load_3d(st + 2 * TILE, &maps.dy, bar, dblk0, c * kChunk, b);
@@ -725,6 +765,20 @@ scan_bwd_agg4_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
     if (c + A::kStages - 1 < c_end) load((it + A::kStages - 1) % A::kStages, c + A::kStages - 1);
     else if constexpr (!TMA) cp_async_commit();
     float* st = smem + (it % A::kStages) * A::kStageFloats;
+    if constexpr (BF) {   // widen the bf16 tiles in place
+      BfTile<TILE, NTH> wdl, wg, wdy;
+      BfTile<kChunk * NP, NTH> wC;
+      wdl.read(st);
+      wg.read(st + TILE);
+      wdy.read(st + 2 * TILE);
+      wC.read(st + 3 * TILE);
+      __syncthreads();
+      wdl.write(st);
+      wg.write(st + TILE);
+      wdy.write(st + 2 * TILE);
+      wC.write(st + 3 * TILE);
+      __syncthreads();
+    }
     const float* s_dl = st;
     float* s_g = st + TILE;             // becomes d_y
     const float* s_dy = st + 2 * TILE;
@@ -815,14 +869,19 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-static bool encode_f32(CUtensorMap* m, const void* base, cuuint32_t rank, const cuuint64_t* dims,
-                       const cuuint64_t* strides, const cuuint32_t* box) {
+static bool encode_as(CUtensorMap* m, CUtensorMapDataType ty, const void* base, cuuint32_t rank,
+                      const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box) {
   const EncodeTiledFn f = encode_fn();
   if (!f) return false;
   const cuuint32_t es[4] = {1, 1, 1, 1};
-  return f(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rank, const_cast<void*>(base), dims, strides, box,
+  return f(m, ty, rank, const_cast<void*>(base), dims, strides, box,
            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static bool encode_f32(CUtensorMap* m, const void* base, cuuint32_t rank, const cuuint64_t* dims,
+                       const cuuint64_t* strides, const cuuint32_t* box) {
+  return encode_as(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, rank, dims, strides, box);
 }
 
 // The maps of one call; the last call's maps are kept and reused when nothing changed.
@@ -831,14 +890,14 @@ static bool make_maps(const Plan& plan, const BwdParams& p, BwdMaps* m) {
   using S = BwdTmemShape<NP>;
   struct Key {
     const void* ptr[8];
-    int64_t dims[4];
+    int64_t dims[5];   // batch, T, d_inner, d_state, bf16 I/O
   };
   static std::mutex mu;
   static Key last_key;
   static BwdMaps last_maps;
   static bool have_last = false;
   const Key key = {{p.delta, p.u, p.gate, p.dy, p.y_ck, p.B, p.C, p.ckpt},
-                   {plan.batch, plan.T, plan.Di, plan.N}};
+                   {plan.batch, plan.T, plan.Di, plan.N, (int64_t)p.io_bf16}};
   std::lock_guard<std::mutex> lock(mu);
   if (have_last && memcmp(&key, &last_key, sizeof(Key)) == 0) {
     *m = last_maps;
@@ -846,22 +905,26 @@ static bool make_maps(const Plan& plan, const BwdParams& p, BwdMaps* m) {
   }
   const cuuint64_t Di = plan.Di, T = plan.T, Bt = plan.batch, N = plan.N;
   const cuuint64_t nck = plan.nchunks - 1;
-  const cuuint64_t dTD[3] = {Di, T, Bt}, sTD[2] = {Di * 4, T * Di * 4};
+  // the I/O tensors' element size: 2 for the fused bf16 call (the checkpoints stay fp32)
+  const cuuint64_t es = p.io_bf16 ? 2 : 4;
+  const CUtensorMapDataType io =
+      p.io_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const cuuint64_t dTD[3] = {Di, T, Bt}, sTD[2] = {Di * es, T * Di * es};
   const cuuint32_t bTD[3] = {(cuuint32_t)S::DC, (cuuint32_t)kChunk, 1};
-  const cuuint64_t dTN[3] = {N, T, Bt}, sTN[2] = {N * 4, T * N * 4};
+  const cuuint64_t dTN[3] = {N, T, Bt}, sTN[2] = {N * es, T * N * es};
   const cuuint32_t bTN[3] = {(cuuint32_t)NP, (cuuint32_t)kChunk, 1};
   const cuuint64_t dCK[4] = {N, Di, nck, Bt}, sCK[3] = {N * 4, Di * N * 4, nck * Di * N * 4};
   const cuuint32_t bCK[4] = {(cuuint32_t)NP, (cuuint32_t)S::DC, 1, 1};
   BwdMaps mm;
   memset(&mm, 0, sizeof(mm));
-  const bool ok = encode_f32(&mm.delta, p.delta, 3, dTD, sTD, bTD) &&
-                  encode_f32(&mm.u, p.u, 3, dTD, sTD, bTD) &&
-                  encode_f32(&mm.gate, p.gate, 3, dTD, sTD, bTD) &&
-                  encode_f32(&mm.dy, p.dy, 3, dTD, sTD, bTD) &&
+  const bool ok = encode_as(&mm.delta, io, p.delta, 3, dTD, sTD, bTD) &&
+                  encode_as(&mm.u, io, p.u, 3, dTD, sTD, bTD) &&
+                  encode_as(&mm.gate, io, p.gate, 3, dTD, sTD, bTD) &&
+                  encode_as(&mm.dy, io, p.dy, 3, dTD, sTD, bTD) &&
                   // the fused call has no stored y: its map is never used
-                  encode_f32(&mm.y, p.y_ck ? p.y_ck : p.delta, 3, dTD, sTD, bTD) &&
-                  encode_f32(&mm.B, p.B, 3, dTN, sTN, bTN) &&
-                  encode_f32(&mm.C, p.C, 3, dTN, sTN, bTN) &&
+                  encode_as(&mm.y, io, p.y_ck ? p.y_ck : p.delta, 3, dTD, sTD, bTD) &&
+                  encode_as(&mm.B, io, p.B, 3, dTN, sTN, bTN) &&
+                  encode_as(&mm.C, io, p.C, 3, dTN, sTN, bTN) &&
                   encode_f32(&mm.ckpt, p.ckpt, 4, dCK, sCK, bCK);
   if (!ok) return false;
   *m = mm;
@@ -888,6 +951,11 @@ static int launch_main(const Plan& plan, const BwdMaps& maps, const BwdParams& p
   auto kern = p.out        ? scan_bwd_tmem_kernel<NP, VEC, TMA, false, true>
               : p.softplus ? scan_bwd_tmem_kernel<NP, VEC, TMA, true, false>
                            : scan_bwd_tmem_kernel<NP, VEC, TMA, false, false>;
+  if constexpr (VEC && TMA) {
+    if (p.io_bf16) kern = scan_bwd_tmem_kernel<NP, true, true, false, true, true>;
+  } else {
+    if (p.io_bf16) return -1;   // bf16 tiles need the TMA path
+  }
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)S::kSmemBytes) != cudaSuccess)
     return -1;
@@ -904,6 +972,7 @@ static int launch_np(const Plan& plan, const BwdParams& p, cudaStream_t s) {
   BwdMaps maps;
   if (vec && plan.nchunks >= 2 && make_maps<NP>(plan, p, &maps))
     return launch_main<NP, true, true>(plan, maps, p, s);
+  if (p.io_bf16) return -1;
   memset(&maps, 0, sizeof(maps));
   return vec ? launch_main<NP, true, false>(plan, maps, p, s)
              : launch_main<NP, false, false>(plan, maps, p, s);
@@ -913,13 +982,18 @@ template <int NP, bool VEC, bool TMA>
 static int launch_agg4(const Plan& plan, const BwdMaps& maps, const BwdParams& p,
                        cudaStream_t s) {
   using A = BwdAgg4Shape<NP>;
-  if (cudaFuncSetAttribute(scan_bwd_agg4_kernel<NP, VEC, TMA>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto kern = scan_bwd_agg4_kernel<NP, VEC, TMA>;
+  if constexpr (VEC && TMA) {
+    if (p.io_bf16) kern = scan_bwd_agg4_kernel<NP, true, true, true>;
+  } else {
+    if (p.io_bf16) return -1;
+  }
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)A::kSmemBytes) != cudaSuccess)
     return -1;
   dim3 grid((unsigned)(plan.bwd.nblk * (plan.bwd.nseg - 1) * plan.bwd.nsub),
             (unsigned)plan.batch);
-  scan_bwd_agg4_kernel<NP, VEC, TMA><<<grid, kWarps * 32, A::kSmemBytes, s>>>(maps, p);
+  kern<<<grid, kWarps * 32, A::kSmemBytes, s>>>(maps, p);
   return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
 }
 
@@ -929,6 +1003,7 @@ static int launch_agg_np(const Plan& plan, const BwdParams& p, cudaStream_t s) {
   BwdMaps maps;
   if (vec && plan.nchunks >= 2 && make_maps<NP>(plan, p, &maps))
     return launch_agg4<NP, true, true>(plan, maps, p, s);
+  if (p.io_bf16) return -1;
   memset(&maps, 0, sizeof(maps));
   return vec ? launch_agg4<NP, true, false>(plan, maps, p, s)
              : launch_agg4<NP, false, false>(plan, maps, p, s);

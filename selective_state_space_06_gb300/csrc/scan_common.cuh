@@ -370,4 +370,74 @@ __device__ __forceinline__ void st_global4_if(float* p, float4 v, bool pred) {
       ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"((unsigned)pred) : "memory");
 }
 
+// ---- bf16 I/O --------------------------------------------------------------------------------
+// bf16 tensors are passed as raw 16-bit patterns. Widening to fp32 is exact (the bf16 bits are
+// the upper half of the fp32 word); narrowing rounds to nearest even (cvt.rn).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;   // the first source goes to the upper half
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// st.global of one bf16 when a < b (as st_global_lt)
+__device__ __forceinline__ void st_global_bf16_lt(uint16_t* p, float v, int a, int b) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\t.reg .b16 h;\n\tsetp.lt.s32 q, %2, %3;\n\t"
+      "cvt.rn.bf16.f32 h, %1;\n\t@q st.global.b16 [%0], h;\n\t}"
+      ::"l"(p), "f"(v), "r"(a), "r"(b) : "memory");
+}
+// four consecutive bf16 (8-byte aligned) when pred
+__device__ __forceinline__ void st_global_bf16x4_if(uint16_t* p, float4 v, bool pred) {
+  const uint32_t lo = pack_bf16x2(v.x, v.y), hi = pack_bf16x2(v.z, v.w);
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %3, 0;\n\t@q st.global.v2.b32 [%0], {%1, %2};\n\t}"
+      ::"l"(p), "r"(lo), "r"(hi), "r"((unsigned)pred) : "memory");
+}
+
+// cp.async of a [kChunk][TW] bf16 tile (rows t0.., columns col0..; zeros past T or W) into the
+// first half of the fp32 slot dst, 8 elements per copy (TW and W multiples of 8).
+template <int TW, int NTH>
+__device__ __forceinline__ void stage_tile_bf16(float* dst, const uint16_t* src, size_t row0,
+                                                int t0, int T, int W, int col0) {
+  static_assert(TW % 8 == 0, "bf16 tiles move in 16-byte groups");
+  uint16_t* d16 = reinterpret_cast<uint16_t*>(dst);
+  for (int q = threadIdx.x; q < kChunk * TW / 8; q += NTH) {
+    const int i = q / (TW / 8), col = (q % (TW / 8)) * 8;
+    const bool v = (t0 + i < T) && (col0 + col < W);
+    cp_async16(d16 + i * TW + col, v ? src + (row0 + t0 + i) * W + col0 + col : src, v);
+  }
+}
+
+// A bf16 tile of E elements that a copy left in the first half of its fp32 slot becomes the
+// fp32 tile in place. read() takes this thread's 16-byte groups into registers; after a barrier
+// (the fp32 writes cover groups other threads read) write() stores them widened.
+template <int E, int NTH>
+struct BfTile {
+  static_assert(E % 8 == 0, "whole 16-byte groups");
+  static constexpr int kGroups = E / 8;
+  static constexpr int kPer = (kGroups + NTH - 1) / NTH;
+  uint4 r[kPer];
+  __device__ __forceinline__ void read(const float* slot) {
+    const uint4* s = reinterpret_cast<const uint4*>(slot);
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int g = threadIdx.x + j * NTH;
+      if (kGroups % NTH == 0 || g < kGroups) r[j] = s[g];
+    }
+  }
+  __device__ __forceinline__ void write(float* slot) const {
+    float4* d = reinterpret_cast<float4*>(slot);
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int g = threadIdx.x + j * NTH;
+      if (kGroups % NTH == 0 || g < kGroups) {
+        d[2 * g] = make_float4(bf16_lo(r[j].x), bf16_hi(r[j].x), bf16_lo(r[j].y), bf16_hi(r[j].y));
+        d[2 * g + 1] =
+            make_float4(bf16_lo(r[j].z), bf16_hi(r[j].z), bf16_lo(r[j].w), bf16_hi(r[j].w));
+      }
+    }
+  }
+};
+
 }  // namespace mscan

@@ -44,7 +44,7 @@ struct FwdShape {
   static constexpr size_t kSmemBytes = (size_t)kFwdStages * kStageFloats * sizeof(float);
 };
 
-template <int NP, bool VEC, bool ST = false>
+template <int NP, bool VEC, bool ST = false, bool BF = false>
 __device__ __forceinline__ void fwd_load_chunk(const FwdParams& p, float* st, int c, int b,
                                                int dblk0) {
   using S = FwdShape<NP>;
@@ -56,7 +56,14 @@ __device__ __forceinline__ void fwd_load_chunk(const FwdParams& p, float* st, in
   float* s_C = s_B + kChunk * NP;
   const int t0 = c * kChunk;
   const size_t rowb = (size_t)b * p.T;
-  if constexpr (VEC) {
+  if constexpr (BF) {   // bf16 tiles into the first half of each slot (widened after the wait)
+    static_assert(ST && VEC, "bf16 input is taken by the states-only forward");
+    stage_tile_bf16<DC, NTH>(s_dl, reinterpret_cast<const uint16_t*>(p.delta), rowb, t0, p.T,
+                             p.Di, dblk0);
+    stage_tile_bf16<DC, NTH>(s_u, reinterpret_cast<const uint16_t*>(p.u), rowb, t0, p.T, p.Di,
+                             dblk0);
+    stage_tile_bf16<NP, NTH>(s_B, reinterpret_cast<const uint16_t*>(p.B), rowb, t0, p.T, p.N, 0);
+  } else if constexpr (VEC) {
     for (int q = threadIdx.x; q < kChunk * DC / 4; q += NTH) {
       const int i = q / (DC / 4), col = (q % (DC / 4)) * 4;
       const int t = t0 + i, d = dblk0 + col;
@@ -113,7 +120,7 @@ struct FwdAggShape {
   static constexpr size_t kSmemBytes = (size_t)kStages * kStageFloats * sizeof(float);
 };
 
-template <int NP, bool VEC>
+template <int NP, bool VEC, bool BF = false>
 __global__ void __launch_bounds__(kAggWarps * 32)
 scan_fwd_agg_kernel(const FwdParams p) {
   using S = FwdShape<NP>;
@@ -157,9 +164,18 @@ scan_fwd_agg_kernel(const FwdParams p) {
 
   auto load = [&](int stage, int c) {
     float* st = smem + stage * A::kStageFloats;
-    stage_tile<DC, NTH, VEC>(st, p.delta, row0, c * kChunk, T, Di, dblk0);
-    stage_tile<DC, NTH, VEC>(st + kChunk * DC, p.u, row0, c * kChunk, T, Di, dblk0);
-    stage_tile<NP, NTH, VEC>(st + 2 * kChunk * DC, p.B, row0, c * kChunk, T, N, 0);
+    if constexpr (BF) {   // bf16 tiles into the first half of each slot
+      stage_tile_bf16<DC, NTH>(st, reinterpret_cast<const uint16_t*>(p.delta), row0, c * kChunk,
+                               T, Di, dblk0);
+      stage_tile_bf16<DC, NTH>(st + kChunk * DC, reinterpret_cast<const uint16_t*>(p.u), row0,
+                               c * kChunk, T, Di, dblk0);
+      stage_tile_bf16<NP, NTH>(st + 2 * kChunk * DC, reinterpret_cast<const uint16_t*>(p.B),
+                               row0, c * kChunk, T, N, 0);
+    } else {
+      stage_tile<DC, NTH, VEC>(st, p.delta, row0, c * kChunk, T, Di, dblk0);
+      stage_tile<DC, NTH, VEC>(st + kChunk * DC, p.u, row0, c * kChunk, T, Di, dblk0);
+      stage_tile<NP, NTH, VEC>(st + 2 * kChunk * DC, p.B, row0, c * kChunk, T, N, 0);
+    }
     cp_async_commit();
   };
 #pragma unroll
@@ -174,6 +190,18 @@ scan_fwd_agg_kernel(const FwdParams p) {
     if (c + A::kStages - 1 < c_end) load((it + A::kStages - 1) % A::kStages, c + A::kStages - 1);
     else cp_async_commit();
     float* st = smem + (it % A::kStages) * A::kStageFloats;
+    if constexpr (BF) {   // widen the bf16 tiles in place
+      BfTile<kChunk * DC, NTH> wdl, wu;
+      BfTile<kChunk * NP, NTH> wB;
+      wdl.read(st);
+      wu.read(st + kChunk * DC);
+      wB.read(st + 2 * kChunk * DC);
+      __syncthreads();
+      wdl.write(st);
+      wu.write(st + kChunk * DC);
+      wB.write(st + 2 * kChunk * DC);
+      __syncthreads();
+    }
     if (p.softplus) {   // raw delta -> delta in shared memory, once per element
       softplus_tile<DC, NTH>(st, T - c * kChunk, Di - dblk0);
       __syncthreads();
@@ -228,10 +256,12 @@ scan_fwd_agg_kernel(const FwdParams p) {
 
 // ST (states only, for the fused forward + backward call): the recurrence and the checkpoints
 // alone; the backward then recomputes y from the states and writes out.
-template <int NP, bool VEC, bool WITH_Y, bool SP, bool ST>
+// BF (with ST): delta, u and B arrive as bf16 and are widened in shared memory.
+template <int NP, bool VEC, bool WITH_Y, bool SP, bool ST, bool BF = false>
 __global__ void __launch_bounds__(kWarps * 32)
 scan_fwd_kernel(const FwdParams p) {
   static_assert(!(ST && (SP || WITH_Y)), "the states-only forward takes the plain delta");
+  static_assert(!BF || ST, "bf16 input is taken by the states-only forward");
   using S = FwdShape<NP>;
   constexpr int G = S::G, DW = S::DW, DC = S::DC, P = S::P, NPT = S::NPT, NPR = S::NPR;
   extern __shared__ __align__(16) float smem[];
@@ -276,7 +306,7 @@ scan_fwd_kernel(const FwdParams p) {
 #pragma unroll
   for (int s = 0; s < kFwdStages - 1; ++s) {
     if (c_begin + s < c_end)
-      fwd_load_chunk<NP, VEC, ST>(p, smem + s * S::kStageFloats, c_begin + s, b, dblk0);
+      fwd_load_chunk<NP, VEC, ST, BF>(p, smem + s * S::kStageFloats, c_begin + s, b, dblk0);
     else
       cp_async_commit();
   }
@@ -319,12 +349,24 @@ scan_fwd_kernel(const FwdParams p) {
     {
       const int cn = c + kFwdStages - 1;
       if (cn < c_end)
-        fwd_load_chunk<NP, VEC, ST>(p, smem + ((it + kFwdStages - 1) % kFwdStages) * S::kStageFloats,
-                                    cn, b, dblk0);
+        fwd_load_chunk<NP, VEC, ST, BF>(
+            p, smem + ((it + kFwdStages - 1) % kFwdStages) * S::kStageFloats, cn, b, dblk0);
       else
         cp_async_commit();
     }
     float* st = smem + (it % kFwdStages) * S::kStageFloats;
+    if constexpr (BF) {   // widen the bf16 tiles in place
+      BfTile<kChunk * DC, kWarps * 32> wdl, wu;
+      BfTile<kChunk * NP, kWarps * 32> wB;
+      wdl.read(st);
+      wu.read(st + kChunk * DC);
+      wB.read(st + 3 * kChunk * DC);
+      __syncthreads();
+      wdl.write(st);
+      wu.write(st + kChunk * DC);
+      wB.write(st + 3 * kChunk * DC);
+      __syncthreads();
+    }
     if constexpr (SP) {   // raw delta -> delta in shared memory, once per element
       softplus_tile<DC, kWarps * 32>(st, p.T - c * kChunk, p.Di - dblk0);
       __syncthreads();
@@ -425,21 +467,29 @@ static int launch_np(const Plan& plan, const FwdParams& p0, cudaStream_t s) {
   auto kern = p0.states_only ? scan_fwd_kernel<NP, VEC, false, false, true>
              : p0.softplus   ? scan_fwd_kernel<NP, VEC, WITH_Y, true, false>
                              : scan_fwd_kernel<NP, VEC, WITH_Y, false, false>;
+  auto agg = scan_fwd_agg_kernel<NP, VEC>;
+  if constexpr (NP >= kTmemMinNP && VEC && !WITH_Y) {   // the bf16 fused call (d_state % 8 == 0)
+    if (p0.io_bf16) {
+      kern = scan_fwd_kernel<NP, true, false, false, true, true>;
+      agg = scan_fwd_agg_kernel<NP, true, true>;
+    }
+  } else {
+    if (p0.io_bf16) return -1;
+  }
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)S::kSmemBytes) != cudaSuccess)
     return -1;
   int n = 0;
   if (plan.fwd.nseg > 1) {
     using A = FwdAggShape<NP>;
-    if (cudaFuncSetAttribute(scan_fwd_agg_kernel<NP, VEC>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(agg, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)A::kSmemBytes) != cudaSuccess)
       return -1;
     const int nblk_a = (int)((plan.Di + A::DC - 1) / A::DC);
     p.agg_k = 1;   // one segment per CTA measured fastest (the kernel accepts more)
     const int ngrp = (plan.fwd.nseg - 1 + p.agg_k - 1) / p.agg_k;
     dim3 ga((unsigned)(nblk_a * ngrp), (unsigned)plan.batch);
-    scan_fwd_agg_kernel<NP, VEC><<<ga, A::NTH, A::kSmemBytes, s>>>(p);
+    agg<<<ga, A::NTH, A::kSmemBytes, s>>>(p);
     if (cudaPeekAtLastError() != cudaSuccess) return -1;
     ++n;
   }

@@ -88,6 +88,7 @@ struct FwdParams {
   int agg_k;                     // pre-pass: consecutive segments per CTA
   int softplus;                  // delta holds the raw delta: the kernels apply softplus
   int states_only;               // checkpoints only: no C, gate reads, no out, y (fused call)
+  int io_bf16;                   // delta, u, B point at bf16 data (states-only forward)
 };
 
 struct BwdParams {
@@ -103,6 +104,8 @@ struct BwdParams {
   int softplus;                    // delta holds the raw delta; d_delta receives d_raw
   float* out;   // fused call: the backward recomputes y from the states and writes out (y_ck
                 // unused); null otherwise
+  int io_bf16;  // fused call only: delta, u, B, C, gate, dy, out, d_delta, d_u, d_B, d_C,
+                // d_gate point at bf16 data (A_log, D, d_A_log, d_D stay fp32)
 };
 
 // TMA descriptors of the tensor-memory backward, encoded on the host for each call:
