@@ -129,7 +129,13 @@ int mamba_scan_bwd_softplus(const float* delta_raw, const float* u, const float*
  * backward forms y = sum_n C*h + D*u from the states it recomputes anyway, so out, y and the
  * gate are not carried through device memory between the passes. For d_state <= 8 the call
  * runs the two passes as the separate entry points do. The checkpoint buffer's contents
- * afterwards are unspecified. Asynchronous on `stream`; device pointers, owned by the caller. */
+ * afterwards are unspecified. Asynchronous on `stream`; device pointers, owned by the caller.
+ * When T spans several backward segments, the backward's segment pre-pass (which reads only
+ * inputs) runs on a library-owned side stream beside the forward: the call records an event on
+ * `stream`, the side stream waits for it, and `stream` waits for the side stream before the
+ * rest of the backward. The side stream and its events are created on the first such call of
+ * each host thread on each device and kept for the thread's lifetime; stream capture sees a
+ * fork and a join. */
 int mamba_scan_fwd_bwd(const float* delta, const float* u, const float* B, const float* C,
                        const float* gate, const float* A_log, const float* D, const float* dy,
                        float* out, void* ckpt, size_t ckpt_bytes, void* scratch,

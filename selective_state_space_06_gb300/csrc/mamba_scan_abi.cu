@@ -308,7 +308,8 @@ static int scan_bwd_impl(const float* delta, const float* u, const float* B, con
                          float* d_C, float* d_A_log, float* d_D, float* d_gate, int64_t batch,
                          int64_t T, int64_t d_inner, int64_t d_state, void* stream,
                          int softplus, float* out = nullptr, bool fuse_out = false,
-                         bool check_only = false, int io_bf16 = 0) {
+                         bool check_only = false, int io_bf16 = 0, int phase = 0,
+                         void* pre_stream = nullptr) {
   Plan plan;
   int rc = check_dims(batch, T, d_inner, d_state, &plan);
   if (rc != MAMBA_OK) return rc;
@@ -362,7 +363,11 @@ static int scan_bwd_impl(const float* delta, const float* u, const float* B, con
   p.out = fuse_out ? out : nullptr;
   if (fuse_out) p.y_ck = nullptr;   // y is recomputed from the states
   p.io_bf16 = io_bf16;
-  const int n = mscan::launch_bwd(plan, p, (cudaStream_t)stream);
+  // phase 0: everything on `stream`; 1: the segment pre-pass alone, on `pre_stream`;
+  // 2: what follows the pre-pass, on `stream` (d_state 9..64)
+  const int n = phase == 1   ? mscan::launch_bwd_agg_tmem(plan, p, (cudaStream_t)pre_stream)
+                : phase == 2 ? mscan::launch_bwd_after_agg(plan, p, (cudaStream_t)stream)
+                             : mscan::launch_bwd(plan, p, (cudaStream_t)stream);
   if (n < 0) return set_cuda_error(cudaGetLastError());
   g_last_launches = n;
   return MAMBA_OK;
@@ -391,6 +396,32 @@ int mamba_scan_bwd_softplus(const float* delta_raw, const float* u, const float*
                        T, d_inner, d_state, stream, 1);
 }
 
+// The fused call's side stream and its two events, one set per (host thread, device), created
+// on first use and kept for the thread's lifetime.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+static bool side_stream(SideStream* out) {
+  thread_local SideStream per_dev[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  SideStream& x = per_dev[dev];
+  if (!x.s) {
+    SideStream n;
+    if (cudaStreamCreateWithFlags(&n.s, cudaStreamNonBlocking) != cudaSuccess) return false;
+    if (cudaEventCreateWithFlags(&n.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&n.join, cudaEventDisableTiming) != cudaSuccess) {
+      if (n.fork) cudaEventDestroy(n.fork);
+      cudaStreamDestroy(n.s);
+      return false;
+    }
+    x = n;
+  }
+  *out = x;
+  return true;
+}
+
 static int fwd_bwd_impl(const float* delta, const float* u, const float* B, const float* C,
                         const float* gate, const float* A_log, const float* D, const float* dy,
                         float* out, void* ckpt, size_t ckpt_bytes, void* scratch,
@@ -411,15 +442,38 @@ static int fwd_bwd_impl(const float* delta, const float* u, const float* B, cons
   // bf16 I/O: the fused path with TMA staging only (16-byte rows of bf16, two chunks or more)
   if (io_bf16 && (!fused || d_inner % 8 != 0 || d_state % 8 != 0 || plan.nchunks < 2))
     return MAMBA_ERR_UNSUPPORTED;
+  // The backward's segment pre-pass reads only inputs, so in the fused path it runs on a side
+  // stream beside the forward (which leaves most issue slots idle); the rest of the backward
+  // waits for both. The fork event is recorded before the forward is enqueued, so the forward's
+  // CTAs are dispatched first.
+  SideStream side;
+  const bool overlap = fused && plan.bwd.nseg > 1 && side_stream(&side);
+  const cudaStream_t s = (cudaStream_t)stream;
+  if (overlap) {
+    if (cudaEventRecord(side.fork, s) != cudaSuccess ||
+        cudaStreamWaitEvent(side.s, side.fork, 0) != cudaSuccess)
+      return set_cuda_error(cudaGetLastError());
+  }
   rc = scan_fwd_impl(delta, u, B, C, gate, A_log, D, out, nullptr, ckpt, ckpt_bytes, batch, T,
                      d_inner, d_state, stream, 0, fused ? 1 : 0, io_bf16);
   if (rc != MAMBA_OK) return rc;
-  const int nf = g_last_launches;
+  int launches = g_last_launches;
+  if (overlap) {
+    rc = scan_bwd_impl(delta, u, B, C, gate, A_log, D, dy, ckpt, ckpt_bytes, scratch,
+                       scratch_bytes, d_delta, d_u, d_B, d_C, d_A_log, d_D, d_gate, batch, T,
+                       d_inner, d_state, stream, 0, out, fused, false, io_bf16, 1, side.s);
+    if (rc == MAMBA_OK) launches += g_last_launches;
+    // joined even after a failed launch, so that a captured stream never keeps an open fork
+    if (cudaEventRecord(side.join, side.s) != cudaSuccess ||
+        cudaStreamWaitEvent(s, side.join, 0) != cudaSuccess)
+      return set_cuda_error(cudaGetLastError());
+    if (rc != MAMBA_OK) return rc;
+  }
   rc = scan_bwd_impl(delta, u, B, C, gate, A_log, D, dy, ckpt, ckpt_bytes, scratch,
                      scratch_bytes, d_delta, d_u, d_B, d_C, d_A_log, d_D, d_gate, batch, T,
-                     d_inner, d_state, stream, 0, out, fused, false, io_bf16);
+                     d_inner, d_state, stream, 0, out, fused, false, io_bf16, overlap ? 2 : 0);
   if (rc != MAMBA_OK) return rc;
-  g_last_launches += nf;
+  g_last_launches += launches;
   return MAMBA_OK;
 }
 

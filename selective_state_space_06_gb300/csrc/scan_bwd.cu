@@ -712,6 +712,27 @@ static int launch_vec(const Plan& plan, const BwdParams& p, cudaStream_t s) {
   return vec ? launch_np<NP, true>(plan, p, s) : launch_np<NP, false>(plan, p, s);
 }
 
+// d_state 9..64, after launch_bwd_agg_tmem: the composition, the backward and the reduction.
+int launch_bwd_after_agg(const Plan& plan, const BwdParams& p, cudaStream_t s) {
+  if (plan.NP < kTmemMinNP) return -1;
+  int n = 0;
+  if (plan.bwd.nseg > 1) {
+    int sms = 152, dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    scan_bwd_compose_kernel<<<sms * 4, 256, 0, s>>>(p);
+    if (cudaPeekAtLastError() != cudaSuccess) return -1;
+    ++n;
+  }
+  const int nm = launch_bwd_main_tmem(plan, p, s);
+  if (nm < 0) return -1;
+  int sms = 152, dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  scan_reduce_kernel<<<sms * 4, 256, 0, s>>>(p);
+  return cudaPeekAtLastError() == cudaSuccess ? n + nm + 1 : -1;
+}
+
 int launch_bwd(const Plan& plan, const BwdParams& p, cudaStream_t s) {
   int n;
   switch (plan.NP) {

@@ -130,5 +130,7 @@ int launch_bwd(const Plan& plan, const BwdParams& p, cudaStream_t stream);
 int launch_bwd_main_tmem(const Plan& plan, const BwdParams& p, cudaStream_t stream);
 // its segment pre-pass (0 kernels when there is one segment)
 int launch_bwd_agg_tmem(const Plan& plan, const BwdParams& p, cudaStream_t stream);
+// what launch_bwd enqueues after that pre-pass: composition, backward, reduction (d_state 9..64)
+int launch_bwd_after_agg(const Plan& plan, const BwdParams& p, cudaStream_t stream);
 
 }  // namespace mscan
