@@ -85,18 +85,28 @@ __device__ __forceinline__ void bwd_tmem_load_chunk(const BwdMaps& maps, const B
   float* s_h0 = st + 5 * TILE + 2 * kChunk * NP;
   if constexpr (TMA) {
     // one thread issues the whole stage; rows past T, channels past d_inner, states past
-    // d_state and the (absent) checkpoint before chunk 0 arrive as zeros. With BF the tiles
-    // are bf16 and land in the first half of their slots; the checkpoint row stays fp32.
+    // d_state and the (absent) checkpoint before chunk 0 arrive as zeros. With BF (fused call)
+    // the tiles are bf16 and land where the fused path has room until it needs it: delta and u
+    // in the halves of the y slot (widened into their own slots before the recompute fills y),
+    // gate and dy in the halves of the gate slot (read as bf16), B and C in the first halves of
+    // their slots (read as bf16 when duplicated). The checkpoint row stays fp32.
     constexpr uint32_t kEl = BF ? 2u : 4u;
     constexpr uint32_t kBytes = (4u * TILE + (FY ? 0u : TILE) + 2u * kChunk * NP) * kEl +
                                 (uint32_t)(DC * NP) * 4u;
     static_assert(BF || kBytes == S::kStageBytes - (FY ? TILE * 4u : 0u), "stage bytes");
     if (threadIdx.x == 0) {
       mbar_expect_tx(bar, kBytes);
-      tma_load_3d(st, &maps.delta, bar, dblk0, t0, b);
-      tma_load_3d(st + TILE, &maps.u, bar, dblk0, t0, b);
-      tma_load_3d(st + 2 * TILE, &maps.gate, bar, dblk0, t0, b);
-      tma_load_3d(st + 3 * TILE, &maps.dy, bar, dblk0, t0, b);
+      if constexpr (BF) {
+        tma_load_3d(st + 4 * TILE, &maps.delta, bar, dblk0, t0, b);
+        tma_load_3d(st + 4 * TILE + TILE / 2, &maps.u, bar, dblk0, t0, b);
+        tma_load_3d(st + 2 * TILE, &maps.gate, bar, dblk0, t0, b);
+        tma_load_3d(st + 2 * TILE + TILE / 2, &maps.dy, bar, dblk0, t0, b);
+      } else {
+        tma_load_3d(st, &maps.delta, bar, dblk0, t0, b);
+        tma_load_3d(st + TILE, &maps.u, bar, dblk0, t0, b);
+        tma_load_3d(st + 2 * TILE, &maps.gate, bar, dblk0, t0, b);
+        tma_load_3d(st + 3 * TILE, &maps.dy, bar, dblk0, t0, b);
+      }
       if constexpr (!FY) tma_load_3d(st + 4 * TILE, &maps.y, bar, dblk0, t0, b);
       tma_load_3d(st + 5 * TILE, &maps.B, bar, 0, t0, b);
       tma_load_3d(st + 5 * TILE + kChunk * NP, &maps.C, bar, 0, t0, b);
@@ -291,28 +301,17 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
         cp_async_commit();
     }
     float* st = smem + (it % kTmemStages) * S::kStageFloats;
-    if constexpr (BF) {   // widen the bf16 tiles in place (the checkpoint row is fp32)
-      BfTile<TILE, NTH> w0, w1, w2, w3;
-      BfTile<kChunk * NP, NTH> wB, wC;
-      w0.read(st);
-      w1.read(st + TILE);
-      w2.read(st + 2 * TILE);
-      w3.read(st + 3 * TILE);
-      wB.read(st + 5 * TILE);
-      wC.read(st + 5 * TILE + kChunk * NP);
-      __syncthreads();
-      w0.write(st);
-      w1.write(st + TILE);
-      w2.write(st + 2 * TILE);
-      w3.write(st + 3 * TILE);
-      wB.write(st + 5 * TILE);
-      wC.write(st + 5 * TILE + kChunk * NP);
-      __syncthreads();
+    if constexpr (BF) {   // delta and u: bf16 halves of the y slot -> their fp32 slots
+      BfTile<TILE, NTH> wdl, wu;
+      wdl.read(st + 4 * TILE);
+      wu.read(st + 4 * TILE + TILE / 2);
+      wdl.write(st);
+      wu.write(st + TILE);
     }
     const float* s_dl = st;
     const float* s_u = st + TILE;
-    float* s_g = st + 2 * TILE;          // becomes d_y
-    const float* s_dy = st + 3 * TILE;
+    float* s_g = st + 2 * TILE;          // becomes d_y (BF: gate and dy as bf16 halves)
+    const float* s_dy = st + 3 * TILE;   // (BF: receives d_y)
     float* s_y = st + 4 * TILE;   // y: loaded, or formed by the recompute (FY)
     const float* s_B = st + 5 * TILE;
     const float* s_C = s_B + kChunk * NP;
@@ -334,8 +333,17 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
           const int i = e / DC, col = e % DC;
           const bool ok = (t0 + i < T) && (dblk0 + col < Di);
           const float4 yv = *reinterpret_cast<const float4*>(s_y + e);
-          const float4 g = *reinterpret_cast<const float4*>(s_g + e);
-          const float4 go = *reinterpret_cast<const float4*>(s_dy + e);
+          float4 g, go;
+          if constexpr (BF) {   // 4 bf16 of gate and of dy from the halves of the gate slot
+            const uint16_t* gd = reinterpret_cast<const uint16_t*>(s_g);
+            const uint2 gw = *reinterpret_cast<const uint2*>(gd + e);
+            const uint2 dw = *reinterpret_cast<const uint2*>(gd + TILE + e);
+            g = make_float4(bf16_lo(gw.x), bf16_hi(gw.x), bf16_lo(gw.y), bf16_hi(gw.y));
+            go = make_float4(bf16_lo(dw.x), bf16_hi(dw.x), bf16_lo(dw.y), bf16_hi(dw.y));
+          } else {
+            g = *reinterpret_cast<const float4*>(s_g + e);
+            go = *reinterpret_cast<const float4*>(s_dy + e);
+          }
           float4 dyo, dgo;
           {
             const float s0 = sigmoid_fast(g.x), s1 = sigmoid_fast(g.y);
@@ -354,7 +362,9 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
               else st_global4_if(p.out + o, ov, ok);
             }
           }
-          *reinterpret_cast<float4*>(s_g + e) = dyo;
+          // d_y: into the gate tile, or (BF, where the gate slot holds bf16 still being read
+          // by other threads) into the dy slot
+          *reinterpret_cast<float4*>((BF ? const_cast<float*>(s_dy) : s_g) + e) = dyo;
           if constexpr (BF)
             st_global_bf16x4_if(reinterpret_cast<uint16_t*>(p.d_gate) + (rowb + t0 + i) * Di +
                                     dblk0 + col, dgo, ok);
@@ -389,7 +399,14 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
     };
     if constexpr (!FY) gating();
     for (int e = threadIdx.x; e < kChunk * NP; e += NTH) {
-      const float bv = s_B[e], cv = s_C[e];
+      float bv, cv;
+      if constexpr (BF) {   // bf16 B and C in the first halves of their slots
+        bv = __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(s_B)[e] << 16);
+        cv = __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(s_C)[e] << 16);
+      } else {
+        bv = s_B[e];
+        cv = s_C[e];
+      }
       *reinterpret_cast<float2*>(s_Bw + 2 * e) = make_float2(bv, bv);
       *reinterpret_cast<float2*>(s_Cw + 2 * e) = make_float2(cv, cv);
       if constexpr (S::SWAP) {
@@ -419,8 +436,9 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
                             reinterpret_cast<const float2*>(s_dl + offc[1])};
     const float2* pu[2] = {reinterpret_cast<const float2*>(s_u + offc[0]),
                            reinterpret_cast<const float2*>(s_u + offc[1])};
-    const float2* pdy[2] = {reinterpret_cast<const float2*>(s_g + offc[0]),
-                            reinterpret_cast<const float2*>(s_g + offc[1])};
+    const float* s_dyv = BF ? s_dy : s_g;   // d_y
+    const float2* pdy[2] = {reinterpret_cast<const float2*>(s_dyv + offc[0]),
+                            reinterpret_cast<const float2*>(s_dyv + offc[1])};
 #pragma unroll 2
     for (int i = 0; i < kChunk; ++i) {
       step_fence();

@@ -409,9 +409,10 @@ __device__ __forceinline__ void stage_tile_bf16(float* dst, const uint16_t* src,
   }
 }
 
-// A bf16 tile of E elements that a copy left in the first half of its fp32 slot becomes the
-// fp32 tile in place. read() takes this thread's 16-byte groups into registers; after a barrier
-// (the fp32 writes cover groups other threads read) write() stores them widened.
+// Widens a bf16 tile of E elements to fp32. read() takes this thread's 16-byte groups into
+// registers and write() stores them widened. In place (the bf16 tile in the first half of its
+// own fp32 slot) a barrier must separate the two, since the fp32 writes cover groups that other
+// threads read; into another slot none is needed.
 template <int E, int NTH>
 struct BfTile {
   static_assert(E % 8 == 0, "whole 16-byte groups");

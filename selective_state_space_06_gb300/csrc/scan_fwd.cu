@@ -56,13 +56,16 @@ __device__ __forceinline__ void fwd_load_chunk(const FwdParams& p, float* st, in
   float* s_C = s_B + kChunk * NP;
   const int t0 = c * kChunk;
   const size_t rowb = (size_t)b * p.T;
-  if constexpr (BF) {   // bf16 tiles into the first half of each slot (widened after the wait)
+  if constexpr (BF) {
+    // bf16 tiles into the slots the states-only forward leaves unused: delta and u share the
+    // gate slot (a half each), B takes the first half of the C slot; they are widened into
+    // their own slots after the wait
     static_assert(ST && VEC, "bf16 input is taken by the states-only forward");
-    stage_tile_bf16<DC, NTH>(s_dl, reinterpret_cast<const uint16_t*>(p.delta), rowb, t0, p.T,
+    stage_tile_bf16<DC, NTH>(s_g, reinterpret_cast<const uint16_t*>(p.delta), rowb, t0, p.T,
                              p.Di, dblk0);
-    stage_tile_bf16<DC, NTH>(s_u, reinterpret_cast<const uint16_t*>(p.u), rowb, t0, p.T, p.Di,
-                             dblk0);
-    stage_tile_bf16<NP, NTH>(s_B, reinterpret_cast<const uint16_t*>(p.B), rowb, t0, p.T, p.N, 0);
+    stage_tile_bf16<DC, NTH>(s_g + kChunk * DC / 2, reinterpret_cast<const uint16_t*>(p.u), rowb,
+                             t0, p.T, p.Di, dblk0);
+    stage_tile_bf16<NP, NTH>(s_C, reinterpret_cast<const uint16_t*>(p.B), rowb, t0, p.T, p.N, 0);
   } else if constexpr (VEC) {
     for (int q = threadIdx.x; q < kChunk * DC / 4; q += NTH) {
       const int i = q / (DC / 4), col = (q % (DC / 4)) * 4;
@@ -355,13 +358,12 @@ scan_fwd_kernel(const FwdParams p) {
         cp_async_commit();
     }
     float* st = smem + (it % kFwdStages) * S::kStageFloats;
-    if constexpr (BF) {   // widen the bf16 tiles in place
+    if constexpr (BF) {   // widen the bf16 tiles into their slots (no overlap: one barrier)
       BfTile<kChunk * DC, kWarps * 32> wdl, wu;
       BfTile<kChunk * NP, kWarps * 32> wB;
-      wdl.read(st);
-      wu.read(st + kChunk * DC);
-      wB.read(st + 3 * kChunk * DC);
-      __syncthreads();
+      wdl.read(st + 2 * kChunk * DC);
+      wu.read(st + 2 * kChunk * DC + kChunk * DC / 2);
+      wB.read(st + 3 * kChunk * DC + kChunk * NP);
       wdl.write(st);
       wu.write(st + kChunk * DC);
       wB.write(st + 3 * kChunk * DC);
