@@ -258,8 +258,8 @@ def run_gpu(args):
         step()
     torch.cuda.synchronize()
 
-    # timed region: K steps; per-step events on the launching stream split fwd from bwd
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    # timed region: K steps; two events per step on the launching stream split fwd from bwd
+    # (the end of step i - 1 is the start of step i)
     mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     sampler = ClockSampler(local)
@@ -274,7 +274,6 @@ def run_gpu(args):
     outer0.record(stream)
     launches = 0
     for i in range(args.steps):
-        starts[i].record(stream)
         ev_mid = mids[i]
         launches += step()
         ends[i].record(stream)
@@ -286,7 +285,7 @@ def run_gpu(args):
     sampler.mark(t_host0, t_host1)
     clocks = sampler.stop()
     total_ms = outer0.elapsed_time(outer1)
-    fwd_ms = [starts[i].elapsed_time(mids[i]) for i in range(args.steps)]
+    fwd_ms = [(ends[i - 1] if i else outer0).elapsed_time(mids[i]) for i in range(args.steps)]
     bwd_ms = [mids[i].elapsed_time(ends[i]) for i in range(args.steps)]
     total_ms = max_over_ranks(pg, total_ms, dev)
 

@@ -264,6 +264,7 @@ scan_bwd_agg_kernel(const BwdParams p) {
 // segment s from later time (zero for the last) replaces the aggregate in the first sub-slot
 // of s; slot 0 receives the carry entering segment 0.
 __global__ void scan_bwd_compose_kernel(const BwdParams p) {
+  pdl_wait();   // the pre-pass's aggregates are visible
   const size_t dn = (size_t)p.Di * p.N;
   const size_t total = (size_t)p.batch * dn;
   const int nslot = p.nseg * p.nsub;
@@ -629,6 +630,7 @@ scan_bwd_kernel(const BwdParams p) {
 // Fixed-order sums of the partials: d_B/d_C over CTAs along d, d_A_log/d_D over
 // (batch, segment).
 __global__ void scan_reduce_kernel(const BwdParams p) {
+  pdl_wait();   // the backward's partials are visible
   const size_t btn = (size_t)p.batch * p.T * p.N;
   const size_t dn = (size_t)p.Di * p.N;
   const size_t total = btn + dn + (size_t)p.Di;
@@ -698,8 +700,8 @@ static int launch_agg_tmem(const Plan& plan, const BwdParams& p, cudaStream_t s)
     int sms = 152, dev = 0;
     if (cudaGetDevice(&dev) == cudaSuccess)
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    scan_bwd_compose_kernel<<<sms * 4, 256, 0, s>>>(p);
-    if (cudaPeekAtLastError() != cudaSuccess) return -1;
+    if (launch_pdl(scan_bwd_compose_kernel, dim3(sms * 4), dim3(256), 0, s, p) != cudaSuccess)
+      return -1;
     ++na;
   }
   const int nm = launch_bwd_main_tmem(plan, p, s);
@@ -720,8 +722,8 @@ int launch_bwd_after_agg(const Plan& plan, const BwdParams& p, cudaStream_t s) {
     int sms = 152, dev = 0;
     if (cudaGetDevice(&dev) == cudaSuccess)
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    scan_bwd_compose_kernel<<<sms * 4, 256, 0, s>>>(p);
-    if (cudaPeekAtLastError() != cudaSuccess) return -1;
+    if (launch_pdl(scan_bwd_compose_kernel, dim3(sms * 4), dim3(256), 0, s, p) != cudaSuccess)
+      return -1;
     ++n;
   }
   const int nm = launch_bwd_main_tmem(plan, p, s);
@@ -729,7 +731,8 @@ int launch_bwd_after_agg(const Plan& plan, const BwdParams& p, cudaStream_t s) {
   int sms = 152, dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  scan_reduce_kernel<<<sms * 4, 256, 0, s>>>(p);
+  if (launch_pdl(scan_reduce_kernel, dim3(sms * 4), dim3(256), 0, s, p) != cudaSuccess)
+    return -1;
   return cudaPeekAtLastError() == cudaSuccess ? n + nm + 1 : -1;
 }
 
@@ -747,7 +750,8 @@ int launch_bwd(const Plan& plan, const BwdParams& p, cudaStream_t s) {
   int sms = 152, dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  scan_reduce_kernel<<<sms * 4, 256, 0, s>>>(p);
+  if (launch_pdl(scan_reduce_kernel, dim3(sms * 4), dim3(256), 0, s, p) != cudaSuccess)
+    return -1;
   return cudaPeekAtLastError() == cudaSuccess ? n + 1 : -1;
 }
 

@@ -172,6 +172,8 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
   float* smem = reinterpret_cast<float*>(
       smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u));   // 128-byte aligned
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kDataFloats);
+  pdl_wait();      // the previous kernel's writes (carries, checkpoints) are visible
+  pdl_release();   // one wave: the reduction may take the room this kernel leaves
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ng = lane & (G - 1), dg = lane >> LG;
@@ -701,6 +703,7 @@ scan_bwd_agg4_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
   float* smem = reinterpret_cast<float*>(
       smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u));   // 128-byte aligned
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + A::kDataFloats);
+  pdl_wait();   // the previous kernel's writes are visible
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ng = lane & (G - 1), dg = lane >> LG;
   const int b = blockIdx.y;
@@ -978,8 +981,9 @@ static int launch_main(const Plan& plan, const BwdMaps& maps, const BwdParams& p
                            (int)S::kSmemBytes) != cudaSuccess)
     return -1;
   dim3 grid((unsigned)(plan.bwd.nblk * plan.bwd.nseg), (unsigned)plan.batch);
-  kern<<<grid, kWarps * 32, S::kSmemBytes, s>>>(maps, p);
-  return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
+  return launch_pdl(kern, grid, dim3(kWarps * 32), S::kSmemBytes, s, maps, p) == cudaSuccess
+             ? 1
+             : -1;
 }
 
 // TMA needs 16-byte strides (d_inner and d_state multiples of 4) and a checkpoint tensor
@@ -1011,7 +1015,8 @@ static int launch_agg4(const Plan& plan, const BwdMaps& maps, const BwdParams& p
     return -1;
   dim3 grid((unsigned)(plan.bwd.nblk * (plan.bwd.nseg - 1) * plan.bwd.nsub),
             (unsigned)plan.batch);
-  kern<<<grid, kWarps * 32, A::kSmemBytes, s>>>(maps, p);
+  if (launch_pdl(kern, grid, dim3(kWarps * 32), A::kSmemBytes, s, maps, p) != cudaSuccess)
+    return -1;
   return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
 }
 

@@ -441,4 +441,33 @@ struct BfTile {
   }
 };
 
+// ---- programmatic dependent launch ---------------------------------------------------------
+// The scan kernels are launched with programmatic stream serialization, so the next one can be
+// scheduled while its predecessor in the stream still runs. Each of them calls pdl_wait() before
+// it touches global memory: that returns once the preceding kernel has completed and its writes
+// are visible (at once when there is no such kernel). The one-wave kernels (forward, tensor-
+// memory backward) call pdl_release() right after, so that the next kernel's CTAs can take the
+// SM room they leave and start as soon as they finish. A launch without the attribute makes
+// both no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 }  // namespace mscan

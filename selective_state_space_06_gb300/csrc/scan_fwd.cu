@@ -268,6 +268,8 @@ scan_fwd_kernel(const FwdParams p) {
   using S = FwdShape<NP>;
   constexpr int G = S::G, DW = S::DW, DC = S::DC, P = S::P, NPT = S::NPT, NPR = S::NPR;
   extern __shared__ __align__(16) float smem[];
+  pdl_wait();      // the previous kernel's writes (inputs, workspace) are visible
+  pdl_release();   // one wave: the next kernel may take the room this one leaves
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ng = lane % G, dg = lane / G;
@@ -496,8 +498,8 @@ static int launch_np(const Plan& plan, const FwdParams& p0, cudaStream_t s) {
     ++n;
   }
   dim3 grid((unsigned)(plan.fwd.nblk * plan.fwd.nseg), (unsigned)plan.batch);
-  kern<<<grid, kWarps * 32, S::kSmemBytes, s>>>(p);
-  return cudaPeekAtLastError() == cudaSuccess ? n + 1 : -1;
+  if (launch_pdl(kern, grid, dim3(kWarps * 32), S::kSmemBytes, s, p) != cudaSuccess) return -1;
+  return n + 1;
 }
 
 template <int NP>
