@@ -130,10 +130,10 @@ int mamba_scan_bwd_softplus(const float* delta_raw, const float* u, const float*
  * gate are not carried through device memory between the passes. For d_state <= 8 the call
  * runs the two passes as the separate entry points do. The checkpoint buffer's contents
  * afterwards are unspecified. Asynchronous on `stream`; device pointers, owned by the caller.
- * When T spans several backward segments, the backward's segment pre-pass (which reads only
- * inputs) runs on a library-owned side stream beside the forward: the call records an event on
- * `stream`, the side stream waits for it, and `stream` waits for the side stream before the
- * rest of the backward. The side stream and its events are created on the first such call of
+ * When T spans several backward segments, the backward's segment pre-pass and the composition
+ * of its carries (which read only inputs) run on a library-owned side stream beside the
+ * forward: the call records an event on `stream`, the side stream waits for it, and `stream`
+ * waits for the side stream before the rest of the backward. The side stream and its events are created on the first such call of
  * each host thread on each device and kept for the thread's lifetime; stream capture sees a
  * fork and a join. */
 int mamba_scan_fwd_bwd(const float* delta, const float* u, const float* B, const float* C,

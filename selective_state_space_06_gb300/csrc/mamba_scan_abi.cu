@@ -363,10 +363,10 @@ static int scan_bwd_impl(const float* delta, const float* u, const float* B, con
   p.out = fuse_out ? out : nullptr;
   if (fuse_out) p.y_ck = nullptr;   // y is recomputed from the states
   p.io_bf16 = io_bf16;
-  // phase 0: everything on `stream`; 1: the segment pre-pass alone, on `pre_stream`;
-  // 2: what follows the pre-pass, on `stream` (d_state 9..64)
-  const int n = phase == 1   ? mscan::launch_bwd_agg_tmem(plan, p, (cudaStream_t)pre_stream)
-                : phase == 2 ? mscan::launch_bwd_after_agg(plan, p, (cudaStream_t)stream)
+  // phase 0: everything on `stream`; 1: the segment pre-pass and the composition of the
+  // carries, on `pre_stream`; 2: the backward and the reduction, on `stream` (d_state 9..64)
+  const int n = phase == 1   ? mscan::launch_bwd_carries(plan, p, (cudaStream_t)pre_stream)
+                : phase == 2 ? mscan::launch_bwd_after_carries(plan, p, (cudaStream_t)stream)
                              : mscan::launch_bwd(plan, p, (cudaStream_t)stream);
   if (n < 0) return set_cuda_error(cudaGetLastError());
   g_last_launches = n;
@@ -442,10 +442,10 @@ static int fwd_bwd_impl(const float* delta, const float* u, const float* B, cons
   // bf16 I/O: the fused path with TMA staging only (16-byte rows of bf16, two chunks or more)
   if (io_bf16 && (!fused || d_inner % 8 != 0 || d_state % 8 != 0 || plan.nchunks < 2))
     return MAMBA_ERR_UNSUPPORTED;
-  // The backward's segment pre-pass reads only inputs, so in the fused path it runs on a side
-  // stream beside the forward (which leaves most issue slots idle); the rest of the backward
-  // waits for both. The fork event is recorded before the forward is enqueued, so the forward's
-  // CTAs are dispatched first.
+  // The backward's segment pre-pass and the composition of its carries read only inputs, so in
+  // the fused path they run on a side stream beside the forward (which leaves most issue slots
+  // idle); the backward proper waits for both. The fork event is recorded before the forward
+  // is enqueued, so the forward's CTAs are dispatched first.
   SideStream side;
   const bool overlap = fused && plan.bwd.nseg > 1 && side_stream(&side);
   const cudaStream_t s = (cudaStream_t)stream;

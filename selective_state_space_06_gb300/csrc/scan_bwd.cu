@@ -714,10 +714,12 @@ static int launch_vec(const Plan& plan, const BwdParams& p, cudaStream_t s) {
   return vec ? launch_np<NP, true>(plan, p, s) : launch_np<NP, false>(plan, p, s);
 }
 
-// d_state 9..64, after launch_bwd_agg_tmem: the composition, the backward and the reduction.
-int launch_bwd_after_agg(const Plan& plan, const BwdParams& p, cudaStream_t s) {
+// d_state 9..64: the segment pre-pass and the composition of its aggregates into carries
+// (they read only inputs), and then, separately, the backward and the reduction.
+int launch_bwd_carries(const Plan& plan, const BwdParams& p, cudaStream_t s) {
   if (plan.NP < kTmemMinNP) return -1;
-  int n = 0;
+  int n = launch_bwd_agg_tmem(plan, p, s);
+  if (n < 0) return -1;
   if (plan.bwd.nseg > 1) {
     int sms = 152, dev = 0;
     if (cudaGetDevice(&dev) == cudaSuccess)
@@ -726,6 +728,11 @@ int launch_bwd_after_agg(const Plan& plan, const BwdParams& p, cudaStream_t s) {
       return -1;
     ++n;
   }
+  return n;
+}
+
+int launch_bwd_after_carries(const Plan& plan, const BwdParams& p, cudaStream_t s) {
+  if (plan.NP < kTmemMinNP) return -1;
   const int nm = launch_bwd_main_tmem(plan, p, s);
   if (nm < 0) return -1;
   int sms = 152, dev = 0;
@@ -733,7 +740,7 @@ int launch_bwd_after_agg(const Plan& plan, const BwdParams& p, cudaStream_t s) {
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (launch_pdl(scan_reduce_kernel, dim3(sms * 4), dim3(256), 0, s, p) != cudaSuccess)
     return -1;
-  return cudaPeekAtLastError() == cudaSuccess ? n + nm + 1 : -1;
+  return nm + 1;
 }
 
 int launch_bwd(const Plan& plan, const BwdParams& p, cudaStream_t s) {

@@ -130,7 +130,9 @@ int launch_bwd(const Plan& plan, const BwdParams& p, cudaStream_t stream);
 int launch_bwd_main_tmem(const Plan& plan, const BwdParams& p, cudaStream_t stream);
 // its segment pre-pass (0 kernels when there is one segment)
 int launch_bwd_agg_tmem(const Plan& plan, const BwdParams& p, cudaStream_t stream);
-// what launch_bwd enqueues after that pre-pass: composition, backward, reduction (d_state 9..64)
-int launch_bwd_after_agg(const Plan& plan, const BwdParams& p, cudaStream_t stream);
+// launch_bwd split in two for d_state 9..64: the pre-pass and the composition of the carries
+// (inputs only), then the backward and the reduction
+int launch_bwd_carries(const Plan& plan, const BwdParams& p, cudaStream_t stream);
+int launch_bwd_after_carries(const Plan& plan, const BwdParams& p, cudaStream_t stream);
 
 }  // namespace mscan
