@@ -82,6 +82,8 @@ __device__ __forceinline__ float silu_f(float p) { return p * sigmoid_fast(p); }
 template <int K, int VW>
 __global__ void __launch_bounds__(256) conv_fwd_kernel(const ConvParams p) {
   using V = Vec<VW>;
+  pdl_wait();      // the previous kernel's writes are visible
+  pdl_release();   // one wave (the run length is picked for that)
   const ConvThread c = conv_thread(p, VW);
   if (!c.valid) return;
   float w[K][VW], bias[VW];
@@ -136,6 +138,8 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(const ConvParams p) {
   using V = Vec<VW>;
   // CTA = (batch row, group of 8 runs, 32 channel groups); warp = run, lane = channel group
   __shared__ float s_red[kConvRunsPerCta][32][(K + 1) * VW];
+  pdl_wait();      // the previous kernel's writes are visible
+  pdl_release();   // the reduction may take the room this kernel leaves
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ncg = p.Di / VW;
   const int ncgb = (ncg + 31) / 32;
@@ -255,6 +259,7 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(const ConvParams p) {
 // d_w and d_bias: one warp per output sums the run groups' partials in a fixed order: lane l takes
 // runs l, l+32, ... in turn, then the lanes are added by a fixed butterfly (deterministic).
 __global__ void conv_reduce_kernel(const ConvParams p) {
+  pdl_wait();   // the backward's partials are visible
   const size_t nw = (size_t)p.Di * p.K;
   const size_t total = nw + (size_t)p.Di;
   const int nk = p.batch * p.ngroups;
@@ -324,34 +329,30 @@ static int launch_k(const ConvParams& p0, bool bwd, cudaStream_t s) {
   const long long ncg = p0.Di / VW;
   ConvParams p = p0;
   if (!bwd) {
-    const void* kern = vec ? (const void*)conv_fwd_kernel<K, 2> : (const void*)conv_fwd_kernel<K, 1>;
-    const long long slots = resident_slots(kern, 256);
+    auto kern = vec ? conv_fwd_kernel<K, 2> : conv_fwd_kernel<K, 1>;
+    const long long slots = resident_slots((const void*)kern, 256);
     p.run = pick_run(p, slots, [&](int nruns) { return (p.batch * nruns * ncg + 255) / 256; });
     p.nruns = (p.T + p.run - 1) / p.run;
     const unsigned blocks = (unsigned)(((long long)p.batch * p.nruns * ncg + 255) / 256);
-    if (vec) conv_fwd_kernel<K, 2><<<blocks, 256, 0, s>>>(p);
-    else conv_fwd_kernel<K, 1><<<blocks, 256, 0, s>>>(p);
-    return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
+    return launch_pdl(kern, dim3(blocks), dim3(256), 0, s, p) == cudaSuccess ? 1 : -1;
   }
   const long long ncgb = (ncg + 31) / 32;
-  const void* kern = vec ? (const void*)conv_bwd_kernel<K, 2> : (const void*)conv_bwd_kernel<K, 1>;
-  const long long slots = resident_slots(kern, 256);
+  auto bkern = vec ? conv_bwd_kernel<K, 2> : conv_bwd_kernel<K, 1>;
+  const long long slots = resident_slots((const void*)bkern, 256);
   p.run = pick_run(p, slots, [&](int nruns) {
     return (long long)p.batch * ((nruns + kConvRunsPerCta - 1) / kConvRunsPerCta) * ncgb;
   });
   p.nruns = (p.T + p.run - 1) / p.run;
   p.ngroups = (p.nruns + kConvRunsPerCta - 1) / kConvRunsPerCta;   // <= the scratch's count
   const unsigned bblocks = (unsigned)((long long)p.batch * p.ngroups * ncgb);
-  if (vec) conv_bwd_kernel<K, 2><<<bblocks, 256, 0, s>>>(p);
-  else conv_bwd_kernel<K, 1><<<bblocks, 256, 0, s>>>(p);
-  if (cudaPeekAtLastError() != cudaSuccess) return -1;
+  if (launch_pdl(bkern, dim3(bblocks), dim3(256), 0, s, p) != cudaSuccess) return -1;
   int sms = 152, dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const size_t outs = (size_t)p.Di * (p.K + 1);
   const unsigned rblocks = (unsigned)std::min<size_t>((outs + 7) / 8, (size_t)sms * 16);
-  conv_reduce_kernel<<<rblocks, 256, 0, s>>>(p);
-  return cudaPeekAtLastError() == cudaSuccess ? 2 : -1;
+  return launch_pdl(conv_reduce_kernel, dim3(rblocks), dim3(256), 0, s, p) == cudaSuccess ? 2
+                                                                                         : -1;
 }
 
 int launch_conv(const ConvParams& p, bool bwd, cudaStream_t s) {
