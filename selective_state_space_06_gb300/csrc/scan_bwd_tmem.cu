@@ -432,8 +432,8 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
           v[k] = (TMA || n < N) ? s_h0[(cl + chan(q, k)) * NP + n] : 0.f;
         h[q][s] = make_float2(v[0], v[1]);
       }
-    // per-thread views of the staged tiles (the step loops are unrolled by two: measured
-    // faster than full unrolling, which runs out of registers)
+    // per-thread views of the staged tiles (measured: the recompute loop fully unrolled, the
+    // reverse walk by two; unrolling the reverse walk further runs short of registers)
     const float2* pdl[2] = {reinterpret_cast<const float2*>(s_dl + offc[0]),
                             reinterpret_cast<const float2*>(s_dl + offc[1])};
     const float2* pu[2] = {reinterpret_cast<const float2*>(s_u + offc[0]),
@@ -441,7 +441,7 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
     const float* s_dyv = BF ? s_dy : s_g;   // d_y
     const float2* pdy[2] = {reinterpret_cast<const float2*>(s_dyv + offc[0]),
                             reinterpret_cast<const float2*>(s_dyv + offc[1])};
-#pragma unroll 2
+#pragma unroll
     for (int i = 0; i < kChunk; ++i) {
       step_fence();
       tmem_st16(taddr + 16 * i, reinterpret_cast<const float2(&)[8]>(h));
