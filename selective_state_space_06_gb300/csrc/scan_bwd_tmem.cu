@@ -433,7 +433,7 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
         h[q][s] = make_float2(v[0], v[1]);
       }
     // per-thread views of the staged tiles (measured: the recompute loop fully unrolled, the
-    // reverse walk by two; unrolling the reverse walk further runs short of registers)
+    // reverse walk by four; both fit the 255 registers a thread may have)
     const float2* pdl[2] = {reinterpret_cast<const float2*>(s_dl + offc[0]),
                             reinterpret_cast<const float2*>(s_dl + offc[1])};
     const float2* pu[2] = {reinterpret_cast<const float2*>(s_u + offc[0]),
@@ -504,7 +504,7 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
     float* const out_du = p.d_u + (rowb + t0) * Di + d_out;
     const int lim_dd = (w_delta && d_out < Di) ? T - t0 : 0;
     const int lim_du = (w_u && d_out < Di) ? T - t0 : 0;
-#pragma unroll 2
+#pragma unroll 4
     for (int ii = 0; ii < kChunk; ++ii) {
       const int i = kChunk - 1 - ii;
       step_fence();
