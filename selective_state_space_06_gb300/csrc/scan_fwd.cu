@@ -383,7 +383,7 @@ scan_fwd_kernel(const FwdParams p) {
     const int t0 = c * kChunk;
 
     if constexpr (ST) {
-#pragma unroll 4
+#pragma unroll
       for (int i = 0; i < kChunk; ++i) {
         const float2 dlv = lds2(s_dl + i * DC + cl);
         const float2 uv = lds2(s_u + i * DC + cl);
