@@ -35,11 +35,11 @@ bool make_plan(int64_t batch, int64_t T, int64_t Di, int64_t N, Plan* pl) {
     q.seg_chunks = (p.nchunks + want - 1) / want;
     q.nseg = (p.nchunks + q.seg_chunks - 1) / q.seg_chunks;
   };
-  auto pass = [&](int npt, int dpt) {
+  auto pass = [&](int npt, int dpt, int warps = kWarps) {
     PassPlan q;
     q.NPT = npt;
     q.G = p.NP / npt;
-    q.DC = kWarps * (32 / q.G) * dpt;
+    q.DC = warps * (32 / q.G) * dpt;
     q.nblk = (int)((Di + q.DC - 1) / q.DC);
     return q;
   };
@@ -67,7 +67,7 @@ bool make_plan(int64_t batch, int64_t T, int64_t Di, int64_t N, Plan* pl) {
     split(q, best_want);
     return q;
   };
-  p.fwd = by_target(pass(states_per_thread_fwd(p.NP), kDPT), target_units_fwd(p.NP));
+  p.fwd = by_target(pass(states_per_thread_fwd(p.NP), kDPT, kFwdWarps), target_units_fwd(p.NP));
   if (p.NP >= kTmemMinNP)
     p.bwd = by_waves(pass(4, kTmemDPT), kTmemSlots);
   else

@@ -38,7 +38,7 @@ struct FwdShape {
   static constexpr int NPR = NPT / 2;                  // float2 pairs of states per thread
   static constexpr int G = NP / NPT;                   // lanes per channel group
   static constexpr int DW = (32 / G) * kDPT;           // channels per warp
-  static constexpr int DC = kWarps * DW;               // channels per CTA
+  static constexpr int DC = kFwdWarps * DW;            // channels per CTA
   static constexpr int P = G >= 2 ? G / 2 : 1;         // steps per output group
   static constexpr int kStageFloats = kChunk * (3 * DC + 2 * NP);
   static constexpr size_t kSmemBytes = (size_t)kFwdStages * kStageFloats * sizeof(float);
@@ -48,7 +48,7 @@ template <int NP, bool VEC, bool ST = false, bool BF = false>
 __device__ __forceinline__ void fwd_load_chunk(const FwdParams& p, float* st, int c, int b,
                                                int dblk0) {
   using S = FwdShape<NP>;
-  constexpr int DC = S::DC, NTH = kWarps * 32;
+  constexpr int DC = S::DC, NTH = kFwdWarps * 32;
   float* s_dl = st;
   float* s_u = st + kChunk * DC;
   float* s_g = st + 2 * kChunk * DC;
@@ -261,7 +261,7 @@ scan_fwd_agg_kernel(const FwdParams p) {
 // alone; the backward then recomputes y from the states and writes out.
 // BF (with ST): delta, u and B arrive as bf16 and are widened in shared memory.
 template <int NP, bool VEC, bool WITH_Y, bool SP, bool ST, bool BF = false>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kFwdWarps * 32)
 scan_fwd_kernel(const FwdParams p) {
   static_assert(!(ST && (SP || WITH_Y)), "the states-only forward takes the plain delta");
   static_assert(!BF || ST, "bf16 input is taken by the states-only forward");
@@ -361,8 +361,8 @@ scan_fwd_kernel(const FwdParams p) {
     }
     float* st = smem + (it % kFwdStages) * S::kStageFloats;
     if constexpr (BF) {   // widen the bf16 tiles into their slots (no overlap: one barrier)
-      BfTile<kChunk * DC, kWarps * 32> wdl, wu;
-      BfTile<kChunk * NP, kWarps * 32> wB;
+      BfTile<kChunk * DC, kFwdWarps * 32> wdl, wu;
+      BfTile<kChunk * NP, kFwdWarps * 32> wB;
       wdl.read(st + 2 * kChunk * DC);
       wu.read(st + 2 * kChunk * DC + kChunk * DC / 2);
       wB.read(st + 3 * kChunk * DC + kChunk * NP);
@@ -372,7 +372,7 @@ scan_fwd_kernel(const FwdParams p) {
       __syncthreads();
     }
     if constexpr (SP) {   // raw delta -> delta in shared memory, once per element
-      softplus_tile<DC, kWarps * 32>(st, p.T - c * kChunk, p.Di - dblk0);
+      softplus_tile<DC, kFwdWarps * 32>(st, p.T - c * kChunk, p.Di - dblk0);
       __syncthreads();
     }
     const float* s_dl = st;
@@ -472,7 +472,7 @@ static int launch_np(const Plan& plan, const FwdParams& p0, cudaStream_t s) {
              : p0.softplus   ? scan_fwd_kernel<NP, VEC, WITH_Y, true, false>
                              : scan_fwd_kernel<NP, VEC, WITH_Y, false, false>;
   auto agg = scan_fwd_agg_kernel<NP, VEC>;
-  if constexpr (NP >= kTmemMinNP && VEC && !WITH_Y) {   // the bf16 fused call (d_state % 8 == 0)
+  if constexpr (NP >= kTmemMinNP && VEC && !WITH_Y && S::DC % 8 == 0) {   // bf16 fused call
     if (p0.io_bf16) {
       kern = scan_fwd_kernel<NP, true, false, false, true, true>;
       agg = scan_fwd_agg_kernel<NP, true, true>;
@@ -498,7 +498,8 @@ static int launch_np(const Plan& plan, const FwdParams& p0, cudaStream_t s) {
     ++n;
   }
   dim3 grid((unsigned)(plan.fwd.nblk * plan.fwd.nseg), (unsigned)plan.batch);
-  if (launch_pdl(kern, grid, dim3(kWarps * 32), S::kSmemBytes, s, p) != cudaSuccess) return -1;
+  if (launch_pdl(kern, grid, dim3(kFwdWarps * 32), S::kSmemBytes, s, p) != cudaSuccess)
+    return -1;
   return n + 1;
 }
 

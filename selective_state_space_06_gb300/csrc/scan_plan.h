@@ -19,6 +19,9 @@ constexpr int kDPT = 2;     // channels per thread
 __host__ __device__ constexpr int states_per_thread_fwd(int NP) { return NP <= 16 ? 2 : 4; }
 __host__ __device__ constexpr int states_per_thread_bwd(int NP) { return NP < 4 ? NP : 4; }
 constexpr int kWarps = 4;   // warps per CTA
+// warps per CTA of the forward scan (measured: 2 warps per CTA runs as fast, 1 is 10 % slower
+// at mamba130m and 57 % at longseq; the CTAs' uneven spread over the SMs does not limit it)
+constexpr int kFwdWarps = 4;
 // Warps per CTA of the segment pre-pass kernels (the main kernels' CTA shape measured best;
 // wider CTAs with several segments each were slower on GB300).
 constexpr int kAggWarps = kWarps;
