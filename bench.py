@@ -13,6 +13,10 @@ The default workload is the Mamba-130M-width layer (batch 8, T 1024, d_inner 153
 --workload picks another. --impl reference times the fp64 CPU oracle on a bounded sample of the
 same workload instead.
 
+Besides the step, `variants` reports (unless --no-variants) the softplus-fused calls, the
+fused forward + backward call (mamba_scan_fwd_bwd) and its bf16 I/O form, and the causal
+conv1d + SiLU step before the scan, each timed on the same workload.
+
 Multi-GPU runs (torchrun) are independent replicas, one per GPU. The scan has no cross-device
 exchange, so there is no collective on the data path. value = all ranks' elements / max time.
 """

@@ -805,7 +805,7 @@ scan_bwd_agg4_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
     const float* s_dy = st + 2 * TILE;
     const float* s_C = st + 3 * TILE;
     if constexpr (VEC) {
-#pragma unroll 2
+#pragma unroll
       for (int e = 4 * threadIdx.x; e < TILE; e += 4 * NTH) {
         const float4 g = *reinterpret_cast<const float4*>(s_g + e);
         const float4 go = *reinterpret_cast<const float4*>(s_dy + e);
