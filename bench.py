@@ -171,8 +171,8 @@ BWD_CALL_KERNELS = ("mamba_scan_bwd call: scan_bwd_agg4_kernel + scan_bwd_compos
                     "scan_bwd_tmem_kernel + scan_reduce_kernel (d_state 16-64)")
 # DRAM bytes read + written by one mamba_scan_bwd call, summed over its kernels, from the ncu
 # capture in profiles/scan_kernels_mamba130m.md (dram__bytes_read.sum + dram__bytes_write.sum;
-# 103.0 + 10.1 + 434.6 + 15.1 MB). Workloads without a capture report null.
-BWD_TRAFFIC_BYTES = {"mamba130m": 562.8e6}
+# 103.1 + 10.1 + 434.2 + 15.1 MB). Workloads without a capture report null.
+BWD_TRAFFIC_BYTES = {"mamba130m": 562.5e6}
 
 
 def time_conv(ms, w, dev, stream, steps, hbm_gbs, K=4) -> dict:
