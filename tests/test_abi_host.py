@@ -136,6 +136,48 @@ def test_bwd_validation_codes(ms):
     assert lib.mamba_scan_bwd(*_bwd_args(dims=(1, 40, 64, 100))) == ms.MAMBA_ERR_UNSUPPORTED
 
 
+def _fused_args(**over):
+    b, T, Di, N = over.pop("dims", (2, 40, 64, 16))
+    big = 1 << 32
+    names = ("delta", "u", "B", "C", "gate", "A_log", "D", "dy", "out", "ckpt", "scratch",
+             "d_delta", "d_u", "d_B", "d_C", "d_A_log", "d_D", "d_gate")
+    ptr = {k: big * (i + 1) for i, k in enumerate(names)}
+    ptr.update(over)
+    return [ptr["delta"], ptr["u"], ptr["B"], ptr["C"], ptr["gate"], ptr["A_log"], ptr["D"],
+            ptr["dy"], ptr["out"], ptr["ckpt"], over.get("ckpt_bytes", 10 ** 9), ptr["scratch"],
+            over.get("scratch_bytes", 10 ** 9), ptr["d_delta"], ptr["d_u"], ptr["d_B"],
+            ptr["d_C"], ptr["d_A_log"], ptr["d_D"], ptr["d_gate"], b, T, Di, N, None]
+
+
+@needs_no_gpu
+def test_fused_validation_codes(ms):
+    """mamba_scan_fwd_bwd checks everything, out included, before its first launch."""
+    lib = ms.raw_library()
+    big = 1 << 32
+    f = lib.mamba_scan_fwd_bwd
+    assert f(*_fused_args(out=None)) == ms.MAMBA_ERR_INVALID_ARG
+    assert f(*_fused_args(out=big * 9 + 8)) == ms.MAMBA_ERR_MISALIGNED
+    assert f(*_fused_args(out=big * 12)) == ms.MAMBA_ERR_INVALID_ARG          # out == d_delta
+    assert f(*_fused_args(scratch_bytes=1024)) == ms.MAMBA_ERR_WORKSPACE
+    assert f(*_fused_args(dims=(1, 40, 64, 65))) == ms.MAMBA_ERR_UNSUPPORTED
+
+
+@needs_no_gpu
+def test_fused_bf16_validation_codes(ms):
+    """The bf16 fused call: sizes it does not take are refused before any launch, and the
+    overlap checks use 2-byte elements for the bf16 tensors."""
+    lib = ms.raw_library()
+    big = 1 << 32
+    f = lib.mamba_scan_fwd_bwd_bf16
+    for dims in ((2, 40, 64, 8), (2, 40, 36, 16), (2, 16, 64, 16), (2, 40, 64, 20)):
+        assert f(*_fused_args(dims=dims)) == ms.MAMBA_ERR_UNSUPPORTED, dims
+    btd16 = 2 * 40 * 64 * 2                                        # bytes of a bf16 [2, 40, 64]
+    # d_u right after out in bf16: no overlap, so validation passes and the launch itself
+    # fails here, where there is no device
+    assert f(*_fused_args(d_u=big * 9 + btd16)) == ms.MAMBA_ERR_CUDA
+    assert f(*_fused_args(d_u=big * 9 + btd16 - 16)) == ms.MAMBA_ERR_INVALID_ARG
+
+
 @needs_no_gpu
 def test_host_entry_validation(ms):
     lib = ms.raw_library()
