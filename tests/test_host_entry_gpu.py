@@ -1,7 +1,8 @@
 """mamba_scan_fwd_bwd_host: forward + backward from host buffers, against the fp64 oracle.
 
-The host entry cuts the batch into slices that run on two streams, so that the copies in both
-directions overlap the kernels; d_A_log and d_D are the slices' sums added in slice order. The
+The host entry cuts the batch into up to four slices, each on its own stream, so that the
+copies in both directions overlap the kernels; d_A_log and d_D are the slices' sums added in
+slice order. The
 outputs must meet the parity bar of the device entry points on every element (out and the
 seven gradients; y is not returned by this call). The shapes cover four slices (mamba130m),
 three slices with a shorter last one (batch 5), and one slice (rows of T*d_inner not a
