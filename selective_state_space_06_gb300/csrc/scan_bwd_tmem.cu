@@ -16,6 +16,10 @@
 //      to tensor memory: 16 steps x 16 floats = 256 columns per thread lane;
 //   2. reverse walk: the state before the step comes back from tensor memory; the state after
 //      it is the one read for the later step. No step is recomputed twice.
+// Variants (template flags): SP takes the raw delta and applies the softplus in shared memory;
+// FY (the fused forward + backward call) forms y = sum_n C*h + D*u during step 1 and runs step
+// 0's gating after it, writing out as well; BF (FY with bf16 I/O) receives its tiles as bf16
+// in shared memory the fused path leaves idle and stores bf16 outputs.
 //
 // Reductions without select instructions where possible. A butterfly level that halves the
 // values a lane keeps normally needs two selects per exchanged value (which half to keep,
