@@ -124,11 +124,12 @@ int mamba_scan_bwd_softplus(const float* delta_raw, const float* u, const float*
  * seven gradients, exactly what mamba_scan_fwd followed by mamba_scan_bwd writes (y is not
  * returned). Same inputs, layouts, checkpoint and scratch buffers (mamba_scan_ckpt_bytes,
  * mamba_scan_scratch_bytes) and error codes; out must not overlap any other argument, and
- * every check runs before the first launch. For d_state 9..64 the forward pass keeps only the
+ * every check runs before the first launch. For d_state 9..16 the forward pass keeps only the
  * chunk-boundary states (it reads neither C nor gate and writes neither out nor y) and the
  * backward forms y = sum_n C*h + D*u from the states it recomputes anyway, so out, y and the
- * gate are not carried through device memory between the passes. For d_state <= 8 the call
- * runs the two passes as the separate entry points do. The checkpoint buffer's contents
+ * gate are not carried through device memory between the passes. For d_state 17..64, where
+ * that reduction costs the backward more than it saves, and for d_state <= 8, the call runs
+ * the two passes as the separate entry points do. The checkpoint buffer's contents
  * afterwards are unspecified. Asynchronous on `stream`; device pointers, owned by the caller.
  * When T spans several backward segments, the backward's segment pre-pass and the composition
  * of its carries (which read only inputs) run on a library-owned side stream beside the
@@ -147,7 +148,8 @@ int mamba_scan_fwd_bwd(const float* delta, const float* u, const float* B, const
  * d_B, d_C, d_gate are bfloat16 (2 bytes per element, same layouts); A_log, D, d_A_log and d_D
  * stay fp32, and so do the checkpoint and scratch buffers (same sizes as for fp32). The
  * kernels widen the inputs to fp32 in shared memory, compute everything in fp32 exactly as the
- * fp32 call does, and round each bf16 output once, to nearest even. Takes 9 <= d_state <= 64,
+ * fp32 call does (forming y in the backward at every d_state), and round each bf16 output
+ * once, to nearest even. Takes 9 <= d_state <= 64,
  * d_inner and d_state multiples of 8 and T > 16 (bf16 rows then start on 16-byte boundaries,
  * which the tensor-memory copies need); other sizes return MAMBA_ERR_UNSUPPORTED before
  * anything is launched. Pointers must be 16-byte aligned. */

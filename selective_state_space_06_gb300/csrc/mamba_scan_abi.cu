@@ -436,18 +436,22 @@ static int fwd_bwd_impl(const float* delta, const float* u, const float* B, cons
   if (rc != MAMBA_OK) return rc;
   Plan plan;
   if (!mscan::make_plan(batch, T, d_inner, d_state, &plan)) return MAMBA_ERR_INVALID_ARG;
-  // d_state 9..64 (the tensor-memory backward): the forward keeps only the checkpoints and the
-  // backward forms y and out; smaller d_state runs the two passes as separate calls do
-  const bool fused = plan.NP >= mscan::kTmemMinNP;
+  // d_state 9..64 runs the tensor-memory backward. Up to d_state 16 the forward keeps only the
+  // checkpoints and the backward forms y and out; above, where forming y costs the backward
+  // more than it saves the forward (measured at d_state 64), the forward writes out and y as
+  // the separate call does, except with bf16 I/O, whose kernels are the fused ones. Smaller
+  // d_state runs the two passes as separate calls do.
+  const bool tmem = plan.NP >= mscan::kTmemMinNP;
+  const bool fused = tmem && (io_bf16 || plan.NP <= 16);
   // bf16 I/O: the fused path with TMA staging only (16-byte rows of bf16, two chunks or more)
-  if (io_bf16 && (!fused || d_inner % 8 != 0 || d_state % 8 != 0 || plan.nchunks < 2))
+  if (io_bf16 && (!tmem || d_inner % 8 != 0 || d_state % 8 != 0 || plan.nchunks < 2))
     return MAMBA_ERR_UNSUPPORTED;
   // The backward's segment pre-pass and the composition of its carries read only inputs, so in
   // the fused path they run on a side stream beside the forward (which leaves most issue slots
   // idle); the backward proper waits for both. The fork event is recorded before the forward
   // is enqueued, so the forward's CTAs are dispatched first.
   SideStream side;
-  const bool overlap = fused && plan.bwd.nseg > 1 && side_stream(&side);
+  const bool overlap = tmem && plan.bwd.nseg > 1 && side_stream(&side);
   const cudaStream_t s = (cudaStream_t)stream;
   if (overlap) {
     if (cudaEventRecord(side.fork, s) != cudaSuccess ||

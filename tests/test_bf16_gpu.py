@@ -9,7 +9,10 @@ d_A_log and d_D stay fp32 and keep the fp32 bar.
 
 Exactly, since widening bf16 to fp32 is exact and the kernels then run the fp32 arithmetic:
 every bf16 output equals the fp32 fused call's output on the same (bf16-valued) inputs,
-rounded to nearest even, bit for bit; d_A_log and d_D equal it outright.
+rounded to nearest even, bit for bit; d_A_log and d_D equal it outright. Above d_state 16 the
+fp32 fused call takes y from the forward (summed in another order), while the bf16 call forms
+it in the backward at every d_state, so there out and d_gate, the outputs that depend on y,
+are left to the oracle bar.
 """
 import numpy as np
 import pytest
@@ -135,7 +138,10 @@ def test_bf16_equals_rounded_fp32_call(shape):
     bf, vals = _bf16_inputs(_inputs(shape))
     got = run_bf16(bf, vals)
     f32 = run_fp32_fused(vals)
+    same_y = shape[3] <= 16   # both calls form y in the backward
     for k in BF_OUT:
+        if not same_y and k in ("out", "d_gate"):
+            continue
         want = f32[k].to(torch.bfloat16)
         assert torch.equal(got[k].view(torch.int16), want.view(torch.int16)), k
     for k in F32_OUT:

@@ -1,14 +1,15 @@
 """mamba_scan_fwd_bwd (forward and backward in one call, dy known up front) against the fp64
 oracle.
 
-For d_state 9..64 the forward pass keeps only the chunk-boundary states and the backward forms
+For d_state 9..16 the forward pass keeps only the chunk-boundary states and the backward forms
 y = sum_n C*h + D*u from its recomputed states, so out and d_gate come from a y summed in
 another order than the separate forward's; they must meet the parity bar like every other
 output. The other six gradients do not depend on y at all: they must equal the separate
-calls' bitwise, since both paths run the same recurrence from the same checkpoints. The shapes
-run every variant of the fused backward (d_state 16, 32, 64; TMA and cp.async staging; one and
-several time segments; T = 1 and T not a multiple of the 16-step chunk) and the d_state <= 8
-path, where the call runs the two passes unfused.
+calls' bitwise, since both paths run the same recurrence from the same checkpoints. Above
+d_state 16 and at d_state <= 8 the call runs the two passes as the separate calls do (with the
+backward's pre-pass beside the forward when T spans several segments). The shapes cover both
+(d_state 5 to 64; TMA and cp.async staging; one and several time segments; T = 1 and T not a
+multiple of the 16-step chunk).
 """
 import numpy as np
 import pytest
