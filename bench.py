@@ -9,9 +9,12 @@ recurrence and the fixed-order reductions.
   e2e    = the same metric through mamba_scan_fwd_bwd_host with pinned HOST buffers: the
            host->device copies of the inputs and the device->host copies of out and all seven
            gradients fall inside the timed region.
-The default workload is the Mamba-130M-width layer (batch 8, T 1024, d_inner 1536, d_state 16).
---workload picks another. --impl reference times the fp64 CPU oracle on a bounded sample of the
-same workload instead.
+The headline workload is the largest single-GPU layer, the long-sequence wide-state scan
+(batch 1, T 65536, d_inner 2560, d_state 64). The same run also times the Mamba-370M- and
+Mamba-1.4B-width layers (d_state 16) and the Mamba-130M-width layer and reports them under
+`per_workload`, each with its forward, backward and step times and its HBM and ALU fractions.
+--workload picks another headline. --impl reference times the fp64 CPU oracle on a bounded
+sample of the same workload instead.
 
 Besides the step, `variants` reports (unless --no-variants) the softplus-fused calls, the
 fused forward + backward call (mamba_scan_fwd_bwd) and its bf16 I/O form, and the causal
@@ -39,7 +42,9 @@ import synth  # noqa: E402
 
 METRIC = "selective-scan fwd+bwd (batch*T*d_inner)/sec"
 UNIT = "elements/s"
-DEFAULT_WORKLOAD = "mamba130m"
+DEFAULT_WORKLOAD = "longseq"
+# the other layers timed in the same run (`per_workload`)
+PER_WORKLOAD = ("mamba370m", "mamba1p4b", "mamba130m")
 
 
 def minimal_bytes(w) -> dict:
@@ -166,13 +171,74 @@ def dist_env():
     return ws, rank, local
 
 
-# The roofline is that of one mamba_scan_bwd call, the dominant part of the step.
-BWD_CALL_KERNELS = ("mamba_scan_bwd call: scan_bwd_agg4_kernel + scan_bwd_compose_kernel + "
+# The roofline is that of one mamba_scan_bwd call, the dominant part of the step (its kernels
+# together; the call is the unit the minimal-traffic count is defined for).
+BWD_CALL_KERNELS = ("mamba_scan_bwd call: segment pre-pass + carry composition + "
                     "scan_bwd_tmem_kernel + scan_reduce_kernel (d_state 16-64)")
-# DRAM bytes read + written by one mamba_scan_bwd call, summed over its kernels, from the ncu
-# capture in profiles/scan_kernels_mamba130m.md (dram__bytes_read.sum + dram__bytes_write.sum;
-# 103.1 + 10.1 + 434.2 + 15.1 MB). Workloads without a capture report null.
-BWD_TRAFFIC_BYTES = {"mamba130m": 562.5e6}
+# Algorithmic compute of the backward call alone per (b, t, d, n): the recompute (3 fp32
+# operations) and the reverse step (8), 1 ex2.
+BWD_FP32_OPS_PER_ELEMENT_STATE = 11
+BWD_EX2_PER_ELEMENT_STATE = 1
+
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum, summed over the call's kernels) of
+# one mamba_scan_bwd call, taken from an ncu capture of these kernels. Each entry carries the
+# digest of the kernel sources it was captured with (kernel_digest() below); once the sources
+# differ the entry no longer describes the kernels and `traffic` is reported as null.
+BWD_TRAFFIC_CAPTURES = {
+    # workload: (bytes per call, kernel digest, how the figure was taken)
+}
+
+
+def kernel_digest() -> str:
+    """sha256 (first 16 hex digits) over the CUDA sources of the library, in name order."""
+    import hashlib
+    d = os.path.join(ROOT, "selective_state_space_06_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(d)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(d, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def bwd_traffic(name: str):
+    cap = BWD_TRAFFIC_CAPTURES.get(name)
+    if cap is None or cap[1] != kernel_digest():
+        return None, None
+    return cap[0], cap[2]
+
+
+def roofline_of(w, fwd_s: float, bwd_s: float, step_s: float, sm_mhz: float, hbm_gbs: float,
+                hbm_source: str) -> dict:
+    """The backward call's roofline. Both of its bounds are given: HBM (minimal bytes over the
+    call's time against the measured copy bandwidth) and fp32 ALU (algorithmic operations over
+    the call's time against 152 SMs x 128 lanes x the sampled clock). `bound` names the one
+    whose floor is higher for this workload, and the top-level fields are that bound's."""
+    mb = minimal_bytes(w)
+    ns = w.btd * w.d_state
+    ghz = sm_mhz / 1e3
+    hbm_ach = mb["bwd"] / bwd_s / 1e9
+    alu_ach = BWD_FP32_OPS_PER_ELEMENT_STATE * ns / bwd_s / 1e9
+    alu_peak = SMS * FP32_LANES_PER_SM * ghz
+    hbm_floor = mb["bwd"] / (hbm_gbs * 1e9)
+    alu_floor = BWD_FP32_OPS_PER_ELEMENT_STATE * ns / (alu_peak * 1e9)
+    traffic, how = bwd_traffic(w.name)
+    hbm = {"achieved": hbm_ach, "peak": hbm_gbs, "unit": "GB/s", "frac": hbm_ach / hbm_gbs,
+           "peak_source": f"{hbm_source} (MEASURED_PEAKS.json hbm_gbs)"
+           if hbm_source == "measured" else "fallback 6.8 TB/s"}
+    alu = {"achieved": alu_ach, "peak": alu_peak, "unit": "Gop/s", "frac": alu_ach / alu_peak,
+           "ops_per_element_state": BWD_FP32_OPS_PER_ELEMENT_STATE,
+           "peak_source": f"152 SMs x 128 fp32 lanes x sampled SM clock {sm_mhz:.0f} MHz"}
+    bound = "alu" if alu_floor > hbm_floor else "hbm"
+    top = alu if bound == "alu" else hbm
+    return {"kernel": BWD_CALL_KERNELS, "bound": bound, "achieved": top["achieved"],
+            "peak": top["peak"], "unit": top["unit"], "frac": top["frac"],
+            "peak_source": top["peak_source"], "traffic": traffic, "traffic_capture": how,
+            "algorithmic_bytes_per_launch": mb["bwd"],
+            "algorithmic_fp32_ops_per_launch": BWD_FP32_OPS_PER_ELEMENT_STATE * ns,
+            "hbm": hbm, "alu": alu,
+            "hbm_frac_fwd": mb["fwd"] / fwd_s / 1e9 / hbm_gbs,
+            "hbm_frac_step": mb["total"] / step_s / 1e9 / hbm_gbs}
 
 
 def time_conv(ms, w, dev, stream, steps, hbm_gbs, K=4) -> dict:
@@ -228,23 +294,15 @@ def time_conv(ms, w, dev, stream, steps, hbm_gbs, K=4) -> dict:
             "bwd_hbm_frac": bwd_bytes / (bwd_ms * 1e-3) / 1e9 / hbm_gbs}
 
 
-def run_gpu(args):
-    import torch
-    import selective_state_space_06_gb300 as ms
+def time_steps(ms, x, bufs, stream, steps, warmup, pg=None, sampler=None) -> dict:
+    """Times `steps` steps (mamba_scan_fwd + mamba_scan_bwd) after `warmup` untimed ones.
 
-    ws, rank, local = dist_env()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    pg = None
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-        pg = dist
-    w = synth.BY_NAME[args.workload]
-    x_np = synth.make_inputs(w, seed=0)
-    x = {k: torch.from_numpy(v).to(dev) for k, v in x_np.items()}
-    bufs = ms.alloc_like_outputs(x["delta"], x["B"], x["A_log"], x["D"])
-    stream = torch.cuda.current_stream(dev)
+    One pair of events brackets the whole timed region (after a barrier and a synchronize). On a
+    regular sample of the steps (at least 64, or all), events on the launching stream also split
+    the forward call from the backward call. An event between two calls stops the second call's
+    first kernel from starting early (programmatic dependent launch), so the other steps run
+    without them, as a caller's would."""
+    import torch
 
     def step(ev_mid=None):
         ms.mamba_scan_fwd(x["delta"], x["u"], x["B"], x["C"], x["gate"], x["A_log"], x["D"],
@@ -258,29 +316,24 @@ def run_gpu(args):
                           stream=stream)
         return nf + ms.mamba_scan_last_launch_count()
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize()
-
-    # timed region: K steps. On a regular sample of them (at least 64, or all), events on the
-    # launching stream split the forward call from the backward call. An event between two
-    # calls stops the second call's first kernel from starting early (programmatic dependent
-    # launch), so the other steps run without them, as a caller's would.
-    stride = max(1, args.steps // 64)
-    sampled = list(range(0, args.steps, stride))
+    stride = max(1, steps // 64)
+    sampled = list(range(0, steps, stride))
     ev = {i: [torch.cuda.Event(enable_timing=True) for _ in range(3)] for i in sampled}
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
+    outer0 = torch.cuda.Event(enable_timing=True)
+    outer1 = torch.cuda.Event(enable_timing=True)
+    if sampler is not None:
+        sampler.start()
+        time.sleep(0.3)
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
     t_host0 = time.time()
-    outer0 = torch.cuda.Event(enable_timing=True)
-    outer1 = torch.cuda.Event(enable_timing=True)
     outer0.record(stream)
     launches = 0
-    for i in range(args.steps):
+    for i in range(steps):
         e = ev.get(i)
         if e is None:
             launches += step()
@@ -293,12 +346,86 @@ def run_gpu(args):
     if pg:
         pg.barrier()
     t_host1 = time.time()
-    sampler.mark(t_host0, t_host1)
-    clocks = sampler.stop()
-    total_ms = outer0.elapsed_time(outer1)
-    fwd_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in sampled]
-    bwd_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in sampled]
-    total_ms = max_over_ranks(pg, total_ms, dev)
+    clocks = None
+    if sampler is not None:
+        sampler.mark(t_host0, t_host1)
+        clocks = sampler.stop()
+    return {"total_ms": outer0.elapsed_time(outer1),
+            "fwd_ms": float(np.mean([ev[i][0].elapsed_time(ev[i][1]) for i in sampled])),
+            "bwd_ms": float(np.mean([ev[i][1].elapsed_time(ev[i][2]) for i in sampled])),
+            "split_steps": len(sampled), "launches": launches, "clocks": clocks}
+
+
+def time_loop(fn, stream, steps: int, warmup: int = 3) -> float:
+    """Mean CUDA-event time in ms of `fn` over `steps` back-to-back calls after `warmup`."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def fused_step(ms, x, bufs, stream):
+    """The forward and backward in one call (dy known up front)."""
+    def f():
+        ms.mamba_scan_fwd_bwd(x["delta"], x["u"], x["B"], x["C"], x["gate"], x["A_log"], x["D"],
+                              x["dy"], bufs["out"], bufs["ckpt"], bufs["scratch"],
+                              bufs["d_delta"], bufs["d_u"], bufs["d_B"], bufs["d_C"],
+                              bufs["d_A_log"], bufs["d_D"], bufs["d_gate"], stream=stream)
+    return f
+
+
+def workload_entry(ms, w, dev, stream, steps, warmup, peaks, index) -> dict:
+    """The step of another workload, timed on its own (same timing rules as the headline)."""
+    import torch
+    x = {k: torch.from_numpy(v).to(dev) for k, v in synth.make_inputs(w, seed=0).items()}
+    bufs = ms.alloc_like_outputs(x["delta"], x["B"], x["A_log"], x["D"])
+    r = time_steps(ms, x, bufs, stream, steps, warmup, sampler=ClockSampler(index))
+    fused_ms = time_loop(fused_step(ms, x, bufs, stream), stream, max(3, min(steps, 50)))
+    del x, bufs
+    torch.cuda.empty_cache()
+    step_s = r["total_ms"] * 1e-3 / steps
+    sm_mhz = float((r["clocks"] or {}).get("sm_mhz") or 2070.0)
+    return {"batch": w.batch, "T": w.T, "d_inner": w.d_inner, "d_state": w.d_state,
+            "value": w.btd / step_s, "unit": UNIT, "ms_per_step": 1e3 * step_s,
+            "fwd_ms": r["fwd_ms"], "bwd_ms": r["bwd_ms"], "steps": steps,
+            "fused_fwd_bwd_ms": fused_ms,
+            "roofline": roofline_of(w, r["fwd_ms"] * 1e-3, r["bwd_ms"] * 1e-3, step_s, sm_mhz,
+                                    peaks["hbm_gbs"], peaks["source"]),
+            "alu_roofline": alu_roofline(w, step_s, sm_mhz), "clocks": r["clocks"]}
+
+
+def run_gpu(args):
+    import torch
+    import selective_state_space_06_gb300 as ms
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    peaks = read_peaks()
+    w = synth.BY_NAME[args.workload]
+    x_np = synth.make_inputs(w, seed=0)
+    x = {k: torch.from_numpy(v).to(dev) for k, v in x_np.items()}
+    bufs = ms.alloc_like_outputs(x["delta"], x["B"], x["A_log"], x["D"])
+    stream = torch.cuda.current_stream(dev)
+
+    r = time_steps(ms, x, bufs, stream, args.steps, args.warmup, pg=pg,
+                   sampler=ClockSampler(local))
+    clocks = r["clocks"]
+    total_ms = max_over_ranks(pg, r["total_ms"], dev)
+    launches = r["launches"]
 
     # end-to-end through the host-buffer entry point (pinned host memory)
     e2e = None
@@ -333,12 +460,13 @@ def run_gpu(args):
         e2e = {"value": job_throughput(w.btd * ke, ws, el), "unit": UNIT,
                "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": ke, "ms_per_step": 1e3 * el / ke}
-        del wsbuf
+        del wsbuf, hin, hout
 
-    # variant: the softplus in front of the scan fused into the kernels (raw delta in,
-    # d_delta_raw out), on the raw delta that gives this workload's delta
     variants = {}
     if not args.no_variants:
+        kv = max(3, min(args.steps, 50))
+        # the softplus in front of the scan fused into the kernels (raw delta in, d_delta_raw
+        # out), on the raw delta that gives this workload's delta
         raw_np = np.log(np.expm1(x_np["delta"].astype(np.float64))).astype(np.float32)
         raw = torch.from_numpy(raw_np).to(dev)
         del raw_np
@@ -351,42 +479,16 @@ def run_gpu(args):
                                        bufs["d_delta"], bufs["d_u"], bufs["d_B"], bufs["d_C"],
                                        bufs["d_A_log"], bufs["d_D"], bufs["d_gate"],
                                        stream=stream)
-        for _ in range(3):
-            step_sp()
-        kv = max(3, min(args.steps, 50))
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        e0.record(stream)
-        for _ in range(kv):
-            step_sp()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ms_sp = e0.elapsed_time(e1) / kv
+        ms_sp = time_loop(step_sp, stream, kv)
         variants["softplus_fused"] = {"ms_per_step": ms_sp, "value": w.btd / (ms_sp * 1e-3),
                                       "unit": UNIT, "steps": kv}
         del raw
-
-        # variant: forward and backward in one call when dy is known up front (the forward
-        # keeps only the checkpoints; the backward forms y and writes out)
-        def step_fused():
-            ms.mamba_scan_fwd_bwd(x["delta"], x["u"], x["B"], x["C"], x["gate"], x["A_log"],
-                                  x["D"], x["dy"], bufs["out"], bufs["ckpt"], bufs["scratch"],
-                                  bufs["d_delta"], bufs["d_u"], bufs["d_B"], bufs["d_C"],
-                                  bufs["d_A_log"], bufs["d_D"], bufs["d_gate"], stream=stream)
-        for _ in range(3):
-            step_fused()
-        torch.cuda.synchronize()
-        e0.record(stream)
-        for _ in range(kv):
-            step_fused()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ms_fu = e0.elapsed_time(e1) / kv
+        # forward and backward in one call when dy is known up front
+        ms_fu = time_loop(fused_step(ms, x, bufs, stream), stream, kv)
         variants["fused_fwd_bwd"] = {"ms_per_step": ms_fu, "value": w.btd / (ms_fu * 1e-3),
                                      "unit": UNIT, "steps": kv,
                                      "launches": ms.mamba_scan_last_launch_count()}
-        # variant: the fused call with bf16 I/O (inputs rounded to bf16; fp32 arithmetic)
+        # the fused call with bf16 I/O (inputs rounded to bf16; fp32 arithmetic)
         if w.d_state % 8 == 0 and w.d_inner % 8 == 0 and 9 <= w.d_state <= 64 and w.T > 16:
             bf = {k: x[k].to(torch.bfloat16) for k in ("delta", "u", "B", "C", "gate", "dy")}
             ob = {k: torch.empty_like(bf["delta"]) for k in ("out", "d_delta", "d_u", "d_gate")}
@@ -399,46 +501,41 @@ def run_gpu(args):
                                            bufs["scratch"], ob["d_delta"], ob["d_u"], ob["d_B"],
                                            ob["d_C"], bufs["d_A_log"], bufs["d_D"],
                                            ob["d_gate"], stream=stream)
-            for _ in range(3):
-                step_bf16()
-            torch.cuda.synchronize()
-            e0.record(stream)
-            for _ in range(kv):
-                step_bf16()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            ms_bf = e0.elapsed_time(e1) / kv
+            ms_bf = time_loop(step_bf16, stream, kv)
             variants["fused_fwd_bwd_bf16"] = {"ms_per_step": ms_bf,
                                               "value": w.btd / (ms_bf * 1e-3), "unit": UNIT,
                                               "steps": kv, "io": "bf16", "arithmetic": "f32"}
             del bf, ob
-        variants["conv1d_silu"] = time_conv(ms, w, dev, stream, kv, read_peaks()["hbm_gbs"])
+        variants["conv1d_silu"] = time_conv(ms, w, dev, stream, kv, peaks["hbm_gbs"])
 
-    mb = minimal_bytes(w)
-    peaks = read_peaks()
-    bwd_mean_s = float(np.mean(bwd_ms)) * 1e-3
-    fwd_mean_s = float(np.mean(fwd_ms)) * 1e-3
-    achieved = mb["bwd"] / bwd_mean_s / 1e9
+    del x, bufs
+    torch.cuda.empty_cache()
+    per_workload = {}
+    if not args.no_per_workload:
+        for name in PER_WORKLOAD:
+            if name != w.name:
+                per_workload[name] = workload_entry(ms, synth.BY_NAME[name], dev, stream,
+                                                    args.steps, args.warmup, peaks, local)
+
+    step_s = total_ms * 1e-3 / args.steps
+    sm_mhz = float((clocks or {}).get("sm_mhz") or 2070.0)
     value = job_throughput(w.btd * args.steps, ws, total_ms * 1e-3)
+    mb = minimal_bytes(w)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": w.name, "batch": w.batch, "T": w.T, "d_inner": w.d_inner,
                    "d_state": w.d_state, "seed": 0,
-                   "l2": "no flush: per-step working set > 126 MB L2 "
-                         f"(inputs {4 * (4 * w.btd + 2 * w.btn) / 1e6:.0f} MB)",
+                   "l2": "no flush: inputs larger than the 126 MB L2 "
+                         f"({4 * (4 * w.btd + 2 * w.btn) / 1e6:.0f} MB read per step)",
                    "parallelism": f"replicas x{ws}"},
-        "fwd_ms": 1e3 * fwd_mean_s, "bwd_ms": 1e3 * bwd_mean_s,
-        "fwd_bwd_split_steps": len(sampled),
-        "hbm_frac_step": (mb["total"] / (total_ms * 1e-3 / args.steps) / 1e9) / peaks["hbm_gbs"],
-        "roofline": {"kernel": BWD_CALL_KERNELS, "bound": "hbm", "achieved": achieved,
-                     "peak": peaks["hbm_gbs"], "peak_source": peaks["source"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": BWD_TRAFFIC_BYTES.get(w.name),
-                     "algorithmic_bytes_per_launch": mb["bwd"]},
-        "alu_roofline": alu_roofline(w, total_ms * 1e-3 / args.steps,
-                                     float(clocks.get("sm_mhz") or 2070.0)),
+        "fwd_ms": r["fwd_ms"], "bwd_ms": r["bwd_ms"], "fwd_bwd_split_steps": r["split_steps"],
+        "hbm_frac_step": (mb["total"] / step_s / 1e9) / peaks["hbm_gbs"],
+        "roofline": roofline_of(w, r["fwd_ms"] * 1e-3, r["bwd_ms"] * 1e-3, step_s, sm_mhz,
+                                peaks["hbm_gbs"], peaks["source"]),
+        "alu_roofline": alu_roofline(w, step_s, sm_mhz),
+        "per_workload": per_workload,
         "variants": variants,
         "gpu_launches": launches,
         "clocks": clocks,
@@ -482,6 +579,29 @@ def _calibrated_rows(w, run, budget_s):
     return int(max(1, min(rows_total, budget_s / max(per_row, 1e-12))))
 
 
+def cpu_info() -> dict:
+    """The host's logical CPU count and CPU model (from /proc/cpuinfo, else lscpu)."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    if model is None:
+        try:
+            r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+            for line in r.stdout.splitlines():
+                if line.strip().lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except Exception:
+            pass
+    return {"nproc": os.cpu_count(), "cpu_model": model or "unknown"}
+
+
 def cpu_baseline(w, budget_s: float = 12.0) -> dict:
     """The oracle as it stands (single-threaded fp64 C, forward + backward per row) on a bounded
     sample of rows of the workload; scaled to elements/s."""
@@ -490,7 +610,7 @@ def cpu_baseline(w, budget_s: float = 12.0) -> dict:
     el = run(rows)
     return {"value": rows * w.T / el, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"{rows} of {w.batch * w.d_inner} rows (b,d) x T={w.T}, fwd+bwd, fp64, "
-                      f"1 thread; {el:.1f} s"}
+                      f"1 thread; {el:.1f} s", **cpu_info()}
 
 
 def run_reference(args):
@@ -517,7 +637,7 @@ def run_reference(args):
         "config": {"workload": w.name, "batch": w.batch, "T": w.T, "d_inner": w.d_inner,
                    "d_state": w.d_state, "seed": 0},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, **cpu_info()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -533,7 +653,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-variants", action="store_true",
-                    help="skip timing the fused-softplus variant")
+                    help="skip timing the variants (softplus, fused, bf16, conv1d)")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="time the headline workload only")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
     if args.warmup < 3:

@@ -209,8 +209,11 @@ int mamba_scan_fwd_bwd_host(const float* delta, const float* u, const float* B, 
  * on every GPU that loads it, until the process exits. Sizes whose
  * mamba_scan_scratch_bytes(...) exceeds that limit are rejected with MAMBA_ERR_NOALLOC_LIMIT
  * before anything is launched. The first call on each device looks up the array's device
- * address (with that device current) and caches it, so that first call should come before any
- * stream capture. All calls on a device share the array, and it keeps the last call's contents.
+ * address (with that device current) and caches it with the identity of the current CUDA
+ * context; a call in another context (after cudaDeviceReset, or under a context the caller made
+ * current) looks it up again. So the first call in a context should come before any stream
+ * capture. A failed look-up returns MAMBA_ERR_CUDA, and mamba_scan_strerror names the CUDA
+ * error. All calls on a device share the array, and it keeps the last call's contents.
  * Nothing needs clearing, because the backward rewrites all the scratch it reads. Calls that
  * overlap on the GPU race on the array: order them (one stream, or explicit events). No
  * cudaMalloc, cudaFree or allocating library routine is called. */
@@ -221,6 +224,25 @@ int mamba_scan_bwd_noalloc(const float* delta, const float* u, const float* B, c
                            float* d_u, float* d_B, float* d_C, float* d_A_log, float* d_D,
                            float* d_gate, int64_t batch, int64_t T, int64_t d_inner,
                            int64_t d_state, void* stream);
+
+/* Failure-path test of the bounded copy waits (for tests only; the paper has no counterpart).
+ * The same arguments and buffers as mamba_scan_bwd, which it runs with one fault planted on the
+ * host side: the tensor-memory backward issues no copy for the last chunk that each of its
+ * CTAs walks, and every copy wait of the call gives up after 1 ms instead of 1 s. So the wait
+ * for that chunk runs out: the kernel sets its fault word, goes on with the stale stage (no
+ * address depends on the data), and exits with no copy in flight, since every copy it did
+ * issue was waited for before use. The next mamba_scan_status then returns MAMBA_ERR_TIMEOUT
+ * and clears the word; the call's outputs are invalid, while later calls are unaffected.
+ * Only sizes that run that kernel with tensor copies are taken (9 <= d_state <= 64, d_inner
+ * and d_state multiples of 4, T > 16); others return MAMBA_ERR_UNSUPPORTED before anything is
+ * launched. */
+int mamba_scan_bwd_test_timeout(const float* delta, const float* u, const float* B,
+                                const float* C, const float* gate, const float* A_log,
+                                const float* D, const float* dy, const void* ckpt,
+                                size_t ckpt_bytes, void* scratch, size_t scratch_bytes,
+                                float* d_delta, float* d_u, float* d_B, float* d_C,
+                                float* d_A_log, float* d_D, float* d_gate, int64_t batch,
+                                int64_t T, int64_t d_inner, int64_t d_state, void* stream);
 
 /* Synchronises `stream` and reports any asynchronous CUDA error (MAMBA_ERR_CUDA) or a
  * kernel that gave up waiting for its own copies (MAMBA_ERR_TIMEOUT; the flag is then

@@ -1,6 +1,7 @@
 // C ABI of libmambascan.so: argument validation, buffer sizing, launches, the host-buffer
 // end-to-end call and error reporting. The contract is documented in include/mamba_scan.h.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>   // header-only; ranges cost a pointer check when no tool listens
 
 #include <stdint.h>
 #include <stdio.h>
@@ -110,6 +111,16 @@ bool make_plan(int64_t batch, int64_t T, int64_t Di, int64_t N, Plan* pl) {
 using mscan::Plan;
 using mscan::round_up;
 
+namespace mscan {
+// An NVTX range around one entry point call (visible in Nsight Systems / ncu range filters).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+}  // namespace mscan
+
 namespace {
 
 thread_local int g_last_launches = 0;
@@ -127,6 +138,14 @@ int set_cuda_error(cudaError_t e) {
   g_last_cuda = e;
   return MAMBA_ERR_CUDA;
 }
+
+}  // namespace
+
+namespace mscan {
+int record_cuda_error(cudaError_t e) { return set_cuda_error(e); }
+}  // namespace mscan
+
+namespace {
 
 // Common size/pointer checks of the device entry points.
 int check_dims(int64_t batch, int64_t T, int64_t Di, int64_t N, Plan* plan) {
@@ -288,6 +307,7 @@ int mamba_scan_fwd(const float* delta, const float* u, const float* B, const flo
                    const float* gate, const float* A_log, const float* D, float* out, float* y,
                    void* ckpt, size_t ckpt_bytes, int64_t batch, int64_t T, int64_t d_inner,
                    int64_t d_state, void* stream) {
+  mscan::NvtxRange nvtx_range("mamba_scan_fwd");
   return scan_fwd_impl(delta, u, B, C, gate, A_log, D, out, y, ckpt, ckpt_bytes, batch, T,
                        d_inner, d_state, stream, 0);
 }
@@ -297,6 +317,7 @@ int mamba_scan_fwd_softplus(const float* delta_raw, const float* u, const float*
                             const float* D, float* out, float* y, void* ckpt,
                             size_t ckpt_bytes, int64_t batch, int64_t T, int64_t d_inner,
                             int64_t d_state, void* stream) {
+  mscan::NvtxRange nvtx_range("mamba_scan_fwd_softplus");
   return scan_fwd_impl(delta_raw, u, B, C, gate, A_log, D, out, y, ckpt, ckpt_bytes, batch, T,
                        d_inner, d_state, stream, 1);
 }
@@ -309,7 +330,7 @@ static int scan_bwd_impl(const float* delta, const float* u, const float* B, con
                          int64_t T, int64_t d_inner, int64_t d_state, void* stream,
                          int softplus, float* out = nullptr, bool fuse_out = false,
                          bool check_only = false, int io_bf16 = 0, int phase = 0,
-                         void* pre_stream = nullptr) {
+                         void* pre_stream = nullptr, int test_timeout = 0) {
   Plan plan;
   int rc = check_dims(batch, T, d_inner, d_state, &plan);
   if (rc != MAMBA_OK) return rc;
@@ -363,6 +384,13 @@ static int scan_bwd_impl(const float* delta, const float* u, const float* B, con
   p.out = fuse_out ? out : nullptr;
   if (fuse_out) p.y_ck = nullptr;   // y is recomputed from the states
   p.io_bf16 = io_bf16;
+  p.wait_limit_ns = 1000000000ull;   // one second per copy wait
+  if (test_timeout) {
+    // the failure-path test: the tensor-memory backward leaves the copies of each CTA's last
+    // chunk unissued and gives up waiting for them after 1 ms
+    p.test_skip_last_copy = 1;
+    p.wait_limit_ns = 1000000ull;
+  }
   // phase 0: everything on `stream`; 1: the segment pre-pass and the composition of the
   // carries, on `pre_stream`; 2: the backward and the reduction, on `stream` (d_state 9..64)
   const int n = phase == 1   ? mscan::launch_bwd_carries(plan, p, (cudaStream_t)pre_stream)
@@ -379,6 +407,7 @@ int mamba_scan_bwd(const float* delta, const float* u, const float* B, const flo
                    float* d_delta, float* d_u, float* d_B, float* d_C, float* d_A_log,
                    float* d_D, float* d_gate, int64_t batch, int64_t T, int64_t d_inner,
                    int64_t d_state, void* stream) {
+  mscan::NvtxRange nvtx_range("mamba_scan_bwd");
   return scan_bwd_impl(delta, u, B, C, gate, A_log, D, dy, ckpt, ckpt_bytes, scratch,
                        scratch_bytes, d_delta, d_u, d_B, d_C, d_A_log, d_D, d_gate, batch, T,
                        d_inner, d_state, stream, 0);
@@ -391,9 +420,29 @@ int mamba_scan_bwd_softplus(const float* delta_raw, const float* u, const float*
                             float* d_delta_raw, float* d_u, float* d_B, float* d_C,
                             float* d_A_log, float* d_D, float* d_gate, int64_t batch, int64_t T,
                             int64_t d_inner, int64_t d_state, void* stream) {
+  mscan::NvtxRange nvtx_range("mamba_scan_bwd_softplus");
   return scan_bwd_impl(delta_raw, u, B, C, gate, A_log, D, dy, ckpt, ckpt_bytes, scratch,
                        scratch_bytes, d_delta_raw, d_u, d_B, d_C, d_A_log, d_D, d_gate, batch,
                        T, d_inner, d_state, stream, 1);
+}
+
+int mamba_scan_bwd_test_timeout(const float* delta, const float* u, const float* B,
+                                const float* C, const float* gate, const float* A_log,
+                                const float* D, const float* dy, const void* ckpt,
+                                size_t ckpt_bytes, void* scratch, size_t scratch_bytes,
+                                float* d_delta, float* d_u, float* d_B, float* d_C,
+                                float* d_A_log, float* d_D, float* d_gate, int64_t batch,
+                                int64_t T, int64_t d_inner, int64_t d_state, void* stream) {
+  mscan::NvtxRange nvtx_range("mamba_scan_bwd_test_timeout");
+  Plan plan;
+  const int rc = check_dims(batch, T, d_inner, d_state, &plan);
+  if (rc != MAMBA_OK) return rc;
+  // only the tensor-memory backward with tensor-copy staging waits on copies it issues itself
+  if (plan.NP < mscan::kTmemMinNP || d_inner % 4 != 0 || d_state % 4 != 0 || plan.nchunks < 2)
+    return MAMBA_ERR_UNSUPPORTED;
+  return scan_bwd_impl(delta, u, B, C, gate, A_log, D, dy, ckpt, ckpt_bytes, scratch,
+                       scratch_bytes, d_delta, d_u, d_B, d_C, d_A_log, d_D, d_gate, batch, T,
+                       d_inner, d_state, stream, 0, nullptr, false, false, 0, 0, nullptr, 1);
 }
 
 // The fused call's side stream and its two events, one set per (host thread, device), created
@@ -487,6 +536,7 @@ int mamba_scan_fwd_bwd(const float* delta, const float* u, const float* B, const
                        size_t scratch_bytes, float* d_delta, float* d_u, float* d_B, float* d_C,
                        float* d_A_log, float* d_D, float* d_gate, int64_t batch, int64_t T,
                        int64_t d_inner, int64_t d_state, void* stream) {
+  mscan::NvtxRange nvtx_range("mamba_scan_fwd_bwd");
   return fwd_bwd_impl(delta, u, B, C, gate, A_log, D, dy, out, ckpt, ckpt_bytes, scratch,
                       scratch_bytes, d_delta, d_u, d_B, d_C, d_A_log, d_D, d_gate, batch, T,
                       d_inner, d_state, stream, 0);
@@ -499,6 +549,7 @@ int mamba_scan_fwd_bwd_bf16(const void* delta, const void* u, const void* B, con
                             void* d_B, void* d_C, float* d_A_log, float* d_D, void* d_gate,
                             int64_t batch, int64_t T, int64_t d_inner, int64_t d_state,
                             void* stream) {
+  mscan::NvtxRange nvtx_range("mamba_scan_fwd_bwd_bf16");
   // the kernels take the bf16 tensors through the same parameter slots (io_bf16 set)
   auto in = [](const void* q) { return static_cast<const float*>(q); };
   auto io = [](void* q) { return static_cast<float*>(q); };
@@ -520,6 +571,7 @@ int mamba_scan_fwd_bwd_host(const float* delta, const float* u, const float* B, 
                             float* d_C, float* d_A_log, float* d_D, float* d_gate,
                             void* workspace, size_t workspace_bytes, int64_t batch, int64_t T,
                             int64_t d_inner, int64_t d_state, void* stream) {
+  mscan::NvtxRange nvtx_range("mamba_scan_fwd_bwd_host");
   Plan plan;
   int rc = check_dims(batch, T, d_inner, d_state, &plan);
   if (rc != MAMBA_OK) return rc;

@@ -11,21 +11,26 @@
 // MAMBA_SCAN_NOALLOC_SCRATCH_BYTES. Every GPU that loads the library holds it until the
 // process exits. In host code the array's name is only a host-side stand-in, not a device
 // address. So the first call on each device, with that device current, asks the runtime for the
-// array's device address (cudaGetSymbolAddress), checks the result and caches it. Every later
-// call on that device reuses the cached address. Because the first call does this set-up, it
-// should come before any stream capture. The call itself allocates nothing: no cudaMalloc, no
-// cudaFree, no allocating library routine.
+// array's device address (cudaGetSymbolAddress), checks the result and caches it together with
+// the identity of the CUDA context it belongs to (cuCtxGetId). A later call in the same context
+// reuses the address; a call in another context (a new primary context after cudaDeviceReset,
+// or a context the caller made current) looks it up again. Because the first call in a context
+// does this set-up, it should come before any stream capture. A failed look-up returns
+// MAMBA_ERR_CUDA with the CUDA error recorded for mamba_scan_strerror. The call itself allocates
+// nothing: no cudaMalloc, no cudaFree, no allocating library routine.
 //
 // Sharing. All calls on a device share the one array, and it keeps the last call's contents.
 // The backward writes every scratch word it later reads (its per-CTA partial sums), so nothing
 // has to be cleared between calls. Calls that overlap on the GPU (different streams, or
 // different host threads without ordering) race on the array and give wrong results: the caller
 // must order them.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
 
 #include "../../include/mamba_scan.h"
+#include "scan_plan.h"
 
 namespace {
 
@@ -33,18 +38,60 @@ constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[MAMBA_SCAN_NOALLOC_SCRATCH_BYTES];
 
+// The driver's context queries, looked up once through the runtime (no driver library linked).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+struct CtxFns {
+  CtxGetCurrentFn get_current = nullptr;
+  CtxGetIdFn get_id = nullptr;
+};
+const CtxFns& ctx_fns() {
+  static CtxFns f;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      f.get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      f.get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  return f;
+}
+
+// Identity of the current context (0 when it cannot be told, or no context is current yet).
+unsigned long long current_context_id() {
+  const CtxFns& f = ctx_fns();
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!f.get_current || !f.get_id || f.get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  if (f.get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
 std::mutex g_setup_mutex;
 void* g_scratch_addr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};
 
-// Device address of g_noalloc_scratch on the current device (set up once per device).
+// Device address of g_noalloc_scratch in the current context of the current device.
 int noalloc_scratch_address(void** out) {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MAMBA_ERR_CUDA;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return mscan::record_cuda_error(e);
+  if (dev < 0 || dev >= kMaxDevices) return mscan::record_cuda_error(cudaErrorInvalidDevice);
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (!g_scratch_addr[dev]) {
+  const unsigned long long ctx = current_context_id();
+  if (!g_scratch_addr[dev] || ctx == 0 || ctx != g_scratch_ctx[dev]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MAMBA_ERR_CUDA;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return mscan::record_cuda_error(e);
+    if (!p) return mscan::record_cuda_error(cudaErrorInvalidSymbol);
     g_scratch_addr[dev] = p;
+    // the look-up makes the device's primary context current when none was
+    g_scratch_ctx[dev] = ctx ? ctx : current_context_id();
   }
   *out = g_scratch_addr[dev];
   return MAMBA_OK;

@@ -150,9 +150,10 @@ __device__ __forceinline__ void bwd_tmem_load_chunk(const BwdMaps& maps, const B
 
 // Waits until stage `stage` (its use number `use`) has landed in shared memory.
 template <bool TMA>
-__device__ __forceinline__ void bwd_tmem_wait_stage(uint64_t* bars, int stage, int use) {
+__device__ __forceinline__ void bwd_tmem_wait_stage(uint64_t* bars, int stage, int use,
+                                                    uint64_t limit_ns) {
   if constexpr (TMA) {
-    if (!mbar_wait(bars + stage, (uint32_t)(use & 1))) atomicOr(&g_bwd_fault, 1u);
+    if (!mbar_wait(bars + stage, (uint32_t)(use & 1), limit_ns)) atomicOr(&g_bwd_fault, 1u);
   } else {
     cp_async_wait<kTmemStages - 2>();
   }
@@ -201,9 +202,11 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
       fence_mbar_init();
     }
   }
+  // the failure-path test leaves the copies of the CTA's last chunk (use nck - 1) unissued
+  const int skip_use = (TMA && p.test_skip_last_copy) ? nck - 1 : -1;
 #pragma unroll
   for (int s = 0; s < kTmemStages - 1; ++s) {
-    if (s < nck)
+    if (s < nck && s != skip_use)
       bwd_tmem_load_chunk<NP, VEC, TMA, FY, BF>(maps, p, smem + s * S::kStageFloats, bars + s,
                                                 last - s, b, dblk0);
     else if constexpr (!TMA)
@@ -295,11 +298,11 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
 
   for (int it = 0; it < nck; ++it) {
     const int c = last - it;
-    bwd_tmem_wait_stage<TMA>(bars, it % kTmemStages, it / kTmemStages);
+    bwd_tmem_wait_stage<TMA>(bars, it % kTmemStages, it / kTmemStages, p.wait_limit_ns);
     __syncthreads();
     {
       const int itn = it + kTmemStages - 1;
-      if (itn < nck)
+      if (itn < nck && itn != skip_use)
         bwd_tmem_load_chunk<NP, VEC, TMA, FY, BF>(maps, p,
                                                   smem + (itn % kTmemStages) * S::kStageFloats,
                                                   bars + itn % kTmemStages, last - itn, b, dblk0);
@@ -781,7 +784,7 @@ scan_bwd_agg4_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
   for (int c = c_begin; c < c_end; ++c) {
     const int it = c - c_begin;
     if constexpr (TMA) {
-      if (!mbar_wait(bars + it % A::kStages, (uint32_t)((it / A::kStages) & 1)))
+      if (!mbar_wait(bars + it % A::kStages, (uint32_t)((it / A::kStages) & 1), p.wait_limit_ns))
         atomicOr(&g_bwd_fault, 2u);
     } else {
       cp_async_wait<A::kStages - 2>();
@@ -894,8 +897,8 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-static bool encode_as(CUtensorMap* m, CUtensorMapDataType ty, const void* base, cuuint32_t rank,
-                      const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box) {
+bool encode_tiled(CUtensorMap* m, CUtensorMapDataType ty, const void* base, cuuint32_t rank,
+                  const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box) {
   const EncodeTiledFn f = encode_fn();
   if (!f) return false;
   const cuuint32_t es[4] = {1, 1, 1, 1};
@@ -906,7 +909,7 @@ static bool encode_as(CUtensorMap* m, CUtensorMapDataType ty, const void* base, 
 
 static bool encode_f32(CUtensorMap* m, const void* base, cuuint32_t rank, const cuuint64_t* dims,
                        const cuuint64_t* strides, const cuuint32_t* box) {
-  return encode_as(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, rank, dims, strides, box);
+  return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, rank, dims, strides, box);
 }
 
 // The maps of one call; the last call's maps are kept and reused when nothing changed.
@@ -942,14 +945,14 @@ static bool make_maps(const Plan& plan, const BwdParams& p, BwdMaps* m) {
   const cuuint32_t bCK[4] = {(cuuint32_t)NP, (cuuint32_t)S::DC, 1, 1};
   BwdMaps mm;
   memset(&mm, 0, sizeof(mm));
-  const bool ok = encode_as(&mm.delta, io, p.delta, 3, dTD, sTD, bTD) &&
-                  encode_as(&mm.u, io, p.u, 3, dTD, sTD, bTD) &&
-                  encode_as(&mm.gate, io, p.gate, 3, dTD, sTD, bTD) &&
-                  encode_as(&mm.dy, io, p.dy, 3, dTD, sTD, bTD) &&
+  const bool ok = encode_tiled(&mm.delta, io, p.delta, 3, dTD, sTD, bTD) &&
+                  encode_tiled(&mm.u, io, p.u, 3, dTD, sTD, bTD) &&
+                  encode_tiled(&mm.gate, io, p.gate, 3, dTD, sTD, bTD) &&
+                  encode_tiled(&mm.dy, io, p.dy, 3, dTD, sTD, bTD) &&
                   // the fused call has no stored y: its map is never used
-                  encode_as(&mm.y, io, p.y_ck ? p.y_ck : p.delta, 3, dTD, sTD, bTD) &&
-                  encode_as(&mm.B, io, p.B, 3, dTN, sTN, bTN) &&
-                  encode_as(&mm.C, io, p.C, 3, dTN, sTN, bTN) &&
+                  encode_tiled(&mm.y, io, p.y_ck ? p.y_ck : p.delta, 3, dTD, sTD, bTD) &&
+                  encode_tiled(&mm.B, io, p.B, 3, dTN, sTN, bTN) &&
+                  encode_tiled(&mm.C, io, p.C, 3, dTN, sTN, bTN) &&
                   encode_f32(&mm.ckpt, p.ckpt, 4, dCK, sCK, bCK);
   if (!ok) return false;
   *m = mm;

@@ -332,17 +332,19 @@ __device__ __forceinline__ uint64_t global_ns() {
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
   return t;
 }
-// Waits for the barrier phase with the given parity, for one second at most. Returns false
-// when the wait gave up (the caller records the fault; the kernel still runs to its end).
+// Waits for the barrier phase with the given parity, for limit_ns at most (one second unless a
+// caller asks for less). Returns false when the wait gave up (the caller records the fault;
+// the kernel still runs to its end).
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (;;) {
 #pragma unroll 1
     for (int k = 0; k < 64; ++k)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > kWaitLimitNs) return false;
+    if (global_ns() - t0 > limit_ns) return false;
   }
 }
 // Tiled TMA loads global -> shared; completion is counted on the barrier in bytes. Elements

@@ -78,6 +78,10 @@ struct Plan {
   size_t off_bagg_L = 0, off_bagg_sd = 0, scratch_elems = 0;
 };
 
+// Records a CUDA error as the one mamba_scan_strerror(MAMBA_ERR_CUDA) reports, and returns
+// MAMBA_ERR_CUDA (for entry points outside mamba_scan_abi.cu).
+int record_cuda_error(cudaError_t e);
+
 // Returns false when the sizes are outside what the kernels support.
 bool make_plan(int64_t batch, int64_t T, int64_t Di, int64_t N, Plan* plan);
 
@@ -109,13 +113,22 @@ struct BwdParams {
                 // unused); null otherwise
   int io_bf16;  // fused call only: delta, u, B, C, gate, dy, out, d_delta, d_u, d_B, d_C,
                 // d_gate point at bf16 data (A_log, D, d_A_log, d_D stay fp32)
+  // Failure-path test only (mamba_scan_bwd_test_timeout): the tensor-memory backward issues no
+  // copy for the last chunk of each CTA, so the wait for it runs out after wait_limit_ns.
+  int test_skip_last_copy;
+  unsigned long long wait_limit_ns;   // bound of every copy wait of the backward's kernels
 };
+
+// Encodes a tiled tensor map (no interleave, no swizzle, zero fill outside the tensor) through
+// the driver entry point; false when the driver or the arguments refuse it.
+bool encode_tiled(CUtensorMap* m, CUtensorMapDataType ty, const void* base, cuuint32_t rank,
+                  const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box);
 
 // TMA descriptors of the tensor-memory backward, encoded on the host for each call:
 // delta, u, gate, dy, y as [batch][T][d_inner] with boxes of 16 steps x DC channels; B, C as
 // [batch][T][d_state] with boxes of 16 steps x NP states; the checkpoints as
 // [batch][chunk][d_inner][d_state] with boxes of DC channels x NP states.
-struct alignas(64) BwdMaps {
+struct BwdMaps {   // each CUtensorMap carries its own 64-byte alignment
   CUtensorMap delta, u, gate, dy, y, B, C, ckpt;
 };
 

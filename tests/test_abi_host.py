@@ -136,6 +136,20 @@ def test_bwd_validation_codes(ms):
     assert lib.mamba_scan_bwd(*_bwd_args(dims=(1, 40, 64, 100))) == ms.MAMBA_ERR_UNSUPPORTED
 
 
+@needs_no_gpu
+def test_bwd_test_timeout_takes_only_the_tensor_copy_path(ms):
+    """The failure-path test entry point validates like mamba_scan_bwd and refuses sizes that do
+    not run the tensor-memory backward with tensor copies, before anything is launched."""
+    lib = ms.raw_library()
+    f = lib.mamba_scan_bwd_test_timeout
+    assert f(*_bwd_args(dims=(1, 40, 64, 8))) == ms.MAMBA_ERR_UNSUPPORTED    # d_state <= 8
+    assert f(*_bwd_args(dims=(1, 40, 66, 16))) == ms.MAMBA_ERR_UNSUPPORTED   # d_inner % 4
+    assert f(*_bwd_args(dims=(1, 16, 64, 16))) == ms.MAMBA_ERR_UNSUPPORTED   # one chunk
+    assert f(*_bwd_args(dims=(1, 40, 64, 100))) == ms.MAMBA_ERR_UNSUPPORTED
+    assert f(*_bwd_args(dy=None)) == ms.MAMBA_ERR_INVALID_ARG
+    assert f(*_bwd_args(scratch_bytes=1024)) == ms.MAMBA_ERR_WORKSPACE
+
+
 def _fused_args(**over):
     b, T, Di, N = over.pop("dims", (2, 40, 64, 16))
     big = 1 << 32

@@ -5,10 +5,13 @@ all device memory is one; a latency-critical loop that forbids cudaMalloc is ano
 the library takes the backward's scratch from a static 64 MiB device array instead of from the
 caller.
 
-The GPU test calls the entry point through the C ABI, twice in a row on the same inputs. Each
-time, it checks the output against mamba_scan_bwd (which takes caller-owned scratch), within
-the tolerance the parity tests use. The file is named so that pytest collects it last. It
-passes when run alone in a fresh process and when run after the other tests.
+The GPU test calls the entry point through the C ABI twice in a row, on two different input
+sets A and B of the same shape. The first call (A) is checked against mamba_scan_bwd within
+the tolerance the parity tests use. The second (B) runs with the array still holding A's
+partial sums, and must equal mamba_scan_bwd on B with freshly NaN-filled caller scratch bit for
+bit: a read of a scratch word the call did not write would show up there, either as A's stale
+value or as NaN. The file is named so that pytest collects it last. It passes when run alone in
+a fresh process and when run after the other tests.
 """
 import ctypes
 
@@ -29,10 +32,39 @@ def _gpu():
         return False
 
 
+def _forward_and_reference(ms, xd):
+    """Forward, then the regular backward with freshly NaN-filled caller scratch."""
+    import torch
+    bufs = ms.alloc_like_outputs(xd["delta"], xd["B"], xd["A_log"], xd["D"])
+    bufs["scratch"].fill_(0xFF)
+    ms.forward_backward(xd, bufs)
+    torch.cuda.synchronize()
+    return bufs, {k: bufs[k].double().cpu().numpy() for k in GRADS}
+
+
+def _noalloc(ms, xd, bufs, shape):
+    import torch
+    b, T, Di, N = shape
+    lib = ms.raw_library()
+    stream = torch.cuda.current_stream().cuda_stream
+    ck = bufs["ckpt"]
+    out = {k: torch.full_like(bufs[k], float("nan")) for k in GRADS}
+    rc = lib.mamba_scan_bwd_noalloc(
+        xd["delta"].data_ptr(), xd["u"].data_ptr(), xd["B"].data_ptr(), xd["C"].data_ptr(),
+        xd["gate"].data_ptr(), xd["A_log"].data_ptr(), xd["D"].data_ptr(), xd["dy"].data_ptr(),
+        ck.data_ptr() if ck is not None else None, ck.numel() if ck is not None else 0,
+        out["d_delta"].data_ptr(), out["d_u"].data_ptr(), out["d_B"].data_ptr(),
+        out["d_C"].data_ptr(), out["d_A_log"].data_ptr(), out["d_D"].data_ptr(),
+        out["d_gate"].data_ptr(), b, T, Di, N, ctypes.c_void_p(stream))
+    assert rc == ms.MAMBA_OK, ms.mamba_scan_strerror(rc)
+    torch.cuda.synchronize()
+    return {k: out[k].double().cpu().numpy() for k in GRADS}
+
+
 @pytest.mark.gpu
 @pytest.mark.parametrize("shape", [(8, 1024, 1536, 16), (2, 37, 50, 5), (1, 300, 40, 64)],
                          ids=["mamba130m", "ragged", "dstate64"])
-def test_noalloc_bwd_matches_bwd_on_two_calls(shape):
+def test_noalloc_bwd_two_calls_on_different_inputs(shape):
     if not _gpu():
         pytest.skip("no CUDA device")
     import torch
@@ -41,32 +73,20 @@ def test_noalloc_bwd_matches_bwd_on_two_calls(shape):
     b, T, Di, N = shape
     need = ms.mamba_scan_scratch_bytes(b, T, Di, N)
     assert 0 < need <= ms.MAMBA_SCAN_NOALLOC_SCRATCH_BYTES
-    x = synth.random_inputs(b, T, Di, N, seed=11)
-    xd = {k: torch.from_numpy(v).to("cuda:0") for k, v in x.items()}
-    bufs = ms.alloc_like_outputs(xd["delta"], xd["B"], xd["A_log"], xd["D"])
-    ms.forward_backward(xd, bufs)          # forward + the regular backward (caller scratch)
-    torch.cuda.synchronize()
-    ref = {k: bufs[k].double().cpu().numpy() for k in GRADS}
+    xa = {k: torch.from_numpy(v).to("cuda:0")
+          for k, v in synth.random_inputs(b, T, Di, N, seed=11).items()}
+    xb = {k: torch.from_numpy(v).to("cuda:0")
+          for k, v in synth.random_inputs(b, T, Di, N, seed=12).items()}
 
-    lib = ms.raw_library()
-    stream = torch.cuda.current_stream().cuda_stream
-    ck = bufs["ckpt"]
-    ck_ptr = ck.data_ptr() if ck is not None else None
-    ck_bytes = ck.numel() if ck is not None else 0
-    for call in range(2):
-        out = {k: torch.full_like(bufs[k], float("nan")) for k in GRADS}
-        rc = lib.mamba_scan_bwd_noalloc(
-            xd["delta"].data_ptr(), xd["u"].data_ptr(), xd["B"].data_ptr(), xd["C"].data_ptr(),
-            xd["gate"].data_ptr(), xd["A_log"].data_ptr(), xd["D"].data_ptr(),
-            xd["dy"].data_ptr(), ck_ptr, ck_bytes,
-            out["d_delta"].data_ptr(), out["d_u"].data_ptr(), out["d_B"].data_ptr(),
-            out["d_C"].data_ptr(), out["d_A_log"].data_ptr(), out["d_D"].data_ptr(),
-            out["d_gate"].data_ptr(), b, T, Di, N, ctypes.c_void_p(stream))
-        assert rc == ms.MAMBA_OK, ms.mamba_scan_strerror(rc)
-        torch.cuda.synchronize()
-        got = {k: out[k].double().cpu().numpy() for k in GRADS}
-        errs = rel_errors(got, ref, GRADS)
-        assert all(e <= TOL for e in errs.values()), (call, errs)
+    bufs_a, ref_a = _forward_and_reference(ms, xa)
+    got_a = _noalloc(ms, xa, bufs_a, shape)                    # call 1: input set A
+    errs = rel_errors(got_a, ref_a, GRADS)
+    assert all(e <= TOL for e in errs.values()), ("A", errs)
+
+    bufs_b, ref_b = _forward_and_reference(ms, xb)
+    got_b = _noalloc(ms, xb, bufs_b, shape)                    # call 2: B, over A's scratch
+    for k in GRADS:
+        assert np.array_equal(got_b[k], ref_b[k]), f"B: {k} differs from mamba_scan_bwd"
 
 
 def test_noalloc_rejects_sizes_beyond_the_static_scratch():
