@@ -416,6 +416,8 @@ def run_gpu(args):
         pg = dist
     peaks = read_peaks()
     w = synth.BY_NAME[args.workload]
+    if args.seq_len:   # a shorter cut of the workload (same recipe), e.g. for counter captures
+        w = w.resized(T=args.seq_len, name=f"{w.name}-T{args.seq_len}")
     x_np = synth.make_inputs(w, seed=0)
     x = {k: torch.from_numpy(v).to(dev) for k, v in x_np.items()}
     bufs = ms.alloc_like_outputs(x["delta"], x["B"], x["A_log"], x["D"])
@@ -656,6 +658,8 @@ def main():
                     help="skip timing the variants (softplus, fused, bf16, conv1d)")
     ap.add_argument("--no-per-workload", action="store_true",
                     help="time the headline workload only")
+    ap.add_argument("--seq-len", type=int, default=0,
+                    help="run the workload at this T instead of its own (same value recipe)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
     if args.warmup < 3:

@@ -172,6 +172,10 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
   using S = BwdTmemShape<NP>;
   constexpr int G = S::G, LG = S::LG, DW = S::DW, DC = S::DC, TILE = S::TILE;
   constexpr int NTH = kWarps * 32;
+  // Without the intra-pair state swap (fewer than 4 channel lanes) and with fp32 tiles, the
+  // lanes read their B and C pairs straight from the stage and splat them in registers: half
+  // the shared-memory bytes of a duplicated {B, B} copy, and no copy to write.
+  constexpr bool DBC = !S::SWAP && !BF;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ uint32_t s_tmem;
   float* smem = reinterpret_cast<float*>(
@@ -325,6 +329,11 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
     const float* s_B = st + 5 * TILE;
     const float* s_C = s_B + kChunk * NP;
     const float* s_h0 = s_C + kChunk * NP;
+    // (DBC) this lane's state pairs pp = 0, 1 of B and C in the stage: states n0 + 2*(pp ^ m1)
+    const float2* qB[2] = {reinterpret_cast<const float2*>(s_B + n0 + 2 * m1),
+                           reinterpret_cast<const float2*>(s_B + n0 + 2 * (1 - m1))};
+    const float2* qC[2] = {reinterpret_cast<const float2*>(s_C + n0 + 2 * m1),
+                           reinterpret_cast<const float2*>(s_C + n0 + 2 * (1 - m1))};
     float* red = S::RED_ALIAS ? st + 4 * TILE : red_fixed;
     float* const red_lane = red + warp * kChunk * 2 * NP + (S::KIND ? mk * NP : 0) + n_res;
     const int t0 = c * kChunk;
@@ -407,7 +416,7 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
       }
     };
     if constexpr (!FY) gating();
-    for (int e = threadIdx.x; e < kChunk * NP; e += NTH) {
+    for (int e = threadIdx.x; e < (DBC ? 0 : kChunk * NP); e += NTH) {
       float bv, cv;
       if constexpr (BF) {   // bf16 B and C in the first halves of their slots
         bv = __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(s_B)[e] << 16);
@@ -461,9 +470,15 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
       }
 #pragma unroll
       for (int pp = 0; pp < 2; ++pp) {
-        const float4 v = pB[pp][i * NP / 2];
-        B2[2 * pp] = make_float2(v.x, v.y);
-        B2[2 * pp + 1] = make_float2(v.z, v.w);
+        if constexpr (DBC) {
+          const float2 v = qB[pp][i * NP / 2];
+          B2[2 * pp] = splat2(v.x);
+          B2[2 * pp + 1] = splat2(v.y);
+        } else {
+          const float4 v = pB[pp][i * NP / 2];
+          B2[2 * pp] = make_float2(v.x, v.y);
+          B2[2 * pp + 1] = make_float2(v.z, v.w);
+        }
       }
 #pragma unroll
       for (int q = 0; q < 2; ++q)
@@ -476,9 +491,15 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
         float2 C2[4];
 #pragma unroll
         for (int pp = 0; pp < 2; ++pp) {
-          const float4 v = pC[pp][i * NP / 2];
-          C2[2 * pp] = make_float2(v.x, v.y);
-          C2[2 * pp + 1] = make_float2(v.z, v.w);
+          if constexpr (DBC) {
+            const float2 v = qC[pp][i * NP / 2];
+            C2[2 * pp] = splat2(v.x);
+            C2[2 * pp + 1] = splat2(v.y);
+          } else {
+            const float4 v = pC[pp][i * NP / 2];
+            C2[2 * pp] = make_float2(v.x, v.y);
+            C2[2 * pp + 1] = make_float2(v.z, v.w);
+          }
         }
         float2 ya[2];
 #pragma unroll
@@ -527,12 +548,21 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
       }
 #pragma unroll
       for (int pp = 0; pp < 2; ++pp) {
-        const float4 vb = pB[pp][i * NP / 2];
-        const float4 vc = pC[pp][i * NP / 2];
-        B2[2 * pp] = make_float2(vb.x, vb.y);
-        B2[2 * pp + 1] = make_float2(vb.z, vb.w);
-        C2[2 * pp] = make_float2(vc.x, vc.y);
-        C2[2 * pp + 1] = make_float2(vc.z, vc.w);
+        if constexpr (DBC) {
+          const float2 vb = qB[pp][i * NP / 2];
+          const float2 vc = qC[pp][i * NP / 2];
+          B2[2 * pp] = splat2(vb.x);
+          B2[2 * pp + 1] = splat2(vb.y);
+          C2[2 * pp] = splat2(vc.x);
+          C2[2 * pp + 1] = splat2(vc.y);
+        } else {
+          const float4 vb = pB[pp][i * NP / 2];
+          const float4 vc = pC[pp][i * NP / 2];
+          B2[2 * pp] = make_float2(vb.x, vb.y);
+          B2[2 * pp + 1] = make_float2(vb.z, vb.w);
+          C2[2 * pp] = make_float2(vc.x, vc.y);
+          C2[2 * pp + 1] = make_float2(vc.z, vc.w);
+        }
       }
       tmem_wait_ld(reinterpret_cast<float2(&)[8]>(hp));
       float2 sa2[2], sb2[2], xb2[4], xc2[4];
@@ -683,8 +713,8 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
 
 // Segment pre-pass with the main kernel's channel blocks (the same aggregates as
 // scan_bwd_agg_kernel: L = sum_t exp(A * sum_{s<=t} delta_s) * d_y_t * C_t[n] and the sum of
-// delta over one sub-segment). A thread owns 4 channels x 4 states, channel-packed, so no
-// value needs a splat and nothing crosses lanes.
+// delta over one sub-segment). A thread owns 4 channels x 4 states, channel-packed; its four
+// states of C come as one plain quad and are splatted in registers, and nothing crosses lanes.
 template <int NP>
 struct BwdAgg4Shape {
   using S = BwdTmemShape<NP>;
@@ -692,8 +722,7 @@ struct BwdAgg4Shape {
   // per stage: delta, gate (-> d_y), dy [kChunk][DC]; C [kChunk][NP]
   static constexpr int kStageFloats = 3 * S::TILE + kChunk * NP;
   static constexpr uint32_t kStageBytes = kStageFloats * sizeof(float);
-  static constexpr int kDupFloats = kChunk * NP * 2;   // {C, C} of the current chunk
-  static constexpr size_t kDataFloats = (size_t)kStages * kStageFloats + kDupFloats;
+  static constexpr size_t kDataFloats = (size_t)kStages * kStageFloats;
   static constexpr size_t kSmemBytes = kDataFloats * sizeof(float) + 8 * kStages + 128;
   static_assert(kStageBytes % 128 == 0, "TMA destinations must stay 128-byte aligned");
 };
@@ -778,9 +807,6 @@ scan_bwd_agg4_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
       L[q][s] = make_float2(0.f, 0.f);
     }
 
-  float* dupC = smem + A::kStages * A::kStageFloats;
-  const float4* pC[2] = {reinterpret_cast<const float4*>(dupC + 2 * n0),
-                         reinterpret_cast<const float4*>(dupC + 2 * n0 + 4)};
   for (int c = c_begin; c < c_end; ++c) {
     const int it = c - c_begin;
     if constexpr (TMA) {
@@ -828,13 +854,10 @@ scan_bwd_agg4_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
       }
     }
     if (p.softplus) softplus_tile<DC, NTH>(st, T - c * kChunk, Di - dblk0);   // raw -> delta
-    for (int e = threadIdx.x; e < kChunk * NP; e += NTH) {
-      const float cv = s_C[e];
-      *reinterpret_cast<float2*>(dupC + 2 * e) = make_float2(cv, cv);
-    }
     __syncthreads();
     const float4* pdl = reinterpret_cast<const float4*>(s_dl + cl);
     const float4* pdy = reinterpret_cast<const float4*>(s_g + cl);
+    const float4* pcq = reinterpret_cast<const float4*>(s_C + n0);
 #pragma unroll
     for (int i = 0; i < kChunk; ++i) {
       const float4 dl = pdl[i * DC / 4];
@@ -842,9 +865,10 @@ scan_bwd_agg4_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
       P2[0] = __fadd2_rn(P2[0], make_float2(dl.x, dl.y));
       P2[1] = __fadd2_rn(P2[1], make_float2(dl.z, dl.w));
       const float2 dy2[2] = {make_float2(dy.x, dy.y), make_float2(dy.z, dy.w)};
-      const float4 c01 = pC[0][i * NP / 2], c23 = pC[1][i * NP / 2];
-      const float2 C2[4] = {make_float2(c01.x, c01.y), make_float2(c01.z, c01.w),
-                            make_float2(c23.x, c23.y), make_float2(c23.z, c23.w)};
+      // the thread's four states of C, splatted in registers (loading a duplicated {C, C}
+      // copy instead doubles the shared-memory bytes of a path bound by them)
+      const float4 cq = pcq[i * NP / 4];
+      const float2 C2[4] = {splat2(cq.x), splat2(cq.y), splat2(cq.z), splat2(cq.w)};
 #pragma unroll
       for (int q = 0; q < 2; ++q)
 #pragma unroll
