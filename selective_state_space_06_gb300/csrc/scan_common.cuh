@@ -118,29 +118,69 @@ __device__ __forceinline__ void step_fence() { asm volatile("" ::: "memory"); }
 // NPR float2 pairs of consecutive states from shared memory (8- or 16-byte aligned).
 template <int NPR>
 __device__ __forceinline__ void lds_pairs(const float* p, float2 (&out)[NPR]) {
-  static_assert(NPR == 1 || NPR == 2, "2 or 4 states per thread");
-  if constexpr (NPR == 2) {
-    const float4 v = lds4(p);
-    out[0] = make_float2(v.x, v.y);
-    out[1] = make_float2(v.z, v.w);
-  } else {
+  static_assert(NPR == 1 || NPR == 2 || NPR == 4, "2, 4 or 8 states per thread");
+  if constexpr (NPR == 1) {
     out[0] = lds2(p);
+  } else {
+#pragma unroll
+    for (int k = 0; k < NPR / 2; ++k) {
+      const float4 v = lds4(p + 4 * k);
+      out[2 * k] = make_float2(v.x, v.y);
+      out[2 * k + 1] = make_float2(v.z, v.w);
+    }
   }
 }
-// NPR float2 pairs to global memory with one vector store.
+// NPR float2 pairs to global memory with 16-byte vector stores (one 8-byte store for NPR 1).
 template <int NPR>
 __device__ __forceinline__ void st_pairs(float* p, const float2 (&v)[NPR]) {
-  if constexpr (NPR == 2) *reinterpret_cast<float4*>(p) = make_float4(v[0].x, v[0].y, v[1].x, v[1].y);
-  else *reinterpret_cast<float2*>(p) = v[0];
+  if constexpr (NPR == 1) {
+    *reinterpret_cast<float2*>(p) = v[0];
+  } else {
+#pragma unroll
+    for (int k = 0; k < NPR / 2; ++k)
+      *reinterpret_cast<float4*>(p + 4 * k) =
+          make_float4(v[2 * k].x, v[2 * k].y, v[2 * k + 1].x, v[2 * k + 1].y);
+  }
+}
+// The same for the states n0 .. n0+2*NPR-1 of a row of N states (N % 4 == 0, n0 % 4 == 0):
+// only the groups of four inside the row are stored; loads give zeros past it.
+template <int NPR>
+__device__ __forceinline__ void st_pairs_row(float* row, int n0, int N, const float2 (&v)[NPR]) {
+  if constexpr (NPR == 1) {
+    if (n0 < N) *reinterpret_cast<float2*>(row + n0) = v[0];
+  } else {
+#pragma unroll
+    for (int k = 0; k < NPR / 2; ++k)
+      if (n0 + 4 * k < N)
+        *reinterpret_cast<float4*>(row + n0 + 4 * k) =
+            make_float4(v[2 * k].x, v[2 * k].y, v[2 * k + 1].x, v[2 * k + 1].y);
+  }
+}
+template <int NPR>
+__device__ __forceinline__ void ld_pairs_row(const float* row, int n0, int N, float2 (&out)[NPR]) {
+  if constexpr (NPR == 1) {
+    out[0] = n0 < N ? *reinterpret_cast<const float2*>(row + n0) : make_float2(0.f, 0.f);
+  } else {
+#pragma unroll
+    for (int k = 0; k < NPR / 2; ++k) {
+      const float4 v = n0 + 4 * k < N ? *reinterpret_cast<const float4*>(row + n0 + 4 * k)
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+      out[2 * k] = make_float2(v.x, v.y);
+      out[2 * k + 1] = make_float2(v.z, v.w);
+    }
+  }
 }
 template <int NPR>
 __device__ __forceinline__ void ld_pairs(const float* p, float2 (&out)[NPR]) {
-  if constexpr (NPR == 2) {
-    const float4 v = *reinterpret_cast<const float4*>(p);
-    out[0] = make_float2(v.x, v.y);
-    out[1] = make_float2(v.z, v.w);
-  } else {
+  if constexpr (NPR == 1) {
     out[0] = *reinterpret_cast<const float2*>(p);
+  } else {
+#pragma unroll
+    for (int k = 0; k < NPR / 2; ++k) {
+      const float4 v = *reinterpret_cast<const float4*>(p + 4 * k);
+      out[2 * k] = make_float2(v.x, v.y);
+      out[2 * k + 1] = make_float2(v.z, v.w);
+    }
   }
 }
 

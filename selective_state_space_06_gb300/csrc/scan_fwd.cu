@@ -240,7 +240,7 @@ scan_fwd_agg_kernel(const FwdParams p) {
           const size_t row = ((size_t)b * p.nseg + seg) * Di + d;
           if (ng == 0) p.agg_sd[row] = sd[j];
           if constexpr (VEC) {
-            if (n0 < N) st_pairs<NPR>(p.agg_h + row * N + n0, h[j]);   // N % 4 == 0 here
+            st_pairs_row<NPR>(p.agg_h + row * N, n0, N, h[j]);   // N % 4 == 0 here
           } else {
 #pragma unroll
             for (int k = 0; k < NPT; ++k)
@@ -327,12 +327,7 @@ scan_fwd_kernel(const FwdParams p) {
       const float sd = p.agg_sd[row];
       float2 hl[NPR];
       if constexpr (VEC) {
-        if (n0 < N) {
-          ld_pairs<NPR>(p.agg_h + row * N + n0, hl);
-        } else {
-#pragma unroll
-          for (int q = 0; q < NPR; ++q) hl[q] = make_float2(0.f, 0.f);
-        }
+        ld_pairs_row<NPR>(p.agg_h + row * N, n0, N, hl);
       } else {
 #pragma unroll
         for (int q = 0; q < NPR; ++q) {
@@ -452,7 +447,7 @@ scan_fwd_kernel(const FwdParams p) {
         const int d = d0 + j;
         if (d >= Di) continue;
         if constexpr (VEC) {
-          if (n0 < N) st_pairs<NPR>(ck + (size_t)d * N + n0, h[j]);
+          st_pairs_row<NPR>(ck + (size_t)d * N, n0, N, h[j]);
         } else {
 #pragma unroll
           for (int k = 0; k < NPT; ++k)
