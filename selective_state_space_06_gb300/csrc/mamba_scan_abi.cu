@@ -68,7 +68,8 @@ bool make_plan(int64_t batch, int64_t T, int64_t Di, int64_t N, Plan* pl) {
     split(q, best_want);
     return q;
   };
-  p.fwd = by_target(pass(states_per_thread_fwd(p.NP), kDPT, kFwdWarps), target_units_fwd(p.NP));
+  p.fwd = by_target(pass(states_per_thread_fwd(p.NP), fwd_channels_per_thread(p.NP), kFwdWarps),
+                    target_units_fwd(p.NP));
   if (p.NP >= kTmemMinNP)
     p.bwd = by_waves(pass(4, kTmemDPT), kTmemSlots);
   else

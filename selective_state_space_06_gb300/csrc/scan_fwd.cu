@@ -9,10 +9,10 @@
 //
 // Mapping. grid = (ceil(d_inner / DC), batch). A CTA owns one batch row b and DC consecutive
 // channels, and walks the whole time axis for them in chunks of kChunk steps.
-//   lane = dg * G + ng :  ng picks the states [NPT*ng, NPT*ng+NPT), and dg picks the channel
-//                         pair [2*dg, 2*dg+2) of the warp's 2*(32/G) channels.
-// A thread keeps 2 channels x NPT states in registers as float2 pairs and updates them with
-// packed fp32x2 FMAs.
+//   lane = dg * G + ng :  ng picks the states [NPT*ng, NPT*ng+NPT), and dg picks the DPT
+//                         channels [DPT*dg, DPT*dg+DPT) of the warp's DPT*(32/G) channels.
+// A thread keeps DPT channels (2, or 4 at d_state 64) x NPT states in registers as float2 pairs
+// of states and updates them with packed fp32x2 FMAs.
 //
 // Staging. Each chunk's tiles (delta, u and gate [kChunk][DC]; B and C [kChunk][NP]) go
 // global -> shared with cp.async, STAGES chunks ahead of the compute. Rows past T and channels
@@ -20,8 +20,8 @@
 // so the control flow needs no tail special cases.
 //
 // y = sum_n C*h. In-thread FMAs first, then a butterfly reduce-scatter over the G state
-// lanes, batched over P = G/2 steps. It leaves each lane the complete y of exactly one
-// (step, channel). That lane then applies D*u and the SiLU gate and stores out. So no
+// lanes, batched over P = G/DPT steps. It leaves each lane the complete y of one (step,
+// channel) (two when G < DPT). That lane then applies D*u and the SiLU gate and stores out. So no
 // sigmoid is computed twice.
 //
 // Every kChunk steps the state goes to the checkpoint buffer [batch][chunk][d][n] (the state
@@ -32,14 +32,32 @@ namespace mscan {
 
 constexpr int kFwdStages = 4;
 
+// The DPT consecutive channels of a thread from one staged row (8- or 16-byte aligned).
+template <int DPT>
+__device__ __forceinline__ void lds_chan(const float* p, float (&v)[DPT]) {
+  static_assert(DPT == 2 || DPT == 4, "2 or 4 channels per thread");
+  if constexpr (DPT == 2) {
+    const float2 t = lds2(p);
+    v[0] = t.x;
+    v[1] = t.y;
+  } else {
+    const float4 t = lds4(p);
+    v[0] = t.x;
+    v[1] = t.y;
+    v[2] = t.z;
+    v[3] = t.w;
+  }
+}
+
 template <int NP>
 struct FwdShape {
   static constexpr int NPT = states_per_thread_fwd(NP);    // states per thread
   static constexpr int NPR = NPT / 2;                  // float2 pairs of states per thread
+  static constexpr int DPT = fwd_channels_per_thread(NP);   // channels per thread
   static constexpr int G = NP / NPT;                   // lanes per channel group
-  static constexpr int DW = (32 / G) * kDPT;           // channels per warp
+  static constexpr int DW = (32 / G) * DPT;            // channels per warp
   static constexpr int DC = kFwdWarps * DW;            // channels per CTA
-  static constexpr int P = G >= 2 ? G / 2 : 1;         // steps per output group
+  static constexpr int P = G >= DPT ? G / DPT : 1;     // steps per output group
   static constexpr int kStageFloats = kChunk * (3 * DC + 2 * NP);
   static constexpr size_t kSmemBytes = (size_t)kFwdStages * kStageFloats * sizeof(float);
 };
@@ -129,6 +147,7 @@ scan_fwd_agg_kernel(const FwdParams p) {
   using S = FwdShape<NP>;
   using A = FwdAggShape<NP>;
   constexpr int G = S::G, DW = S::DW, NPT = S::NPT, NPR = S::NPR, DC = A::DC, NTH = A::NTH;
+  constexpr int DPT = S::DPT;
   extern __shared__ __align__(16) float smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ng = lane % G, dg = lane / G;
@@ -136,7 +155,7 @@ scan_fwd_agg_kernel(const FwdParams p) {
   const int nblk_a = (p.Di + DC - 1) / DC;
   const int blk = blockIdx.x % nblk_a, grp = blockIdx.x / nblk_a;
   const int dblk0 = blk * DC;
-  const int cl = warp * DW + dg * kDPT;
+  const int cl = warp * DW + dg * DPT;
   const int d0 = dblk0 + cl;
   const int n0 = ng * NPT;
   const int Di = p.Di, N = p.N, T = p.T;
@@ -146,12 +165,13 @@ scan_fwd_agg_kernel(const FwdParams p) {
   const int c_end = min(p.nchunks, seg_hi * p.seg_chunks);
   const size_t row0 = (size_t)b * T;
 
-  float2 a2[kDPT][NPR], h[kDPT][NPR];
-  float sd[kDPT] = {0.f, 0.f};
+  float2 a2[DPT][NPR], h[DPT][NPR];
+  float sd[DPT];
 #pragma unroll
-  for (int j = 0; j < kDPT; ++j) {
+  for (int j = 0; j < DPT; ++j) {
     const int d = d0 + j;
     const bool dv = d < Di;
+    sd[j] = 0.f;
     float t4[NPT];
 #pragma unroll
     for (int k = 0; k < NPT; ++k) {
@@ -214,14 +234,15 @@ scan_fwd_agg_kernel(const FwdParams p) {
     const float* s_B = st + 2 * kChunk * DC;
 #pragma unroll
     for (int i = 0; i < kChunk; ++i) {
-      const float2 dlv = lds2(s_dl + i * DC + cl);
-      const float2 uv = lds2(s_u + i * DC + cl);
+      float dlv[DPT], uv[DPT];
+      lds_chan<DPT>(s_dl + i * DC + cl, dlv);
+      lds_chan<DPT>(s_u + i * DC + cl, uv);
       float2 Bp[NPR];
       lds_pairs<NPR>(s_B + i * NP + n0, Bp);
 #pragma unroll
-      for (int j = 0; j < kDPT; ++j) {
-        const float dl = j ? dlv.y : dlv.x;
-        const float uu = j ? uv.y : uv.x;
+      for (int j = 0; j < DPT; ++j) {
+        const float dl = dlv[j];
+        const float uu = uv[j];
         sd[j] += dl;
         const float2 dl2 = splat2(dl), du2 = splat2(dl * uu);
 #pragma unroll
@@ -234,7 +255,7 @@ scan_fwd_agg_kernel(const FwdParams p) {
     if ((c + 1) % p.seg_chunks == 0) {   // the last chunk of a segment: emit, then restart
       const int seg = c / p.seg_chunks;
 #pragma unroll
-      for (int j = 0; j < kDPT; ++j) {
+      for (int j = 0; j < DPT; ++j) {
         const int d = d0 + j;
         if (d < Di) {
           const size_t row = ((size_t)b * p.nseg + seg) * Di + d;
@@ -267,6 +288,7 @@ scan_fwd_kernel(const FwdParams p) {
   static_assert(!BF || ST, "bf16 input is taken by the states-only forward");
   using S = FwdShape<NP>;
   constexpr int G = S::G, DW = S::DW, DC = S::DC, P = S::P, NPT = S::NPT, NPR = S::NPR;
+  constexpr int DPT = S::DPT;
   extern __shared__ __align__(16) float smem[];
   pdl_wait();      // the previous kernel's writes (inputs, workspace) are visible
   pdl_release();   // one wave: the next kernel may take the room this one leaves
@@ -276,17 +298,17 @@ scan_fwd_kernel(const FwdParams p) {
   const int b = blockIdx.y;
   const int blk = blockIdx.x % p.nblk, seg = blockIdx.x / p.nblk;
   const int dblk0 = blk * DC;
-  const int cl = warp * DW + dg * kDPT;   // first channel of this thread inside the CTA tile
+  const int cl = warp * DW + dg * DPT;    // first channel of this thread inside the CTA tile
   const int d0 = dblk0 + cl;
   const int n0 = ng * NPT;
   const int Di = p.Di, N = p.N, T = p.T;
   const int c_begin = seg * p.seg_chunks;
   const int c_end = min(p.nchunks, c_begin + p.seg_chunks);
 
-  float2 a2[kDPT][NPR], h[kDPT][NPR];
-  float Dd[kDPT];
+  float2 a2[DPT][NPR], h[DPT][NPR];
+  float Dd[DPT];
 #pragma unroll
-  for (int j = 0; j < kDPT; ++j) {
+  for (int j = 0; j < DPT; ++j) {
     const int d = d0 + j;
     const bool dv = d < Di;
     Dd[j] = dv ? p.D[d] : 0.f;
@@ -303,7 +325,7 @@ scan_fwd_kernel(const FwdParams p) {
     }
   }
 
-  using RSy = ReduceScatter<2 * P, G / 2, 1>;
+  using RSy = ReduceScatter<DPT * P, G / 2, 1>;
   const int ybase = RSy::base(lane);
   constexpr int kY = RSy::kept();
   const size_t rowb = (size_t)b * T;
@@ -320,7 +342,7 @@ scan_fwd_kernel(const FwdParams p) {
   // h <- exp(A * sum(delta)) * h + (segment end state from zero)
   for (int sp = 0; sp < seg; ++sp) {
 #pragma unroll
-    for (int j = 0; j < kDPT; ++j) {
+    for (int j = 0; j < DPT; ++j) {
       const int d = d0 + j;
       if (d >= Di) continue;
       const size_t row = ((size_t)b * p.nseg + sp) * Di + d;
@@ -380,14 +402,15 @@ scan_fwd_kernel(const FwdParams p) {
     if constexpr (ST) {
 #pragma unroll
       for (int i = 0; i < kChunk; ++i) {
-        const float2 dlv = lds2(s_dl + i * DC + cl);
-        const float2 uv = lds2(s_u + i * DC + cl);
+        float dlv[DPT], uv[DPT];
+        lds_chan<DPT>(s_dl + i * DC + cl, dlv);
+        lds_chan<DPT>(s_u + i * DC + cl, uv);
         float2 Bp[NPR];
         lds_pairs<NPR>(s_B + i * NP + n0, Bp);
 #pragma unroll
-        for (int j = 0; j < kDPT; ++j) {
-          const float dl = j ? dlv.y : dlv.x;
-          const float uu = j ? uv.y : uv.x;
+        for (int j = 0; j < DPT; ++j) {
+          const float dl = dlv[j];
+          const float uu = uv[j];
           const float2 dl2 = splat2(dl), du2 = splat2(dl * uu);
 #pragma unroll
           for (int pp = 0; pp < NPR; ++pp)
@@ -397,19 +420,20 @@ scan_fwd_kernel(const FwdParams p) {
     } else {
 #pragma unroll
       for (int gi = 0; gi < kChunk / P; ++gi) {
-        float yv[2 * P];
+        float yv[DPT * P];
 #pragma unroll
         for (int tt = 0; tt < P; ++tt) {
           const int i = gi * P + tt;
-          const float2 dlv = lds2(s_dl + i * DC + cl);
-          const float2 uv = lds2(s_u + i * DC + cl);
+          float dlv[DPT], uv[DPT];
+          lds_chan<DPT>(s_dl + i * DC + cl, dlv);
+          lds_chan<DPT>(s_u + i * DC + cl, uv);
           float2 Bp[NPR], Cp[NPR];
           lds_pairs<NPR>(s_B + i * NP + n0, Bp);
           lds_pairs<NPR>(s_C + i * NP + n0, Cp);
 #pragma unroll
-          for (int j = 0; j < kDPT; ++j) {
-            const float dl = j ? dlv.y : dlv.x;
-            const float uu = j ? uv.y : uv.x;
+          for (int j = 0; j < DPT; ++j) {
+            const float dl = dlv[j];
+            const float uu = uv[j];
             const float2 dl2 = splat2(dl), du2 = splat2(dl * uu);
             float2 ya = make_float2(0.f, 0.f);
 #pragma unroll
@@ -418,19 +442,22 @@ scan_fwd_kernel(const FwdParams p) {
               h[j][pp] = fma2(da, h[j][pp], mul2(du2, Bp[pp]));
               ya = fma2(Cp[pp], h[j][pp], ya);
             }
-            yv[tt * 2 + j] = ya.x + ya.y;
+            yv[tt * DPT + j] = ya.x + ya.y;
           }
         }
         RSy::run(yv, lane);
 #pragma unroll
         for (int r = 0; r < kY; ++r) {
           const int idx = ybase + r;
-          const int tt = idx >> 1, j = idx & 1;
+          const int tt = idx / DPT, j = idx % DPT;
           const int i = gi * P + tt;
           const int t = t0 + i, d = d0 + j;
           const float uu = s_u[i * DC + cl + j];
           const float g = s_g[i * DC + cl + j];
-          const float y = fmaf(j ? Dd[1] : Dd[0], uu, yv[r]);
+          float Dj = Dd[0];   // Dd[j] without a dynamically indexed register array
+#pragma unroll
+          for (int k = 1; k < DPT; ++k) Dj = j == k ? Dd[k] : Dj;
+          const float y = fmaf(Dj, uu, yv[r]);
           const bool ok = (t < T) && (d < Di);
           const size_t o = (rowb + t) * Di + d;
           st_global_if(p.out + o, y * (g * sigmoid_fast(g)), ok);
@@ -443,7 +470,7 @@ scan_fwd_kernel(const FwdParams p) {
     if (c + 1 < p.nchunks) {
       float* ck = p.ckpt + ((size_t)b * (p.nchunks - 1) + c) * (size_t)Di * N;
 #pragma unroll
-      for (int j = 0; j < kDPT; ++j) {
+      for (int j = 0; j < DPT; ++j) {
         const int d = d0 + j;
         if (d >= Di) continue;
         if constexpr (VEC) {

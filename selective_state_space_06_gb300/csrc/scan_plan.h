@@ -18,6 +18,12 @@ constexpr int kDPT = 2;     // channels per thread
 // and with 4 beyond; the backward is fastest with 4 (fewer cross-lane reductions per element).
 __host__ __device__ constexpr int states_per_thread_fwd(int NP) { return NP <= 16 ? 2 : 4; }
 __host__ __device__ constexpr int states_per_thread_bwd(int NP) { return NP < 4 ? NP : 4; }
+// Channels per thread of the forward kernels (2 or 4). Each thread loads the B and C values of
+// its states once per step for all of its channels, so more channels per thread deliver fewer
+// shared-memory bytes per (element, state). Measured on GB300: 4 at d_state 64 (longseq
+// forward 4.53 -> 4.18 ms, where the kernel is bound by the shared-memory data path), 2 below
+// (4 at d_state 16 is slower: half the warps, mamba130m forward 0.111 -> 0.138 ms).
+__host__ __device__ constexpr int fwd_channels_per_thread(int NP) { return NP == 64 ? 4 : 2; }
 constexpr int kWarps = 4;   // warps per CTA
 // warps per CTA of the forward scan (measured: 2 warps per CTA runs as fast, 1 is 10 % slower
 // at mamba130m and 57 % at longseq; the CTAs' uneven spread over the SMs does not limit it)
