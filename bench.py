@@ -181,23 +181,33 @@ BWD_FP32_OPS_PER_ELEMENT_STATE = 11
 BWD_EX2_PER_ELEMENT_STATE = 1
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum, summed over the call's kernels) of
-# one mamba_scan_bwd call, taken from an ncu capture of these kernels. Each entry carries the
-# digest of the kernel sources it was captured with (kernel_digest() below); once the sources
-# differ the entry no longer describes the kernels and `traffic` is reported as null.
+# one mamba_scan_bwd call, taken from an ncu capture of these kernels (the launch list with
+# those two metrics, run on this bench's own command with --steps 3 --warmup 3). Each entry
+# carries the digest of the sources of the backward call's kernels and of their launch plan
+# (kernel_digest() below); once those sources differ, the entry no longer describes the
+# kernels and `traffic` is reported as null. The long-sequence figure was captured at
+# T = 8192 (--seq-len 8192) and scaled by 8: every term of it is proportional to T except the
+# carry composition's reads (under 1 % of it).
 BWD_TRAFFIC_CAPTURES = {
     # workload: (bytes per call, kernel digest, how the figure was taken)
+    "mamba370m": (1625.9e6, "234e669ad63f046c", "ncu capture at the full size"),
+    "mamba1p4b": (1625.8e6, "234e669ad63f046c", "ncu capture at the full size"),
+    "mamba130m": (556.4e6, "234e669ad63f046c", "ncu capture at the full size"),
+    "longseq": (8 * 1943.4e6, "234e669ad63f046c", "ncu capture at T = 8192, scaled by 8"),
 }
+# the files that define the backward call's kernels and their launch plan
+BWD_KERNEL_SOURCES = ("scan_common.cuh", "scan_plan.h", "scan_plan.cu", "scan_bwd.cu",
+                      "scan_bwd_tmem.cu")
 
 
 def kernel_digest() -> str:
-    """sha256 (first 16 hex digits) over the CUDA sources of the library, in name order."""
+    """sha256 (first 16 hex digits) over the backward call's kernel and plan sources."""
     import hashlib
     d = os.path.join(ROOT, "selective_state_space_06_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(d)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(d, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in BWD_KERNEL_SOURCES:
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libmambascan.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["scan_fwd.cu", "scan_bwd.cu", "scan_bwd_tmem.cu", "mamba_scan_abi.cu", "conv1d.cu", "conv_abi.cu", "mamba_scan_noalloc.cu"]
+SOURCES = ["scan_plan.cu", "scan_fwd.cu", "scan_bwd.cu", "scan_bwd_tmem.cu", "mamba_scan_abi.cu", "conv1d.cu", "conv_abi.cu", "mamba_scan_noalloc.cu"]
 
 
 def nvcc() -> str:

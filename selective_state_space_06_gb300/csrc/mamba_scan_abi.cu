@@ -13,102 +13,6 @@
 #include "../../include/mamba_scan.h"
 #include "scan_plan.h"
 
-namespace mscan {
-
-static constexpr size_t kAlignFloats = 64;  // 256-byte alignment of scratch regions
-
-size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-
-bool make_plan(int64_t batch, int64_t T, int64_t Di, int64_t N, Plan* pl) {
-  if (batch < 1 || T < 1 || Di < 1 || N < 1) return false;
-  if (N > kMaxState || batch > 65535) return false;
-  if (T > INT32_MAX || Di > INT32_MAX) return false;
-  const double btd = (double)batch * (double)T * (double)Di;
-  const double btn = (double)batch * (double)T * (double)N;
-  if (btd >= 2147483648.0 || btn >= 2147483648.0) return false;
-  Plan p;
-  p.batch = batch; p.T = T; p.Di = Di; p.N = N;
-  p.NP = N <= 4 ? 4 : N <= 8 ? 8 : N <= 16 ? 16 : N <= 32 ? 32 : 64;
-  p.nchunks = (int)((T + kChunk - 1) / kChunk);
-  auto split = [&](PassPlan& q, int want) {
-    if (want < 1) want = 1;
-    if (want > p.nchunks) want = p.nchunks;
-    q.seg_chunks = (p.nchunks + want - 1) / want;
-    q.nseg = (p.nchunks + q.seg_chunks - 1) / q.seg_chunks;
-  };
-  auto pass = [&](int npt, int dpt, int warps = kWarps) {
-    PassPlan q;
-    q.NPT = npt;
-    q.G = p.NP / npt;
-    q.DC = warps * (32 / q.G) * dpt;
-    q.nblk = (int)((Di + q.DC - 1) / q.DC);
-    return q;
-  };
-  auto by_target = [&](PassPlan q, int target) {
-    const int64_t rows = (int64_t)batch * q.nblk;
-    split(q, (int)std::min<int64_t>((target + rows - 1) / rows, p.nchunks));
-    return q;
-  };
-  // Segments for a kernel with `slots` resident CTAs: the fewest chunk steps on the critical
-  // path (whole waves times chunks per segment, plus about one chunk of start-up per CTA) plus
-  // the pre-pass, which costs about a quarter of the main kernel per chunk and covers every
-  // segment but the first.
-  auto by_waves = [&](PassPlan q, int slots) {
-    const int64_t rows = (int64_t)batch * q.nblk;
-    double best = 1e300;
-    int best_want = 1;
-    for (int want = 1; want <= std::min(p.nchunks, 64); ++want) {
-      const int sc = (p.nchunks + want - 1) / want;
-      const int ns = (p.nchunks + sc - 1) / sc;
-      const int64_t waves = (rows * ns + slots - 1) / slots;
-      const double cost = (double)waves * (sc + 1) +
-                          0.25 * (double)(ns - 1) / ns * (double)p.nchunks * rows / slots;
-      if (cost < best - 1e-9) { best = cost; best_want = want; }
-    }
-    split(q, best_want);
-    return q;
-  };
-  p.fwd = by_target(pass(states_per_thread_fwd(p.NP), fwd_channels_per_thread(p.NP), kFwdWarps),
-                    target_units_fwd(p.NP));
-  if (p.NP >= kTmemMinNP)
-    p.bwd = by_waves(pass(4, kTmemDPT), kTmemSlots);
-  else
-    p.bwd = by_target(pass(states_per_thread_bwd(p.NP), kDPT), target_units_bwd(p.NP));
-  p.bwd.sub_chunks = p.bwd.seg_chunks;
-  p.bwd.nsub = 1;
-  if (p.NP >= kTmemMinNP && p.bwd.nseg > 1) {
-    // pre-pass CTAs: batch x (the main kernel's channel blocks) x (segments 1 .. nseg-1) x nsub
-    const int64_t base = (int64_t)batch * p.bwd.nblk * (p.bwd.nseg - 1);
-    int64_t k = (kBwdAggTarget + base - 1) / base;
-    k = std::max<int64_t>(1, std::min<int64_t>(k, p.bwd.seg_chunks));
-    p.bwd.sub_chunks = (int)((p.bwd.seg_chunks + k - 1) / k);
-    p.bwd.nsub = (p.bwd.seg_chunks + p.bwd.sub_chunks - 1) / p.bwd.sub_chunks;
-  }
-  const size_t bdn = (size_t)batch * (size_t)Di * (size_t)N;
-  const size_t bd = (size_t)batch * (size_t)Di;
-  size_t ck = round_up((size_t)(p.nchunks - 1) * bdn, kAlignFloats);
-  if (p.fwd.nseg > 1) {
-    p.off_fagg_h = ck; ck = round_up(ck + (size_t)p.fwd.nseg * bdn, kAlignFloats);
-    p.off_fagg_sd = ck; ck = round_up(ck + (size_t)p.fwd.nseg * bd, kAlignFloats);
-  }
-  p.off_y = ck; ck = round_up(ck + (size_t)batch * (size_t)T * (size_t)Di, kAlignFloats);
-  p.ckpt_elems = ck;
-  const size_t part_bc = (size_t)p.bwd.nblk * (size_t)batch * (size_t)T * (size_t)N;
-  size_t off = 0;
-  p.off_partB = off; off = round_up(off + part_bc, kAlignFloats);
-  p.off_partC = off; off = round_up(off + part_bc, kAlignFloats);
-  p.off_partA = off; off = round_up(off + (size_t)p.bwd.nseg * bdn, kAlignFloats);
-  p.off_partD = off; off = round_up(off + (size_t)p.bwd.nseg * bd, kAlignFloats);
-  const size_t nslot = (size_t)p.bwd.nseg * p.bwd.nsub;
-  p.off_bagg_L = off; off = round_up(off + nslot * bdn, kAlignFloats);
-  p.off_bagg_sd = off; off = round_up(off + nslot * bd, kAlignFloats);
-  p.scratch_elems = off;
-  *pl = p;
-  return true;
-}
-
-}  // namespace mscan
-
 using mscan::Plan;
 using mscan::round_up;
 
@@ -159,17 +63,69 @@ int check_dims(int64_t batch, int64_t T, int64_t Di, int64_t N, Plan* plan) {
 // set of checkpoint + scratch buffers per slice, then the slices' d_A_log / d_D sums.
 constexpr int kHostSlices = 4;
 
+// A batch smaller than the slice count is cut into blocks of channels instead (each slice is
+// then the whole batch over dcs consecutive channels, a scan of its own); the smallest block
+// worth a slice of its own:
+constexpr int64_t kMinSliceChannels = 64;
+
 struct HostLayout {
   int64_t rows = 0;            // batch rows per slice
   int nslices = 0;
   size_t off_in[8], off_out[8], off_ck[kHostSlices], off_sc[kHostSlices], off_part = 0;
   size_t ck_bytes = 0, sc_bytes = 0, total = 0;
   size_t dn_pad = 0, dd_pad = 0;   // floats
+  // channel slices: each slice's compact inputs and outputs [batch][T][dcs], its A_log / D
+  // rows and d_A_log / d_D rows (one region per slice), the shared B and C, and the slices'
+  // d_B | d_C partials with their fixed-order sum
+  bool by_channels = false;
+  int64_t dcs = 0;
+  size_t off_slice[kHostSlices] = {};
+  size_t sl_in[4] = {}, sl_A = 0, sl_D = 0, sl_out[4] = {}, sl_dA = 0, sl_dD = 0;   // in a slice
+  size_t off_bc = 0, off_bcpart = 0, off_bcsum = 0;
 };
+
+static bool host_layout_channels(int64_t batch, int64_t T, int64_t Di, int64_t N,
+                                 HostLayout* L) {
+  HostLayout h;
+  h.by_channels = true;
+  const int64_t want = std::min<int64_t>(kHostSlices, Di / kMinSliceChannels);
+  h.dcs = round_up((size_t)((Di + want - 1) / want), 4);
+  h.nslices = (int)((Di + h.dcs - 1) / h.dcs);
+  h.rows = batch;
+  Plan slice;
+  if (!mscan::make_plan(batch, T, h.dcs, N, &slice)) return false;
+  // a narrower last slice needs no more checkpoint or scratch than a full one
+  h.ck_bytes = slice.ckpt_elems * sizeof(float);
+  h.sc_bytes = slice.scratch_elems * sizeof(float);
+  const size_t a = 256;
+  const size_t btd_s = (size_t)batch * T * h.dcs * 4, btn = (size_t)batch * T * N * 4;
+  size_t off = 0;   // inside one slice region
+  for (int i = 0; i < 4; ++i) { h.sl_in[i] = off; off = round_up(off + btd_s, a); }
+  h.sl_A = off; off = round_up(off + (size_t)h.dcs * N * 4, a);
+  h.sl_D = off; off = round_up(off + (size_t)h.dcs * 4, a);
+  for (int i = 0; i < 4; ++i) { h.sl_out[i] = off; off = round_up(off + btd_s, a); }
+  h.sl_dA = off; off = round_up(off + (size_t)h.dcs * N * 4, a);
+  h.sl_dD = off; off = round_up(off + (size_t)h.dcs * 4, a);
+  const size_t slice_bytes = off;
+  off = 0;
+  for (int k = 0; k < h.nslices; ++k) {
+    h.off_slice[k] = off; off = round_up(off + slice_bytes, a);
+    h.off_ck[k] = off; off = round_up(off + h.ck_bytes, a);
+    h.off_sc[k] = off; off = round_up(off + h.sc_bytes, a);
+  }
+  h.off_bc = off; off = round_up(off + 2 * btn, a);
+  h.off_bcpart = off; off = round_up(off + (size_t)h.nslices * 2 * btn, a);
+  h.off_bcsum = off; off = round_up(off + 2 * btn, a);
+  h.total = off;
+  *L = h;
+  return true;
+}
 
 bool host_layout(int64_t batch, int64_t T, int64_t Di, int64_t N, HostLayout* L) {
   Plan whole;
   if (!mscan::make_plan(batch, T, Di, N, &whole)) return false;
+  if (batch < kHostSlices && Di % 4 == 0 && Di >= 2 * kMinSliceChannels)
+    return host_layout_channels(batch, T, Di, N, L);
   HostLayout h;
   // slices start on 16-byte boundaries only when a batch row is a multiple of 4 floats
   const bool sliceable = (T * Di) % 4 == 0 && (T * N) % 4 == 0;
@@ -566,6 +522,110 @@ size_t mamba_scan_host_workspace_bytes(int64_t batch, int64_t T, int64_t d_inner
   return L.total;
 }
 
+// mamba_scan_fwd_bwd_host for a batch smaller than the slice count: slice k is the whole batch
+// over channels [k*dcs, k*dcs + dcs) and runs as a scan of its own on its own stream. Its
+// inputs come in with 2-D copies (rows of dcs floats out of the host's rows of d_inner), its
+// outputs go back the same way, its rows of A_log, D, d_A_log and d_D are plain ranges, and
+// d_B, d_C (sums over d_inner) are the slices' sums added in slice order by a small kernel.
+static int run_channel_slices(const HostLayout& L, char* w, const float* delta, const float* u,
+                              const float* B, const float* C, const float* gate,
+                              const float* A_log, const float* D, const float* dy, float* out,
+                              float* d_delta, float* d_u, float* d_B, float* d_C,
+                              float* d_A_log, float* d_D, float* d_gate, int64_t batch,
+                              int64_t T, int64_t d_inner, int64_t d_state, cudaStream_t s0) {
+  AuxStreams ax;
+  if (!aux_streams(&ax)) return set_cuda_error(cudaGetLastError());
+  ax.s[0] = s0;
+  auto at = [&](size_t off) { return (float*)(w + off); };
+  const size_t rows = (size_t)batch * T;                 // rows of the [batch*T][d_inner] view
+  const size_t btn = rows * (size_t)d_state;             // floats of B (and C)
+  float* w_B = at(L.off_bc);
+  float* w_C = w_B + btn;
+  cudaError_t e;
+  // B and C (shared by every slice) first, on the caller's stream
+  if ((e = cudaMemcpyAsync(w_B, B, btn * 4, cudaMemcpyHostToDevice, s0)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(w_C, C, btn * 4, cudaMemcpyHostToDevice, s0)) != cudaSuccess ||
+      (e = cudaEventRecord(ax.ev[kHostSlices], s0)) != cudaSuccess)
+    return set_cuda_error(e);
+  for (int k = 1; k < L.nslices; ++k)
+    if ((e = cudaStreamWaitEvent(ax.s[k], ax.ev[kHostSlices], 0)) != cudaSuccess)
+      return set_cuda_error(e);
+  int launches = 0;
+  const size_t hp = (size_t)d_inner * 4;   // host row pitch
+  for (int k = 0; k < L.nslices; ++k) {
+    cudaStream_t st = ax.s[k];
+    const int64_t d0 = (int64_t)k * L.dcs, nd = std::min<int64_t>(L.dcs, d_inner - d0);
+    const size_t dp = (size_t)nd * 4;        // device row pitch (compact slice)
+    char* sl = w + L.off_slice[k];
+    float* in[4];
+    float* outv[4];
+    for (int i = 0; i < 4; ++i) {
+      in[i] = (float*)(sl + L.sl_in[i]);
+      outv[i] = (float*)(sl + L.sl_out[i]);
+    }
+    float* sA = (float*)(sl + L.sl_A);
+    float* sD = (float*)(sl + L.sl_D);
+    float* sdA = (float*)(sl + L.sl_dA);
+    float* sdD = (float*)(sl + L.sl_dD);
+    float* part = at(L.off_bcpart) + (size_t)k * 2 * btn;   // d_B | d_C of this slice
+    const float* hin[4] = {delta, u, gate, dy};
+    // one slice's copies at a time in each direction (slice order), each at the link's rate
+    if (k > 0 && (e = cudaStreamWaitEvent(st, ax.ev_in[k - 1], 0)) != cudaSuccess)
+      return set_cuda_error(e);
+    for (int i = 0; i < 4; ++i)
+      if ((e = cudaMemcpy2DAsync(in[i], dp, hin[i] + d0, hp, dp, rows, cudaMemcpyHostToDevice,
+                                 st)) != cudaSuccess)
+        return set_cuda_error(e);
+    if ((e = cudaMemcpyAsync(sA, A_log + (size_t)d0 * d_state, (size_t)nd * d_state * 4,
+                             cudaMemcpyHostToDevice, st)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(sD, D + d0, dp, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
+        (e = cudaEventRecord(ax.ev_in[k], st)) != cudaSuccess)
+      return set_cuda_error(e);
+    float* ck = at(L.off_ck[k]);
+    float* sc = at(L.off_sc[k]);
+    int rc = mamba_scan_fwd(in[0], in[1], w_B, w_C, in[2], sA, sD, outv[0], nullptr,
+                            L.ck_bytes ? ck : nullptr, L.ck_bytes, batch, T, nd, d_state, st);
+    if (rc != MAMBA_OK) return rc;
+    launches += g_last_launches;
+    rc = mamba_scan_bwd(in[0], in[1], w_B, w_C, in[2], sA, sD, in[3], L.ck_bytes ? ck : nullptr,
+                        L.ck_bytes, sc, L.sc_bytes, outv[1], outv[2], part, part + btn, sdA, sdD,
+                        outv[3], batch, T, nd, d_state, st);
+    if (rc != MAMBA_OK) return rc;
+    launches += g_last_launches;
+    float* hout[4] = {out, d_delta, d_u, d_gate};
+    if (k > 0 && (e = cudaStreamWaitEvent(st, ax.ev_out[k - 1], 0)) != cudaSuccess)
+      return set_cuda_error(e);
+    for (int i = 0; i < 4; ++i)
+      if ((e = cudaMemcpy2DAsync(hout[i] + d0, hp, outv[i], dp, dp, rows, cudaMemcpyDeviceToHost,
+                                 st)) != cudaSuccess)
+        return set_cuda_error(e);
+    if ((e = cudaMemcpyAsync(d_A_log + (size_t)d0 * d_state, sdA, (size_t)nd * d_state * 4,
+                             cudaMemcpyDeviceToHost, st)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(d_D + d0, sdD, dp, cudaMemcpyDeviceToHost, st)) != cudaSuccess ||
+        (e = cudaEventRecord(ax.ev_out[k], st)) != cudaSuccess)
+      return set_cuda_error(e);
+  }
+  // d_B and d_C: the slices' sums, added in slice order
+  for (int k = 1; k < L.nslices; ++k)
+    if ((e = cudaEventRecord(ax.ev[k], ax.s[k])) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(s0, ax.ev[k], 0)) != cudaSuccess)
+      return set_cuda_error(e);
+  float* sum = at(L.off_bcsum);
+  const size_t n = 2 * btn;
+  mscan::sum_slices<<<(unsigned)std::min<size_t>((n + 255) / 256, 65535), 256, 0, s0>>>(
+      at(L.off_bcpart), L.nslices, n, sum);
+  if ((e = cudaPeekAtLastError()) != cudaSuccess) return set_cuda_error(e);
+  ++launches;
+  if ((e = cudaMemcpyAsync(d_B, sum, btn * 4, cudaMemcpyDeviceToHost, s0)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(d_C, sum + btn, btn * 4, cudaMemcpyDeviceToHost, s0)) != cudaSuccess)
+    return set_cuda_error(e);
+  e = cudaStreamSynchronize(s0);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  g_last_launches = launches;
+  if (mscan::bwd_take_fault()) return MAMBA_ERR_TIMEOUT;
+  return MAMBA_OK;
+}
+
 int mamba_scan_fwd_bwd_host(const float* delta, const float* u, const float* B, const float* C,
                             const float* gate, const float* A_log, const float* D,
                             const float* dy, float* out, float* d_delta, float* d_u, float* d_B,
@@ -584,6 +644,10 @@ int mamba_scan_fwd_bwd_host(const float* delta, const float* u, const float* B, 
   if (!host_layout(batch, T, d_inner, d_state, &L)) return MAMBA_ERR_INVALID_ARG;
   if (workspace_bytes < L.total) return MAMBA_ERR_WORKSPACE;
   char* w = (char*)workspace;
+  if (L.by_channels)
+    return run_channel_slices(L, w, delta, u, B, C, gate, A_log, D, dy, out, d_delta, d_u, d_B,
+                              d_C, d_A_log, d_D, d_gate, batch, T, d_inner, d_state,
+                              (cudaStream_t)stream);
   auto at = [&](size_t off) { return (float*)(w + off); };
   float *w_delta = at(L.off_in[0]), *w_u = at(L.off_in[1]), *w_gate = at(L.off_in[2]),
         *w_dy = at(L.off_in[3]), *w_B = at(L.off_in[4]), *w_C = at(L.off_in[5]),

@@ -88,8 +88,10 @@ struct Plan {
 // MAMBA_ERR_CUDA (for entry points outside mamba_scan_abi.cu).
 int record_cuda_error(cudaError_t e);
 
-// Returns false when the sizes are outside what the kernels support.
+// Returns false when the sizes are outside what the kernels support (scan_plan.cu).
 bool make_plan(int64_t batch, int64_t T, int64_t Di, int64_t N, Plan* plan);
+// x rounded up to a multiple of a
+size_t round_up(size_t x, size_t a);
 
 struct FwdParams {
   const float* delta; const float* u; const float* B; const float* C; const float* gate;

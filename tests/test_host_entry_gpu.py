@@ -1,12 +1,15 @@
 """mamba_scan_fwd_bwd_host: forward + backward from host buffers, against the fp64 oracle.
 
-The host entry cuts the batch into up to four slices, each on its own stream, so that the
-copies in both directions overlap the kernels; d_A_log and d_D are the slices' sums added in
-slice order. The
-outputs must meet the parity bar of the device entry points on every element (out and the
-seven gradients; y is not returned by this call). The shapes cover four slices (mamba130m),
-three slices with a shorter last one (batch 5), and one slice (rows of T*d_inner not a
-multiple of 4 floats, where slices could not start on 16-byte boundaries).
+The host entry cuts the work into up to four slices, each on its own stream, so that the
+copies in both directions overlap the kernels. A batch of four rows or more is cut by batch
+rows (d_A_log and d_D are then the slices' sums added in slice order); a smaller batch is cut
+into blocks of channels (each slice the whole batch over its channels, moved with 2-D copies;
+d_B and d_C are then the slices' sums added in slice order). The outputs must meet the parity
+bar of the device entry points on every element (out and the seven gradients; y is not
+returned by this call). The shapes cover four batch slices (mamba130m), three with a shorter
+last one (batch 5), one slice (rows of T*d_inner not a multiple of 4 floats, where slices
+could not start on 16-byte boundaries), and channel slices at batch 1 (d_state 64, with a
+narrower last block) and batch 2 (d_state 16).
 """
 import numpy as np
 import pytest
@@ -49,8 +52,10 @@ def _run_host(x, repeat=2):
     return results
 
 
-@pytest.mark.parametrize("shape", [(8, 1024, 1536, 16), (5, 100, 64, 16), (3, 37, 50, 5)],
-                         ids=["mamba130m_4slices", "batch5_3slices", "ragged_1slice"])
+@pytest.mark.parametrize("shape", [(8, 1024, 1536, 16), (5, 100, 64, 16), (3, 37, 50, 5),
+                                   (1, 300, 260, 64), (2, 200, 512, 16)],
+                         ids=["mamba130m_4slices", "batch5_3slices", "ragged_1slice",
+                              "batch1_channel_slices", "batch2_channel_slices"])
 def test_host_entry_matches_oracle(shape):
     if shape[0] == 8:
         x = synth.make_inputs(synth.BY_NAME["mamba130m"])
