@@ -65,6 +65,10 @@ extern "C" {
 #define MAMBA_ERR_TIMEOUT 7     /* reported by mamba_scan_status: a kernel gave up waiting
                                    (1 s) for one of its own asynchronous copies; the outputs
                                    of the calls since the last status check are invalid     */
+#define MAMBA_ERR_BOUNDS 8      /* reported by mamba_scan_status of a bounds-checked build
+                                   (libmambascan_checked.so): a kernel computed an offset
+                                   outside its buffer; the access was not made, and the
+                                   outputs since the last status check are invalid          */
 
 /* Bytes of the checkpoint buffer that mamba_scan_fwd writes and mamba_scan_bwd reads. The
  * forward stores the state h at every 16-step chunk boundary of the time axis, so that the
@@ -247,10 +251,25 @@ int mamba_scan_bwd_test_timeout(const float* delta, const float* u, const float*
                                 float* d_A_log, float* d_D, float* d_gate, int64_t batch,
                                 int64_t T, int64_t d_inner, int64_t d_state, void* stream);
 
-/* Synchronises `stream` and reports any asynchronous CUDA error (MAMBA_ERR_CUDA) or a
- * kernel that gave up waiting for its own copies (MAMBA_ERR_TIMEOUT; the flag is then
- * cleared). MAMBA_OK otherwise. */
+/* Synchronises `stream` and reports any asynchronous CUDA error (MAMBA_ERR_CUDA), a
+ * kernel that gave up waiting for its own copies (MAMBA_ERR_TIMEOUT), or, in a bounds-checked
+ * build, an access a kernel computed outside its buffer (MAMBA_ERR_BOUNDS). Each flag is
+ * cleared once reported. MAMBA_OK otherwise. */
 int mamba_scan_status(void* stream);
+
+/* Bounds-checked build. The library compiled with -DMAMBA_BOUNDS_CHECK
+ * (libmambascan_checked.so, the same source) checks every global access whose offset a kernel
+ * computes against the length of its buffer, taken from the call's sizes. An access outside
+ * is not made (a load reads zero, a store is dropped) and is recorded for mamba_scan_status.
+ * No check traps. TMA copies are bounded by their tensor maps and are not checked again.
+ * mamba_scan_bounds_checked returns 1 in that build and 0 in the default one.
+ * mamba_scan_test_bounds_shrink (test hook) makes every kernel take each buffer `elements`
+ * elements shorter than it is, so a test can see the check fire while every access it blocks
+ * is inside the real buffer; 0 restores the real lengths. It returns MAMBA_ERR_UNSUPPORTED in
+ * the default build and MAMBA_ERR_INVALID_ARG for a negative count. It applies to the
+ * device current at the call. */
+int mamba_scan_bounds_checked(void);
+int mamba_scan_test_bounds_shrink(int64_t elements);
 
 /* Static, human-readable text of a return code. When the code is MAMBA_ERR_CUDA it names the
  * last CUDA error this library saw. Never NULL. */

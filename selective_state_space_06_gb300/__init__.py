@@ -8,13 +8,15 @@ raises ImportError. To build it, run ``python selective_state_space_06_gb300/bui
 The functions mirror the C ABI in include/mamba_scan.h and keep its names:
   mamba_scan_ckpt_bytes, mamba_scan_scratch_bytes, mamba_scan_fwd, mamba_scan_bwd,
   mamba_scan_host_workspace_bytes, mamba_scan_fwd_bwd_host, mamba_scan_status,
-  mamba_scan_strerror, mamba_scan_last_launch_count.
+  mamba_scan_strerror, mamba_scan_last_launch_count, mamba_scan_bounds_checked,
+  mamba_scan_test_bounds_shrink (the bounds-checked build: checked_library(), using_library()).
 Tensor arguments are torch tensors: float32, contiguous, on a CUDA device. The host entry point
 takes CPU tensors instead. ``stream`` defaults to torch's current stream on the tensors' device.
 Nonzero return codes raise MambaScanError.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -36,6 +38,7 @@ MAMBA_ERR_CUDA = 4
 MAMBA_ERR_UNSUPPORTED = 5
 MAMBA_ERR_NOALLOC_LIMIT = 6
 MAMBA_ERR_TIMEOUT = 7
+MAMBA_ERR_BOUNDS = 8
 MAMBA_SCAN_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 EXPORTED = (
@@ -45,48 +48,60 @@ EXPORTED = (
     "mamba_scan_fwd_softplus", "mamba_scan_bwd_softplus", "mamba_scan_fwd_bwd",
     "mamba_scan_fwd_bwd_bf16", "mamba_scan_bwd_test_timeout",
     "mamba_conv_scratch_bytes", "mamba_conv_fwd", "mamba_conv_bwd",
+    "mamba_scan_bounds_checked", "mamba_scan_test_bounds_shrink",
 )
 
 _vp = ctypes.c_void_p
 _i64 = ctypes.c_int64
 _sz = ctypes.c_size_t
 
-_lib.mamba_scan_ckpt_bytes.argtypes = [_i64] * 4
-_lib.mamba_scan_ckpt_bytes.restype = _sz
-_lib.mamba_scan_scratch_bytes.argtypes = [_i64] * 4
-_lib.mamba_scan_scratch_bytes.restype = _sz
-_lib.mamba_scan_host_workspace_bytes.argtypes = [_i64] * 4
-_lib.mamba_scan_host_workspace_bytes.restype = _sz
-_lib.mamba_scan_fwd.argtypes = [_vp] * 10 + [_sz] + [_i64] * 4 + [_vp]
-_lib.mamba_scan_fwd.restype = ctypes.c_int
-_lib.mamba_scan_bwd.argtypes = [_vp] * 9 + [_sz, _vp, _sz] + [_vp] * 7 + [_i64] * 4 + [_vp]
-_lib.mamba_scan_bwd.restype = ctypes.c_int
-_lib.mamba_conv_scratch_bytes.argtypes = [_i64] * 4
-_lib.mamba_conv_scratch_bytes.restype = _sz
-_lib.mamba_conv_fwd.argtypes = [_vp] * 4 + [_i64] * 4 + [_vp]
-_lib.mamba_conv_fwd.restype = ctypes.c_int
-_lib.mamba_conv_bwd.argtypes = [_vp] * 5 + [_sz] + [_vp] * 3 + [_i64] * 4 + [_vp]
-_lib.mamba_conv_bwd.restype = ctypes.c_int
-_lib.mamba_scan_fwd_softplus.argtypes = _lib.mamba_scan_fwd.argtypes
-_lib.mamba_scan_fwd_softplus.restype = ctypes.c_int
-_lib.mamba_scan_bwd_softplus.argtypes = _lib.mamba_scan_bwd.argtypes
-_lib.mamba_scan_bwd_softplus.restype = ctypes.c_int
-_lib.mamba_scan_bwd_test_timeout.argtypes = _lib.mamba_scan_bwd.argtypes
-_lib.mamba_scan_bwd_test_timeout.restype = ctypes.c_int
-_lib.mamba_scan_fwd_bwd.argtypes = [_vp] * 10 + [_sz, _vp, _sz] + [_vp] * 7 + [_i64] * 4 + [_vp]
-_lib.mamba_scan_fwd_bwd.restype = ctypes.c_int
-_lib.mamba_scan_fwd_bwd_bf16.argtypes = _lib.mamba_scan_fwd_bwd.argtypes
-_lib.mamba_scan_fwd_bwd_bf16.restype = ctypes.c_int
-_lib.mamba_scan_bwd_noalloc.argtypes = [_vp] * 9 + [_sz] + [_vp] * 7 + [_i64] * 4 + [_vp]
-_lib.mamba_scan_bwd_noalloc.restype = ctypes.c_int
-_lib.mamba_scan_fwd_bwd_host.argtypes = [_vp] * 17 + [_sz] + [_i64] * 4 + [_vp]
-_lib.mamba_scan_fwd_bwd_host.restype = ctypes.c_int
-_lib.mamba_scan_status.argtypes = [_vp]
-_lib.mamba_scan_status.restype = ctypes.c_int
-_lib.mamba_scan_strerror.argtypes = [ctypes.c_int]
-_lib.mamba_scan_strerror.restype = ctypes.c_char_p
-_lib.mamba_scan_last_launch_count.argtypes = []
-_lib.mamba_scan_last_launch_count.restype = ctypes.c_int
+
+def _configure(lib: ctypes.CDLL) -> ctypes.CDLL:
+    """Sets the argument and result types of every exported function of ``lib``."""
+    lib.mamba_scan_ckpt_bytes.argtypes = [_i64] * 4
+    lib.mamba_scan_ckpt_bytes.restype = _sz
+    lib.mamba_scan_scratch_bytes.argtypes = [_i64] * 4
+    lib.mamba_scan_scratch_bytes.restype = _sz
+    lib.mamba_scan_host_workspace_bytes.argtypes = [_i64] * 4
+    lib.mamba_scan_host_workspace_bytes.restype = _sz
+    lib.mamba_scan_fwd.argtypes = [_vp] * 10 + [_sz] + [_i64] * 4 + [_vp]
+    lib.mamba_scan_fwd.restype = ctypes.c_int
+    lib.mamba_scan_bwd.argtypes = [_vp] * 9 + [_sz, _vp, _sz] + [_vp] * 7 + [_i64] * 4 + [_vp]
+    lib.mamba_scan_bwd.restype = ctypes.c_int
+    lib.mamba_conv_scratch_bytes.argtypes = [_i64] * 4
+    lib.mamba_conv_scratch_bytes.restype = _sz
+    lib.mamba_conv_fwd.argtypes = [_vp] * 4 + [_i64] * 4 + [_vp]
+    lib.mamba_conv_fwd.restype = ctypes.c_int
+    lib.mamba_conv_bwd.argtypes = [_vp] * 5 + [_sz] + [_vp] * 3 + [_i64] * 4 + [_vp]
+    lib.mamba_conv_bwd.restype = ctypes.c_int
+    lib.mamba_scan_fwd_softplus.argtypes = lib.mamba_scan_fwd.argtypes
+    lib.mamba_scan_fwd_softplus.restype = ctypes.c_int
+    lib.mamba_scan_bwd_softplus.argtypes = lib.mamba_scan_bwd.argtypes
+    lib.mamba_scan_bwd_softplus.restype = ctypes.c_int
+    lib.mamba_scan_bwd_test_timeout.argtypes = lib.mamba_scan_bwd.argtypes
+    lib.mamba_scan_bwd_test_timeout.restype = ctypes.c_int
+    lib.mamba_scan_fwd_bwd.argtypes = [_vp] * 10 + [_sz, _vp, _sz] + [_vp] * 7 + [_i64] * 4 + [_vp]
+    lib.mamba_scan_fwd_bwd.restype = ctypes.c_int
+    lib.mamba_scan_fwd_bwd_bf16.argtypes = lib.mamba_scan_fwd_bwd.argtypes
+    lib.mamba_scan_fwd_bwd_bf16.restype = ctypes.c_int
+    lib.mamba_scan_bwd_noalloc.argtypes = [_vp] * 9 + [_sz] + [_vp] * 7 + [_i64] * 4 + [_vp]
+    lib.mamba_scan_bwd_noalloc.restype = ctypes.c_int
+    lib.mamba_scan_fwd_bwd_host.argtypes = [_vp] * 17 + [_sz] + [_i64] * 4 + [_vp]
+    lib.mamba_scan_fwd_bwd_host.restype = ctypes.c_int
+    lib.mamba_scan_status.argtypes = [_vp]
+    lib.mamba_scan_status.restype = ctypes.c_int
+    lib.mamba_scan_strerror.argtypes = [ctypes.c_int]
+    lib.mamba_scan_strerror.restype = ctypes.c_char_p
+    lib.mamba_scan_last_launch_count.argtypes = []
+    lib.mamba_scan_last_launch_count.restype = ctypes.c_int
+    lib.mamba_scan_bounds_checked.argtypes = []
+    lib.mamba_scan_bounds_checked.restype = ctypes.c_int
+    lib.mamba_scan_test_bounds_shrink.argtypes = [_i64]
+    lib.mamba_scan_test_bounds_shrink.restype = ctypes.c_int
+    return lib
+
+
+_configure(_lib)
 
 
 class MambaScanError(RuntimeError):
@@ -102,6 +117,41 @@ def raw_library() -> ctypes.CDLL:
 
 def mamba_scan_strerror(code: int) -> str:
     return _lib.mamba_scan_strerror(int(code)).decode()
+
+
+CHECKED_LIB_PATH = os.path.join(_HERE, "libmambascan_checked.so")
+
+
+def checked_library() -> ctypes.CDLL:
+    """The ctypes handle of the bounds-checked build (libmambascan_checked.so: the same sources
+    compiled with -DMAMBA_BOUNDS_CHECK, built by ``build.build(checked=True)``), with the same
+    function signatures as the default library."""
+    if not os.path.exists(CHECKED_LIB_PATH):
+        raise ImportError(f"{CHECKED_LIB_PATH} is missing: build it with build.build(checked=True)")
+    return _configure(ctypes.CDLL(CHECKED_LIB_PATH))
+
+
+@contextlib.contextmanager
+def using_library(lib: ctypes.CDLL):
+    """Routes every function of this module through ``lib`` (for instance checked_library())
+    inside the ``with`` block; the default library again afterwards."""
+    global _lib
+    old = _lib
+    _lib = lib
+    try:
+        yield lib
+    finally:
+        _lib = old
+
+
+def mamba_scan_bounds_checked() -> bool:
+    return bool(_lib.mamba_scan_bounds_checked())
+
+
+def mamba_scan_test_bounds_shrink(elements: int) -> None:
+    rc = _lib.mamba_scan_test_bounds_shrink(int(elements))
+    if rc != MAMBA_OK:
+        raise MambaScanError(rc, "mamba_scan_test_bounds_shrink")
 
 
 def mamba_scan_ckpt_bytes(batch: int, T: int, d_inner: int, d_state: int) -> int:

@@ -76,6 +76,12 @@ __device__ __forceinline__ ConvThread conv_thread(const ConvParams& p, int VW) {
 
 __device__ __forceinline__ float silu_f(float p) { return p * sigmoid_fast(p); }
 
+// base + off for a load of n elements; in the bounds-checked build an access outside the first
+// len elements is recorded and redirected to the buffer's first element
+__device__ __forceinline__ const float* at(const float* base, size_t off, size_t n, size_t len) {
+  return inb(off, n, len) ? base + off : base;
+}
+
 // The register windows are rings of K slots indexed by (t - t0) mod K. Steps go in batches of
 // K, so inside a batch every slot index is a compile-time constant and nothing is shifted; the
 // loads of a batch are issued together, ahead of its arithmetic.
@@ -89,11 +95,14 @@ __global__ void __launch_bounds__(256) conv_fwd_kernel(const ConvParams p) {
   float w[K][VW], bias[VW];
 #pragma unroll
   for (int v = 0; v < VW; ++v) {
-    bias[v] = p.bias[c.d0 + v];
+    bias[v] = inb(c.d0 + v, 1, p.Di) ? p.bias[c.d0 + v] : 0.f;
 #pragma unroll
-    for (int j = 0; j < K; ++j) w[j][v] = p.w[(size_t)(c.d0 + v) * K + j];
+    for (int j = 0; j < K; ++j)
+      w[j][v] = inb((size_t)(c.d0 + v) * K + j, 1, (size_t)p.Di * K)
+                    ? p.w[(size_t)(c.d0 + v) * K + j] : 0.f;
   }
   const size_t row = (size_t)c.b * p.T;
+  const size_t nx = (size_t)p.batch * p.T * p.Di;
   const float* __restrict__ xg = p.x;
   float* __restrict__ ug = p.u;
   float ring[K][VW];   // x[t'] at slot (t' - t0) mod K; the K-1 steps before t0 first (0 before t = 0)
@@ -101,7 +110,7 @@ __global__ void __launch_bounds__(256) conv_fwd_kernel(const ConvParams p) {
   for (int s = 1; s < K; ++s) {
     const int ts = c.t0 - K + s;
     if (ts >= 0) {
-      V::unpack(V::load(xg + (row + ts) * p.Di + c.d0), ring[s]);
+      V::unpack(V::load(at(xg, (row + ts) * p.Di + c.d0, VW, nx)), ring[s]);
     } else {
 #pragma unroll
       for (int v = 0; v < VW; ++v) ring[s][v] = 0.f;
@@ -111,7 +120,7 @@ __global__ void __launch_bounds__(256) conv_fwd_kernel(const ConvParams p) {
     float xb[K][VW];
 #pragma unroll
     for (int q = 0; q < K; ++q)   // past the run: a repeated in-range load, unused
-      V::unpack(V::load(xg + (row + min(tb + q, c.t1 - 1)) * p.Di + c.d0), xb[q]);
+      V::unpack(V::load(at(xg, (row + min(tb + q, c.t1 - 1)) * p.Di + c.d0, VW, nx)), xb[q]);
 #pragma unroll
     for (int q = 0; q < K; ++q) {
       const int t = tb + q;
@@ -125,7 +134,7 @@ __global__ void __launch_bounds__(256) conv_fwd_kernel(const ConvParams p) {
         for (int j = 0; j < K; ++j) acc = fmaf(w[j][v], ring[(q + 1 + j) % K][v], acc);
         out[v] = silu_f(acc);
       }
-      if (t < c.t1) V::store(ug + (row + t) * p.Di + c.d0, out);
+      if (t < c.t1 && inb((row + t) * p.Di + c.d0, VW, nx)) V::store(ug + (row + t) * p.Di + c.d0, out);
     }
   }
 }
@@ -156,11 +165,14 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(const ConvParams p) {
   float w[K][VW], bias[VW];
 #pragma unroll
   for (int v = 0; v < VW; ++v) {
-    bias[v] = p.bias[c.d0 + v];
+    bias[v] = inb(c.d0 + v, 1, p.Di) ? p.bias[c.d0 + v] : 0.f;
 #pragma unroll
-    for (int j = 0; j < K; ++j) w[j][v] = p.w[(size_t)(c.d0 + v) * K + j];
+    for (int j = 0; j < K; ++j)
+      w[j][v] = inb((size_t)(c.d0 + v) * K + j, 1, (size_t)p.Di * K)
+                    ? p.w[(size_t)(c.d0 + v) * K + j] : 0.f;
   }
   const size_t row = (size_t)c.b * p.T;
+  const size_t nx = (size_t)p.batch * p.T * p.Di;
   const float* __restrict__ xg = p.x;
   const float* __restrict__ dug = p.d_u;
   float* __restrict__ dxg = p.d_x;
@@ -180,7 +192,7 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(const ConvParams p) {
   for (int s = 1; s < K; ++s) {
     const int ts = c.t0 - K + s;
     if (c.valid && ts >= 0) {
-      V::unpack(V::load(xg + (row + ts) * p.Di + c.d0), xr[s]);
+      V::unpack(V::load(at(xg, (row + ts) * p.Di + c.d0, VW, nx)), xr[s]);
     } else {
 #pragma unroll
       for (int v = 0; v < VW; ++v) xr[s][v] = 0.f;
@@ -193,8 +205,8 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(const ConvParams p) {
 #pragma unroll
     for (int q = 0; q < K; ++q) {   // past the end: a repeated in-range load, unused
       const int t = min(tb + q, t_last);
-      V::unpack(V::load(xg + (row + t) * p.Di + c.d0), xb[q]);
-      V::unpack(V::load(dug + (row + t) * p.Di + c.d0), db[q]);
+      V::unpack(V::load(at(xg, (row + t) * p.Di + c.d0, VW, nx)), xb[q]);
+      V::unpack(V::load(at(dug, (row + t) * p.Di + c.d0, VW, nx)), db[q]);
     }
 #pragma unroll
     for (int q = 0; q < K; ++q) {
@@ -229,7 +241,7 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(const ConvParams p) {
           for (int m = 0; m < K; ++m) acc = fmaf(dr[(q + 1 + m) % K][v], w[K - 1 - m][v], acc);
           dx[v] = acc;
         }
-        V::store(dxg + (row + to) * p.Di + c.d0, dx);
+        if (inb((row + to) * p.Di + c.d0, VW, nx)) V::store(dxg + (row + to) * p.Di + c.d0, dx);
       }
     }
   }
@@ -250,8 +262,13 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(const ConvParams p) {
 #pragma unroll
       for (int r = 0; r < kConvRunsPerCta; ++r) acc += s_red[r][lane][i];
       const int v = i % VW, j = i / VW;
-      if (j < K) p.part_w[(part * p.Di + c.d0 + v) * K + j] = acc;
-      else p.part_b[part * p.Di + c.d0 + v] = acc;
+      const size_t nparts = (size_t)p.batch * p.ngroups;
+      if (j < K) {
+        if (inb((part * p.Di + c.d0 + v) * K + j, 1, nparts * p.Di * K))
+          p.part_w[(part * p.Di + c.d0 + v) * K + j] = acc;
+      } else if (inb(part * p.Di + c.d0 + v, 1, nparts * p.Di)) {
+        p.part_b[part * p.Di + c.d0 + v] = acc;
+      }
     }
   }
 }
@@ -277,7 +294,8 @@ __global__ void conv_reduce_kernel(const ConvParams p) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int k = k0 + 32 * i;
-        v[i] = k < nk ? part[(size_t)k * stride + q] : 0.f;
+        v[i] = (k < nk && inb((size_t)k * stride + q, 1, (size_t)nk * stride))
+                   ? part[(size_t)k * stride + q] : 0.f;
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc += v[i];
@@ -368,5 +386,7 @@ int launch_conv(const ConvParams& p, bool bwd, cudaStream_t s) {
     default: return -1;
   }
 }
+
+MSCAN_OOB_HOOKS(conv)
 
 }  // namespace mscan

@@ -44,6 +44,13 @@ int set_cuda_error(cudaError_t e) {
   return MAMBA_ERR_CUDA;
 }
 
+// the bounds-checked build's fault words of every kernel file, read and cleared (0 in the
+// default build, without any CUDA call)
+unsigned int take_oob() {
+  return mscan::fwd_take_oob() | mscan::bwd_take_oob() | mscan::tmem_take_oob() |
+         mscan::conv_take_oob();
+}
+
 }  // namespace
 
 namespace mscan {
@@ -623,6 +630,7 @@ static int run_channel_slices(const HostLayout& L, char* w, const float* delta, 
   if (e != cudaSuccess) return set_cuda_error(e);
   g_last_launches = launches;
   if (mscan::bwd_take_fault()) return MAMBA_ERR_TIMEOUT;
+  if (take_oob()) return MAMBA_ERR_BOUNDS;
   return MAMBA_OK;
 }
 
@@ -737,6 +745,7 @@ int mamba_scan_fwd_bwd_host(const float* delta, const float* u, const float* B, 
   if (e != cudaSuccess) return set_cuda_error(e);
   g_last_launches = launches;
   if (mscan::bwd_take_fault()) return MAMBA_ERR_TIMEOUT;
+  if (take_oob()) return MAMBA_ERR_BOUNDS;
   return MAMBA_OK;
 }
 
@@ -745,6 +754,25 @@ int mamba_scan_status(void* stream) {
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return set_cuda_error(e);
   if (mscan::bwd_take_fault()) return MAMBA_ERR_TIMEOUT;
+  if (take_oob()) return MAMBA_ERR_BOUNDS;
+  return MAMBA_OK;
+}
+
+int mamba_scan_bounds_checked(void) {
+#ifdef MAMBA_BOUNDS_CHECK
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+int mamba_scan_test_bounds_shrink(int64_t elements) {
+  if (!mamba_scan_bounds_checked()) return MAMBA_ERR_UNSUPPORTED;
+  if (elements < 0) return MAMBA_ERR_INVALID_ARG;
+  const unsigned long long s = (unsigned long long)elements;
+  if (mscan::fwd_set_oob_shrink(s) || mscan::bwd_set_oob_shrink(s) ||
+      mscan::tmem_set_oob_shrink(s) || mscan::conv_set_oob_shrink(s))
+    return set_cuda_error(cudaGetLastError());
   return MAMBA_OK;
 }
 
@@ -761,6 +789,9 @@ const char* mamba_scan_strerror(int code) {
       return "mamba_scan_bwd_noalloc: these sizes need more scratch than the static 64 MiB array";
     case MAMBA_ERR_TIMEOUT:
       return "a kernel gave up waiting for its asynchronous copies; recent outputs are invalid";
+    case MAMBA_ERR_BOUNDS:
+      return "bounds-checked build: a kernel computed an offset outside its buffer (the access "
+             "was not made); recent outputs are invalid";
     default: return "unknown error code";
   }
 }

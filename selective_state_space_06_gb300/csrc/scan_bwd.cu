@@ -69,7 +69,7 @@ __device__ __forceinline__ void bwd_load_chunk(const BwdParams& p, float* st, in
     for (int q = threadIdx.x; q < kChunk * DC / 4; q += NTH) {
       const int i = q / (DC / 4), col = (q % (DC / 4)) * 4;
       const int t = t0 + i, d = dblk0 + col;
-      const bool v = t < p.T && d < p.Di;
+      const bool v = t < p.T && d < p.Di && inb((rowb + t) * p.Di + d, 4, p.n_io());
       const size_t go = v ? (rowb + t) * p.Di + d : 0;
       cp_async16(s_dl + i * DC + col, p.delta + go, v);
       cp_async16(s_u + i * DC + col, p.u + go, v);
@@ -79,7 +79,7 @@ __device__ __forceinline__ void bwd_load_chunk(const BwdParams& p, float* st, in
     for (int q = threadIdx.x; q < kChunk * NP / 4; q += NTH) {
       const int i = q / (NP / 4), n = (q % (NP / 4)) * 4;
       const int t = t0 + i;
-      const bool v = t < p.T && n < p.N;
+      const bool v = t < p.T && n < p.N && inb((rowb + t) * p.N + n, 4, p.n_bc());
       const size_t go = v ? (rowb + t) * p.N + n : 0;
       cp_async16(s_B + i * NP + n, p.B + go, v);
       cp_async16(s_C + i * NP + n, p.C + go, v);
@@ -88,7 +88,7 @@ __device__ __forceinline__ void bwd_load_chunk(const BwdParams& p, float* st, in
     for (int q = threadIdx.x; q < kChunk * DC; q += NTH) {
       const int i = q / DC, col = q % DC;
       const int t = t0 + i, d = dblk0 + col;
-      const bool v = t < p.T && d < p.Di;
+      const bool v = t < p.T && d < p.Di && inb((rowb + t) * p.Di + d, 1, p.n_io());
       const size_t go = v ? (rowb + t) * p.Di + d : 0;
       cp_async4(s_dl + i * DC + col, p.delta + go, v);
       cp_async4(s_u + i * DC + col, p.u + go, v);
@@ -98,29 +98,29 @@ __device__ __forceinline__ void bwd_load_chunk(const BwdParams& p, float* st, in
     for (int q = threadIdx.x; q < kChunk * NP; q += NTH) {
       const int i = q / NP, n = q % NP;
       const int t = t0 + i;
-      const bool v = t < p.T && n < p.N;
+      const bool v = t < p.T && n < p.N && inb((rowb + t) * p.N + n, 1, p.n_bc());
       const size_t go = v ? (rowb + t) * p.N + n : 0;
       cp_async4(s_B + i * NP + n, p.B + go, v);
       cp_async4(s_C + i * NP + n, p.C + go, v);
     }
   }
   stage_tile<DC, NTH, VEC>(s_C + kChunk * NP + DC * NP, p.y_ck, (size_t)b * p.T, t0, p.T, p.Di,
-                           dblk0);
+                           dblk0, p.n_io());
   {
     // state entering chunk c (checkpoint slot c-1); zeros for the first chunk
     float* s_h0 = s_C + kChunk * NP;
     const bool have = c > 0;
-    const float* src = have ? p.ckpt + (((size_t)b * (p.nchunks - 1) + (c - 1)) * p.Di + dblk0) * p.N
-                            : p.ckpt;
+    const size_t src0 = have ? (((size_t)b * (p.nchunks - 1) + (c - 1)) * p.Di + dblk0) * p.N : 0;
+    const float* src = p.ckpt + src0;
     const int rowlen = DC * p.N;
     if constexpr (VEC) {
       for (int q = threadIdx.x * 4; q < rowlen; q += NTH * 4) {
-        const bool v = have && (dblk0 + q / p.N < p.Di);
+        const bool v = have && (dblk0 + q / p.N < p.Di) && inb(src0 + q, 4, p.n_ck());
         cp_async16(s_h0 + q, v ? src + q : p.delta, v);
       }
     } else {
       for (int q = threadIdx.x; q < rowlen; q += NTH) {
-        const bool v = have && (dblk0 + q / p.N < p.Di);
+        const bool v = have && (dblk0 + q / p.N < p.Di) && inb(src0 + q, 1, p.n_ck());
         cp_async4(s_h0 + q, v ? src + q : p.delta, v);
       }
     }
@@ -182,7 +182,8 @@ scan_bwd_agg_kernel(const BwdParams p) {
 #pragma unroll
     for (int k = 0; k < NPT; ++k) {
       const int n = n0 + k;
-      t4[k] = (dv && n < N) ? -expf(p.A_log[(size_t)d * N + n]) * kLog2e : 0.f;
+      t4[k] = (dv && n < N && inb((size_t)d * N + n, 1, (size_t)Di * N))
+                  ? -expf(p.A_log[(size_t)d * N + n]) * kLog2e : 0.f;
     }
 #pragma unroll
     for (int q = 0; q < NPR; ++q) {
@@ -193,10 +194,10 @@ scan_bwd_agg_kernel(const BwdParams p) {
 
   auto load = [&](int stage, int c) {
     float* st = smem + stage * A::kStageFloats;
-    stage_tile<DC, NTH, VEC>(st, p.delta, row0, c * kChunk, T, Di, dblk0);
-    stage_tile<DC, NTH, VEC>(st + kChunk * DC, p.gate, row0, c * kChunk, T, Di, dblk0);
-    stage_tile<DC, NTH, VEC>(st + 2 * kChunk * DC, p.dy, row0, c * kChunk, T, Di, dblk0);
-    stage_tile<NP, NTH, VEC>(st + 3 * kChunk * DC, p.C, row0, c * kChunk, T, N, 0);
+    stage_tile<DC, NTH, VEC>(st, p.delta, row0, c * kChunk, T, Di, dblk0, p.n_io());
+    stage_tile<DC, NTH, VEC>(st + kChunk * DC, p.gate, row0, c * kChunk, T, Di, dblk0, p.n_io());
+    stage_tile<DC, NTH, VEC>(st + 2 * kChunk * DC, p.dy, row0, c * kChunk, T, Di, dblk0, p.n_io());
+    stage_tile<NP, NTH, VEC>(st + 3 * kChunk * DC, p.C, row0, c * kChunk, T, N, 0, p.n_bc());
     cp_async_commit();
   };
 #pragma unroll
@@ -245,8 +246,8 @@ scan_bwd_agg_kernel(const BwdParams p) {
 #pragma unroll
   for (int j = 0; j < kDPT; ++j) {
     const int d = d0 + j;
-    if (d < Di) {
-      const size_t row = ((size_t)b * p.nseg * p.nsub + slot) * Di + d;
+    const size_t row = ((size_t)b * p.nseg * p.nsub + slot) * Di + d;
+    if (d < Di && inb(row, 1, p.n_agg_sd()) && inb(row * N, N, p.n_agg_l())) {
       if (ng == 0) p.agg_sd[row] = sd[j];
       if constexpr (VEC) {
         if (n0 < N) st_pairs<NPR>(p.agg_L + row * N + n0, L[j]);   // N % 4 == 0 here
@@ -272,7 +273,7 @@ __global__ void scan_bwd_compose_kernel(const BwdParams p) {
        e += (size_t)gridDim.x * blockDim.x) {
     const size_t b = e / dn, q = e % dn;
     const size_t d = q / p.N;
-    const float a2 = -expf(p.A_log[q]) * kLog2e;
+    const float a2 = inb(q, 1, dn) ? -expf(p.A_log[q]) * kLog2e : 0.f;
     float carry = 0.f;
     for (int sg = p.nseg - 1; sg >= 1; --sg) {
       const float carry_in = carry;
@@ -284,15 +285,18 @@ __global__ void scan_bwd_compose_kernel(const BwdParams p) {
         for (int k = 0; k < 8; ++k) {
           const int j = j0 - k;
           const size_t row = b * nslot + (size_t)sg * p.nsub + (j >= 0 ? j : 0);
-          Lv[k] = j >= 0 ? p.agg_L[row * dn + q] : 0.f;
-          sv[k] = j >= 0 ? p.agg_sd[row * p.Di + d] : 0.f;
+          const bool in = j >= 0 && inb(row * dn + q, 1, p.n_agg_l()) &&
+                          inb(row * p.Di + d, 1, p.n_agg_sd());
+          Lv[k] = in ? p.agg_L[row * dn + q] : 0.f;
+          sv[k] = in ? p.agg_sd[row * p.Di + d] : 0.f;
         }
 #pragma unroll
         for (int k = 0; k < 8; ++k) carry = fmaf(ex2_sfu(sv[k] * a2), carry, Lv[k]);
       }
-      p.agg_L[(b * nslot + (size_t)sg * p.nsub) * dn + q] = carry_in;
+      const size_t o = (b * nslot + (size_t)sg * p.nsub) * dn + q;
+      if (inb(o, 1, p.n_agg_l())) p.agg_L[o] = carry_in;
     }
-    p.agg_L[(b * nslot) * dn + q] = carry;
+    if (inb((b * nslot) * dn + q, 1, p.n_agg_l())) p.agg_L[(b * nslot) * dn + q] = carry;
   }
 }
 
@@ -346,13 +350,14 @@ scan_bwd_kernel(const BwdParams p) {
   for (int j = 0; j < kDPT; ++j) {
     const int d = d0 + j;
     const bool dv = d < Di;
-    Dd[j] = dv ? p.D[d] : 0.f;
+    Dd[j] = (dv && inb(d, 1, Di)) ? p.D[d] : 0.f;
     dD[j] = 0.f;
     float t4[NPT];
 #pragma unroll
     for (int k = 0; k < NPT; ++k) {
       const int n = n0 + k;
-      t4[k] = (dv && n < N) ? -expf(p.A_log[(size_t)d * N + n]) * kLog2e : 0.f;
+      t4[k] = (dv && n < N && inb((size_t)d * N + n, 1, (size_t)Di * N))
+                  ? -expf(p.A_log[(size_t)d * N + n]) * kLog2e : 0.f;
     }
 #pragma unroll
     for (int q = 0; q < NPR; ++q) {
@@ -384,8 +389,8 @@ scan_bwd_kernel(const BwdParams p) {
 #pragma unroll
     for (int j = 0; j < kDPT; ++j) {
       const int d = d0 + j;
-      if (d >= Di) continue;
       const size_t row = ((size_t)b * p.nseg + sp) * Di + d;
+      if (d >= Di || !inb(row, 1, p.n_agg_sd()) || !inb(row * N, N, p.n_agg_l())) continue;
       const float sd = p.agg_sd[row];
       float2 Lv[NPR];
       if constexpr (VEC) {
@@ -440,8 +445,8 @@ scan_bwd_kernel(const BwdParams p) {
     for (int k = 0; k < kChunk * DC / NTH; ++k) {
       const int e = k * NTH + threadIdx.x;
       const int i = e / DC, col = e % DC;
-      const bool ok = (t0 + i < T) && (dblk0 + col < Di);
       const size_t o = (rowb + t0 + i) * Di + dblk0 + col;
+      const bool ok = (t0 + i < T) && (dblk0 + col < Di) && inb(o, 1, p.n_io());
       const float yv = s_y[e];
       const float g = s_g[e], go = s_dy[e];
       const float s = sigmoid_fast(g);
@@ -587,8 +592,8 @@ scan_bwd_kernel(const BwdParams p) {
           const float uu = s_u[e], dl = s_dl[e], dyj = s_g[e];
           const float Dj = j ? Dd[1] : Dd[0];
           const float sA = vn[2 * r], sB = vn[2 * r + 1];
-          const bool ok = (t < T) && (d < Di);
           const size_t o = (rowb + t) * Di + d;
+          const bool ok = (t < T) && (d < Di) && inb(o, 1, p.n_io());
           const float fac = p.softplus ? s_dy[e] : 1.f;
           st_global_if(p.d_delta + o, fmaf(sA, kLn2, uu * sB) * fac, ok);
           st_global_if(p.d_u + o, fmaf(dyj, Dj, dl * sB), ok);
@@ -606,7 +611,7 @@ scan_bwd_kernel(const BwdParams p) {
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) sum += red[(w * kChunk + i) * 2 * NP + kn];
         const size_t o = (((size_t)blk * p.batch + b) * T + t) * N + n;
-        (kind ? p.partC : p.partB)[o] = sum;
+        if (inb(o, 1, p.n_part_bc())) (kind ? p.partC : p.partB)[o] = sum;
       }
     }
   }
@@ -616,8 +621,8 @@ scan_bwd_kernel(const BwdParams p) {
 #pragma unroll
   for (int j = 0; j < kDPT; ++j) {
     const int d = d0 + j;
-    if (d >= Di) continue;
     const size_t row = ((size_t)b * p.nseg + seg) * Di + d;
+    if (d >= Di || !inb(row, 1, p.n_part_d()) || !inb(row * N, N, p.n_part_a())) continue;
 #pragma unroll
     for (int k = 0; k < NPT; ++k) {
       const float2 aa = a2[j][k >> 1], ac = accA[j][k >> 1];
@@ -639,6 +644,7 @@ __global__ void scan_reduce_kernel(const BwdParams p) {
     if (e < btn) {
       float sb = 0.f, sc = 0.f;
       for (int k = 0; k < p.nblk; ++k) {
+        if (!inb((size_t)k * btn + e, 1, p.n_part_bc())) break;
         sb += p.partB[(size_t)k * btn + e];
         sc += p.partC[(size_t)k * btn + e];
       }
@@ -653,12 +659,14 @@ __global__ void scan_reduce_kernel(const BwdParams p) {
     } else if (e < btn + dn) {
       const size_t q = e - btn;
       float sa = 0.f;
-      for (int k = 0; k < p.batch * p.nseg; ++k) sa += p.partA[(size_t)k * dn + q];
+      for (int k = 0; k < p.batch * p.nseg; ++k)
+        if (inb((size_t)k * dn + q, 1, p.n_part_a())) sa += p.partA[(size_t)k * dn + q];
       p.d_A_log[q] = sa;
     } else {
       const size_t q = e - btn - dn;
       float sd = 0.f;
-      for (int k = 0; k < p.batch * p.nseg; ++k) sd += p.partD[(size_t)k * p.Di + q];
+      for (int k = 0; k < p.batch * p.nseg; ++k)
+        if (inb((size_t)k * p.Di + q, 1, p.n_part_d())) sd += p.partD[(size_t)k * p.Di + q];
       p.d_D[q] = sd;
     }
   }
@@ -761,5 +769,7 @@ int launch_bwd(const Plan& plan, const BwdParams& p, cudaStream_t s) {
     return -1;
   return cudaPeekAtLastError() == cudaSuccess ? n + 1 : -1;
 }
+
+MSCAN_OOB_HOOKS(bwd)
 
 }  // namespace mscan

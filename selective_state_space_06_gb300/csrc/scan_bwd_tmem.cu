@@ -15,7 +15,12 @@
 //   1. forward recompute of the chunk from its checkpoint. The state before every step goes
 //      to tensor memory: 16 steps x 16 floats = 256 columns per thread lane;
 //   2. reverse walk: the state before the step comes back from tensor memory; the state after
-//      it is the one read for the later step. No step is recomputed twice.
+//      it is the one read for the later step. No step is recomputed twice. A step's d_delta
+//      and d_u go into its (then dead) rows of the delta and u tiles, and the whole chunk is
+//      stored as coalesced rows after the walk.
+// When the y tile is free after the gating step (d_state 32 and 64, unfused), the gating step
+// also leaves delta*u there, so the recompute and the reverse walk load it instead of forming
+// it per step.
 // Variants (template flags): SP takes the raw delta and applies the softplus in shared memory;
 // FY (the fused forward + backward call) forms y = sum_n C*h + D*u during step 1 and runs step
 // 0's gating after it, writing out as well; BF (FY with bf16 I/O) receives its tiles as bf16
@@ -118,29 +123,31 @@ __device__ __forceinline__ void bwd_tmem_load_chunk(const BwdMaps& maps, const B
     }
   } else {
     const size_t row0 = (size_t)b * p.T;
-    stage_tile<DC, NTH, VEC>(st, p.delta, row0, t0, p.T, p.Di, dblk0);
-    stage_tile<DC, NTH, VEC>(st + TILE, p.u, row0, t0, p.T, p.Di, dblk0);
-    stage_tile<DC, NTH, VEC>(st + 2 * TILE, p.gate, row0, t0, p.T, p.Di, dblk0);
-    stage_tile<DC, NTH, VEC>(st + 3 * TILE, p.dy, row0, t0, p.T, p.Di, dblk0);
-    if constexpr (!FY) stage_tile<DC, NTH, VEC>(st + 4 * TILE, p.y_ck, row0, t0, p.T, p.Di, dblk0);
-    stage_tile<NP, NTH, VEC>(st + 5 * TILE, p.B, row0, t0, p.T, p.N, 0);
-    stage_tile<NP, NTH, VEC>(st + 5 * TILE + kChunk * NP, p.C, row0, t0, p.T, p.N, 0);
+    const size_t nio = p.n_io(), nbc = p.n_bc();
+    stage_tile<DC, NTH, VEC>(st, p.delta, row0, t0, p.T, p.Di, dblk0, nio);
+    stage_tile<DC, NTH, VEC>(st + TILE, p.u, row0, t0, p.T, p.Di, dblk0, nio);
+    stage_tile<DC, NTH, VEC>(st + 2 * TILE, p.gate, row0, t0, p.T, p.Di, dblk0, nio);
+    stage_tile<DC, NTH, VEC>(st + 3 * TILE, p.dy, row0, t0, p.T, p.Di, dblk0, nio);
+    if constexpr (!FY)
+      stage_tile<DC, NTH, VEC>(st + 4 * TILE, p.y_ck, row0, t0, p.T, p.Di, dblk0, nio);
+    stage_tile<NP, NTH, VEC>(st + 5 * TILE, p.B, row0, t0, p.T, p.N, 0, nbc);
+    stage_tile<NP, NTH, VEC>(st + 5 * TILE + kChunk * NP, p.C, row0, t0, p.T, p.N, 0, nbc);
     // state entering chunk c (checkpoint slot c-1), rows of N states at a stride of NP;
     // zeros for the first chunk and for channels past d_inner
     const bool have = c > 0;
-    const float* src =
-        have ? p.ckpt + (((size_t)b * (p.nchunks - 1) + (c - 1)) * p.Di + dblk0) * p.N : p.ckpt;
+    const size_t src0 = have ? (((size_t)b * (p.nchunks - 1) + (c - 1)) * p.Di + dblk0) * p.N : 0;
+    const float* src = p.ckpt + src0;
     const int rowlen = DC * p.N;
     if constexpr (VEC) {
       for (int q = threadIdx.x * 4; q < rowlen; q += NTH * 4) {
         const int row = q / p.N, col = q % p.N;
-        const bool v = have && (dblk0 + row < p.Di);
+        const bool v = have && (dblk0 + row < p.Di) && inb(src0 + q, 4, p.n_ck());
         cp_async16(s_h0 + row * NP + col, v ? src + q : p.delta, v);
       }
     } else {
       for (int q = threadIdx.x; q < rowlen; q += NTH) {
         const int row = q / p.N, col = q % p.N;
-        const bool v = have && (dblk0 + row < p.Di);
+        const bool v = have && (dblk0 + row < p.Di) && inb(src0 + q, 1, p.n_ck());
         cp_async4(s_h0 + row * NP + col, v ? src + q : p.delta, v);
       }
     }
@@ -176,6 +183,14 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
   // lanes read their B and C pairs straight from the stage and splat them in registers: half
   // the shared-memory bytes of a duplicated {B, B} copy, and no copy to write.
   constexpr bool DBC = !S::SWAP && !BF;
+  // delta*u formed once per element by the gating step, into the y tile (free after it unless
+  // it holds the warps' d_B / d_C rows, or the fused call forms y there)
+  constexpr bool DU = !FY && !S::RED_ALIAS;
+  // d_delta / d_u staged in shared memory and stored as whole rows after the walk (below) at
+  // d_state 32 and 64. At d_state 16 a CTA covers 128 channels, and writing its staged chunk
+  // out after the walk measured slower (404 against 397 us at mamba370m) than one predicated
+  // store per lane and step, which the walk hides among its arithmetic.
+  constexpr bool STAGE = DC <= 64;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ uint32_t s_tmem;
   float* smem = reinterpret_cast<float*>(
@@ -234,7 +249,7 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
   const int wsel = lane & (G / 4 - 1);
   const bool w_delta = wsel == 0;
   const bool w_u = (G == 4) ? true : wsel == 1;
-  const float D_out = d_out < Di ? p.D[d_out] : 0.f;
+  const float D_out = (d_out < Di && inb(d_out, 1, Di)) ? p.D[d_out] : 0.f;
   float dD_out = 0.f;
 
   float2 a2[2][4], dh[2][4], accA[2][4];
@@ -247,7 +262,8 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const int d = d0 + chan(q, k);
-        v[k] = (d < Di && n < N) ? -expf(p.A_log[(size_t)d * N + n]) * kLog2e : 0.f;
+        v[k] = (d < Di && n < N && inb((size_t)d * N + n, 1, (size_t)Di * N))
+                   ? -expf(p.A_log[(size_t)d * N + n]) * kLog2e : 0.f;
       }
       a2[q][s] = make_float2(v[0], v[1]);
       dh[q][s] = accA[q][s] = make_float2(0.f, 0.f);
@@ -265,7 +281,8 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
           const int d = d0 + chan(q, k);
-          L[k] = (d < Di && n < N) ? p.agg_L[(rowbase + d) * N + n] : 0.f;
+          L[k] = (d < Di && n < N && inb((rowbase + d) * N + n, 1, p.n_agg_l()))
+                     ? p.agg_L[(rowbase + d) * N + n] : 0.f;
         }
         dh[q][s] = make_float2(L[0], L[1]);
       }
@@ -349,7 +366,8 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
         for (int k = 0; k < TILE / (4 * NTH); ++k) {
           const int e = 4 * (k * NTH + threadIdx.x);
           const int i = e / DC, col = e % DC;
-          const bool ok = (t0 + i < T) && (dblk0 + col < Di);
+          const bool ok = (t0 + i < T) && (dblk0 + col < Di) &&
+                          inb((rowb + t0 + i) * Di + dblk0 + col, 4, p.n_io());
           const float4 yv = *reinterpret_cast<const float4*>(s_y + e);
           float4 g, go;
           if constexpr (BF) {   // 4 bf16 of gate and of dy from the halves of the gate slot
@@ -394,6 +412,12 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
 #pragma unroll
             for (int k4 = 0; k4 < 4; ++k4) softplus_both(dl[k4], dl[k4], fac[k4]);
           }
+          if constexpr (DU) {   // delta*u over the y values just read (this thread's own)
+            const float4 d4 = *reinterpret_cast<const float4*>(s_dl + e);
+            const float4 u4 = *reinterpret_cast<const float4*>(s_u + e);
+            *reinterpret_cast<float4*>(s_y + e) =
+                make_float4(d4.x * u4.x, d4.y * u4.y, d4.z * u4.z, d4.w * u4.w);
+          }
         }
       } else {
         static_assert(TILE % NTH == 0, "tile must split evenly over the CTA");
@@ -401,8 +425,8 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
         for (int k = 0; k < TILE / NTH; ++k) {
           const int e = k * NTH + threadIdx.x;
           const int i = e / DC, col = e % DC;
-          const bool ok = (t0 + i < T) && (dblk0 + col < Di);
           const size_t o = (rowb + t0 + i) * Di + dblk0 + col;
+          const bool ok = (t0 + i < T) && (dblk0 + col < Di) && inb(o, 1, p.n_io());
           const float yv = s_y[e];
           const float g = s_g[e], go = s_dy[e];
           const float sg = sigmoid_fast(g);
@@ -412,6 +436,7 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
           if (SP && ok) {   // raw -> delta, and the factor d_raw / d_delta
             softplus_both(s_dl[e], const_cast<float*>(s_dl)[e], const_cast<float*>(s_dy)[e]);
           }
+          if constexpr (DU) s_y[e] = s_dl[e] * s_u[e];
         }
       }
     };
@@ -457,6 +482,8 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
     const float* s_dyv = BF ? s_dy : s_g;   // d_y
     const float2* pdy[2] = {reinterpret_cast<const float2*>(s_dyv + offc[0]),
                             reinterpret_cast<const float2*>(s_dyv + offc[1])};
+    const float2* pdu[2] = {reinterpret_cast<const float2*>(s_y + offc[0]),
+                            reinterpret_cast<const float2*>(s_y + offc[1])};
 #pragma unroll
     for (int i = 0; i < kChunk; ++i) {
       step_fence();
@@ -465,8 +492,12 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         dl2[q] = pdl[q][i * DC / 2];
-        u2[q] = pu[q][i * DC / 2];
-        du2[q] = mul2(dl2[q], u2[q]);
+        if constexpr (DU) {
+          du2[q] = pdu[q][i * DC / 2];
+        } else {
+          u2[q] = pu[q][i * DC / 2];
+          du2[q] = mul2(dl2[q], u2[q]);
+        }
       }
 #pragma unroll
       for (int pp = 0; pp < 2; ++pp) {
@@ -510,8 +541,8 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
         }
         // same reduce-scatter as the d_delta sums: level G/2 over the channel pairs, level G/4
         // inside the pair, then the remaining state lanes
-        ya[0] = make_float2(ya[0].x + __shfl_xor_sync(kFull, ya[1].x, G / 2),
-                            ya[0].y + __shfl_xor_sync(kFull, ya[1].y, G / 2));
+        ya[0] = add2(ya[0], make_float2(__shfl_xor_sync(kFull, ya[1].x, G / 2),
+                                        __shfl_xor_sync(kFull, ya[1].y, G / 2)));
         float yv = (mx ? ya[0].y : ya[0].x) +
                    __shfl_xor_sync(kFull, mx ? ya[0].x : ya[0].y, G / 4);
 #pragma unroll
@@ -527,11 +558,22 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
     }
 
     // ---- 2. reverse walk (Phase B3) ------------------------------------------------------
-    // output rows of this chunk for the lane's channel; rows at or past T are not stored
-    float* const out_dd = p.d_delta + (rowb + t0) * Di + d_out;
-    float* const out_du = p.d_u + (rowb + t0) * Di + d_out;
-    const int lim_dd = (w_delta && d_out < Di) ? T - t0 : 0;
-    const int lim_du = (w_u && d_out < Di) ? T - t0 : 0;
+    // The lane's d_delta and d_u of step i overwrite row i of the delta tile and of the d_y
+    // tile. d_delta is a sum over the state lanes of terms formed from each lane's delta of the
+    // step, and d_u one of terms formed from each lane's d_y, so neither store can issue before
+    // every lane's loads of the row it overwrites have returned; no later step reads row i.
+    // The stores of step i are issued in step i-1, behind that step's shared-memory loads:
+    // shared-memory accesses of a warp are served in order, and a store issued at the end of
+    // its own step would hold the next step's loads behind the step's reductions.
+    float* const row_dd = const_cast<float*>(s_dl) + cl + j_out;
+    float* const row_du = const_cast<float*>(s_dyv) + cl + j_out;
+    const float* const row_u = s_u + cl + j_out;
+    float pend_dd = 0.f, pend_du = 0.f;   // the previous step's d_delta and d_u
+    // without staging: this lane's output rows of the chunk; rows at or past T are not stored
+    const size_t o_row = (rowb + t0) * Di + d_out;
+    const bool o_ok = d_out < Di && inb((rowb + min(T, t0 + kChunk) - 1) * Di + d_out, 1, p.n_io());
+    const int lim_dd = (w_delta && o_ok) ? T - t0 : 0;
+    const int lim_du = (w_u && o_ok) ? T - t0 : 0;
 #pragma unroll 4
     for (int ii = 0; ii < kChunk; ++ii) {
       const int i = kChunk - 1 - ii;
@@ -542,9 +584,13 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         dl2[q] = pdl[q][i * DC / 2];
-        u2[q] = pu[q][i * DC / 2];
         dy2[q] = pdy[q][i * DC / 2];
-        du2[q] = mul2(dl2[q], u2[q]);
+        if constexpr (DU) {
+          du2[q] = pdu[q][i * DC / 2];
+        } else {
+          u2[q] = pu[q][i * DC / 2];
+          du2[q] = mul2(dl2[q], u2[q]);
+        }
       }
 #pragma unroll
       for (int pp = 0; pp < 2; ++pp) {
@@ -563,6 +609,10 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
           C2[2 * pp] = make_float2(vc.x, vc.y);
           C2[2 * pp + 1] = make_float2(vc.z, vc.w);
         }
+      }
+      if constexpr (STAGE) {   // (row i + 1: for ii = 0 the predicate is off, nothing accessed)
+        st_shared_if(row_dd + (i + 1) * DC, pend_dd, w_delta && ii > 0);
+        st_shared_if(row_du + (i + 1) * DC, pend_du, w_u && ii > 0);
       }
       tmem_wait_ld(reinterpret_cast<float2(&)[8]>(hp));
       float2 sa2[2], sb2[2], xb2[4], xc2[4];
@@ -614,10 +664,10 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
         *reinterpret_cast<float2*>(rrow + NP) = make_float2(v[4], v[5]);
       }
       // sums over n: level G/2 over the channel pairs (lanes with that bit hold them swapped)
-      sa2[0] = make_float2(sa2[0].x + __shfl_xor_sync(kFull, sa2[1].x, G / 2),
-                           sa2[0].y + __shfl_xor_sync(kFull, sa2[1].y, G / 2));
-      sb2[0] = make_float2(sb2[0].x + __shfl_xor_sync(kFull, sb2[1].x, G / 2),
-                           sb2[0].y + __shfl_xor_sync(kFull, sb2[1].y, G / 2));
+      sa2[0] = add2(sa2[0], make_float2(__shfl_xor_sync(kFull, sa2[1].x, G / 2),
+                                        __shfl_xor_sync(kFull, sa2[1].y, G / 2)));
+      sb2[0] = add2(sb2[0], make_float2(__shfl_xor_sync(kFull, sb2[1].x, G / 2),
+                                        __shfl_xor_sync(kFull, sb2[1].y, G / 2)));
       // level G/4: inside the pair, with selects
       float sA = (mx ? sa2[0].y : sa2[0].x) +
                  __shfl_xor_sync(kFull, mx ? sa2[0].x : sa2[0].y, G / 4);
@@ -629,21 +679,26 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
         sB += __shfl_xor_sync(kFull, sB, m);
       }
       {
-        const float uo = mx ? u2[0].y : u2[0].x;
+        float uo;
+        if constexpr (DU) uo = row_u[i * DC];
+        else uo = mx ? u2[0].y : u2[0].x;
         const float dlo = mx ? dl2[0].y : dl2[0].x;
         const float dyo = mx ? dy2[0].y : dy2[0].x;
         dD_out = fmaf(dyo, uo, dD_out);
-        const size_t o = (size_t)i * Di;
         float ddo = fmaf(sA, kLn2, uo * sB);
         if constexpr (SP) ddo *= s_dy[i * DC + cl + j_out];   // d_raw = d_delta * softplus'
-        if constexpr (BF) {
-          st_global_bf16_lt(reinterpret_cast<uint16_t*>(p.d_delta) + (rowb + t0) * Di + d_out + o,
-                            ddo, i, lim_dd);
-          st_global_bf16_lt(reinterpret_cast<uint16_t*>(p.d_u) + (rowb + t0) * Di + d_out + o,
-                            fmaf(dyo, D_out, dlo * sB), i, lim_du);
+        const float duo = fmaf(dyo, D_out, dlo * sB);
+        if constexpr (STAGE) {
+          pend_dd = ddo;
+          pend_du = duo;
+        } else if constexpr (BF) {
+          uint16_t* const o16 = reinterpret_cast<uint16_t*>(p.d_delta) + o_row + (size_t)i * Di;
+          st_global_bf16_lt(o16, ddo, i, lim_dd);
+          st_global_bf16_lt(reinterpret_cast<uint16_t*>(p.d_u) + o_row + (size_t)i * Di, duo, i,
+                            lim_du);
         } else {
-          st_global_lt(out_dd + o, ddo, i, lim_dd);
-          st_global_lt(out_du + o, fmaf(dyo, D_out, dlo * sB), i, lim_du);
+          st_global_lt(p.d_delta + o_row + (size_t)i * Di, ddo, i, lim_dd);
+          st_global_lt(p.d_u + o_row + (size_t)i * Di, duo, i, lim_du);
         }
       }
 #pragma unroll
@@ -651,7 +706,39 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
 #pragma unroll
         for (int s = 0; s < 4; ++s) h[q][s] = hp[q][s];
     }
+    if constexpr (STAGE) {
+      st_shared_if(row_dd, pend_dd, w_delta);   // step 0
+      st_shared_if(row_du, pend_du, w_u);
+    }
     __syncthreads();
+    // d_delta and d_u of the chunk, out of the tiles the walk left them in, as whole rows
+    const float* const s_duo = s_dyv;
+    if constexpr (!STAGE) {
+    } else if constexpr (VEC) {   // four consecutive channels at a time (all inside d_inner or none)
+#pragma unroll
+      for (int k = 0; k < TILE / (4 * NTH); ++k) {
+        const int e = 4 * (k * NTH + threadIdx.x);
+        const int i = e / DC, col = e % DC;
+        const size_t o = (rowb + t0 + i) * Di + dblk0 + col;
+        const bool ok = (t0 + i < T) && (dblk0 + col < Di) && inb(o, 4, p.n_io());
+        const float4 vd = lds4(s_dl + e), vu = lds4(s_duo + e);
+        if constexpr (BF) {
+          st_global_bf16x4_if(reinterpret_cast<uint16_t*>(p.d_delta) + o, vd, ok);
+          st_global_bf16x4_if(reinterpret_cast<uint16_t*>(p.d_u) + o, vu, ok);
+        } else {
+          st_global4_if(p.d_delta + o, vd, ok);
+          st_global4_if(p.d_u + o, vu, ok);
+        }
+      }
+    } else {
+      for (int e = threadIdx.x; e < TILE; e += NTH) {
+        const int i = e / DC, col = e % DC;
+        const size_t o = (rowb + t0 + i) * Di + dblk0 + col;
+        const bool ok = (t0 + i < T) && (dblk0 + col < Di) && inb(o, 1, p.n_io());
+        st_global_if(p.d_delta + o, s_dl[e], ok);
+        st_global_if(p.d_u + o, s_duo[e], ok);
+      }
+    }
     // CTA partial of d_B / d_C for this chunk: fixed-order sum over the warps
     if constexpr (VEC) {   // four consecutive states at a time (d_state % 4 == 0)
       for (int e = 4 * threadIdx.x; e < kChunk * 2 * NP; e += 4 * NTH) {
@@ -665,7 +752,8 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
           sum = make_float4(sum.x + v.x, sum.y + v.y, sum.z + v.z, sum.w + v.w);
         }
         const size_t o = (((size_t)blk * p.batch + b) * T + t) * N + n;
-        st_global4_if((kind ? p.partC : p.partB) + o, sum, t < T && n < N);
+        st_global4_if((kind ? p.partC : p.partB) + o, sum,
+                      t < T && n < N && inb(o, 4, p.n_part_bc()));
       }
     } else {
       for (int e = threadIdx.x; e < kChunk * 2 * NP; e += NTH) {
@@ -677,7 +765,7 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
 #pragma unroll
           for (int w = 0; w < kWarps; ++w) sum += red[(w * kChunk + i) * 2 * NP + kn];
           const size_t o = (((size_t)blk * p.batch + b) * T + t) * N + n;
-          (kind ? p.partC : p.partB)[o] = sum;
+          if (inb(o, 1, p.n_part_bc())) (kind ? p.partC : p.partB)[o] = sum;
         }
       }
     }
@@ -700,10 +788,12 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
           const int d = d0 + chan(q, k);
           const float aa = k ? a2[q][s].y : a2[q][s].x;
           const float ac = k ? accA[q][s].y : accA[q][s].x;
-          if (d < Di && n < N) p.partA[(rowbase + d) * N + n] = kLn2 * aa * ac;
+          if (d < Di && n < N && inb((rowbase + d) * N + n, 1, p.n_part_a()))
+            p.partA[(rowbase + d) * N + n] = kLn2 * aa * ac;
         }
       }
-    if (w_delta && d_out < Di) p.partD[rowbase + d_out] = dD_out;
+    if (w_delta && d_out < Di && inb(rowbase + d_out, 1, p.n_part_d()))
+      p.partD[rowbase + d_out] = dD_out;
   }
 
   tmem_fence_before_sync();
@@ -768,10 +858,10 @@ scan_bwd_agg4_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
         tma_load_3d(st + 3 * TILE, &maps.C, bar, 0, c * kChunk, b);
       }
     } else {
-      stage_tile<DC, NTH, VEC>(st, p.delta, row0, c * kChunk, T, Di, dblk0);
-      stage_tile<DC, NTH, VEC>(st + TILE, p.gate, row0, c * kChunk, T, Di, dblk0);
-      stage_tile<DC, NTH, VEC>(st + 2 * TILE, p.dy, row0, c * kChunk, T, Di, dblk0);
-      stage_tile<NP, NTH, VEC>(st + 3 * TILE, p.C, row0, c * kChunk, T, N, 0);
+      stage_tile<DC, NTH, VEC>(st, p.delta, row0, c * kChunk, T, Di, dblk0, p.n_io());
+      stage_tile<DC, NTH, VEC>(st + TILE, p.gate, row0, c * kChunk, T, Di, dblk0, p.n_io());
+      stage_tile<DC, NTH, VEC>(st + 2 * TILE, p.dy, row0, c * kChunk, T, Di, dblk0, p.n_io());
+      stage_tile<NP, NTH, VEC>(st + 3 * TILE, p.C, row0, c * kChunk, T, N, 0, p.n_bc());
       cp_async_commit();
     }
   };
@@ -801,7 +891,8 @@ scan_bwd_agg4_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const int d = d0 + 2 * q + k;
-        v[k] = (d < Di && n < N) ? -expf(p.A_log[(size_t)d * N + n]) * kLog2e : 0.f;
+        v[k] = (d < Di && n < N && inb((size_t)d * N + n, 1, (size_t)Di * N))
+                   ? -expf(p.A_log[(size_t)d * N + n]) * kLog2e : 0.f;
       }
       a2[q][s] = make_float2(v[0], v[1]);
       L[q][s] = make_float2(0.f, 0.f);
@@ -888,7 +979,8 @@ scan_bwd_agg4_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
       const int d = d0 + 2 * q + k;
-      if (d >= Di) continue;
+      if (d >= Di || !inb(rowbase + d, 1, p.n_agg_sd()) || !inb((rowbase + d) * N, N, p.n_agg_l()))
+        continue;
       if (ng == 0) p.agg_sd[rowbase + d] = k ? P2[q].y : P2[q].x;
       float v[4];
 #pragma unroll
@@ -1081,5 +1173,7 @@ int launch_bwd_main_tmem(const Plan& plan, const BwdParams& p, cudaStream_t s) {
     default: return -1;
   }
 }
+
+MSCAN_OOB_HOOKS(tmem)
 
 }  // namespace mscan

@@ -12,6 +12,46 @@ constexpr float kLog2e = 1.4426950408889634f;  // log2(e)
 constexpr float kLn2 = 0.6931471805599453f;    // ln(2)
 constexpr unsigned kFull = 0xffffffffu;
 
+// ---- bounds-checked builds -------------------------------------------------------------------
+// Built with -DMAMBA_BOUNDS_CHECK, every global access whose offset a kernel computes is first
+// checked against the length of its buffer (elements, from the sizes the launch carries). An
+// access outside is not made: a load reads zero, a store is dropped, and the translation
+// unit's fault word records it (mamba_scan_status then reports MAMBA_ERR_BOUNDS). The test hook
+// g_oob_shrink takes every length that many elements smaller, so a test can watch the check
+// fire on the last elements of each buffer while every access it blocks is still in bounds.
+// Without the macro inb() is the constant true and every check compiles away.
+#ifdef MAMBA_BOUNDS_CHECK
+static __device__ unsigned int g_oob;
+static __device__ unsigned long long g_oob_shrink;
+// elements [off, off + n) lie inside the first len - shrink elements
+__device__ __forceinline__ bool inb(size_t off, size_t n, size_t len) {
+  const size_t s = (size_t)g_oob_shrink;
+  if (off + n <= len && len - (off + n) >= s) return true;
+  atomicOr(&g_oob, 1u);
+  return false;
+}
+// host side of this translation unit's fault word: name##_take_oob() returns it and clears it,
+// name##_set_oob_shrink() sets the test hook
+#define MSCAN_OOB_HOOKS(name)                                                       \
+  unsigned int name##_take_oob() {                                                  \
+    unsigned int v = 0;                                                             \
+    if (cudaMemcpyFromSymbol(&v, g_oob, sizeof(v)) != cudaSuccess) return 0;        \
+    if (v) {                                                                        \
+      const unsigned int zero = 0;                                                  \
+      cudaMemcpyToSymbol(g_oob, &zero, sizeof(zero));                               \
+    }                                                                               \
+    return v;                                                                       \
+  }                                                                                 \
+  int name##_set_oob_shrink(unsigned long long s) {                                 \
+    return cudaMemcpyToSymbol(g_oob_shrink, &s, sizeof(s)) == cudaSuccess ? 0 : -1; \
+  }
+#else
+__device__ __forceinline__ constexpr bool inb(size_t, size_t, size_t) { return true; }
+#define MSCAN_OOB_HOOKS(name)                                      \
+  unsigned int name##_take_oob() { return 0; }                     \
+  int name##_set_oob_shrink(unsigned long long) { return -1; }
+#endif
+
 
 // 2^x on the special-function unit (PTX ex2.approx.ftz.f32). In the scan x <= 0, so the result
 // lies in [0, 1]; very negative x flushes to 0.
@@ -34,6 +74,7 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
 // Packed fp32x2 arithmetic (one issue slot for two lanes of work on sm_100+).
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
 __device__ __forceinline__ float2 splat2(float v) { return make_float2(v, v); }
 __device__ __forceinline__ float2 ex2_2(float2 x) { return make_float2(ex2_sfu(x.x), ex2_sfu(x.y)); }
 
@@ -203,20 +244,23 @@ __device__ __forceinline__ void cp_async_wait() {
 // Stages rows t0 .. t0+kChunk-1 of a row-major [.., T, W] tensor, columns col0 .. col0+TW-1,
 // into a [kChunk][TW] shared tile with cp.async; rows past T and columns past W become zeros.
 // VEC needs W % 4 == 0 and col0 % 4 == 0 (then every 16-byte piece is inside or outside W).
+// len: elements of src (the bounds-checked build checks every copy against it).
 template <int TW, int NTH, bool VEC>
 __device__ __forceinline__ void stage_tile(float* dst, const float* src, size_t row0, int t0,
-                                           int T, int W, int col0) {
+                                           int T, int W, int col0, size_t len) {
   if constexpr (VEC) {
     for (int q = threadIdx.x; q < kChunk * TW / 4; q += NTH) {
       const int i = q / (TW / 4), col = (q % (TW / 4)) * 4;
-      const bool v = (t0 + i < T) && (col0 + col < W);
-      cp_async16(dst + i * TW + col, v ? src + (row0 + t0 + i) * W + col0 + col : src, v);
+      const size_t off = (row0 + t0 + i) * W + col0 + col;
+      const bool v = (t0 + i < T) && (col0 + col < W) && inb(off, 4, len);
+      cp_async16(dst + i * TW + col, v ? src + off : src, v);
     }
   } else {
     for (int q = threadIdx.x; q < kChunk * TW; q += NTH) {
       const int i = q / TW, col = q % TW;
-      const bool v = (t0 + i < T) && (col0 + col < W);
-      cp_async4(dst + i * TW + col, v ? src + (row0 + t0 + i) * W + col0 + col : src, v);
+      const size_t off = (row0 + t0 + i) * W + col0 + col;
+      const bool v = (t0 + i < T) && (col0 + col < W) && inb(off, 1, len);
+      cp_async4(dst + i * TW + col, v ? src + off : src, v);
     }
   }
 }
@@ -441,13 +485,14 @@ __device__ __forceinline__ void st_global_bf16x4_if(uint16_t* p, float4 v, bool 
 // first half of the fp32 slot dst, 8 elements per copy (TW and W multiples of 8).
 template <int TW, int NTH>
 __device__ __forceinline__ void stage_tile_bf16(float* dst, const uint16_t* src, size_t row0,
-                                                int t0, int T, int W, int col0) {
+                                                int t0, int T, int W, int col0, size_t len) {
   static_assert(TW % 8 == 0, "bf16 tiles move in 16-byte groups");
   uint16_t* d16 = reinterpret_cast<uint16_t*>(dst);
   for (int q = threadIdx.x; q < kChunk * TW / 8; q += NTH) {
     const int i = q / (TW / 8), col = (q % (TW / 8)) * 8;
-    const bool v = (t0 + i < T) && (col0 + col < W);
-    cp_async16(d16 + i * TW + col, v ? src + (row0 + t0 + i) * W + col0 + col : src, v);
+    const size_t off = (row0 + t0 + i) * W + col0 + col;
+    const bool v = (t0 + i < T) && (col0 + col < W) && inb(off, 8, len);
+    cp_async16(d16 + i * TW + col, v ? src + off : src, v);
   }
 }
 

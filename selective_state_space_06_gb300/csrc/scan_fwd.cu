@@ -12,7 +12,9 @@
 //   lane = dg * G + ng :  ng picks the states [NPT*ng, NPT*ng+NPT), and dg picks the DPT
 //                         channels [DPT*dg, DPT*dg+DPT) of the warp's DPT*(32/G) channels.
 // A thread keeps DPT channels (2, or 4 at d_state 64) x NPT states in registers as float2 pairs
-// of states and updates them with packed fp32x2 FMAs.
+// of channels, x[q][s] = (channel 2q, channel 2q+1) of state s, and updates them with packed
+// fp32x2 FMAs: the per-channel delta*u and the sums over n then come out as channel pairs with
+// no scalar multiply or horizontal add.
 //
 // Staging. Each chunk's tiles (delta, u and gate [kChunk][DC]; B and C [kChunk][NP]) go
 // global -> shared with cp.async, STAGES chunks ahead of the compute. Rows past T and channels
@@ -49,6 +51,58 @@ __device__ __forceinline__ void lds_chan(const float* p, float (&v)[DPT]) {
   }
 }
 
+// The NPT/2 state pairs of channel k (0 or 1) of a channel pair x[s], s < NPT, for the row
+// stores (checkpoints, aggregates) whose rows hold one channel's states.
+template <int NPT>
+__device__ __forceinline__ void chan_states(const float2 (&x)[NPT], int k, float2 (&out)[NPT / 2]) {
+#pragma unroll
+  for (int pp = 0; pp < NPT / 2; ++pp)
+    out[pp] = k ? make_float2(x[2 * pp].y, x[2 * pp + 1].y) : make_float2(x[2 * pp].x, x[2 * pp + 1].x);
+}
+
+// element s of a float2 pair array (s compile-time)
+__device__ __forceinline__ float pair_el(const float2* v, int s) {
+  return (s & 1) ? v[s >> 1].y : v[s >> 1].x;
+}
+
+// a2[q][s] = A[d, n] * log2(e) = -exp(A_log[d, n]) * log2(e) for the channels d0 + 2q,
+// d0 + 2q + 1 and the states n0 + s; zero outside d_inner x d_state (a no-op decay there).
+template <int DP, int NPT>
+__device__ __forceinline__ void load_a2(const FwdParams& p, int d0, int n0,
+                                        float2 (&a2)[DP][NPT]) {
+  const int Di = p.Di, N = p.N;
+#pragma unroll
+  for (int q = 0; q < DP; ++q)
+#pragma unroll
+    for (int s = 0; s < NPT; ++s) {
+      float v[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int d = d0 + 2 * q + k, n = n0 + s;
+        v[k] = (d < Di && n < N && inb((size_t)d * N + n, 1, (size_t)Di * N))
+                   ? -expf(p.A_log[(size_t)d * N + n]) * kLog2e : 0.f;
+      }
+      a2[q][s] = make_float2(v[0], v[1]);
+    }
+}
+
+// One step of the recurrence on the thread's channel pairs, h = exp(delta*A)*h + delta*u*B,
+// from the step's delta and u of its 2*DP channels and the B pairs of its NPT states; dl2
+// receives the delta pairs.
+template <int DP, int NPT>
+__device__ __forceinline__ void fwd_step(const float (&dlv)[2 * DP], const float (&uv)[2 * DP],
+                                         const float2 (&Bp)[NPT / 2], const float2 (&a2)[DP][NPT],
+                                         float2 (&h)[DP][NPT], float2 (&dl2)[DP]) {
+#pragma unroll
+  for (int q = 0; q < DP; ++q) {
+    dl2[q] = make_float2(dlv[2 * q], dlv[2 * q + 1]);
+    const float2 du2 = mul2(dl2[q], make_float2(uv[2 * q], uv[2 * q + 1]));
+#pragma unroll
+    for (int s = 0; s < NPT; ++s)
+      h[q][s] = fma2(ex2_2(mul2(dl2[q], a2[q][s])), h[q][s], mul2(du2, splat2(pair_el(Bp, s))));
+  }
+}
+
 template <int NP>
 struct FwdShape {
   static constexpr int NPT = states_per_thread_fwd(NP);    // states per thread
@@ -80,15 +134,16 @@ __device__ __forceinline__ void fwd_load_chunk(const FwdParams& p, float* st, in
     // their own slots after the wait
     static_assert(ST && VEC, "bf16 input is taken by the states-only forward");
     stage_tile_bf16<DC, NTH>(s_g, reinterpret_cast<const uint16_t*>(p.delta), rowb, t0, p.T,
-                             p.Di, dblk0);
+                             p.Di, dblk0, p.n_io());
     stage_tile_bf16<DC, NTH>(s_g + kChunk * DC / 2, reinterpret_cast<const uint16_t*>(p.u), rowb,
-                             t0, p.T, p.Di, dblk0);
-    stage_tile_bf16<NP, NTH>(s_C, reinterpret_cast<const uint16_t*>(p.B), rowb, t0, p.T, p.N, 0);
+                             t0, p.T, p.Di, dblk0, p.n_io());
+    stage_tile_bf16<NP, NTH>(s_C, reinterpret_cast<const uint16_t*>(p.B), rowb, t0, p.T, p.N, 0,
+                             p.n_bc());
   } else if constexpr (VEC) {
     for (int q = threadIdx.x; q < kChunk * DC / 4; q += NTH) {
       const int i = q / (DC / 4), col = (q % (DC / 4)) * 4;
       const int t = t0 + i, d = dblk0 + col;
-      const bool v = t < p.T && d < p.Di;
+      const bool v = t < p.T && d < p.Di && inb((rowb + t) * p.Di + d, 4, p.n_io());
       const size_t go = v ? (rowb + t) * p.Di + d : 0;
       cp_async16(s_dl + i * DC + col, p.delta + go, v);
       cp_async16(s_u + i * DC + col, p.u + go, v);
@@ -97,7 +152,7 @@ __device__ __forceinline__ void fwd_load_chunk(const FwdParams& p, float* st, in
     for (int q = threadIdx.x; q < kChunk * NP / 4; q += NTH) {
       const int i = q / (NP / 4), n = (q % (NP / 4)) * 4;
       const int t = t0 + i;
-      const bool v = t < p.T && n < p.N;
+      const bool v = t < p.T && n < p.N && inb((rowb + t) * p.N + n, 4, p.n_bc());
       const size_t go = v ? (rowb + t) * p.N + n : 0;
       cp_async16(s_B + i * NP + n, p.B + go, v);
       if constexpr (!ST) cp_async16(s_C + i * NP + n, p.C + go, v);
@@ -106,7 +161,7 @@ __device__ __forceinline__ void fwd_load_chunk(const FwdParams& p, float* st, in
     for (int q = threadIdx.x; q < kChunk * DC; q += NTH) {
       const int i = q / DC, col = q % DC;
       const int t = t0 + i, d = dblk0 + col;
-      const bool v = t < p.T && d < p.Di;
+      const bool v = t < p.T && d < p.Di && inb((rowb + t) * p.Di + d, 1, p.n_io());
       const size_t go = v ? (rowb + t) * p.Di + d : 0;
       cp_async4(s_dl + i * DC + col, p.delta + go, v);
       cp_async4(s_u + i * DC + col, p.u + go, v);
@@ -115,7 +170,7 @@ __device__ __forceinline__ void fwd_load_chunk(const FwdParams& p, float* st, in
     for (int q = threadIdx.x; q < kChunk * NP; q += NTH) {
       const int i = q / NP, n = q % NP;
       const int t = t0 + i;
-      const bool v = t < p.T && n < p.N;
+      const bool v = t < p.T && n < p.N && inb((rowb + t) * p.N + n, 1, p.n_bc());
       const size_t go = v ? (rowb + t) * p.N + n : 0;
       cp_async4(s_B + i * NP + n, p.B + go, v);
       if constexpr (!ST) cp_async4(s_C + i * NP + n, p.C + go, v);
@@ -165,39 +220,29 @@ scan_fwd_agg_kernel(const FwdParams p) {
   const int c_end = min(p.nchunks, seg_hi * p.seg_chunks);
   const size_t row0 = (size_t)b * T;
 
-  float2 a2[DPT][NPR], h[DPT][NPR];
-  float sd[DPT];
+  constexpr int DP = DPT / 2;
+  float2 a2[DP][NPT], h[DP][NPT], sd2[DP];   // channel pairs (see the file comment)
+  load_a2<DP, NPT>(p, d0, n0, a2);
 #pragma unroll
-  for (int j = 0; j < DPT; ++j) {
-    const int d = d0 + j;
-    const bool dv = d < Di;
-    sd[j] = 0.f;
-    float t4[NPT];
+  for (int q = 0; q < DP; ++q) {
+    sd2[q] = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int k = 0; k < NPT; ++k) {
-      const int n = n0 + k;
-      t4[k] = (dv && n < N) ? -expf(p.A_log[(size_t)d * N + n]) * kLog2e : 0.f;
-    }
-#pragma unroll
-    for (int q = 0; q < NPR; ++q) {
-      a2[j][q] = make_float2(t4[2 * q], t4[2 * q + 1]);
-      h[j][q] = make_float2(0.f, 0.f);
-    }
+    for (int s = 0; s < NPT; ++s) h[q][s] = make_float2(0.f, 0.f);
   }
 
   auto load = [&](int stage, int c) {
     float* st = smem + stage * A::kStageFloats;
     if constexpr (BF) {   // bf16 tiles into the first half of each slot
       stage_tile_bf16<DC, NTH>(st, reinterpret_cast<const uint16_t*>(p.delta), row0, c * kChunk,
-                               T, Di, dblk0);
+                               T, Di, dblk0, p.n_io());
       stage_tile_bf16<DC, NTH>(st + kChunk * DC, reinterpret_cast<const uint16_t*>(p.u), row0,
-                               c * kChunk, T, Di, dblk0);
+                               c * kChunk, T, Di, dblk0, p.n_io());
       stage_tile_bf16<NP, NTH>(st + 2 * kChunk * DC, reinterpret_cast<const uint16_t*>(p.B),
-                               row0, c * kChunk, T, N, 0);
+                               row0, c * kChunk, T, N, 0, p.n_bc());
     } else {
-      stage_tile<DC, NTH, VEC>(st, p.delta, row0, c * kChunk, T, Di, dblk0);
-      stage_tile<DC, NTH, VEC>(st + kChunk * DC, p.u, row0, c * kChunk, T, Di, dblk0);
-      stage_tile<NP, NTH, VEC>(st + 2 * kChunk * DC, p.B, row0, c * kChunk, T, N, 0);
+      stage_tile<DC, NTH, VEC>(st, p.delta, row0, c * kChunk, T, Di, dblk0, p.n_io());
+      stage_tile<DC, NTH, VEC>(st + kChunk * DC, p.u, row0, c * kChunk, T, Di, dblk0, p.n_io());
+      stage_tile<NP, NTH, VEC>(st + 2 * kChunk * DC, p.B, row0, c * kChunk, T, N, 0, p.n_bc());
     }
     cp_async_commit();
   };
@@ -237,41 +282,36 @@ scan_fwd_agg_kernel(const FwdParams p) {
       float dlv[DPT], uv[DPT];
       lds_chan<DPT>(s_dl + i * DC + cl, dlv);
       lds_chan<DPT>(s_u + i * DC + cl, uv);
-      float2 Bp[NPR];
+      float2 Bp[NPR], dl2[DP];
       lds_pairs<NPR>(s_B + i * NP + n0, Bp);
+      fwd_step<DP, NPT>(dlv, uv, Bp, a2, h, dl2);
 #pragma unroll
-      for (int j = 0; j < DPT; ++j) {
-        const float dl = dlv[j];
-        const float uu = uv[j];
-        sd[j] += dl;
-        const float2 dl2 = splat2(dl), du2 = splat2(dl * uu);
-#pragma unroll
-        for (int q = 0; q < NPR; ++q) {
-          const float2 da = ex2_2(mul2(dl2, a2[j][q]));
-          h[j][q] = fma2(da, h[j][q], mul2(du2, Bp[q]));
-        }
-      }
+      for (int q = 0; q < DP; ++q) sd2[q] = add2(sd2[q], dl2[q]);
     }
     if ((c + 1) % p.seg_chunks == 0) {   // the last chunk of a segment: emit, then restart
       const int seg = c / p.seg_chunks;
 #pragma unroll
       for (int j = 0; j < DPT; ++j) {
-        const int d = d0 + j;
-        if (d < Di) {
-          const size_t row = ((size_t)b * p.nseg + seg) * Di + d;
-          if (ng == 0) p.agg_sd[row] = sd[j];
+        const int d = d0 + j, q = j >> 1, k = j & 1;
+        const size_t row = ((size_t)b * p.nseg + seg) * Di + d;
+        if (d < Di && inb(row, 1, p.n_agg_sd()) && inb(row * N, N, p.n_agg_h())) {
+          if (ng == 0) p.agg_sd[row] = k ? sd2[q].y : sd2[q].x;
+          float2 hs[NPR];
+          chan_states<NPT>(h[q], k, hs);
           if constexpr (VEC) {
-            st_pairs_row<NPR>(p.agg_h + row * N, n0, N, h[j]);   // N % 4 == 0 here
+            st_pairs_row<NPR>(p.agg_h + row * N, n0, N, hs);   // N % 4 == 0 here
           } else {
 #pragma unroll
-            for (int k = 0; k < NPT; ++k)
-              if (n0 + k < N)
-                p.agg_h[row * N + n0 + k] = (k & 1) ? h[j][k >> 1].y : h[j][k >> 1].x;
+            for (int s = 0; s < NPT; ++s)
+              if (n0 + s < N) p.agg_h[row * N + n0 + s] = pair_el(hs, s);
           }
         }
-        sd[j] = 0.f;
+      }
 #pragma unroll
-        for (int q = 0; q < NPR; ++q) h[j][q] = make_float2(0.f, 0.f);
+      for (int q = 0; q < DP; ++q) {
+        sd2[q] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int s = 0; s < NPT; ++s) h[q][s] = make_float2(0.f, 0.f);
       }
     }
   }
@@ -305,25 +345,19 @@ scan_fwd_kernel(const FwdParams p) {
   const int c_begin = seg * p.seg_chunks;
   const int c_end = min(p.nchunks, c_begin + p.seg_chunks);
 
-  float2 a2[DPT][NPR], h[DPT][NPR];
+  constexpr int DP = DPT / 2;
+  float2 a2[DP][NPT], h[DP][NPT];   // channel pairs (see the file comment)
   float Dd[DPT];
+  load_a2<DP, NPT>(p, d0, n0, a2);
 #pragma unroll
   for (int j = 0; j < DPT; ++j) {
     const int d = d0 + j;
-    const bool dv = d < Di;
-    Dd[j] = dv ? p.D[d] : 0.f;
-    float t4[NPT];
-#pragma unroll
-    for (int k = 0; k < NPT; ++k) {
-      const int n = n0 + k;
-      t4[k] = (dv && n < N) ? -expf(p.A_log[(size_t)d * N + n]) * kLog2e : 0.f;
-    }
-#pragma unroll
-    for (int q = 0; q < NPR; ++q) {
-      a2[j][q] = make_float2(t4[2 * q], t4[2 * q + 1]);
-      h[j][q] = make_float2(0.f, 0.f);
-    }
+    Dd[j] = (d < Di && inb(d, 1, Di)) ? p.D[d] : 0.f;
   }
+#pragma unroll
+  for (int q = 0; q < DP; ++q)
+#pragma unroll
+    for (int s = 0; s < NPT; ++s) h[q][s] = make_float2(0.f, 0.f);
 
   using RSy = ReduceScatter<DPT * P, G / 2, 1>;
   const int ybase = RSy::base(lane);
@@ -340,27 +374,37 @@ scan_fwd_kernel(const FwdParams p) {
 
   // state entering the segment: compose the earlier segments' aggregates,
   // h <- exp(A * sum(delta)) * h + (segment end state from zero)
+  // (a channel past d_inner takes sum 0 and state 0: the identity)
   for (int sp = 0; sp < seg; ++sp) {
+    float sdv[DPT];
+    float2 hl[DPT][NPR];
 #pragma unroll
     for (int j = 0; j < DPT; ++j) {
       const int d = d0 + j;
-      if (d >= Di) continue;
       const size_t row = ((size_t)b * p.nseg + sp) * Di + d;
-      const float sd = p.agg_sd[row];
-      float2 hl[NPR];
+      const bool ok = d < Di && inb(row, 1, p.n_agg_sd()) && inb(row * N, N, p.n_agg_h());
+      sdv[j] = ok ? p.agg_sd[row] : 0.f;
+#pragma unroll
+      for (int q = 0; q < NPR; ++q) hl[j][q] = make_float2(0.f, 0.f);
+      if (!ok) continue;
       if constexpr (VEC) {
-        ld_pairs_row<NPR>(p.agg_h + row * N, n0, N, hl);
+        ld_pairs_row<NPR>(p.agg_h + row * N, n0, N, hl[j]);
       } else {
 #pragma unroll
         for (int q = 0; q < NPR; ++q) {
           const int n = n0 + 2 * q;
-          hl[q] = make_float2(n < N ? p.agg_h[row * N + n] : 0.f,
-                              n + 1 < N ? p.agg_h[row * N + n + 1] : 0.f);
+          hl[j][q] = make_float2(n < N ? p.agg_h[row * N + n] : 0.f,
+                                 n + 1 < N ? p.agg_h[row * N + n + 1] : 0.f);
         }
       }
+    }
 #pragma unroll
-      for (int q = 0; q < NPR; ++q)
-        h[j][q] = fma2(ex2_2(mul2(splat2(sd), a2[j][q])), h[j][q], hl[q]);
+    for (int q = 0; q < DP; ++q) {
+      const float2 sd2 = make_float2(sdv[2 * q], sdv[2 * q + 1]);
+#pragma unroll
+      for (int s = 0; s < NPT; ++s)
+        h[q][s] = fma2(ex2_2(mul2(sd2, a2[q][s])), h[q][s],
+                       make_float2(pair_el(hl[2 * q], s), pair_el(hl[2 * q + 1], s)));
     }
   }
 
@@ -405,17 +449,9 @@ scan_fwd_kernel(const FwdParams p) {
         float dlv[DPT], uv[DPT];
         lds_chan<DPT>(s_dl + i * DC + cl, dlv);
         lds_chan<DPT>(s_u + i * DC + cl, uv);
-        float2 Bp[NPR];
+        float2 Bp[NPR], dl2[DP];
         lds_pairs<NPR>(s_B + i * NP + n0, Bp);
-#pragma unroll
-        for (int j = 0; j < DPT; ++j) {
-          const float dl = dlv[j];
-          const float uu = uv[j];
-          const float2 dl2 = splat2(dl), du2 = splat2(dl * uu);
-#pragma unroll
-          for (int pp = 0; pp < NPR; ++pp)
-            h[j][pp] = fma2(ex2_2(mul2(dl2, a2[j][pp])), h[j][pp], mul2(du2, Bp[pp]));
-        }
+        fwd_step<DP, NPT>(dlv, uv, Bp, a2, h, dl2);
       }
     } else {
 #pragma unroll
@@ -427,22 +463,17 @@ scan_fwd_kernel(const FwdParams p) {
           float dlv[DPT], uv[DPT];
           lds_chan<DPT>(s_dl + i * DC + cl, dlv);
           lds_chan<DPT>(s_u + i * DC + cl, uv);
-          float2 Bp[NPR], Cp[NPR];
+          float2 Bp[NPR], Cp[NPR], dl2[DP];
           lds_pairs<NPR>(s_B + i * NP + n0, Bp);
           lds_pairs<NPR>(s_C + i * NP + n0, Cp);
+          fwd_step<DP, NPT>(dlv, uv, Bp, a2, h, dl2);
 #pragma unroll
-          for (int j = 0; j < DPT; ++j) {
-            const float dl = dlv[j];
-            const float uu = uv[j];
-            const float2 dl2 = splat2(dl), du2 = splat2(dl * uu);
-            float2 ya = make_float2(0.f, 0.f);
+          for (int q = 0; q < DP; ++q) {   // y of the channel pair: sum over the states
+            float2 ya = mul2(splat2(Cp[0].x), h[q][0]);
 #pragma unroll
-            for (int pp = 0; pp < NPR; ++pp) {
-              const float2 da = ex2_2(mul2(dl2, a2[j][pp]));
-              h[j][pp] = fma2(da, h[j][pp], mul2(du2, Bp[pp]));
-              ya = fma2(Cp[pp], h[j][pp], ya);
-            }
-            yv[tt * DPT + j] = ya.x + ya.y;
+            for (int s = 1; s < NPT; ++s) ya = fma2(splat2(pair_el(Cp, s)), h[q][s], ya);
+            yv[tt * DPT + 2 * q] = ya.x;
+            yv[tt * DPT + 2 * q + 1] = ya.y;
           }
         }
         RSy::run(yv, lane);
@@ -458,8 +489,8 @@ scan_fwd_kernel(const FwdParams p) {
 #pragma unroll
           for (int k = 1; k < DPT; ++k) Dj = j == k ? Dd[k] : Dj;
           const float y = fmaf(Dj, uu, yv[r]);
-          const bool ok = (t < T) && (d < Di);
           const size_t o = (rowb + t) * Di + d;
+          const bool ok = (t < T) && (d < Di) && inb(o, 1, p.n_io());
           st_global_if(p.out + o, y * (g * sigmoid_fast(g)), ok);
           st_global_if(p.y_ck + o, y, ok);            // kept for the backward's d_gate
           if constexpr (WITH_Y) st_global_if(p.y + o, y, ok);
@@ -472,13 +503,15 @@ scan_fwd_kernel(const FwdParams p) {
 #pragma unroll
       for (int j = 0; j < DPT; ++j) {
         const int d = d0 + j;
-        if (d >= Di) continue;
+        if (d >= Di || !inb((size_t)(ck - p.ckpt) + (size_t)d * N, N, p.n_ck())) continue;
+        float2 hs[NPR];
+        chan_states<NPT>(h[j >> 1], j & 1, hs);
         if constexpr (VEC) {
-          st_pairs_row<NPR>(ck + (size_t)d * N, n0, N, h[j]);
+          st_pairs_row<NPR>(ck + (size_t)d * N, n0, N, hs);
         } else {
 #pragma unroll
-          for (int k = 0; k < NPT; ++k)
-            if (n0 + k < N) ck[(size_t)d * N + n0 + k] = (k & 1) ? h[j][k >> 1].y : h[j][k >> 1].x;
+          for (int s = 0; s < NPT; ++s)
+            if (n0 + s < N) ck[(size_t)d * N + n0 + s] = pair_el(hs, s);
         }
       }
     }
@@ -542,5 +575,7 @@ int launch_fwd(const Plan& plan, const FwdParams& p, cudaStream_t s) {
     default: return -1;
   }
 }
+
+MSCAN_OOB_HOOKS(fwd)
 
 }  // namespace mscan

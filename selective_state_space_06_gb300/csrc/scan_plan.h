@@ -104,6 +104,12 @@ struct FwdParams {
   int softplus;                  // delta holds the raw delta: the kernels apply softplus
   int states_only;               // checkpoints only: no C, gate reads, no out, y (fused call)
   int io_bf16;                   // delta, u, B point at bf16 data (states-only forward)
+  // buffer lengths in elements, for the bounds-checked build
+  __host__ __device__ size_t n_io() const { return (size_t)batch * T * Di; }
+  __host__ __device__ size_t n_bc() const { return (size_t)batch * T * N; }
+  __host__ __device__ size_t n_ck() const { return (size_t)batch * (nchunks - 1) * Di * N; }
+  __host__ __device__ size_t n_agg_h() const { return (size_t)batch * nseg * Di * N; }
+  __host__ __device__ size_t n_agg_sd() const { return (size_t)batch * nseg * Di; }
 };
 
 struct BwdParams {
@@ -125,6 +131,15 @@ struct BwdParams {
   // copy for the last chunk of each CTA, so the wait for it runs out after wait_limit_ns.
   int test_skip_last_copy;
   unsigned long long wait_limit_ns;   // bound of every copy wait of the backward's kernels
+  // buffer lengths in elements, for the bounds-checked build
+  __host__ __device__ size_t n_io() const { return (size_t)batch * T * Di; }
+  __host__ __device__ size_t n_bc() const { return (size_t)batch * T * N; }
+  __host__ __device__ size_t n_ck() const { return (size_t)batch * (nchunks - 1) * Di * N; }
+  __host__ __device__ size_t n_part_bc() const { return (size_t)nblk * batch * T * N; }
+  __host__ __device__ size_t n_part_a() const { return (size_t)batch * nseg * Di * N; }
+  __host__ __device__ size_t n_part_d() const { return (size_t)batch * nseg * Di; }
+  __host__ __device__ size_t n_agg_l() const { return (size_t)batch * nseg * nsub * Di * N; }
+  __host__ __device__ size_t n_agg_sd() const { return (size_t)batch * nseg * nsub * Di; }
 };
 
 // Encodes a tiled tensor map (no interleave, no swizzle, zero fill outside the tensor) through
@@ -143,6 +158,17 @@ struct BwdMaps {   // each CUtensorMap carries its own 64-byte alignment
 // Reads and clears the fault word that the backward kernels set when a bounded wait on an
 // asynchronous copy gave up (0: none). Synchronises with the device.
 unsigned bwd_take_fault();
+// Fault words of the bounds-checked build, one per kernel file (scan_common.cuh,
+// MSCAN_OOB_HOOKS): take returns the word and clears it; set_oob_shrink sets the test hook and
+// returns -1 in the default build.
+unsigned int fwd_take_oob();
+unsigned int bwd_take_oob();
+unsigned int tmem_take_oob();
+unsigned int conv_take_oob();
+int fwd_set_oob_shrink(unsigned long long s);
+int bwd_set_oob_shrink(unsigned long long s);
+int tmem_set_oob_shrink(unsigned long long s);
+int conv_set_oob_shrink(unsigned long long s);
 
 // Each returns the number of kernels enqueued (>= 1) or -1 on a launch error.
 // launch_fwd enqueues the segment pre-pass (when nseg > 1) and the forward scan; launch_bwd

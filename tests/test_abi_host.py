@@ -210,3 +210,13 @@ def test_binding_rejects_cpu_tensors(ms):
     with pytest.raises(ValueError):
         ms.mamba_scan_fwd(t, t, torch.zeros(1, 4, 16), torch.zeros(1, 4, 16), t,
                           torch.zeros(4, 16), torch.zeros(4), t)
+
+
+def test_default_build_is_unchecked(ms):
+    # the bounds-checked build is a separate library; the default one has no shrink hook and
+    # refuses it before touching CUDA
+    assert not ms.mamba_scan_bounds_checked()
+    lib = ms.raw_library()
+    assert lib.mamba_scan_test_bounds_shrink(1) == ms.MAMBA_ERR_UNSUPPORTED
+    assert lib.mamba_scan_test_bounds_shrink(-1) == ms.MAMBA_ERR_UNSUPPORTED
+    assert "bounds-checked build" in ms.mamba_scan_strerror(ms.MAMBA_ERR_BOUNDS)
