@@ -183,9 +183,11 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
   // lanes read their B and C pairs straight from the stage and splat them in registers: half
   // the shared-memory bytes of a duplicated {B, B} copy, and no copy to write.
   constexpr bool DBC = !S::SWAP && !BF;
-  // delta*u formed once per element by the gating step, into the y tile (free after it unless
-  // it holds the warps' d_B / d_C rows, or the fused call forms y there)
-  constexpr bool DU = !FY && !S::RED_ALIAS;
+  // delta*u formed once per element by the gating step, into a tile that is free after it: the
+  // raw dy tile when nothing reads it later (fp32 without softplus), else the y tile unless it
+  // holds the warps' d_B / d_C rows. Not in the fused call, whose gating follows the recompute.
+  constexpr int DU_TILE = FY ? 0 : (!SP && !BF) ? 3 : !S::RED_ALIAS ? 4 : 0;
+  constexpr bool DU = DU_TILE != 0;
   // d_delta / d_u staged in shared memory and stored as whole rows after the walk (below) at
   // d_state 32 and 64. At d_state 16 a CTA covers 128 channels, and writing its staged chunk
   // out after the walk measured slower (404 against 397 us at mamba370m) than one predicated
@@ -343,6 +345,7 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
     float* s_g = st + 2 * TILE;          // becomes d_y (BF: gate and dy as bf16 halves)
     const float* s_dy = st + 3 * TILE;   // (BF: receives d_y)
     float* s_y = st + 4 * TILE;   // y: loaded, or formed by the recompute (FY)
+    float* const s_du = st + (DU ? DU_TILE : 4) * TILE;   // delta*u (DU)
     const float* s_B = st + 5 * TILE;
     const float* s_C = s_B + kChunk * NP;
     const float* s_h0 = s_C + kChunk * NP;
@@ -415,7 +418,7 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
           if constexpr (DU) {   // delta*u over the y values just read (this thread's own)
             const float4 d4 = *reinterpret_cast<const float4*>(s_dl + e);
             const float4 u4 = *reinterpret_cast<const float4*>(s_u + e);
-            *reinterpret_cast<float4*>(s_y + e) =
+            *reinterpret_cast<float4*>(s_du + e) =
                 make_float4(d4.x * u4.x, d4.y * u4.y, d4.z * u4.z, d4.w * u4.w);
           }
         }
@@ -436,7 +439,7 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
           if (SP && ok) {   // raw -> delta, and the factor d_raw / d_delta
             softplus_both(s_dl[e], const_cast<float*>(s_dl)[e], const_cast<float*>(s_dy)[e]);
           }
-          if constexpr (DU) s_y[e] = s_dl[e] * s_u[e];
+          if constexpr (DU) s_du[e] = s_dl[e] * s_u[e];
         }
       }
     };
@@ -482,8 +485,8 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
     const float* s_dyv = BF ? s_dy : s_g;   // d_y
     const float2* pdy[2] = {reinterpret_cast<const float2*>(s_dyv + offc[0]),
                             reinterpret_cast<const float2*>(s_dyv + offc[1])};
-    const float2* pdu[2] = {reinterpret_cast<const float2*>(s_y + offc[0]),
-                            reinterpret_cast<const float2*>(s_y + offc[1])};
+    const float2* pdu[2] = {reinterpret_cast<const float2*>(s_du + offc[0]),
+                            reinterpret_cast<const float2*>(s_du + offc[1])};
 #pragma unroll
     for (int i = 0; i < kChunk; ++i) {
       step_fence();
@@ -581,6 +584,8 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
       float2 hp[2][4];   // state before step i
       tmem_ld16(taddr + 16 * i, reinterpret_cast<float2(&)[8]>(hp));
       float2 dl2[2], u2[2], dy2[2], du2[2], B2[4], C2[4];
+      float u_lane = 0.f;   // (DU) u of the lane's output channel, for d_delta
+      if constexpr (DU) u_lane = row_u[i * DC];
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         dl2[q] = pdl[q][i * DC / 2];
@@ -680,7 +685,7 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
       }
       {
         float uo;
-        if constexpr (DU) uo = row_u[i * DC];
+        if constexpr (DU) uo = u_lane;
         else uo = mx ? u2[0].y : u2[0].x;
         const float dlo = mx ? dl2[0].y : dl2[0].x;
         const float dyo = mx ? dy2[0].y : dy2[0].x;
