@@ -629,7 +629,7 @@ static int run_channel_slices(const HostLayout& L, char* w, const float* delta, 
   e = cudaStreamSynchronize(s0);
   if (e != cudaSuccess) return set_cuda_error(e);
   g_last_launches = launches;
-  if (mscan::bwd_take_fault()) return MAMBA_ERR_TIMEOUT;
+  if (mscan::bwd_take_fault() | mscan::fwd_take_fault()) return MAMBA_ERR_TIMEOUT;
   if (take_oob()) return MAMBA_ERR_BOUNDS;
   return MAMBA_OK;
 }
@@ -744,7 +744,7 @@ int mamba_scan_fwd_bwd_host(const float* delta, const float* u, const float* B, 
   e = cudaStreamSynchronize(s0);
   if (e != cudaSuccess) return set_cuda_error(e);
   g_last_launches = launches;
-  if (mscan::bwd_take_fault()) return MAMBA_ERR_TIMEOUT;
+  if (mscan::bwd_take_fault() | mscan::fwd_take_fault()) return MAMBA_ERR_TIMEOUT;
   if (take_oob()) return MAMBA_ERR_BOUNDS;
   return MAMBA_OK;
 }
@@ -753,7 +753,7 @@ int mamba_scan_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return set_cuda_error(e);
-  if (mscan::bwd_take_fault()) return MAMBA_ERR_TIMEOUT;
+  if (mscan::bwd_take_fault() | mscan::fwd_take_fault()) return MAMBA_ERR_TIMEOUT;
   if (take_oob()) return MAMBA_ERR_BOUNDS;
   return MAMBA_OK;
 }

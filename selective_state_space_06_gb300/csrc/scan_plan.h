@@ -155,9 +155,19 @@ struct BwdMaps {   // each CUtensorMap carries its own 64-byte alignment
   CUtensorMap delta, u, gate, dy, y, B, C, ckpt;
 };
 
+// TMA descriptors of the forward kernels (d_state 64, d_inner a multiple of 4, fp32 inputs):
+// delta, u, gate as [batch][T][d_inner] with boxes of 16 steps x DC channels;
+// B, C as [batch][T][d_state] with boxes of 16 steps x NP states. Maps of tensors a variant
+// does not read are encoded on delta or B and never used.
+struct FwdMaps {
+  CUtensorMap delta, u, gate, B, C;
+};
+
 // Reads and clears the fault word that the backward kernels set when a bounded wait on an
 // asynchronous copy gave up (0: none). Synchronises with the device.
 unsigned bwd_take_fault();
+// The same for the forward kernels' copy waits.
+unsigned fwd_take_fault();
 // Fault words of the bounds-checked build, one per kernel file (scan_common.cuh,
 // MSCAN_OOB_HOOKS): take returns the word and clears it; set_oob_shrink sets the test hook and
 // returns -1 in the default build.
