@@ -188,13 +188,14 @@ int mamba_conv_bwd(const float* x, const float* w, const float* bias, const floa
  * and the seven gradients device->host, and synchronises `stream` before it returns. All
  * tensor pointers here are HOST pointers, with the same layouts as above. `workspace` is DEVICE
  * memory of at least mamba_scan_host_workspace_bytes(...) bytes, owned by the caller.
- * The work is cut into up to 4 slices. The first runs on `stream`, the others on streams of
- * the library, so that copies in both directions overlap the kernels of other slices. A batch
- * of 4 rows or more is cut by batch rows (when a batch row of T*d_inner and of T*d_state floats
- * is a multiple of 4); d_A_log and d_D are then the slices' sums added in slice order. A
- * smaller batch with d_inner a multiple of 4 and at least 128 is cut into blocks of channels
- * (at least 64 each): each slice is the whole batch over its channels, moved with 2-D copies,
- * and d_B and d_C are the slices' sums added in slice order. Either way the result is
+ * The work is cut into slices. The first runs on `stream`, the others on streams of the
+ * library, so that copies in both directions overlap the kernels of other slices. A batch of 4
+ * rows or more is cut into up to 4 slices of batch rows (when a batch row of T*d_inner and of
+ * T*d_state floats is a multiple of 4); d_A_log and d_D are then the slices' sums added in
+ * slice order. A smaller batch with d_inner a multiple of 4 and at least 128 is cut into up to
+ * 8 blocks of channels (at least 64 each): each slice is the whole batch over its channels,
+ * moved with 2-D copies, and d_B and d_C are the slices' sums added in slice order. Either way
+ * the result is
  * deterministic, but rounded differently from one mamba_scan_bwd call over the whole problem.
  * Calls on the same device share the library's streams, so calls from different host threads
  * are serialised by the device, not run side by side. */

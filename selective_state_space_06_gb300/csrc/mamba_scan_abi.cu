@@ -68,7 +68,10 @@ int check_dims(int64_t batch, int64_t T, int64_t Di, int64_t N, Plan* plan) {
 
 // Device workspace of mamba_scan_fwd_bwd_host: the whole batch's inputs and outputs, then one
 // set of checkpoint + scratch buffers per slice, then the slices' d_A_log / d_D sums.
-constexpr int kHostSlices = 4;
+// At most kHostSlices slices (streams, workspace regions); a batch is cut into at most
+// kBatchSlices slices of whole rows.
+constexpr int kHostSlices = 8;
+constexpr int kBatchSlices = 4;
 
 // A batch smaller than the slice count is cut into blocks of channels instead (each slice is
 // then the whole batch over dcs consecutive channels, a scan of its own); the smallest block
@@ -131,12 +134,12 @@ static bool host_layout_channels(int64_t batch, int64_t T, int64_t Di, int64_t N
 bool host_layout(int64_t batch, int64_t T, int64_t Di, int64_t N, HostLayout* L) {
   Plan whole;
   if (!mscan::make_plan(batch, T, Di, N, &whole)) return false;
-  if (batch < kHostSlices && Di % 4 == 0 && Di >= 2 * kMinSliceChannels)
+  if (batch < kBatchSlices && Di % 4 == 0 && Di >= 2 * kMinSliceChannels)
     return host_layout_channels(batch, T, Di, N, L);
   HostLayout h;
   // slices start on 16-byte boundaries only when a batch row is a multiple of 4 floats
   const bool sliceable = (T * Di) % 4 == 0 && (T * N) % 4 == 0;
-  h.nslices = sliceable ? (int)std::min<int64_t>(batch, kHostSlices) : 1;
+  h.nslices = sliceable ? (int)std::min<int64_t>(batch, kBatchSlices) : 1;
   h.rows = (batch + h.nslices - 1) / h.nslices;
   h.nslices = (int)((batch + h.rows - 1) / h.rows);
   Plan slice;

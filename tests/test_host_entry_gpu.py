@@ -53,9 +53,10 @@ def _run_host(x, repeat=2):
 
 
 @pytest.mark.parametrize("shape", [(8, 1024, 1536, 16), (5, 100, 64, 16), (3, 37, 50, 5),
-                                   (1, 300, 260, 64), (2, 200, 512, 16)],
+                                   (1, 300, 260, 64), (2, 200, 512, 16), (1, 150, 600, 64)],
                          ids=["mamba130m_4slices", "batch5_3slices", "ragged_1slice",
-                              "batch1_channel_slices", "batch2_channel_slices"])
+                              "batch1_4_channel_slices", "batch2_8_channel_slices",
+                              "batch1_8_channel_slices_narrow_last"])
 def test_host_entry_matches_oracle(shape):
     if shape[0] == 8:
         x = synth.make_inputs(synth.BY_NAME["mamba130m"])
