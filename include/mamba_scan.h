@@ -252,6 +252,19 @@ int mamba_scan_bwd_test_timeout(const float* delta, const float* u, const float*
                                 float* d_A_log, float* d_D, float* d_gate, int64_t batch,
                                 int64_t T, int64_t d_inner, int64_t d_state, void* stream);
 
+/* Failure-path test of the forward's bounded copy waits: mamba_scan_fwd, except that the
+ * forward kernel leaves the tensor copies of the last chunk each CTA walks unissued and gives
+ * up waiting for them after 1 ms. The next mamba_scan_status then returns MAMBA_ERR_TIMEOUT
+ * (and clears it); out, y and the checkpoints of that call are invalid. Every copy that was
+ * issued is waited for before use, so none is in flight when a CTA exits. Only sizes that run
+ * the forward with tensor copies are taken (33 <= d_state <= 64, d_inner and d_state multiples
+ * of 4, T > 16); others return MAMBA_ERR_UNSUPPORTED before anything is launched. */
+int mamba_scan_fwd_test_timeout(const float* delta, const float* u, const float* B,
+                                const float* C, const float* gate, const float* A_log,
+                                const float* D, float* out, float* y, void* ckpt,
+                                size_t ckpt_bytes, int64_t batch, int64_t T, int64_t d_inner,
+                                int64_t d_state, void* stream);
+
 /* Synchronises `stream` and reports any asynchronous CUDA error (MAMBA_ERR_CUDA), a
  * kernel that gave up waiting for its own copies (MAMBA_ERR_TIMEOUT), or, in a bounds-checked
  * build, an access a kernel computed outside its buffer (MAMBA_ERR_BOUNDS). Each flag is

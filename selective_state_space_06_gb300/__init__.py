@@ -46,7 +46,7 @@ EXPORTED = (
     "mamba_scan_host_workspace_bytes", "mamba_scan_fwd_bwd_host", "mamba_scan_status",
     "mamba_scan_strerror", "mamba_scan_last_launch_count", "mamba_scan_bwd_noalloc",
     "mamba_scan_fwd_softplus", "mamba_scan_bwd_softplus", "mamba_scan_fwd_bwd",
-    "mamba_scan_fwd_bwd_bf16", "mamba_scan_bwd_test_timeout",
+    "mamba_scan_fwd_bwd_bf16", "mamba_scan_bwd_test_timeout", "mamba_scan_fwd_test_timeout",
     "mamba_conv_scratch_bytes", "mamba_conv_fwd", "mamba_conv_bwd",
     "mamba_scan_bounds_checked", "mamba_scan_test_bounds_shrink",
 )
@@ -79,6 +79,8 @@ def _configure(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.mamba_scan_bwd_softplus.argtypes = lib.mamba_scan_bwd.argtypes
     lib.mamba_scan_bwd_softplus.restype = ctypes.c_int
     lib.mamba_scan_bwd_test_timeout.argtypes = lib.mamba_scan_bwd.argtypes
+    lib.mamba_scan_fwd_test_timeout.argtypes = lib.mamba_scan_fwd.argtypes
+    lib.mamba_scan_fwd_test_timeout.restype = ctypes.c_int
     lib.mamba_scan_bwd_test_timeout.restype = ctypes.c_int
     lib.mamba_scan_fwd_bwd.argtypes = [_vp] * 10 + [_sz, _vp, _sz] + [_vp] * 7 + [_i64] * 4 + [_vp]
     lib.mamba_scan_fwd_bwd.restype = ctypes.c_int
@@ -255,6 +257,14 @@ def mamba_scan_bwd_softplus(delta_raw, u, B, C, gate, A_log, D, dy, ckpt, scratc
     to the raw delta."""
     mamba_scan_bwd(delta_raw, u, B, C, gate, A_log, D, dy, ckpt, scratch, d_delta_raw, d_u, d_B,
                    d_C, d_A_log, d_D, d_gate, stream, _fn="mamba_scan_bwd_softplus")
+
+
+def mamba_scan_fwd_test_timeout(delta, u, B, C, gate, A_log, D, out, y=None, ckpt=None,
+                                stream=None):
+    """Failure-path test only: mamba_scan_fwd with the copies of each CTA's last chunk left
+    unissued and 1 ms copy waits, so that the next mamba_scan_status raises MAMBA_ERR_TIMEOUT."""
+    mamba_scan_fwd(delta, u, B, C, gate, A_log, D, out, y, ckpt, stream,
+                   _fn="mamba_scan_fwd_test_timeout")
 
 
 def mamba_scan_bwd_test_timeout(delta, u, B, C, gate, A_log, D, dy, ckpt, scratch, d_delta,

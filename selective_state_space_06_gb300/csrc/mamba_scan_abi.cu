@@ -232,7 +232,7 @@ static int scan_fwd_impl(const float* delta, const float* u, const float* B, con
                          const float* gate, const float* A_log, const float* D, float* out,
                          float* y, void* ckpt, size_t ckpt_bytes, int64_t batch, int64_t T,
                          int64_t d_inner, int64_t d_state, void* stream, int softplus,
-                         int states_only = 0, int io_bf16 = 0) {
+                         int states_only = 0, int io_bf16 = 0, int test_timeout = 0) {
   Plan plan;
   int rc = check_dims(batch, T, d_inner, d_state, &plan);
   if (rc != MAMBA_OK) return rc;
@@ -264,6 +264,13 @@ static int scan_fwd_impl(const float* delta, const float* u, const float* B, con
   p.softplus = softplus;
   p.states_only = states_only;
   p.io_bf16 = io_bf16;
+  p.wait_limit_ns = 1000000000ull;   // one second per copy wait
+  if (test_timeout) {
+    // the failure-path test: the forward with tensor copies leaves the copies of each CTA's
+    // last chunk unissued and gives up waiting for them after 1 ms
+    p.test_skip_last_copy = 1;
+    p.wait_limit_ns = 1000000ull;
+  }
   const int n = mscan::launch_fwd(plan, p, (cudaStream_t)stream);
   if (n < 0) return set_cuda_error(cudaGetLastError());
   g_last_launches = n;
@@ -277,6 +284,23 @@ int mamba_scan_fwd(const float* delta, const float* u, const float* B, const flo
   mscan::NvtxRange nvtx_range("mamba_scan_fwd");
   return scan_fwd_impl(delta, u, B, C, gate, A_log, D, out, y, ckpt, ckpt_bytes, batch, T,
                        d_inner, d_state, stream, 0);
+}
+
+int mamba_scan_fwd_test_timeout(const float* delta, const float* u, const float* B,
+                                const float* C, const float* gate, const float* A_log,
+                                const float* D, float* out, float* y, void* ckpt,
+                                size_t ckpt_bytes, int64_t batch, int64_t T, int64_t d_inner,
+                                int64_t d_state, void* stream) {
+  mscan::NvtxRange nvtx_range("mamba_scan_fwd_test_timeout");
+  Plan plan;
+  const int rc = check_dims(batch, T, d_inner, d_state, &plan);
+  if (rc != MAMBA_OK) return rc;
+  // only the forward with tensor-copy staging (d_state 33..64, d_inner and d_state multiples
+  // of 4) waits on copies it issues itself
+  if (plan.NP != mscan::kMaxState || d_inner % 4 != 0 || d_state % 4 != 0 || plan.nchunks < 2)
+    return MAMBA_ERR_UNSUPPORTED;
+  return scan_fwd_impl(delta, u, B, C, gate, A_log, D, out, y, ckpt, ckpt_bytes, batch, T,
+                       d_inner, d_state, stream, 0, 0, 0, 1);
 }
 
 int mamba_scan_fwd_softplus(const float* delta_raw, const float* u, const float* B,

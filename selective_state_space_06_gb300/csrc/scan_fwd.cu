@@ -149,8 +149,11 @@ __device__ __forceinline__ void fwd_tma_tiles(const FwdMaps& maps, uint64_t* bar
 
 // Waits until stage `stage` of a TMA ring holds chunk use number `use` (bounded; a wait that
 // gives up sets the fault word and the kernel runs on with the stale stage).
-__device__ __forceinline__ void fwd_tma_wait(uint64_t* bars, int stages, int it) {
-  if (!mbar_wait(bars + it % stages, (uint32_t)((it / stages) & 1))) atomicOr(&g_fwd_fault, 1u);
+__device__ __forceinline__ void fwd_tma_wait(uint64_t* bars, int stages, int it,
+                                             unsigned long long limit_ns) {
+  if (!mbar_wait(bars + it % stages, (uint32_t)((it / stages) & 1),
+                 limit_ns ? limit_ns : kWaitLimitNs))
+    atomicOr(&g_fwd_fault, 1u);
 }
 
 template <int NP, bool VEC, bool ST = false, bool BF = false>
@@ -307,7 +310,7 @@ scan_fwd_agg_kernel(const __grid_constant__ FwdMaps maps, const FwdParams p) {
   }
   for (int c = c_begin; c < c_end; ++c) {
     const int it = c - c_begin;
-    if constexpr (TMA) fwd_tma_wait(bars, A::kStages, it);
+    if constexpr (TMA) fwd_tma_wait(bars, A::kStages, it, p.wait_limit_ns);
     else cp_async_wait<A::kStages - 2>();
     __syncthreads();
     if (c + A::kStages - 1 < c_end) load((it + A::kStages - 1) % A::kStages, c + A::kStages - 1);
@@ -428,12 +431,15 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const FwdParams p) {
 
   auto issue = [&](int stage, int c) {
     float* st = smem + stage * S::kStageFloats;
-    if constexpr (TMA)
+    if constexpr (TMA) {
+      // the failure-path test leaves the CTA's last chunk without copies
+      if (p.test_skip_last_copy && c == c_end - 1) return;
       fwd_tma_tiles<NP>(maps, bars + stage, c, b, dblk0, st, st + kChunk * DC,
                         ST ? nullptr : st + 2 * kChunk * DC, st + 3 * kChunk * DC,
                         ST ? nullptr : st + 3 * kChunk * DC + kChunk * NP);
-    else
+    } else {
       fwd_load_chunk<NP, VEC, ST, BF>(p, st, c, b, dblk0);
+    }
   };
   if constexpr (TMA) {
     if (threadIdx.x == 0) {
@@ -487,7 +493,7 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const FwdParams p) {
 
   for (int c = c_begin; c < c_end; ++c) {
     const int it = c - c_begin;
-    if constexpr (TMA) fwd_tma_wait(bars, NS, it);
+    if constexpr (TMA) fwd_tma_wait(bars, NS, it, p.wait_limit_ns);
     else cp_async_wait<NS - 2>();
     __syncthreads();
     {

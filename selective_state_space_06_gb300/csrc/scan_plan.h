@@ -104,6 +104,11 @@ struct FwdParams {
   int softplus;                  // delta holds the raw delta: the kernels apply softplus
   int states_only;               // checkpoints only: no C, gate reads, no out, y (fused call)
   int io_bf16;                   // delta, u, B point at bf16 data (states-only forward)
+  // Failure-path test only (mamba_scan_fwd_test_timeout): the forward kernel with tensor
+  // copies (d_state 64) issues no copy for the last chunk of each CTA, so the wait for it runs
+  // out after wait_limit_ns.
+  int test_skip_last_copy;
+  unsigned long long wait_limit_ns;   // bound of every copy wait of the forward (0: one second)
   // buffer lengths in elements, for the bounds-checked build
   __host__ __device__ size_t n_io() const { return (size_t)batch * T * Di; }
   __host__ __device__ size_t n_bc() const { return (size_t)batch * T * N; }

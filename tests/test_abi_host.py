@@ -150,6 +150,23 @@ def test_bwd_test_timeout_takes_only_the_tensor_copy_path(ms):
     assert f(*_bwd_args(scratch_bytes=1024)) == ms.MAMBA_ERR_WORKSPACE
 
 
+@needs_no_gpu
+def test_fwd_test_timeout_takes_only_the_tensor_copy_path(ms):
+    """The forward's failure-path test entry point validates like mamba_scan_fwd and refuses
+    sizes that do not run the forward with tensor copies (d_state 33..64, d_inner and d_state
+    multiples of 4, more than one chunk), before anything is launched."""
+    lib = ms.raw_library()
+    f = lib.mamba_scan_fwd_test_timeout
+    assert f(*_fwd_args(dims=(1, 40, 64, 16))) == ms.MAMBA_ERR_UNSUPPORTED    # d_state 16
+    assert f(*_fwd_args(dims=(1, 40, 64, 32))) == ms.MAMBA_ERR_UNSUPPORTED    # d_state 32
+    assert f(*_fwd_args(dims=(1, 40, 66, 64))) == ms.MAMBA_ERR_UNSUPPORTED    # d_inner % 4
+    assert f(*_fwd_args(dims=(1, 40, 64, 62))) == ms.MAMBA_ERR_UNSUPPORTED    # d_state % 4
+    assert f(*_fwd_args(dims=(1, 16, 64, 64))) == ms.MAMBA_ERR_UNSUPPORTED    # one chunk
+    assert f(*_fwd_args(dims=(1, 40, 64, 100))) == ms.MAMBA_ERR_UNSUPPORTED
+    assert f(*_fwd_args(dims=(1, 40, 64, 64), delta=None)) == ms.MAMBA_ERR_INVALID_ARG
+    assert f(*_fwd_args(dims=(1, 40, 64, 64), ckpt_bytes=64)) == ms.MAMBA_ERR_WORKSPACE
+
+
 def _fused_args(**over):
     b, T, Di, N = over.pop("dims", (2, 40, 64, 16))
     big = 1 << 32
