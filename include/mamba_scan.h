@@ -193,8 +193,9 @@ int mamba_conv_bwd(const float* x, const float* w, const float* bias, const floa
  * rows or more is cut into up to 4 slices of batch rows (when a batch row of T*d_inner and of
  * T*d_state floats is a multiple of 4); d_A_log and d_D are then the slices' sums added in
  * slice order. A smaller batch with d_inner a multiple of 4 and at least 128 is cut into up to
- * 8 blocks of channels (at least 64 each): each slice is the whole batch over its channels,
- * moved with 2-D copies, and d_B and d_C are the slices' sums added in slice order. Either way
+ * 6 blocks of channels (at least 64 each; the first and the last about half as wide as the
+ * others): each slice is the whole batch over its channels, moved with 2-D copies, and d_B and
+ * d_C are the slices' sums added in slice order. Either way
  * the result is
  * deterministic, but rounded differently from one mamba_scan_bwd call over the whole problem.
  * Calls on the same device share the library's streams, so calls from different host threads

@@ -77,6 +77,11 @@ constexpr int kBatchSlices = 4;
 // then the whole batch over dcs consecutive channels, a scan of its own); the smallest block
 // worth a slice of its own:
 constexpr int64_t kMinSliceChannels = 64;
+// Channel slices: at most kChanSlices, the first and the last half as wide as the others. The
+// pipeline's head (the first slice's copies in) and tail (the last slice's kernels and copies
+// out) then take half as long, while the middle slices keep rows wide enough for 2-D copies at
+// the link's full rate (rows of 1280 bytes copy 15-20 % slower than rows of 2048 bytes and up).
+constexpr int kChanSlices = 6;
 
 struct HostLayout {
   int64_t rows = 0;            // batch rows per slice
@@ -88,7 +93,8 @@ struct HostLayout {
   // rows and d_A_log / d_D rows (one region per slice), the shared B and C, and the slices'
   // d_B | d_C partials with their fixed-order sum
   bool by_channels = false;
-  int64_t dcs = 0;
+  int64_t dcs = 0;                     // the widest slice's channels
+  int64_t sd0[kHostSlices] = {}, sdw[kHostSlices] = {};   // each slice's first channel, width
   size_t off_slice[kHostSlices] = {};
   size_t sl_in[4] = {}, sl_A = 0, sl_D = 0, sl_out[4] = {}, sl_dA = 0, sl_dD = 0;   // in a slice
   size_t off_bc = 0, off_bcpart = 0, off_bcsum = 0;
@@ -98,15 +104,29 @@ static bool host_layout_channels(int64_t batch, int64_t T, int64_t Di, int64_t N
                                  HostLayout* L) {
   HostLayout h;
   h.by_channels = true;
-  const int64_t want = std::min<int64_t>(kHostSlices, Di / kMinSliceChannels);
-  h.dcs = round_up((size_t)((Di + want - 1) / want), 4);
-  h.nslices = (int)((Di + h.dcs - 1) / h.dcs);
+  // n slices of widths u, 2u, ..., 2u and the rest (about u), u a multiple of 4 and at least
+  // kMinSliceChannels (the caller takes d_inner >= 2 * kMinSliceChannels, a multiple of 4)
+  const int n = (int)std::max<int64_t>(
+      2, std::min<int64_t>(kChanSlices, Di / (2 * kMinSliceChannels) + 1));
+  const int64_t unit = Di / (2 * (n - 1)) / 4 * 4;
+  int64_t d0 = 0;
+  for (int k = 0; k < n; ++k) {
+    const int64_t w = k == n - 1 ? Di - d0 : (k == 0 ? unit : 2 * unit);
+    h.sd0[k] = d0;
+    h.sdw[k] = w;
+    h.dcs = std::max(h.dcs, w);
+    d0 += w;
+  }
+  h.nslices = n;
   h.rows = batch;
-  Plan slice;
-  if (!mscan::make_plan(batch, T, h.dcs, N, &slice)) return false;
-  // a narrower last slice needs no more checkpoint or scratch than a full one
-  h.ck_bytes = slice.ckpt_elems * sizeof(float);
-  h.sc_bytes = slice.scratch_elems * sizeof(float);
+  // checkpoint and scratch buffers sized for every slice's plan (a narrower slice may cut its
+  // time axis into more segments)
+  for (int k = 0; k < n; ++k) {
+    Plan slice;
+    if (!mscan::make_plan(batch, T, h.sdw[k], N, &slice)) return false;
+    h.ck_bytes = std::max(h.ck_bytes, slice.ckpt_elems * sizeof(float));
+    h.sc_bytes = std::max(h.sc_bytes, slice.scratch_elems * sizeof(float));
+  }
   const size_t a = 256;
   const size_t btd_s = (size_t)batch * T * h.dcs * 4, btn = (size_t)batch * T * N * 4;
   size_t off = 0;   // inside one slice region
@@ -588,7 +608,7 @@ static int run_channel_slices(const HostLayout& L, char* w, const float* delta, 
   const size_t hp = (size_t)d_inner * 4;   // host row pitch
   for (int k = 0; k < L.nslices; ++k) {
     cudaStream_t st = ax.s[k];
-    const int64_t d0 = (int64_t)k * L.dcs, nd = std::min<int64_t>(L.dcs, d_inner - d0);
+    const int64_t d0 = L.sd0[k], nd = L.sdw[k];
     const size_t dp = (size_t)nd * 4;        // device row pitch (compact slice)
     char* sl = w + L.off_slice[k];
     float* in[4];
