@@ -196,6 +196,11 @@ struct AuxStreams {
   cudaEvent_t ev[kHostSlices + 1] = {};      // slice done; [kHostSlices]: A_log, D copied
   cudaEvent_t ev_in[kHostSlices] = {};       // slice's host->device copies done
   cudaEvent_t ev_out[kHostSlices] = {};      // slice's device->host copies done
+  // channel slices: the device->host copies go on a stream of their own, in slice order
+  cudaStream_t d2h = nullptr;
+  cudaEvent_t ev_fwd[kHostSlices] = {};      // slice's forward done (out is final)
+  cudaEvent_t ev_bwd[kHostSlices] = {};      // slice's backward done
+  cudaEvent_t ev_end = nullptr;              // the last device->host copy done
 };
 bool aux_streams(AuxStreams* out) {
   static std::mutex mu;
@@ -212,8 +217,13 @@ bool aux_streams(AuxStreams* out) {
       if (cudaEventCreateWithFlags(&x.ev[i], cudaEventDisableTiming) != cudaSuccess) return false;
     for (int i = 0; i < kHostSlices; ++i)
       if (cudaEventCreateWithFlags(&x.ev_in[i], cudaEventDisableTiming) != cudaSuccess ||
-          cudaEventCreateWithFlags(&x.ev_out[i], cudaEventDisableTiming) != cudaSuccess)
+          cudaEventCreateWithFlags(&x.ev_out[i], cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&x.ev_fwd[i], cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&x.ev_bwd[i], cudaEventDisableTiming) != cudaSuccess)
         return false;
+    if (cudaStreamCreateWithFlags(&x.d2h, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&x.ev_end, cudaEventDisableTiming) != cudaSuccess)
+      return false;
     ready[dev] = true;
   }
   *out = x;
@@ -641,37 +651,58 @@ static int run_channel_slices(const HostLayout& L, char* w, const float* delta, 
                             L.ck_bytes ? ck : nullptr, L.ck_bytes, batch, T, nd, d_state, st);
     if (rc != MAMBA_OK) return rc;
     launches += g_last_launches;
+    if ((e = cudaEventRecord(ax.ev_fwd[k], st)) != cudaSuccess) return set_cuda_error(e);
     rc = mamba_scan_bwd(in[0], in[1], w_B, w_C, in[2], sA, sD, in[3], L.ck_bytes ? ck : nullptr,
                         L.ck_bytes, sc, L.sc_bytes, outv[1], outv[2], part, part + btn, sdA, sdD,
                         outv[3], batch, T, nd, d_state, st);
     if (rc != MAMBA_OK) return rc;
     launches += g_last_launches;
+    if ((e = cudaEventRecord(ax.ev_bwd[k], st)) != cudaSuccess) return set_cuda_error(e);
+  }
+  // The copies out run on the library's device->host stream, one after another in slice order
+  // (each at the link's rate), so that the slices' kernels never wait behind them: a slice's out
+  // as soon as its forward is done, its gradients once its backward is done. The device->host
+  // direction carries as many bytes as the other but can only start after the first slice's
+  // forward, so it is the pipeline's critical path.
+  cudaStream_t sd = ax.d2h;
+  for (int k = 0; k < L.nslices; ++k) {
+    const int64_t d0 = L.sd0[k], nd = L.sdw[k];
+    const size_t dp = (size_t)nd * 4;
+    char* sl = w + L.off_slice[k];
+    float* outv[4];
+    for (int i = 0; i < 4; ++i) outv[i] = (float*)(sl + L.sl_out[i]);
+    float* sdA = (float*)(sl + L.sl_dA);
+    float* sdD = (float*)(sl + L.sl_dD);
     float* hout[4] = {out, d_delta, d_u, d_gate};
-    if (k > 0 && (e = cudaStreamWaitEvent(st, ax.ev_out[k - 1], 0)) != cudaSuccess)
+    if ((e = cudaStreamWaitEvent(sd, ax.ev_fwd[k], 0)) != cudaSuccess ||
+        (e = cudaMemcpy2DAsync(hout[0] + d0, hp, outv[0], dp, dp, rows, cudaMemcpyDeviceToHost,
+                               sd)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(sd, ax.ev_bwd[k], 0)) != cudaSuccess)
       return set_cuda_error(e);
-    for (int i = 0; i < 4; ++i)
+    for (int i = 1; i < 4; ++i)
       if ((e = cudaMemcpy2DAsync(hout[i] + d0, hp, outv[i], dp, dp, rows, cudaMemcpyDeviceToHost,
-                                 st)) != cudaSuccess)
+                                 sd)) != cudaSuccess)
         return set_cuda_error(e);
     if ((e = cudaMemcpyAsync(d_A_log + (size_t)d0 * d_state, sdA, (size_t)nd * d_state * 4,
-                             cudaMemcpyDeviceToHost, st)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(d_D + d0, sdD, dp, cudaMemcpyDeviceToHost, st)) != cudaSuccess ||
-        (e = cudaEventRecord(ax.ev_out[k], st)) != cudaSuccess)
+                             cudaMemcpyDeviceToHost, sd)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(d_D + d0, sdD, dp, cudaMemcpyDeviceToHost, sd)) != cudaSuccess)
       return set_cuda_error(e);
   }
-  // d_B and d_C: the slices' sums, added in slice order
+  // d_B and d_C: the slices' sums, added in slice order, then copied out behind the rest
   for (int k = 1; k < L.nslices; ++k)
-    if ((e = cudaEventRecord(ax.ev[k], ax.s[k])) != cudaSuccess ||
-        (e = cudaStreamWaitEvent(s0, ax.ev[k], 0)) != cudaSuccess)
-      return set_cuda_error(e);
+    if ((e = cudaStreamWaitEvent(s0, ax.ev_bwd[k], 0)) != cudaSuccess) return set_cuda_error(e);
   float* sum = at(L.off_bcsum);
   const size_t n = 2 * btn;
   mscan::sum_slices<<<(unsigned)std::min<size_t>((n + 255) / 256, 65535), 256, 0, s0>>>(
       at(L.off_bcpart), L.nslices, n, sum);
   if ((e = cudaPeekAtLastError()) != cudaSuccess) return set_cuda_error(e);
   ++launches;
-  if ((e = cudaMemcpyAsync(d_B, sum, btn * 4, cudaMemcpyDeviceToHost, s0)) != cudaSuccess ||
-      (e = cudaMemcpyAsync(d_C, sum + btn, btn * 4, cudaMemcpyDeviceToHost, s0)) != cudaSuccess)
+  if ((e = cudaEventRecord(ax.ev[0], s0)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(sd, ax.ev[0], 0)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(d_B, sum, btn * 4, cudaMemcpyDeviceToHost, sd)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(d_C, sum + btn, btn * 4, cudaMemcpyDeviceToHost, sd)) != cudaSuccess ||
+      (e = cudaEventRecord(ax.ev_end, sd)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(s0, ax.ev_end, 0)) != cudaSuccess)
     return set_cuda_error(e);
   e = cudaStreamSynchronize(s0);
   if (e != cudaSuccess) return set_cuda_error(e);
