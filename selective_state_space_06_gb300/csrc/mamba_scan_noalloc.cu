@@ -38,7 +38,8 @@ constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[MAMBA_SCAN_NOALLOC_SCRATCH_BYTES];
 
-// The driver's context queries, looked up once through the runtime (no driver library linked).
+// The CUDA driver API's context queries, looked up once through the runtime (no driver library
+// linked).
 typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
 typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
 struct CtxFns {
