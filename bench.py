@@ -564,17 +564,23 @@ def run_gpu(args):
 
 def _oracle_rows_runner(w):
     """(run(rows) -> seconds) for the oracle over the first `rows` rows of the workload, with
-    the output arrays allocated once outside the timed calls."""
+    every output array allocated once outside the timed calls (the forward's out and y, the
+    backward's per-row gradients and its accumulators, zeroed before each call)."""
     import oracle
     x = oracle.as64(synth.make_inputs(w, seed=0))
     b, T, Di, N = w.shape()
     out = np.full((b, T, Di), np.nan)
     y = np.full((b, T, Di), np.nan)
+    per_row = {k: np.full((b, T, Di), np.nan) for k in ("d_delta", "d_u", "d_gate")}
+    acc = {"d_B": np.zeros((b, T, N)), "d_C": np.zeros((b, T, N)),
+           "d_A_log": np.zeros((Di, N)), "d_D": np.zeros(Di)}
 
     def run(rows):
+        for a in acc.values():
+            a.fill(0.0)
         t0 = time.perf_counter()
         oracle.fwd(x, rows=(0, rows), out=out, y=y)
-        oracle.bwd(x, rows=(0, rows))
+        oracle.bwd_rows_into(x, (0, rows), per_row, acc)
         return time.perf_counter() - t0
     return run
 

@@ -167,6 +167,15 @@ def bwd(x: dict, threads: int = 1, rows=None, lib=None) -> dict:
     return per_row
 
 
+def bwd_rows_into(x: dict, rows, per_row: dict, acc: dict, lib=None) -> None:
+    """The computation of bwd() over the row range ``rows`` into caller-owned float64 arrays:
+    per_row holds d_delta, d_u, d_gate [batch,T,d_inner] (rows outside the range untouched);
+    acc holds d_B, d_C [batch,T,d_state], d_A_log [d_inner,d_state], d_D [d_inner], which the
+    range's contributions are added to. For timing the oracle without allocating its outputs
+    in every call."""
+    _bwd_range(as64(x), rows[0], rows[1], per_row, acc, lib)
+
+
 def loss(x: dict, lib=None) -> float:
     """Scalar loss sum(dy * out) whose gradients ``bwd`` returns."""
     out, _ = fwd(x, lib=lib)

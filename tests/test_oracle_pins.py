@@ -399,6 +399,21 @@ def test_row_split_threads_consistent():
         np.testing.assert_allclose(g4[k], g1[k], rtol=1e-13, atol=1e-13)
 
 
+def test_bwd_rows_into_matches_bwd():
+    # Two row ranges written into caller-owned arrays give what one bwd() call gives.
+    x = synth.random_inputs(2, 9, 5, 3, seed=4)
+    ref = oracle.bwd(x)
+    b, T, Di, N = 2, 9, 5, 3
+    per_row = {k: np.full((b, T, Di), np.nan) for k in ("d_delta", "d_u", "d_gate")}
+    acc = {"d_B": np.zeros((b, T, N)), "d_C": np.zeros((b, T, N)),
+           "d_A_log": np.zeros((Di, N)), "d_D": np.zeros(Di)}
+    oracle.bwd_rows_into(x, (0, 4), per_row, acc)
+    oracle.bwd_rows_into(x, (4, b * Di), per_row, acc)
+    for k in GRAD_KEYS:
+        got = per_row[k] if k in per_row else acc[k]
+        np.testing.assert_allclose(got, ref[k], rtol=1e-13, atol=1e-13)
+
+
 MUTANTS = {
     "carry_without_decay": ("dh[n] = da * g_h;", "dh[n] = g_h;"),
     "dropped_A_term_in_d_delta": ("ddl += g_h * (A[n] * da * hp + uu * bn);", "ddl += g_h * (uu * bn);"),
