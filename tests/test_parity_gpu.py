@@ -71,6 +71,35 @@ def test_edge_shapes(shape):
     assert_parity(run_gpu(x), oracle_all(x), label=str(shape))
 
 
+# d_state 32 and 64 with several blocks of channels (32 channels per block at d_state 64, 64
+# at d_state 32), vectorised (d_inner and d_state multiples of 4): the d_B / d_C partials of
+# the blocks are summed by the reduction in block order.
+MULTI_BLOCK_SHAPES = [
+    (2, 333, 128, 64),   # 4 blocks, ragged T
+    (1, 100, 64, 64),    # 2 blocks
+    (1, 200, 256, 48),   # 8 blocks; states 48..63 padding
+    (1, 64, 192, 64),    # 6 blocks
+    (1, 50, 100, 64),    # 4 blocks, the last one ragged (channels 96..99)
+    (2, 90, 256, 32),    # d_state 32: 4 blocks of 64 channels
+    (1, 77, 128, 24),    # d_state 24 (padded to 32): 2 blocks
+    (3, 1000, 512, 64),  # 16 blocks, several time segments per row
+]
+
+
+@pytest.mark.parametrize("shape", MULTI_BLOCK_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_multi_block_shapes(shape):
+    x = synth.random_inputs(*shape, seed=sum(shape) + 1, a_log_random=True)
+    assert_parity(run_gpu(x), oracle_all(x), label=str(shape))
+
+
+def test_multi_block_bitwise_deterministic():
+    x = synth.random_inputs(1, 400, 256, 64, seed=5, a_log_random=True)
+    a = run_gpu(x)
+    b = run_gpu(x)
+    for k in OUT_KEYS:
+        assert np.array_equal(a[k], b[k], equal_nan=False), k
+
+
 def test_delta_zero():
     x = synth.random_inputs(2, 40, 70, 16, seed=1)
     x["delta"][:] = 0.0
