@@ -463,15 +463,22 @@ def run_gpu(args):
         if pg:
             pg.barrier()
         t0 = time.perf_counter()
+        marks = [t0]
         for _ in range(ke):
-            e2e_step()
-        el = time.perf_counter() - t0
+            e2e_step()   # returns once the step's results are in host memory
+            marks.append(time.perf_counter())
+        el = marks[-1] - t0
         el = max_over_ranks(pg, el, dev)
+        per_call = sorted(1e3 * (b - a) for a, b in zip(marks, marks[1:]))
         h2d = sum(v.numel() * 4 for k, v in hin.items())
         d2h = sum(v.numel() * 4 for v in hout.values())
+        # value and ms_per_step: all steps (the mean); the median and the slowest step show
+        # how much of the mean comes from occasional slow calls on the shared host
         e2e = {"value": job_throughput(w.btd * ke, ws, el), "unit": UNIT,
                "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "steps": ke, "ms_per_step": 1e3 * el / ke}
+               "d2h_bytes_per_step": d2h, "steps": ke, "ms_per_step": 1e3 * el / ke,
+               "median_ms_per_step_rank0": per_call[len(per_call) // 2],
+               "max_ms_per_step_rank0": per_call[-1]}
         del wsbuf, hin, hout
 
     variants = {}

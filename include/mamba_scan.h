@@ -198,8 +198,9 @@ int mamba_conv_bwd(const float* x, const float* w, const float* bias, const floa
  * d_C are the slices' sums added in slice order. Either way
  * the result is
  * deterministic, but rounded differently from one mamba_scan_bwd call over the whole problem.
- * Calls on the same device share the library's streams, so calls from different host threads
- * are serialised by the device, not run side by side. */
+ * Calls on the same device share the library's streams and events: calls from different host
+ * threads run one at a time (each holds a per-device lock from its first enqueue to its
+ * return). */
 size_t mamba_scan_host_workspace_bytes(int64_t batch, int64_t T, int64_t d_inner, int64_t d_state);
 int mamba_scan_fwd_bwd_host(const float* delta, const float* u, const float* B, const float* C,
                             const float* gate, const float* A_log, const float* D,

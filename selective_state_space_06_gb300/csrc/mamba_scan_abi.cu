@@ -201,15 +201,23 @@ struct AuxStreams {
   cudaEvent_t ev_fwd[kHostSlices] = {};      // slice's forward done (out is final)
   cudaEvent_t ev_bwd[kHostSlices] = {};      // slice's backward done
   cudaEvent_t ev_end = nullptr;              // the last device->host copy done
+  // Held by a call from its first enqueue to its return. Calls from several host threads share
+  // these streams and events, and an event recorded by one call must not be re-recorded by
+  // another between that record and the waits on it (on the caller's own stream, such a
+  // re-record would point the waits at the other call's work). Held through the final
+  // synchronisation too, so that the fault words read after it belong to this call.
+  std::mutex* enqueue = nullptr;
 };
 bool aux_streams(AuxStreams* out) {
   static std::mutex mu;
+  static std::mutex enqueue_mu[64];
   static AuxStreams aux[64];
   static bool ready[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
   std::lock_guard<std::mutex> lock(mu);
   AuxStreams& x = aux[dev];
+  x.enqueue = &enqueue_mu[dev];
   if (!ready[dev]) {
     for (int i = 1; i < kHostSlices; ++i)
       if (cudaStreamCreateWithFlags(&x.s[i], cudaStreamNonBlocking) != cudaSuccess) return false;
@@ -599,6 +607,7 @@ static int run_channel_slices(const HostLayout& L, char* w, const float* delta, 
                               int64_t T, int64_t d_inner, int64_t d_state, cudaStream_t s0) {
   AuxStreams ax;
   if (!aux_streams(&ax)) return set_cuda_error(cudaGetLastError());
+  std::lock_guard<std::mutex> hold(*ax.enqueue);
   ax.s[0] = s0;
   auto at = [&](size_t off) { return (float*)(w + off); };
   const size_t rows = (size_t)batch * T;                 // rows of the [batch*T][d_inner] view
@@ -750,6 +759,7 @@ int mamba_scan_fwd_bwd_host(const float* delta, const float* u, const float* B, 
   cudaStream_t s0 = (cudaStream_t)stream;
   AuxStreams ax;
   if (!aux_streams(&ax)) return set_cuda_error(cudaGetLastError());
+  std::lock_guard<std::mutex> hold(*ax.enqueue);
   ax.s[0] = s0;
   auto cp = [&](void* dst, const void* src, size_t n, cudaMemcpyKind k, cudaStream_t st) {
     return cudaMemcpyAsync(dst, src, n, k, st);

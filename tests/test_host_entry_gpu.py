@@ -67,3 +67,56 @@ def test_host_entry_matches_oracle(shape):
     assert_parity(first, ref, keys=KEYS, label=f"host {shape}")
     for k in KEYS:   # bitwise repeatable from call to call
         assert np.array_equal(first[k], second[k]), k
+
+
+def _host_call(ms, torch, x, stream):
+    """One host-entry call on `stream` with its own workspace and pinned outputs."""
+    b, T, Di = x["delta"].shape
+    N = x["B"].shape[2]
+    hin = {k: torch.from_numpy(np.ascontiguousarray(x[k])).pin_memory() for k in IN_KEYS}
+    shapes = {"out": (b, T, Di), "d_delta": (b, T, Di), "d_u": (b, T, Di), "d_gate": (b, T, Di),
+              "d_B": (b, T, N), "d_C": (b, T, N), "d_A_log": (Di, N), "d_D": (Di,)}
+    ws = torch.empty(ms.mamba_scan_host_workspace_bytes(b, T, Di, N), dtype=torch.uint8,
+                     device="cuda:0")
+    hout = {k: torch.full(s, float("nan")).pin_memory() for k, s in shapes.items()}
+    ms.mamba_scan_fwd_bwd_host(hin["delta"], hin["u"], hin["B"], hin["C"], hin["gate"],
+                               hin["A_log"], hin["D"], hin["dy"], hout["out"],
+                               hout["d_delta"], hout["d_u"], hout["d_B"], hout["d_C"],
+                               hout["d_A_log"], hout["d_D"], hout["d_gate"], ws, stream=stream)
+    return {k: v.numpy().copy() for k, v in hout.items()}
+
+
+@pytest.mark.parametrize("shape", [(1, 300, 260, 64), (5, 100, 64, 16)],
+                         ids=["channel_slices", "batch_slices"])
+def test_host_entry_concurrent_threads(shape):
+    """Two host threads call the host entry at the same time, each on its own stream and
+    inputs. The calls share the library's streams and events; every result must equal the same
+    call made alone, bit for bit."""
+    import threading
+    import torch
+    import selective_state_space_06_gb300 as ms
+    xs = [synth.random_inputs(*shape, seed=40 + i, a_log_random=True) for i in range(2)]
+    solo = [_host_call(ms, torch, x, torch.cuda.current_stream()) for x in xs]
+    got = [[], []]
+    errors = []
+
+    def worker(i):
+        try:
+            torch.cuda.set_device(0)
+            s = torch.cuda.Stream()
+            for _ in range(3):
+                got[i].append(_host_call(ms, torch, xs[i], s))
+        except Exception as e:   # reported by the main thread
+            errors.append(repr(e))
+
+    th = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in th:
+        t.start()
+    for t in th:
+        t.join()
+    assert errors == []
+    for i in range(2):
+        assert len(got[i]) == 3
+        for r in got[i]:
+            for k in KEYS:
+                assert np.array_equal(r[k], solo[i][k]), (i, k)
