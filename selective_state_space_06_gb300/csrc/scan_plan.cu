@@ -60,8 +60,16 @@ bool make_plan(int64_t batch, int64_t T, int64_t Di, int64_t N, Plan* pl) {
     split(q, best_want);
     return q;
   };
-  p.fwd = by_target(pass(states_per_thread_fwd(p.NP), fwd_channels_per_thread(p.NP), kFwdWarps),
-                    target_units_fwd(p.NP));
+  {
+    const PassPlan q =
+        pass(states_per_thread_fwd(p.NP), fwd_channels_per_thread(p.NP), kFwdWarps);
+    const int64_t rows = (int64_t)batch * q.nblk;
+    // d_state 64: the most segments whose CTAs fit in kFwdWaves64 waves (at least one segment)
+    const int64_t target =
+        p.NP == 64 ? std::max<int64_t>(1, (int64_t)kFwdWaves64 * kFwdSlots64 / rows) * rows
+                   : (int64_t)target_units_fwd(p.NP);
+    p.fwd = by_target(q, (int)std::min<int64_t>(target, INT32_MAX));
+  }
   if (p.NP >= kTmemMinNP)
     p.bwd = by_waves(pass(4, kTmemDPT), kTmemSlots);
   else

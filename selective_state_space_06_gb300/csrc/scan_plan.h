@@ -46,6 +46,13 @@ constexpr int kMaxState = 64;
 // below that its pre-pass costs more than the extra parallelism gains (measured on GB300).
 __host__ __device__ constexpr int target_units_fwd(int NP) { return NP <= 16 ? 1 : 2048; }
 __host__ __device__ constexpr int target_units_bwd(int NP) { return 2048; }
+// At d_state 64 the forward (tensor copies, 3 stages) keeps 5 CTAs per SM, and its segments are
+// chosen so that its CTAs fill kFwdWaves64 whole waves of them (as nearly as the batch rows x
+// channel blocks allow). Measured at the long-sequence layer (80 channel blocks) on GB300: the
+// forward call took 3.72 ms with 38 segments (4 waves), 3.73 with 57 (6 waves), 3.78 with 19
+// (2) or 76 (8), 3.77 with 64 (6.7 waves) and 3.83 with 26 (2.7 waves, a target of 2048 CTAs).
+constexpr int kFwdSlots64 = 5 * 152;
+constexpr int kFwdWaves64 = 4;
 // The backward for d_state > 8 runs scan_bwd_tmem_kernel: 4 channels x 4 states per thread,
 // at most 2 CTAs per SM (its tensor-memory columns), so its segments are chosen to fill whole
 // waves of 2 x 152 CTAs.
