@@ -187,13 +187,13 @@ BWD_EX2_PER_ELEMENT_STATE = 1
 # (kernel_digest() below); once those sources differ, the entry no longer describes the
 # kernels and `traffic` is reported as null. The long-sequence figure was captured at
 # T = 8192 (--seq-len 8192) and scaled by 8: every term of it is proportional to T except the
-# carry composition's reads (under 1 % of it).
+# pre-pass aggregates and the carry composition's reads of them (about 2 % of it).
 BWD_TRAFFIC_CAPTURES = {
     # workload: (bytes per call, kernel digest, how the figure was taken)
-    "mamba370m": (1625.7e6, "35f1e7afdf32b6ae", "ncu capture at the full size"),
-    "mamba1p4b": (1625.9e6, "35f1e7afdf32b6ae", "ncu capture at the full size"),
-    "mamba130m": (556.2e6, "35f1e7afdf32b6ae", "ncu capture at the full size"),
-    "longseq": (8 * 1942.6e6, "35f1e7afdf32b6ae", "ncu capture at T = 8192, scaled by 8"),
+    "mamba370m": (1625.6e6, "01cc1ea4dc8e175e", "ncu capture at the full size"),
+    "mamba1p4b": (1625.9e6, "01cc1ea4dc8e175e", "ncu capture at the full size"),
+    "mamba130m": (550.7e6, "01cc1ea4dc8e175e", "ncu capture at the full size"),
+    "longseq": (8 * 1962.4e6, "01cc1ea4dc8e175e", "ncu capture at T = 8192, scaled by 8"),
 }
 # the files that define the backward call's kernels and their launch plan
 BWD_KERNEL_SOURCES = ("scan_common.cuh", "scan_plan.h", "scan_plan.cu", "scan_bwd.cu",

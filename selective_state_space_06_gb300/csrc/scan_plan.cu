@@ -78,9 +78,17 @@ bool make_plan(int64_t batch, int64_t T, int64_t Di, int64_t N, Plan* pl) {
   p.bwd.nsub = 1;
   if (p.NP >= kTmemMinNP && p.bwd.nseg > 1) {
     // pre-pass CTAs: batch x (the main kernel's channel blocks) x (segments 1 .. nseg-1) x nsub
+    // k sub-segments per segment: the fewest chunk steps on the critical path, counted as
+    // whole waves of resident pre-pass CTAs times (chunks per sub-segment + 2 of start-up)
     const int64_t base = (int64_t)batch * p.bwd.nblk * (p.bwd.nseg - 1);
-    int64_t k = (kBwdAggTarget + base - 1) / base;
-    k = std::max<int64_t>(1, std::min<int64_t>(k, p.bwd.seg_chunks));
+    const int64_t slots = (int64_t)bwd_agg_ctas_per_sm(p.NP) * kSMs;
+    int64_t k = 1;
+    double best = 1e300;
+    for (int64_t kk = 1; kk <= p.bwd.seg_chunks; ++kk) {
+      const int64_t sub = (p.bwd.seg_chunks + kk - 1) / kk;
+      const double cost = (double)((base * kk + slots - 1) / slots) * (double)(sub + 2);
+      if (cost < best - 1e-9) { best = cost; k = kk; }
+    }
     p.bwd.sub_chunks = (int)((p.bwd.seg_chunks + k - 1) / k);
     p.bwd.nsub = (p.bwd.seg_chunks + p.bwd.sub_chunks - 1) / p.bwd.sub_chunks;
   }

@@ -31,8 +31,14 @@ constexpr int kFwdWarps = 4;
 // Warps per CTA of the segment pre-pass kernels (the main kernels' CTA shape measured best;
 // wider CTAs with several segments each were slower on GB300).
 constexpr int kAggWarps = kWarps;
-// CTAs to aim for in the backward pre-pass of the tensor-memory path (two waves of four)
-constexpr int kBwdAggTarget = 2 * 4 * 152;
+constexpr int kSMs = 152;   // GB300
+// Resident CTAs per SM of the backward pre-pass of the tensor-memory path
+// (scan_bwd_agg4_kernel): 4 at d_state 16 (its two stages take 51 KB of shared memory), 7 at
+// d_state 32 and 64 (70 registers per thread). Its sub-segments are chosen to fill whole waves
+// of them. Measured on GB300 at the long-sequence layer: the backward call took 8.69 ms with 8
+// sub-segments per segment (11 waves), 8.70 with 2 (3 waves) and 8.80 with 1 (1440 CTAs, 1.35
+// waves: the earlier fixed target of 1216 CTAs).
+__host__ __device__ constexpr int bwd_agg_ctas_per_sm(int NP) { return NP <= 16 ? 4 : 7; }
 constexpr int kChunk = 16;  // time steps per chunk (= checkpoint interval)
 constexpr int kMaxState = 64;
 
