@@ -89,7 +89,7 @@ template <int K, int VW>
 __global__ void __launch_bounds__(256) conv_fwd_kernel(const ConvParams p) {
   using V = Vec<VW>;
   pdl_wait();      // the previous kernel's writes are visible
-  pdl_release();   // one wave (the run length is picked for that)
+  pdl_release();   // the next kernel may take the room the last wave leaves
   const ConvThread c = conv_thread(p, VW);
   if (!c.valid) return;
   float w[K][VW], bias[VW];

@@ -199,7 +199,7 @@ scan_bwd_tmem_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
       smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u));   // 128-byte aligned
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kDataFloats);
   pdl_wait();      // the previous kernel's writes (carries, checkpoints) are visible
-  pdl_release();   // one wave: the reduction may take the room this kernel leaves
+  pdl_release();   // the reduction may take the room the last wave leaves
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ng = lane & (G - 1), dg = lane >> LG;

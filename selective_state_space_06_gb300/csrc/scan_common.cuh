@@ -532,10 +532,10 @@ struct BfTile {
 // The scan kernels are launched with programmatic stream serialization, so the next one can be
 // scheduled while its predecessor in the stream still runs. Each of them calls pdl_wait() before
 // it touches global memory: that returns once the preceding kernel has completed and its writes
-// are visible (at once when there is no such kernel). The one-wave kernels (forward, tensor-
-// memory backward) call pdl_release() right after, so that the next kernel's CTAs can take the
-// SM room they leave and start as soon as they finish. A launch without the attribute makes
-// both no-ops.
+// are visible (at once when there is no such kernel). The forward and the tensor-memory
+// backward call pdl_release() right after. The next kernel may then launch once every CTA of
+// the grid has started (its last wave is resident), and its CTAs take the SM room that wave
+// leaves as it finishes. A launch without the attribute makes both no-ops.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void pdl_release() {
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");

@@ -396,7 +396,7 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const FwdParams p) {
   extern __shared__ __align__(128) float smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NS * S::kStageFloats);   // (TMA)
   pdl_wait();      // the previous kernel's writes (inputs, workspace) are visible
-  pdl_release();   // one wave: the next kernel may take the room this one leaves
+  pdl_release();   // the next kernel may take the room the last wave leaves
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ng = lane % G, dg = lane / G;
