@@ -114,6 +114,40 @@ def make_inputs(w: Workload, seed: int = 0, with_dy: bool = True) -> dict:
     return x
 
 
+# the [batch, T, *] inputs in the order iter_input_chunks yields them
+CHUNKED_KEYS = ("delta", "u", "gate", "dy", "B", "C")
+
+
+def iter_input_chunks(w: Workload, seed: int = 0, chunk: int = 1 << 26):
+    """The [batch, T, *] inputs of make_inputs(w, seed) in pieces, for sizes whose float64 draws
+    would not fit in host memory at once. Yields (name, start, values): float32 values of the
+    flattened (C-order) tensor from element `start` on. Each tensor's stream is drawn in the
+    same order as in make_inputs, so the pieces join into exactly make_inputs' values."""
+    b, T, Di, N = w.shape()
+    for name in CHUNKED_KEYS:
+        n = b * T * (N if name in ("B", "C") else Di)
+        g = _rng(seed, w.wid, name)
+        for start in range(0, n, chunk):
+            v = g.standard_normal(size=min(chunk, n - start), dtype=np.float64)
+            if name == "delta":
+                v = softplus64(w.delta_scale * v + w.delta_shift)
+            elif name in ("B", "C"):
+                v = w.bc_scale * v
+            yield name, start, v.astype(np.float32)
+
+
+def small_inputs(w: Workload, seed: int = 0) -> dict:
+    """A_log [d_inner, d_state] and D [d_inner] of make_inputs(w, seed)."""
+    b, T, Di, N = w.shape()
+    A_log = np.ascontiguousarray(
+        np.broadcast_to(np.log(np.arange(1, N + 1, dtype=np.float64)), (Di, N))).astype(np.float32)
+    if w.d_const:
+        D = np.ones(Di, dtype=np.float32)
+    else:
+        D = _rng(seed, w.wid, "D").uniform(0.5, 1.5, size=Di).astype(np.float32)
+    return {"A_log": A_log, "D": D}
+
+
 def random_inputs(batch, T, d_inner, d_state, seed=0, a_log_random=False) -> dict:
     """Generic asymmetric inputs for small cases (edge cases, pins).
 
