@@ -221,8 +221,8 @@ __device__ __forceinline__ void fwd_load_chunk(const FwdParams& p, float* st, in
 
 // Segment pre-pass of the forward: for every segment but the last, run the recurrence from a
 // zero state and keep the end state and the sum of delta over the segment, per (b, d, n).
-// Since h_end = exp(A * sum(delta)) * h_start + h_end(from zero), the main kernel composes these
-// to obtain the exact state entering each segment. A CTA covers kAggWarps warps of
+// Since h_end = exp(A * sum(delta)) * h_start + h_end(from zero), scan_fwd_compose_kernel
+// composes these into the exact state entering each segment. A CTA covers kAggWarps warps of
 // channels and agg_k consecutive segments, with the chunk pipeline running straight through the
 // segment boundaries.
 template <int NP>
@@ -382,9 +382,11 @@ scan_fwd_agg_kernel(const __grid_constant__ FwdMaps maps, const FwdParams p) {
 // ST (states only, for the fused forward + backward call): the recurrence and the checkpoints
 // alone; the backward then recomputes y from the states and writes out.
 // BF (with ST): delta, u and B arrive as bf16 and are widened in shared memory.
-// TMA: the tiles arrive by tensor copies (FwdMaps) into a ring of kStagesTma stages.
+// TMA: the tiles arrive by tensor copies (FwdMaps) into a ring of kStagesTma stages; its shared
+// memory leaves room for 5 CTAs per SM, and the register bound keeps that many resident (the
+// segment plan counts on it).
 template <int NP, bool VEC, bool WITH_Y, bool SP, bool ST, bool BF = false, bool TMA = false>
-__global__ void __launch_bounds__(kFwdWarps * 32)
+__global__ void __launch_bounds__(kFwdWarps * 32, TMA ? kFwdSlots64 / kSMs : 1)
 scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const FwdParams p) {
   static_assert(!(ST && (SP || WITH_Y)), "the states-only forward takes the plain delta");
   static_assert(!BF || ST, "bf16 input is taken by the states-only forward");
@@ -455,39 +457,30 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const FwdParams p) {
     else if constexpr (!TMA) cp_async_commit();
   }
 
-  // state entering the segment: compose the earlier segments' aggregates,
-  // h <- exp(A * sum(delta)) * h + (segment end state from zero)
-  // (a channel past d_inner takes sum 0 and state 0: the identity)
-  for (int sp = 0; sp < seg; ++sp) {
-    float sdv[DPT];
-    float2 hl[DPT][NPR];
+  // state entering the segment: scan_fwd_compose_kernel left it in the slot of the previous
+  // segment's aggregate (a channel past d_inner starts from 0)
+  if (seg > 0) {
 #pragma unroll
     for (int j = 0; j < DPT; ++j) {
       const int d = d0 + j;
-      const size_t row = ((size_t)b * p.nseg + sp) * Di + d;
-      const bool ok = d < Di && inb(row, 1, p.n_agg_sd()) && inb(row * N, N, p.n_agg_h());
-      sdv[j] = ok ? p.agg_sd[row] : 0.f;
-#pragma unroll
-      for (int q = 0; q < NPR; ++q) hl[j][q] = make_float2(0.f, 0.f);
-      if (!ok) continue;
+      const size_t row = ((size_t)b * p.nseg + seg - 1) * Di + d;
+      if (d >= Di || !inb(row * N, N, p.n_agg_h())) continue;
+      float2 hl[NPR];
       if constexpr (VEC) {
-        ld_pairs_row<NPR>(p.agg_h + row * N, n0, N, hl[j]);
+        ld_pairs_row<NPR>(p.agg_h + row * N, n0, N, hl);
       } else {
 #pragma unroll
         for (int q = 0; q < NPR; ++q) {
           const int n = n0 + 2 * q;
-          hl[j][q] = make_float2(n < N ? p.agg_h[row * N + n] : 0.f,
-                                 n + 1 < N ? p.agg_h[row * N + n + 1] : 0.f);
+          hl[q] = make_float2(n < N ? p.agg_h[row * N + n] : 0.f,
+                              n + 1 < N ? p.agg_h[row * N + n + 1] : 0.f);
         }
       }
-    }
 #pragma unroll
-    for (int q = 0; q < DP; ++q) {
-      const float2 sd2 = make_float2(sdv[2 * q], sdv[2 * q + 1]);
-#pragma unroll
-      for (int s = 0; s < NPT; ++s)
-        h[q][s] = fma2(ex2_2(mul2(sd2, a2[q][s])), h[q][s],
-                       make_float2(pair_el(hl[2 * q], s), pair_el(hl[2 * q + 1], s)));
+      for (int s = 0; s < NPT; ++s) {
+        if (j & 1) h[j >> 1][s].y = pair_el(hl, s);
+        else h[j >> 1][s].x = pair_el(hl, s);
+      }
     }
   }
 
@@ -603,6 +596,55 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const FwdParams p) {
   if constexpr (!TMA) cp_async_wait<0>();
 }
 
+// The state entering every segment but the first, from the pre-pass's aggregates, composed in
+// segment order: h <- exp(A * sum(delta)) * h + (segment end state from zero). One thread walks
+// the segments of one (batch row, channel, state); the state after segment s overwrites the
+// aggregate of segment s, which nothing reads afterwards, and is the state entering segment
+// s + 1. The arithmetic is the main kernel's own per step (ex2 of the product, one fma).
+__global__ void scan_fwd_compose_kernel(const FwdParams p) {
+  pdl_wait();   // the pre-pass's aggregates are visible
+  const size_t dn = (size_t)p.Di * p.N;
+  const size_t total = (size_t)p.batch * dn;
+  for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < total;
+       e += (size_t)gridDim.x * blockDim.x) {
+    const size_t b = e / dn, q = e % dn;
+    const size_t d = q / p.N;
+    const float a2 = inb(q, 1, dn) ? -expf(p.A_log[q]) * kLog2e : 0.f;
+    float h = 0.f;
+    // eight segments at a time: their loads do not depend on h, so they are all in flight
+    for (int s0 = 0; s0 < p.nseg - 1; s0 += 8) {
+      float Lv[8], sv[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int sg = s0 + k;
+        const size_t row = b * p.nseg + (sg < p.nseg - 1 ? sg : 0);
+        const bool in = sg < p.nseg - 1 && inb(row * dn + q, 1, p.n_agg_h()) &&
+                        inb(row * p.Di + d, 1, p.n_agg_sd());
+        Lv[k] = in ? p.agg_h[row * dn + q] : 0.f;
+        sv[k] = in ? p.agg_sd[row * p.Di + d] : 0.f;
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int sg = s0 + k;
+        if (sg >= p.nseg - 1) break;
+        h = fmaf(ex2_sfu(sv[k] * a2), h, Lv[k]);
+        const size_t o = (b * p.nseg + sg) * dn + q;
+        if (inb(o, 1, p.n_agg_h())) p.agg_h[o] = h;
+      }
+    }
+  }
+}
+
+// the composition between the pre-pass and the main kernel (when there are segments)
+static int launch_compose(const FwdParams& p, cudaStream_t s) {
+  int sms = 152, dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return launch_pdl(scan_fwd_compose_kernel, dim3(sms * 4), dim3(256), 0, s, p) == cudaSuccess
+             ? 1
+             : -1;
+}
+
 // ---- host side ---------------------------------------------------------------------------------
 
 unsigned fwd_take_fault() {
@@ -688,7 +730,8 @@ static int launch_np_tma(const Plan& plan, const FwdParams& p0, cudaStream_t s) 
     dim3 ga((unsigned)(nblk_a * ngrp), (unsigned)plan.batch);
     agg<<<ga, A::NTH, A::kSmemBytesTma, s>>>(maps, p);
     if (cudaPeekAtLastError() != cudaSuccess) return -1;
-    ++n;
+    if (launch_compose(p, s) < 0) return -1;
+    n += 2;
   }
   dim3 grid((unsigned)(plan.fwd.nblk * plan.fwd.nseg), (unsigned)plan.batch);
   if (launch_pdl(kern, grid, dim3(kFwdWarps * 32), S::kSmemBytesTma, s, maps, p) != cudaSuccess)
@@ -738,7 +781,8 @@ static int launch_np(const Plan& plan, const FwdParams& p0, cudaStream_t s) {
     dim3 ga((unsigned)(nblk_a * ngrp), (unsigned)plan.batch);
     agg<<<ga, A::NTH, A::kSmemBytes, s>>>(none, p);
     if (cudaPeekAtLastError() != cudaSuccess) return -1;
-    ++n;
+    if (launch_compose(p, s) < 0) return -1;
+    n += 2;
   }
   dim3 grid((unsigned)(plan.fwd.nblk * plan.fwd.nseg), (unsigned)plan.batch);
   if (launch_pdl(kern, grid, dim3(kFwdWarps * 32), S::kSmemBytes, s, none, p) != cudaSuccess)

@@ -54,11 +54,14 @@ __host__ __device__ constexpr int target_units_fwd(int NP) { return NP <= 16 ? 1
 __host__ __device__ constexpr int target_units_bwd(int NP) { return 2048; }
 // At d_state 64 the forward (tensor copies, 3 stages) keeps 5 CTAs per SM, and its segments are
 // chosen so that its CTAs fill kFwdWaves64 whole waves of them (as nearly as the batch rows x
-// channel blocks allow). Measured at the long-sequence layer (80 channel blocks) on GB300: the
-// forward call took 3.72 ms with 38 segments (4 waves), 3.73 with 57 (6 waves), 3.78 with 19
-// (2) or 76 (8), 3.77 with 64 (6.7 waves) and 3.83 with 26 (2.7 waves, a target of 2048 CTAs).
+// channel blocks allow). Measured at the long-sequence layer (80 channel blocks) on GB300, with
+// the segments' start states composed by a kernel of their own: the forward call took 3.66 ms
+// with 76 segments (8 waves), 3.67 with 57 (6) or 114 (12), 3.68 with 152 (16) and 3.69 with 38
+// (4). (When each CTA composed the aggregates of all earlier segments itself, that cost grew
+// with the segment count, and 38 segments were best at 3.72 ms; a fixed target of 2048 CTAs,
+// 26 segments and 2.7 waves, took 3.83 ms.)
 constexpr int kFwdSlots64 = 5 * 152;
-constexpr int kFwdWaves64 = 4;
+constexpr int kFwdWaves64 = 8;
 // The backward for d_state > 8 runs scan_bwd_tmem_kernel: 4 channels x 4 states per thread,
 // at most 2 CTAs per SM (its tensor-memory columns), so its segments are chosen to fill whole
 // waves of 2 x 152 CTAs.
@@ -199,7 +202,8 @@ int tmem_set_oob_shrink(unsigned long long s);
 int conv_set_oob_shrink(unsigned long long s);
 
 // Each returns the number of kernels enqueued (>= 1) or -1 on a launch error.
-// launch_fwd enqueues the segment pre-pass (when nseg > 1) and the forward scan; launch_bwd
+// launch_fwd enqueues the segment pre-pass and the composition of its aggregates (when
+// nseg > 1) and the forward scan; launch_bwd
 // enqueues the backward pre-pass (when nseg > 1), the backward scan and the fixed-order
 // reduction.
 int launch_fwd(const Plan& plan, const FwdParams& p, cudaStream_t stream);
