@@ -114,7 +114,8 @@ struct FwdShape {
   static constexpr int DPT = fwd_channels_per_thread(NP);   // channels per thread
   static constexpr int G = NP / NPT;                   // lanes per channel group
   static constexpr int DW = (32 / G) * DPT;            // channels per warp
-  static constexpr int DC = kFwdWarps * DW;            // channels per CTA
+  static constexpr int NW = fwd_warps(NP);             // warps per CTA
+  static constexpr int DC = NW * DW;                   // channels per CTA
   static constexpr int P = G >= DPT ? G / DPT : 1;     // steps per output group
   static constexpr int kStageFloats = kChunk * (3 * DC + 2 * NP);
   static constexpr size_t kSmemBytes = (size_t)kFwdStages * kStageFloats * sizeof(float);
@@ -160,7 +161,7 @@ template <int NP, bool VEC, bool ST = false, bool BF = false>
 __device__ __forceinline__ void fwd_load_chunk(const FwdParams& p, float* st, int c, int b,
                                                int dblk0) {
   using S = FwdShape<NP>;
-  constexpr int DC = S::DC, NTH = kFwdWarps * 32;
+  constexpr int DC = S::DC, NTH = S::NW * 32;
   float* s_dl = st;
   float* s_u = st + kChunk * DC;
   float* s_g = st + 2 * kChunk * DC;
@@ -222,13 +223,13 @@ __device__ __forceinline__ void fwd_load_chunk(const FwdParams& p, float* st, in
 // Segment pre-pass of the forward: for every segment but the last, run the recurrence from a
 // zero state and keep the end state and the sum of delta over the segment, per (b, d, n).
 // Since h_end = exp(A * sum(delta)) * h_start + h_end(from zero), scan_fwd_compose_kernel
-// composes these into the exact state entering each segment. A CTA covers kAggWarps warps of
-// channels and agg_k consecutive segments, with the chunk pipeline running straight through the
-// segment boundaries.
+// composes these into the exact state entering each segment. A CTA has the main kernel's warps
+// and channels (its tensor-copy boxes are the main kernel's) and agg_k consecutive segments,
+// with the chunk pipeline running straight through the segment boundaries.
 template <int NP>
 struct FwdAggShape {
   using S = FwdShape<NP>;
-  static constexpr int AW = kAggWarps;
+  static constexpr int AW = S::NW;   // the main kernel's CTA shape
   static constexpr int DC = AW * S::DW;
   static constexpr int NTH = AW * 32;
   static constexpr int kStages = 4;
@@ -239,7 +240,7 @@ struct FwdAggShape {
 };
 
 template <int NP, bool VEC, bool BF = false, bool TMA = false>
-__global__ void __launch_bounds__(kAggWarps * 32)
+__global__ void __launch_bounds__(fwd_warps(NP) * 32)
 scan_fwd_agg_kernel(const __grid_constant__ FwdMaps maps, const FwdParams p) {
   static_assert(!TMA || (VEC && !BF), "TMA staging takes fp32 tiles of whole 16-byte groups");
   using S = FwdShape<NP>;
@@ -386,7 +387,7 @@ scan_fwd_agg_kernel(const __grid_constant__ FwdMaps maps, const FwdParams p) {
 // memory leaves room for 5 CTAs per SM, and the register bound keeps that many resident (the
 // segment plan counts on it).
 template <int NP, bool VEC, bool WITH_Y, bool SP, bool ST, bool BF = false, bool TMA = false>
-__global__ void __launch_bounds__(kFwdWarps * 32, TMA ? kFwdSlots64 / kSMs : 1)
+__global__ void __launch_bounds__(fwd_warps(NP) * 32, TMA ? kFwdSlots64 / kSMs : 1)
 scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const FwdParams p) {
   static_assert(!(ST && (SP || WITH_Y)), "the states-only forward takes the plain delta");
   static_assert(!BF || ST, "bf16 input is taken by the states-only forward");
@@ -496,8 +497,8 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const FwdParams p) {
     }
     float* st = smem + (it % NS) * S::kStageFloats;
     if constexpr (BF) {   // widen the bf16 tiles into their slots (no overlap: one barrier)
-      BfTile<kChunk * DC, kFwdWarps * 32> wdl, wu;
-      BfTile<kChunk * NP, kFwdWarps * 32> wB;
+      BfTile<kChunk * DC, S::NW * 32> wdl, wu;
+      BfTile<kChunk * NP, S::NW * 32> wB;
       wdl.read(st + 2 * kChunk * DC);
       wu.read(st + 2 * kChunk * DC + kChunk * DC / 2);
       wB.read(st + 3 * kChunk * DC + kChunk * NP);
@@ -507,7 +508,7 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const FwdParams p) {
       __syncthreads();
     }
     if constexpr (SP) {   // raw delta -> delta in shared memory, once per element
-      softplus_tile<DC, kFwdWarps * 32>(st, p.T - c * kChunk, p.Di - dblk0);
+      softplus_tile<DC, S::NW * 32>(st, p.T - c * kChunk, p.Di - dblk0);
       __syncthreads();
     }
     const float* s_dl = st;
@@ -734,7 +735,7 @@ static int launch_np_tma(const Plan& plan, const FwdParams& p0, cudaStream_t s) 
     n += 2;
   }
   dim3 grid((unsigned)(plan.fwd.nblk * plan.fwd.nseg), (unsigned)plan.batch);
-  if (launch_pdl(kern, grid, dim3(kFwdWarps * 32), S::kSmemBytesTma, s, maps, p) != cudaSuccess)
+  if (launch_pdl(kern, grid, dim3(S::NW * 32), S::kSmemBytesTma, s, maps, p) != cudaSuccess)
     return -1;
   return n + 1;
 }
@@ -785,7 +786,7 @@ static int launch_np(const Plan& plan, const FwdParams& p0, cudaStream_t s) {
     n += 2;
   }
   dim3 grid((unsigned)(plan.fwd.nblk * plan.fwd.nseg), (unsigned)plan.batch);
-  if (launch_pdl(kern, grid, dim3(kFwdWarps * 32), S::kSmemBytes, s, none, p) != cudaSuccess)
+  if (launch_pdl(kern, grid, dim3(S::NW * 32), S::kSmemBytes, s, none, p) != cudaSuccess)
     return -1;
   return n + 1;
 }

@@ -62,7 +62,7 @@ bool make_plan(int64_t batch, int64_t T, int64_t Di, int64_t N, Plan* pl) {
   };
   {
     const PassPlan q =
-        pass(states_per_thread_fwd(p.NP), fwd_channels_per_thread(p.NP), kFwdWarps);
+        pass(states_per_thread_fwd(p.NP), fwd_channels_per_thread(p.NP), fwd_warps(p.NP));
     const int64_t rows = (int64_t)batch * q.nblk;
     // d_state 64: the most segments whose CTAs fit in kFwdWaves64 waves (at least one segment)
     const int64_t target =

@@ -25,11 +25,15 @@ __host__ __device__ constexpr int states_per_thread_bwd(int NP) { return NP < 4 
 // (4 at d_state 16 is slower: half the warps, mamba130m forward 0.111 -> 0.138 ms).
 __host__ __device__ constexpr int fwd_channels_per_thread(int NP) { return NP == 64 ? 4 : 2; }
 constexpr int kWarps = 4;   // warps per CTA
-// warps per CTA of the forward scan (measured: 2 warps per CTA runs as fast, 1 is 10 % slower
-// at mamba130m and 57 % at longseq; the CTAs' uneven spread over the SMs does not limit it)
-constexpr int kFwdWarps = 4;
-// Warps per CTA of the segment pre-pass kernels (the main kernels' CTA shape measured best;
-// wider CTAs with several segments each were slower on GB300).
+// Warps per CTA of the forward scan. Measured on GB300: at d_state 16, where the forward has no
+// time segments and its CTAs are as many as the batch rows x channel blocks (512 at mamba370m,
+// 3.4 per SM), 2 warps per CTA (twice the CTAs, spread more evenly) took 0.230 ms at mamba370m
+// and 0.093 at mamba130m against 0.240 and 0.098 with 4, and 1 warp 0.257 and 0.104. At d_state
+// 64 (segments filling whole waves) 4 warps are best: longseq's forward took 3.66 ms, against
+// 3.74 with 2 and 4.45 with 1.
+__host__ __device__ constexpr int fwd_warps(int NP) { return NP <= 16 ? 2 : 4; }
+// Warps per CTA of the backward pre-pass at d_state <= 8 (the main kernel's CTA shape measured
+// best; wider CTAs with several segments each were slower on GB300).
 constexpr int kAggWarps = kWarps;
 constexpr int kSMs = 152;   // GB300
 // Resident CTAs per SM of the backward pre-pass of the tensor-memory path
