@@ -308,10 +308,10 @@ def time_steps(ms, x, bufs, stream, steps, warmup, pg=None, sampler=None) -> dic
     """Times `steps` steps (mamba_scan_fwd + mamba_scan_bwd) after `warmup` untimed ones.
 
     One pair of events brackets the whole timed region (after a barrier and a synchronize). On a
-    regular sample of the steps (at least 64, or all), events on the launching stream also split
-    the forward call from the backward call. An event between two calls stops the second call's
-    first kernel from starting early (programmatic dependent launch), so the other steps run
-    without them, as a caller's would."""
+    regular sample of the steps (every fourth step, or more sparsely beyond 256 steps), events on
+    the launching stream also split the forward call from the backward call. An event between
+    two calls stops the second call's first kernel from starting early (programmatic dependent
+    launch), so the other steps run without them, as a caller's would."""
     import torch
 
     def step(ev_mid=None):
@@ -329,7 +329,7 @@ def time_steps(ms, x, bufs, stream, steps, warmup, pg=None, sampler=None) -> dic
     for _ in range(warmup):
         step()
     torch.cuda.synchronize()
-    stride = max(1, steps // 64)
+    stride = max(4, steps // 64)
     sampled = list(range(0, steps, stride))
     ev = {i: [torch.cuda.Event(enable_timing=True) for _ in range(3)] for i in sampled}
     outer0 = torch.cuda.Event(enable_timing=True)
