@@ -232,7 +232,10 @@ struct FwdAggShape {
   static constexpr int AW = S::NW;   // the main kernel's CTA shape
   static constexpr int DC = AW * S::DW;
   static constexpr int NTH = AW * 32;
-  static constexpr int kStages = 4;
+  // 3 stages: at d_state 64 the pre-pass then keeps 7 CTAs per SM (its registers' limit)
+  // instead of 6 (its shared memory's with 4 stages); measured on GB300, the longseq forward
+  // call took 3.65 ms against 3.67 with 4 stages (and 3.65 with 2)
+  static constexpr int kStages = 3;
   static constexpr int kStageFloats = kChunk * (2 * DC + NP);   // delta, u, B
   static constexpr size_t kSmemBytes = (size_t)kStages * kStageFloats * sizeof(float);
   static constexpr size_t kSmemBytesTma = kSmemBytes + 8 * kStages;   // + the barriers
