@@ -190,10 +190,10 @@ BWD_EX2_PER_ELEMENT_STATE = 1
 # pre-pass aggregates and the carry composition's reads of them (about 2 % of it).
 BWD_TRAFFIC_CAPTURES = {
     # workload: (bytes per call, kernel digest, how the figure was taken)
-    "mamba370m": (1625.8e6, "69864eb531da2c80", "ncu capture at the full size"),
-    "mamba1p4b": (1625.9e6, "69864eb531da2c80", "ncu capture at the full size"),
-    "mamba130m": (550.8e6, "69864eb531da2c80", "ncu capture at the full size"),
-    "longseq": (8 * 1962.3e6, "69864eb531da2c80", "ncu capture at T = 8192, scaled by 8"),
+    "mamba370m": (1625.6e6, "6e01a96729b114b0", "ncu capture at the full size"),
+    "mamba1p4b": (1626.1e6, "6e01a96729b114b0", "ncu capture at the full size"),
+    "mamba130m": (550.7e6, "6e01a96729b114b0", "ncu capture at the full size"),
+    "longseq": (8 * 1962.2e6, "6e01a96729b114b0", "ncu capture at T = 8192, scaled by 8"),
 }
 # the files that define the backward call's kernels and their launch plan
 BWD_KERNEL_SOURCES = ("scan_common.cuh", "scan_plan.h", "scan_plan.cu", "scan_bwd.cu",

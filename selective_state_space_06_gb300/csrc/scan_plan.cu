@@ -84,7 +84,8 @@ bool make_plan(int64_t batch, int64_t T, int64_t Di, int64_t N, Plan* pl) {
     const int64_t slots = (int64_t)bwd_agg_ctas_per_sm(p.NP) * kSMs;
     int64_t k = 1;
     double best = 1e300;
-    for (int64_t kk = 1; kk <= p.bwd.seg_chunks; ++kk) {
+    // (at most 1024 sub-segments a segment: bounds the search, and the carries' composition)
+    for (int64_t kk = 1; kk <= std::min<int64_t>(p.bwd.seg_chunks, 1024); ++kk) {
       const int64_t sub = (p.bwd.seg_chunks + kk - 1) / kk;
       const double cost = (double)((base * kk + slots - 1) / slots) * (double)(sub + 2);
       if (cost < best - 1e-9) { best = cost; k = kk; }
